@@ -1,0 +1,153 @@
+"""Seeded synthetic inputs shared by the tests, the smoke check and the bench.
+
+This module holds the workload shapes and the random-number recipe only: it
+does no attention arithmetic.  Both the CUDA path and the fp64 oracle consume
+the tensors it returns, so the two sides see identical bits.
+
+Recipe: ``torch.Generator().manual_seed(seed)``; every tensor is drawn as
+float32 ``randn`` (i.i.d. N(0, 1)) and rounded to the storage dtype.  The
+draw order is fixed (decode: L, q, k-cache, v-cache; prefill: q, k, v).
+"""
+import math
+from dataclasses import dataclass, field
+
+import torch
+
+BF16_QNAN_BITS = 0x7FC0  # bf16 quiet NaN used to poison unused cache capacity
+
+
+@dataclass(frozen=True)
+class PrefillShape:
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    Sq: int
+    Sk: int
+    D: int
+    causal: bool
+    dtype: torch.dtype
+    scale: float
+
+    @property
+    def flops(self) -> float:
+        """Algorithmic FLOPs: 4*B*Hq*Sq*Sk*D (two matmuls of 2*Sq*Sk*D each per
+        head), halved when causal (the 2*B*Hq*Sq*Sk*D causal convention)."""
+        f = 4.0 * self.B * self.Hq * self.Sq * self.Sk * self.D
+        return f / 2 if self.causal else f
+
+
+@dataclass(frozen=True)
+class DecodeShape:
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    cap: int
+    D: int
+    scale: float
+    dtype: torch.dtype = field(default=torch.bfloat16)
+
+
+# The five workloads: four prefill shapes and one single-token decode.
+TINY_CAUSAL_GQA = PrefillShape("tiny_causal_gqa_prefill_b1_hq2_hkv1_s128_d64_bf16",
+                               1, 2, 1, 128, 128, 64, True, torch.bfloat16, 1.0 / math.sqrt(64))
+RAGGED_NONCAUSAL = PrefillShape("ragged_noncausal_prefill_b2_h8_sq1000_sk1536_d64_fp16",
+                                2, 8, 8, 1000, 1536, 64, False, torch.float16, 1.0 / 8.0)
+MHA_CAUSAL = PrefillShape("mha_causal_prefill_b4_h16_s4096_d128_bf16",
+                          4, 16, 16, 4096, 4096, 128, True, torch.bfloat16, 1.0 / math.sqrt(128))
+GQA_CAUSAL_8K = PrefillShape("gqa_causal_prefill_b1_hq128_hkv8_s8192_d128_bf16",
+                             1, 128, 8, 8192, 8192, 128, True, torch.bfloat16, 1.0 / math.sqrt(128))
+DECODE_1TOK = DecodeShape("single_token_decode_b1_hq8_hkv2_d128_cap65536_bf16",
+                          1, 8, 2, 65536, 128, 1.0 / math.sqrt(128))
+
+PREFILL_SHAPES = [TINY_CAUSAL_GQA, RAGGED_NONCAUSAL, MHA_CAUSAL, GQA_CAUSAL_8K]
+
+
+def _randn(g: torch.Generator, shape, dtype) -> torch.Tensor:
+    return torch.randn(*shape, generator=g, dtype=torch.float32).to(dtype)
+
+
+def prefill_inputs(B, Hq, Hkv, Sq, Sk, D, dtype=torch.bfloat16, seed=0):
+    """q [B,Sq,Hq,D], k/v [B,Sk,Hkv,D] on the CPU, i.i.d. N(0,1) rounded to dtype."""
+    g = torch.Generator().manual_seed(seed)
+    q = _randn(g, (B, Sq, Hq, D), dtype)
+    k = _randn(g, (B, Sk, Hkv, D), dtype)
+    v = _randn(g, (B, Sk, Hkv, D), dtype)
+    return q, k, v
+
+
+def prefill_inputs_for(shape: PrefillShape, seed=0):
+    return prefill_inputs(shape.B, shape.Hq, shape.Hkv, shape.Sq, shape.Sk, shape.D,
+                          shape.dtype, seed)
+
+
+def draw_valid_length(cap: int, seed=0) -> int:
+    """The seeded valid length in [1, cap] (the first draw of the decode recipe)."""
+    g = torch.Generator().manual_seed(seed)
+    return 1 + int(torch.randint(0, cap, (1,), generator=g).item())
+
+
+def decode_inputs(B, Hq, Hkv, cap, D, dtype=torch.bfloat16, seed=0, L=None,
+                  poison_k=True, poison_v=True):
+    """Single-token decode inputs on the CPU.
+
+    Returns (q [B,1,Hq,D], kcache [B,cap,Hkv,D], vcache [B,cap,Hkv,D], L).
+    L is drawn from the seed in [1, cap] unless given.  Entries at token
+    positions >= L are overwritten with the bf16 quiet NaN 0x7FC0 (V always
+    poisoned, K as well unless poison_k=False), as in the unused-capacity
+    reproduction of rocm-libraries #13108's review.
+    """
+    g = torch.Generator().manual_seed(seed)
+    L_seeded = 1 + int(torch.randint(0, max(cap, 1), (1,), generator=g).item())
+    if L is None:
+        L = L_seeded
+    q = _randn(g, (B, 1, Hq, D), dtype)
+    kc = _randn(g, (B, cap, Hkv, D), dtype)
+    vc = _randn(g, (B, cap, Hkv, D), dtype)
+    lo = max(0, min(int(L), cap))
+    if lo < cap:
+        nan = poison_value(dtype)
+        if poison_k:
+            kc[:, lo:] = nan
+        if poison_v:
+            vc[:, lo:] = nan
+    return q, kc, vc, int(L)
+
+
+def decode_inputs_for(shape: DecodeShape, seed=0, L=None):
+    return decode_inputs(shape.B, shape.Hq, shape.Hkv, shape.cap, shape.D, shape.dtype,
+                         seed, L)
+
+
+def poison_value(dtype) -> torch.Tensor:
+    """A scalar NaN of the given dtype; for bf16 exactly the bit pattern 0x7FC0."""
+    if dtype == torch.bfloat16:
+        return torch.tensor([BF16_QNAN_BITS], dtype=torch.int16).view(torch.bfloat16)[0]
+    return torch.tensor(float("nan"), dtype=dtype)
+
+
+def sample_rows(B, Hq, Hkv, Sq, n=4096, seed=0):
+    """Seeded sample of query rows (b, h, i), int64 [m, 3], m <= n + specials.
+
+    Always contains the rows i in {0, 1, 127, 128, 255, 256, Sq-1} (clipped to
+    [0, Sq)) for the first and last query head of every GQA group and for
+    b in {0, B-1}; the rest is uniform from the seed.
+    """
+    G = Hq // Hkv
+    heads = sorted({h for kv in range(Hkv) for h in (kv * G, kv * G + G - 1)})
+    rows_i = sorted({i for i in (0, 1, 127, 128, 255, 256, Sq - 1) if 0 <= i < Sq})
+    bs = sorted({0, B - 1})
+    special = [(b, h, i) for b in bs for h in heads for i in rows_i]
+    g = torch.Generator().manual_seed(seed + 1)
+    m = max(0, n - len(special))
+    rb = torch.randint(0, B, (m,), generator=g)
+    rh = torch.randint(0, Hq, (m,), generator=g)
+    ri = torch.randint(0, Sq, (m,), generator=g)
+    rand = list(zip(rb.tolist(), rh.tolist(), ri.tolist()))
+    seen, out = set(), []
+    for t in special + rand:
+        if t not in seen:
+            seen.add(t)
+            out.append(t)
+    return torch.tensor(out, dtype=torch.int64).reshape(-1, 3)

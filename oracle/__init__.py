@@ -1,0 +1,131 @@
+"""fp64 CPU attention oracle -- TEST INFRASTRUCTURE ONLY.
+
+Only tests/, ``__graft_entry__.smoke()`` and the cpu_baseline / reference leg
+of ``bench.py`` may import this package.  The CUDA product path
+(``attention_fa_fwd_04_gb300``) never imports it and shares no code with it.
+
+The arithmetic lives in ``attn_oracle.c`` (plain C, fp64, one query row at a
+time: explicit scores, max-subtracted exponentials, one division).  This module
+only widens the caller's bf16/fp16 tensors to float64 (exact) and marshals
+arguments.  See ``attn_oracle.c`` for the definition and its sources:
+
+- tessera #90 "compiler-generated flash_attn fwd+bwd", flash_attn forward
+  commit note (scale*Q@K^T, causal/ragged mask, softmax, P@V);
+- "Dense flash-attention prefill (gfx950 / MI355X)", opening paragraph
+  (forward, MHA or GQA, causal);
+- rocm-libraries #13108 "minimal single-token attention decode", interface
+  description (Sq=1, token-major cache, device valid length).
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        lib = ctypes.CDLL(path)
+        dp = ctypes.POINTER(ctypes.c_double)
+        lp = ctypes.POINTER(ctypes.c_int64)
+        i64, i32, f64 = ctypes.c_int64, ctypes.c_int, ctypes.c_double
+        lib.oracle_attention_rows.argtypes = [dp, dp, dp, dp, lp, i64, i32, i32,
+                                              i32, i64, i64, i32, f64, i32, i32]
+        lib.oracle_attention_rows.restype = i32
+        lib.oracle_attention_probs.argtypes = [dp, dp, dp, dp, dp, i32, i32, i64,
+                                               i32, i32, i32, i64, i64, i32, f64, i32]
+        lib.oracle_attention_probs.restype = i32
+        lib.oracle_decode.argtypes = [dp, dp, dp, dp, i32, i32, i32, i64, i32, i64, f64]
+        lib.oracle_decode.restype = i32
+        _lib = lib
+    return _lib
+
+
+def _f64(t) -> np.ndarray:
+    """Exact widening of a torch tensor (bf16/fp16/fp32/fp64) or array to a
+    C-contiguous float64 numpy array."""
+    if hasattr(t, "detach"):
+        import torch
+        return np.ascontiguousarray(t.detach().to("cpu", torch.float64).numpy())
+    return np.ascontiguousarray(np.asarray(t, dtype=np.float64))
+
+
+def _ptr(a: np.ndarray, ctype=ctypes.c_double):
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def default_threads() -> int:
+    return max(1, len(os.sched_getaffinity(0)))
+
+
+def attention(q, k, v, scale: float, causal: bool, rows=None, nthreads=None):
+    """O for q [B,Sq,Hq,D], k/v [B,Sk,Hkv,D].
+
+    rows=None: full output, float64 [B,Sq,Hq,D].
+    rows=int array [n,3] of (b, h, i): float64 [n, D], row r = O[b,i,h,:].
+    """
+    lib = _load()
+    B, Sq, Hq, D = q.shape
+    Bk, Sk, Hkv, Dk = k.shape
+    assert Bk == B and Dk == D and tuple(v.shape) == tuple(k.shape)
+    kd, vd = _f64(k), _f64(v)
+    if rows is None:
+        b, i, h = np.meshgrid(np.arange(B), np.arange(Sq), np.arange(Hq), indexing="ij")
+        rows_arr = np.stack([b.ravel(), h.ravel(), i.ravel()], axis=1).astype(np.int64)
+        q_rows = _f64(q).reshape(-1, D)  # [B*Sq*Hq, D] in (b, i, h) order
+    else:
+        rows_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1, 3))
+        qt = q[rows_arr[:, 0], rows_arr[:, 2], rows_arr[:, 1], :] if len(rows_arr) else q.reshape(0, D)
+        q_rows = _f64(qt).reshape(-1, D)
+    q_rows = np.ascontiguousarray(q_rows)
+    n = rows_arr.shape[0]
+    out = np.zeros((n, D), dtype=np.float64)
+    if n:
+        rc = lib.oracle_attention_rows(
+            _ptr(q_rows), _ptr(kd), _ptr(vd), _ptr(out), _ptr(rows_arr, ctypes.c_int64),
+            n, B, Hq, Hkv, Sq, Sk, D, float(scale), int(bool(causal)),
+            int(nthreads or default_threads()))
+        if rc != 0:
+            raise RuntimeError(f"oracle_attention_rows failed with status {rc}")
+    if rows is None:
+        return out.reshape(B, Sq, Hq, D)
+    return out
+
+
+def probs(q, k, v, scale: float, causal: bool, b: int, h: int, i: int):
+    """(p [Sk], o [D]) of one query row: p over all Sk keys, 0 where masked."""
+    lib = _load()
+    B, Sq, Hq, D = q.shape
+    _, Sk, Hkv, _ = k.shape
+    kd, vd = _f64(k), _f64(v)
+    qrow = np.ascontiguousarray(_f64(q[b, i, h]))
+    p = np.zeros(max(Sk, 1), dtype=np.float64)
+    o = np.zeros(D, dtype=np.float64)
+    rc = lib.oracle_attention_probs(_ptr(qrow), _ptr(kd), _ptr(vd), _ptr(p), _ptr(o),
+                                    b, h, i, B, Hq, Hkv, Sq, Sk, D, float(scale),
+                                    int(bool(causal)))
+    if rc != 0:
+        raise RuntimeError(f"oracle_attention_probs failed with status {rc}")
+    return p[:Sk], o
+
+
+def decode(q, kcache, vcache, L: int, scale: float):
+    """Single-token decode. q [B,1,Hq,D] or [B,Hq,D]; caches [B,cap,Hkv,D];
+    L = valid length (host int), clamped to [0, cap].  Returns float64 [B,Hq,D]."""
+    lib = _load()
+    qd = _f64(q)
+    B, cap, Hkv, D = kcache.shape
+    qd = np.ascontiguousarray(qd.reshape(B, -1, D))
+    Hq = qd.shape[1]
+    kd, vd = _f64(kcache), _f64(vcache)
+    out = np.zeros((B, Hq, D), dtype=np.float64)
+    rc = lib.oracle_decode(_ptr(qd), _ptr(kd), _ptr(vd), _ptr(out), B, Hq, Hkv, cap, D,
+                           int(L), float(scale))
+    if rc != 0:
+        raise RuntimeError(f"oracle_decode failed with status {rc}")
+    return out

@@ -1,0 +1,352 @@
+"""Pins for the fp64 oracle: things the pages and the mathematics fix, chosen so
+that a plausible mistake in the oracle (a dropped term, a wrong sign or index,
+a transposed operand, a wrong mask edge, a wrong GQA map) fails one of them.
+
+Sources for what the oracle computes: tessera #90 (flash_attn forward commit
+note: scale*Q@K^T, causal/ragged mask, softmax, P@V); "Dense flash-attention
+prefill (gfx950 / MI355X)" (MHA or GQA, causal; parity checked against
+torch.nn.functional.scaled_dot_product_attention in its Measured section);
+rocm-libraries #13108 (decode over the first L tokens of a token-major cache;
+the unused-capacity NaN reproduction).
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import fa_inputs
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def f64(t):
+    return t.to(torch.float64).numpy()
+
+
+# ---------------------------------------------------------------------------
+# 1. Brute force on tiny shapes: whole-matrix numpy formulation
+#    (S = scale*Q K^T over all (i, j) at once, additive -inf mask, softmax
+#    along keys, P V), a different computation order from the oracle's
+#    per-row loop.
+# ---------------------------------------------------------------------------
+def brute_force(q, k, v, scale, causal):
+    q, k, v = f64(q), f64(k), f64(v)
+    B, Sq, Hq, D = q.shape
+    _, Sk, Hkv, _ = k.shape
+    G = Hq // Hkv
+    out = np.zeros_like(q)
+    for b in range(B):
+        for h in range(Hq):
+            Q = q[b, :, h, :]                       # [Sq, D]
+            K = k[b, :, h // G, :]                  # [Sk, D]
+            V = v[b, :, h // G, :]
+            S = scale * (Q @ K.T)                   # [Sq, Sk]
+            if causal:
+                ii = np.arange(Sq)[:, None]
+                jj = np.arange(Sk)[None, :]
+                S = np.where(jj <= ii + (Sk - Sq), S, -np.inf)
+            for i in range(Sq):
+                row = S[i]
+                if np.all(np.isneginf(row)):
+                    continue                        # no visible key: 0
+                e = np.exp(row - row.max())
+                out[b, i, h] = (e / e.sum()) @ V
+    return out
+
+
+TINY = [
+    # B, Hq, Hkv, Sq, Sk, D, causal, dtype, scale
+    (1, 2, 1, 7, 7, 8, True, torch.bfloat16, 0.3),
+    (2, 4, 2, 5, 11, 16, True, torch.bfloat16, 0.25),
+    (2, 4, 4, 9, 4, 8, True, torch.float16, 0.5),     # Sq > Sk: fully masked rows
+    (1, 3, 1, 6, 13, 4, False, torch.float16, 1.0),
+    (2, 4, 2, 16, 16, 8, False, torch.bfloat16, 0.125),
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Sq,Sk,D,causal,dt,scale", TINY)
+def test_brute_force_tiny(B, Hq, Hkv, Sq, Sk, D, causal, dt, scale):
+    q, k, v = fa_inputs.prefill_inputs(B, Hq, Hkv, Sq, Sk, D, dt, seed=3)
+    o = oracle.attention(q, k, v, scale, causal)
+    ref = brute_force(q, k, v, scale, causal)
+    np.testing.assert_allclose(o, ref, rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# 2. Library routine: torch fp64 scaled_dot_product_attention on the CPU (the
+#    routine the gfx950 prefill README measures its parity against).  GQA via
+#    repeat_interleave of K/V heads; bottom-right causal via an explicit mask.
+# ---------------------------------------------------------------------------
+def sdpa_ref(q, k, v, scale, causal):
+    G = q.shape[2] // k.shape[2]
+    qt = q.to(torch.float64).permute(0, 2, 1, 3)                        # [B,Hq,Sq,D]
+    kt = k.to(torch.float64).repeat_interleave(G, dim=2).permute(0, 2, 1, 3)
+    vt = v.to(torch.float64).repeat_interleave(G, dim=2).permute(0, 2, 1, 3)
+    Sq, Sk = q.shape[1], k.shape[1]
+    mask = None
+    if causal:
+        ii = torch.arange(Sq)[:, None]
+        jj = torch.arange(Sk)[None, :]
+        mask = jj <= ii + (Sk - Sq)
+    o = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=mask,
+                                                         scale=scale)
+    return o.permute(0, 2, 1, 3).numpy()
+
+
+@pytest.mark.parametrize("shape", [fa_inputs.TINY_CAUSAL_GQA, fa_inputs.RAGGED_NONCAUSAL],
+                         ids=lambda s: s.name)
+def test_matches_torch_sdpa_fp64(shape):
+    q, k, v = fa_inputs.prefill_inputs_for(shape, seed=0)
+    o = oracle.attention(q, k, v, shape.scale, shape.causal)
+    ref = sdpa_ref(q, k, v, shape.scale, shape.causal)
+    np.testing.assert_allclose(o, ref, rtol=0, atol=1e-11)
+
+
+def test_matches_torch_sdpa_sq_lt_sk_causal():
+    q, k, v = fa_inputs.prefill_inputs(2, 6, 3, 37, 70, 16, torch.bfloat16, seed=5)
+    o = oracle.attention(q, k, v, 0.2, True)
+    np.testing.assert_allclose(o, sdpa_ref(q, k, v, 0.2, True), rtol=0, atol=1e-11)
+
+
+def test_sampled_rows_equal_full_output():
+    q, k, v = fa_inputs.prefill_inputs(2, 4, 2, 33, 33, 16, torch.bfloat16, seed=9)
+    full = oracle.attention(q, k, v, 0.25, True)
+    rows = fa_inputs.sample_rows(2, 4, 2, 33, n=40, seed=1)
+    part = oracle.attention(q, k, v, 0.25, True, rows=rows)
+    r = rows.numpy()
+    np.testing.assert_array_equal(part, full[r[:, 0], r[:, 2], r[:, 1]])
+
+
+# ---------------------------------------------------------------------------
+# 3. Softmax rows sum to one; masked keys get exactly zero weight.
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("causal", [True, False])
+def test_probabilities_sum_to_one(causal):
+    q, k, v = fa_inputs.prefill_inputs(1, 4, 2, 12, 20, 8, torch.bfloat16, seed=2)
+    for h in range(4):
+        for i in (0, 5, 11):
+            p, o = oracle.probs(q, k, v, 0.4, causal, 0, h, i)
+            assert abs(p.sum() - 1.0) < 1e-14
+            assert np.all(p >= 0)
+            if causal:
+                last = i + (20 - 12)
+                assert np.all(p[last + 1:] == 0.0) and p[last] > 0
+            # O is the p-weighted sum of the head's V rows
+            np.testing.assert_allclose(o, p @ f64(v)[0, :, h // 2, :], atol=1e-13)
+
+
+# ---------------------------------------------------------------------------
+# 4. Uniform scores (Q = 0): O row i is the mean of V over its visible keys.
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("causal", [True, False])
+def test_zero_query_gives_mean_of_visible_values(causal):
+    B, Hq, Hkv, Sq, Sk, D = 2, 4, 2, 10, 14, 8
+    _, k, v = fa_inputs.prefill_inputs(B, Hq, Hkv, Sq, Sk, D, torch.bfloat16, seed=4)
+    q = torch.zeros(B, Sq, Hq, D, dtype=torch.bfloat16)
+    o = oracle.attention(q, k, v, 0.7, causal)
+    vv = f64(v)
+    for b in range(B):
+        for h in range(Hq):
+            for i in range(Sq):
+                n = min(Sk, i + (Sk - Sq) + 1) if causal else Sk
+                np.testing.assert_allclose(o[b, i, h], vv[b, :n, h // 2].mean(axis=0),
+                                           atol=1e-14)
+
+
+# ---------------------------------------------------------------------------
+# 5. One visible key returns that key's V exactly: causal row 0 (Sq == Sk) and
+#    decode with valid length 1.
+# ---------------------------------------------------------------------------
+def test_causal_row0_is_first_value_exactly():
+    q, k, v = fa_inputs.prefill_inputs(2, 4, 2, 9, 9, 16, torch.bfloat16, seed=6)
+    o = oracle.attention(q, k, v, 0.3, True)
+    vv = f64(v)
+    for b in range(2):
+        for h in range(4):
+            assert np.array_equal(o[b, 0, h], vv[b, 0, h // 2])
+
+
+def test_decode_valid_length_one_is_first_value_exactly():
+    q, kc, vc, L = fa_inputs.decode_inputs(1, 8, 2, 16, 128, seed=1, L=1)
+    o = oracle.decode(q, kc, vc, L, 1 / math.sqrt(128))
+    vv = f64(vc)
+    for h in range(8):
+        assert np.array_equal(o[0, h], vv[0, 0, h // 4])
+
+
+# ---------------------------------------------------------------------------
+# 6. GQA equals MHA with K/V heads repeated G times (contiguous groups).
+# ---------------------------------------------------------------------------
+def test_gqa_equals_mha_with_repeated_kv():
+    B, Hq, Hkv, Sq, Sk, D = 2, 8, 2, 11, 17, 16
+    q, k, v = fa_inputs.prefill_inputs(B, Hq, Hkv, Sq, Sk, D, torch.bfloat16, seed=8)
+    G = Hq // Hkv
+    o_gqa = oracle.attention(q, k, v, 0.25, True)
+    o_mha = oracle.attention(q, k.repeat_interleave(G, dim=2), v.repeat_interleave(G, dim=2),
+                             0.25, True)
+    assert np.array_equal(o_gqa, o_mha)
+    # and NOT the interleaved (h % Hkv) map: the two differ on this input
+    o_wrong = oracle.attention(q, k.repeat(1, 1, G, 1), v.repeat(1, 1, G, 1), 0.25, True)
+    assert np.max(np.abs(o_gqa - o_wrong)) > 1e-3
+
+
+# ---------------------------------------------------------------------------
+# 7. Unused cache capacity: NaN tails give the same output as zero tails, and
+#    the worked example of rocm-libraries #13108's review (capacity 128, valid
+#    length 1, V tail = bf16 0x7fc0 -> output equals the first V token).
+# ---------------------------------------------------------------------------
+def test_decode_nan_tail_equals_zero_tail():
+    q, kc, vc, L = fa_inputs.decode_inputs(2, 8, 2, 300, 64, seed=3, L=123)
+    assert torch.isnan(vc[:, L:].float()).all() and torch.isnan(kc[:, L:].float()).all()
+    kz, vz = kc.clone(), vc.clone()
+    kz[:, L:] = 0
+    vz[:, L:] = 0
+    a = oracle.decode(q, kc, vc, L, 0.125)
+    b = oracle.decode(q, kz, vz, L, 0.125)
+    assert np.isfinite(a).all()
+    assert np.array_equal(a, b)
+
+
+def read_fixture(name):
+    kv = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                key, val = line.split(None, 1)
+                kv[key] = val
+    return kv
+
+
+def test_golden_nan_tail_worked_example():
+    fx = read_fixture("nan_tail_decode.txt")
+    B, Hq, Hkv, D, cap = (int(fx[k]) for k in ("B", "Hq", "Hkv", "D", "cap"))
+    L = int(fx["valid_length"])
+    assert cap * Hkv * D == int(fx["v_buffer_elements"])
+    q, kc, vc, _ = fa_inputs.decode_inputs(B, Hq, Hkv, cap, D, seed=0, L=L, poison_k=False)
+    assert (vc[:, L:].view(torch.int16) == int(fx["v_tail_bits"], 16)).all()
+    o = oracle.decode(q, kc, vc, L, 1 / math.sqrt(D))
+    first_v = f64(vc)[0, 0]
+    G = Hq // Hkv
+    for h in range(Hq):
+        ref = first_v[h // G]
+        tol = float(fx["tolerance_abs"]) + float(fx["tolerance_rel"]) * np.abs(ref)
+        assert np.all(np.abs(o[0, h] - ref) <= tol)
+        assert np.array_equal(o[0, h], ref)  # one visible key: exact
+
+
+# ---------------------------------------------------------------------------
+# 8. Decode equals non-causal prefill with Sq=1 over the first L tokens; the
+#    valid length is clamped to [0, cap].
+# ---------------------------------------------------------------------------
+def test_decode_equals_prefill_over_valid_prefix():
+    q, kc, vc, L = fa_inputs.decode_inputs(2, 8, 2, 64, 32, seed=2, L=41)
+    o_dec = oracle.decode(q, kc, vc, L, 0.2)
+    o_pre = oracle.attention(q, kc[:, :L], vc[:, :L], 0.2, False)
+    np.testing.assert_allclose(o_dec, o_pre[:, 0], rtol=0, atol=0)
+
+
+def test_decode_clamps_valid_length():
+    q, kc, vc, _ = fa_inputs.decode_inputs(1, 4, 1, 20, 16, seed=4, L=20)
+    assert np.array_equal(oracle.decode(q, kc, vc, 0, 0.3), np.zeros((1, 4, 16)))
+    assert np.array_equal(oracle.decode(q, kc, vc, -5, 0.3), np.zeros((1, 4, 16)))
+    assert np.array_equal(oracle.decode(q, kc, vc, 25, 0.3), oracle.decode(q, kc, vc, 20, 0.3))
+
+
+# ---------------------------------------------------------------------------
+# 9. Index and operand checks.
+# ---------------------------------------------------------------------------
+def test_dominant_key_selects_its_value_row():
+    """A key aligned with the query and a large scale takes all the weight: the
+    output must be that key's V row (catches K/V index mix-ups and a
+    transposed Q K^T)."""
+    B, Hq, Hkv, Sq, Sk, D = 1, 2, 1, 4, 6, 8
+    _, k, v = fa_inputs.prefill_inputs(B, Hq, Hkv, Sq, Sk, D, torch.float16, seed=12)
+    q = torch.zeros(B, Sq, Hq, D, dtype=torch.float16)
+    target = [3, 0, 5, 2]                       # key picked by row i
+    k[0, :, 0, :] = 0
+    for j in range(Sk):
+        k[0, j, 0, j % D] = 1.0                 # key j = unit vector e_j
+    for i, j in enumerate(target):
+        q[0, i, :, j % D] = 1.0
+    o = oracle.attention(q, k, v, 200.0, False)
+    vv = f64(v)
+    for i, j in enumerate(target):
+        for h in range(Hq):
+            np.testing.assert_allclose(o[0, i, h], vv[0, j, 0], atol=1e-12)
+
+
+def test_causal_mask_edge_bottom_right():
+    """Row i sees key i + (Sk - Sq) and not key i + (Sk - Sq) + 1."""
+    B, Hq, Hkv, Sq, Sk, D = 1, 2, 1, 6, 10, 8
+    q, k, v = fa_inputs.prefill_inputs(B, Hq, Hkv, Sq, Sk, D, torch.bfloat16, seed=13)
+    base = oracle.attention(q, k, v, 0.3, True)
+    i = 2
+    last = i + Sk - Sq
+    v2 = v.clone()
+    v2[0, last + 1] += 1.0
+    o2 = oracle.attention(q, k, v2, 0.3, True)
+    assert np.array_equal(o2[0, : i + 1], base[0, : i + 1])
+    v3 = v.clone()
+    v3[0, last] += 1.0
+    o3 = oracle.attention(q, k, v3, 0.3, True)
+    assert np.max(np.abs(o3[0, i] - base[0, i])) > 1e-6
+    assert np.array_equal(o3[0, :i], base[0, :i])
+
+
+def test_fully_masked_rows_are_zero():
+    q, k, v = fa_inputs.prefill_inputs(1, 2, 1, 8, 3, 8, torch.bfloat16, seed=14)
+    o = oracle.attention(q, k, v, 0.5, True)
+    # Sq - Sk = 5 leading rows see no key (bottom-right alignment)
+    assert np.array_equal(o[0, :5], np.zeros((5, 2, 8)))
+    assert np.all(np.abs(o[0, 5:]) > 0)
+
+
+def test_noncausal_key_permutation_invariance():
+    q, k, v = fa_inputs.prefill_inputs(1, 2, 2, 5, 12, 8, torch.bfloat16, seed=15)
+    perm = torch.randperm(12, generator=torch.Generator().manual_seed(0))
+    a = oracle.attention(q, k, v, 0.4, False)
+    b = oracle.attention(q, k[:, perm], v[:, perm], 0.4, False)
+    np.testing.assert_allclose(a, b, atol=1e-14)
+
+
+def test_scale_multiplies_scores():
+    q, k, v = fa_inputs.prefill_inputs(1, 2, 1, 5, 5, 8, torch.float32, seed=16)
+    a = oracle.attention(q * 2, k, v, 0.25, True)
+    b = oracle.attention(q, k, v, 0.5, True)
+    np.testing.assert_allclose(a, b, atol=1e-13)
+
+
+def test_softmax_shift_invariance_against_closed_form_two_keys():
+    """Two keys: O = sigmoid(s0 - s1) v0 + sigmoid(s1 - s0) v1."""
+    q = torch.tensor([[[[1.0, 2.0]]]], dtype=torch.float64)            # [1,1,1,2]
+    k = torch.tensor([[[[0.5, -1.0]], [[2.0, 0.25]]]], dtype=torch.float64)  # [1,2,1,2]
+    v = torch.tensor([[[[3.0, -2.0]], [[-1.0, 4.0]]]], dtype=torch.float64)
+    scale = 0.7
+    s0 = scale * (1.0 * 0.5 + 2.0 * -1.0)
+    s1 = scale * (1.0 * 2.0 + 2.0 * 0.25)
+    w0 = 1.0 / (1.0 + math.exp(s1 - s0))
+    ref = w0 * np.array([3.0, -2.0]) + (1 - w0) * np.array([-1.0, 4.0])
+    o = oracle.attention(q, k, v, scale, False)
+    np.testing.assert_allclose(o[0, 0, 0], ref, atol=1e-15)
+
+
+# ---------------------------------------------------------------------------
+# 10. Stored oracle values (tests/golden/oracle_tiny.txt, written by
+#     tests/golden/make_golden.py from the oracle alone): drift guard.
+# ---------------------------------------------------------------------------
+def test_golden_oracle_values_unchanged():
+    with open(os.path.join(GOLDEN, "oracle_tiny.txt")) as f:
+        lines = [ln for ln in f.read().splitlines() if ln and not ln.startswith("#")]
+    assert len(lines) % 2 == 0 and lines
+    for hdr, vals in zip(lines[0::2], lines[1::2]):
+        _, name, B, Hq, Hkv, Sq, Sk, D, causal, dts, scale, seed = hdr.split()
+        dt = torch.bfloat16 if dts == "bf16" else torch.float16
+        q, k, v = fa_inputs.prefill_inputs(int(B), int(Hq), int(Hkv), int(Sq), int(Sk),
+                                           int(D), dt, int(seed))
+        o = oracle.attention(q, k, v, float(scale), bool(int(causal)))
+        ref = np.array([float(x) for x in vals.split()])
+        np.testing.assert_allclose(o.ravel(), ref, rtol=0, atol=1e-15)
