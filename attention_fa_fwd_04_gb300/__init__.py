@@ -1,0 +1,178 @@
+"""Python binding of libfa_gb300.so (the C ABI declared in include/fa.h).
+
+Argument marshalling only: every step of the attention runs in the CUDA
+kernels of the library.  PyTorch supplies device memory and streams.  There is
+no fallback: if the library is missing or cannot be loaded, every call raises.
+
+Raw entry points (same names and argument order as the C ABI; pointers are
+integers, ``stream`` a ``cudaStream_t`` value):
+    fa_prefill_fwd, fa_decode_fwd, fa_status_string, fa_device_error,
+    fa_num_sms, fa_prefill_work_item
+Tensor conveniences (contiguous CUDA tensors, caller-owned outputs):
+    prefill(q, k, v, scale, causal, out=None, stream=None)
+    decode(q, kcache, vcache, valid_len, scale, out=None, stream=None)
+"""
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libfa_gb300.so")
+
+FA_BF16, FA_FP16 = 0, 1
+FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = 0, 1, 2, 3, 4
+
+# Every symbol include/fa.h declares (checked by the tests against the header).
+EXPORTS = ("fa_prefill_fwd", "fa_decode_fwd", "fa_status_string", "fa_device_error",
+           "fa_num_sms", "fa_prefill_work_item")
+
+_lib = None
+
+
+class FAError(RuntimeError):
+    def __init__(self, status, what):
+        self.status = status
+        super().__init__(f"{what}: {fa_status_string(status)} (status {status})")
+
+
+def load(path: str = LIB_PATH):
+    """Load the library (once).  Raises if it is not built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(
+            f"{path} not found: build it with `python -c \"import __graft_entry__ as g; "
+            f"g.build()\"` (nvcc, sm_103a)")
+    lib = ctypes.CDLL(path)
+    vp, i32, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    lib.fa_prefill_fwd.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, i32, i32, vp]
+    lib.fa_prefill_fwd.restype = i32
+    lib.fa_decode_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp]
+    lib.fa_decode_fwd.restype = i32
+    lib.fa_status_string.argtypes = [i32]
+    lib.fa_status_string.restype = ctypes.c_char_p
+    lib.fa_device_error.argtypes = [i32, ctypes.POINTER(ctypes.c_uint)]
+    lib.fa_device_error.restype = i32
+    lib.fa_num_sms.argtypes = []
+    lib.fa_num_sms.restype = i32
+    ip = ctypes.POINTER(ctypes.c_int)
+    lib.fa_prefill_work_item.argtypes = [i32, i32, i32, i32, i32, i32, i32, ip, ip, ip]
+    lib.fa_prefill_work_item.restype = i32
+    _lib = lib
+    return lib
+
+
+# ----------------------------------------------------------------------------
+# Raw C-ABI mirrors
+# ----------------------------------------------------------------------------
+def fa_prefill_fwd(q, k, v, o, B, Hq, Hkv, Sq, Sk, D, scale, causal, dtype, stream):
+    return load().fa_prefill_fwd(q, k, v, o, B, Hq, Hkv, Sq, Sk, D, scale, causal, dtype, stream)
+
+
+def fa_decode_fwd(q, kcache, vcache, valid_len_dev, o, B, Hq, Hkv, cap, D, scale, stream):
+    return load().fa_decode_fwd(q, kcache, vcache, valid_len_dev, o, B, Hq, Hkv, cap, D, scale,
+                                stream)
+
+
+def fa_status_string(status) -> str:
+    return load().fa_status_string(int(status)).decode()
+
+
+def fa_device_error(reset=1):
+    """(status, detail bits) of the device-side error word; synchronises."""
+    detail = ctypes.c_uint(0)
+    st = load().fa_device_error(int(reset), ctypes.byref(detail))
+    return st, detail.value
+
+
+def fa_num_sms() -> int:
+    return load().fa_num_sms()
+
+
+def fa_prefill_work_item(w, B, Hq, Hkv, Sq, Sk=0, causal=1):
+    """(n_items, b, hq, qblock) of the persistent scheduler's item w."""
+    b, hq, qb = ctypes.c_int(-1), ctypes.c_int(-1), ctypes.c_int(-1)
+    n = load().fa_prefill_work_item(w, B, Hq, Hkv, Sq, Sk, causal, ctypes.byref(b),
+                                     ctypes.byref(hq), ctypes.byref(qb))
+    return n, b.value, hq.value, qb.value
+
+
+# ----------------------------------------------------------------------------
+# Tensor conveniences
+# ----------------------------------------------------------------------------
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _dtype_code(t):
+    import torch
+    if t.dtype == torch.bfloat16:
+        return FA_BF16
+    if t.dtype == torch.float16:
+        return FA_FP16
+    raise TypeError(f"unsupported dtype {t.dtype} (bf16 or fp16)")
+
+
+def _check(t, name):
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+
+
+def prefill(q, k, v, scale, causal, out=None, stream=None):
+    """O = softmax(scale * Q K^T [+ causal mask]) V.
+
+    q [B,Sq,Hq,D], k/v [B,Sk,Hkv,D]: contiguous CUDA bf16/fp16 tensors.
+    Returns ``out`` (allocated like q if None).  Enqueued on ``stream``
+    (default: torch's current stream); no host synchronisation.
+    """
+    import torch
+    B, Sq, Hq, D = q.shape
+    Bk, Sk, Hkv, Dk = k.shape
+    if Bk != B or Dk != D or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("shape mismatch between q, k, v")
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k, v must share a dtype")
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, n)
+    if out is None:
+        out = torch.empty_like(q)
+    _check(out, "out")
+    st = fa_prefill_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, Hq, Hkv,
+                        Sq, Sk, D, float(scale), int(bool(causal)), _dtype_code(q),
+                        _stream_handle(stream))
+    if st != FA_OK:
+        raise FAError(st, "fa_prefill_fwd")
+    return out
+
+
+def decode(q, kcache, vcache, valid_len, scale, out=None, stream=None):
+    """Single-token decode over the first L tokens of the cache.
+
+    q [B,1,Hq,D] (or [B,Hq,D]) bf16; kcache/vcache [B,cap,Hkv,D] bf16;
+    valid_len: int32 CUDA tensor holding L (read on the device only).
+    Returns ``out`` shaped like q.
+    """
+    import torch
+    B, cap, Hkv, D = kcache.shape
+    Hq = q.shape[-2]
+    if q.shape[0] != B or q.shape[-1] != D or q.numel() != B * Hq * D:
+        raise ValueError("q must be [B,1,Hq,D] matching the cache")
+    if tuple(vcache.shape) != tuple(kcache.shape):
+        raise ValueError("kcache and vcache shapes differ")
+    for t, n in ((q, "q"), (kcache, "kcache"), (vcache, "vcache"), (valid_len, "valid_len")):
+        _check(t, n)
+    if valid_len.dtype != torch.int32:
+        raise TypeError("valid_len must be an int32 CUDA tensor")
+    if q.dtype != torch.bfloat16 or kcache.dtype != torch.bfloat16 or vcache.dtype != torch.bfloat16:
+        raise TypeError("decode takes bf16 q/kcache/vcache")
+    if out is None:
+        out = torch.empty_like(q)
+    _check(out, "out")
+    st = fa_decode_fwd(q.data_ptr(), kcache.data_ptr(), vcache.data_ptr(), valid_len.data_ptr(),
+                       out.data_ptr(), B, Hq, Hkv, cap, D, float(scale), _stream_handle(stream))
+    if st != FA_OK:
+        raise FAError(st, "fa_decode_fwd")
+    return out

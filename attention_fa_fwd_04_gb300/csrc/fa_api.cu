@@ -1,0 +1,160 @@
+// fa_api.cu -- the C ABI (include/fa.h): argument validation, tensor-map
+// encoding, stream-ordered scratch for the decode partials, status mapping.
+// Every step of the attention itself runs in the kernels of fa_prefill.cu and
+// fa_decode.cu; this file only validates, marshals and enqueues.
+#include <math.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "fa.h"
+#include "fa_internal.h"
+
+namespace fa {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+int encode_tmap_rows(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                     uint64_t d3, uint32_t box_rows) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn) return 1;
+  const cuuint64_t dims[4] = {d0, d1, d2, d3};
+  const cuuint64_t strides[3] = {d0 * 2, d0 * d1 * 2, d0 * d1 * d2 * 2};
+  const cuuint32_t box[4] = {64, 1, box_rows, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : 1;
+}
+
+int sm_count() {
+  static int cache[64];
+  static std::once_flag once;
+  std::call_once(once, [] {
+    for (int i = 0; i < 64; ++i) cache[i] = 0;
+  });
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return -1;
+  if (dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+  if (dev < 64) cache[dev] = n;
+  return n;
+}
+
+}  // namespace fa
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static int cuda_status(int e) {
+  if (e == 0) return FA_OK;
+  cudaGetLastError();  // clear a sticky launch-config error so later calls start clean
+  return FA_ERR_CUDA;
+}
+
+extern "C" int fa_prefill_fwd(const void* q, const void* k, const void* v, void* o, int B,
+                              int Hq, int Hkv, int Sq, int Sk, int D, float scale, int causal,
+                              int dtype, cudaStream_t stream) {
+  if (B < 0 || Hq < 0 || Hkv < 0 || Sq < 0 || Sk < 0) return FA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return FA_ERR_INVALID_ARG;
+  if (dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_INVALID_ARG;
+  if (!isfinite(scale)) return FA_ERR_INVALID_ARG;
+  if (B == 0 || Hq == 0 || Sq == 0) return FA_OK;  // empty problem: nothing to write
+  if (Hkv == 0 || Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
+  if (!q || !o || !aligned16(q) || !aligned16(o)) return FA_ERR_INVALID_ARG;
+  if (Sk > 0 && (!k || !v || !aligned16(k) || !aligned16(v))) return FA_ERR_INVALID_ARG;
+  // Work items (B * Hq * ceil(Sq/256)) and element counts must fit the kernel's
+  // 32-bit item index and the tensor maps' 40-bit byte strides.
+  const int64_t items = (int64_t)B * Hq * ((Sq + 255) / 256);
+  if (items > INT32_MAX) return FA_ERR_INVALID_ARG;
+  if ((int64_t)Sq * Hq * D * 2 >= (1ll << 40) || (int64_t)Sk * Hkv * D * 2 >= (1ll << 40))
+    return FA_ERR_INVALID_ARG;
+  return cuda_status(fa::launch_prefill(q, k, v, o, B, Hq, Hkv, Sq, Sk, D, scale, causal,
+                                        dtype == FA_BF16, stream));
+}
+
+extern "C" int fa_decode_fwd(const void* q, const void* kcache, const void* vcache,
+                             const int32_t* valid_len_dev, void* o, int B, int Hq, int Hkv,
+                             int cap, int D, float scale, cudaStream_t stream) {
+  if (B < 0 || Hq < 0 || Hkv < 0 || cap < 0) return FA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return FA_ERR_INVALID_ARG;
+  if (!isfinite(scale)) return FA_ERR_INVALID_ARG;
+  if (B == 0 || Hq == 0) return FA_OK;
+  if (Hkv == 0 || Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
+  if (B > 65535 || (int64_t)Hkv * ((Hq / Hkv + 15) / 16) > 65535) return FA_ERR_INVALID_ARG;
+  if (!q || !o || !aligned16(q) || !aligned16(o)) return FA_ERR_INVALID_ARG;
+  if (cap > 0 && (!kcache || !vcache || !valid_len_dev || !aligned16(kcache) ||
+                  !aligned16(vcache) || (reinterpret_cast<uintptr_t>(valid_len_dev) & 3u)))
+    return FA_ERR_INVALID_ARG;
+  if ((int64_t)cap * Hkv * D * 2 >= (1ll << 40)) return FA_ERR_INVALID_ARG;
+  if (cap == 0)
+    return cuda_status(fa::launch_decode(q, kcache, vcache, valid_len_dev, o, B, Hq, Hkv, 0, D,
+                                         scale, nullptr, 0, stream));
+  const size_t nf = fa::decode_scratch_floats(B, Hq, Hkv, cap, D);
+  void* scratch = nullptr;
+  cudaError_t e = cudaMallocAsync(&scratch, nf * sizeof(float), stream);
+  if (e != cudaSuccess) return cuda_status(e);
+  int r = fa::launch_decode(q, kcache, vcache, valid_len_dev, o, B, Hq, Hkv, cap, D, scale,
+                            static_cast<float*>(scratch), nf, stream);
+  cudaError_t ef = cudaFreeAsync(scratch, stream);
+  if (r != 0) return cuda_status(r);
+  return cuda_status(ef);
+}
+
+extern "C" const char* fa_status_string(int status) {
+  switch (status) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG: invalid argument";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: unsupported configuration";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA: CUDA call or kernel launch failed";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a device pipeline wait hit its time limit";
+    default: return "unknown status";
+  }
+}
+
+extern "C" int fa_device_error(int reset, unsigned int* detail) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return FA_ERR_CUDA;
+  unsigned int a = 0, b = 0;
+  if (fa::read_prefill_error(&a, reset) != 0) return FA_ERR_CUDA;
+  if (fa::read_decode_error(&b, reset) != 0) return FA_ERR_CUDA;
+  if (detail) *detail = a | (b << 16);
+  return (a | b) ? FA_ERR_TIMEOUT : FA_OK;
+}
+
+extern "C" int fa_num_sms(void) { return fa::sm_count(); }
+
+extern "C" int fa_prefill_work_item(int w, int B, int Hq, int Hkv, int Sq, int Sk, int causal,
+                                    int* b, int* hq, int* qblock) {
+  (void)Sk;
+  (void)causal;
+  if (B < 0 || Hq < 0 || Hkv <= 0 || Sq < 0 || (Hq % Hkv) != 0) return -1;
+  const int64_t n_qb = (Sq + 255) / 256;
+  const int64_t n = (int64_t)B * Hq * n_qb;
+  if (n > INT32_MAX) return -1;
+  if (w >= 0 && w < n) {
+    int bb, hh, qq;
+    fa::prefill_item_host(w, B, Hq, Hkv, (int)n_qb, &bb, &hh, &qq);
+    if (b) *b = bb;
+    if (hq) *hq = hh;
+    if (qblock) *qblock = qq;
+  }
+  return (int)n;
+}

@@ -1,0 +1,471 @@
+// fa_decode.cu -- single-token decode: split-KV kernel + log-sum-exp combine.
+//
+// What it computes: for every query head h of every batch entry b,
+//   O[b,h,:] = sum_{j<L} p_j V[b,j,h/G,:] / sum_{j<L} p_j,
+//   p_j = exp(scale * <q[b,h], K[b,j,h/G]> - max),
+// over the first L tokens of a token-major [B, cap, Hkv, D] cache, where L is
+// an int32 in device memory (rocm-libraries #13108 "minimal single-token
+// attention decode", interface description).  The same PR's review showed that
+// loading whole tiles lets NaN in unused capacity reach P@V through 0*NaN; here
+// every K/V row at a token >= L is overwritten with zeros in shared memory
+// before any MMA touches the tile, and its score is set to -inf.  Split-KV is
+// the step that PR names as its next optimisation.
+//
+// Design (HBM-bound: 2*L*Hkv*D*2 bytes read, ~4 flop per byte):
+//   grid   = (nsplit, Hkv * ceil(G/16), B), one CTA per SM, sized from cap and
+//            the SM count (not from L, which the host never reads);
+//   CTA    = 1 producer warp issuing TMA tile loads (64 tokens x D, K and V,
+//            128-byte swizzle) into a 6-stage mbarrier ring, and 4 consumer
+//            warps that each own whole tiles: S = Q K^T and O += P V with
+//            mma.sync m16n8k16 (the group's query heads padded to M = 16), an
+//            exp2 online softmax per warp, then a cross-warp merge in shared
+//            memory into one (max, sum, o[D]) partial per head and split;
+//   combine= one CTA per (b, head) merges the split partials with weights
+//            exp2(m_s - M); launched with programmatic dependent launch so its
+//            launch overlaps the split kernel.
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "fa_internal.h"
+#include "fa_ptx.cuh"
+
+namespace fa {
+
+__device__ unsigned int g_decode_err = 0;
+
+namespace dec {
+constexpr int TT = 64;        // tokens per tile
+constexpr int NSTAGE = 6;     // ring depth (tiles in flight per CTA)
+constexpr int NWARPS = 4;     // consumer warps
+constexpr int THREADS = (NWARPS + 1) * 32;
+constexpr int HB = 16;        // query heads per CTA: the MMA's M
+constexpr int HALF_BYTES = TT * 128;  // TT rows x 64 elements x 2 bytes
+
+template <int D>
+struct Cfg {
+  static constexpr int HALVES = D / 64;
+  static constexpr int KV_BYTES = HALVES * HALF_BYTES;  // one K (or V) tile
+  static constexpr int STAGE_BYTES = 2 * KV_BYTES;      // K tile + V tile
+  static constexpr int SMEM_STAGES = NSTAGE * STAGE_BYTES;
+  static constexpr int SMEM_RED = HB * D * 4 + NWARPS * HB * 2 * 4;
+  static constexpr int SMEM_BAR = 2 * NSTAGE * 8 + 16;
+  static constexpr int SMEM_TOTAL = 1024 + SMEM_STAGES + SMEM_RED + SMEM_BAR;
+};
+}  // namespace dec
+
+struct DecodeParams {
+  const __nv_bfloat16* q;    // [B, Hq, D]
+  const int32_t* valid_len;  // device scalar L
+  float* part_o;             // [B, Hq, nsplit, D] unnormalised partial outputs
+  float* part_ml;            // [B, Hq, nsplit, 2] (row max in log2 units, row sum)
+  __nv_bfloat16* o;          // [B, Hq, D]
+  int B, Hq, Hkv, cap, G, nsplit, n_hb;
+  float c;                   // scale * log2(e)
+};
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+template <int D>
+__global__ void __launch_bounds__(dec::THREADS, 1)
+    decode_split_kernel(const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV, const DecodeParams p) {
+  using C = dec::Cfg<D>;
+  constexpr int TT = dec::TT, NSTAGE = dec::NSTAGE, HB = dec::HB, NW = dec::NWARPS;
+  constexpr float NEG_INF = -INFINITY;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint8_t* stages = smem;
+  float* red_o = reinterpret_cast<float*>(smem + C::SMEM_STAGES);  // [HB][D]
+  float* red_ml = red_o + HB * D;                                  // [NW][HB][2]
+  uint64_t* full = reinterpret_cast<uint64_t*>(red_ml + NW * HB * 2);
+  uint64_t* empty = full + NSTAGE;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + NSTAGE);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int split = blockIdx.x;
+  const int hkv = blockIdx.y / p.n_hb, hb = blockIdx.y % p.n_hb;
+  const int b = blockIdx.z;
+
+  // The combine grid may become resident now; it blocks until this grid ends.
+  pdl_launch_dependents();
+
+  int L = *p.valid_len;
+  L = L < 0 ? 0 : (L > p.cap ? p.cap : L);
+  const int tiles_total = (L + TT - 1) / TT;
+  const int tps = (tiles_total + p.nsplit - 1) / p.nsplit;
+  const int t_begin = split * tps;
+  int n_tiles = tiles_total - t_begin;
+  n_tiles = n_tiles < 0 ? 0 : (n_tiles > tps ? tps : n_tiles);
+
+  for (int x = threadIdx.x; x < HB * D; x += dec::THREADS) red_o[x] = 0.f;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NSTAGE; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  const int g = lane >> 2, tq = lane & 3;
+  float m0 = NEG_INF, m1 = NEG_INF, l0 = 0.f, l1 = 0.f;
+  float acc[D / 8][4];
+#pragma unroll
+  for (int nd = 0; nd < D / 8; ++nd) acc[nd][0] = acc[nd][1] = acc[nd][2] = acc[nd][3] = 0.f;
+
+  if (warp == NW) {
+    // ---------------- producer: one lane issues all TMA loads ----------------
+    if (lane == 0 && n_tiles > 0) {
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      const uint64_t pol = l2_policy_evict_first();
+      int t = 0;
+      for (; t < n_tiles; ++t) {
+        const int s = t % NSTAGE;
+        const uint32_t ph = (t / NSTAGE) & 1;
+        if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, &g_decode_err, 1)) break;
+        mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+        const int tok = (t_begin + t) * TT;
+        uint8_t* st = stages + s * C::STAGE_BYTES;
+#pragma unroll
+        for (int h = 0; h < C::HALVES; ++h)
+          tma_load_4d_hint(st + h * dec::HALF_BYTES, &tmK, &full[s], h * 64, hkv, tok, b, pol);
+#pragma unroll
+        for (int h = 0; h < C::HALVES; ++h)
+          tma_load_4d_hint(st + C::KV_BYTES + h * dec::HALF_BYTES, &tmV, &full[s], h * 64, hkv,
+                           tok, b, pol);
+      }
+      if (t < n_tiles) {
+        // Aborted: let the loads already issued land before the CTA exits.
+        for (int u = (t - NSTAGE > 0 ? t - NSTAGE : 0); u < t; ++u)
+          mbar_wait_drain(&full[u % NSTAGE], (u / NSTAGE) & 1);
+      }
+    }
+  } else {
+    // ---------------- consumers: whole tiles, round-robin over warps ----------------
+    // Q as the MMA's A operand (rows = the CTA's query heads, padded to 16).
+    const int hi0 = hb * HB + g, hi1 = hi0 + 8;
+    const bool ok0 = hi0 < p.G, ok1 = hi1 < p.G;
+    const uint32_t* q0 = reinterpret_cast<const uint32_t*>(
+        p.q + ((size_t)b * p.Hq + (size_t)hkv * p.G + (ok0 ? hi0 : 0)) * D);
+    const uint32_t* q1 = reinterpret_cast<const uint32_t*>(
+        p.q + ((size_t)b * p.Hq + (size_t)hkv * p.G + (ok1 ? hi1 : 0)) * D);
+    uint32_t qa[D / 16][4];
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      qa[kk][0] = ok0 ? q0[kk * 8 + tq] : 0u;
+      qa[kk][1] = ok1 ? q1[kk * 8 + tq] : 0u;
+      qa[kk][2] = ok0 ? q0[kk * 8 + 4 + tq] : 0u;
+      qa[kk][3] = ok1 ? q1[kk * 8 + 4 + tq] : 0u;
+    }
+
+    for (int t = warp; t < n_tiles; t += NW) {
+      const int s = t % NSTAGE;
+      const uint32_t ph = (t / NSTAGE) & 1;
+      if (!mbar_wait(&full[s], ph, abort_flag, &g_decode_err, 2)) break;
+      uint8_t* st = stages + s * C::STAGE_BYTES;
+      const int tok0 = (t_begin + t) * TT;
+      const int nvalid = (L - tok0) < TT ? (L - tok0) : TT;
+      if (nvalid < TT) {
+        // Tokens >= L: zero their K and V rows before any MMA reads the tile.
+        const int nz = TT - nvalid;
+        for (int x = lane; x < 2 * C::HALVES * nz * 8; x += 32) {
+          const int chunk = x & 7;
+          int r = x >> 3;
+          const int row = nvalid + r % nz;
+          r /= nz;
+          const int half = r % C::HALVES;
+          const int kv = r / C::HALVES;
+          *reinterpret_cast<uint4*>(st + kv * C::KV_BYTES + half * dec::HALF_BYTES + row * 128 +
+                                    chunk * 16) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+      }
+
+      // S = Q K^T: 16 heads x 64 tokens, 8 n-blocks of 8 tokens.
+      float sc[8][4];
+#pragma unroll
+      for (int nb = 0; nb < 8; ++nb) sc[nb][0] = sc[nb][1] = sc[nb][2] = sc[nb][3] = 0.f;
+      const uint32_t kbase = smem_u32(st);
+      const int mi = lane >> 3;
+#pragma unroll
+      for (int np = 0; np < 4; ++np) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const int tok = np * 16 + (mi >> 1) * 8 + (lane & 7);
+          const int chunk = kk * 2 + (mi & 1);
+          const uint32_t addr = kbase + (chunk >> 3) * dec::HALF_BYTES + tok * 128 +
+                                ((((chunk & 7) ^ (tok & 7))) << 4);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(addr, b0, b1, b2, b3);
+          mma_bf16_16816(sc[2 * np], qa[kk], b0, b1);
+          mma_bf16_16816(sc[2 * np + 1], qa[kk], b2, b3);
+        }
+      }
+      // Scale into the log2 domain, then mask tokens >= L.
+#pragma unroll
+      for (int nb = 0; nb < 8; ++nb)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          sc[nb][e] *= p.c;
+          if (nvalid < TT && nb * 8 + 2 * tq + (e & 1) >= nvalid) sc[nb][e] = NEG_INF;
+        }
+      // Online softmax over this warp's tiles.
+      float mx0 = NEG_INF, mx1 = NEG_INF;
+#pragma unroll
+      for (int nb = 0; nb < 8; ++nb) {
+        mx0 = fmaxf(mx0, fmaxf(sc[nb][0], sc[nb][1]));
+        mx1 = fmaxf(mx1, fmaxf(sc[nb][2], sc[nb][3]));
+      }
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+      const float base0 = mn0 == NEG_INF ? 0.f : mn0;
+      const float base1 = mn1 == NEG_INF ? 0.f : mn1;
+      const float f0 = fast_exp2(m0 - base0), f1 = fast_exp2(m1 - base1);
+      m0 = mn0;
+      m1 = mn1;
+      float rs0 = 0.f, rs1 = 0.f;
+#pragma unroll
+      for (int nb = 0; nb < 8; ++nb) {
+        sc[nb][0] = fast_exp2(sc[nb][0] - base0);
+        sc[nb][1] = fast_exp2(sc[nb][1] - base0);
+        sc[nb][2] = fast_exp2(sc[nb][2] - base1);
+        sc[nb][3] = fast_exp2(sc[nb][3] - base1);
+        rs0 += sc[nb][0] + sc[nb][1];
+        rs1 += sc[nb][2] + sc[nb][3];
+      }
+      l0 = l0 * f0 + rs0;
+      l1 = l1 * f1 + rs1;
+#pragma unroll
+      for (int nd = 0; nd < D / 8; ++nd) {
+        acc[nd][0] *= f0;
+        acc[nd][1] *= f0;
+        acc[nd][2] *= f1;
+        acc[nd][3] *= f1;
+      }
+      // O += P V: P from the S accumulators (C layout == A layout), V via
+      // transposing ldmatrix.
+      const uint32_t vbase = kbase + C::KV_BYTES;
+#pragma unroll
+      for (int k2 = 0; k2 < 4; ++k2) {
+        uint32_t a[4];
+        a[0] = pack_bf16(sc[2 * k2][0], sc[2 * k2][1]);
+        a[1] = pack_bf16(sc[2 * k2][2], sc[2 * k2][3]);
+        a[2] = pack_bf16(sc[2 * k2 + 1][0], sc[2 * k2 + 1][1]);
+        a[3] = pack_bf16(sc[2 * k2 + 1][2], sc[2 * k2 + 1][3]);
+#pragma unroll
+        for (int dn = 0; dn < D / 16; ++dn) {
+          const int tok = k2 * 16 + (mi & 1) * 8 + (lane & 7);
+          const int chunk = dn * 2 + (mi >> 1);
+          const uint32_t addr = vbase + (chunk >> 3) * dec::HALF_BYTES + tok * 128 +
+                                ((((chunk & 7) ^ (tok & 7))) << 4);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(addr, b0, b1, b2, b3);
+          mma_bf16_16816(acc[2 * dn], a, b0, b1);
+          mma_bf16_16816(acc[2 * dn + 1], a, b2, b3);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+    // Per-warp row sums (each quad holds one row's partial sums).
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    if (tq == 0) {
+      red_ml[(warp * HB + g) * 2 + 0] = m0;
+      red_ml[(warp * HB + g) * 2 + 1] = l0;
+      red_ml[(warp * HB + g + 8) * 2 + 0] = m1;
+      red_ml[(warp * HB + g + 8) * 2 + 1] = l1;
+    }
+  }
+  __syncthreads();
+
+  // Cross-warp merge into red_o (unnormalised, relative to the CTA row max).
+  if (warp < NW) {
+    float M0 = NEG_INF, M1 = NEG_INF;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      M0 = fmaxf(M0, red_ml[(w * HB + g) * 2]);
+      M1 = fmaxf(M1, red_ml[(w * HB + g + 8) * 2]);
+    }
+    const float w0 = (m0 == NEG_INF) ? 0.f : fast_exp2(m0 - M0);
+    const float w1 = (m1 == NEG_INF) ? 0.f : fast_exp2(m1 - M1);
+    if (w0 > 0.f) {
+#pragma unroll
+      for (int nd = 0; nd < D / 8; ++nd) {
+        atomicAdd(&red_o[g * D + nd * 8 + 2 * tq], acc[nd][0] * w0);
+        atomicAdd(&red_o[g * D + nd * 8 + 2 * tq + 1], acc[nd][1] * w0);
+      }
+    }
+    if (w1 > 0.f) {
+#pragma unroll
+      for (int nd = 0; nd < D / 8; ++nd) {
+        atomicAdd(&red_o[(g + 8) * D + nd * 8 + 2 * tq], acc[nd][2] * w1);
+        atomicAdd(&red_o[(g + 8) * D + nd * 8 + 2 * tq + 1], acc[nd][3] * w1);
+      }
+    }
+  }
+  __syncthreads();
+
+  // Write this split's partial for the CTA's valid heads.
+  const size_t head0 = (size_t)b * p.Hq + (size_t)hkv * p.G + (size_t)hb * HB;
+  const int nh = (p.G - hb * HB) < HB ? (p.G - hb * HB) : HB;
+  for (int x = threadIdx.x; x < nh * D; x += dec::THREADS) {
+    const int row = x / D, d = x % D;
+    p.part_o[((head0 + row) * p.nsplit + split) * D + d] = red_o[x];
+  }
+  if (threadIdx.x < nh) {
+    const int row = threadIdx.x;
+    float M = NEG_INF;
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, red_ml[(w * HB + row) * 2]);
+    float Ls = 0.f;
+    for (int w = 0; w < NW; ++w) {
+      const float mw = red_ml[(w * HB + row) * 2];
+      if (mw != NEG_INF) Ls += red_ml[(w * HB + row) * 2 + 1] * fast_exp2(mw - M);
+    }
+    p.part_ml[((head0 + row) * p.nsplit + split) * 2 + 0] = M;
+    p.part_ml[((head0 + row) * p.nsplit + split) * 2 + 1] = Ls;
+  }
+}
+
+// One CTA per (head, batch): O = sum_s w_s o_s / sum_s w_s l_s, w_s = exp2(m_s - M).
+// Splits that saw no token (l_s == 0) get weight 0 without touching o_s.
+template <int D>
+__global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams p) {
+  pdl_wait_primary();
+  const int h = blockIdx.x, b = blockIdx.y;
+  const size_t base = ((size_t)b * p.Hq + h) * p.nsplit;
+  float M = -INFINITY;
+  for (int s = 0; s < p.nsplit; ++s) M = fmaxf(M, p.part_ml[(base + s) * 2]);
+  for (int d = threadIdx.x; d < D; d += blockDim.x) {
+    float num = 0.f, den = 0.f;
+    for (int s = 0; s < p.nsplit; ++s) {
+      const float ls = p.part_ml[(base + s) * 2 + 1];
+      if (ls > 0.f) {
+        const float w = fast_exp2(p.part_ml[(base + s) * 2] - M);
+        num += w * p.part_o[(base + s) * D + d];
+        den += w * ls;
+      }
+    }
+    const float out = den > 0.f ? num / den : 0.f;
+    p.o[((size_t)b * p.Hq + h) * D + d] = __float2bfloat16_rn(out);
+  }
+}
+
+// Degenerate cache (cap == 0): every output is zero.
+__global__ void decode_zero_kernel(__nv_bfloat16* o, size_t n) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
+       i += (size_t)gridDim.x * blockDim.x)
+    o[i] = __float2bfloat16_rn(0.f);
+}
+
+static int decode_nsplit(int B, int Hq, int Hkv, int cap) {
+  const int G = Hq / Hkv;
+  const int n_hb = (G + dec::HB - 1) / dec::HB;
+  const long units = (long)B * Hkv * n_hb;
+  const int sms = sm_count() > 0 ? sm_count() : 148;
+  long ns = sms / (units > 0 ? units : 1);
+  const long max_tiles = ((long)cap + dec::TT - 1) / dec::TT;
+  if (ns > max_tiles) ns = max_tiles;
+  if (ns < 1) ns = 1;
+  return (int)ns;
+}
+
+size_t decode_scratch_floats(int B, int Hq, int Hkv, int cap, int D) {
+  const size_t ns = (size_t)decode_nsplit(B, Hq, Hkv, cap);
+  return (size_t)B * Hq * ns * ((size_t)D + 2);
+}
+
+template <int D>
+static int launch_decode_t(const void* q, const void* kc, const void* vc, const int32_t* vl,
+                           void* o, int B, int Hq, int Hkv, int cap, float scale, float* scratch,
+                           cudaStream_t stream) {
+  using C = dec::Cfg<D>;
+  CUtensorMap tk, tv;
+  if (encode_tmap_rows(&tk, kc, D, Hkv, cap, B, dec::TT)) return cudaErrorInvalidValue;
+  if (encode_tmap_rows(&tv, vc, D, Hkv, cap, B, dec::TT)) return cudaErrorInvalidValue;
+  static int attr_set[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM_TOTAL);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = 1;
+  }
+  DecodeParams p;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.valid_len = vl;
+  const int ns = decode_nsplit(B, Hq, Hkv, cap);
+  p.part_o = scratch;
+  p.part_ml = scratch + (size_t)B * Hq * ns * D;
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.cap = cap;
+  p.G = Hq / Hkv;
+  p.nsplit = ns;
+  p.n_hb = (p.G + dec::HB - 1) / dec::HB;
+  p.c = scale * 1.4426950408889634f;
+
+  dim3 grid(ns, Hkv * p.n_hb, B);
+  decode_split_kernel<D><<<grid, dec::THREADS, C::SMEM_TOTAL, stream>>>(tk, tv, p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(Hq, B, 1);
+  cfg.blockDim = dim3(128, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, decode_combine_kernel<D>, p);
+  return e;
+}
+
+int launch_decode(const void* q, const void* kc, const void* vc, const int32_t* valid_len,
+                  void* o, int B, int Hq, int Hkv, int cap, int D, float scale, float* scratch,
+                  size_t scratch_floats, cudaStream_t stream) {
+  if (B == 0 || Hq == 0) return cudaSuccess;
+  if (cap == 0) {
+    const size_t n = (size_t)B * Hq * D;
+    decode_zero_kernel<<<(unsigned)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096), 256, 0,
+                         stream>>>(static_cast<__nv_bfloat16*>(o), n);
+    return cudaGetLastError();
+  }
+  if (scratch_floats < decode_scratch_floats(B, Hq, Hkv, cap, D)) return cudaErrorInvalidValue;
+  if (D == 64)
+    return launch_decode_t<64>(q, kc, vc, valid_len, o, B, Hq, Hkv, cap, scale, scratch, stream);
+  return launch_decode_t<128>(q, kc, vc, valid_len, o, B, Hq, Hkv, cap, scale, scratch, stream);
+}
+
+int read_decode_error(unsigned int* out, int reset) {
+  unsigned int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_decode_err, sizeof(v));
+  if (e != cudaSuccess) return e;
+  if (reset && v) {
+    const unsigned int z = 0;
+    e = cudaMemcpyToSymbol(g_decode_err, &z, sizeof(z));
+    if (e != cudaSuccess) return e;
+  }
+  *out = v;
+  return cudaSuccess;
+}
+
+}  // namespace fa

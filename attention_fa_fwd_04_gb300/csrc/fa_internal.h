@@ -1,0 +1,40 @@
+// fa_internal.h -- host-side declarations shared by the C-ABI layer and the
+// kernel translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fa {
+
+// Tensor map over a contiguous [d3][d2][d1][d0] tensor of 16-bit elements,
+// 128-byte swizzle, zero fill outside the tensor, box (64, 1, box_rows, 1).
+// Returns 0 on success.
+int encode_tmap_rows(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                     uint64_t d3, uint32_t box_rows);
+
+// SM count of the current device (cached per device), or -1.
+int sm_count();
+
+// Enqueue the prefill kernel.  Returns a cudaError_t (0 = success).
+int launch_prefill(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv,
+                   int Sq, int Sk, int D, float scale, int causal, bool bf16, cudaStream_t stream);
+
+// Enqueue split + combine decode kernels with the given fp32 scratch
+// (partials).  scratch_floats is its size in floats.  Returns a cudaError_t.
+int launch_decode(const void* q, const void* kc, const void* vc, const int32_t* valid_len,
+                  void* o, int B, int Hq, int Hkv, int cap, int D, float scale, float* scratch,
+                  size_t scratch_floats, cudaStream_t stream);
+
+// Scratch floats the decode needs for these sizes.
+size_t decode_scratch_floats(int B, int Hq, int Hkv, int cap, int D);
+
+// Device error words of the kernel translation units (read + optionally clear).
+int read_prefill_error(unsigned int* out, int reset);
+int read_decode_error(unsigned int* out, int reset);
+
+// Work-item decode of the persistent prefill scheduler (host copy).
+void prefill_item_host(int w, int B, int Hq, int Hkv, int n_qb, int* b, int* hq, int* qb);
+
+}  // namespace fa

@@ -1,0 +1,599 @@
+// fa_prefill.cu -- dense flash-attention forward on the 5th-generation tensor
+// cores (tcgen05 + TMEM), warp-specialised and persistent.
+//
+// What it computes (tessera #90 "compiler-generated flash_attn fwd+bwd",
+// flash_attn forward commit note; "Dense flash-attention prefill (gfx950 /
+// MI355X)", opening paragraph):
+//   O[b,i,h,:] = sum_j p_ij V[b,j,h/G,:] / sum_j p_ij,
+//   p_ij = exp(scale * <Q[b,i,h], K[b,j,h/G]> - m_i), over the keys j visible
+//   to row i (all Sk keys, or j <= i + Sk - Sq when causal).
+//
+// Work unit ("Persistent (grid-stride) mode" of the gfx950 README): 256 query
+// rows of one query head, held as two 128-row Q tiles.  A persistent grid of
+// one CTA per SM walks the units in kv-head-major order (all query heads that
+// share a K/V head run together, so K/V stay in L2), longest causal units
+// first.
+//
+// CTA = 10 warps:
+//   warps 0-3  softmax/epilogue for Q tile 0 (TMEM lanes 0-127)
+//   warps 4-7  softmax/epilogue for Q tile 1
+//   warp  8    TMA producer: Q tiles, then K_j / V_j tiles into an NSTAGE ring
+//   warp  9    TMEM allocator and MMA issuer (one lane)
+// TMEM (512 columns): S0 | S1 | O0 | O1; P_i (bf16) is written over the first
+// half of S_i and fed to the P@V MMA straight from TMEM (no register or shared
+// memory relayout -- the role the transposed-PV lever plays on gfx950).
+// MMA issue order per KV step j: PV0(j), S0(j+1), PV1(j), S1(j+1), so each
+// softmax group has two MMA blocks of time to turn S_i into P_i.
+// Softmax: exp2 domain with scale*log2(e) folded into one FMA; lazy rescale
+// (O and l are rescaled only when a row max grows by more than 2^8 in the
+// exp2 domain; the gfx950 README's "lazy" lever); causal and Sk-tail masks only
+// on the tiles that need them (its "diagonal-only causal masking").
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <math.h>
+
+#include "fa_internal.h"
+#include "fa_ptx.cuh"
+
+namespace fa {
+
+__device__ unsigned int g_prefill_err = 0;
+
+namespace pf {
+constexpr int BM = 128;         // rows per Q tile
+constexpr int BN = 128;         // keys per K/V tile
+constexpr int QBLOCK = 2 * BM;  // query rows per work item
+constexpr int THREADS = 320;
+constexpr int HALF_BYTES = 128 * 128;  // 128 rows x 64 elements x 2 bytes
+constexpr float TAU = 8.0f;            // lazy-rescale threshold (log2 domain)
+
+template <int D>
+struct Cfg {
+  static constexpr int HALVES = D / 64;
+  static constexpr int TILE_BYTES = HALVES * HALF_BYTES;  // one 128-row tile
+  static constexpr int NSTAGE = (D == 128) ? 5 : 9;
+  static constexpr int SMEM_Q = 2 * TILE_BYTES;
+  static constexpr int SMEM_KV = NSTAGE * TILE_BYTES;
+  static constexpr int SMEM_BAR = 256;
+  static constexpr int SMEM_TOTAL = 1024 + SMEM_Q + SMEM_KV + SMEM_BAR;
+  static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O0 = 256, COL_O1 = 256 + D;
+  static constexpr uint32_t TMEM_COLS = 512;
+};
+}  // namespace pf
+
+struct PrefillParams {
+  void* o;  // [B, Sq, Hq, D]
+  int B, Hq, Hkv, Sq, Sk, G, causal, n_qb, n_items;
+  float c;  // scale * log2(e)
+};
+
+// Work item w -> (b, hq, qb): kv-head-major, then batch, then query blocks in
+// decreasing order (longest causal rows first), then the query heads of the
+// GQA group.
+__host__ __device__ __forceinline__ void prefill_item(int w, int B, int Hq, int Hkv, int n_qb,
+                                                      int* b, int* hq, int* qb) {
+  const int G = Hq / Hkv;
+  const int per_b = n_qb * G;
+  const int per_kv = B * per_b;
+  const int hkv = w / per_kv;
+  int r = w - hkv * per_kv;
+  *b = r / per_b;
+  r -= *b * per_b;
+  const int qr = r / G;
+  *hq = hkv * G + (r - qr * G);
+  *qb = n_qb - 1 - qr;
+}
+
+void prefill_item_host(int w, int B, int Hq, int Hkv, int n_qb, int* b, int* hq, int* qb) {
+  prefill_item(w, B, Hq, Hkv, n_qb, b, hq, qb);
+}
+
+// Number of K/V tiles Q tile rows [row0, row0+BM) need (0 if the tile is past
+// Sq or sees no key).
+__device__ __forceinline__ int kv_tiles_for(int row0, int Sq, int Sk, int causal) {
+  if (row0 >= Sq || Sk <= 0) return 0;
+  int nk = Sk;
+  if (causal) {
+    const int last_row = (row0 + pf::BM - 1 < Sq - 1) ? row0 + pf::BM - 1 : Sq - 1;
+    const int lim = last_row + (Sk - Sq) + 1;  // keys [0, lim) visible to the last row
+    nk = lim < Sk ? lim : Sk;
+    if (nk <= 0) return 0;
+  }
+  return (nk + pf::BN - 1) / pf::BN;
+}
+
+template <typename T>
+struct Pack2;
+template <>
+struct Pack2<__nv_bfloat16> {
+  static __device__ __forceinline__ uint32_t pack(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+};
+template <>
+struct Pack2<__half> {
+  static __device__ __forceinline__ uint32_t pack(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+};
+
+template <typename T>
+struct IsBF16 {
+  static constexpr bool value = false;
+};
+template <>
+struct IsBF16<__nv_bfloat16> {
+  static constexpr bool value = true;
+};
+
+template <int D, typename T>
+__global__ void __launch_bounds__(pf::THREADS, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
+  using C = pf::Cfg<D>;
+  constexpr bool kBF16 = IsBF16<T>::value;
+  constexpr int NSTAGE = C::NSTAGE;
+  constexpr float NEG_INF = -INFINITY;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint8_t* sQ = smem;
+  uint8_t* sKV = smem + C::SMEM_Q;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + C::SMEM_KV);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + NSTAGE;
+  uint64_t* q_full = bars + 2 * NSTAGE;
+  uint64_t* q_empty = q_full + 1;
+  uint64_t* s_full = q_full + 2;  // [2]
+  uint64_t* p_full = q_full + 4;  // [2]
+  uint64_t* o_full = q_full + 6;  // [2]
+  uint64_t* drain = q_full + 8;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(q_full + 9);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NSTAGE; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], pf::BM);
+      mbar_init(&o_full[i], 1);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(tmem_holder, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  const int off = p.Sk - p.Sq;  // bottom-right causal offset
+
+  if (warp == 8) {
+    // ============================ TMA producer ============================
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      const uint64_t pol_q = l2_policy_evict_first();
+      const uint64_t pol_kv = l2_policy_evict_last();
+      uint32_t kv_cnt = 0, local = 0;
+      bool ok = true;
+      for (int w = blockIdx.x; w < p.n_items && ok; w += gridDim.x, ++local) {
+        int b, hq, qb;
+        prefill_item(w, p.B, p.Hq, p.Hkv, p.n_qb, &b, &hq, &qb);
+        const int hkv = hq / p.G;
+        const int row0 = qb * pf::QBLOCK;
+        const int n0 = kv_tiles_for(row0, p.Sq, p.Sk, p.causal);
+        const int n1 = kv_tiles_for(row0 + pf::BM, p.Sq, p.Sk, p.causal);
+        const int n = n0 > n1 ? n0 : n1;
+        if (local > 0 && !(ok = mbar_wait(q_empty, (local - 1) & 1, abort_flag, &g_prefill_err, 1)))
+          break;
+        mbar_arrive_expect_tx(q_full, 2 * C::TILE_BYTES);
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+          for (int h = 0; h < C::HALVES; ++h)
+            tma_load_4d_hint(sQ + i * C::TILE_BYTES + h * pf::HALF_BYTES, &tmQ, q_full, h * 64, hq,
+                             row0 + i * pf::BM, b, pol_q);
+        for (int j = 0; j < n && ok; ++j) {
+#pragma unroll
+          for (int sel = 0; sel < 2; ++sel) {
+            const int s = kv_cnt % NSTAGE;
+            const uint32_t ph = (kv_cnt / NSTAGE) & 1;
+            if (!(ok = mbar_wait(&empty[s], ph ^ 1, abort_flag, &g_prefill_err, 2))) break;
+            mbar_arrive_expect_tx(&full[s], C::TILE_BYTES);
+            const CUtensorMap* m = sel ? &tmV : &tmK;
+#pragma unroll
+            for (int h = 0; h < C::HALVES; ++h)
+              tma_load_4d_hint(sKV + s * C::TILE_BYTES + h * pf::HALF_BYTES, m, &full[s], h * 64,
+                               hkv, j * pf::BN, b, pol_kv);
+            ++kv_cnt;
+          }
+        }
+      }
+      if (!ok) {
+        // Aborted: wait (bounded) for the loads already in flight.
+        const uint32_t first = kv_cnt > (uint32_t)NSTAGE ? kv_cnt - NSTAGE : 0u;
+        for (uint32_t u = first; u < kv_cnt; ++u)
+          mbar_wait_drain(&full[u % NSTAGE], (u / NSTAGE) & 1);
+        if (local > 0) mbar_wait_drain(q_full, (local - 1) & 1);
+      }
+    }
+  } else if (warp == 9) {
+    // ============================ MMA issuer ============================
+    if (lane == 0) {
+      constexpr uint32_t IDESC_S = idesc_f16(pf::BM, pf::BN, kBF16, false);
+      constexpr uint32_t IDESC_O = idesc_f16(pf::BM, D, kBF16, true);
+      const uint32_t sq_addr = smem_u32(sQ);
+      const uint32_t skv_addr = smem_u32(sKV);
+      uint32_t kv_cnt = 0, local = 0, p_cnt0 = 0, p_cnt1 = 0;
+      bool ok = true;
+
+      // S_i = Q_i K^T over D/16 k-steps (K-major A and B, 128-byte swizzle).
+      auto issue_s = [&](int i, int stage) {
+        const uint32_t d_tmem = tmem + (i ? C::COL_S1 : C::COL_S0);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t hoff = (k >> 2) * pf::HALF_BYTES + (k & 3) * 32;
+          const uint64_t a = sdesc_sw128(sq_addr + i * C::TILE_BYTES + hoff, 16, 1024);
+          const uint64_t bd = sdesc_sw128(skv_addr + stage * C::TILE_BYTES + hoff, 16, 1024);
+          mma_ss(d_tmem, a, bd, IDESC_S, k > 0 ? 1u : 0u);
+        }
+      };
+      // O_i (+)= P_i V over BN/16 k-steps; P_i from TMEM, V MN-major in smem.
+      auto issue_pv = [&](int i, int stage, bool accumulate) {
+        const uint32_t d_tmem = tmem + (i ? C::COL_O1 : C::COL_O0);
+        const uint32_t p_tmem = tmem + (i ? C::COL_S1 : C::COL_S0);
+#pragma unroll
+        for (int k = 0; k < pf::BN / 16; ++k) {
+          const uint64_t bd =
+              sdesc_sw128(skv_addr + stage * C::TILE_BYTES + k * 16 * 128, pf::HALF_BYTES, 1024);
+          mma_ts(d_tmem, p_tmem + k * 8, bd, IDESC_O, (accumulate || k > 0) ? 1u : 0u);
+        }
+      };
+
+      for (int w = blockIdx.x; w < p.n_items && ok; w += gridDim.x, ++local) {
+        int b, hq, qb;
+        prefill_item(w, p.B, p.Hq, p.Hkv, p.n_qb, &b, &hq, &qb);
+        const int row0 = qb * pf::QBLOCK;
+        const int nt0 = kv_tiles_for(row0, p.Sq, p.Sk, p.causal);
+        const int nt1 = kv_tiles_for(row0 + pf::BM, p.Sq, p.Sk, p.causal);
+        const int n = nt0 > nt1 ? nt0 : nt1;
+        if (!(ok = mbar_wait(q_full, local & 1, abort_flag, &g_prefill_err, 3))) break;
+        tc_fence_after();
+        if (n == 0) {
+          mma_commit(q_empty);
+          continue;
+        }
+        // K_0 -> S_0(0), S_1(0)
+        int sK = kv_cnt % NSTAGE;
+        if (!(ok = mbar_wait(&full[sK], (kv_cnt / NSTAGE) & 1, abort_flag, &g_prefill_err, 4)))
+          break;
+        tc_fence_after();
+        ++kv_cnt;
+        if (nt0 > 0) {
+          issue_s(0, sK);
+          mma_commit(&s_full[0]);
+        }
+        if (nt1 > 0) {
+          issue_s(1, sK);
+          mma_commit(&s_full[1]);
+        }
+        mma_commit(&empty[sK]);
+        if (n == 1) mma_commit(q_empty);
+
+        for (int j = 0; j < n && ok; ++j) {
+          const int sV = kv_cnt % NSTAGE;
+          if (!(ok = mbar_wait(&full[sV], (kv_cnt / NSTAGE) & 1, abort_flag, &g_prefill_err, 5)))
+            break;
+          tc_fence_after();
+          ++kv_cnt;
+          const bool has_next = j + 1 < n;
+          if (has_next) {
+            sK = kv_cnt % NSTAGE;
+            if (!(ok = mbar_wait(&full[sK], (kv_cnt / NSTAGE) & 1, abort_flag, &g_prefill_err, 6)))
+              break;
+            tc_fence_after();
+            ++kv_cnt;
+          }
+          if (j < nt0) {
+            if (!(ok = mbar_wait(&p_full[0], p_cnt0 & 1, abort_flag, &g_prefill_err, 7))) break;
+            ++p_cnt0;
+            tc_fence_after();
+            issue_pv(0, sV, j > 0);
+            if (j == nt0 - 1) mma_commit(&o_full[0]);
+            if (j + 1 < nt0) {
+              issue_s(0, sK);
+              mma_commit(&s_full[0]);
+            }
+          }
+          if (j < nt1) {
+            if (!(ok = mbar_wait(&p_full[1], p_cnt1 & 1, abort_flag, &g_prefill_err, 8))) break;
+            ++p_cnt1;
+            tc_fence_after();
+            issue_pv(1, sV, j > 0);
+            if (j == nt1 - 1) mma_commit(&o_full[1]);
+            if (j + 1 < nt1) {
+              issue_s(1, sK);
+              mma_commit(&s_full[1]);
+            }
+          }
+          if (!ok) break;
+          mma_commit(&empty[sV]);
+          if (has_next) {
+            mma_commit(&empty[sK]);
+            if (j + 1 == n - 1) mma_commit(q_empty);
+          }
+        }
+      }
+      // Every MMA issued by this thread has completed before TMEM is freed.
+      mma_commit(drain);
+      mbar_wait_drain(drain, 0);
+    }
+  } else {
+    // ======================= softmax + epilogue (2 groups) =======================
+    const int i = warp >> 2;          // Q tile handled by this warpgroup
+    const int wq = warp & 3;          // TMEM lane quarter
+    const int r = wq * 32 + lane;     // row within the Q tile
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+    const uint32_t tS = t_lane + (i ? C::COL_S1 : C::COL_S0);
+    const uint32_t tO = t_lane + (i ? C::COL_O1 : C::COL_O0);
+    const float c = p.c;
+    const bool neg_scale = c < 0.f;
+    uint32_t s_cnt = 0, o_cnt = 0;
+    bool ok = true;
+    T* const O = static_cast<T*>(p.o);
+
+    for (int w = blockIdx.x; w < p.n_items && ok; w += gridDim.x) {
+      int b, hq, qb;
+      prefill_item(w, p.B, p.Hq, p.Hkv, p.n_qb, &b, &hq, &qb);
+      const int row0 = qb * pf::QBLOCK + i * pf::BM;
+      const int grow = row0 + r;
+      const int n_i = kv_tiles_for(row0, p.Sq, p.Sk, p.causal);
+      T* const orow = O + ((size_t)b * p.Sq + grow) * (size_t)p.Hq * D + (size_t)hq * D;
+      if (n_i == 0) {
+        if (grow < p.Sq) {
+#pragma unroll
+          for (int x = 0; x < D / 8; ++x)
+            reinterpret_cast<uint4*>(orow)[x] = make_uint4(0u, 0u, 0u, 0u);
+        }
+        continue;
+      }
+      float m_used = NEG_INF;  // running max in the log2 domain (scaled units)
+      float l = 0.f;
+      for (int j = 0; j < n_i; ++j) {
+        if (!(ok = mbar_wait(&s_full[i], s_cnt & 1, abort_flag, &g_prefill_err, 9 + i))) break;
+        ++s_cnt;
+        tc_fence_after();
+        uint32_t sr[4][32];
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) tmem_ld32(tS + q4 * 32, sr[q4]);
+        tmem_wait_ld();
+        float* s = reinterpret_cast<float*>(&sr[0][0]);
+
+        const int kv0 = j * pf::BN;
+        const bool need_mask =
+            (kv0 + pf::BN > p.Sk) || (p.causal && kv0 + pf::BN - 1 > row0 + off);
+        // Row max in the log2 domain.  Masked tiles are scaled first and get
+        // -inf at hidden keys (cc = 1 afterwards); mask-free tiles take the max
+        // (or, for a negative scale, the min) of the raw scores times c.
+        float mx, cc = c;
+        if (need_mask) {
+          const int lim_c = p.causal ? grow + off + 1 : p.Sk;  // keys [0, lim) visible
+          const int lim = (lim_c < p.Sk ? lim_c : p.Sk) - kv0;
+#pragma unroll
+          for (int x = 0; x < pf::BN; ++x) s[x] = (x < lim) ? s[x] * c : NEG_INF;
+          cc = 1.f;
+          float a0 = s[0], a1 = s[1], a2 = s[2], a3 = s[3];
+#pragma unroll
+          for (int x = 4; x < pf::BN; x += 4) {
+            a0 = fmaxf(a0, s[x]);
+            a1 = fmaxf(a1, s[x + 1]);
+            a2 = fmaxf(a2, s[x + 2]);
+            a3 = fmaxf(a3, s[x + 3]);
+          }
+          mx = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
+        } else if (!neg_scale) {
+          float a0 = s[0], a1 = s[1], a2 = s[2], a3 = s[3];
+#pragma unroll
+          for (int x = 4; x < pf::BN; x += 4) {
+            a0 = fmaxf(a0, s[x]);
+            a1 = fmaxf(a1, s[x + 1]);
+            a2 = fmaxf(a2, s[x + 2]);
+            a3 = fmaxf(a3, s[x + 3]);
+          }
+          mx = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * c;
+        } else {
+          float a0 = s[0], a1 = s[1], a2 = s[2], a3 = s[3];
+#pragma unroll
+          for (int x = 4; x < pf::BN; x += 4) {
+            a0 = fminf(a0, s[x]);
+            a1 = fminf(a1, s[x + 1]);
+            a2 = fminf(a2, s[x + 2]);
+            a3 = fminf(a3, s[x + 3]);
+          }
+          mx = fminf(fminf(a0, a1), fminf(a2, a3)) * c;
+        }
+        const float m_new = fmaxf(m_used, mx);
+        // Lazy rescale: only when the max grew by more than TAU (log2 domain).
+        // On the first tile O holds nothing yet (the first P@V overwrites it).
+        float f = 1.f;
+        bool resc = false;
+        if (j == 0) {
+          m_used = m_new;
+        } else {
+          resc = (m_new - m_used) > pf::TAU;
+          if (resc) {
+            f = fast_exp2(m_used - m_new);
+            l *= f;
+            m_used = m_new;
+          }
+        }
+        const float base = (m_used == NEG_INF) ? 0.f : m_used;
+        // P = exp2(s*c - base), packed to the input type, written over S.
+        float l0 = 0.f, l1 = 0.f;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int x = 0; x < 32; ++x) {
+            const float p0 = fast_exp2(fmaf(s[hh * 64 + 2 * x], cc, -base));
+            const float p1 = fast_exp2(fmaf(s[hh * 64 + 2 * x + 1], cc, -base));
+            l0 += p0;
+            l1 += p1;
+            pk[x] = Pack2<T>::pack(p0, p1);
+          }
+          tmem_st32(tS + hh * 32, pk);
+        }
+        l += l0 + l1;
+        // O *= f for the rows whose max moved.  P_i(j) is not consumed before
+        // p_full is signalled below, and P_i(j-1) @ V has completed (it was
+        // issued before S_i(j), whose completion we waited for).
+        if (__any_sync(0xffffffffu, resc)) {
+#pragma unroll
+          for (int q4 = 0; q4 < D / 32; ++q4) {
+            uint32_t orr[32];
+            tmem_ld32(tO + q4 * 32, orr);
+            tmem_wait_ld();
+#pragma unroll
+            for (int x = 0; x < 32; ++x) orr[x] = __float_as_uint(__uint_as_float(orr[x]) * f);
+            tmem_st32(tO + q4 * 32, orr);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&p_full[i]);
+      }
+      if (!ok) break;
+      // Epilogue: O / l, rounded once, 16-byte stores.
+      if (!(ok = mbar_wait(&o_full[i], o_cnt & 1, abort_flag, &g_prefill_err, 11 + i))) break;
+      ++o_cnt;
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+      for (int q4 = 0; q4 < D / 32; ++q4) {
+        uint32_t orr[32];
+        tmem_ld32(tO + q4 * 32, orr);
+        tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int x = 0; x < 16; ++x)
+          pk[x] = Pack2<T>::pack(__uint_as_float(orr[2 * x]) * inv,
+                                 __uint_as_float(orr[2 * x + 1]) * inv);
+        if (grow < p.Sq) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + q4 * 32);
+#pragma unroll
+          for (int x = 0; x < 4; ++x)
+            dst[x] = make_uint4(pk[4 * x], pk[4 * x + 1], pk[4 * x + 2], pk[4 * x + 3]);
+        }
+      }
+      tc_fence_before();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// Sk == 0: no key is visible to any row, O = 0.
+template <typename T>
+__global__ void prefill_zero_kernel(T* o, size_t n) {
+  for (size_t x = blockIdx.x * (size_t)blockDim.x + threadIdx.x; x < n;
+       x += (size_t)gridDim.x * blockDim.x)
+    o[x] = T(0.f);
+}
+
+template <int D, typename T>
+static int launch_prefill_t(const void* q, const void* k, const void* v, void* o, int B, int Hq,
+                            int Hkv, int Sq, int Sk, float scale, int causal,
+                            cudaStream_t stream) {
+  using C = pf::Cfg<D>;
+  CUtensorMap tq, tk, tv;
+  if (encode_tmap_rows(&tq, q, D, Hq, Sq, B, pf::BM)) return cudaErrorInvalidValue;
+  if (encode_tmap_rows(&tk, k, D, Hkv, Sk, B, pf::BN)) return cudaErrorInvalidValue;
+  if (encode_tmap_rows(&tv, v, D, Hkv, Sk, B, pf::BN)) return cudaErrorInvalidValue;
+  static int attr_set[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, T>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM_TOTAL);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = 1;
+  }
+  PrefillParams p;
+  p.o = o;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.Sq = Sq;
+  p.Sk = Sk;
+  p.G = Hq / Hkv;
+  p.causal = causal ? 1 : 0;
+  p.n_qb = (Sq + pf::QBLOCK - 1) / pf::QBLOCK;
+  p.n_items = B * Hq * p.n_qb;
+  p.c = scale * 1.4426950408889634f;
+  const int sms = sm_count() > 0 ? sm_count() : 148;
+  const int grid = p.n_items < sms ? p.n_items : sms;
+  prefill_kernel<D, T><<<grid, pf::THREADS, C::SMEM_TOTAL, stream>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+int launch_prefill(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv,
+                   int Sq, int Sk, int D, float scale, int causal, bool bf16,
+                   cudaStream_t stream) {
+  if (B == 0 || Hq == 0 || Sq == 0) return cudaSuccess;
+  if (Sk == 0) {
+    const size_t n = (size_t)B * Sq * Hq * D;
+    const unsigned blocks = (unsigned)((n + 255) / 256 < 8192 ? (n + 255) / 256 : 8192);
+    if (bf16)
+      prefill_zero_kernel<__nv_bfloat16><<<blocks, 256, 0, stream>>>(
+          static_cast<__nv_bfloat16*>(o), n);
+    else
+      prefill_zero_kernel<__half><<<blocks, 256, 0, stream>>>(static_cast<__half*>(o), n);
+    return cudaGetLastError();
+  }
+  if (D == 64)
+    return bf16 ? launch_prefill_t<64, __nv_bfloat16>(q, k, v, o, B, Hq, Hkv, Sq, Sk, scale,
+                                                       causal, stream)
+                : launch_prefill_t<64, __half>(q, k, v, o, B, Hq, Hkv, Sq, Sk, scale, causal,
+                                               stream);
+  return bf16 ? launch_prefill_t<128, __nv_bfloat16>(q, k, v, o, B, Hq, Hkv, Sq, Sk, scale,
+                                                      causal, stream)
+              : launch_prefill_t<128, __half>(q, k, v, o, B, Hq, Hkv, Sq, Sk, scale, causal,
+                                              stream);
+}
+
+int read_prefill_error(unsigned int* out, int reset) {
+  unsigned int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_prefill_err, sizeof(v));
+  if (e != cudaSuccess) return e;
+  if (reset && v) {
+    const unsigned int z = 0;
+    e = cudaMemcpyToSymbol(g_prefill_err, &z, sizeof(z));
+    if (e != cudaSuccess) return e;
+  }
+  *out = v;
+  return cudaSuccess;
+}
+
+}  // namespace fa

@@ -1,0 +1,147 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) flash-attention forward library
+ *         (libfa_gb300.so).
+ *
+ * Two operations:
+ *
+ *   fa_prefill_fwd  dense attention forward, O = softmax(scale * Q K^T + mask) V,
+ *                   for bf16/fp16, head_dim 64 or 128, MHA or GQA, causal or
+ *                   not, Sq != Sk allowed.
+ *                   Defined by: "Dense flash-attention prefill (gfx950 / MI355X)"
+ *                   (opening paragraph: forward-only, bf16/fp16, head_dim
+ *                   64/128, MHA or GQA, causal) and tessera #90
+ *                   "compiler-generated flash_attn fwd+bwd" (flash_attn forward
+ *                   commit note: S = scale*Q@K^T, causal/ragged mask, online
+ *                   softmax, O += P@V; Sq/Sk/scale/causal are runtime values).
+ *
+ *   fa_decode_fwd   single-token attention over a KV cache whose valid length
+ *                   lives in device memory, split over the sequence and merged
+ *                   with a log-sum-exp combine.
+ *                   Defined by: rocm-libraries #13108 "minimal single-token
+ *                   attention decode" (interface description: Sq=1, contiguous
+ *                   token-major K/V cache, device INT32 valid length, O only;
+ *                   review finding: unused cache capacity may hold NaN and must
+ *                   not reach the output; split-KV named as the next step).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Tensors are contiguous, row-major, in device memory (or memory the device
+ *   can address), 16-byte aligned:
+ *       q, o   : [B, Sq, Hq,  D]     (decode: Sq = 1)
+ *       k, v   : [B, Sk, Hkv, D]     (decode: [B, cap, Hkv, D], token-major)
+ *   Query head h reads K/V head h / (Hq / Hkv) (contiguous GQA groups).
+ * - The caller owns and allocates every tensor, including o.  The library
+ *   keeps no pointer after the call returns.
+ * - Work is enqueued on `stream`; no call synchronises the host.  A status of
+ *   FA_OK means the work was validated and enqueued; device-side failures
+ *   (a pipeline wait that exceeded its time limit) are reported by
+ *   fa_device_error().
+ * - Arguments are validated before anything touches the GPU; invalid
+ *   arguments return FA_ERR_INVALID_ARG and enqueue nothing.
+ * - Empty problems (B == 0, Sq == 0 or Hq == 0) are valid and enqueue nothing.
+ *   Rows with no visible key (Sk == 0, or causal rows i with i + Sk - Sq < 0)
+ *   produce O = 0.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { FA_BF16 = 0, FA_FP16 = 1 } fa_dtype_t;
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,  /* bad pointer, size, head config or dtype         */
+  FA_ERR_UNSUPPORTED = 2,  /* valid request this build does not implement     */
+  FA_ERR_CUDA = 3,         /* a CUDA runtime/driver call or launch failed     */
+  FA_ERR_TIMEOUT = 4       /* a device-side pipeline wait hit its time limit  */
+} fa_status_t;
+
+/*
+ * fa_prefill_fwd -- attention forward for a batch of full sequences.
+ *
+ *   q      [B, Sq, Hq, D]   bf16 or fp16 (dtype), read only
+ *   k, v   [B, Sk, Hkv, D]  same dtype, read only
+ *   o      [B, Sq, Hq, D]   same dtype, written (every element of every row)
+ *   Hq % Hkv == 0; D in {64, 128}; Sq, Sk >= 0; B, Hq, Hkv >= 0.
+ *   scale  multiplies Q K^T (any finite value, applied as passed).
+ *   causal nonzero: row i sees keys j <= i + (Sk - Sq) (bottom-right aligned;
+ *          equals the usual top-left mask when Sq == Sk).
+ *   dtype  FA_BF16 or FA_FP16.
+ *
+ * Arithmetic: Q K^T and P V on the tensor cores with fp32 accumulation;
+ * softmax in fp32 (exp2 domain); P rounded to the input dtype before P V;
+ * O = (P V) / l rounded once to the output dtype (round to nearest even).
+ *
+ * Returns FA_OK, FA_ERR_INVALID_ARG (null/misaligned pointer, negative size,
+ * Hq % Hkv != 0, D not 64/128, unknown dtype, non-finite scale),
+ * or FA_ERR_CUDA (tensor-map encode, attribute or launch failure).
+ */
+int fa_prefill_fwd(const void* q, const void* k, const void* v, void* o,
+                   int B, int Hq, int Hkv, int Sq, int Sk, int D,
+                   float scale, int causal, int dtype, cudaStream_t stream);
+
+/*
+ * fa_decode_fwd -- one new query token per sequence against a KV cache.
+ *
+ *   q              [B, 1, Hq, D]      bf16, read only
+ *   kcache, vcache [B, cap, Hkv, D]   bf16, token-major, read only
+ *   valid_len_dev  one int32 in device memory: the number of valid tokens L,
+ *                  shared by the batch.  It is read by the kernels only (never
+ *                  by the host), so the call never synchronises.  L is
+ *                  clamped to [0, cap]; L == 0 gives O = 0.
+ *   o              [B, 1, Hq, D]      bf16, written
+ *   Hq % Hkv == 0; D in {64, 128}; cap >= 0.
+ *
+ * Cache entries at token positions >= L may hold anything, NaN and Inf
+ * included: they are never used in arithmetic (zeroed in shared memory before
+ * any MMA and given probability zero).
+ *
+ * Scratch: the split partials (fp32) are allocated stream-ordered on `stream`
+ * (cudaMallocAsync / cudaFreeAsync), so calls on different streams never share
+ * scratch.  Two kernels are enqueued: the split kernel and the combine.
+ *
+ * Returns FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED (dtype other than
+ * bf16), or FA_ERR_CUDA.
+ */
+int fa_decode_fwd(const void* q, const void* kcache, const void* vcache,
+                  const int32_t* valid_len_dev, void* o,
+                  int B, int Hq, int Hkv, int cap, int D, float scale,
+                  cudaStream_t stream);
+
+/* Static, human-readable name of a status code (never NULL). */
+const char* fa_status_string(int status);
+
+/*
+ * fa_device_error -- read (and if reset != 0, clear) the device-side error
+ * word of the current device.  Synchronises the current device.  Returns
+ * FA_OK if no kernel reported a failure, FA_ERR_TIMEOUT if a pipeline wait
+ * hit its time limit, FA_ERR_CUDA if the read itself failed.
+ * If detail != NULL it receives the raw error bits.
+ */
+int fa_device_error(int reset, unsigned int* detail);
+
+/* Number of SMs the persistent prefill grid uses on the current device
+ * (queried once per device), or a negative value on failure. */
+int fa_num_sms(void);
+
+/*
+ * fa_prefill_work_item -- host copy of the persistent scheduler's work-item
+ * decode, for inspection and tests.  Work item w in [0, n_items) maps to
+ * (b, hq, qblock); a qblock is 256 query rows.  Returns the number of items
+ * n_items = B * Hq * ceil(Sq / 256), and fills *b, *hq, *qblock when
+ * 0 <= w < n_items (the pointers may be NULL).  Returns -1 on bad arguments.
+ */
+int fa_prefill_work_item(int w, int B, int Hq, int Hkv, int Sq, int Sk, int causal,
+                         int* b, int* hq, int* qblock);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */
