@@ -23,7 +23,7 @@ FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = 0, 
 
 # Every symbol include/fa.h declares (checked by the tests against the header).
 EXPORTS = ("fa_prefill_fwd", "fa_decode_fwd", "fa_status_string", "fa_device_error",
-           "fa_num_sms", "fa_prefill_work_item")
+           "fa_last_cuda_error", "fa_num_sms", "fa_prefill_work_item")
 
 _lib = None
 
@@ -31,7 +31,11 @@ _lib = None
 class FAError(RuntimeError):
     def __init__(self, status, what):
         self.status = status
-        super().__init__(f"{what}: {fa_status_string(status)} (status {status})")
+        extra = ""
+        if status == FA_ERR_CUDA:
+            code, site = fa_last_cuda_error()
+            extra = f"; cudaError {code} at {site}"
+        super().__init__(f"{what}: {fa_status_string(status)} (status {status}{extra})")
 
 
 def load(path: str = LIB_PATH):
@@ -53,6 +57,8 @@ def load(path: str = LIB_PATH):
     lib.fa_status_string.restype = ctypes.c_char_p
     lib.fa_device_error.argtypes = [i32, ctypes.POINTER(ctypes.c_uint)]
     lib.fa_device_error.restype = i32
+    lib.fa_last_cuda_error.argtypes = [ctypes.POINTER(ctypes.c_char_p)]
+    lib.fa_last_cuda_error.restype = i32
     lib.fa_num_sms.argtypes = []
     lib.fa_num_sms.restype = i32
     ip = ctypes.POINTER(ctypes.c_int)
@@ -83,6 +89,13 @@ def fa_device_error(reset=1):
     detail = ctypes.c_uint(0)
     st = load().fa_device_error(int(reset), ctypes.byref(detail))
     return st, detail.value
+
+
+def fa_last_cuda_error():
+    """(raw cudaError_t, failing call) of this thread's latest FA_ERR_CUDA."""
+    site = ctypes.c_char_p()
+    code = load().fa_last_cuda_error(ctypes.byref(site))
+    return code, (site.value or b"").decode()
 
 
 def fa_num_sms() -> int:

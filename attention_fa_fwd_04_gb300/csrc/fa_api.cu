@@ -64,9 +64,15 @@ int sm_count() {
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-static int cuda_status(int e) {
+// Raw CUDA error and call site of the most recent FA_ERR_CUDA in this thread.
+static thread_local int t_last_cuda_error = 0;
+static thread_local const char* t_last_site = "";
+
+static int cuda_status(int e, const char* site) {
   if (e == 0) return FA_OK;
-  cudaGetLastError();  // clear a sticky launch-config error so later calls start clean
+  t_last_cuda_error = e;
+  t_last_site = site;
+  cudaGetLastError();  // clear a non-sticky error so later calls start clean
   return FA_ERR_CUDA;
 }
 
@@ -88,7 +94,8 @@ extern "C" int fa_prefill_fwd(const void* q, const void* k, const void* v, void*
   if ((int64_t)Sq * Hq * D * 2 >= (1ll << 40) || (int64_t)Sk * Hkv * D * 2 >= (1ll << 40))
     return FA_ERR_INVALID_ARG;
   return cuda_status(fa::launch_prefill(q, k, v, o, B, Hq, Hkv, Sq, Sk, D, scale, causal,
-                                        dtype == FA_BF16, stream));
+                                        dtype == FA_BF16, stream),
+                     "prefill launch");
 }
 
 extern "C" int fa_decode_fwd(const void* q, const void* kcache, const void* vcache,
@@ -107,16 +114,17 @@ extern "C" int fa_decode_fwd(const void* q, const void* kcache, const void* vcac
   if ((int64_t)cap * Hkv * D * 2 >= (1ll << 40)) return FA_ERR_INVALID_ARG;
   if (cap == 0)
     return cuda_status(fa::launch_decode(q, kcache, vcache, valid_len_dev, o, B, Hq, Hkv, 0, D,
-                                         scale, nullptr, 0, stream));
+                                         scale, nullptr, 0, stream),
+                       "decode zero-fill launch");
   const size_t nf = fa::decode_scratch_floats(B, Hq, Hkv, cap, D);
   void* scratch = nullptr;
   cudaError_t e = cudaMallocAsync(&scratch, nf * sizeof(float), stream);
-  if (e != cudaSuccess) return cuda_status(e);
+  if (e != cudaSuccess) return cuda_status(e, "decode cudaMallocAsync");
   int r = fa::launch_decode(q, kcache, vcache, valid_len_dev, o, B, Hq, Hkv, cap, D, scale,
                             static_cast<float*>(scratch), nf, stream);
   cudaError_t ef = cudaFreeAsync(scratch, stream);
-  if (r != 0) return cuda_status(r);
-  return cuda_status(ef);
+  if (r != 0) return cuda_status(r, "decode launch");
+  return cuda_status(ef, "decode cudaFreeAsync");
 }
 
 extern "C" const char* fa_status_string(int status) {
@@ -140,6 +148,11 @@ extern "C" int fa_device_error(int reset, unsigned int* detail) {
 }
 
 extern "C" int fa_num_sms(void) { return fa::sm_count(); }
+
+extern "C" int fa_last_cuda_error(const char** site) {
+  if (site) *site = t_last_site;
+  return t_last_cuda_error;
+}
 
 extern "C" int fa_prefill_work_item(int w, int B, int Hq, int Hkv, int Sq, int Sk, int causal,
                                     int* b, int* hq, int* qblock) {

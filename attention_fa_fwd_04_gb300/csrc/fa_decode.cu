@@ -34,21 +34,29 @@ namespace fa {
 __device__ unsigned int g_decode_err = 0;
 
 namespace dec {
-constexpr int TT = 64;        // tokens per tile
-constexpr int NSTAGE = 6;     // ring depth (tiles in flight per CTA)
+constexpr int TT = 32;        // tokens per tile
 constexpr int NWARPS = 4;     // consumer warps
 constexpr int THREADS = (NWARPS + 1) * 32;
 constexpr int HB = 16;        // query heads per CTA: the MMA's M
 constexpr int HALF_BYTES = TT * 128;  // TT rows x 64 elements x 2 bytes
 
+// Tile t lives in stage t % NSTAGE and is consumed by warp t % NWARPS.  With
+// NSTAGE a multiple of NWARPS every stage belongs to exactly one warp, which
+// therefore waits on that stage's phases strictly in order.  (A parity wait
+// must never run ahead by a phase: if two warps shared a stage, the faster one
+// could see the stage's previous phase as "complete" and consume a tile that
+// has not landed.)
 template <int D>
 struct Cfg {
   static constexpr int HALVES = D / 64;
+  static constexpr int NSTAGE = (D == 128) ? 8 : 16;    // 128 KiB of tiles in flight
   static constexpr int KV_BYTES = HALVES * HALF_BYTES;  // one K (or V) tile
   static constexpr int STAGE_BYTES = 2 * KV_BYTES;      // K tile + V tile
   static constexpr int SMEM_STAGES = NSTAGE * STAGE_BYTES;
+  static_assert(NSTAGE % NWARPS == 0, "each stage must belong to one consumer warp");
   static constexpr int SMEM_RED = HB * D * 4 + NWARPS * HB * 2 * 4;
   static constexpr int SMEM_BAR = 2 * NSTAGE * 8 + 16;
+  static_assert(HALF_BYTES % 1024 == 0, "128-byte-swizzled tiles need 1 KiB alignment");
   static constexpr int SMEM_TOTAL = 1024 + SMEM_STAGES + SMEM_RED + SMEM_BAR;
 };
 }  // namespace dec
@@ -73,7 +81,7 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
     decode_split_kernel(const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const DecodeParams p) {
   using C = dec::Cfg<D>;
-  constexpr int TT = dec::TT, NSTAGE = dec::NSTAGE, HB = dec::HB, NW = dec::NWARPS;
+  constexpr int TT = dec::TT, NSTAGE = C::NSTAGE, HB = dec::HB, NW = dec::NWARPS;
   constexpr float NEG_INF = -INFINITY;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -118,16 +126,19 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
   for (int nd = 0; nd < D / 8; ++nd) acc[nd][0] = acc[nd][1] = acc[nd][2] = acc[nd][3] = 0.f;
 
   if (warp == NW) {
-    // ---------------- producer: one lane issues all TMA loads ----------------
-    if (lane == 0 && n_tiles > 0) {
+    // ---------------- producer warp: lanes stay converged, lane 0 issues ----------------
+    const bool leader = lane == 0;
+    if (leader && n_tiles > 0) {
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      const uint64_t pol = l2_policy_evict_first();
-      int t = 0;
-      for (; t < n_tiles; ++t) {
-        const int s = t % NSTAGE;
-        const uint32_t ph = (t / NSTAGE) & 1;
-        if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, &g_decode_err, 1)) break;
+    }
+    const uint64_t pol = l2_policy_evict_first();
+    int t = 0;
+    for (; t < n_tiles; ++t) {
+      const int s = t % NSTAGE;
+      const uint32_t ph = (t / NSTAGE) & 1;
+      if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, &g_decode_err, 1)) break;
+      if (leader) {
         mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
         const int tok = (t_begin + t) * TT;
         uint8_t* st = stages + s * C::STAGE_BYTES;
@@ -139,12 +150,14 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
           tma_load_4d_hint(st + C::KV_BYTES + h * dec::HALF_BYTES, &tmV, &full[s], h * 64, hkv,
                            tok, b, pol);
       }
-      if (t < n_tiles) {
-        // Aborted: let the loads already issued land before the CTA exits.
-        for (int u = (t - NSTAGE > 0 ? t - NSTAGE : 0); u < t; ++u)
-          mbar_wait_drain(&full[u % NSTAGE], (u / NSTAGE) & 1);
-      }
+      __syncwarp();
     }
+    if (t < n_tiles) {
+      // Aborted: let the loads already issued land before the CTA exits.
+      for (int u = (t - NSTAGE > 0 ? t - NSTAGE : 0); u < t; ++u)
+        mbar_wait_drain(&full[u % NSTAGE], (u / NSTAGE) & 1);
+    }
+    __syncwarp();
   } else {
     // ---------------- consumers: whole tiles, round-robin over warps ----------------
     // Q as the MMA's A operand (rows = the CTA's query heads, padded to 16).
@@ -167,6 +180,7 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
       const int s = t % NSTAGE;
       const uint32_t ph = (t / NSTAGE) & 1;
       if (!mbar_wait(&full[s], ph, abort_flag, &g_decode_err, 2)) break;
+      __syncwarp();  // ldmatrix / mma.sync below are warp-collective
       uint8_t* st = stages + s * C::STAGE_BYTES;
       const int tok0 = (t_begin + t) * TT;
       const int nvalid = (L - tok0) < TT ? (L - tok0) : TT;
@@ -187,14 +201,15 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
         __syncwarp();
       }
 
-      // S = Q K^T: 16 heads x 64 tokens, 8 n-blocks of 8 tokens.
-      float sc[8][4];
+      // S = Q K^T: 16 heads x TT tokens, TT/8 n-blocks of 8 tokens.
+      constexpr int NB = TT / 8;
+      float sc[NB][4];
 #pragma unroll
-      for (int nb = 0; nb < 8; ++nb) sc[nb][0] = sc[nb][1] = sc[nb][2] = sc[nb][3] = 0.f;
+      for (int nb = 0; nb < NB; ++nb) sc[nb][0] = sc[nb][1] = sc[nb][2] = sc[nb][3] = 0.f;
       const uint32_t kbase = smem_u32(st);
       const int mi = lane >> 3;
 #pragma unroll
-      for (int np = 0; np < 4; ++np) {
+      for (int np = 0; np < NB / 2; ++np) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const int tok = np * 16 + (mi >> 1) * 8 + (lane & 7);
@@ -209,7 +224,7 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
       }
       // Scale into the log2 domain, then mask tokens >= L.
 #pragma unroll
-      for (int nb = 0; nb < 8; ++nb)
+      for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           sc[nb][e] *= p.c;
@@ -218,7 +233,7 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
       // Online softmax over this warp's tiles.
       float mx0 = NEG_INF, mx1 = NEG_INF;
 #pragma unroll
-      for (int nb = 0; nb < 8; ++nb) {
+      for (int nb = 0; nb < NB; ++nb) {
         mx0 = fmaxf(mx0, fmaxf(sc[nb][0], sc[nb][1]));
         mx1 = fmaxf(mx1, fmaxf(sc[nb][2], sc[nb][3]));
       }
@@ -234,7 +249,7 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
       m1 = mn1;
       float rs0 = 0.f, rs1 = 0.f;
 #pragma unroll
-      for (int nb = 0; nb < 8; ++nb) {
+      for (int nb = 0; nb < NB; ++nb) {
         sc[nb][0] = fast_exp2(sc[nb][0] - base0);
         sc[nb][1] = fast_exp2(sc[nb][1] - base0);
         sc[nb][2] = fast_exp2(sc[nb][2] - base1);
@@ -255,7 +270,7 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
       // transposing ldmatrix.
       const uint32_t vbase = kbase + C::KV_BYTES;
 #pragma unroll
-      for (int k2 = 0; k2 < 4; ++k2) {
+      for (int k2 = 0; k2 < TT / 16; ++k2) {
         uint32_t a[4];
         a[0] = pack_bf16(sc[2 * k2][0], sc[2 * k2][1]);
         a[1] = pack_bf16(sc[2 * k2][2], sc[2 * k2][3]);
@@ -277,6 +292,7 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
       if (lane == 0) mbar_arrive(&empty[s]);
     }
     // Per-warp row sums (each quad holds one row's partial sums).
+    __syncwarp();
     l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
     l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
@@ -319,7 +335,12 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
 
   // Write this split's partial for the CTA's valid heads.
   const size_t head0 = (size_t)b * p.Hq + (size_t)hkv * p.G + (size_t)hb * HB;
-  const int nh = (p.G - hb * HB) < HB ? (p.G - hb * HB) : HB;
+  int nh = (p.G - hb * HB) < HB ? (p.G - hb * HB) : HB;
+  // Self-check: partial rows must lie inside the scratch (records and skips).
+  if (b >= p.B || split >= p.nsplit || head0 + nh > (size_t)p.B * p.Hq) {
+    if (threadIdx.x == 0) atomicOr(&g_decode_err, kErrBounds);
+    nh = 0;
+  }
   for (int x = threadIdx.x; x < nh * D; x += dec::THREADS) {
     const int row = x / D, d = x % D;
     p.part_o[((head0 + row) * p.nsplit + split) * D + d] = red_o[x];
@@ -344,6 +365,10 @@ template <int D>
 __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams p) {
   pdl_wait_primary();
   const int h = blockIdx.x, b = blockIdx.y;
+  if (h >= p.Hq || b >= p.B) {
+    if (threadIdx.x == 0) atomicOr(&g_decode_err, kErrBounds << 4);
+    return;
+  }
   const size_t base = ((size_t)b * p.Hq + h) * p.nsplit;
   float M = -INFINITY;
   for (int s = 0; s < p.nsplit; ++s) M = fmaxf(M, p.part_ml[(base + s) * 2]);

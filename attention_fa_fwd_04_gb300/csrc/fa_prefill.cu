@@ -182,69 +182,84 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
 
   const int off = p.Sk - p.Sq;  // bottom-right causal offset
 
+  // The producer and MMA warps run their loops with all 32 lanes converged:
+  // every lane waits on the barriers, lane 0 alone issues TMA / MMA / commit,
+  // and __syncwarp() follows each issue.  (A warp must never reach the
+  // warp-aligned CTA barrier below, or tcgen05.dealloc, with lanes still
+  // inside a role loop.)
+  const bool leader = lane == 0;
   if (warp == 8) {
     // ============================ TMA producer ============================
-    if (lane == 0) {
+    if (leader) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      const uint64_t pol_q = l2_policy_evict_first();
-      const uint64_t pol_kv = l2_policy_evict_last();
-      uint32_t kv_cnt = 0, local = 0;
-      bool ok = true;
-      for (int w = blockIdx.x; w < p.n_items && ok; w += gridDim.x, ++local) {
-        int b, hq, qb;
-        prefill_item(w, p.B, p.Hq, p.Hkv, p.n_qb, &b, &hq, &qb);
-        const int hkv = hq / p.G;
-        const int row0 = qb * pf::QBLOCK;
-        const int n0 = kv_tiles_for(row0, p.Sq, p.Sk, p.causal);
-        const int n1 = kv_tiles_for(row0 + pf::BM, p.Sq, p.Sk, p.causal);
-        const int n = n0 > n1 ? n0 : n1;
-        if (local > 0 && !(ok = mbar_wait(q_empty, (local - 1) & 1, abort_flag, &g_prefill_err, 1)))
-          break;
+    }
+    const uint64_t pol_q = l2_policy_evict_first();
+    const uint64_t pol_kv = l2_policy_evict_last();
+    uint32_t kv_cnt = 0, local = 0;
+    bool ok = true, q_issued = false;
+    for (int w = blockIdx.x; w < p.n_items && ok; w += gridDim.x, ++local) {
+      int b, hq, qb;
+      prefill_item(w, p.B, p.Hq, p.Hkv, p.n_qb, &b, &hq, &qb);
+      const int hkv = hq / p.G;
+      const int row0 = qb * pf::QBLOCK;
+      const int n0 = kv_tiles_for(row0, p.Sq, p.Sk, p.causal);
+      const int n1 = kv_tiles_for(row0 + pf::BM, p.Sq, p.Sk, p.causal);
+      const int n = n0 > n1 ? n0 : n1;
+      q_issued = false;
+      if (local > 0 && !(ok = mbar_wait(q_empty, (local - 1) & 1, abort_flag, &g_prefill_err, 1)))
+        break;
+      if (leader) {
         mbar_arrive_expect_tx(q_full, 2 * C::TILE_BYTES);
 #pragma unroll
         for (int i = 0; i < 2; ++i)
 #pragma unroll
           for (int h = 0; h < C::HALVES; ++h)
-            tma_load_4d_hint(sQ + i * C::TILE_BYTES + h * pf::HALF_BYTES, &tmQ, q_full, h * 64, hq,
-                             row0 + i * pf::BM, b, pol_q);
-        for (int j = 0; j < n && ok; ++j) {
+            tma_load_4d_hint(sQ + i * C::TILE_BYTES + h * pf::HALF_BYTES, &tmQ, q_full, h * 64,
+                             hq, row0 + i * pf::BM, b, pol_q);
+      }
+      __syncwarp();
+      q_issued = true;
+      for (int j = 0; j < n && ok; ++j) {
 #pragma unroll
-          for (int sel = 0; sel < 2; ++sel) {
-            const int s = kv_cnt % NSTAGE;
-            const uint32_t ph = (kv_cnt / NSTAGE) & 1;
-            if (!(ok = mbar_wait(&empty[s], ph ^ 1, abort_flag, &g_prefill_err, 2))) break;
+        for (int sel = 0; sel < 2; ++sel) {
+          const int s = kv_cnt % NSTAGE;
+          const uint32_t ph = (kv_cnt / NSTAGE) & 1;
+          if (!(ok = mbar_wait(&empty[s], ph ^ 1, abort_flag, &g_prefill_err, 2))) break;
+          if (leader) {
             mbar_arrive_expect_tx(&full[s], C::TILE_BYTES);
             const CUtensorMap* m = sel ? &tmV : &tmK;
 #pragma unroll
             for (int h = 0; h < C::HALVES; ++h)
               tma_load_4d_hint(sKV + s * C::TILE_BYTES + h * pf::HALF_BYTES, m, &full[s], h * 64,
                                hkv, j * pf::BN, b, pol_kv);
-            ++kv_cnt;
           }
+          __syncwarp();
+          ++kv_cnt;
         }
       }
-      if (!ok) {
-        // Aborted: wait (bounded) for the loads already in flight.
-        const uint32_t first = kv_cnt > (uint32_t)NSTAGE ? kv_cnt - NSTAGE : 0u;
-        for (uint32_t u = first; u < kv_cnt; ++u)
-          mbar_wait_drain(&full[u % NSTAGE], (u / NSTAGE) & 1);
-        if (local > 0) mbar_wait_drain(q_full, (local - 1) & 1);
-      }
     }
+    if (!ok) {
+      // Aborted: wait (bounded) for the loads already in flight before exiting.
+      const uint32_t first = kv_cnt > (uint32_t)NSTAGE ? kv_cnt - NSTAGE : 0u;
+      for (uint32_t u = first; u < kv_cnt; ++u)
+        mbar_wait_drain(&full[u % NSTAGE], (u / NSTAGE) & 1);
+      if (q_issued) mbar_wait_drain(q_full, local & 1);
+    }
+    __syncwarp();
   } else if (warp == 9) {
     // ============================ MMA issuer ============================
-    if (lane == 0) {
-      constexpr uint32_t IDESC_S = idesc_f16(pf::BM, pf::BN, kBF16, false);
-      constexpr uint32_t IDESC_O = idesc_f16(pf::BM, D, kBF16, true);
-      const uint32_t sq_addr = smem_u32(sQ);
-      const uint32_t skv_addr = smem_u32(sKV);
-      uint32_t kv_cnt = 0, local = 0, p_cnt0 = 0, p_cnt1 = 0;
-      bool ok = true;
+    constexpr uint32_t IDESC_S = idesc_f16(pf::BM, pf::BN, kBF16, false);
+    constexpr uint32_t IDESC_O = idesc_f16(pf::BM, D, kBF16, true);
+    const uint32_t sq_addr = smem_u32(sQ);
+    const uint32_t skv_addr = smem_u32(sKV);
+    uint32_t kv_cnt = 0, local = 0, p_cnt0 = 0, p_cnt1 = 0;
+    bool ok = true;
 
-      // S_i = Q_i K^T over D/16 k-steps (K-major A and B, 128-byte swizzle).
-      auto issue_s = [&](int i, int stage) {
+    // S_i = Q_i K^T over D/16 k-steps (K-major A and B, 128-byte swizzle).
+    auto issue_s = [&](int i, int stage) {
+      if (leader) {
         const uint32_t d_tmem = tmem + (i ? C::COL_S1 : C::COL_S0);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
@@ -253,9 +268,12 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
           const uint64_t bd = sdesc_sw128(skv_addr + stage * C::TILE_BYTES + hoff, 16, 1024);
           mma_ss(d_tmem, a, bd, IDESC_S, k > 0 ? 1u : 0u);
         }
-      };
-      // O_i (+)= P_i V over BN/16 k-steps; P_i from TMEM, V MN-major in smem.
-      auto issue_pv = [&](int i, int stage, bool accumulate) {
+      }
+      __syncwarp();
+    };
+    // O_i (+)= P_i V over BN/16 k-steps; P_i from TMEM, V MN-major in smem.
+    auto issue_pv = [&](int i, int stage, bool accumulate) {
+      if (leader) {
         const uint32_t d_tmem = tmem + (i ? C::COL_O1 : C::COL_O0);
         const uint32_t p_tmem = tmem + (i ? C::COL_S1 : C::COL_S0);
 #pragma unroll
@@ -264,86 +282,93 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
               sdesc_sw128(skv_addr + stage * C::TILE_BYTES + k * 16 * 128, pf::HALF_BYTES, 1024);
           mma_ts(d_tmem, p_tmem + k * 8, bd, IDESC_O, (accumulate || k > 0) ? 1u : 0u);
         }
-      };
+      }
+      __syncwarp();
+    };
+    // tcgen05.commit from the issuing lane: arrive on *bar once its MMAs are done.
+    auto commit = [&](uint64_t* bar) {
+      if (leader) mma_commit(bar);
+      __syncwarp();
+    };
 
-      for (int w = blockIdx.x; w < p.n_items && ok; w += gridDim.x, ++local) {
-        int b, hq, qb;
-        prefill_item(w, p.B, p.Hq, p.Hkv, p.n_qb, &b, &hq, &qb);
-        const int row0 = qb * pf::QBLOCK;
-        const int nt0 = kv_tiles_for(row0, p.Sq, p.Sk, p.causal);
-        const int nt1 = kv_tiles_for(row0 + pf::BM, p.Sq, p.Sk, p.causal);
-        const int n = nt0 > nt1 ? nt0 : nt1;
-        if (!(ok = mbar_wait(q_full, local & 1, abort_flag, &g_prefill_err, 3))) break;
-        tc_fence_after();
-        if (n == 0) {
-          mma_commit(q_empty);
-          continue;
-        }
-        // K_0 -> S_0(0), S_1(0)
-        int sK = kv_cnt % NSTAGE;
-        if (!(ok = mbar_wait(&full[sK], (kv_cnt / NSTAGE) & 1, abort_flag, &g_prefill_err, 4)))
+    for (int w = blockIdx.x; w < p.n_items && ok; w += gridDim.x, ++local) {
+      int b, hq, qb;
+      prefill_item(w, p.B, p.Hq, p.Hkv, p.n_qb, &b, &hq, &qb);
+      const int row0 = qb * pf::QBLOCK;
+      const int nt0 = kv_tiles_for(row0, p.Sq, p.Sk, p.causal);
+      const int nt1 = kv_tiles_for(row0 + pf::BM, p.Sq, p.Sk, p.causal);
+      const int n = nt0 > nt1 ? nt0 : nt1;
+      if (!(ok = mbar_wait(q_full, local & 1, abort_flag, &g_prefill_err, 3))) break;
+      tc_fence_after();
+      if (n == 0) {
+        commit(q_empty);
+        continue;
+      }
+      // K_0 -> S_0(0), S_1(0)
+      int sK = kv_cnt % NSTAGE;
+      if (!(ok = mbar_wait(&full[sK], (kv_cnt / NSTAGE) & 1, abort_flag, &g_prefill_err, 4)))
+        break;
+      tc_fence_after();
+      ++kv_cnt;
+      if (nt0 > 0) {
+        issue_s(0, sK);
+        commit(&s_full[0]);
+      }
+      if (nt1 > 0) {
+        issue_s(1, sK);
+        commit(&s_full[1]);
+      }
+      commit(&empty[sK]);
+      if (n == 1) commit(q_empty);
+
+      for (int j = 0; j < n && ok; ++j) {
+        const int sV = kv_cnt % NSTAGE;
+        if (!(ok = mbar_wait(&full[sV], (kv_cnt / NSTAGE) & 1, abort_flag, &g_prefill_err, 5)))
           break;
         tc_fence_after();
         ++kv_cnt;
-        if (nt0 > 0) {
-          issue_s(0, sK);
-          mma_commit(&s_full[0]);
-        }
-        if (nt1 > 0) {
-          issue_s(1, sK);
-          mma_commit(&s_full[1]);
-        }
-        mma_commit(&empty[sK]);
-        if (n == 1) mma_commit(q_empty);
-
-        for (int j = 0; j < n && ok; ++j) {
-          const int sV = kv_cnt % NSTAGE;
-          if (!(ok = mbar_wait(&full[sV], (kv_cnt / NSTAGE) & 1, abort_flag, &g_prefill_err, 5)))
+        const bool has_next = j + 1 < n;
+        if (has_next) {
+          sK = kv_cnt % NSTAGE;
+          if (!(ok = mbar_wait(&full[sK], (kv_cnt / NSTAGE) & 1, abort_flag, &g_prefill_err, 6)))
             break;
           tc_fence_after();
           ++kv_cnt;
-          const bool has_next = j + 1 < n;
-          if (has_next) {
-            sK = kv_cnt % NSTAGE;
-            if (!(ok = mbar_wait(&full[sK], (kv_cnt / NSTAGE) & 1, abort_flag, &g_prefill_err, 6)))
-              break;
-            tc_fence_after();
-            ++kv_cnt;
-          }
-          if (j < nt0) {
-            if (!(ok = mbar_wait(&p_full[0], p_cnt0 & 1, abort_flag, &g_prefill_err, 7))) break;
-            ++p_cnt0;
-            tc_fence_after();
-            issue_pv(0, sV, j > 0);
-            if (j == nt0 - 1) mma_commit(&o_full[0]);
-            if (j + 1 < nt0) {
-              issue_s(0, sK);
-              mma_commit(&s_full[0]);
-            }
-          }
-          if (j < nt1) {
-            if (!(ok = mbar_wait(&p_full[1], p_cnt1 & 1, abort_flag, &g_prefill_err, 8))) break;
-            ++p_cnt1;
-            tc_fence_after();
-            issue_pv(1, sV, j > 0);
-            if (j == nt1 - 1) mma_commit(&o_full[1]);
-            if (j + 1 < nt1) {
-              issue_s(1, sK);
-              mma_commit(&s_full[1]);
-            }
-          }
-          if (!ok) break;
-          mma_commit(&empty[sV]);
-          if (has_next) {
-            mma_commit(&empty[sK]);
-            if (j + 1 == n - 1) mma_commit(q_empty);
+        }
+        if (j < nt0) {
+          if (!(ok = mbar_wait(&p_full[0], p_cnt0 & 1, abort_flag, &g_prefill_err, 7))) break;
+          ++p_cnt0;
+          tc_fence_after();
+          issue_pv(0, sV, j > 0);
+          if (j == nt0 - 1) commit(&o_full[0]);
+          if (j + 1 < nt0) {
+            issue_s(0, sK);
+            commit(&s_full[0]);
           }
         }
+        if (j < nt1) {
+          if (!(ok = mbar_wait(&p_full[1], p_cnt1 & 1, abort_flag, &g_prefill_err, 8))) break;
+          ++p_cnt1;
+          tc_fence_after();
+          issue_pv(1, sV, j > 0);
+          if (j == nt1 - 1) commit(&o_full[1]);
+          if (j + 1 < nt1) {
+            issue_s(1, sK);
+            commit(&s_full[1]);
+          }
+        }
+        commit(&empty[sV]);
+        if (has_next) {
+          commit(&empty[sK]);
+          if (j + 1 == n - 1) commit(q_empty);
+        }
       }
-      // Every MMA issued by this thread has completed before TMEM is freed.
-      mma_commit(drain);
-      mbar_wait_drain(drain, 0);
     }
+    // Every MMA this warp issued has completed (and its commits have landed)
+    // before the CTA barrier that precedes the TMEM dealloc.
+    commit(drain);
+    mbar_wait_drain(drain, 0);
+    __syncwarp();
   } else {
     // ======================= softmax + epilogue (2 groups) =======================
     const int i = warp >> 2;          // Q tile handled by this warpgroup
@@ -366,7 +391,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       const int n_i = kv_tiles_for(row0, p.Sq, p.Sk, p.causal);
       T* const orow = O + ((size_t)b * p.Sq + grow) * (size_t)p.Hq * D + (size_t)hq * D;
       if (n_i == 0) {
-        if (grow < p.Sq) {
+        if (grow < p.Sq && b < p.B && hq < p.Hq) {
 #pragma unroll
           for (int x = 0; x < D / 8; ++x)
             reinterpret_cast<uint4*>(orow)[x] = make_uint4(0u, 0u, 0u, 0u);
@@ -378,6 +403,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       for (int j = 0; j < n_i; ++j) {
         if (!(ok = mbar_wait(&s_full[i], s_cnt & 1, abort_flag, &g_prefill_err, 9 + i))) break;
         ++s_cnt;
+        __syncwarp();  // tcgen05.ld below is warp-collective
         tc_fence_after();
         uint32_t sr[4][32];
 #pragma unroll
@@ -482,6 +508,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       // Epilogue: O / l, rounded once, 16-byte stores.
       if (!(ok = mbar_wait(&o_full[i], o_cnt & 1, abort_flag, &g_prefill_err, 11 + i))) break;
       ++o_cnt;
+      __syncwarp();
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
@@ -495,6 +522,11 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
           pk[x] = Pack2<T>::pack(__uint_as_float(orr[2 * x]) * inv,
                                  __uint_as_float(orr[2 * x + 1]) * inv);
         if (grow < p.Sq) {
+          // Self-check: the row must lie inside O (records and skips otherwise).
+          if (b >= p.B || hq >= p.Hq) {
+            atomicOr(&g_prefill_err, kErrBounds);
+            continue;
+          }
           uint4* dst = reinterpret_cast<uint4*>(orow + q4 * 32);
 #pragma unroll
           for (int x = 0; x < 4; ++x)
@@ -508,6 +540,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
   tc_fence_before();
   __syncthreads();
   if (warp == 9) {
+    __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }

@@ -13,6 +13,7 @@ namespace fa {
 // Device error word: bit 0 = a pipeline wait timed out; bits 8.. = which wait.
 // ---------------------------------------------------------------------------
 constexpr unsigned int kErrTimeout = 1u;
+constexpr unsigned int kErrBounds = 2u;  // a global store index failed its self-check
 constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;  // 2 s per wait
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

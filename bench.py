@@ -161,14 +161,22 @@ def run_ours(args, rank, world, local_rank):
                                PREFILL.Hq, PREFILL.Hkv, PREFILL.Sq, PREFILL.Sk, PREFILL.D,
                                PREFILL.scale, 1, fa.FA_BF16, sh)
         if st:
-            raise fa.FAError(st, "fa_prefill_fwd")
+            fail(st, "fa_prefill_fwd")
 
     def decode(qq, kk, vv, vl, out):
         st = fa.fa_decode_fwd(qq.data_ptr(), kk.data_ptr(), vv.data_ptr(), vl.data_ptr(),
                               out.data_ptr(), DECODE.B, DECODE.Hq, DECODE.Hkv, DECODE.cap,
                               DECODE.D, DECODE.scale, sh)
         if st:
-            raise fa.FAError(st, "fa_decode_fwd")
+            fail(st, "fa_decode_fwd")
+
+    def fail(st, what):
+        err = fa.FAError(st, what)  # captures the CUDA code before anything else runs
+        try:
+            torch.cuda.synchronize()  # never leave with work in flight
+        except Exception as e:  # noqa: BLE001
+            raise err from e
+        raise err
 
     n_ev = 6
     steps_total = args.warmup + args.steps

@@ -126,6 +126,13 @@ const char* fa_status_string(int status);
  */
 int fa_device_error(int reset, unsigned int* detail);
 
+/*
+ * fa_last_cuda_error -- the raw cudaError_t behind the most recent
+ * FA_ERR_CUDA returned to the calling thread (0 if none), and, if site is not
+ * NULL, a static string naming the call that failed.
+ */
+int fa_last_cuda_error(const char** site);
+
 /* Number of SMs the persistent prefill grid uses on the current device
  * (queried once per device), or a negative value on failure. */
 int fa_num_sms(void);
