@@ -6,8 +6,8 @@ no fallback: if the library is missing or cannot be loaded, every call raises.
 
 Raw entry points (same names and argument order as the C ABI; pointers are
 integers, ``stream`` a ``cudaStream_t`` value):
-    fa_prefill_fwd, fa_decode_fwd, fa_status_string, fa_device_error,
-    fa_num_sms, fa_prefill_work_item
+    fa_prefill_fwd, fa_decode_fwd, fa_decode_fwd_noalloc, fa_status_string,
+    fa_device_error, fa_last_cuda_error, fa_num_sms, fa_prefill_work_item
 Tensor conveniences (contiguous CUDA tensors, caller-owned outputs):
     prefill(q, k, v, scale, causal, out=None, stream=None)
     decode(q, kcache, vcache, valid_len, scale, out=None, stream=None)
@@ -20,10 +20,11 @@ LIB_PATH = os.path.join(HERE, "libfa_gb300.so")
 
 FA_BF16, FA_FP16 = 0, 1
 FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = 0, 1, 2, 3, 4
+FA_ERR_TOO_LARGE = 5
 
 # Every symbol include/fa.h declares (checked by the tests against the header).
-EXPORTS = ("fa_prefill_fwd", "fa_decode_fwd", "fa_status_string", "fa_device_error",
-           "fa_last_cuda_error", "fa_num_sms", "fa_prefill_work_item")
+EXPORTS = ("fa_prefill_fwd", "fa_decode_fwd", "fa_decode_fwd_noalloc", "fa_status_string",
+           "fa_device_error", "fa_last_cuda_error", "fa_num_sms", "fa_prefill_work_item")
 
 _lib = None
 
@@ -53,6 +54,8 @@ def load(path: str = LIB_PATH):
     lib.fa_prefill_fwd.restype = i32
     lib.fa_decode_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp]
     lib.fa_decode_fwd.restype = i32
+    lib.fa_decode_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp]
+    lib.fa_decode_fwd_noalloc.restype = i32
     lib.fa_status_string.argtypes = [i32]
     lib.fa_status_string.restype = ctypes.c_char_p
     lib.fa_device_error.argtypes = [i32, ctypes.POINTER(ctypes.c_uint)]
@@ -78,6 +81,19 @@ def fa_prefill_fwd(q, k, v, o, B, Hq, Hkv, Sq, Sk, D, scale, causal, dtype, stre
 def fa_decode_fwd(q, kcache, vcache, valid_len_dev, o, B, Hq, Hkv, cap, D, scale, stream):
     return load().fa_decode_fwd(q, kcache, vcache, valid_len_dev, o, B, Hq, Hkv, cap, D, scale,
                                 stream)
+
+
+def fa_decode_fwd_noalloc(q, kcache, vcache, valid_len_dev, o, B, Hq, Hkv, cap, D, scale,
+                          stream):
+    """fa_decode_fwd without any device allocation: for callers that must not
+    allocate while they run (memory reserved once at start-up, allocator locks
+    held, runtimes that forbid allocation after initialisation).  Its partials
+    live in a fixed 4 MiB array inside the library, shared by every call on the
+    device; calls overlapping on the GPU race on it.  Make the first call on a
+    device before any stream capture (it looks up the array's address).
+    Returns FA_ERR_TOO_LARGE for requests whose partials do not fit."""
+    return load().fa_decode_fwd_noalloc(q, kcache, vcache, valid_len_dev, o, B, Hq, Hkv, cap, D,
+                                        scale, stream)
 
 
 def fa_status_string(status) -> str:

@@ -59,7 +59,8 @@ typedef enum {
   FA_ERR_INVALID_ARG = 1,  /* bad pointer, size, head config or dtype         */
   FA_ERR_UNSUPPORTED = 2,  /* valid request this build does not implement     */
   FA_ERR_CUDA = 3,         /* a CUDA runtime/driver call or launch failed     */
-  FA_ERR_TIMEOUT = 4       /* a device-side pipeline wait hit its time limit  */
+  FA_ERR_TIMEOUT = 4,      /* a device-side pipeline wait hit its time limit  */
+  FA_ERR_TOO_LARGE = 5     /* request exceeds fa_decode_fwd_noalloc's scratch */
 } fa_status_t;
 
 /*
@@ -113,6 +114,36 @@ int fa_decode_fwd(const void* q, const void* kcache, const void* vcache,
                   const int32_t* valid_len_dev, void* o,
                   int B, int Hq, int Hkv, int cap, int D, float scale,
                   cudaStream_t stream);
+
+/*
+ * fa_decode_fwd_noalloc -- fa_decode_fwd for callers that cannot allocate
+ * device memory during the call.
+ *
+ * No counterpart in the source material: the pages describe no
+ * allocation-free variant; this is a deployment convenience of this library.
+ *
+ * Same arguments, layouts, results and errors as fa_decode_fwd, but the split
+ * partials live in one fixed device array inside the library (4 MiB of fp32,
+ * held by every GPU that loads the library until the process exits) instead of
+ * memory from cudaMallocAsync.  It calls no allocating routine.  Meant for
+ * code that must not allocate while it runs: serving loops with memory reserved
+ * once at start-up, code running under an allocator lock, runtimes that forbid
+ * allocation after initialisation.
+ *
+ * - Requests whose partials need more than the array holds
+ *   (B * Hq * nsplit * (D + 2) floats, nsplit <= SM count) return
+ *   FA_ERR_TOO_LARGE and enqueue nothing.
+ * - The array is shared by all calls on a device: calls whose kernels overlap
+ *   on the GPU (different streams with no ordering) race on it; calls ordered
+ *   on one stream are safe.  No contents need to start at zero.
+ * - The first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current).  Make that first call
+ *   before any stream capture on the device.
+ */
+int fa_decode_fwd_noalloc(const void* q, const void* kcache, const void* vcache,
+                          const int32_t* valid_len_dev, void* o,
+                          int B, int Hq, int Hkv, int cap, int D, float scale,
+                          cudaStream_t stream);
 
 /* Static, human-readable name of a status code (never NULL). */
 const char* fa_status_string(int status);
