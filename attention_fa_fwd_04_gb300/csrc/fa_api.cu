@@ -106,7 +106,8 @@ extern "C" int fa_decode_fwd(const void* q, const void* kcache, const void* vcac
   if (!isfinite(scale)) return FA_ERR_INVALID_ARG;
   if (B == 0 || Hq == 0) return FA_OK;
   if (Hkv == 0 || Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
-  if (B > 65535 || (int64_t)Hkv * ((Hq / Hkv + 15) / 16) > 65535) return FA_ERR_INVALID_ARG;
+  if (B > 65535 || Hq > 65535 || (int64_t)Hkv * ((Hq / Hkv + 15) / 16) > 65535)
+    return FA_ERR_INVALID_ARG;
   if (!q || !o || !aligned16(q) || !aligned16(o)) return FA_ERR_INVALID_ARG;
   if (cap > 0 && (!kcache || !vcache || !valid_len_dev || !aligned16(kcache) ||
                   !aligned16(vcache) || (reinterpret_cast<uintptr_t>(valid_len_dev) & 3u)))

@@ -54,7 +54,7 @@ struct Cfg {
   static constexpr int STAGE_BYTES = 2 * KV_BYTES;      // K tile + V tile
   static constexpr int SMEM_STAGES = NSTAGE * STAGE_BYTES;
   static_assert(NSTAGE % NWARPS == 0, "each stage must belong to one consumer warp");
-  static constexpr int SMEM_RED = HB * D * 4 + NWARPS * HB * 2 * 4;
+  static constexpr int SMEM_RED = NWARPS * HB * D * 4 + NWARPS * HB * 2 * 4;
   static constexpr int SMEM_BAR = 2 * NSTAGE * 8 + 16;
   static_assert(HALF_BYTES % 1024 == 0, "128-byte-swizzled tiles need 1 KiB alignment");
   static constexpr int SMEM_TOTAL = 1024 + SMEM_STAGES + SMEM_RED + SMEM_BAR;
@@ -86,8 +86,8 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* stages = smem;
-  float* red_o = reinterpret_cast<float*>(smem + C::SMEM_STAGES);  // [HB][D]
-  float* red_ml = red_o + HB * D;                                  // [NW][HB][2]
+  float* red_o = reinterpret_cast<float*>(smem + C::SMEM_STAGES);  // [NW][HB][D]
+  float* red_ml = red_o + NW * HB * D;                             // [NW][HB][2]
   uint64_t* full = reinterpret_cast<uint64_t*>(red_ml + NW * HB * 2);
   uint64_t* empty = full + NSTAGE;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + NSTAGE);
@@ -108,7 +108,6 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
   int n_tiles = tiles_total - t_begin;
   n_tiles = n_tiles < 0 ? 0 : (n_tiles > tps ? tps : n_tiles);
 
-  for (int x = threadIdx.x; x < HB * D; x += dec::THREADS) red_o[x] = 0.f;
   if (threadIdx.x == 0) {
     for (int s = 0; s < NSTAGE; ++s) {
       mbar_init(&full[s], 1);
@@ -303,37 +302,23 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
       red_ml[(warp * HB + g + 8) * 2 + 0] = m1;
       red_ml[(warp * HB + g + 8) * 2 + 1] = l1;
     }
-  }
-  __syncthreads();
-
-  // Cross-warp merge into red_o (unnormalised, relative to the CTA row max).
-  if (warp < NW) {
-    float M0 = NEG_INF, M1 = NEG_INF;
+    // This warp's unnormalised O rows (only the CTA's real heads are kept).
+    float* my_o = red_o + warp * HB * D;
+    const int nh_rows = (p.G - hb * HB) < HB ? (p.G - hb * HB) : HB;
 #pragma unroll
-    for (int w = 0; w < NW; ++w) {
-      M0 = fmaxf(M0, red_ml[(w * HB + g) * 2]);
-      M1 = fmaxf(M1, red_ml[(w * HB + g + 8) * 2]);
-    }
-    const float w0 = (m0 == NEG_INF) ? 0.f : fast_exp2(m0 - M0);
-    const float w1 = (m1 == NEG_INF) ? 0.f : fast_exp2(m1 - M1);
-    if (w0 > 0.f) {
-#pragma unroll
-      for (int nd = 0; nd < D / 8; ++nd) {
-        atomicAdd(&red_o[g * D + nd * 8 + 2 * tq], acc[nd][0] * w0);
-        atomicAdd(&red_o[g * D + nd * 8 + 2 * tq + 1], acc[nd][1] * w0);
-      }
-    }
-    if (w1 > 0.f) {
-#pragma unroll
-      for (int nd = 0; nd < D / 8; ++nd) {
-        atomicAdd(&red_o[(g + 8) * D + nd * 8 + 2 * tq], acc[nd][2] * w1);
-        atomicAdd(&red_o[(g + 8) * D + nd * 8 + 2 * tq + 1], acc[nd][3] * w1);
-      }
+    for (int nd = 0; nd < D / 8; ++nd) {
+      if (g < nh_rows)
+        *reinterpret_cast<float2*>(&my_o[g * D + nd * 8 + 2 * tq]) =
+            make_float2(acc[nd][0], acc[nd][1]);
+      if (g + 8 < nh_rows)
+        *reinterpret_cast<float2*>(&my_o[(g + 8) * D + nd * 8 + 2 * tq]) =
+            make_float2(acc[nd][2], acc[nd][3]);
     }
   }
   __syncthreads();
 
-  // Write this split's partial for the CTA's valid heads.
+  // Merge the warps' partials (weights exp2(m_w - M)) and write this split's
+  // partial for the CTA's heads.
   const size_t head0 = (size_t)b * p.Hq + (size_t)hkv * p.G + (size_t)hb * HB;
   int nh = (p.G - hb * HB) < HB ? (p.G - hb * HB) : HB;
   // Self-check: partial rows must lie inside the scratch (records and skips).
@@ -343,7 +328,18 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
   }
   for (int x = threadIdx.x; x < nh * D; x += dec::THREADS) {
     const int row = x / D, d = x % D;
-    p.part_o[((head0 + row) * p.nsplit + split) * D + d] = red_o[x];
+    float M = NEG_INF;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, red_ml[(w * HB + row) * 2]);
+    float o = 0.f;
+    if (M != NEG_INF) {
+#pragma unroll
+      for (int w = 0; w < NW; ++w) {
+        const float mw = red_ml[(w * HB + row) * 2];
+        if (mw != NEG_INF) o += red_o[(w * HB + row) * D + d] * fast_exp2(mw - M);
+      }
+    }
+    p.part_o[((head0 + row) * p.nsplit + split) * D + d] = o;
   }
   if (threadIdx.x < nh) {
     const int row = threadIdx.x;
@@ -359,31 +355,63 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
   }
 }
 
-// One CTA per (head, batch): O = sum_s w_s o_s / sum_s w_s l_s, w_s = exp2(m_s - M).
-// Splits that saw no token (l_s == 0) get weight 0 without touching o_s.
+// Combine: one CTA per (32 output columns, head, batch), 8 warps.  Warp w
+// folds splits w, w+8, ... with an online log-sum-exp merge (lane = column),
+// then warp 0 merges the 8 warp results.  Splits that saw no token (l_s == 0)
+// are skipped without touching o_s.  All loads of a warp are independent, so
+// the kernel costs about one L2 round trip; it is launched with programmatic
+// dependent launch and waits for the split grid in griddepcontrol.wait.
+constexpr int kCombineWarps = 8;
+
 template <int D>
-__global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(const DecodeParams p) {
   pdl_wait_primary();
-  const int h = blockIdx.x, b = blockIdx.y;
+  __shared__ float sM[kCombineWarps], sL[kCombineWarps], sA[kCombineWarps][32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int d = blockIdx.x * 32 + lane;
+  const int h = blockIdx.y, b = blockIdx.z;
   if (h >= p.Hq || b >= p.B) {
     if (threadIdx.x == 0) atomicOr(&g_decode_err, kErrBounds << 4);
     return;
   }
   const size_t base = ((size_t)b * p.Hq + h) * p.nsplit;
-  float M = -INFINITY;
-  for (int s = 0; s < p.nsplit; ++s) M = fmaxf(M, p.part_ml[(base + s) * 2]);
-  for (int d = threadIdx.x; d < D; d += blockDim.x) {
+  float M = -INFINITY, Ls = 0.f, acc = 0.f;
+#pragma unroll 4
+  for (int s = warp; s < p.nsplit; s += kCombineWarps) {
+    const float ls = p.part_ml[(base + s) * 2 + 1];
+    const float ms = p.part_ml[(base + s) * 2];
+    const float os = (d < D) ? p.part_o[(base + s) * D + d] : 0.f;
+    if (ls > 0.f) {
+      const float mn = fmaxf(M, ms);
+      const float a = fast_exp2(M - mn), w = fast_exp2(ms - mn);  // M = -inf -> a = 0
+      acc = acc * a + os * w;
+      Ls = Ls * a + ls * w;
+      M = mn;
+    }
+  }
+  if (lane == 0) {
+    sM[warp] = M;
+    sL[warp] = Ls;
+  }
+  sA[warp][lane] = acc;
+  __syncthreads();
+  if (warp == 0) {
+    float Mx = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kCombineWarps; ++w) Mx = fmaxf(Mx, sM[w]);
     float num = 0.f, den = 0.f;
-    for (int s = 0; s < p.nsplit; ++s) {
-      const float ls = p.part_ml[(base + s) * 2 + 1];
-      if (ls > 0.f) {
-        const float w = fast_exp2(p.part_ml[(base + s) * 2] - M);
-        num += w * p.part_o[(base + s) * D + d];
-        den += w * ls;
+    if (Mx != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kCombineWarps; ++w) {
+        if (sM[w] != -INFINITY) {
+          const float wt = fast_exp2(sM[w] - Mx);
+          num += sA[w][lane] * wt;
+          den += sL[w] * wt;
+        }
       }
     }
     const float out = den > 0.f ? num / den : 0.f;
-    p.o[((size_t)b * p.Hq + h) * D + d] = __float2bfloat16_rn(out);
+    if (d < D) p.o[((size_t)b * p.Hq + h) * D + d] = __float2bfloat16_rn(out);
   }
 }
 
@@ -451,8 +479,8 @@ static int launch_decode_t(const void* q, const void* kc, const void* vc, const 
   if (e != cudaSuccess) return e;
 
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(Hq, B, 1);
-  cfg.blockDim = dim3(128, 1, 1);
+  cfg.gridDim = dim3((D + 31) / 32, Hq, B);
+  cfg.blockDim = dim3(kCombineWarps * 32, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
