@@ -14,11 +14,12 @@
 // share a K/V head run together, so K/V stay in L2), longest causal units
 // first.
 //
-// CTA = 10 warps:
+// CTA = 12 warps (3 warpgroups):
 //   warps 0-3  softmax/epilogue for Q tile 0 (TMEM lanes 0-127)
 //   warps 4-7  softmax/epilogue for Q tile 1
 //   warp  8    TMA producer: Q tiles, then K_j / V_j tiles into an NSTAGE ring
 //   warp  9    TMEM allocator and MMA issuer (one lane)
+//   warps 10-11 idle (they complete warpgroup 2 for the register split)
 // TMEM (512 columns): S0 | S1 | O0 | O1; P_i (bf16) is written over the first
 // half of S_i and fed to the P@V MMA straight from TMEM (no register or shared
 // memory relayout -- the role the transposed-PV lever plays on gfx950).
@@ -43,7 +44,14 @@ namespace pf {
 constexpr int BM = 128;         // rows per Q tile
 constexpr int BN = 128;         // keys per K/V tile
 constexpr int QBLOCK = 2 * BM;  // query rows per work item
-constexpr int THREADS = 320;
+constexpr int THREADS = 384;  // 3 warpgroups
+// Register split (setmaxnreg): the block launches with 168 registers per
+// thread (384 x 168 = 64512).  The two softmax warpgroups take 208 each, the
+// producer/MMA warpgroup keeps 88: 256*208 + 128*88 = 64512, exactly the
+// launch pool (a larger sum would make setmaxnreg.inc wait forever).
+constexpr uint32_t REGS_LAUNCH = 168, REGS_SOFTMAX = 208, REGS_ISSUE = 88;
+static_assert(256 * REGS_SOFTMAX + 128 * REGS_ISSUE <= THREADS * REGS_LAUNCH,
+              "register split exceeds the launch allocation");
 constexpr int HALF_BYTES = 128 * 128;  // 128 rows x 64 elements x 2 bytes
 constexpr float TAU = 8.0f;            // lazy-rescale threshold (log2 domain)
 
@@ -188,7 +196,10 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
   // warp-aligned CTA barrier below, or tcgen05.dealloc, with lanes still
   // inside a role loop.)
   const bool leader = lane == 0;
-  if (warp == 8) {
+  if (warp >= 8) {
+   // ------------------ warpgroup 2: TMA producer and MMA issuer ------------------
+   regs_decrease<pf::REGS_ISSUE>();
+   if (warp == 8) {
     // ============================ TMA producer ============================
     if (leader) {
       tma_prefetch_desc(&tmQ);
@@ -369,8 +380,10 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
     commit(drain);
     mbar_wait_drain(drain, 0);
     __syncwarp();
+   }
   } else {
     // ======================= softmax + epilogue (2 groups) =======================
+    regs_increase<pf::REGS_SOFTMAX>();
     const int i = warp >> 2;          // Q tile handled by this warpgroup
     const int wq = warp & 3;          // TMEM lane quarter
     const int r = wq * 32 + lane;     // row within the Q tile
@@ -405,101 +418,127 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
         ++s_cnt;
         __syncwarp();  // tcgen05.ld below is warp-collective
         tc_fence_after();
-        uint32_t sr[4][32];
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) tmem_ld32(tS + q4 * 32, sr[q4]);
-        tmem_wait_ld();
-        float* s = reinterpret_cast<float*>(&sr[0][0]);
-
         const int kv0 = j * pf::BN;
         const bool need_mask =
             (kv0 + pf::BN > p.Sk) || (p.causal && kv0 + pf::BN - 1 > row0 + off);
-        // Row max in the log2 domain.  Masked tiles are scaled first and get
-        // -inf at hidden keys (cc = 1 afterwards); mask-free tiles take the max
-        // (or, for a negative scale, the min) of the raw scores times c.
-        float mx, cc = c;
+        int lim = pf::BN;  // keys [0, lim) of this tile are visible to this row
         if (need_mask) {
-          const int lim_c = p.causal ? grow + off + 1 : p.Sk;  // keys [0, lim) visible
-          const int lim = (lim_c < p.Sk ? lim_c : p.Sk) - kv0;
-#pragma unroll
-          for (int x = 0; x < pf::BN; ++x) s[x] = (x < lim) ? s[x] * c : NEG_INF;
-          cc = 1.f;
-          float a0 = s[0], a1 = s[1], a2 = s[2], a3 = s[3];
-#pragma unroll
-          for (int x = 4; x < pf::BN; x += 4) {
-            a0 = fmaxf(a0, s[x]);
-            a1 = fmaxf(a1, s[x + 1]);
-            a2 = fmaxf(a2, s[x + 2]);
-            a3 = fmaxf(a3, s[x + 3]);
-          }
-          mx = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
-        } else if (!neg_scale) {
-          float a0 = s[0], a1 = s[1], a2 = s[2], a3 = s[3];
-#pragma unroll
-          for (int x = 4; x < pf::BN; x += 4) {
-            a0 = fmaxf(a0, s[x]);
-            a1 = fmaxf(a1, s[x + 1]);
-            a2 = fmaxf(a2, s[x + 2]);
-            a3 = fmaxf(a3, s[x + 3]);
-          }
-          mx = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * c;
-        } else {
-          float a0 = s[0], a1 = s[1], a2 = s[2], a3 = s[3];
-#pragma unroll
-          for (int x = 4; x < pf::BN; x += 4) {
-            a0 = fminf(a0, s[x]);
-            a1 = fminf(a1, s[x + 1]);
-            a2 = fminf(a2, s[x + 2]);
-            a3 = fminf(a3, s[x + 3]);
-          }
-          mx = fminf(fminf(a0, a1), fminf(a2, a3)) * c;
+          const int lim_c = p.causal ? grow + off + 1 : p.Sk;
+          lim = (lim_c < p.Sk ? lim_c : p.Sk) - kv0;
         }
-        const float m_new = fmaxf(m_used, mx);
-        // Lazy rescale: only when the max grew by more than TAU (log2 domain).
-        // On the first tile O holds nothing yet (the first P@V overwrites it).
-        float f = 1.f;
-        bool resc = false;
+        // Raw-domain fill for hidden keys: becomes -inf once multiplied by c.
+        const float hide = neg_scale ? -NEG_INF : NEG_INF;
+        uint32_t sr[4][32];
+        float mx = hide;  // running max (min if c < 0) of this tile's raw scores
+        float2 la = make_float2(0.f, 0.f), lb = make_float2(0.f, 0.f);  // tile row sum
+
+        // Chunk q (32 keys): hide masked keys, fold into the running max.
+        auto mask_and_max = [&](uint32_t (&r)[32], int q) {
+          float* v = reinterpret_cast<float*>(r);
+          if (need_mask) {
+#pragma unroll
+            for (int x = 0; x < 32; ++x)
+              if (q * 32 + x >= lim) v[x] = hide;
+          }
+          float a = v[0], b = v[1];
+          if (!neg_scale) {
+#pragma unroll
+            for (int x = 2; x < 30; x += 4) {
+              a = max3f(a, v[x], v[x + 1]);
+              b = max3f(b, v[x + 2], v[x + 3]);
+            }
+            mx = max3f(mx, max3f(a, b, v[30]), v[31]);
+          } else {
+#pragma unroll
+            for (int x = 2; x < 30; x += 4) {
+              a = min3f(a, v[x], v[x + 1]);
+              b = min3f(b, v[x + 2], v[x + 3]);
+            }
+            mx = min3f(mx, min3f(a, b, v[30]), v[31]);
+          }
+        };
+        // Chunk q: P = exp2(s*c - base) packed to the input type, written over
+        // S at columns [16q, 16q+16) (keys 32q..32q+31); row sum into la/lb.
+        auto exp_store = [&](uint32_t (&r)[32], int q, float base) {
+          const float* v = reinterpret_cast<const float*>(r);
+          const float2 c2 = make_float2(c, c), nb2 = make_float2(-base, -base);
+          uint32_t pk[16];
+#pragma unroll
+          for (int t = 0; t < 16; ++t) {
+            const float2 a = __ffma2_rn(make_float2(v[2 * t], v[2 * t + 1]), c2, nb2);
+            const float2 pp = make_float2(fast_exp2(a.x), fast_exp2(a.y));
+            if (t & 1)
+              lb = __fadd2_rn(lb, pp);
+            else
+              la = __fadd2_rn(la, pp);
+            pk[t] = Pack2<T>::pack(pp.x, pp.y);
+          }
+          tmem_st16(tS + q * 16, pk);
+        };
+
         if (j == 0) {
-          m_used = m_new;
+          // First tile of the item: no running max yet -- max first, then P.
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) tmem_ld32(tS + q4 * 32, sr[q4]);
+          tmem_wait_ld();
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) reg_fence32(sr[q4]);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) mask_and_max(sr[q4], q4);
+          m_used = mx * c;
+          const float base = (m_used == NEG_INF) ? 0.f : m_used;
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) exp_store(sr[q4], q4, base);
         } else {
-          resc = (m_new - m_used) > pf::TAU;
-          if (resc) {
-            f = fast_exp2(m_used - m_new);
-            l *= f;
-            m_used = m_new;
+          // Later tiles: exponentiate against the running max while the next
+          // chunk streams in from TMEM, track the new max alongside, and redo
+          // the tile only if the max grew by more than TAU (lazy rescale).
+          const float base_old = (m_used == NEG_INF) ? 0.f : m_used;
+          tmem_ld32(tS, sr[0]);
+          tmem_wait_ld();
+          reg_fence32(sr[0]);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            if (q4 < 3) tmem_ld32(tS + (q4 + 1) * 32, sr[q4 + 1]);
+            mask_and_max(sr[q4], q4);
+            exp_store(sr[q4], q4, base_old);
+            if (q4 < 3) {
+              tmem_wait_ld();
+              reg_fence32(sr[q4 + 1]);
+            }
+          }
+          const float m_new = fmaxf(m_used, mx * c);
+          const bool resc = (m_new - m_used) > pf::TAU;
+          if (__any_sync(0xffffffffu, resc)) {
+            // Rare: some row's max moved by more than TAU.  Rescale its l and
+            // O by 2^(m_used - m_new) and rewrite this tile's P (the scores
+            // are still in registers).  P_i(j-1) @ V has completed (it was
+            // issued before S_i(j)); P_i(j) is not read before p_full below.
+            float f = 1.f;
+            if (resc) {
+              f = fast_exp2(m_used - m_new);
+              l *= f;
+              m_used = m_new;
+            }
+            const float base = (m_used == NEG_INF) ? 0.f : m_used;
+            tmem_wait_st();
+            la = make_float2(0.f, 0.f);
+            lb = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) exp_store(sr[q4], q4, base);
+#pragma unroll
+            for (int q4 = 0; q4 < D / 32; ++q4) {
+              uint32_t orr[32];
+              tmem_ld32(tO + q4 * 32, orr);
+              tmem_wait_ld();
+              reg_fence32(orr);
+#pragma unroll
+              for (int x = 0; x < 32; ++x) orr[x] = __float_as_uint(__uint_as_float(orr[x]) * f);
+              tmem_st32(tO + q4 * 32, orr);
+            }
           }
         }
-        const float base = (m_used == NEG_INF) ? 0.f : m_used;
-        // P = exp2(s*c - base), packed to the input type, written over S.
-        float l0 = 0.f, l1 = 0.f;
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          uint32_t pk[32];
-#pragma unroll
-          for (int x = 0; x < 32; ++x) {
-            const float p0 = fast_exp2(fmaf(s[hh * 64 + 2 * x], cc, -base));
-            const float p1 = fast_exp2(fmaf(s[hh * 64 + 2 * x + 1], cc, -base));
-            l0 += p0;
-            l1 += p1;
-            pk[x] = Pack2<T>::pack(p0, p1);
-          }
-          tmem_st32(tS + hh * 32, pk);
-        }
-        l += l0 + l1;
-        // O *= f for the rows whose max moved.  P_i(j) is not consumed before
-        // p_full is signalled below, and P_i(j-1) @ V has completed (it was
-        // issued before S_i(j), whose completion we waited for).
-        if (__any_sync(0xffffffffu, resc)) {
-#pragma unroll
-          for (int q4 = 0; q4 < D / 32; ++q4) {
-            uint32_t orr[32];
-            tmem_ld32(tO + q4 * 32, orr);
-            tmem_wait_ld();
-#pragma unroll
-            for (int x = 0; x < 32; ++x) orr[x] = __float_as_uint(__uint_as_float(orr[x]) * f);
-            tmem_st32(tO + q4 * 32, orr);
-          }
-        }
+        l += (la.x + la.y) + (lb.x + lb.y);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&p_full[i]);
@@ -516,6 +555,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
         uint32_t orr[32];
         tmem_ld32(tO + q4 * 32, orr);
         tmem_wait_ld();
+        reg_fence32(orr);
         uint32_t pk[16];
 #pragma unroll
         for (int x = 0; x < 16; ++x)
@@ -585,6 +625,9 @@ static int launch_prefill_t(const void* q, const void* k, const void* v, void* o
   p.n_qb = (Sq + pf::QBLOCK - 1) / pf::QBLOCK;
   p.n_items = B * Hq * p.n_qb;
   p.c = scale * 1.4426950408889634f;
+  // scale == 0: every visible score is 0.  A tiny positive c keeps that (all
+  // exp2 arguments round to 0) while hidden keys still map to -inf, never NaN.
+  if (p.c == 0.f) p.c = 1e-30f;
   const int sms = sm_count() > 0 ? sm_count() : 148;
   const int grid = p.n_items < sms ? p.n_items : sms;
   prefill_kernel<D, T><<<grid, pf::THREADS, C::SMEM_TOTAL, stream>>>(tq, tk, tv, p);
