@@ -142,6 +142,9 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
                    const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
   using C = pf::Cfg<D>;
   constexpr bool kBF16 = IsBF16<T>::value;
+  // Largest row sum of unnormalised P a step may leave (see the lazy rescale
+  // below): 2^60 for bf16 P (range to 2^127), 2^15 for fp16 P (max 65504).
+  constexpr float PBIG = kBF16 ? 1.152921504606846976e18f : 32768.f;
   constexpr int NSTAGE = C::NSTAGE;
   constexpr float NEG_INF = -INFINITY;
 
@@ -302,6 +305,10 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       __syncwarp();
     };
 
+    // K_j / V_j of an item sit at ring positions kb + 2j / kb + 2j + 1.
+    auto ring_wait = [&](uint32_t idx, unsigned int site) {
+      return mbar_wait(&full[idx % NSTAGE], (idx / NSTAGE) & 1, abort_flag, &g_prefill_err, site);
+    };
     for (int w = blockIdx.x; w < p.n_items && ok; w += gridDim.x, ++local) {
       int b, hq, qb;
       prefill_item(w, p.B, p.Hq, p.Hkv, p.n_qb, &b, &hq, &qb);
@@ -315,37 +322,32 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
         commit(q_empty);
         continue;
       }
+      const uint32_t kb = kv_cnt;
+      kv_cnt += 2 * n;
       // K_0 -> S_0(0), S_1(0)
-      int sK = kv_cnt % NSTAGE;
-      if (!(ok = mbar_wait(&full[sK], (kv_cnt / NSTAGE) & 1, abort_flag, &g_prefill_err, 4)))
-        break;
+      if (!(ok = ring_wait(kb, 4))) break;
       tc_fence_after();
-      ++kv_cnt;
       if (nt0 > 0) {
-        issue_s(0, sK);
+        issue_s(0, kb % NSTAGE);
         commit(&s_full[0]);
       }
       if (nt1 > 0) {
-        issue_s(1, sK);
+        issue_s(1, kb % NSTAGE);
         commit(&s_full[1]);
       }
-      commit(&empty[sK]);
+      commit(&empty[kb % NSTAGE]);
       if (n == 1) commit(q_empty);
+      // Operands of step 0: V_0 and K_1.
+      if (!(ok = ring_wait(kb + 1, 5))) break;
+      if (n > 1 && !(ok = ring_wait(kb + 2, 6))) break;
+      tc_fence_after();
 
+      // Per step j: PV0(j), S0(j+1), PV1(j), [operand waits of step j+1],
+      // S1(j+1).  The waits sit where PV1(j) still fills the MMA queue, so
+      // their latency leaves less of the tensor pipe idle.
       for (int j = 0; j < n && ok; ++j) {
-        const int sV = kv_cnt % NSTAGE;
-        if (!(ok = mbar_wait(&full[sV], (kv_cnt / NSTAGE) & 1, abort_flag, &g_prefill_err, 5)))
-          break;
-        tc_fence_after();
-        ++kv_cnt;
-        const bool has_next = j + 1 < n;
-        if (has_next) {
-          sK = kv_cnt % NSTAGE;
-          if (!(ok = mbar_wait(&full[sK], (kv_cnt / NSTAGE) & 1, abort_flag, &g_prefill_err, 6)))
-            break;
-          tc_fence_after();
-          ++kv_cnt;
-        }
+        const int sV = (kb + 2 * j + 1) % NSTAGE;
+        const int sK = (kb + 2 * j + 2) % NSTAGE;  // K_{j+1}
         if (j < nt0) {
           if (!(ok = mbar_wait(&p_full[0], p_cnt0 & 1, abort_flag, &g_prefill_err, 7))) break;
           ++p_cnt0;
@@ -363,13 +365,16 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
           tc_fence_after();
           issue_pv(1, sV, j > 0);
           if (j == nt1 - 1) commit(&o_full[1]);
+        }
+        commit(&empty[sV]);
+        if (j + 1 < n) {
+          if (!(ok = ring_wait(kb + 2 * j + 3, 5))) break;                  // V_{j+1}
+          if (j + 2 < n && !(ok = ring_wait(kb + 2 * j + 4, 6))) break;     // K_{j+2}
+          tc_fence_after();
           if (j + 1 < nt1) {
             issue_s(1, sK);
             commit(&s_full[1]);
           }
-        }
-        commit(&empty[sV]);
-        if (has_next) {
           commit(&empty[sK]);
           if (j + 1 == n - 1) commit(q_empty);
         }
@@ -476,13 +481,16 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
           tmem_st16(tS + q * 16, pk);
         };
 
+        // All four 32-column loads in flight at once: tcgen05.wait::ld waits
+        // for every outstanding load, so finer pipelining would serialise on
+        // the TMEM load latency.
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) tmem_ld32(tS + q4 * 32, sr[q4]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) reg_fence32(sr[q4]);
         if (j == 0) {
           // First tile of the item: no running max yet -- max first, then P.
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) tmem_ld32(tS + q4 * 32, sr[q4]);
-          tmem_wait_ld();
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) reg_fence32(sr[q4]);
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) mask_and_max(sr[q4], q4);
           m_used = mx * c;
@@ -490,33 +498,37 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) exp_store(sr[q4], q4, base);
         } else {
-          // Later tiles: exponentiate against the running max while the next
-          // chunk streams in from TMEM, track the new max alongside, and redo
-          // the tile only if the max grew by more than TAU (lazy rescale).
+          // Later tiles: exponentiate against the running max m_used without
+          // computing this tile's max.  Every P of a row is bounded by the
+          // row's tile sum, so a sum <= PBIG guarantees P fits the input type
+          // and the fp32 sums (the lazy-rescale idea of the gfx950 README with
+          // the threshold moved from the max to the sum).  Rows above it (their
+          // max grew by ~log2(PBIG)), and rows that had no visible key before
+          // (m_used = -inf: P was taken against 0), take the slow path, which
+          // finds the true max from the scores still in registers.
           const float base_old = (m_used == NEG_INF) ? 0.f : m_used;
-          tmem_ld32(tS, sr[0]);
-          tmem_wait_ld();
-          reg_fence32(sr[0]);
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
-            if (q4 < 3) tmem_ld32(tS + (q4 + 1) * 32, sr[q4 + 1]);
-            mask_and_max(sr[q4], q4);
-            exp_store(sr[q4], q4, base_old);
-            if (q4 < 3) {
-              tmem_wait_ld();
-              reg_fence32(sr[q4 + 1]);
+            if (need_mask) {
+              float* v = reinterpret_cast<float*>(sr[q4]);
+#pragma unroll
+              for (int x = 0; x < 32; ++x)
+                if (q4 * 32 + x >= lim) v[x] = hide;
             }
+            exp_store(sr[q4], q4, base_old);
           }
-          const float m_new = fmaxf(m_used, mx * c);
-          const bool resc = (m_new - m_used) > pf::TAU;
+          const float lt = (la.x + la.y) + (lb.x + lb.y);
+          const bool resc = !(lt <= PBIG) || (m_used == NEG_INF && lim > 0);
           if (__any_sync(0xffffffffu, resc)) {
-            // Rare: some row's max moved by more than TAU.  Rescale its l and
-            // O by 2^(m_used - m_new) and rewrite this tile's P (the scores
-            // are still in registers).  P_i(j-1) @ V has completed (it was
+            // Rare: rescale l and O by 2^(m_used - m_new) for those rows and
+            // rewrite this tile's P.  P_i(j-1) @ V has completed (it was
             // issued before S_i(j)); P_i(j) is not read before p_full below.
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) mask_and_max(sr[q4], q4);
             float f = 1.f;
             if (resc) {
-              f = fast_exp2(m_used - m_new);
+              const float m_new = fmaxf(m_used, mx * c);
+              f = (m_used == NEG_INF) ? 0.f : fast_exp2(m_used - m_new);
               l *= f;
               m_used = m_new;
             }
