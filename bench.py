@@ -69,6 +69,21 @@ def stored_traffic(kernel, src_hash):
     return None
 
 
+def max_over_ranks(values, dist=None, device="cpu"):
+    """Element-wise maximum of a list of per-rank timings over all ranks (the
+    job is as slow as its slowest replica); identity without a process group."""
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    if dist is not None and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_rate(work_per_rank, world, seconds):
+    """Whole-job throughput: the work of all replicas over the (max) time."""
+    return world * work_per_rank / seconds
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled during the timed region."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -232,10 +247,7 @@ def run_ours(args, rank, world, local_rank):
     t_pre = sum(e[0].elapsed_time(e[1]) for e in timed) / 1e3   # seconds
     t_dec1 = sum(e[2].elapsed_time(e[3]) for e in timed) / 1e3
     t_dec2 = sum(e[4].elapsed_time(e[5]) for e in timed) / 1e3
-    times = torch.tensor([t_pre, t_dec1, t_dec2, wall], dtype=torch.float64, device=dev)
-    if dist:
-        dist.all_reduce(times, op=dist.ReduceOp.MAX)
-    t_pre, t_dec1, t_dec2, wall = times.tolist()
+    t_pre, t_dec1, t_dec2, wall = max_over_ranks([t_pre, t_dec1, t_dec2, wall], dist, dev)
     K = args.steps
 
     # ---------------- end to end through the C ABI with host buffers ----------------
@@ -248,7 +260,7 @@ def run_ours(args, rank, world, local_rank):
 
     pk, pk_src = peaks()
     flops = PREFILL.flops
-    tflops = world * flops * K / t_pre / 1e12
+    tflops = job_rate(flops * K, world, t_pre) / 1e12
     pre_ms = t_pre / K * 1e3
     achieved = flops / (t_pre / K) / 1e12
     pre_hash = source_hash("attention_fa_fwd_04_gb300/csrc/fa_prefill.cu",
@@ -360,10 +372,7 @@ def run_e2e(args, fa, torch, dev, q_h, k_h, v_h, sh, stream, dist):
     e1.record(stream)
     torch.cuda.synchronize()
     t = e0.elapsed_time(e1) / 1e3
-    tt = torch.tensor([t], dtype=torch.float64, device=dev)
-    if dist:
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-    t = tt.item()
+    t = max_over_ranks([t], dist, dev)[0]
     world = dist.get_world_size() if dist else 1
     h2d = (q_h.numel() + k_h.numel() + v_h.numel()) * 2
     return {"value": round(world * PREFILL.flops * n / t / 1e12, 2), "unit": "TFLOP/s",
