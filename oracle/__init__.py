@@ -29,7 +29,10 @@ _lib = None
 def _load():
     global _lib
     if _lib is None:
-        path = _build.build()
+        # A planted-mistake copy of the oracle, compiled by the mutation test
+        # (tests/test_oracle_mutants.py), is loaded through this variable so that
+        # the pins can be shown to catch it.
+        path = os.environ.get("FA_ORACLE_LIB_OVERRIDE") or _build.build()
         lib = ctypes.CDLL(path)
         dp = ctypes.POINTER(ctypes.c_double)
         lp = ctypes.POINTER(ctypes.c_int64)

@@ -254,6 +254,9 @@ def test_decode_clamps_valid_length():
     assert np.array_equal(oracle.decode(q, kc, vc, 0, 0.3), np.zeros((1, 4, 16)))
     assert np.array_equal(oracle.decode(q, kc, vc, -5, 0.3), np.zeros((1, 4, 16)))
     assert np.array_equal(oracle.decode(q, kc, vc, 25, 0.3), oracle.decode(q, kc, vc, 20, 0.3))
+    # L = cap: every cached token is visible, i.e. non-causal prefill over the cache
+    full = oracle.attention(q, kc, vc, 0.3, False)[:, 0]
+    np.testing.assert_allclose(oracle.decode(q, kc, vc, 20, 0.3), full, rtol=0, atol=0)
 
 
 # ---------------------------------------------------------------------------
@@ -332,6 +335,24 @@ def test_softmax_shift_invariance_against_closed_form_two_keys():
     ref = w0 * np.array([3.0, -2.0]) + (1 - w0) * np.array([-1.0, 4.0])
     o = oracle.attention(q, k, v, scale, False)
     np.testing.assert_allclose(o[0, 0, 0], ref, atol=1e-15)
+
+
+@pytest.mark.parametrize("scale", [500.0, -500.0])
+def test_scores_far_outside_exp_range_closed_form(scale):
+    """Softmax is shift invariant, so scores of +-1000 (exp overflows or
+    underflows in fp64) still have the closed form of the two-key case:
+    w0 = 1 / (1 + exp(s1 - s0)).  Here |s1 - s0| = 2000, so all the weight
+    goes to the larger score and O is that key's V row exactly."""
+    q = torch.tensor([[[[1.0, 2.0]]]], dtype=torch.float64)
+    k = torch.tensor([[[[0.5, -1.0]], [[2.0, 0.25]]]], dtype=torch.float64)
+    v = torch.tensor([[[[3.0, -2.0]], [[-1.0, 4.0]]]], dtype=torch.float64)
+    o = oracle.attention(q, k, v, scale, False)
+    want = [-1.0, 4.0] if scale > 0 else [3.0, -2.0]   # s0 = -1.5*scale, s1 = 2.5*scale
+    np.testing.assert_array_equal(o[0, 0, 0], want)
+    # same shift on both keys (s0 = s1 = -1000 or +1000): the plain mean
+    k_eq = torch.tensor([[[[2.0, 0.0]], [[0.0, 1.0]]]], dtype=torch.float64)
+    o_eq = oracle.attention(q, k_eq, v, scale, False)
+    np.testing.assert_array_equal(o_eq[0, 0, 0], [1.0, 1.0])
 
 
 # ---------------------------------------------------------------------------
