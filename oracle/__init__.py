@@ -40,11 +40,16 @@ def _load():
         lib.oracle_attention_rows.argtypes = [dp, dp, dp, dp, lp, i64, i32, i32,
                                               i32, i64, i64, i32, f64, i32, i32]
         lib.oracle_attention_rows.restype = i32
+        lib.oracle_attention_rows_lse.argtypes = [dp, dp, dp, dp, dp, lp, i64, i32, i32,
+                                                  i32, i64, i64, i32, f64, i32, i32]
+        lib.oracle_attention_rows_lse.restype = i32
         lib.oracle_attention_probs.argtypes = [dp, dp, dp, dp, dp, i32, i32, i64,
                                                i32, i32, i32, i64, i64, i32, f64, i32]
         lib.oracle_attention_probs.restype = i32
         lib.oracle_decode.argtypes = [dp, dp, dp, dp, i32, i32, i32, i64, i32, i64, f64]
         lib.oracle_decode.restype = i32
+        lib.oracle_decode_lse.argtypes = [dp, dp, dp, dp, dp, i32, i32, i32, i64, i32, i64, f64]
+        lib.oracle_decode_lse.restype = i32
         _lib = lib
     return _lib
 
@@ -66,11 +71,14 @@ def default_threads() -> int:
     return max(1, len(os.sched_getaffinity(0)))
 
 
-def attention(q, k, v, scale: float, causal: bool, rows=None, nthreads=None):
+def attention(q, k, v, scale: float, causal: bool, rows=None, nthreads=None,
+              return_lse=False):
     """O for q [B,Sq,Hq,D], k/v [B,Sk,Hkv,D].
 
     rows=None: full output, float64 [B,Sq,Hq,D].
     rows=int array [n,3] of (b, h, i): float64 [n, D], row r = O[b,i,h,:].
+    return_lse: also return the log-sum-exp of each row's scores (-inf for a
+    row with no visible key): [B,Hq,Sq] for rows=None, else [n].
     """
     lib = _load()
     B, Sq, Hq, D = q.shape
@@ -88,16 +96,18 @@ def attention(q, k, v, scale: float, causal: bool, rows=None, nthreads=None):
     q_rows = np.ascontiguousarray(q_rows)
     n = rows_arr.shape[0]
     out = np.zeros((n, D), dtype=np.float64)
+    lse = np.full(n, -np.inf, dtype=np.float64)
     if n:
-        rc = lib.oracle_attention_rows(
-            _ptr(q_rows), _ptr(kd), _ptr(vd), _ptr(out), _ptr(rows_arr, ctypes.c_int64),
-            n, B, Hq, Hkv, Sq, Sk, D, float(scale), int(bool(causal)),
-            int(nthreads or default_threads()))
+        rc = lib.oracle_attention_rows_lse(
+            _ptr(q_rows), _ptr(kd), _ptr(vd), _ptr(out), _ptr(lse),
+            _ptr(rows_arr, ctypes.c_int64), n, B, Hq, Hkv, Sq, Sk, D, float(scale),
+            int(bool(causal)), int(nthreads or default_threads()))
         if rc != 0:
             raise RuntimeError(f"oracle_attention_rows failed with status {rc}")
     if rows is None:
-        return out.reshape(B, Sq, Hq, D)
-    return out
+        out = out.reshape(B, Sq, Hq, D)
+        lse = np.ascontiguousarray(lse.reshape(B, Sq, Hq).transpose(0, 2, 1))
+    return (out, lse) if return_lse else out
 
 
 def probs(q, k, v, scale: float, causal: bool, b: int, h: int, i: int):
@@ -117,9 +127,10 @@ def probs(q, k, v, scale: float, causal: bool, b: int, h: int, i: int):
     return p[:Sk], o
 
 
-def decode(q, kcache, vcache, L: int, scale: float):
+def decode(q, kcache, vcache, L: int, scale: float, return_lse=False):
     """Single-token decode. q [B,1,Hq,D] or [B,Hq,D]; caches [B,cap,Hkv,D];
-    L = valid length (host int), clamped to [0, cap].  Returns float64 [B,Hq,D]."""
+    L = valid length (host int), clamped to [0, cap].  Returns float64 [B,Hq,D]
+    (and the log-sum-exp [B,Hq] when return_lse)."""
     lib = _load()
     qd = _f64(q)
     B, cap, Hkv, D = kcache.shape
@@ -127,8 +138,9 @@ def decode(q, kcache, vcache, L: int, scale: float):
     Hq = qd.shape[1]
     kd, vd = _f64(kcache), _f64(vcache)
     out = np.zeros((B, Hq, D), dtype=np.float64)
-    rc = lib.oracle_decode(_ptr(qd), _ptr(kd), _ptr(vd), _ptr(out), B, Hq, Hkv, cap, D,
-                           int(L), float(scale))
+    lse = np.full((B, Hq), -np.inf, dtype=np.float64)
+    rc = lib.oracle_decode_lse(_ptr(qd), _ptr(kd), _ptr(vd), _ptr(out), _ptr(lse), B, Hq, Hkv,
+                               cap, D, int(L), float(scale))
     if rc != 0:
         raise RuntimeError(f"oracle_decode failed with status {rc}")
-    return out
+    return (out, lse) if return_lse else out

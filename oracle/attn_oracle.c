@@ -37,6 +37,15 @@
  * score vector, max-subtracted exponentials, one normalising division.
  * Cache entries at j >= L are never read, so NaN contents there cannot reach
  * the result.
+ *
+ * Optional second output, the natural log of the softmax denominator of each
+ * row (its log-sum-exp over the visible keys),
+ *   lse[b,h,i] = log sum_j exp(s_j) = max_j s_j + log sum_j exp(s_j - max),
+ * and -inf for a row that sees no key.  It is the per-row statistic a
+ * backward pass recomputes P from (tessera #90, flash-attention backward
+ * commit note: the "_pre" kernel's logsumexp L) and the one a split or
+ * sequence-parallel combine merges by; rocm-libraries #13108 lists the LSE
+ * output among the pieces its first decode milestone leaves out.
  */
 #include <math.h>
 #include <pthread.h>
@@ -50,15 +59,17 @@
  *   vbase  : V[b, 0, kv, 0]; value j is at vbase + j*kstride
  *   o      : D doubles out
  *   p_out  : optional, n_vis probabilities out (normalised)
+ *   lse    : optional, the row's log-sum-exp out
  *   s      : scratch, n_vis doubles
  */
 static void attend_row(const double* q, const double* kbase, const double* vbase,
                        int64_t kstride, int64_t n_vis, int D, double scale,
-                       double* o, double* p_out, double* s) {
+                       double* o, double* p_out, double* lse, double* s) {
   int d;
   int64_t j;
   for (d = 0; d < D; ++d) o[d] = 0.0;
-  if (n_vis <= 0) return; /* no visible key: output 0 */
+  if (lse) *lse = -INFINITY;
+  if (n_vis <= 0) return; /* no visible key: output 0, log-sum-exp -inf */
 
   /* scores s_j = scale * <q, k_j> */
   double m = -INFINITY;
@@ -82,6 +93,7 @@ static void attend_row(const double* q, const double* kbase, const double* vbase
     for (d = 0; d < D; ++d) o[d] += pj * vj[d];
   }
   for (d = 0; d < D; ++d) o[d] /= l;
+  if (lse) *lse = m + log(l);
   if (p_out)
     for (j = 0; j < n_vis; ++j) p_out[j] = s[j] / l;
 }
@@ -99,6 +111,7 @@ typedef struct {
   const double* k;      /* [B, Sk, Hkv, D] */
   const double* v;      /* [B, Sk, Hkv, D] */
   double* o_rows;       /* [nrows, D] */
+  double* lse_rows;     /* [nrows] or NULL */
   const int64_t* rows;  /* [nrows, 3] = (b, h, i) */
   int64_t nrows;
   int B, Hq, Hkv, D, causal;
@@ -124,19 +137,20 @@ static void* rows_worker(void* arg) {
     const double* vb = J->v + (b * J->Sk * J->Hkv + kv) * J->D;
     attend_row(J->q_rows + r * J->D, kb, vb, kstride,
                visible_keys(i, J->Sq, J->Sk, J->causal), J->D, J->scale,
-               J->o_rows + r * J->D, NULL, s);
+               J->o_rows + r * J->D, NULL, J->lse_rows ? J->lse_rows + r : NULL, s);
   }
   free(s);
   J->status = 0;
   return NULL;
 }
 
-/* Attention for an explicit list of query rows.
- * Returns 0 on success, nonzero on bad arguments or allocation failure. */
-int oracle_attention_rows(const double* q_rows, const double* k, const double* v,
-                          double* o_rows, const int64_t* rows, int64_t nrows,
-                          int B, int Hq, int Hkv, int64_t Sq, int64_t Sk, int D,
-                          double scale, int causal, int nthreads) {
+/* Attention for an explicit list of query rows; lse_rows (nrows doubles) may
+ * be NULL.  Returns 0 on success, nonzero on bad arguments or allocation
+ * failure. */
+int oracle_attention_rows_lse(const double* q_rows, const double* k, const double* v,
+                              double* o_rows, double* lse_rows, const int64_t* rows,
+                              int64_t nrows, int B, int Hq, int Hkv, int64_t Sq, int64_t Sk,
+                              int D, double scale, int causal, int nthreads) {
   if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || D <= 0 || Sq < 0 || Sk < 0)
     return 2;
   int64_t r;
@@ -154,6 +168,7 @@ int oracle_attention_rows(const double* q_rows, const double* k, const double* v
   for (t = 0; t < nthreads; ++t) {
     rows_job_t* J = &jobs[t];
     J->q_rows = q_rows; J->k = k; J->v = v; J->o_rows = o_rows; J->rows = rows;
+    J->lse_rows = lse_rows;
     J->nrows = nrows; J->B = B; J->Hq = Hq; J->Hkv = Hkv; J->D = D;
     J->causal = causal; J->Sq = Sq; J->Sk = Sk; J->scale = scale;
     J->r0 = nrows * t / nthreads;
@@ -170,6 +185,14 @@ int oracle_attention_rows(const double* q_rows, const double* k, const double* v
   free(jobs);
   free(th);
   return rc;
+}
+
+int oracle_attention_rows(const double* q_rows, const double* k, const double* v,
+                          double* o_rows, const int64_t* rows, int64_t nrows,
+                          int B, int Hq, int Hkv, int64_t Sq, int64_t Sk, int D,
+                          double scale, int causal, int nthreads) {
+  return oracle_attention_rows_lse(q_rows, k, v, o_rows, NULL, rows, nrows, B, Hq, Hkv, Sq, Sk,
+                                   D, scale, causal, nthreads);
 }
 
 /* Softmax probabilities of one query row over all Sk keys (masked keys get 0).
@@ -190,16 +213,17 @@ int oracle_attention_probs(const double* q_row, const double* k, const double* v
   for (j = 0; j < Sk; ++j) p_out[j] = 0.0;
   const double* kb = k + ((int64_t)b * Sk * Hkv + kv) * D;
   const double* vb = v + ((int64_t)b * Sk * Hkv + kv) * D;
-  attend_row(q_row, kb, vb, (int64_t)Hkv * D, n_vis, D, scale, o_out, p_out, s);
+  attend_row(q_row, kb, vb, (int64_t)Hkv * D, n_vis, D, scale, o_out, p_out, NULL, s);
   free(s);
   return 0;
 }
 
 /* Single-token decode: q [B, Hq, D], caches [B, cap, Hkv, D], valid length L
- * shared by the batch and clamped to [0, cap]; o [B, Hq, D]. */
-int oracle_decode(const double* q, const double* kcache, const double* vcache,
-                  double* o, int B, int Hq, int Hkv, int64_t cap, int D,
-                  int64_t L, double scale) {
+ * shared by the batch and clamped to [0, cap]; o [B, Hq, D]; lse [B, Hq] or
+ * NULL. */
+int oracle_decode_lse(const double* q, const double* kcache, const double* vcache,
+                      double* o, double* lse, int B, int Hq, int Hkv, int64_t cap, int D,
+                      int64_t L, double scale) {
   if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || D <= 0 || cap < 0) return 2;
   if (L < 0) L = 0;
   if (L > cap) L = cap;
@@ -213,9 +237,16 @@ int oracle_decode(const double* q, const double* kcache, const double* vcache,
       const double* kb = kcache + ((int64_t)b * cap * Hkv + kv) * D;
       const double* vb = vcache + ((int64_t)b * cap * Hkv + kv) * D;
       attend_row(q + ((int64_t)b * Hq + h) * D, kb, vb, (int64_t)Hkv * D, L, D,
-                 scale, o + ((int64_t)b * Hq + h) * D, NULL, s);
+                 scale, o + ((int64_t)b * Hq + h) * D, NULL,
+                 lse ? lse + (int64_t)b * Hq + h : NULL, s);
     }
   }
   free(s);
   return 0;
+}
+
+int oracle_decode(const double* q, const double* kcache, const double* vcache,
+                  double* o, int B, int Hq, int Hkv, int64_t cap, int D,
+                  int64_t L, double scale) {
+  return oracle_decode_lse(q, kcache, vcache, o, NULL, B, Hq, Hkv, cap, D, L, scale);
 }

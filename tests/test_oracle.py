@@ -356,7 +356,109 @@ def test_scores_far_outside_exp_range_closed_form(scale):
 
 
 # ---------------------------------------------------------------------------
-# 10. Stored oracle values (tests/golden/oracle_tiny.txt, written by
+# 10. Log-sum-exp output: log sum_j exp(s_j) over the visible keys of a row.
+# ---------------------------------------------------------------------------
+def brute_force_lse(q, k, v, scale, causal):
+    """[B, Hq, Sq]: numpy logaddexp.reduce over the explicit masked score
+    matrix (a different formulation from the oracle's max + log(sum))."""
+    q, k = f64(q), f64(k)
+    B, Sq, Hq, D = q.shape
+    _, Sk, Hkv, _ = k.shape
+    G = Hq // Hkv
+    out = np.full((B, Hq, Sq), -np.inf)
+    for b in range(B):
+        for h in range(Hq):
+            S = scale * (q[b, :, h, :] @ k[b, :, h // G, :].T)
+            for i in range(Sq):
+                vis = np.arange(Sk) <= i + (Sk - Sq) if causal else np.ones(Sk, bool)
+                if vis.any():
+                    out[b, h, i] = np.logaddexp.reduce(S[i, vis])
+    return out
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Sq,Sk,D,causal,dt,scale", TINY)
+def test_lse_brute_force_tiny(B, Hq, Hkv, Sq, Sk, D, causal, dt, scale):
+    q, k, v = fa_inputs.prefill_inputs(B, Hq, Hkv, Sq, Sk, D, dt, seed=3)
+    _, lse = oracle.attention(q, k, v, scale, causal, return_lse=True)
+    ref = brute_force_lse(q, k, v, scale, causal)
+    assert np.array_equal(np.isneginf(lse), np.isneginf(ref))
+    fin = np.isfinite(ref)
+    np.testing.assert_allclose(lse[fin], ref[fin], rtol=0, atol=1e-12)
+
+
+def test_lse_matches_torch_logsumexp_ragged():
+    shape = fa_inputs.RAGGED_NONCAUSAL
+    q, k, v = fa_inputs.prefill_inputs_for(shape, seed=0)
+    _, lse = oracle.attention(q, k, v, shape.scale, False, return_lse=True)
+    G = shape.Hq // shape.Hkv
+    qt = q.to(torch.float64).permute(0, 2, 1, 3)
+    kt = k.to(torch.float64).repeat_interleave(G, dim=2).permute(0, 2, 1, 3)
+    ref = torch.logsumexp(shape.scale * (qt @ kt.transpose(-1, -2)), dim=-1).numpy()
+    np.testing.assert_allclose(lse, ref, rtol=0, atol=1e-11)
+
+
+def test_lse_zero_query_is_log_of_visible_count():
+    """All scores 0: lse = log(number of visible keys); -inf with none."""
+    B, Hq, Hkv, Sq, Sk, D = 1, 2, 1, 9, 6, 8
+    _, k, v = fa_inputs.prefill_inputs(B, Hq, Hkv, Sq, Sk, D, torch.bfloat16, seed=4)
+    q = torch.zeros(B, Sq, Hq, D, dtype=torch.bfloat16)
+    _, lse = oracle.attention(q, k, v, 0.7, True, return_lse=True)
+    for i in range(Sq):
+        n = max(0, min(Sk, i + (Sk - Sq) + 1))
+        want = math.log(n) if n else -math.inf
+        for h in range(Hq):
+            assert lse[0, h, i] == pytest.approx(want, abs=1e-15) if n else lse[0, h, i] == want
+
+
+def test_lse_single_visible_key_is_that_score():
+    """Causal row 0 (Sq = Sk) sees key 0 only: lse = scale * <q_0, k_0>."""
+    q, k, v = fa_inputs.prefill_inputs(1, 3, 1, 5, 5, 16, torch.float32, seed=6)
+    _, lse = oracle.attention(q, k, v, 0.3, True, return_lse=True)
+    for h in range(3):
+        want = 0.3 * float(np.dot(f64(q)[0, 0, h], f64(k)[0, 0, 0]))
+        assert lse[0, h, 0] == pytest.approx(want, abs=1e-13)
+
+
+def test_lse_two_keys_closed_form_and_far_range():
+    """Two keys: lse = max(s0, s1) + log(1 + exp(-|s0 - s1|)); with |s| ~ 1000
+    (exp overflows in fp64) the same closed form gives the larger score."""
+    q = torch.tensor([[[[1.0, 2.0]]]], dtype=torch.float64)
+    k = torch.tensor([[[[0.5, -1.0]], [[2.0, 0.25]]]], dtype=torch.float64)
+    v = torch.zeros(1, 2, 1, 2, dtype=torch.float64)
+    for scale in (0.7, 500.0, -500.0):
+        s0, s1 = scale * -1.5, scale * 2.5
+        want = max(s0, s1) + math.log1p(math.exp(-abs(s0 - s1)))
+        _, lse = oracle.attention(q, k, v, scale, False, return_lse=True)
+        assert lse[0, 0, 0] == pytest.approx(want, rel=1e-15, abs=1e-15)
+
+
+def test_lse_normalises_the_probabilities():
+    """exp(s_j - lse) are the softmax probabilities: they sum to one and equal
+    the oracle's P row."""
+    q, k, v = fa_inputs.prefill_inputs(1, 2, 1, 7, 11, 8, torch.bfloat16, seed=8)
+    _, lse = oracle.attention(q, k, v, 0.4, True, return_lse=True)
+    qd, kd = f64(q), f64(k)
+    for h in range(2):
+        for i in (0, 3, 6):
+            p, _ = oracle.probs(q, k, v, 0.4, True, b=0, h=h, i=i)
+            s = 0.4 * (kd[0, :, 0, :] @ qd[0, i, h])
+            vis = p > 0
+            np.testing.assert_allclose(np.exp(s[vis] - lse[0, h, i]), p[vis], rtol=1e-13)
+            assert np.exp(s[vis] - lse[0, h, i]).sum() == pytest.approx(1.0, abs=1e-14)
+
+
+def test_decode_lse_equals_prefill_lse_and_ignores_nan_tail():
+    q, kc, vc, L = fa_inputs.decode_inputs(2, 8, 2, 64, 32, seed=2, L=41)
+    _, lse_dec = oracle.decode(q, kc, vc, L, 0.2, return_lse=True)
+    _, lse_pre = oracle.attention(q, kc[:, :L], vc[:, :L], 0.2, False, return_lse=True)
+    np.testing.assert_array_equal(lse_dec, lse_pre[:, :, 0])
+    assert np.all(np.isfinite(lse_dec))
+    _, lse0 = oracle.decode(q, kc, vc, 0, 0.2, return_lse=True)
+    assert np.all(np.isneginf(lse0))
+
+
+# ---------------------------------------------------------------------------
+# 11. Stored oracle values (tests/golden/oracle_tiny.txt, written by
 #     tests/golden/make_golden.py from the oracle alone): drift guard.
 # ---------------------------------------------------------------------------
 def test_golden_oracle_values_unchanged():

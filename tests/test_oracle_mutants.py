@@ -64,6 +64,12 @@ MUTANTS = [
      "if (L > cap) L = cap;", "if (L >= cap) L = cap - 1;"),
     ("probabilities_not_normalised",
      "p_out[j] = s[j] / l;", "p_out[j] = s[j];"),
+    ("lse_without_max",
+     "if (lse) *lse = m + log(l);", "if (lse) *lse = log(l);"),
+    ("lse_log_of_mean",
+     "if (lse) *lse = m + log(l);", "if (lse) *lse = m + log(l / (double)n_vis);"),
+    ("lse_empty_row_zero",
+     "if (lse) *lse = -INFINITY;", "if (lse) *lse = 0.0;"),
 ]
 
 PIN_ARGS = ["-m", "pytest", os.path.join(ROOT, "tests", "test_oracle.py"), "-x", "-q",
