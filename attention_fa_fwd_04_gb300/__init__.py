@@ -6,11 +6,13 @@ no fallback: if the library is missing or cannot be loaded, every call raises.
 
 Raw entry points (same names and argument order as the C ABI; pointers are
 integers, ``stream`` a ``cudaStream_t`` value):
-    fa_prefill_fwd, fa_decode_fwd, fa_decode_fwd_noalloc, fa_status_string,
-    fa_device_error, fa_last_cuda_error, fa_num_sms, fa_prefill_work_item
+    fa_prefill_fwd, fa_prefill_fwd_lse, fa_decode_fwd, fa_decode_fwd_lse,
+    fa_decode_fwd_noalloc, fa_status_string, fa_device_error, fa_last_cuda_error,
+    fa_num_sms, fa_prefill_work_item
 Tensor conveniences (contiguous CUDA tensors, caller-owned outputs):
-    prefill(q, k, v, scale, causal, out=None, stream=None)
-    decode(q, kcache, vcache, valid_len, scale, out=None, stream=None)
+    prefill(q, k, v, scale, causal, out=None, stream=None, lse=None)
+    decode(q, kcache, vcache, valid_len, scale, out=None, stream=None, lse=None)
+    (lse=True allocates the fp32 log-sum-exp output; a tensor is used as is.)
 """
 import ctypes
 import os
@@ -23,8 +25,9 @@ FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = 0, 
 FA_ERR_TOO_LARGE = 5
 
 # Every symbol include/fa.h declares (checked by the tests against the header).
-EXPORTS = ("fa_prefill_fwd", "fa_decode_fwd", "fa_decode_fwd_noalloc", "fa_status_string",
-           "fa_device_error", "fa_last_cuda_error", "fa_num_sms", "fa_prefill_work_item")
+EXPORTS = ("fa_prefill_fwd", "fa_prefill_fwd_lse", "fa_decode_fwd", "fa_decode_fwd_lse",
+           "fa_decode_fwd_noalloc", "fa_status_string", "fa_device_error", "fa_last_cuda_error",
+           "fa_num_sms", "fa_prefill_work_item")
 
 _lib = None
 
@@ -52,8 +55,13 @@ def load(path: str = LIB_PATH):
     vp, i32, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
     lib.fa_prefill_fwd.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, i32, i32, vp]
     lib.fa_prefill_fwd.restype = i32
+    lib.fa_prefill_fwd_lse.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, i32,
+                                       i32, vp]
+    lib.fa_prefill_fwd_lse.restype = i32
     lib.fa_decode_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp]
     lib.fa_decode_fwd.restype = i32
+    lib.fa_decode_fwd_lse.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp]
+    lib.fa_decode_fwd_lse.restype = i32
     lib.fa_decode_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp]
     lib.fa_decode_fwd_noalloc.restype = i32
     lib.fa_status_string.argtypes = [i32]
@@ -78,9 +86,20 @@ def fa_prefill_fwd(q, k, v, o, B, Hq, Hkv, Sq, Sk, D, scale, causal, dtype, stre
     return load().fa_prefill_fwd(q, k, v, o, B, Hq, Hkv, Sq, Sk, D, scale, causal, dtype, stream)
 
 
+def fa_prefill_fwd_lse(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, causal, dtype, stream):
+    return load().fa_prefill_fwd_lse(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, causal, dtype,
+                                     stream)
+
+
 def fa_decode_fwd(q, kcache, vcache, valid_len_dev, o, B, Hq, Hkv, cap, D, scale, stream):
     return load().fa_decode_fwd(q, kcache, vcache, valid_len_dev, o, B, Hq, Hkv, cap, D, scale,
                                 stream)
+
+
+def fa_decode_fwd_lse(q, kcache, vcache, valid_len_dev, o, lse, B, Hq, Hkv, cap, D, scale,
+                      stream):
+    return load().fa_decode_fwd_lse(q, kcache, vcache, valid_len_dev, o, lse, B, Hq, Hkv, cap, D,
+                                    scale, stream)
 
 
 def fa_decode_fwd_noalloc(q, kcache, vcache, valid_len_dev, o, B, Hq, Hkv, cap, D, scale,
@@ -150,12 +169,24 @@ def _check(t, name):
         raise ValueError(f"{name} must be a contiguous CUDA tensor")
 
 
-def prefill(q, k, v, scale, causal, out=None, stream=None):
+def _lse_tensor(lse, shape, like):
+    import torch
+    if lse is True:
+        return torch.empty(shape, dtype=torch.float32, device=like.device)
+    if lse.dtype != torch.float32 or tuple(lse.shape) != tuple(shape):
+        raise ValueError(f"lse must be a float32 tensor of shape {tuple(shape)}")
+    _check(lse, "lse")
+    return lse
+
+
+def prefill(q, k, v, scale, causal, out=None, stream=None, lse=None):
     """O = softmax(scale * Q K^T [+ causal mask]) V.
 
     q [B,Sq,Hq,D], k/v [B,Sk,Hkv,D]: contiguous CUDA bf16/fp16 tensors.
     Returns ``out`` (allocated like q if None).  Enqueued on ``stream``
     (default: torch's current stream); no host synchronisation.
+    lse: None, True (allocate) or a float32 [B,Hq,Sq] tensor; when given,
+    returns (out, lse) with each row's log-sum-exp (-inf: no visible key).
     """
     import torch
     B, Sq, Hq, D = q.shape
@@ -169,6 +200,14 @@ def prefill(q, k, v, scale, causal, out=None, stream=None):
     if out is None:
         out = torch.empty_like(q)
     _check(out, "out")
+    if lse is not None and lse is not False:
+        lse = _lse_tensor(lse, (B, Hq, Sq), q)
+        st = fa_prefill_fwd_lse(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                lse.data_ptr(), B, Hq, Hkv, Sq, Sk, D, float(scale),
+                                int(bool(causal)), _dtype_code(q), _stream_handle(stream))
+        if st != FA_OK:
+            raise FAError(st, "fa_prefill_fwd_lse")
+        return out, lse
     st = fa_prefill_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, Hq, Hkv,
                         Sq, Sk, D, float(scale), int(bool(causal)), _dtype_code(q),
                         _stream_handle(stream))
@@ -177,12 +216,13 @@ def prefill(q, k, v, scale, causal, out=None, stream=None):
     return out
 
 
-def decode(q, kcache, vcache, valid_len, scale, out=None, stream=None):
+def decode(q, kcache, vcache, valid_len, scale, out=None, stream=None, lse=None):
     """Single-token decode over the first L tokens of the cache.
 
     q [B,1,Hq,D] (or [B,Hq,D]) bf16; kcache/vcache [B,cap,Hkv,D] bf16;
     valid_len: int32 CUDA tensor holding L (read on the device only).
-    Returns ``out`` shaped like q.
+    Returns ``out`` shaped like q; with lse (True or a float32 [B,Hq] tensor)
+    returns (out, lse).
     """
     import torch
     B, cap, Hkv, D = kcache.shape
@@ -200,6 +240,14 @@ def decode(q, kcache, vcache, valid_len, scale, out=None, stream=None):
     if out is None:
         out = torch.empty_like(q)
     _check(out, "out")
+    if lse is not None and lse is not False:
+        lse = _lse_tensor(lse, (B, Hq), q)
+        st = fa_decode_fwd_lse(q.data_ptr(), kcache.data_ptr(), vcache.data_ptr(),
+                               valid_len.data_ptr(), out.data_ptr(), lse.data_ptr(), B, Hq, Hkv,
+                               cap, D, float(scale), _stream_handle(stream))
+        if st != FA_OK:
+            raise FAError(st, "fa_decode_fwd_lse")
+        return out, lse
     st = fa_decode_fwd(q.data_ptr(), kcache.data_ptr(), vcache.data_ptr(), valid_len.data_ptr(),
                        out.data_ptr(), B, Hq, Hkv, cap, D, float(scale), _stream_handle(stream))
     if st != FA_OK:

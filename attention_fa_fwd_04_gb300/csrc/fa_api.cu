@@ -76,9 +76,11 @@ static int cuda_status(int e, const char* site) {
   return FA_ERR_CUDA;
 }
 
-extern "C" int fa_prefill_fwd(const void* q, const void* k, const void* v, void* o, int B,
-                              int Hq, int Hkv, int Sq, int Sk, int D, float scale, int causal,
-                              int dtype, cudaStream_t stream) {
+static bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+static int prefill_impl(const void* q, const void* k, const void* v, void* o, float* lse,
+                        bool want_lse, int B, int Hq, int Hkv, int Sq, int Sk, int D,
+                        float scale, int causal, int dtype, cudaStream_t stream) {
   if (B < 0 || Hq < 0 || Hkv < 0 || Sq < 0 || Sk < 0) return FA_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return FA_ERR_INVALID_ARG;
   if (dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_INVALID_ARG;
@@ -86,6 +88,7 @@ extern "C" int fa_prefill_fwd(const void* q, const void* k, const void* v, void*
   if (B == 0 || Hq == 0 || Sq == 0) return FA_OK;  // empty problem: nothing to write
   if (Hkv == 0 || Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
   if (!q || !o || !aligned16(q) || !aligned16(o)) return FA_ERR_INVALID_ARG;
+  if (want_lse && (!lse || !aligned4(lse))) return FA_ERR_INVALID_ARG;
   if (Sk > 0 && (!k || !v || !aligned16(k) || !aligned16(v))) return FA_ERR_INVALID_ARG;
   // Work items (B * Hq * ceil(Sq/256)) and element counts must fit the kernel's
   // 32-bit item index and the tensor maps' 40-bit byte strides.
@@ -93,14 +96,28 @@ extern "C" int fa_prefill_fwd(const void* q, const void* k, const void* v, void*
   if (items > INT32_MAX) return FA_ERR_INVALID_ARG;
   if ((int64_t)Sq * Hq * D * 2 >= (1ll << 40) || (int64_t)Sk * Hkv * D * 2 >= (1ll << 40))
     return FA_ERR_INVALID_ARG;
-  return cuda_status(fa::launch_prefill(q, k, v, o, B, Hq, Hkv, Sq, Sk, D, scale, causal,
-                                        dtype == FA_BF16, stream),
+  return cuda_status(fa::launch_prefill(q, k, v, o, want_lse ? lse : nullptr, B, Hq, Hkv, Sq, Sk,
+                                        D, scale, causal, dtype == FA_BF16, stream),
                      "prefill launch");
 }
 
-extern "C" int fa_decode_fwd(const void* q, const void* kcache, const void* vcache,
-                             const int32_t* valid_len_dev, void* o, int B, int Hq, int Hkv,
-                             int cap, int D, float scale, cudaStream_t stream) {
+extern "C" int fa_prefill_fwd(const void* q, const void* k, const void* v, void* o, int B,
+                              int Hq, int Hkv, int Sq, int Sk, int D, float scale, int causal,
+                              int dtype, cudaStream_t stream) {
+  return prefill_impl(q, k, v, o, nullptr, false, B, Hq, Hkv, Sq, Sk, D, scale, causal, dtype,
+                      stream);
+}
+
+extern "C" int fa_prefill_fwd_lse(const void* q, const void* k, const void* v, void* o,
+                                  float* lse, int B, int Hq, int Hkv, int Sq, int Sk, int D,
+                                  float scale, int causal, int dtype, cudaStream_t stream) {
+  return prefill_impl(q, k, v, o, lse, true, B, Hq, Hkv, Sq, Sk, D, scale, causal, dtype,
+                      stream);
+}
+
+static int decode_impl(const void* q, const void* kcache, const void* vcache,
+                       const int32_t* valid_len_dev, void* o, float* lse, bool want_lse, int B,
+                       int Hq, int Hkv, int cap, int D, float scale, cudaStream_t stream) {
   if (B < 0 || Hq < 0 || Hkv < 0 || cap < 0) return FA_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return FA_ERR_INVALID_ARG;
   if (!isfinite(scale)) return FA_ERR_INVALID_ARG;
@@ -109,23 +126,40 @@ extern "C" int fa_decode_fwd(const void* q, const void* kcache, const void* vcac
   if (B > 65535 || Hq > 65535 || (int64_t)Hkv * ((Hq / Hkv + 15) / 16) > 65535)
     return FA_ERR_INVALID_ARG;
   if (!q || !o || !aligned16(q) || !aligned16(o)) return FA_ERR_INVALID_ARG;
+  if (want_lse && (!lse || !aligned4(lse))) return FA_ERR_INVALID_ARG;
+  if (!want_lse) lse = nullptr;
   if (cap > 0 && (!kcache || !vcache || !valid_len_dev || !aligned16(kcache) ||
                   !aligned16(vcache) || (reinterpret_cast<uintptr_t>(valid_len_dev) & 3u)))
     return FA_ERR_INVALID_ARG;
   if ((int64_t)cap * Hkv * D * 2 >= (1ll << 40)) return FA_ERR_INVALID_ARG;
   if (cap == 0)
-    return cuda_status(fa::launch_decode(q, kcache, vcache, valid_len_dev, o, B, Hq, Hkv, 0, D,
-                                         scale, nullptr, 0, stream),
+    return cuda_status(fa::launch_decode(q, kcache, vcache, valid_len_dev, o, lse, B, Hq, Hkv, 0,
+                                         D, scale, nullptr, 0, stream),
                        "decode zero-fill launch");
   const size_t nf = fa::decode_scratch_floats(B, Hq, Hkv, cap, D);
   void* scratch = nullptr;
   cudaError_t e = cudaMallocAsync(&scratch, nf * sizeof(float), stream);
   if (e != cudaSuccess) return cuda_status(e, "decode cudaMallocAsync");
-  int r = fa::launch_decode(q, kcache, vcache, valid_len_dev, o, B, Hq, Hkv, cap, D, scale,
+  int r = fa::launch_decode(q, kcache, vcache, valid_len_dev, o, lse, B, Hq, Hkv, cap, D, scale,
                             static_cast<float*>(scratch), nf, stream);
   cudaError_t ef = cudaFreeAsync(scratch, stream);
   if (r != 0) return cuda_status(r, "decode launch");
   return cuda_status(ef, "decode cudaFreeAsync");
+}
+
+extern "C" int fa_decode_fwd(const void* q, const void* kcache, const void* vcache,
+                             const int32_t* valid_len_dev, void* o, int B, int Hq, int Hkv,
+                             int cap, int D, float scale, cudaStream_t stream) {
+  return decode_impl(q, kcache, vcache, valid_len_dev, o, nullptr, false, B, Hq, Hkv, cap, D,
+                     scale, stream);
+}
+
+extern "C" int fa_decode_fwd_lse(const void* q, const void* kcache, const void* vcache,
+                                 const int32_t* valid_len_dev, void* o, float* lse, int B,
+                                 int Hq, int Hkv, int cap, int D, float scale,
+                                 cudaStream_t stream) {
+  return decode_impl(q, kcache, vcache, valid_len_dev, o, lse, true, B, Hq, Hkv, cap, D, scale,
+                     stream);
 }
 
 extern "C" const char* fa_status_string(int status) {

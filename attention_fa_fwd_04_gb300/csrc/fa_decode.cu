@@ -54,7 +54,7 @@ struct Cfg {
   static constexpr int STAGE_BYTES = 2 * KV_BYTES;      // K tile + V tile
   static constexpr int SMEM_STAGES = NSTAGE * STAGE_BYTES;
   static_assert(NSTAGE % NWARPS == 0, "each stage must belong to one consumer warp");
-  static constexpr int SMEM_RED = NWARPS * HB * D * 4 + NWARPS * HB * 2 * 4;
+  static constexpr int SMEM_RED = NWARPS * HB * D * 4 + NWARPS * HB * 2 * 4 + NWARPS * HB * 4;
   static constexpr int SMEM_BAR = 2 * NSTAGE * 8 + 16;
   static_assert(HALF_BYTES % 1024 == 0, "128-byte-swizzled tiles need 1 KiB alignment");
   static constexpr int SMEM_TOTAL = 1024 + SMEM_STAGES + SMEM_RED + SMEM_BAR;
@@ -67,6 +67,7 @@ struct DecodeParams {
   float* part_o;             // [B, Hq, nsplit, D] unnormalised partial outputs
   float* part_ml;            // [B, Hq, nsplit, 2] (row max in log2 units, row sum)
   __nv_bfloat16* o;          // [B, Hq, D]
+  float* lse;                // [B, Hq] natural-log log-sum-exp per head, or null
   int B, Hq, Hkv, cap, G, nsplit, n_hb;
   float c;                   // scale * log2(e)
 };
@@ -88,7 +89,8 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
   uint8_t* stages = smem;
   float* red_o = reinterpret_cast<float*>(smem + C::SMEM_STAGES);  // [NW][HB][D]
   float* red_ml = red_o + NW * HB * D;                             // [NW][HB][2]
-  uint64_t* full = reinterpret_cast<uint64_t*>(red_ml + NW * HB * 2);
+  float* red_w = red_ml + NW * HB * 2;                             // [NW][HB] merge weights
+  uint64_t* full = reinterpret_cast<uint64_t*>(red_w + NW * HB);
   uint64_t* empty = full + NSTAGE;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + NSTAGE);
 
@@ -99,15 +101,13 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
 
   // The combine grid may become resident now; it blocks until this grid ends.
   pdl_launch_dependents();
-
-  int L = *p.valid_len;
-  L = L < 0 ? 0 : (L > p.cap ? p.cap : L);
-  const int tiles_total = (L + TT - 1) / TT;
-  const int tps = (tiles_total + p.nsplit - 1) / p.nsplit;
-  const int t_begin = split * tps;
-  int n_tiles = tiles_total - t_begin;
-  n_tiles = n_tiles < 0 ? 0 : (n_tiles > tps ? tps : n_tiles);
-
+  // Prologue that reads nothing an earlier kernel may still be writing (the
+  // tensor maps are kernel parameters); this kernel is launched as a
+  // programmatic dependent, so it overlaps the tail of the previous grid.
+  if (threadIdx.x == dec::NWARPS * 32) {  // producer lane 0: fetch the maps early
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < NSTAGE; ++s) {
       mbar_init(&full[s], 1);
@@ -116,6 +116,18 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
+  // Everything below reads q, L and the caches, and writes the partials (which
+  // the previous call's combine may still be reading): wait for the previous
+  // grid in the stream to complete.
+  pdl_wait_primary();
+
+  int L = *p.valid_len;
+  L = L < 0 ? 0 : (L > p.cap ? p.cap : L);
+  const int tiles_total = (L + TT - 1) / TT;
+  const int tps = (tiles_total + p.nsplit - 1) / p.nsplit;
+  const int t_begin = split * tps;
+  int n_tiles = tiles_total - t_begin;
+  n_tiles = n_tiles < 0 ? 0 : (n_tiles > tps ? tps : n_tiles);
   __syncthreads();
 
   const int g = lane >> 2, tq = lane & 3;
@@ -127,10 +139,6 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
   if (warp == NW) {
     // ---------------- producer warp: lanes stay converged, lane 0 issues ----------------
     const bool leader = lane == 0;
-    if (leader && n_tiles > 0) {
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
-    }
     const uint64_t pol = l2_policy_evict_first();
     int t = 0;
     for (; t < n_tiles; ++t) {
@@ -318,7 +326,8 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
   __syncthreads();
 
   // Merge the warps' partials (weights exp2(m_w - M)) and write this split's
-  // partial for the CTA's heads.
+  // partial for the CTA's heads: the weights once per row, then the outputs
+  // four columns per thread.
   const size_t head0 = (size_t)b * p.Hq + (size_t)hkv * p.G + (size_t)hb * HB;
   int nh = (p.G - hb * HB) < HB ? (p.G - hb * HB) : HB;
   // Self-check: partial rows must lie inside the scratch (records and skips).
@@ -326,100 +335,131 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
     if (threadIdx.x == 0) atomicOr(&g_decode_err, kErrBounds);
     nh = 0;
   }
-  for (int x = threadIdx.x; x < nh * D; x += dec::THREADS) {
-    const int row = x / D, d = x % D;
-    float M = NEG_INF;
-#pragma unroll
-    for (int w = 0; w < NW; ++w) M = fmaxf(M, red_ml[(w * HB + row) * 2]);
-    float o = 0.f;
-    if (M != NEG_INF) {
-#pragma unroll
-      for (int w = 0; w < NW; ++w) {
-        const float mw = red_ml[(w * HB + row) * 2];
-        if (mw != NEG_INF) o += red_o[(w * HB + row) * D + d] * fast_exp2(mw - M);
-      }
-    }
-    p.part_o[((head0 + row) * p.nsplit + split) * D + d] = o;
-  }
   if (threadIdx.x < nh) {
     const int row = threadIdx.x;
     float M = NEG_INF;
+#pragma unroll
     for (int w = 0; w < NW; ++w) M = fmaxf(M, red_ml[(w * HB + row) * 2]);
     float Ls = 0.f;
+#pragma unroll
     for (int w = 0; w < NW; ++w) {
       const float mw = red_ml[(w * HB + row) * 2];
-      if (mw != NEG_INF) Ls += red_ml[(w * HB + row) * 2 + 1] * fast_exp2(mw - M);
+      const float wt = (mw == NEG_INF) ? 0.f : fast_exp2(mw - M);
+      red_w[w * HB + row] = wt;
+      Ls += red_ml[(w * HB + row) * 2 + 1] * wt;
     }
     p.part_ml[((head0 + row) * p.nsplit + split) * 2 + 0] = M;
     p.part_ml[((head0 + row) * p.nsplit + split) * 2 + 1] = Ls;
   }
+  __syncthreads();
+  for (int x = threadIdx.x; x < nh * (D / 4); x += dec::THREADS) {
+    const int row = x / (D / 4), d4 = x % (D / 4);
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      const float wt = red_w[w * HB + row];
+      const float4 v = reinterpret_cast<const float4*>(red_o + (w * HB + row) * D)[d4];
+      o.x += v.x * wt;
+      o.y += v.y * wt;
+      o.z += v.z * wt;
+      o.w += v.w * wt;
+    }
+    reinterpret_cast<float4*>(p.part_o + ((head0 + row) * p.nsplit + split) * D)[d4] = o;
+  }
 }
 
-// Combine: one CTA per (32 output columns, head, batch), 8 warps.  Warp w
-// folds splits w, w+8, ... with an online log-sum-exp merge (lane = column),
-// then warp 0 merges the 8 warp results.  Splits that saw no token (l_s == 0)
-// are skipped without touching o_s.  All loads of a warp are independent, so
-// the kernel costs about one L2 round trip; it is launched with programmatic
-// dependent launch and waits for the split grid in griddepcontrol.wait.
+// Combine: one CTA per (32 output columns, head, batch), 8 warps, up to
+// kMaxSplits splits.  Every load is issued before any result is needed -- the
+// split statistics (thread t: split t) and the partial outputs (lane = column,
+// warp w: splits w, w+8, ...) -- so the kernel costs about one L2 round trip:
+//   M = max over splits that saw a token (l_s > 0),
+//   O = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s.
+// Splits with l_s == 0 get weight 0 (their m_s may be -inf).  Launched with
+// programmatic dependent launch; waits for the split grid in
+// griddepcontrol.wait.
 constexpr int kCombineWarps = 8;
+constexpr int kCombineThreads = kCombineWarps * 32;
+constexpr int kMaxSplits = kCombineThreads;
+constexpr int kSplitsPerWarp = kMaxSplits / kCombineWarps;
 
 template <int D>
-__global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const DecodeParams p) {
+  // A programmatic dependent launched after this grid (the next call's split
+  // kernel) may start its prologue now; it waits for this grid to complete
+  // before it reads or writes anything.
+  pdl_launch_dependents();
   pdl_wait_primary();
-  __shared__ float sM[kCombineWarps], sL[kCombineWarps], sA[kCombineWarps][32];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __shared__ float sW[kMaxSplits];
+  __shared__ float sRed[kCombineWarps];
+  __shared__ float sAcc[kCombineWarps][32];
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int d = blockIdx.x * 32 + lane;
   const int h = blockIdx.y, b = blockIdx.z;
-  if (h >= p.Hq || b >= p.B) {
-    if (threadIdx.x == 0) atomicOr(&g_decode_err, kErrBounds << 4);
+  if (h >= p.Hq || b >= p.B || p.nsplit > kMaxSplits) {
+    if (t == 0) atomicOr(&g_decode_err, kErrBounds << 4);
     return;
   }
   const size_t base = ((size_t)b * p.Hq + h) * p.nsplit;
-  float M = -INFINITY, Ls = 0.f, acc = 0.f;
-#pragma unroll 4
-  for (int s = warp; s < p.nsplit; s += kCombineWarps) {
-    const float ls = p.part_ml[(base + s) * 2 + 1];
-    const float ms = p.part_ml[(base + s) * 2];
-    const float os = (d < D) ? p.part_o[(base + s) * D + d] : 0.f;
-    if (ls > 0.f) {
-      const float mn = fmaxf(M, ms);
-      const float a = fast_exp2(M - mn), w = fast_exp2(ms - mn);  // M = -inf -> a = 0
-      acc = acc * a + os * w;
-      Ls = Ls * a + ls * w;
-      M = mn;
-    }
+  float ov[kSplitsPerWarp];
+#pragma unroll
+  for (int k = 0; k < kSplitsPerWarp; ++k) {
+    const int sp = warp + k * kCombineWarps;
+    ov[k] = (sp < p.nsplit && d < D) ? p.part_o[(base + sp) * D + d] : 0.f;
   }
-  if (lane == 0) {
-    sM[warp] = M;
-    sL[warp] = Ls;
+  float m_t = -INFINITY, l_t = 0.f;
+  if (t < p.nsplit) {
+    l_t = p.part_ml[(base + t) * 2 + 1];
+    m_t = l_t > 0.f ? p.part_ml[(base + t) * 2] : -INFINITY;
   }
-  sA[warp][lane] = acc;
+  // M = block max of m_t.
+  float M = m_t;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  if (lane == 0) sRed[warp] = M;
+  __syncthreads();
+  M = sRed[0];
+#pragma unroll
+  for (int w = 1; w < kCombineWarps; ++w) M = fmaxf(M, sRed[w]);
+  const float w_t = (m_t == -INFINITY) ? 0.f : fast_exp2(m_t - M);  // M = -inf -> all 0
+  sW[t] = w_t;
+  float den = w_t * l_t;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+  __syncthreads();  // sW complete; sRed (max) consumed
+  if (lane == 0) sRed[warp] = den;
+  float acc = 0.f;
+#pragma unroll
+  for (int k = 0; k < kSplitsPerWarp; ++k) {
+    const int sp = warp + k * kCombineWarps;
+    if (sp < p.nsplit) acc += ov[k] * sW[sp];
+  }
+  sAcc[warp][lane] = acc;
   __syncthreads();
   if (warp == 0) {
-    float Mx = -INFINITY;
+    float num = 0.f, dsum = 0.f;
 #pragma unroll
-    for (int w = 0; w < kCombineWarps; ++w) Mx = fmaxf(Mx, sM[w]);
-    float num = 0.f, den = 0.f;
-    if (Mx != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < kCombineWarps; ++w) {
-        if (sM[w] != -INFINITY) {
-          const float wt = fast_exp2(sM[w] - Mx);
-          num += sA[w][lane] * wt;
-          den += sL[w] * wt;
-        }
-      }
+    for (int w = 0; w < kCombineWarps; ++w) {
+      num += sAcc[w][lane];
+      dsum += sRed[w];
     }
-    const float out = den > 0.f ? num / den : 0.f;
+    const float out = dsum > 0.f ? num / dsum : 0.f;
     if (d < D) p.o[((size_t)b * p.Hq + h) * D + d] = __float2bfloat16_rn(out);
+    // log sum_j exp(s_j) = ln2 * (M + log2 sum_s 2^(m_s - M) l_s), M in log2 units.
+    if (p.lse && lane == 0 && blockIdx.x == 0)
+      p.lse[(size_t)b * p.Hq + h] = dsum > 0.f ? 0.6931471805599453f * (M + __log2f(dsum))
+                                               : -INFINITY;
   }
 }
 
-// Degenerate cache (cap == 0): every output is zero.
-__global__ void decode_zero_kernel(__nv_bfloat16* o, size_t n) {
+// Degenerate cache (cap == 0): every output is zero, every log-sum-exp -inf.
+__global__ void decode_zero_kernel(__nv_bfloat16* o, size_t n, float* lse, size_t nl) {
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
        i += (size_t)gridDim.x * blockDim.x)
     o[i] = __float2bfloat16_rn(0.f);
+  if (lse)
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < nl;
+         i += (size_t)gridDim.x * blockDim.x)
+      lse[i] = -INFINITY;
 }
 
 static int decode_nsplit(int B, int Hq, int Hkv, int cap) {
@@ -430,6 +470,7 @@ static int decode_nsplit(int B, int Hq, int Hkv, int cap) {
   long ns = sms / (units > 0 ? units : 1);
   const long max_tiles = ((long)cap + dec::TT - 1) / dec::TT;
   if (ns > max_tiles) ns = max_tiles;
+  if (ns > kMaxSplits) ns = kMaxSplits;  // the combine's one-pass limit
   if (ns < 1) ns = 1;
   return (int)ns;
 }
@@ -441,8 +482,8 @@ size_t decode_scratch_floats(int B, int Hq, int Hkv, int cap, int D) {
 
 template <int D>
 static int launch_decode_t(const void* q, const void* kc, const void* vc, const int32_t* vl,
-                           void* o, int B, int Hq, int Hkv, int cap, float scale, float* scratch,
-                           cudaStream_t stream) {
+                           void* o, float* lse, int B, int Hq, int Hkv, int cap, float scale,
+                           float* scratch, cudaStream_t stream) {
   using C = dec::Cfg<D>;
   CUtensorMap tk, tv;
   if (encode_tmap_rows(&tk, kc, D, Hkv, cap, B, dec::TT)) return cudaErrorInvalidValue;
@@ -455,6 +496,12 @@ static int launch_decode_t(const void* q, const void* kc, const void* vc, const 
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_TOTAL);
     if (e != cudaSuccess) return e;
+    // Same shared-memory carveout as the split kernel, so that combine CTAs
+    // can become resident beside split CTAs and wait there.
+    e = cudaFuncSetAttribute(decode_combine_kernel<D>,
+                             cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
     attr_set[dev] = 1;
   }
   DecodeParams p;
@@ -464,6 +511,7 @@ static int launch_decode_t(const void* q, const void* kc, const void* vc, const 
   p.part_o = scratch;
   p.part_ml = scratch + (size_t)B * Hq * ns * D;
   p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
   p.B = B;
   p.Hq = Hq;
   p.Hkv = Hkv;
@@ -473,19 +521,26 @@ static int launch_decode_t(const void* q, const void* kc, const void* vc, const 
   p.n_hb = (p.G + dec::HB - 1) / dec::HB;
   p.c = scale * 1.4426950408889634f;
 
-  dim3 grid(ns, Hkv * p.n_hb, B);
-  decode_split_kernel<D><<<grid, dec::THREADS, C::SMEM_TOTAL, stream>>>(tk, tv, p);
-  cudaError_t e = cudaGetLastError();
+  // Both kernels are programmatic dependents of the grid before them: each
+  // runs only its prologue before griddepcontrol.wait.
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t sc = {};
+  sc.gridDim = dim3(ns, Hkv * p.n_hb, B);
+  sc.blockDim = dim3(dec::THREADS, 1, 1);
+  sc.dynamicSmemBytes = C::SMEM_TOTAL;
+  sc.stream = stream;
+  sc.attrs = attr;
+  sc.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&sc, decode_split_kernel<D>, tk, tv, p);
   if (e != cudaSuccess) return e;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((D + 31) / 32, Hq, B);
-  cfg.blockDim = dim3(kCombineWarps * 32, 1, 1);
+  cfg.blockDim = dim3(kCombineThreads, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   e = cudaLaunchKernelEx(&cfg, decode_combine_kernel<D>, p);
@@ -493,19 +548,21 @@ static int launch_decode_t(const void* q, const void* kc, const void* vc, const 
 }
 
 int launch_decode(const void* q, const void* kc, const void* vc, const int32_t* valid_len,
-                  void* o, int B, int Hq, int Hkv, int cap, int D, float scale, float* scratch,
-                  size_t scratch_floats, cudaStream_t stream) {
+                  void* o, float* lse, int B, int Hq, int Hkv, int cap, int D, float scale,
+                  float* scratch, size_t scratch_floats, cudaStream_t stream) {
   if (B == 0 || Hq == 0) return cudaSuccess;
   if (cap == 0) {
     const size_t n = (size_t)B * Hq * D;
     decode_zero_kernel<<<(unsigned)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096), 256, 0,
-                         stream>>>(static_cast<__nv_bfloat16*>(o), n);
+                         stream>>>(static_cast<__nv_bfloat16*>(o), n, lse, (size_t)B * Hq);
     return cudaGetLastError();
   }
   if (scratch_floats < decode_scratch_floats(B, Hq, Hkv, cap, D)) return cudaErrorInvalidValue;
   if (D == 64)
-    return launch_decode_t<64>(q, kc, vc, valid_len, o, B, Hq, Hkv, cap, scale, scratch, stream);
-  return launch_decode_t<128>(q, kc, vc, valid_len, o, B, Hq, Hkv, cap, scale, scratch, stream);
+    return launch_decode_t<64>(q, kc, vc, valid_len, o, lse, B, Hq, Hkv, cap, scale, scratch,
+                               stream);
+  return launch_decode_t<128>(q, kc, vc, valid_len, o, lse, B, Hq, Hkv, cap, scale, scratch,
+                              stream);
 }
 
 int read_decode_error(unsigned int* out, int reset) {

@@ -90,8 +90,8 @@ extern "C" int fa_decode_fwd_noalloc(const void* q, const void* kcache, const vo
   if ((int64_t)cap * Hkv * D * 2 >= (1ll << 40)) return FA_ERR_INVALID_ARG;
   if (cap == 0) {
     // No cache: O = 0, no partials needed.
-    return fa::launch_decode(q, kcache, vcache, valid_len_dev, o, B, Hq, Hkv, 0, D, scale,
-                             nullptr, 0, stream) == 0
+    return fa::launch_decode(q, kcache, vcache, valid_len_dev, o, nullptr, B, Hq, Hkv, 0, D,
+                             scale, nullptr, 0, stream) == 0
                ? FA_OK
                : FA_ERR_CUDA;
   }
@@ -100,7 +100,7 @@ extern "C" int fa_decode_fwd_noalloc(const void* q, const void* kcache, const vo
   cudaError_t err = cudaSuccess;
   float* scratch = scratch_for_current_device(&err);
   if (!scratch) return FA_ERR_CUDA;
-  const int r = fa::launch_decode(q, kcache, vcache, valid_len_dev, o, B, Hq, Hkv, cap, D, scale,
-                                  scratch, kNoAllocScratchFloats, stream);
+  const int r = fa::launch_decode(q, kcache, vcache, valid_len_dev, o, nullptr, B, Hq, Hkv, cap,
+                                  D, scale, scratch, kNoAllocScratchFloats, stream);
   return r == 0 ? FA_OK : FA_ERR_CUDA;
 }

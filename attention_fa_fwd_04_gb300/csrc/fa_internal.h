@@ -17,15 +17,18 @@ int encode_tmap_rows(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d
 // SM count of the current device (cached per device), or -1.
 int sm_count();
 
-// Enqueue the prefill kernel.  Returns a cudaError_t (0 = success).
-int launch_prefill(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv,
-                   int Sq, int Sk, int D, float scale, int causal, bool bf16, cudaStream_t stream);
+// Enqueue the prefill kernel; lse ([B, Hq, Sq] fp32) may be null.  Returns a
+// cudaError_t (0 = success).
+int launch_prefill(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                   int Hq, int Hkv, int Sq, int Sk, int D, float scale, int causal, bool bf16,
+                   cudaStream_t stream);
 
 // Enqueue split + combine decode kernels with the given fp32 scratch
-// (partials).  scratch_floats is its size in floats.  Returns a cudaError_t.
+// (partials); lse ([B, Hq] fp32) may be null.  scratch_floats is the scratch
+// size in floats.  Returns a cudaError_t.
 int launch_decode(const void* q, const void* kc, const void* vc, const int32_t* valid_len,
-                  void* o, int B, int Hq, int Hkv, int cap, int D, float scale, float* scratch,
-                  size_t scratch_floats, cudaStream_t stream);
+                  void* o, float* lse, int B, int Hq, int Hkv, int cap, int D, float scale,
+                  float* scratch, size_t scratch_floats, cudaStream_t stream);
 
 // Scratch floats the decode needs for these sizes.
 size_t decode_scratch_floats(int B, int Hq, int Hkv, int cap, int D);

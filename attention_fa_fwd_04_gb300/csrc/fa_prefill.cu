@@ -70,7 +70,8 @@ struct Cfg {
 }  // namespace pf
 
 struct PrefillParams {
-  void* o;  // [B, Sq, Hq, D]
+  void* o;     // [B, Sq, Hq, D]
+  float* lse;  // [B, Hq, Sq] natural-log log-sum-exp per row, or null
   int B, Hq, Hkv, Sq, Sk, G, causal, n_qb, n_items;
   float c;  // scale * log2(e)
 };
@@ -413,6 +414,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
 #pragma unroll
           for (int x = 0; x < D / 8; ++x)
             reinterpret_cast<uint4*>(orow)[x] = make_uint4(0u, 0u, 0u, 0u);
+          if (p.lse) p.lse[((size_t)b * p.Hq + hq) * p.Sq + grow] = NEG_INF;
         }
         continue;
       }
@@ -562,6 +564,11 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       __syncwarp();
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
+      // log sum_j exp(s_j) = ln2 * (m_used + log2 l): m_used is the row max of
+      // s * log2(e) the P values were taken against.
+      if (p.lse && grow < p.Sq && b < p.B && hq < p.Hq)
+        p.lse[((size_t)b * p.Hq + hq) * p.Sq + grow] =
+            l > 0.f ? 0.6931471805599453f * (m_used + __log2f(l)) : NEG_INF;
 #pragma unroll
       for (int q4 = 0; q4 < D / 32; ++q4) {
         uint32_t orr[32];
@@ -598,17 +605,21 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
   }
 }
 
-// Sk == 0: no key is visible to any row, O = 0.
+// Sk == 0: no key is visible to any row, O = 0 and log-sum-exp -inf.
 template <typename T>
-__global__ void prefill_zero_kernel(T* o, size_t n) {
+__global__ void prefill_zero_kernel(T* o, size_t n, float* lse, size_t nl) {
   for (size_t x = blockIdx.x * (size_t)blockDim.x + threadIdx.x; x < n;
        x += (size_t)gridDim.x * blockDim.x)
     o[x] = T(0.f);
+  if (lse)
+    for (size_t x = blockIdx.x * (size_t)blockDim.x + threadIdx.x; x < nl;
+         x += (size_t)gridDim.x * blockDim.x)
+      lse[x] = -INFINITY;
 }
 
 template <int D, typename T>
-static int launch_prefill_t(const void* q, const void* k, const void* v, void* o, int B, int Hq,
-                            int Hkv, int Sq, int Sk, float scale, int causal,
+static int launch_prefill_t(const void* q, const void* k, const void* v, void* o, float* lse,
+                            int B, int Hq, int Hkv, int Sq, int Sk, float scale, int causal,
                             cudaStream_t stream) {
   using C = pf::Cfg<D>;
   CUtensorMap tq, tk, tv;
@@ -627,6 +638,7 @@ static int launch_prefill_t(const void* q, const void* k, const void* v, void* o
   }
   PrefillParams p;
   p.o = o;
+  p.lse = lse;
   p.B = B;
   p.Hq = Hq;
   p.Hkv = Hkv;
@@ -646,28 +658,29 @@ static int launch_prefill_t(const void* q, const void* k, const void* v, void* o
   return cudaGetLastError();
 }
 
-int launch_prefill(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv,
-                   int Sq, int Sk, int D, float scale, int causal, bool bf16,
+int launch_prefill(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                   int Hq, int Hkv, int Sq, int Sk, int D, float scale, int causal, bool bf16,
                    cudaStream_t stream) {
   if (B == 0 || Hq == 0 || Sq == 0) return cudaSuccess;
   if (Sk == 0) {
-    const size_t n = (size_t)B * Sq * Hq * D;
+    const size_t n = (size_t)B * Sq * Hq * D, nl = (size_t)B * Hq * Sq;
     const unsigned blocks = (unsigned)((n + 255) / 256 < 8192 ? (n + 255) / 256 : 8192);
     if (bf16)
       prefill_zero_kernel<__nv_bfloat16><<<blocks, 256, 0, stream>>>(
-          static_cast<__nv_bfloat16*>(o), n);
+          static_cast<__nv_bfloat16*>(o), n, lse, nl);
     else
-      prefill_zero_kernel<__half><<<blocks, 256, 0, stream>>>(static_cast<__half*>(o), n);
+      prefill_zero_kernel<__half><<<blocks, 256, 0, stream>>>(static_cast<__half*>(o), n, lse,
+                                                              nl);
     return cudaGetLastError();
   }
   if (D == 64)
-    return bf16 ? launch_prefill_t<64, __nv_bfloat16>(q, k, v, o, B, Hq, Hkv, Sq, Sk, scale,
+    return bf16 ? launch_prefill_t<64, __nv_bfloat16>(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, scale,
                                                        causal, stream)
-                : launch_prefill_t<64, __half>(q, k, v, o, B, Hq, Hkv, Sq, Sk, scale, causal,
-                                               stream);
-  return bf16 ? launch_prefill_t<128, __nv_bfloat16>(q, k, v, o, B, Hq, Hkv, Sq, Sk, scale,
+                : launch_prefill_t<64, __half>(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, scale,
+                                               causal, stream);
+  return bf16 ? launch_prefill_t<128, __nv_bfloat16>(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, scale,
                                                       causal, stream)
-              : launch_prefill_t<128, __half>(q, k, v, o, B, Hq, Hkv, Sq, Sk, scale, causal,
+              : launch_prefill_t<128, __half>(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, scale, causal,
                                               stream);
 }
 

@@ -23,6 +23,17 @@
  *                   review finding: unused cache capacity may hold NaN and must
  *                   not reach the output; split-KV named as the next step).
  *
+ *   fa_prefill_fwd_lse, fa_decode_fwd_lse
+ *                   the same operations, also writing each row's log-sum-exp
+ *                   lse = log sum_j exp(scale * <q, k_j>) over its visible keys
+ *                   (fp32, natural log; -inf for a row with no visible key).
+ *                   It is the per-row statistic a backward pass recomputes P
+ *                   from (tessera #90, flash-attention backward commit note:
+ *                   the "_pre" kernel's logsumexp) and the one partial results
+ *                   over key ranges are merged by; rocm-libraries #13108 lists
+ *                   the LSE output among what its first decode milestone
+ *                   leaves out.
+ *
  * Conventions shared by every entry point
  * ---------------------------------------
  * - Tensors are contiguous, row-major, in device memory (or memory the device
@@ -88,6 +99,19 @@ int fa_prefill_fwd(const void* q, const void* k, const void* v, void* o,
                    float scale, int causal, int dtype, cudaStream_t stream);
 
 /*
+ * fa_prefill_fwd_lse -- fa_prefill_fwd that also writes
+ *
+ *   lse    [B, Hq, Sq]  fp32, 4-byte aligned, written:
+ *          lse[b,h,i] = log sum_j exp(scale * <q[b,i,h], k[b,j,h/G]>) over the
+ *          keys row i sees; -inf for a row that sees none.
+ *
+ * Everything else as fa_prefill_fwd; lse == NULL is FA_ERR_INVALID_ARG.
+ */
+int fa_prefill_fwd_lse(const void* q, const void* k, const void* v, void* o, float* lse,
+                       int B, int Hq, int Hkv, int Sq, int Sk, int D,
+                       float scale, int causal, int dtype, cudaStream_t stream);
+
+/*
  * fa_decode_fwd -- one new query token per sequence against a KV cache.
  *
  *   q              [B, 1, Hq, D]      bf16, read only
@@ -105,7 +129,11 @@ int fa_prefill_fwd(const void* q, const void* k, const void* v, void* o,
  *
  * Scratch: the split partials (fp32) are allocated stream-ordered on `stream`
  * (cudaMallocAsync / cudaFreeAsync), so calls on different streams never share
- * scratch.  Two kernels are enqueued: the split kernel and the combine.
+ * scratch.  Two kernels are enqueued: the split kernel and the combine, each
+ * launched as a programmatic dependent of the grid before it on the stream:
+ * before its griddepcontrol.wait a kernel only initialises shared-memory
+ * barriers and prefetches its tensor maps, so it reads nothing an earlier
+ * kernel may still be writing.
  *
  * Returns FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED (dtype other than
  * bf16), or FA_ERR_CUDA.
@@ -114,6 +142,19 @@ int fa_decode_fwd(const void* q, const void* kcache, const void* vcache,
                   const int32_t* valid_len_dev, void* o,
                   int B, int Hq, int Hkv, int cap, int D, float scale,
                   cudaStream_t stream);
+
+/*
+ * fa_decode_fwd_lse -- fa_decode_fwd that also writes
+ *
+ *   lse    [B, Hq]  fp32, 4-byte aligned, written: the log-sum-exp of each
+ *          head's scores over the L valid tokens; -inf when L == 0.
+ *
+ * Everything else as fa_decode_fwd; lse == NULL is FA_ERR_INVALID_ARG.
+ */
+int fa_decode_fwd_lse(const void* q, const void* kcache, const void* vcache,
+                      const int32_t* valid_len_dev, void* o, float* lse,
+                      int B, int Hq, int Hkv, int cap, int D, float scale,
+                      cudaStream_t stream);
 
 /*
  * fa_decode_fwd_noalloc -- fa_decode_fwd for callers that cannot allocate

@@ -88,3 +88,19 @@ def test_decode_empty_problems_are_noops(lib):
     import attention_fa_fwd_04_gb300 as fa
     assert fa.fa_decode_fwd(0, 0, 0, 0, 0, 0, 8, 2, 128, 128, 0.1, 0) == fa.FA_OK
     assert fa.fa_decode_fwd(0, 0, 0, 0, 0, 1, 0, 2, 128, 128, 0.1, 0) == fa.FA_OK
+
+
+def test_lse_variants_reject_missing_or_misaligned_lse(lib):
+    import attention_fa_fwd_04_gb300 as fa
+    for lse in (0, FAKE + 2):
+        assert fa.fa_prefill_fwd_lse(FAKE, FAKE, FAKE, FAKE, lse, 1, 4, 2, 16, 16, 64, 0.125, 1,
+                                     fa.FA_BF16, 0) == fa.FA_ERR_INVALID_ARG
+        assert fa.fa_decode_fwd_lse(FAKE, FAKE, FAKE, FAKE, FAKE, lse, 1, 8, 2, 128, 128, 0.088,
+                                    0) == fa.FA_ERR_INVALID_ARG
+    # the remaining argument rules are the plain entry points'
+    assert fa.fa_prefill_fwd_lse(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 2, 16, 16, 96, 0.125, 1,
+                                 fa.FA_BF16, 0) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_decode_fwd_lse(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 3, 2, 128, 128, 0.088,
+                                0) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_prefill_fwd_lse(0, 0, 0, 0, 0, 0, 4, 2, 16, 16, 64, 0.1, 1, fa.FA_BF16,
+                                 0) == fa.FA_OK
