@@ -14,15 +14,20 @@
 // Design (HBM-bound: 2*L*Hkv*D*2 bytes read, ~4 flop per byte):
 //   grid   = (nsplit, Hkv * ceil(G/16), B), one CTA per SM, sized from cap and
 //            the SM count (not from L, which the host never reads);
-//   CTA    = 1 producer warp issuing TMA tile loads (64 tokens x D, K and V,
-//            128-byte swizzle) into a 6-stage mbarrier ring, and 4 consumer
+//   CTA    = 1 producer warp issuing TMA tile loads (32 tokens x D, K and V,
+//            128-byte swizzle) into an 8-stage mbarrier ring (16 for D = 64,
+//            128 KiB in flight), and 4 consumer
 //            warps that each own whole tiles: S = Q K^T and O += P V with
 //            mma.sync m16n8k16 (the group's query heads padded to M = 16), an
 //            exp2 online softmax per warp, then a cross-warp merge in shared
 //            memory into one (max, sum, o[D]) partial per head and split;
-//   combine= one CTA per (b, head) merges the split partials with weights
-//            exp2(m_s - M); launched with programmatic dependent launch so its
-//            launch overlaps the split kernel.
+//   combine= one CTA per (32 columns, head, b) merges the split partials with
+//            weights exp2(m_s - M).
+// Both kernels are launched as programmatic dependents of the grid before
+// them.  Before its griddepcontrol.wait the split kernel only initialises its
+// barriers and prefetches (tensor maps, and its first K/V tiles into L2), so
+// in a sequence of calls the next call's prologue and first HBM reads overlap
+// the current call's merge, combine and grid boundaries.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -39,6 +44,9 @@ constexpr int NWARPS = 4;     // consumer warps
 constexpr int THREADS = (NWARPS + 1) * 32;
 constexpr int HB = 16;        // query heads per CTA: the MMA's M
 constexpr int HALF_BYTES = TT * 128;  // TT rows x 64 elements x 2 bytes
+// Bytes of K/V per CTA warmed in L2 before the grid wait: with one CTA per SM
+// that is at most about half of L2 in flight, whatever the cache length.
+constexpr int PREFETCH_BYTES = 384 * 1024;
 
 // Tile t lives in stage t % NSTAGE and is consumed by warp t % NWARPS.  With
 // NSTAGE a multiple of NWARPS every stage belongs to exactly one warp, which
@@ -107,6 +115,28 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
   if (threadIdx.x == dec::NWARPS * 32) {  // producer lane 0: fetch the maps early
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
+  } else if (lane == 0 && warp < NW) {
+    // Consumer lanes warm L2 with this CTA's first tiles while the previous
+    // grid finishes (HBM is otherwise idle then).  L is read without ordering
+    // here, so the tile range may be stale; that only wastes the prefetch --
+    // nothing read before griddepcontrol.wait below reaches shared memory or
+    // registers, and L2 stays coherent with any write still to come.
+    int Ls = ld_relaxed_gpu(p.valid_len);
+    Ls = Ls < 0 ? 0 : (Ls > p.cap ? p.cap : Ls);
+    const int tt = (Ls + TT - 1) / TT;
+    const int tp = (tt + p.nsplit - 1) / p.nsplit;
+    const int tb = split * tp;
+    int nt = tt - tb;
+    nt = nt < 0 ? 0 : (nt > tp ? tp : nt);
+    if (nt > dec::PREFETCH_BYTES / C::STAGE_BYTES) nt = dec::PREFETCH_BYTES / C::STAGE_BYTES;
+    for (int t = warp; t < nt; t += NW) {
+      const int tok = (tb + t) * TT;
+#pragma unroll
+      for (int h = 0; h < C::HALVES; ++h) {
+        tma_prefetch_l2_4d(&tmK, h * 64, hkv, tok, b);
+        tma_prefetch_l2_4d(&tmV, h * 64, hkv, tok, b);
+      }
+    }
   }
   if (threadIdx.x == 0) {
     for (int s = 0; s < NSTAGE; ++s) {
