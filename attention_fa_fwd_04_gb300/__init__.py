@@ -6,11 +6,13 @@ no fallback: if the library is missing or cannot be loaded, every call raises.
 
 Raw entry points (same names and argument order as the C ABI; pointers are
 integers, ``stream`` a ``cudaStream_t`` value):
-    fa_prefill_fwd, fa_prefill_fwd_lse, fa_decode_fwd, fa_decode_fwd_lse,
+    fa_prefill_fwd, fa_prefill_fwd_lse, fa_prefill_varlen_fwd, fa_decode_fwd, fa_decode_fwd_lse,
     fa_decode_fwd_noalloc, fa_status_string, fa_device_error, fa_last_cuda_error,
     fa_num_sms, fa_prefill_work_item
 Tensor conveniences (contiguous CUDA tensors, caller-owned outputs):
     prefill(q, k, v, scale, causal, out=None, stream=None, lse=None)
+    prefill_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, scale, causal,
+                   out=None, stream=None, lse=None)
     decode(q, kcache, vcache, valid_len, scale, out=None, stream=None, lse=None)
     (lse=True allocates the fp32 log-sum-exp output; a tensor is used as is.)
 """
@@ -25,7 +27,8 @@ FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = 0, 
 FA_ERR_TOO_LARGE = 5
 
 # Every symbol include/fa.h declares (checked by the tests against the header).
-EXPORTS = ("fa_prefill_fwd", "fa_prefill_fwd_lse", "fa_decode_fwd", "fa_decode_fwd_lse",
+EXPORTS = ("fa_prefill_fwd", "fa_prefill_fwd_lse", "fa_prefill_varlen_fwd", "fa_decode_fwd",
+           "fa_decode_fwd_lse",
            "fa_decode_fwd_noalloc", "fa_status_string", "fa_device_error", "fa_last_cuda_error",
            "fa_num_sms", "fa_prefill_work_item")
 
@@ -58,6 +61,9 @@ def load(path: str = LIB_PATH):
     lib.fa_prefill_fwd_lse.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, i32,
                                        i32, vp]
     lib.fa_prefill_fwd_lse.restype = i32
+    lib.fa_prefill_varlen_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
+                                          i32, i32, f32, i32, i32, vp]
+    lib.fa_prefill_varlen_fwd.restype = i32
     lib.fa_decode_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp]
     lib.fa_decode_fwd.restype = i32
     lib.fa_decode_fwd_lse.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp]
@@ -89,6 +95,13 @@ def fa_prefill_fwd(q, k, v, o, B, Hq, Hkv, Sq, Sk, D, scale, causal, dtype, stre
 def fa_prefill_fwd_lse(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, causal, dtype, stream):
     return load().fa_prefill_fwd_lse(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, causal, dtype,
                                      stream)
+
+
+def fa_prefill_varlen_fwd(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, B, Hq, Hkv, total_q,
+                          total_k, max_seqlen_q, D, scale, causal, dtype, stream):
+    return load().fa_prefill_varlen_fwd(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, B, Hq, Hkv,
+                                        total_q, total_k, max_seqlen_q, D, scale, causal, dtype,
+                                        stream)
 
 
 def fa_decode_fwd(q, kcache, vcache, valid_len_dev, o, B, Hq, Hkv, cap, D, scale, stream):
@@ -214,6 +227,47 @@ def prefill(q, k, v, scale, causal, out=None, stream=None, lse=None):
     if st != FA_OK:
         raise FAError(st, "fa_prefill_fwd")
     return out
+
+
+def prefill_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, scale, causal, out=None,
+                   stream=None, lse=None):
+    """Attention over packed sequences of different lengths.
+
+    q [total_q,Hq,D], k/v [total_k,Hkv,D]: contiguous CUDA bf16/fp16 tensors;
+    cu_seqlens_q / cu_seqlens_k: int32 CUDA tensors [B+1] (prefix sums of the
+    lengths, read on the device only); max_seqlen_q >= every query length.
+    Returns ``out`` ([total_q,Hq,D]), or (out, lse) with lse [Hq,total_q] fp32
+    when lse is True or a tensor.
+    """
+    import torch
+    total_q, Hq, D = q.shape
+    total_k, Hkv, Dk = k.shape
+    if Dk != D or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("shape mismatch between q, k, v")
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k, v must share a dtype")
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (cu_seqlens_q, "cu_seqlens_q"),
+                 (cu_seqlens_k, "cu_seqlens_k")):
+        _check(t, n)
+    if cu_seqlens_q.dtype != torch.int32 or cu_seqlens_k.dtype != torch.int32:
+        raise TypeError("cu_seqlens must be int32 CUDA tensors")
+    if cu_seqlens_q.numel() != cu_seqlens_k.numel() or cu_seqlens_q.numel() < 1:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must both hold B+1 entries")
+    B = cu_seqlens_q.numel() - 1
+    if out is None:
+        out = torch.empty_like(q)
+    _check(out, "out")
+    lse_ptr = 0
+    if lse is not None and lse is not False:
+        lse = _lse_tensor(lse, (Hq, total_q), q)
+        lse_ptr = lse.data_ptr()
+    st = fa_prefill_varlen_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse_ptr,
+                               cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(), B, Hq, Hkv,
+                               total_q, total_k, int(max_seqlen_q), D, float(scale),
+                               int(bool(causal)), _dtype_code(q), _stream_handle(stream))
+    if st != FA_OK:
+        raise FAError(st, "fa_prefill_varlen_fwd")
+    return (out, lse) if lse_ptr else out
 
 
 def decode(q, kcache, vcache, valid_len, scale, out=None, stream=None, lse=None):

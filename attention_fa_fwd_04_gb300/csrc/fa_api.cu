@@ -115,6 +115,34 @@ extern "C" int fa_prefill_fwd_lse(const void* q, const void* k, const void* v, v
                       stream);
 }
 
+extern "C" int fa_prefill_varlen_fwd(const void* q, const void* k, const void* v, void* o,
+                                     float* lse, const int32_t* cu_seqlens_q,
+                                     const int32_t* cu_seqlens_k, int B, int Hq, int Hkv,
+                                     int total_q, int total_k, int max_seqlen_q, int D,
+                                     float scale, int causal, int dtype, cudaStream_t stream) {
+  if (B < 0 || Hq < 0 || Hkv < 0 || total_q < 0 || total_k < 0 || max_seqlen_q < 0)
+    return FA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return FA_ERR_INVALID_ARG;
+  if (dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_INVALID_ARG;
+  if (!isfinite(scale)) return FA_ERR_INVALID_ARG;
+  if (B == 0 || Hq == 0 || total_q == 0) return FA_OK;  // no query row: nothing to write
+  if (Hkv == 0 || Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
+  if (max_seqlen_q > total_q) return FA_ERR_INVALID_ARG;
+  if (!q || !o || !aligned16(q) || !aligned16(o)) return FA_ERR_INVALID_ARG;
+  if (lse && !aligned4(lse)) return FA_ERR_INVALID_ARG;
+  if (!cu_seqlens_q || !cu_seqlens_k || !aligned4(cu_seqlens_q) || !aligned4(cu_seqlens_k))
+    return FA_ERR_INVALID_ARG;
+  if (total_k > 0 && (!k || !v || !aligned16(k) || !aligned16(v))) return FA_ERR_INVALID_ARG;
+  const int64_t items = (int64_t)B * Hq * ((max_seqlen_q + 255) / 256);
+  if (items > INT32_MAX) return FA_ERR_INVALID_ARG;
+  if ((int64_t)total_q * Hq * D * 2 >= (1ll << 40) || (int64_t)total_k * Hkv * D * 2 >= (1ll << 40))
+    return FA_ERR_INVALID_ARG;
+  return cuda_status(fa::launch_prefill_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, B, Hq,
+                                               Hkv, total_q, total_k, max_seqlen_q, D, scale,
+                                               causal, dtype == FA_BF16, stream),
+                     "prefill varlen launch");
+}
+
 static int decode_impl(const void* q, const void* kcache, const void* vcache,
                        const int32_t* valid_len_dev, void* o, float* lse, bool want_lse, int B,
                        int Hq, int Hkv, int cap, int D, float scale, cudaStream_t stream) {

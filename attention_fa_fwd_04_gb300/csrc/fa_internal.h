@@ -23,6 +23,14 @@ int launch_prefill(const void* q, const void* k, const void* v, void* o, float* 
                    int Hq, int Hkv, int Sq, int Sk, int D, float scale, int causal, bool bf16,
                    cudaStream_t stream);
 
+// Enqueue the prefill kernel over packed sequences: q/o [total_q, Hq, D],
+// k/v [total_k, Hkv, D], cu_q / cu_k device prefix sums [B + 1], lse
+// ([Hq, total_q] fp32) may be null.  Returns a cudaError_t.
+int launch_prefill_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                          const int32_t* cu_q, const int32_t* cu_k, int B, int Hq, int Hkv,
+                          int total_q, int total_k, int max_seqlen_q, int D, float scale,
+                          int causal, bool bf16, cudaStream_t stream);
+
 // Enqueue split + combine decode kernels with the given fp32 scratch
 // (partials); lse ([B, Hq] fp32) may be null.  scratch_floats is the scratch
 // size in floats.  Returns a cudaError_t.

@@ -70,11 +70,53 @@ struct Cfg {
 }  // namespace pf
 
 struct PrefillParams {
-  void* o;     // [B, Sq, Hq, D]
-  float* lse;  // [B, Hq, Sq] natural-log log-sum-exp per row, or null
+  void* o;     // [B, Sq, Hq, D]; packed sequences: [total_q, Hq, D]
+  float* lse;  // [B, Hq, Sq]; packed: [Hq, total_q]; natural-log log-sum-exp, or null
+  // Packed (variable-length) sequences: prefix sums of the sequence lengths,
+  // [B + 1] each, in device memory; null for a dense batch.  Sq is then the
+  // longest query length (it sizes the schedule) and Sk is unused.
+  const int32_t* cu_q;
+  const int32_t* cu_k;
+  int total_q, total_k;
   int B, Hq, Hkv, Sq, Sk, G, causal, n_qb, n_items;
   float c;  // scale * log2(e)
 };
+
+// Rows of one sequence of the batch.
+struct SeqSpan {
+  int q0, k0;   // first query / key row in the tensor maps' row coordinate
+  int tb;       // tensor-map batch coordinate
+  int Sq, Sk;   // its lengths
+  size_t orow;  // packed row index of its query row 0 (O is [rows, Hq, D])
+};
+
+// Every role calls this with the same arguments and so takes the same
+// decision.  Packed offsets that are not 0 <= cu[b] <= cu[b+1] <= total, or a
+// query length beyond the schedule's n_qb * 256 rows, make the sequence empty
+// and set the bounds bit of the error word.
+__device__ __forceinline__ SeqSpan seq_span(const PrefillParams& p, int b, unsigned int* err) {
+  SeqSpan s;
+  if (!p.cu_q) {
+    s.q0 = 0;
+    s.k0 = 0;
+    s.tb = b;
+    s.Sq = p.Sq;
+    s.Sk = p.Sk;
+    s.orow = (size_t)b * p.Sq;
+    return s;
+  }
+  const int q0 = p.cu_q[b], q1 = p.cu_q[b + 1], k0 = p.cu_k[b], k1 = p.cu_k[b + 1];
+  const bool ok = 0 <= q0 && q0 <= q1 && q1 <= p.total_q && 0 <= k0 && k0 <= k1 &&
+                  k1 <= p.total_k && q1 - q0 <= p.n_qb * 256;
+  if (!ok && err) atomicOr(err, kErrBounds);
+  s.q0 = ok ? q0 : 0;
+  s.k0 = ok ? k0 : 0;
+  s.tb = 0;
+  s.Sq = ok ? q1 - q0 : 0;
+  s.Sk = ok ? k1 - k0 : 0;
+  s.orow = (size_t)s.q0;
+  return s;
+}
 
 // Work item w -> (b, hq, qb): kv-head-major, then batch, then query blocks in
 // decreasing order (longest causal rows first), then the query heads of the
@@ -192,8 +234,6 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
-  const int off = p.Sk - p.Sq;  // bottom-right causal offset
-
   // The producer and MMA warps run their loops with all 32 lanes converged:
   // every lane waits on the barriers, lane 0 alone issues TMA / MMA / commit,
   // and __syncwarp() follows each issue.  (A warp must never reach the
@@ -218,9 +258,10 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       int b, hq, qb;
       prefill_item(w, p.B, p.Hq, p.Hkv, p.n_qb, &b, &hq, &qb);
       const int hkv = hq / p.G;
+      const SeqSpan sq = seq_span(p, b, nullptr);
       const int row0 = qb * pf::QBLOCK;
-      const int n0 = kv_tiles_for(row0, p.Sq, p.Sk, p.causal);
-      const int n1 = kv_tiles_for(row0 + pf::BM, p.Sq, p.Sk, p.causal);
+      const int n0 = kv_tiles_for(row0, sq.Sq, sq.Sk, p.causal);
+      const int n1 = kv_tiles_for(row0 + pf::BM, sq.Sq, sq.Sk, p.causal);
       const int n = n0 > n1 ? n0 : n1;
       q_issued = false;
       if (local > 0 && !(ok = mbar_wait(q_empty, (local - 1) & 1, abort_flag, &g_prefill_err, 1)))
@@ -232,7 +273,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
 #pragma unroll
           for (int h = 0; h < C::HALVES; ++h)
             tma_load_4d_hint(sQ + i * C::TILE_BYTES + h * pf::HALF_BYTES, &tmQ, q_full, h * 64,
-                             hq, row0 + i * pf::BM, b, pol_q);
+                             hq, sq.q0 + row0 + i * pf::BM, sq.tb, pol_q);
       }
       __syncwarp();
       q_issued = true;
@@ -248,7 +289,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
 #pragma unroll
             for (int h = 0; h < C::HALVES; ++h)
               tma_load_4d_hint(sKV + s * C::TILE_BYTES + h * pf::HALF_BYTES, m, &full[s], h * 64,
-                               hkv, j * pf::BN, b, pol_kv);
+                               hkv, sq.k0 + j * pf::BN, sq.tb, pol_kv);
           }
           __syncwarp();
           ++kv_cnt;
@@ -313,9 +354,10 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
     for (int w = blockIdx.x; w < p.n_items && ok; w += gridDim.x, ++local) {
       int b, hq, qb;
       prefill_item(w, p.B, p.Hq, p.Hkv, p.n_qb, &b, &hq, &qb);
+      const SeqSpan sq = seq_span(p, b, nullptr);
       const int row0 = qb * pf::QBLOCK;
-      const int nt0 = kv_tiles_for(row0, p.Sq, p.Sk, p.causal);
-      const int nt1 = kv_tiles_for(row0 + pf::BM, p.Sq, p.Sk, p.causal);
+      const int nt0 = kv_tiles_for(row0, sq.Sq, sq.Sk, p.causal);
+      const int nt1 = kv_tiles_for(row0 + pf::BM, sq.Sq, sq.Sk, p.causal);
       const int n = nt0 > nt1 ? nt0 : nt1;
       if (!(ok = mbar_wait(q_full, local & 1, abort_flag, &g_prefill_err, 3))) break;
       tc_fence_after();
@@ -405,16 +447,26 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
     for (int w = blockIdx.x; w < p.n_items && ok; w += gridDim.x) {
       int b, hq, qb;
       prefill_item(w, p.B, p.Hq, p.Hkv, p.n_qb, &b, &hq, &qb);
+      // (the bounds bit for bad packed offsets is set by one thread per item)
+      const SeqSpan sq = seq_span(p, b, (i == 0 && r == 0) ? &g_prefill_err : nullptr);
+      const int Sq = sq.Sq, Sk = sq.Sk, off = Sk - Sq;  // bottom-right causal offset
       const int row0 = qb * pf::QBLOCK + i * pf::BM;
       const int grow = row0 + r;
-      const int n_i = kv_tiles_for(row0, p.Sq, p.Sk, p.causal);
-      T* const orow = O + ((size_t)b * p.Sq + grow) * (size_t)p.Hq * D + (size_t)hq * D;
+      const int n_i = kv_tiles_for(row0, Sq, Sk, p.causal);
+      T* const orow = O + (sq.orow + grow) * (size_t)p.Hq * D + (size_t)hq * D;
+      float* const lse_row =
+          p.lse ? p.lse + (p.cu_q ? (size_t)hq * p.total_q + sq.orow + grow
+                                  : ((size_t)b * p.Hq + hq) * p.Sq + grow)
+                : nullptr;
+      // Self-check: the row must lie inside O (records and skips otherwise).
+      const bool row_ok = grow < Sq && b < p.B && hq < p.Hq &&
+                          (!p.cu_q || sq.orow + grow < (size_t)p.total_q);
       if (n_i == 0) {
-        if (grow < p.Sq && b < p.B && hq < p.Hq) {
+        if (row_ok) {
 #pragma unroll
           for (int x = 0; x < D / 8; ++x)
             reinterpret_cast<uint4*>(orow)[x] = make_uint4(0u, 0u, 0u, 0u);
-          if (p.lse) p.lse[((size_t)b * p.Hq + hq) * p.Sq + grow] = NEG_INF;
+          if (lse_row) *lse_row = NEG_INF;
         }
         continue;
       }
@@ -427,11 +479,11 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
         tc_fence_after();
         const int kv0 = j * pf::BN;
         const bool need_mask =
-            (kv0 + pf::BN > p.Sk) || (p.causal && kv0 + pf::BN - 1 > row0 + off);
+            (kv0 + pf::BN > Sk) || (p.causal && kv0 + pf::BN - 1 > row0 + off);
         int lim = pf::BN;  // keys [0, lim) of this tile are visible to this row
         if (need_mask) {
-          const int lim_c = p.causal ? grow + off + 1 : p.Sk;
-          lim = (lim_c < p.Sk ? lim_c : p.Sk) - kv0;
+          const int lim_c = p.causal ? grow + off + 1 : Sk;
+          lim = (lim_c < Sk ? lim_c : Sk) - kv0;
         }
         // Raw-domain fill for hidden keys: becomes -inf once multiplied by c.
         const float hide = neg_scale ? -NEG_INF : NEG_INF;
@@ -566,9 +618,8 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       const float inv = l > 0.f ? 1.f / l : 0.f;
       // log sum_j exp(s_j) = ln2 * (m_used + log2 l): m_used is the row max of
       // s * log2(e) the P values were taken against.
-      if (p.lse && grow < p.Sq && b < p.B && hq < p.Hq)
-        p.lse[((size_t)b * p.Hq + hq) * p.Sq + grow] =
-            l > 0.f ? 0.6931471805599453f * (m_used + __log2f(l)) : NEG_INF;
+      if (lse_row && row_ok)
+        *lse_row = l > 0.f ? 0.6931471805599453f * (m_used + __log2f(l)) : NEG_INF;
 #pragma unroll
       for (int q4 = 0; q4 < D / 32; ++q4) {
         uint32_t orr[32];
@@ -580,9 +631,8 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
         for (int x = 0; x < 16; ++x)
           pk[x] = Pack2<T>::pack(__uint_as_float(orr[2 * x]) * inv,
                                  __uint_as_float(orr[2 * x + 1]) * inv);
-        if (grow < p.Sq) {
-          // Self-check: the row must lie inside O (records and skips otherwise).
-          if (b >= p.B || hq >= p.Hq) {
+        if (grow < Sq) {
+          if (!row_ok) {
             atomicOr(&g_prefill_err, kErrBounds);
             continue;
           }
@@ -617,15 +667,32 @@ __global__ void prefill_zero_kernel(T* o, size_t n, float* lse, size_t nl) {
       lse[x] = -INFINITY;
 }
 
+// Dense batch: cu_q == nullptr, rows = Sq / Sk per sequence.  Packed
+// sequences: cu_q / cu_k device prefix sums, Sq = longest query length,
+// rows_q / rows_k = total packed rows.
+struct PrefillShape {
+  int B, Hq, Hkv, Sq, Sk;
+  const int32_t* cu_q;
+  const int32_t* cu_k;
+  int total_q, total_k;
+};
+
 template <int D, typename T>
 static int launch_prefill_t(const void* q, const void* k, const void* v, void* o, float* lse,
-                            int B, int Hq, int Hkv, int Sq, int Sk, float scale, int causal,
+                            const PrefillShape& sh, float scale, int causal,
                             cudaStream_t stream) {
   using C = pf::Cfg<D>;
+  const bool packed = sh.cu_q != nullptr;
   CUtensorMap tq, tk, tv;
-  if (encode_tmap_rows(&tq, q, D, Hq, Sq, B, pf::BM)) return cudaErrorInvalidValue;
-  if (encode_tmap_rows(&tk, k, D, Hkv, Sk, B, pf::BN)) return cudaErrorInvalidValue;
-  if (encode_tmap_rows(&tv, v, D, Hkv, Sk, B, pf::BN)) return cudaErrorInvalidValue;
+  if (packed) {
+    if (encode_tmap_rows(&tq, q, D, sh.Hq, sh.total_q, 1, pf::BM)) return cudaErrorInvalidValue;
+    if (encode_tmap_rows(&tk, k, D, sh.Hkv, sh.total_k, 1, pf::BN)) return cudaErrorInvalidValue;
+    if (encode_tmap_rows(&tv, v, D, sh.Hkv, sh.total_k, 1, pf::BN)) return cudaErrorInvalidValue;
+  } else {
+    if (encode_tmap_rows(&tq, q, D, sh.Hq, sh.Sq, sh.B, pf::BM)) return cudaErrorInvalidValue;
+    if (encode_tmap_rows(&tk, k, D, sh.Hkv, sh.Sk, sh.B, pf::BN)) return cudaErrorInvalidValue;
+    if (encode_tmap_rows(&tv, v, D, sh.Hkv, sh.Sk, sh.B, pf::BN)) return cudaErrorInvalidValue;
+  }
   static int attr_set[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -639,15 +706,19 @@ static int launch_prefill_t(const void* q, const void* k, const void* v, void* o
   PrefillParams p;
   p.o = o;
   p.lse = lse;
-  p.B = B;
-  p.Hq = Hq;
-  p.Hkv = Hkv;
-  p.Sq = Sq;
-  p.Sk = Sk;
-  p.G = Hq / Hkv;
+  p.cu_q = sh.cu_q;
+  p.cu_k = sh.cu_k;
+  p.total_q = sh.total_q;
+  p.total_k = sh.total_k;
+  p.B = sh.B;
+  p.Hq = sh.Hq;
+  p.Hkv = sh.Hkv;
+  p.Sq = sh.Sq;
+  p.Sk = sh.Sk;
+  p.G = sh.Hq / sh.Hkv;
   p.causal = causal ? 1 : 0;
-  p.n_qb = (Sq + pf::QBLOCK - 1) / pf::QBLOCK;
-  p.n_items = B * Hq * p.n_qb;
+  p.n_qb = (sh.Sq + pf::QBLOCK - 1) / pf::QBLOCK;
+  p.n_items = sh.B * sh.Hq * p.n_qb;
   p.c = scale * 1.4426950408889634f;
   // scale == 0: every visible score is 0.  A tiny positive c keeps that (all
   // exp2 arguments round to 0) while hidden keys still map to -inf, never NaN.
@@ -658,12 +729,15 @@ static int launch_prefill_t(const void* q, const void* k, const void* v, void* o
   return cudaGetLastError();
 }
 
-int launch_prefill(const void* q, const void* k, const void* v, void* o, float* lse, int B,
-                   int Hq, int Hkv, int Sq, int Sk, int D, float scale, int causal, bool bf16,
-                   cudaStream_t stream) {
-  if (B == 0 || Hq == 0 || Sq == 0) return cudaSuccess;
-  if (Sk == 0) {
-    const size_t n = (size_t)B * Sq * Hq * D, nl = (size_t)B * Hq * Sq;
+static int launch_prefill_shape(const void* q, const void* k, const void* v, void* o,
+                                float* lse, const PrefillShape& sh, int D, float scale,
+                                int causal, bool bf16, cudaStream_t stream) {
+  const bool packed = sh.cu_q != nullptr;
+  const int rows_q = packed ? sh.total_q : sh.B * sh.Sq;
+  if (sh.B == 0 || sh.Hq == 0 || rows_q == 0) return cudaSuccess;
+  if ((packed ? sh.total_k : sh.Sk) == 0) {
+    // No key anywhere: O = 0 and every log-sum-exp -inf.
+    const size_t n = (size_t)rows_q * sh.Hq * D, nl = (size_t)rows_q * sh.Hq;
     const unsigned blocks = (unsigned)((n + 255) / 256 < 8192 ? (n + 255) / 256 : 8192);
     if (bf16)
       prefill_zero_kernel<__nv_bfloat16><<<blocks, 256, 0, stream>>>(
@@ -674,14 +748,25 @@ int launch_prefill(const void* q, const void* k, const void* v, void* o, float* 
     return cudaGetLastError();
   }
   if (D == 64)
-    return bf16 ? launch_prefill_t<64, __nv_bfloat16>(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, scale,
-                                                       causal, stream)
-                : launch_prefill_t<64, __half>(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, scale,
-                                               causal, stream);
-  return bf16 ? launch_prefill_t<128, __nv_bfloat16>(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, scale,
-                                                      causal, stream)
-              : launch_prefill_t<128, __half>(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, scale, causal,
-                                              stream);
+    return bf16 ? launch_prefill_t<64, __nv_bfloat16>(q, k, v, o, lse, sh, scale, causal, stream)
+                : launch_prefill_t<64, __half>(q, k, v, o, lse, sh, scale, causal, stream);
+  return bf16 ? launch_prefill_t<128, __nv_bfloat16>(q, k, v, o, lse, sh, scale, causal, stream)
+              : launch_prefill_t<128, __half>(q, k, v, o, lse, sh, scale, causal, stream);
+}
+
+int launch_prefill(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                   int Hq, int Hkv, int Sq, int Sk, int D, float scale, int causal, bool bf16,
+                   cudaStream_t stream) {
+  const PrefillShape sh{B, Hq, Hkv, Sq, Sk, nullptr, nullptr, 0, 0};
+  return launch_prefill_shape(q, k, v, o, lse, sh, D, scale, causal, bf16, stream);
+}
+
+int launch_prefill_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                          const int32_t* cu_q, const int32_t* cu_k, int B, int Hq, int Hkv,
+                          int total_q, int total_k, int max_seqlen_q, int D, float scale,
+                          int causal, bool bf16, cudaStream_t stream) {
+  const PrefillShape sh{B, Hq, Hkv, max_seqlen_q, 0, cu_q, cu_k, total_q, total_k};
+  return launch_prefill_shape(q, k, v, o, lse, sh, D, scale, causal, bf16, stream);
 }
 
 int read_prefill_error(unsigned int* out, int reset) {

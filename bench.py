@@ -280,6 +280,7 @@ def run_ours(args, rank, world, local_rank):
 
     # ---------------- end to end through the C ABI with host buffers ----------------
     e2e = run_e2e(args, fa, torch, dev, q_h, k_h, v_h, sh, stream, dist)
+    varlen = run_varlen(args, fa, torch, dev, sh, stream)
 
     if rank != 0:
         if dist:
@@ -376,9 +377,11 @@ def run_ours(args, rank, world, local_rank):
             "kernels": ["fa::decode_split_kernel<128>", "fa::decode_combine_kernel<128>"],
         },
         "e2e": e2e,
+        "varlen": varlen,
         "gpu_launches": (5 + 2 * (n_r1 + n_r2)) * K,
         "gpu_launches_note": f"per step: 1 prefill + {2 + n_r1 + n_r2} decode calls x "
-                             "(split + combine)",
+                             "(split + combine); the varlen and e2e runs follow the timed "
+                             "region",
         "clocks": clk,
         "wall_s_timed": round(wall, 3),
     }
@@ -387,6 +390,45 @@ def run_ours(args, rank, world, local_rank):
     if dist:
         dist.destroy_process_group()
     return out
+
+
+def run_varlen(args, fa, torch, dev, sh, stream):
+    """Packed variable-length causal prefill: 16 seeded sequence lengths in
+    [1, 4096] at the headline's heads (Hq 128 / Hkv 8, D 128, bf16), one launch
+    of fa_prefill_varlen_fwd per timed iteration (inputs larger than L2)."""
+    lens = fa_inputs.varlen_lengths()
+    Hq, Hkv, D = PREFILL.Hq, PREFILL.Hkv, PREFILL.D
+    q_h, k_h, v_h, cq, ck = fa_inputs.varlen_inputs(lens, lens, Hq, Hkv, D, seed=0)
+    q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
+    cqd, ckd = cq.to(dev), ck.to(dev)
+    o = torch.empty_like(q)
+    tq, tk, mx = q.shape[0], k.shape[0], max(lens)
+
+    def launch():
+        st = fa.fa_prefill_varlen_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), 0,
+                                      cqd.data_ptr(), ckd.data_ptr(), len(lens), Hq, Hkv, tq, tk,
+                                      mx, D, PREFILL.scale, 1, fa.FA_BF16, sh)
+        if st:
+            raise fa.FAError(st, "fa_prefill_varlen_fwd")
+    for _ in range(3):
+        launch()
+    n = max(3, min(args.steps, 20))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(n):
+        launch()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    st, detail = fa.fa_device_error()
+    if st != fa.FA_OK:
+        raise RuntimeError(f"device error word {detail:#x} in the varlen run")
+    t = e0.elapsed_time(e1) / 1e3 / n
+    flops = sum(2.0 * Hq * x * x * D for x in lens)
+    return {"value": round(flops / t / 1e12, 2), "unit": "TFLOP/s", "ms": round(t * 1e3, 4),
+            "workload": f"packed causal prefill, {len(lens)} sequences, lengths {lens} "
+                        f"({tq} tokens), Hq{Hq}/Hkv{Hkv} D{D} bf16",
+            "flop_convention": "sum_b 2*Hq*Sq_b*Sk_b*D (causal)", "launches": n}
 
 
 def run_e2e(args, fa, torch, dev, q_h, k_h, v_h, sh, stream, dist):

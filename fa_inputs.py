@@ -8,6 +8,7 @@ Recipe: ``torch.Generator().manual_seed(seed)``; every tensor is drawn as
 float32 ``randn`` (i.i.d. N(0, 1)) and rounded to the storage dtype.  The
 draw order is fixed (decode: L, q, k-cache, v-cache; prefill: q, k, v).
 """
+import itertools
 import math
 from dataclasses import dataclass, field
 
@@ -86,6 +87,25 @@ def draw_valid_length(cap: int, seed=0) -> int:
     """The seeded valid length in [1, cap] (the first draw of the decode recipe)."""
     g = torch.Generator().manual_seed(seed)
     return 1 + int(torch.randint(0, cap, (1,), generator=g).item())
+
+
+def varlen_lengths(n=16, max_len=4096, seed=0):
+    """Seeded sequence lengths in [1, max_len] for a packed (varlen) batch."""
+    g = torch.Generator().manual_seed(seed)
+    return [1 + int(x) for x in torch.randint(0, max_len, (n,), generator=g).tolist()]
+
+
+def varlen_inputs(lens_q, lens_k, Hq, Hkv, D, dtype=torch.bfloat16, seed=0):
+    """Packed q [sum lens_q, Hq, D], k/v [sum lens_k, Hkv, D] (seeded N(0,1) in
+    dtype) and the int32 prefix sums cu_q, cu_k ([B+1], host tensors)."""
+    g = torch.Generator().manual_seed(seed)
+    tq, tk = sum(lens_q), sum(lens_k)
+    q = _randn(g, (tq, Hq, D), dtype)
+    k = _randn(g, (tk, Hkv, D), dtype)
+    v = _randn(g, (tk, Hkv, D), dtype)
+    cu_q = torch.tensor([0] + list(itertools.accumulate(lens_q)), dtype=torch.int32)
+    cu_k = torch.tensor([0] + list(itertools.accumulate(lens_k)), dtype=torch.int32)
+    return q, k, v, cu_q, cu_k
 
 
 def decode_inputs(B, Hq, Hkv, cap, D, dtype=torch.bfloat16, seed=0, L=None,

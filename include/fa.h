@@ -112,6 +112,32 @@ int fa_prefill_fwd_lse(const void* q, const void* k, const void* v, void* o, flo
                        float scale, int causal, int dtype, cudaStream_t stream);
 
 /*
+ * fa_prefill_varlen_fwd -- fa_prefill_fwd over a batch of packed sequences of
+ * different lengths (the gfx950 prefill README's TODO list names this
+ * follow-up: packed varlen with per-sequence persistent scheduling).
+ *
+ *   q, o           [total_q, Hq, D]   sequences packed back to back
+ *   k, v           [total_k, Hkv, D]
+ *   cu_seqlens_q   [B + 1] int32 in device memory: sequence b's query rows are
+ *   cu_seqlens_k   [cu_seqlens_q[b], cu_seqlens_q[b+1]), its keys likewise.
+ *                  Read by the kernel only.
+ *   max_seqlen_q   >= every query length (sizes the persistent schedule)
+ *   lse            NULL, or [Hq, total_q] fp32 written with each row's
+ *                  log-sum-exp (-inf for a row with no visible key)
+ *
+ * Causal masking is bottom-right per sequence: row i of sequence b sees keys
+ * j <= i + (Sk_b - Sq_b).  Keys of the neighbouring packed sequence that share
+ * a tile are masked like keys past Sk.  Offsets that are not
+ * 0 <= cu[b] <= cu[b+1] <= total, or a query length above max_seqlen_q, make
+ * that sequence's rows unwritten and set the bounds bit reported by
+ * fa_device_error().  Other rules as fa_prefill_fwd.
+ */
+int fa_prefill_varlen_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                          const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                          int B, int Hq, int Hkv, int total_q, int total_k, int max_seqlen_q,
+                          int D, float scale, int causal, int dtype, cudaStream_t stream);
+
+/*
  * fa_decode_fwd -- one new query token per sequence against a KV cache.
  *
  *   q              [B, 1, Hq, D]      bf16, read only

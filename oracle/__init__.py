@@ -110,6 +110,30 @@ def attention(q, k, v, scale: float, causal: bool, rows=None, nthreads=None,
     return (out, lse) if return_lse else out
 
 
+def attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, scale: float, causal: bool,
+                     return_lse=False, nthreads=None):
+    """Packed sequences: q [total_q,Hq,D], k/v [total_k,Hkv,D], cu_seqlens_* host
+    sequences of B+1 prefix sums.  Sequence b is the dense problem on rows
+    [cu_q[b], cu_q[b+1]) and keys [cu_k[b], cu_k[b+1]) (bottom-right causal
+    within it), computed by the dense oracle above.  Returns float64
+    [total_q,Hq,D] (and lse [Hq,total_q] when return_lse)."""
+    cq = [int(x) for x in cu_seqlens_q]
+    ck = [int(x) for x in cu_seqlens_k]
+    total_q, Hq, D = q.shape
+    out = np.zeros((total_q, Hq, D), dtype=np.float64)
+    lse = np.full((Hq, total_q), -np.inf, dtype=np.float64)
+    for b in range(len(cq) - 1):
+        q0, q1, k0, k1 = cq[b], cq[b + 1], ck[b], ck[b + 1]
+        if q1 == q0:
+            continue
+        o_b, l_b = attention(q[q0:q1].unsqueeze(0), k[k0:k1].unsqueeze(0),
+                             v[k0:k1].unsqueeze(0), scale, causal, nthreads=nthreads,
+                             return_lse=True)
+        out[q0:q1] = o_b[0]
+        lse[:, q0:q1] = l_b[0]
+    return (out, lse) if return_lse else out
+
+
 def probs(q, k, v, scale: float, causal: bool, b: int, h: int, i: int):
     """(p [Sk], o [D]) of one query row: p over all Sk keys, 0 where masked."""
     lib = _load()

@@ -458,7 +458,46 @@ def test_decode_lse_equals_prefill_lse_and_ignores_nan_tail():
 
 
 # ---------------------------------------------------------------------------
-# 11. Stored oracle values (tests/golden/oracle_tiny.txt, written by
+# 11. Packed (variable-length) sequences: each sequence is its own dense
+#     problem; a packed batch of equal lengths is the dense batch.
+# ---------------------------------------------------------------------------
+def test_varlen_equal_lengths_equal_dense_batch():
+    B, Hq, Hkv, Sq, Sk, D = 3, 4, 2, 9, 13, 8
+    q, k, v = fa_inputs.prefill_inputs(B, Hq, Hkv, Sq, Sk, D, torch.bfloat16, seed=21)
+    cq = [b * Sq for b in range(B + 1)]
+    ck = [b * Sk for b in range(B + 1)]
+    for causal in (True, False):
+        o_d, l_d = oracle.attention(q, k, v, 0.3, causal, return_lse=True)
+        o_v, l_v = oracle.attention_varlen(q.reshape(B * Sq, Hq, D), k.reshape(B * Sk, Hkv, D),
+                                           v.reshape(B * Sk, Hkv, D), cq, ck, 0.3, causal,
+                                           return_lse=True)
+        np.testing.assert_array_equal(o_v, o_d.reshape(B * Sq, Hq, D))
+        np.testing.assert_array_equal(l_v, l_d.transpose(1, 0, 2).reshape(Hq, B * Sq))
+
+
+def test_varlen_sequences_are_independent_and_empty_ones_write_nothing():
+    """Changing one sequence's keys leaves the other sequences' rows unchanged;
+    a sequence without keys gives O = 0 and lse = -inf; one without queries
+    owns no rows."""
+    lens_q, lens_k = [5, 0, 7, 3], [6, 4, 0, 9]
+    cq = np.concatenate([[0], np.cumsum(lens_q)])
+    ck = np.concatenate([[0], np.cumsum(lens_k)])
+    g = torch.Generator().manual_seed(22)
+    q = torch.randn(int(cq[-1]), 4, 8, generator=g).to(torch.bfloat16)
+    k = torch.randn(int(ck[-1]), 2, 8, generator=g).to(torch.bfloat16)
+    v = torch.randn(int(ck[-1]), 2, 8, generator=g).to(torch.bfloat16)
+    o, l = oracle.attention_varlen(q, k, v, cq, ck, 0.4, True, return_lse=True)
+    assert np.array_equal(o[5:12], np.zeros((7, 4, 8)))       # sequence 2 has no keys
+    assert np.all(np.isneginf(l[:, 5:12]))
+    k2 = k.clone()
+    k2[10:19] += 1.0                                          # sequence 3's keys only
+    o2 = oracle.attention_varlen(q, k2, v, cq, ck, 0.4, True)
+    assert np.array_equal(o2[:12], o[:12])
+    assert np.max(np.abs(o2[12:] - o[12:])) > 1e-6
+
+
+# ---------------------------------------------------------------------------
+# 12. Stored oracle values (tests/golden/oracle_tiny.txt, written by
 #     tests/golden/make_golden.py from the oracle alone): drift guard.
 # ---------------------------------------------------------------------------
 def test_golden_oracle_values_unchanged():

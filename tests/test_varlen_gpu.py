@@ -1,0 +1,108 @@
+"""Packed variable-length prefill on the GPU (fa_prefill_varlen_fwd) against
+the fp64 oracle applied sequence by sequence ("Dense flash-attention prefill
+(gfx950 / MI355X)", TODO list: packed varlen with per-sequence scheduling).
+
+Sequences of different query and key lengths share one launch; causal masking
+is bottom-right within each sequence; lengths straddle the 128-row tiles and
+256-row work units, include 0 and 1, and keys of the next packed sequence
+share tiles with the current one."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests.parity import compare
+from tests.test_lse_gpu import lse_compare
+
+pytestmark = pytest.mark.gpu
+
+
+def packed_inputs(lens_q, lens_k, Hq, Hkv, D, dtype, seed):
+    g = torch.Generator().manual_seed(seed)
+    tq, tk = sum(lens_q), sum(lens_k)
+    q = torch.randn(tq, Hq, D, generator=g).to(dtype)
+    k = torch.randn(tk, Hkv, D, generator=g).to(dtype)
+    v = torch.randn(tk, Hkv, D, generator=g).to(dtype)
+    cq = np.concatenate([[0], np.cumsum(lens_q)]).astype(np.int32)
+    ck = np.concatenate([[0], np.cumsum(lens_k)]).astype(np.int32)
+    return q, k, v, cq, ck
+
+
+def run_varlen(fa, q, k, v, cq, ck, scale, causal, lse=True, max_sq=None):
+    dev = torch.device("cuda", 0)
+    cqd = torch.from_numpy(cq).to(dev)
+    ckd = torch.from_numpy(ck).to(dev)
+    max_sq = int(np.max(np.diff(cq))) if max_sq is None else max_sq
+    out, l = fa.prefill_varlen(q.to(dev), k.to(dev), v.to(dev), cqd, ckd, max_sq, scale, causal,
+                               lse=lse)
+    torch.cuda.synchronize()
+    st, detail = fa.fa_device_error()
+    assert st == fa.FA_OK, f"device error word {detail:#x}"
+    return out.float().cpu().numpy(), l.cpu().numpy()
+
+
+CASES = [
+    # lens_q, lens_k, Hq, Hkv, D, causal, dtype
+    ([1, 100, 257, 0, 1000], [1, 300, 257, 50, 999], 8, 2, 128, True, torch.bfloat16),
+    ([128, 129, 255, 256, 513], [128, 129, 255, 256, 513], 4, 4, 64, True, torch.float16),
+    ([77, 384, 5], [700, 130, 64], 8, 1, 128, False, torch.bfloat16),
+    ([600, 33], [0, 640], 4, 2, 64, True, torch.bfloat16),      # a sequence with no keys
+]
+
+
+@pytest.mark.parametrize("lens_q,lens_k,Hq,Hkv,D,causal,dt", CASES)
+def test_varlen_against_oracle(fa, lens_q, lens_k, Hq, Hkv, D, causal, dt):
+    q, k, v, cq, ck = packed_inputs(lens_q, lens_k, Hq, Hkv, D, dt, seed=sum(lens_q))
+    scale = 1 / math.sqrt(D)
+    o, l = run_varlen(fa, q, k, v, cq, ck, scale, causal)
+    ref, ref_l = oracle.attention_varlen(q, k, v, cq, ck, scale, causal, return_lse=True)
+    compare(o, ref)
+    lse_compare(l, ref_l)
+
+
+def test_varlen_equal_lengths_match_dense_bit_exactly(fa):
+    """Equal lengths: the packed launch runs the same tiles as the dense one."""
+    B, Hq, Hkv, S, D = 3, 8, 2, 700, 128
+    g = torch.Generator().manual_seed(5)
+    q = torch.randn(B, S, Hq, D, generator=g).to(torch.bfloat16)
+    k = torch.randn(B, S, Hkv, D, generator=g).to(torch.bfloat16)
+    v = torch.randn(B, S, Hkv, D, generator=g).to(torch.bfloat16)
+    dev = torch.device("cuda", 0)
+    dense, dl = fa.prefill(q.to(dev), k.to(dev), v.to(dev), 0.088, True, lse=True)
+    cq = np.arange(B + 1, dtype=np.int32) * S
+    o, l = run_varlen(fa, q.reshape(B * S, Hq, D), k.reshape(B * S, Hkv, D),
+                      v.reshape(B * S, Hkv, D), cq, cq, 0.088, True)
+    assert np.array_equal(o, dense.float().cpu().numpy().reshape(B * S, Hq, D))
+    assert np.array_equal(l, dl.cpu().numpy().transpose(1, 0, 2).reshape(Hq, B * S))
+
+
+def test_varlen_without_lse_and_empty_batch(fa):
+    q, k, v, cq, ck = packed_inputs([40, 90], [40, 90], 4, 2, 64, torch.bfloat16, seed=9)
+    dev = torch.device("cuda", 0)
+    out = fa.prefill_varlen(q.to(dev), k.to(dev), v.to(dev), torch.from_numpy(cq).to(dev),
+                            torch.from_numpy(ck).to(dev), 90, 0.125, True)
+    torch.cuda.synchronize()
+    compare(out.float().cpu().numpy(), oracle.attention_varlen(q, k, v, cq, ck, 0.125, True))
+    # B = 0 and total_q = 0 are valid no-ops
+    assert fa.fa_prefill_varlen_fwd(0, 0, 0, 0, 0, 0, 0, 0, 4, 2, 0, 0, 0, 64, 0.1, 1,
+                                    fa.FA_BF16, 0) == fa.FA_OK
+
+
+def test_varlen_offsets_past_the_tensor_are_reported(fa):
+    """cu_seqlens beyond total rows: the sequence is skipped (no access outside
+    q/k/v/o) and the bounds bit of the device error word is set; the valid
+    sequence is still computed."""
+    q, k, v, cq, ck = packed_inputs([50, 60], [50, 60], 4, 2, 64, torch.bfloat16, seed=10)
+    bad_q = cq.copy()
+    bad_q[2] = cq[2] + 1000          # sequence 1 claims rows past total_q
+    dev = torch.device("cuda", 0)
+    out = torch.zeros(q.shape, dtype=q.dtype, device=dev)
+    fa.prefill_varlen(q.to(dev), k.to(dev), v.to(dev), torch.from_numpy(bad_q).to(dev),
+                      torch.from_numpy(ck).to(dev), 60, 0.125, True, out=out)
+    torch.cuda.synchronize()
+    st, detail = fa.fa_device_error()
+    assert st != fa.FA_OK and (detail & 2)
+    ref = oracle.attention_varlen(q[:50], k[:50], v[:50], [0, 50], [0, 50], 0.125, True)
+    compare(out[:50].float().cpu().numpy(), ref)
