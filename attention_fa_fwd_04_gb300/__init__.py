@@ -7,6 +7,7 @@ no fallback: if the library is missing or cannot be loaded, every call raises.
 Raw entry points (same names and argument order as the C ABI; pointers are
 integers, ``stream`` a ``cudaStream_t`` value):
     fa_prefill_fwd, fa_prefill_fwd_lse, fa_prefill_varlen_fwd, fa_decode_fwd, fa_decode_fwd_lse,
+    fa_decode_paged_fwd,
     fa_decode_fwd_noalloc, fa_status_string, fa_device_error, fa_last_cuda_error,
     fa_num_sms, fa_prefill_work_item
 Tensor conveniences (contiguous CUDA tensors, caller-owned outputs):
@@ -14,6 +15,8 @@ Tensor conveniences (contiguous CUDA tensors, caller-owned outputs):
     prefill_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, scale, causal,
                    out=None, stream=None, lse=None)
     decode(q, kcache, vcache, valid_len, scale, out=None, stream=None, lse=None)
+    decode_paged(q, kpages, vpages, page_table, seqlens, scale, out=None, stream=None,
+                 lse=None)
     (lse=True allocates the fp32 log-sum-exp output; a tensor is used as is.)
 """
 import ctypes
@@ -25,10 +28,11 @@ LIB_PATH = os.path.join(HERE, "libfa_gb300.so")
 FA_BF16, FA_FP16 = 0, 1
 FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = 0, 1, 2, 3, 4
 FA_ERR_TOO_LARGE = 5
+FA_ERR_BOUNDS = 6
 
 # Every symbol include/fa.h declares (checked by the tests against the header).
 EXPORTS = ("fa_prefill_fwd", "fa_prefill_fwd_lse", "fa_prefill_varlen_fwd", "fa_decode_fwd",
-           "fa_decode_fwd_lse",
+           "fa_decode_fwd_lse", "fa_decode_paged_fwd",
            "fa_decode_fwd_noalloc", "fa_status_string", "fa_device_error", "fa_last_cuda_error",
            "fa_num_sms", "fa_prefill_work_item")
 
@@ -68,6 +72,9 @@ def load(path: str = LIB_PATH):
     lib.fa_decode_fwd.restype = i32
     lib.fa_decode_fwd_lse.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp]
     lib.fa_decode_fwd_lse.restype = i32
+    lib.fa_decode_paged_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
+                                        i32, f32, vp]
+    lib.fa_decode_paged_fwd.restype = i32
     lib.fa_decode_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp]
     lib.fa_decode_fwd_noalloc.restype = i32
     lib.fa_status_string.argtypes = [i32]
@@ -107,6 +114,12 @@ def fa_prefill_varlen_fwd(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, B, Hq, Hk
 def fa_decode_fwd(q, kcache, vcache, valid_len_dev, o, B, Hq, Hkv, cap, D, scale, stream):
     return load().fa_decode_fwd(q, kcache, vcache, valid_len_dev, o, B, Hq, Hkv, cap, D, scale,
                                 stream)
+
+
+def fa_decode_paged_fwd(q, kpages, vpages, page_table, seqlens, o, lse, B, Hq, Hkv, num_pages,
+                        page_size, max_pages, D, scale, stream):
+    return load().fa_decode_paged_fwd(q, kpages, vpages, page_table, seqlens, o, lse, B, Hq, Hkv,
+                                      num_pages, page_size, max_pages, D, scale, stream)
 
 
 def fa_decode_fwd_lse(q, kcache, vcache, valid_len_dev, o, lse, B, Hq, Hkv, cap, D, scale,
@@ -307,3 +320,42 @@ def decode(q, kcache, vcache, valid_len, scale, out=None, stream=None, lse=None)
     if st != FA_OK:
         raise FAError(st, "fa_decode_fwd")
     return out
+
+
+def decode_paged(q, kpages, vpages, page_table, seqlens, scale, out=None, stream=None, lse=None):
+    """Single-token decode of B sequences over a paged cache.
+
+    q [B,1,Hq,D] (or [B,Hq,D]) bf16; kpages/vpages [num_pages,page_size,Hkv,D]
+    bf16; page_table int32 CUDA [B,max_pages]; seqlens int32 CUDA [B].  Returns
+    ``out`` shaped like q, or (out, lse) with lse [B,Hq] fp32 when lse is True
+    or a tensor.
+    """
+    import torch
+    num_pages, page_size, Hkv, D = kpages.shape
+    B, max_pages = page_table.shape
+    Hq = q.shape[-2]
+    if q.shape[0] != B or q.shape[-1] != D or q.numel() != B * Hq * D:
+        raise ValueError("q must be [B,1,Hq,D] matching the page table and pages")
+    if tuple(vpages.shape) != tuple(kpages.shape):
+        raise ValueError("kpages and vpages shapes differ")
+    for t, n in ((q, "q"), (kpages, "kpages"), (vpages, "vpages"), (page_table, "page_table"),
+                 (seqlens, "seqlens")):
+        _check(t, n)
+    if page_table.dtype != torch.int32 or seqlens.dtype != torch.int32 or seqlens.numel() != B:
+        raise TypeError("page_table and seqlens must be int32 CUDA tensors ([B,max_pages], [B])")
+    if q.dtype != torch.bfloat16 or kpages.dtype != torch.bfloat16 or vpages.dtype != torch.bfloat16:
+        raise TypeError("decode takes bf16 q and pages")
+    if out is None:
+        out = torch.empty_like(q)
+    _check(out, "out")
+    lse_ptr = 0
+    if lse is not None and lse is not False:
+        lse = _lse_tensor(lse, (B, Hq), q)
+        lse_ptr = lse.data_ptr()
+    st = fa_decode_paged_fwd(q.data_ptr(), kpages.data_ptr(), vpages.data_ptr(),
+                             page_table.data_ptr(), seqlens.data_ptr(), out.data_ptr(), lse_ptr,
+                             B, Hq, Hkv, num_pages, page_size, max_pages, D, float(scale),
+                             _stream_handle(stream))
+    if st != FA_OK:
+        raise FAError(st, "fa_decode_paged_fwd")
+    return (out, lse) if lse_ptr else out

@@ -175,6 +175,50 @@ static int decode_impl(const void* q, const void* kcache, const void* vcache,
   return cuda_status(ef, "decode cudaFreeAsync");
 }
 
+extern "C" int fa_decode_paged_fwd(const void* q, const void* kpages, const void* vpages,
+                                   const int32_t* page_table, const int32_t* seqlens, void* o,
+                                   float* lse, int B, int Hq, int Hkv, int num_pages,
+                                   int page_size, int max_pages, int D, float scale,
+                                   cudaStream_t stream) {
+  if (B < 0 || Hq < 0 || Hkv < 0 || num_pages < 0 || max_pages < 0) return FA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return FA_ERR_INVALID_ARG;
+  if (!isfinite(scale)) return FA_ERR_INVALID_ARG;
+  if (page_size < 32 || page_size % 32 != 0) return FA_ERR_INVALID_ARG;
+  if (B == 0 || Hq == 0) return FA_OK;
+  if (Hkv == 0 || Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
+  if (B > 65535 || Hq > 65535 || (int64_t)Hkv * ((Hq / Hkv + 15) / 16) > 65535)
+    return FA_ERR_INVALID_ARG;
+  if ((int64_t)max_pages * page_size > INT32_MAX) return FA_ERR_INVALID_ARG;
+  if (!q || !o || !aligned16(q) || !aligned16(o)) return FA_ERR_INVALID_ARG;
+  if (lse && !aligned4(lse)) return FA_ERR_INVALID_ARG;
+  if (max_pages > 0 &&
+      (num_pages < 1 || !kpages || !vpages || !aligned16(kpages) || !aligned16(vpages) ||
+       !page_table || !seqlens || !aligned4(page_table) || !aligned4(seqlens)))
+    return FA_ERR_INVALID_ARG;
+  if ((int64_t)num_pages * page_size * Hkv * D * 2 >= (1ll << 40)) return FA_ERR_INVALID_ARG;
+  fa::DecodeLayout ly;
+  ly.valid_len = seqlens;
+  ly.len_stride = 1;
+  ly.page_table = page_table;
+  ly.page_size = page_size;
+  ly.max_pages = max_pages;
+  ly.num_pages = num_pages;
+  const int cap = max_pages * page_size;
+  if (cap == 0)
+    return cuda_status(fa::launch_decode_layout(q, kpages, vpages, ly, o, lse, B, Hq, Hkv, D,
+                                                scale, nullptr, 0, stream),
+                       "paged decode zero-fill launch");
+  const size_t nf = fa::decode_scratch_floats(B, Hq, Hkv, cap, D);
+  void* scratch = nullptr;
+  cudaError_t e = cudaMallocAsync(&scratch, nf * sizeof(float), stream);
+  if (e != cudaSuccess) return cuda_status(e, "paged decode cudaMallocAsync");
+  int r = fa::launch_decode_layout(q, kpages, vpages, ly, o, lse, B, Hq, Hkv, D, scale,
+                                   static_cast<float*>(scratch), nf, stream);
+  cudaError_t ef = cudaFreeAsync(scratch, stream);
+  if (r != 0) return cuda_status(r, "paged decode launch");
+  return cuda_status(ef, "paged decode cudaFreeAsync");
+}
+
 extern "C" int fa_decode_fwd(const void* q, const void* kcache, const void* vcache,
                              const int32_t* valid_len_dev, void* o, int B, int Hq, int Hkv,
                              int cap, int D, float scale, cudaStream_t stream) {
@@ -199,6 +243,8 @@ extern "C" const char* fa_status_string(int status) {
     case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a device pipeline wait hit its time limit";
     case FA_ERR_TOO_LARGE:
       return "FA_ERR_TOO_LARGE: request needs more scratch than fa_decode_fwd_noalloc's fixed array";
+    case FA_ERR_BOUNDS:
+      return "FA_ERR_BOUNDS: a device-side bounds check skipped an access (offsets or page ids out of range)";
     default: return "unknown status";
   }
 }
@@ -208,8 +254,9 @@ extern "C" int fa_device_error(int reset, unsigned int* detail) {
   unsigned int a = 0, b = 0;
   if (fa::read_prefill_error(&a, reset) != 0) return FA_ERR_CUDA;
   if (fa::read_decode_error(&b, reset) != 0) return FA_ERR_CUDA;
-  if (detail) *detail = a | (b << 16);
-  return (a | b) ? FA_ERR_TIMEOUT : FA_OK;
+  if (detail) *detail = (a & 0xFFFFu) | (b << 16);
+  if ((a | b) & 1u) return FA_ERR_TIMEOUT;
+  return (a | b) ? FA_ERR_BOUNDS : FA_OK;
 }
 
 extern "C" int fa_num_sms(void) { return fa::sm_count(); }

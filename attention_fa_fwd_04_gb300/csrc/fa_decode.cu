@@ -63,7 +63,7 @@ struct Cfg {
   static constexpr int SMEM_STAGES = NSTAGE * STAGE_BYTES;
   static_assert(NSTAGE % NWARPS == 0, "each stage must belong to one consumer warp");
   static constexpr int SMEM_RED = NWARPS * HB * D * 4 + NWARPS * HB * 2 * 4 + NWARPS * HB * 4;
-  static constexpr int SMEM_BAR = 2 * NSTAGE * 8 + 16;
+  static constexpr int SMEM_BAR = 2 * NSTAGE * 8 + 16 + NSTAGE * 4;
   static_assert(HALF_BYTES % 1024 == 0, "128-byte-swizzled tiles need 1 KiB alignment");
   static constexpr int SMEM_TOTAL = 1024 + SMEM_STAGES + SMEM_RED + SMEM_BAR;
 };
@@ -71,7 +71,12 @@ struct Cfg {
 
 struct DecodeParams {
   const __nv_bfloat16* q;    // [B, Hq, D]
-  const int32_t* valid_len;  // device scalar L
+  const int32_t* valid_len;  // device: L of batch entry b is valid_len[b * len_stride]
+  int len_stride;            // 0: one L for the batch; 1: one per sequence
+  // Paged caches: K/V pages [num_pages, page_size, Hkv, D], page_table
+  // [B, max_pages] (device).  Null for contiguous [B, cap, Hkv, D] caches.
+  const int32_t* page_table;
+  int page_size, max_pages, num_pages;
   float* part_o;             // [B, Hq, nsplit, D] unnormalised partial outputs
   float* part_ml;            // [B, Hq, nsplit, 2] (row max in log2 units, row sum)
   __nv_bfloat16* o;          // [B, Hq, D]
@@ -85,7 +90,9 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-template <int D>
+// PAGED: K/V tiles are addressed through the page table (instantiated
+// separately so the contiguous path carries none of the paging code).
+template <int D, bool PAGED>
 __global__ void __launch_bounds__(dec::THREADS, 1)
     decode_split_kernel(const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const DecodeParams p) {
@@ -101,6 +108,9 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(red_w + NW * HB);
   uint64_t* empty = full + NSTAGE;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + NSTAGE);
+  // Per stage: 1 when the producer could not map the tile to a valid page (its
+  // tokens then count as masked); written before the stage's full barrier.
+  volatile int* stage_bad = abort_flag + 4;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int split = blockIdx.x;
@@ -115,7 +125,7 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
   if (threadIdx.x == dec::NWARPS * 32) {  // producer lane 0: fetch the maps early
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
-  } else if (lane == 0 && warp < NW) {
+  } else if (!PAGED && lane == 0 && warp < NW) {
     // Consumer lanes warm L2 with this CTA's first tiles while the previous
     // grid finishes (HBM is otherwise idle then).  L is read without ordering
     // here, so the tile range may be stale; that only wastes the prefetch --
@@ -151,7 +161,7 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
   // grid in the stream to complete.
   pdl_wait_primary();
 
-  int L = *p.valid_len;
+  int L = PAGED ? p.valid_len[(size_t)b * p.len_stride] : *p.valid_len;
   L = L < 0 ? 0 : (L > p.cap ? p.cap : L);
   const int tiles_total = (L + TT - 1) / TT;
   const int tps = (tiles_total + p.nsplit - 1) / p.nsplit;
@@ -170,22 +180,42 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
     // ---------------- producer warp: lanes stay converged, lane 0 issues ----------------
     const bool leader = lane == 0;
     const uint64_t pol = l2_policy_evict_first();
+    // Paged caches: lane l holds the page id of logical page pg_base + l, so
+    // the page-table reads of 32 pages cost one load latency.
+    int pg_base = -(1 << 30), pid_lane = 0;
     int t = 0;
     for (; t < n_tiles; ++t) {
       const int s = t % NSTAGE;
       const uint32_t ph = (t / NSTAGE) & 1;
+      const int tok = (t_begin + t) * TT;
+      int row = tok, tb = b, bad = 0;  // tensor-map row / batch coordinates of the tile
+      if constexpr (PAGED) {
+        const int page = tok / p.page_size;
+        if (page < pg_base || page >= pg_base + 32) {  // warp-uniform
+          pg_base = page;
+          const int pg = pg_base + lane;
+          pid_lane = pg < p.max_pages ? p.page_table[(size_t)b * p.max_pages + pg] : -1;
+        }
+        const int pid = __shfl_sync(0xffffffffu, pid_lane, page - pg_base);
+        bad = (pid < 0 || pid >= p.num_pages) ? 1 : 0;
+        row = tok - page * p.page_size;
+        tb = bad ? 0 : pid;  // a bad id loads page 0, and the tile is masked
+      }
       if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, &g_decode_err, 1)) break;
       if (leader) {
+        if constexpr (PAGED) {
+          stage_bad[s] = bad;
+          if (bad) atomicOr(&g_decode_err, kErrBounds);
+        }
         mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
-        const int tok = (t_begin + t) * TT;
         uint8_t* st = stages + s * C::STAGE_BYTES;
 #pragma unroll
         for (int h = 0; h < C::HALVES; ++h)
-          tma_load_4d_hint(st + h * dec::HALF_BYTES, &tmK, &full[s], h * 64, hkv, tok, b, pol);
+          tma_load_4d_hint(st + h * dec::HALF_BYTES, &tmK, &full[s], h * 64, hkv, row, tb, pol);
 #pragma unroll
         for (int h = 0; h < C::HALVES; ++h)
           tma_load_4d_hint(st + C::KV_BYTES + h * dec::HALF_BYTES, &tmV, &full[s], h * 64, hkv,
-                           tok, b, pol);
+                           row, tb, pol);
       }
       __syncwarp();
     }
@@ -220,9 +250,10 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
       __syncwarp();  // ldmatrix / mma.sync below are warp-collective
       uint8_t* st = stages + s * C::STAGE_BYTES;
       const int tok0 = (t_begin + t) * TT;
-      const int nvalid = (L - tok0) < TT ? (L - tok0) : TT;
+      // Tokens >= L (and every token of a tile with no valid page) are masked.
+      const int nvalid = (PAGED && stage_bad[s]) ? 0 : ((L - tok0) < TT ? (L - tok0) : TT);
       if (nvalid < TT) {
-        // Tokens >= L: zero their K and V rows before any MMA reads the tile.
+        // Masked tokens: zero their K and V rows before any MMA reads the tile.
         const int nz = TT - nvalid;
         for (int x = lane; x < 2 * C::HALVES * nz * 8; x += 32) {
           const int chunk = x & 7;
@@ -511,20 +542,32 @@ size_t decode_scratch_floats(int B, int Hq, int Hkv, int cap, int D) {
 }
 
 template <int D>
-static int launch_decode_t(const void* q, const void* kc, const void* vc, const int32_t* vl,
-                           void* o, float* lse, int B, int Hq, int Hkv, int cap, float scale,
+static int launch_decode_t(const void* q, const void* kc, const void* vc, const DecodeLayout& ly,
+                           void* o, float* lse, int B, int Hq, int Hkv, float scale,
                            float* scratch, cudaStream_t stream) {
   using C = dec::Cfg<D>;
+  const bool paged = ly.page_table != nullptr;
+  const int cap = paged ? ly.max_pages * ly.page_size : ly.cap;
   CUtensorMap tk, tv;
-  if (encode_tmap_rows(&tk, kc, D, Hkv, cap, B, dec::TT)) return cudaErrorInvalidValue;
-  if (encode_tmap_rows(&tv, vc, D, Hkv, cap, B, dec::TT)) return cudaErrorInvalidValue;
+  if (paged) {
+    if (encode_tmap_rows(&tk, kc, D, Hkv, ly.page_size, ly.num_pages, dec::TT))
+      return cudaErrorInvalidValue;
+    if (encode_tmap_rows(&tv, vc, D, Hkv, ly.page_size, ly.num_pages, dec::TT))
+      return cudaErrorInvalidValue;
+  } else {
+    if (encode_tmap_rows(&tk, kc, D, Hkv, cap, B, dec::TT)) return cudaErrorInvalidValue;
+    if (encode_tmap_rows(&tv, vc, D, Hkv, cap, B, dec::TT)) return cudaErrorInvalidValue;
+  }
   static int attr_set[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D>,
+    cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_TOTAL);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(decode_split_kernel<D, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_TOTAL);
     if (e != cudaSuccess) return e;
     // Same shared-memory carveout as the split kernel, so that combine CTAs
     // can become resident beside split CTAs and wait there.
@@ -536,7 +579,12 @@ static int launch_decode_t(const void* q, const void* kc, const void* vc, const 
   }
   DecodeParams p;
   p.q = static_cast<const __nv_bfloat16*>(q);
-  p.valid_len = vl;
+  p.valid_len = ly.valid_len;
+  p.len_stride = ly.len_stride;
+  p.page_table = ly.page_table;
+  p.page_size = ly.page_size;
+  p.max_pages = ly.max_pages;
+  p.num_pages = ly.num_pages;
   const int ns = decode_nsplit(B, Hq, Hkv, cap);
   p.part_o = scratch;
   p.part_ml = scratch + (size_t)B * Hq * ns * D;
@@ -563,7 +611,8 @@ static int launch_decode_t(const void* q, const void* kc, const void* vc, const 
   sc.stream = stream;
   sc.attrs = attr;
   sc.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&sc, decode_split_kernel<D>, tk, tv, p);
+  cudaError_t e = paged ? cudaLaunchKernelEx(&sc, decode_split_kernel<D, true>, tk, tv, p)
+                        : cudaLaunchKernelEx(&sc, decode_split_kernel<D, false>, tk, tv, p);
   if (e != cudaSuccess) return e;
 
   cudaLaunchConfig_t cfg = {};
@@ -577,10 +626,11 @@ static int launch_decode_t(const void* q, const void* kc, const void* vc, const 
   return e;
 }
 
-int launch_decode(const void* q, const void* kc, const void* vc, const int32_t* valid_len,
-                  void* o, float* lse, int B, int Hq, int Hkv, int cap, int D, float scale,
-                  float* scratch, size_t scratch_floats, cudaStream_t stream) {
+int launch_decode_layout(const void* q, const void* kc, const void* vc, const DecodeLayout& ly,
+                         void* o, float* lse, int B, int Hq, int Hkv, int D, float scale,
+                         float* scratch, size_t scratch_floats, cudaStream_t stream) {
   if (B == 0 || Hq == 0) return cudaSuccess;
+  const int cap = ly.page_table ? ly.max_pages * ly.page_size : ly.cap;
   if (cap == 0) {
     const size_t n = (size_t)B * Hq * D;
     decode_zero_kernel<<<(unsigned)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096), 256, 0,
@@ -589,10 +639,19 @@ int launch_decode(const void* q, const void* kc, const void* vc, const int32_t* 
   }
   if (scratch_floats < decode_scratch_floats(B, Hq, Hkv, cap, D)) return cudaErrorInvalidValue;
   if (D == 64)
-    return launch_decode_t<64>(q, kc, vc, valid_len, o, lse, B, Hq, Hkv, cap, scale, scratch,
-                               stream);
-  return launch_decode_t<128>(q, kc, vc, valid_len, o, lse, B, Hq, Hkv, cap, scale, scratch,
-                              stream);
+    return launch_decode_t<64>(q, kc, vc, ly, o, lse, B, Hq, Hkv, scale, scratch, stream);
+  return launch_decode_t<128>(q, kc, vc, ly, o, lse, B, Hq, Hkv, scale, scratch, stream);
+}
+
+int launch_decode(const void* q, const void* kc, const void* vc, const int32_t* valid_len,
+                  void* o, float* lse, int B, int Hq, int Hkv, int cap, int D, float scale,
+                  float* scratch, size_t scratch_floats, cudaStream_t stream) {
+  DecodeLayout ly;
+  ly.valid_len = valid_len;
+  ly.len_stride = 0;
+  ly.cap = cap;
+  return launch_decode_layout(q, kc, vc, ly, o, lse, B, Hq, Hkv, D, scale, scratch,
+                              scratch_floats, stream);
 }
 
 int read_decode_error(unsigned int* out, int reset) {

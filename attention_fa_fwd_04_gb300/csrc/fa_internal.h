@@ -38,6 +38,23 @@ int launch_decode(const void* q, const void* kc, const void* vc, const int32_t* 
                   void* o, float* lse, int B, int Hq, int Hkv, int cap, int D, float scale,
                   float* scratch, size_t scratch_floats, cudaStream_t stream);
 
+// Where the decode's K/V live and how long each sequence is.
+//   contiguous caches [B, cap, Hkv, D]: page_table == nullptr, cap = capacity;
+//   paged caches [num_pages, page_size, Hkv, D] with page_table [B, max_pages]
+//   (device; page_size a multiple of 32): capacity max_pages * page_size.
+//   valid_len: device int32, L of batch entry b at valid_len[b * len_stride].
+struct DecodeLayout {
+  const int32_t* valid_len = nullptr;
+  int len_stride = 0;
+  int cap = 0;
+  const int32_t* page_table = nullptr;
+  int page_size = 0, max_pages = 0, num_pages = 0;
+};
+
+int launch_decode_layout(const void* q, const void* kc, const void* vc, const DecodeLayout& ly,
+                         void* o, float* lse, int B, int Hq, int Hkv, int D, float scale,
+                         float* scratch, size_t scratch_floats, cudaStream_t stream);
+
 // Scratch floats the decode needs for these sizes.
 size_t decode_scratch_floats(int B, int Hq, int Hkv, int cap, int D);
 

@@ -71,7 +71,8 @@ typedef enum {
   FA_ERR_UNSUPPORTED = 2,  /* valid request this build does not implement     */
   FA_ERR_CUDA = 3,         /* a CUDA runtime/driver call or launch failed     */
   FA_ERR_TIMEOUT = 4,      /* a device-side pipeline wait hit its time limit  */
-  FA_ERR_TOO_LARGE = 5     /* request exceeds fa_decode_fwd_noalloc's scratch */
+  FA_ERR_TOO_LARGE = 5,    /* request exceeds fa_decode_fwd_noalloc's scratch */
+  FA_ERR_BOUNDS = 6        /* a device-side bounds check skipped an access     */
 } fa_status_t;
 
 /*
@@ -170,6 +171,35 @@ int fa_decode_fwd(const void* q, const void* kcache, const void* vcache,
                   cudaStream_t stream);
 
 /*
+ * fa_decode_paged_fwd -- single-token decode for a batch of sequences with
+ * their own lengths, over a paged KV cache (the decode PR's deferred items:
+ * batched shapes and non-contiguous KV storage).
+ *
+ *   q              [B, 1, Hq, D]                    bf16, read only
+ *   kpages, vpages [num_pages, page_size, Hkv, D]   bf16, read only
+ *   page_table     [B, max_pages] int32, device: sequence b's tokens
+ *                  [p*page_size, (p+1)*page_size) live in physical page
+ *                  page_table[b][p]
+ *   seqlens        [B] int32, device: sequence b's valid length, clamped to
+ *                  [0, max_pages * page_size]
+ *   o              [B, 1, Hq, D]                    bf16, written
+ *   lse            NULL, or [B, Hq] fp32 written with each head's log-sum-exp
+ *   page_size      a positive multiple of 32
+ *
+ * Only the pages that hold a sequence's first seqlens[b] tokens are read; page
+ * ids of a valid page must lie in [0, num_pages).  A page id outside that
+ * range masks that page's tokens and sets the bounds bit reported by
+ * fa_device_error().  Entries of pages past a sequence's length, and token
+ * slots past its length in its last page, may hold anything (NaN included).
+ * A contiguous cache with per-sequence lengths is the case page_size = cap,
+ * max_pages = 1, page_table[b] = b.  Other rules as fa_decode_fwd.
+ */
+int fa_decode_paged_fwd(const void* q, const void* kpages, const void* vpages,
+                        const int32_t* page_table, const int32_t* seqlens, void* o, float* lse,
+                        int B, int Hq, int Hkv, int num_pages, int page_size, int max_pages,
+                        int D, float scale, cudaStream_t stream);
+
+/*
  * fa_decode_fwd_lse -- fa_decode_fwd that also writes
  *
  *   lse    [B, Hq]  fp32, 4-byte aligned, written: the log-sum-exp of each
@@ -217,10 +247,14 @@ const char* fa_status_string(int status);
 
 /*
  * fa_device_error -- read (and if reset != 0, clear) the device-side error
- * word of the current device.  Synchronises the current device.  Returns
+ * words of the current device.  Synchronises the current device.  Returns
  * FA_OK if no kernel reported a failure, FA_ERR_TIMEOUT if a pipeline wait
- * hit its time limit, FA_ERR_CUDA if the read itself failed.
- * If detail != NULL it receives the raw error bits.
+ * hit its time limit, FA_ERR_BOUNDS if only bounds checks fired (packed
+ * offsets or page ids out of range, or an index self-check), FA_ERR_CUDA if
+ * the read itself failed.
+ * If detail != NULL it receives the raw bits: the prefill word in bits 0-15,
+ * the decode word in bits 16-31; in each, bit 0 = a wait timed out (bits 8-15:
+ * which wait), bit 1 = a bounds check fired.
  */
 int fa_device_error(int reset, unsigned int* detail);
 

@@ -134,6 +134,32 @@ def attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, scale: float, causal: 
     return (out, lse) if return_lse else out
 
 
+def decode_paged(q, kpages, vpages, page_table, seqlens, scale: float, return_lse=False):
+    """Single-token decode of B sequences over a paged cache: sequence b's
+    token t lives in page page_table[b][t // page_size], slot t % page_size.
+    Each sequence's first seqlens[b] tokens (clamped to the table's capacity)
+    are gathered into a contiguous cache and passed to the decode oracle above.
+    q [B,1,Hq,D] or [B,Hq,D]; pages [num_pages,page_size,Hkv,D]; page_table,
+    seqlens host int sequences.  Returns float64 [B,Hq,D] (and lse [B,Hq])."""
+    import torch
+    num_pages, page_size, Hkv, D = kpages.shape
+    table = [[int(x) for x in row] for row in page_table]
+    B = len(table)
+    qd = q.reshape(B, -1, D)
+    Hq = qd.shape[1]
+    out = np.zeros((B, Hq, D), dtype=np.float64)
+    lse = np.full((B, Hq), -np.inf, dtype=np.float64)
+    for b in range(B):
+        L = max(0, min(int(seqlens[b]), len(table[b]) * page_size))
+        n_pages = -(-L // page_size)
+        pages = torch.tensor(table[b][:n_pages], dtype=torch.long)
+        kc = kpages[pages].reshape(1, n_pages * page_size, Hkv, D)
+        vc = vpages[pages].reshape(1, n_pages * page_size, Hkv, D)
+        o_b, l_b = decode(qd[b:b + 1], kc, vc, L, scale, return_lse=True)
+        out[b], lse[b] = o_b[0], l_b[0]
+    return (out, lse) if return_lse else out
+
+
 def probs(q, k, v, scale: float, causal: bool, b: int, h: int, i: int):
     """(p [Sk], o [D]) of one query row: p over all Sk keys, 0 where masked."""
     lib = _load()

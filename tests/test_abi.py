@@ -40,7 +40,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_status_strings(lib):
     import attention_fa_fwd_04_gb300 as fa
-    for st in range(5):
+    for st in range(7):
         assert fa.fa_status_string(st).startswith("FA_")
     assert fa.fa_status_string(99) == "unknown status"
 

@@ -496,6 +496,48 @@ def test_varlen_sequences_are_independent_and_empty_ones_write_nothing():
     assert np.max(np.abs(o2[12:] - o[12:])) > 1e-6
 
 
+def test_paged_decode_identity_pages_equal_contiguous_decode():
+    """Pages laid out in order (page_table[b] = b*P .. b*P + P-1) are the
+    contiguous cache: the same result, bit for bit, per sequence length."""
+    B, Hq, Hkv, D, ps, P = 3, 8, 2, 16, 32, 4
+    cap = ps * P
+    q, kc, vc, _ = fa_inputs.decode_inputs(B, Hq, Hkv, cap, D, seed=23, L=cap)
+    kp = kc.reshape(B * P, ps, Hkv, D)
+    vp = vc.reshape(B * P, ps, Hkv, D)
+    table = [[b * P + p for p in range(P)] for b in range(B)]
+    lens = [1, 77, cap]
+    o, l = oracle.decode_paged(q, kp, vp, table, lens, 0.3, return_lse=True)
+    for b in range(B):
+        ob, lb = oracle.decode(q[b:b + 1], kc[b:b + 1], vc[b:b + 1], lens[b], 0.3,
+                               return_lse=True)
+        np.testing.assert_array_equal(o[b], ob[0])
+        np.testing.assert_array_equal(l[b], lb[0])
+
+
+def test_paged_decode_follows_the_page_table():
+    """Scattering the same pages to other physical slots, with the table
+    updated to match, leaves the result unchanged; pointing the table at a
+    different page changes it."""
+    B, Hq, Hkv, D, ps, P = 2, 4, 1, 8, 32, 3
+    q, kc, vc, _ = fa_inputs.decode_inputs(B, Hq, Hkv, ps * P, D, seed=24, L=ps * P)
+    kp = kc.reshape(B * P, ps, Hkv, D)
+    vp = vc.reshape(B * P, ps, Hkv, D)
+    table = [[b * P + p for p in range(P)] for b in range(B)]
+    lens = [80, 96]
+    base = oracle.decode_paged(q, kp, vp, table, lens, 0.5)
+    perm = torch.randperm(B * P, generator=torch.Generator().manual_seed(1))
+    inv = torch.empty_like(perm)
+    inv[perm] = torch.arange(B * P)
+    kp2, vp2 = kp[perm], vp[perm]                    # physical slot i holds old page perm[i]
+    table2 = [[int(inv[x]) for x in row] for row in table]
+    np.testing.assert_array_equal(oracle.decode_paged(q, kp2, vp2, table2, lens, 0.5), base)
+    table3 = [row[:] for row in table]
+    table3[1][0] = table[0][0]                        # sequence 1 reads sequence 0's first page
+    changed = oracle.decode_paged(q, kp, vp, table3, lens, 0.5)
+    np.testing.assert_array_equal(changed[0], base[0])
+    assert np.max(np.abs(changed[1] - base[1])) > 1e-6
+
+
 # ---------------------------------------------------------------------------
 # 12. Stored oracle values (tests/golden/oracle_tiny.txt, written by
 #     tests/golden/make_golden.py from the oracle alone): drift guard.
