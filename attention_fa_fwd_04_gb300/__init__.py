@@ -73,7 +73,7 @@ def load(path: str = LIB_PATH):
     lib.fa_decode_fwd_lse.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp]
     lib.fa_decode_fwd_lse.restype = i32
     lib.fa_decode_paged_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
-                                        i32, f32, vp]
+                                        i32, i32, f32, vp]
     lib.fa_decode_paged_fwd.restype = i32
     lib.fa_decode_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp]
     lib.fa_decode_fwd_noalloc.restype = i32
@@ -116,10 +116,10 @@ def fa_decode_fwd(q, kcache, vcache, valid_len_dev, o, B, Hq, Hkv, cap, D, scale
                                 stream)
 
 
-def fa_decode_paged_fwd(q, kpages, vpages, page_table, seqlens, o, lse, B, Hq, Hkv, num_pages,
-                        page_size, max_pages, D, scale, stream):
-    return load().fa_decode_paged_fwd(q, kpages, vpages, page_table, seqlens, o, lse, B, Hq, Hkv,
-                                      num_pages, page_size, max_pages, D, scale, stream)
+def fa_decode_paged_fwd(q, kpages, vpages, page_table, seqlens, o, lse, B, Sq, Hq, Hkv,
+                        num_pages, page_size, max_pages, D, scale, stream):
+    return load().fa_decode_paged_fwd(q, kpages, vpages, page_table, seqlens, o, lse, B, Sq, Hq,
+                                      Hkv, num_pages, page_size, max_pages, D, scale, stream)
 
 
 def fa_decode_fwd_lse(q, kcache, vcache, valid_len_dev, o, lse, B, Hq, Hkv, cap, D, scale,
@@ -323,19 +323,21 @@ def decode(q, kcache, vcache, valid_len, scale, out=None, stream=None, lse=None)
 
 
 def decode_paged(q, kpages, vpages, page_table, seqlens, scale, out=None, stream=None, lse=None):
-    """Single-token decode of B sequences over a paged cache.
+    """Decode of Sq new tokens for each of B sequences over a paged cache.
 
-    q [B,1,Hq,D] (or [B,Hq,D]) bf16; kpages/vpages [num_pages,page_size,Hkv,D]
-    bf16; page_table int32 CUDA [B,max_pages]; seqlens int32 CUDA [B].  Returns
-    ``out`` shaped like q, or (out, lse) with lse [B,Hq] fp32 when lse is True
-    or a tensor.
+    q [B,Sq,Hq,D] (or [B,Hq,D] for Sq = 1) bf16; kpages/vpages
+    [num_pages,page_size,Hkv,D] bf16; page_table int32 CUDA [B,max_pages];
+    seqlens int32 CUDA [B] (lengths including the new tokens).  Returns ``out``
+    shaped like q, or (out, lse) with lse [B,Sq,Hq] fp32 when lse is True or a
+    tensor.
     """
     import torch
     num_pages, page_size, Hkv, D = kpages.shape
     B, max_pages = page_table.shape
     Hq = q.shape[-2]
-    if q.shape[0] != B or q.shape[-1] != D or q.numel() != B * Hq * D:
-        raise ValueError("q must be [B,1,Hq,D] matching the page table and pages")
+    Sq = q.shape[1] if q.dim() == 4 else 1
+    if q.shape[0] != B or q.shape[-1] != D or q.numel() != B * Sq * Hq * D:
+        raise ValueError("q must be [B,Sq,Hq,D] matching the page table and pages")
     if tuple(vpages.shape) != tuple(kpages.shape):
         raise ValueError("kpages and vpages shapes differ")
     for t, n in ((q, "q"), (kpages, "kpages"), (vpages, "vpages"), (page_table, "page_table"),
@@ -350,11 +352,11 @@ def decode_paged(q, kpages, vpages, page_table, seqlens, scale, out=None, stream
     _check(out, "out")
     lse_ptr = 0
     if lse is not None and lse is not False:
-        lse = _lse_tensor(lse, (B, Hq), q)
+        lse = _lse_tensor(lse, (B, Sq, Hq), q)
         lse_ptr = lse.data_ptr()
     st = fa_decode_paged_fwd(q.data_ptr(), kpages.data_ptr(), vpages.data_ptr(),
                              page_table.data_ptr(), seqlens.data_ptr(), out.data_ptr(), lse_ptr,
-                             B, Hq, Hkv, num_pages, page_size, max_pages, D, float(scale),
+                             B, Sq, Hq, Hkv, num_pages, page_size, max_pages, D, float(scale),
                              _stream_handle(stream))
     if st != FA_OK:
         raise FAError(st, "fa_decode_paged_fwd")

@@ -177,16 +177,18 @@ static int decode_impl(const void* q, const void* kcache, const void* vcache,
 
 extern "C" int fa_decode_paged_fwd(const void* q, const void* kpages, const void* vpages,
                                    const int32_t* page_table, const int32_t* seqlens, void* o,
-                                   float* lse, int B, int Hq, int Hkv, int num_pages,
+                                   float* lse, int B, int Sq, int Hq, int Hkv, int num_pages,
                                    int page_size, int max_pages, int D, float scale,
                                    cudaStream_t stream) {
-  if (B < 0 || Hq < 0 || Hkv < 0 || num_pages < 0 || max_pages < 0) return FA_ERR_INVALID_ARG;
+  if (B < 0 || Sq < 0 || Hq < 0 || Hkv < 0 || num_pages < 0 || max_pages < 0)
+    return FA_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return FA_ERR_INVALID_ARG;
   if (!isfinite(scale)) return FA_ERR_INVALID_ARG;
   if (page_size < 32 || page_size % 32 != 0) return FA_ERR_INVALID_ARG;
-  if (B == 0 || Hq == 0) return FA_OK;
+  if (B == 0 || Sq == 0 || Hq == 0) return FA_OK;
   if (Hkv == 0 || Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
-  if (B > 65535 || Hq > 65535 || (int64_t)Hkv * ((Hq / Hkv + 15) / 16) > 65535)
+  if (B > 65535 || (int64_t)Sq * Hq > 65535 ||
+      (int64_t)Hkv * (((int64_t)Sq * (Hq / Hkv) + 15) / 16) > 65535)
     return FA_ERR_INVALID_ARG;
   if ((int64_t)max_pages * page_size > INT32_MAX) return FA_ERR_INVALID_ARG;
   if (!q || !o || !aligned16(q) || !aligned16(o)) return FA_ERR_INVALID_ARG;
@@ -203,12 +205,13 @@ extern "C" int fa_decode_paged_fwd(const void* q, const void* kpages, const void
   ly.page_size = page_size;
   ly.max_pages = max_pages;
   ly.num_pages = num_pages;
+  ly.Sq = Sq;
   const int cap = max_pages * page_size;
   if (cap == 0)
     return cuda_status(fa::launch_decode_layout(q, kpages, vpages, ly, o, lse, B, Hq, Hkv, D,
                                                 scale, nullptr, 0, stream),
                        "paged decode zero-fill launch");
-  const size_t nf = fa::decode_scratch_floats(B, Hq, Hkv, cap, D);
+  const size_t nf = fa::decode_scratch_floats(B, Hq, Hkv, cap, D, Sq);
   void* scratch = nullptr;
   cudaError_t e = cudaMallocAsync(&scratch, nf * sizeof(float), stream);
   if (e != cudaSuccess) return cuda_status(e, "paged decode cudaMallocAsync");

@@ -82,8 +82,20 @@ struct DecodeParams {
   __nv_bfloat16* o;          // [B, Hq, D]
   float* lse;                // [B, Hq] natural-log log-sum-exp per head, or null
   int B, Hq, Hkv, cap, G, nsplit, n_hb;
+  // New query tokens per sequence (paged path; 1 otherwise).  The MMA's 16
+  // rows are (token, head) pairs r = s * G + g of one kv head; token s sees
+  // the keys [0, L - Sq + s] (bottom-right causal).
+  int Sq;
   float c;                   // scale * log2(e)
 };
+
+// Query row of MMA row r (r = s * G + g) of kv head hkv in batch entry b: the
+// index of (b, s, hkv * G + g) in [B, Sq, Hq].
+__device__ __forceinline__ size_t decode_qrow(const DecodeParams& p, int b, int hkv, int r,
+                                              int Sq) {
+  const int s = r / p.G, g = r - s * p.G;
+  return ((size_t)b * Sq + s) * p.Hq + (size_t)hkv * p.G + g;
+}
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -162,6 +174,7 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
   pdl_wait_primary();
 
   int L = PAGED ? p.valid_len[(size_t)b * p.len_stride] : *p.valid_len;
+  const int Sq = PAGED ? p.Sq : 1;  // compile-time 1 on the contiguous path
   L = L < 0 ? 0 : (L > p.cap ? p.cap : L);
   const int tiles_total = (L + TT - 1) / TT;
   const int tps = (tiles_total + p.nsplit - 1) / p.nsplit;
@@ -229,11 +242,14 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
     // ---------------- consumers: whole tiles, round-robin over warps ----------------
     // Q as the MMA's A operand (rows = the CTA's query heads, padded to 16).
     const int hi0 = hb * HB + g, hi1 = hi0 + 8;
-    const bool ok0 = hi0 < p.G, ok1 = hi1 < p.G;
+    const bool ok0 = hi0 < Sq * p.G, ok1 = hi1 < Sq * p.G;
     const uint32_t* q0 = reinterpret_cast<const uint32_t*>(
-        p.q + ((size_t)b * p.Hq + (size_t)hkv * p.G + (ok0 ? hi0 : 0)) * D);
+        p.q + decode_qrow(p, b, hkv, ok0 ? hi0 : 0, Sq) * D);
     const uint32_t* q1 = reinterpret_cast<const uint32_t*>(
-        p.q + ((size_t)b * p.Hq + (size_t)hkv * p.G + (ok1 ? hi1 : 0)) * D);
+        p.q + decode_qrow(p, b, hkv, ok1 ? hi1 : 0, Sq) * D);
+    // Keys each of the thread's two rows may see (causal among new tokens).
+    const int vis0 = L - Sq + 1 + (ok0 ? hi0 / p.G : 0);
+    const int vis1 = L - Sq + 1 + (ok1 ? hi1 / p.G : 0);
     uint32_t qa[D / 16][4];
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
@@ -290,13 +306,20 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
           mma_bf16_16816(sc[2 * np + 1], qa[kk], b2, b3);
         }
       }
-      // Scale into the log2 domain, then mask tokens >= L.
+      // Scale into the log2 domain, then mask tokens >= L (and, with several
+      // new tokens, the keys after each row's own position).
 #pragma unroll
       for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           sc[nb][e] *= p.c;
-          if (nvalid < TT && nb * 8 + 2 * tq + (e & 1) >= nvalid) sc[nb][e] = NEG_INF;
+          if constexpr (PAGED) {
+            if (tok0 + nb * 8 + 2 * tq + (e & 1) >= ((e < 2) ? vis0 : vis1) ||
+                nb * 8 + 2 * tq + (e & 1) >= nvalid)
+              sc[nb][e] = NEG_INF;
+          } else {
+            if (nvalid < TT && nb * 8 + 2 * tq + (e & 1) >= nvalid) sc[nb][e] = NEG_INF;
+          }
         }
       // Online softmax over this warp's tiles.
       float mx0 = NEG_INF, mx1 = NEG_INF;
@@ -373,7 +396,7 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
     }
     // This warp's unnormalised O rows (only the CTA's real heads are kept).
     float* my_o = red_o + warp * HB * D;
-    const int nh_rows = (p.G - hb * HB) < HB ? (p.G - hb * HB) : HB;
+    const int nh_rows = (Sq * p.G - hb * HB) < HB ? (Sq * p.G - hb * HB) : HB;
 #pragma unroll
     for (int nd = 0; nd < D / 8; ++nd) {
       if (g < nh_rows)
@@ -389,10 +412,12 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
   // Merge the warps' partials (weights exp2(m_w - M)) and write this split's
   // partial for the CTA's heads: the weights once per row, then the outputs
   // four columns per thread.
-  const size_t head0 = (size_t)b * p.Hq + (size_t)hkv * p.G + (size_t)hb * HB;
-  int nh = (p.G - hb * HB) < HB ? (p.G - hb * HB) : HB;
+  int nh = (Sq * p.G - hb * HB) < HB ? (Sq * p.G - hb * HB) : HB;
+  // Query row of CTA row `row` (partials and outputs are indexed by it).
+  auto qrow = [&](int row) { return decode_qrow(p, b, hkv, hb * HB + row, Sq); };
   // Self-check: partial rows must lie inside the scratch (records and skips).
-  if (b >= p.B || split >= p.nsplit || head0 + nh > (size_t)p.B * p.Hq) {
+  if (b >= p.B || split >= p.nsplit ||
+      (nh > 0 && qrow(nh - 1) >= (size_t)p.B * Sq * p.Hq)) {
     if (threadIdx.x == 0) atomicOr(&g_decode_err, kErrBounds);
     nh = 0;
   }
@@ -409,8 +434,8 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
       red_w[w * HB + row] = wt;
       Ls += red_ml[(w * HB + row) * 2 + 1] * wt;
     }
-    p.part_ml[((head0 + row) * p.nsplit + split) * 2 + 0] = M;
-    p.part_ml[((head0 + row) * p.nsplit + split) * 2 + 1] = Ls;
+    p.part_ml[(qrow(row) * p.nsplit + split) * 2 + 0] = M;
+    p.part_ml[(qrow(row) * p.nsplit + split) * 2 + 1] = Ls;
   }
   __syncthreads();
   for (int x = threadIdx.x; x < nh * (D / 4); x += dec::THREADS) {
@@ -425,7 +450,7 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
       o.z += v.z * wt;
       o.w += v.w * wt;
     }
-    reinterpret_cast<float4*>(p.part_o + ((head0 + row) * p.nsplit + split) * D)[d4] = o;
+    reinterpret_cast<float4*>(p.part_o + (qrow(row) * p.nsplit + split) * D)[d4] = o;
   }
 }
 
@@ -456,11 +481,11 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const D
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int d = blockIdx.x * 32 + lane;
   const int h = blockIdx.y, b = blockIdx.z;
-  if (h >= p.Hq || b >= p.B || p.nsplit > kMaxSplits) {
+  if (h >= p.Sq * p.Hq || b >= p.B || p.nsplit > kMaxSplits) {
     if (t == 0) atomicOr(&g_decode_err, kErrBounds << 4);
     return;
   }
-  const size_t base = ((size_t)b * p.Hq + h) * p.nsplit;
+  const size_t base = ((size_t)b * p.Sq * p.Hq + h) * p.nsplit;  // h: row in [Sq, Hq]
   float ov[kSplitsPerWarp];
 #pragma unroll
   for (int k = 0; k < kSplitsPerWarp; ++k) {
@@ -504,10 +529,10 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const D
       dsum += sRed[w];
     }
     const float out = dsum > 0.f ? num / dsum : 0.f;
-    if (d < D) p.o[((size_t)b * p.Hq + h) * D + d] = __float2bfloat16_rn(out);
+    if (d < D) p.o[((size_t)b * p.Sq * p.Hq + h) * D + d] = __float2bfloat16_rn(out);
     // log sum_j exp(s_j) = ln2 * (M + log2 sum_s 2^(m_s - M) l_s), M in log2 units.
     if (p.lse && lane == 0 && blockIdx.x == 0)
-      p.lse[(size_t)b * p.Hq + h] = dsum > 0.f ? 0.6931471805599453f * (M + __log2f(dsum))
+      p.lse[(size_t)b * p.Sq * p.Hq + h] = dsum > 0.f ? 0.6931471805599453f * (M + __log2f(dsum))
                                                : -INFINITY;
   }
 }
@@ -523,9 +548,9 @@ __global__ void decode_zero_kernel(__nv_bfloat16* o, size_t n, float* lse, size_
       lse[i] = -INFINITY;
 }
 
-static int decode_nsplit(int B, int Hq, int Hkv, int cap) {
+static int decode_nsplit(int B, int Hq, int Hkv, int cap, int Sq) {
   const int G = Hq / Hkv;
-  const int n_hb = (G + dec::HB - 1) / dec::HB;
+  const int n_hb = (Sq * G + dec::HB - 1) / dec::HB;
   const long units = (long)B * Hkv * n_hb;
   const int sms = sm_count() > 0 ? sm_count() : 148;
   long ns = sms / (units > 0 ? units : 1);
@@ -536,9 +561,9 @@ static int decode_nsplit(int B, int Hq, int Hkv, int cap) {
   return (int)ns;
 }
 
-size_t decode_scratch_floats(int B, int Hq, int Hkv, int cap, int D) {
-  const size_t ns = (size_t)decode_nsplit(B, Hq, Hkv, cap);
-  return (size_t)B * Hq * ns * ((size_t)D + 2);
+size_t decode_scratch_floats(int B, int Hq, int Hkv, int cap, int D, int Sq) {
+  const size_t ns = (size_t)decode_nsplit(B, Hq, Hkv, cap, Sq);
+  return (size_t)B * Sq * Hq * ns * ((size_t)D + 2);
 }
 
 template <int D>
@@ -585,9 +610,11 @@ static int launch_decode_t(const void* q, const void* kc, const void* vc, const 
   p.page_size = ly.page_size;
   p.max_pages = ly.max_pages;
   p.num_pages = ly.num_pages;
-  const int ns = decode_nsplit(B, Hq, Hkv, cap);
+  const int Sq = paged ? ly.Sq : 1;
+  const int ns = decode_nsplit(B, Hq, Hkv, cap, Sq);
   p.part_o = scratch;
-  p.part_ml = scratch + (size_t)B * Hq * ns * D;
+  p.part_ml = scratch + (size_t)B * Sq * Hq * ns * D;
+  p.Sq = Sq;
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;
   p.B = B;
@@ -596,7 +623,7 @@ static int launch_decode_t(const void* q, const void* kc, const void* vc, const 
   p.cap = cap;
   p.G = Hq / Hkv;
   p.nsplit = ns;
-  p.n_hb = (p.G + dec::HB - 1) / dec::HB;
+  p.n_hb = (Sq * p.G + dec::HB - 1) / dec::HB;
   p.c = scale * 1.4426950408889634f;
 
   // Both kernels are programmatic dependents of the grid before them: each
@@ -616,7 +643,7 @@ static int launch_decode_t(const void* q, const void* kc, const void* vc, const 
   if (e != cudaSuccess) return e;
 
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((D + 31) / 32, Hq, B);
+  cfg.gridDim = dim3((D + 31) / 32, Sq * Hq, B);
   cfg.blockDim = dim3(kCombineThreads, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
@@ -632,12 +659,13 @@ int launch_decode_layout(const void* q, const void* kc, const void* vc, const De
   if (B == 0 || Hq == 0) return cudaSuccess;
   const int cap = ly.page_table ? ly.max_pages * ly.page_size : ly.cap;
   if (cap == 0) {
-    const size_t n = (size_t)B * Hq * D;
+    const size_t rows = (size_t)B * (ly.page_table ? ly.Sq : 1) * Hq, n = rows * D;
     decode_zero_kernel<<<(unsigned)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096), 256, 0,
-                         stream>>>(static_cast<__nv_bfloat16*>(o), n, lse, (size_t)B * Hq);
+                         stream>>>(static_cast<__nv_bfloat16*>(o), n, lse, rows);
     return cudaGetLastError();
   }
-  if (scratch_floats < decode_scratch_floats(B, Hq, Hkv, cap, D)) return cudaErrorInvalidValue;
+  const int Sq = ly.page_table ? ly.Sq : 1;
+  if (scratch_floats < decode_scratch_floats(B, Hq, Hkv, cap, D, Sq)) return cudaErrorInvalidValue;
   if (D == 64)
     return launch_decode_t<64>(q, kc, vc, ly, o, lse, B, Hq, Hkv, scale, scratch, stream);
   return launch_decode_t<128>(q, kc, vc, ly, o, lse, B, Hq, Hkv, scale, scratch, stream);

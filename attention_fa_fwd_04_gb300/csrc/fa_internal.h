@@ -49,14 +49,15 @@ struct DecodeLayout {
   int cap = 0;
   const int32_t* page_table = nullptr;
   int page_size = 0, max_pages = 0, num_pages = 0;
+  int Sq = 1;  // new query tokens per sequence (paged layout only)
 };
 
 int launch_decode_layout(const void* q, const void* kc, const void* vc, const DecodeLayout& ly,
                          void* o, float* lse, int B, int Hq, int Hkv, int D, float scale,
                          float* scratch, size_t scratch_floats, cudaStream_t stream);
 
-// Scratch floats the decode needs for these sizes.
-size_t decode_scratch_floats(int B, int Hq, int Hkv, int cap, int D);
+// Scratch floats the decode needs for these sizes (Sq new tokens per sequence).
+size_t decode_scratch_floats(int B, int Hq, int Hkv, int cap, int D, int Sq = 1);
 
 // Device error words of the kernel translation units (read + optionally clear).
 int read_prefill_error(unsigned int* out, int reset);

@@ -171,19 +171,27 @@ int fa_decode_fwd(const void* q, const void* kcache, const void* vcache,
                   cudaStream_t stream);
 
 /*
- * fa_decode_paged_fwd -- single-token decode for a batch of sequences with
- * their own lengths, over a paged KV cache (the decode PR's deferred items:
- * batched shapes and non-contiguous KV storage).
+ * fa_decode_paged_fwd -- decode of Sq new tokens per sequence (Sq = 1: the
+ * single-token step; Sq > 1: tokens proposed by speculative decoding) for a
+ * batch of sequences with their own lengths, over a paged KV cache (the
+ * decode PR's deferred items: batched shapes, several query tokens, and
+ * non-contiguous KV storage).
  *
- *   q              [B, 1, Hq, D]                    bf16, read only
+ *   q              [B, Sq, Hq, D]                   bf16, read only
  *   kpages, vpages [num_pages, page_size, Hkv, D]   bf16, read only
  *   page_table     [B, max_pages] int32, device: sequence b's tokens
  *                  [p*page_size, (p+1)*page_size) live in physical page
  *                  page_table[b][p]
- *   seqlens        [B] int32, device: sequence b's valid length, clamped to
- *                  [0, max_pages * page_size]
- *   o              [B, 1, Hq, D]                    bf16, written
- *   lse            NULL, or [B, Hq] fp32 written with each head's log-sum-exp
+ *   seqlens        [B] int32, device: sequence b's valid length L (including
+ *                  its Sq new tokens, whose K/V are already in the cache),
+ *                  clamped to [0, max_pages * page_size]
+ *   o              [B, Sq, Hq, D]                   bf16, written
+ *   lse            NULL, or [B, Sq, Hq] fp32 written with each row's
+ *                  log-sum-exp
+ *
+ * New token s (0-based) sits at position L - Sq + s and sees the keys
+ * [0, L - Sq + s] (bottom-right causal); rows that see no key give O = 0 and
+ * lse = -inf.
  *   page_size      a positive multiple of 32
  *
  * Only the pages that hold a sequence's first seqlens[b] tokens are read; page
@@ -196,8 +204,8 @@ int fa_decode_fwd(const void* q, const void* kcache, const void* vcache,
  */
 int fa_decode_paged_fwd(const void* q, const void* kpages, const void* vpages,
                         const int32_t* page_table, const int32_t* seqlens, void* o, float* lse,
-                        int B, int Hq, int Hkv, int num_pages, int page_size, int max_pages,
-                        int D, float scale, cudaStream_t stream);
+                        int B, int Sq, int Hq, int Hkv, int num_pages, int page_size,
+                        int max_pages, int D, float scale, cudaStream_t stream);
 
 /*
  * fa_decode_fwd_lse -- fa_decode_fwd that also writes

@@ -135,28 +135,31 @@ def attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, scale: float, causal: 
 
 
 def decode_paged(q, kpages, vpages, page_table, seqlens, scale: float, return_lse=False):
-    """Single-token decode of B sequences over a paged cache: sequence b's
+    """Decode of Sq new tokens per sequence over a paged cache: sequence b's
     token t lives in page page_table[b][t // page_size], slot t % page_size.
-    Each sequence's first seqlens[b] tokens (clamped to the table's capacity)
-    are gathered into a contiguous cache and passed to the decode oracle above.
-    q [B,1,Hq,D] or [B,Hq,D]; pages [num_pages,page_size,Hkv,D]; page_table,
-    seqlens host int sequences.  Returns float64 [B,Hq,D] (and lse [B,Hq])."""
+    Each sequence's first L = seqlens[b] tokens (clamped to the table's
+    capacity) are gathered into a contiguous cache; its Sq new query tokens
+    are the last Sq positions, so the dense oracle with bottom-right causal
+    masking (Sq rows against L keys) gives the result.
+    q [B,Sq,Hq,D] (or [B,Hq,D] for Sq = 1); pages [num_pages,page_size,Hkv,D];
+    page_table, seqlens host int sequences.  Returns float64 [B,Sq,Hq,D] (and
+    lse [B,Sq,Hq])."""
     import torch
     num_pages, page_size, Hkv, D = kpages.shape
     table = [[int(x) for x in row] for row in page_table]
     B = len(table)
-    qd = q.reshape(B, -1, D)
-    Hq = qd.shape[1]
-    out = np.zeros((B, Hq, D), dtype=np.float64)
-    lse = np.full((B, Hq), -np.inf, dtype=np.float64)
+    qd = q.reshape(B, -1, q.shape[-2], D)
+    Sq, Hq = qd.shape[1], qd.shape[2]
+    out = np.zeros((B, Sq, Hq, D), dtype=np.float64)
+    lse = np.full((B, Sq, Hq), -np.inf, dtype=np.float64)
     for b in range(B):
         L = max(0, min(int(seqlens[b]), len(table[b]) * page_size))
         n_pages = -(-L // page_size)
         pages = torch.tensor(table[b][:n_pages], dtype=torch.long)
-        kc = kpages[pages].reshape(1, n_pages * page_size, Hkv, D)
-        vc = vpages[pages].reshape(1, n_pages * page_size, Hkv, D)
-        o_b, l_b = decode(qd[b:b + 1], kc, vc, L, scale, return_lse=True)
-        out[b], lse[b] = o_b[0], l_b[0]
+        kc = kpages[pages].reshape(1, n_pages * page_size, Hkv, D)[:, :L]
+        vc = vpages[pages].reshape(1, n_pages * page_size, Hkv, D)[:, :L]
+        o_b, l_b = attention(qd[b:b + 1], kc, vc, scale, True, return_lse=True)
+        out[b], lse[b] = o_b[0], l_b[0].T
     return (out, lse) if return_lse else out
 
 

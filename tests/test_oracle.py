@@ -510,8 +510,8 @@ def test_paged_decode_identity_pages_equal_contiguous_decode():
     for b in range(B):
         ob, lb = oracle.decode(q[b:b + 1], kc[b:b + 1], vc[b:b + 1], lens[b], 0.3,
                                return_lse=True)
-        np.testing.assert_array_equal(o[b], ob[0])
-        np.testing.assert_array_equal(l[b], lb[0])
+        np.testing.assert_array_equal(o[b, 0], ob[0])
+        np.testing.assert_array_equal(l[b, 0], lb[0])
 
 
 def test_paged_decode_follows_the_page_table():
@@ -536,6 +536,27 @@ def test_paged_decode_follows_the_page_table():
     changed = oracle.decode_paged(q, kp, vp, table3, lens, 0.5)
     np.testing.assert_array_equal(changed[0], base[0])
     assert np.max(np.abs(changed[1] - base[1])) > 1e-6
+
+
+def test_paged_decode_several_new_tokens_is_causal_within_them():
+    """Sq new tokens: token s equals a single-token decode over the first
+    L - Sq + s + 1 tokens (it sees itself and the tokens before it)."""
+    B, Sq, Hq, Hkv, D, ps, P = 2, 3, 4, 2, 8, 32, 3
+    g = torch.Generator().manual_seed(25)
+    kp = torch.randn(B * P, ps, Hkv, D, generator=g).to(torch.bfloat16)
+    vp = torch.randn(B * P, ps, Hkv, D, generator=g).to(torch.bfloat16)
+    q = torch.randn(B, Sq, Hq, D, generator=g).to(torch.bfloat16)
+    table = [[b * P + p for p in range(P)] for b in range(B)]
+    lens = [70, 2]                      # sequence 1: token 0 of 3 sees no key
+    o, l = oracle.decode_paged(q, kp, vp, table, lens, 0.4, return_lse=True)
+    for b in range(B):
+        kc = kp[b * P:(b + 1) * P].reshape(1, P * ps, Hkv, D)
+        vc = vp[b * P:(b + 1) * P].reshape(1, P * ps, Hkv, D)
+        for s_ in range(Sq):
+            vis = lens[b] - Sq + s_ + 1
+            ob, lb = oracle.decode(q[b:b + 1, s_], kc, vc, max(vis, 0), 0.4, return_lse=True)
+            np.testing.assert_array_equal(o[b, s_], ob[0])
+            np.testing.assert_array_equal(l[b, s_], lb[0])
 
 
 # ---------------------------------------------------------------------------

@@ -46,7 +46,7 @@ def run_paged(fa, q, kp, vp, table, lens, scale, lse=True):
     torch.cuda.synchronize()
     st, detail = fa.fa_device_error()
     assert st == fa.FA_OK, f"device error word {detail:#x}"
-    return out.float().cpu().numpy().reshape(q.shape[0], -1, q.shape[-1]), l.cpu().numpy()
+    return out.float().cpu().numpy().reshape(q.shape), l.cpu().numpy()
 
 
 @pytest.mark.parametrize("B,Hq,Hkv,D,page_size,max_pages,lens", [
@@ -102,3 +102,22 @@ def test_paged_bad_page_id_is_masked_and_reported(fa):
     keepv = torch.cat([vc[:, :2 * ps], vc[:, 3 * ps:]], dim=1)
     ref = oracle.decode(q, keep, keepv, 3 * ps, 0.088)
     compare(out.float().cpu().numpy().reshape(1, Hq, D), ref)
+
+
+@pytest.mark.parametrize("B,Sq,Hq,Hkv,D,page_size,max_pages,lens", [
+    (2, 4, 8, 2, 128, 64, 16, [700, 3]),        # 4 tokens x 4 heads = 16 MMA rows; L < Sq
+    (3, 2, 32, 4, 64, 32, 30, [1, 960, 513]),   # 2 x 8 rows per kv head
+    (1, 5, 8, 1, 128, 128, 8, [1000]),          # 5 x 8 = 40 rows: three 16-row blocks
+])
+def test_paged_decode_several_new_tokens(fa, B, Sq, Hq, Hkv, D, page_size, max_pages, lens):
+    """Sq new tokens per sequence (speculative decoding): bottom-right causal
+    among the new tokens, each row with its own visible length."""
+    q1, kp, vp, table, L = paged_inputs(B, Hq, Hkv, D, page_size, max_pages, lens, seed=Sq + D)
+    g = torch.Generator().manual_seed(Sq)
+    q = torch.randn(B, Sq, Hq, D, generator=g).to(torch.bfloat16)
+    scale = 1 / math.sqrt(D)
+    o, l = run_paged(fa, q, kp, vp, table, L, scale)
+    ref, ref_l = oracle.decode_paged(q, kp, vp, table.tolist(), L.tolist(), scale,
+                                     return_lse=True)
+    compare(o, ref)
+    lse_compare(l, ref_l)
