@@ -50,6 +50,9 @@ def _load():
         lib.oracle_decode.restype = i32
         lib.oracle_decode_lse.argtypes = [dp, dp, dp, dp, dp, i32, i32, i32, i64, i32, i64, f64]
         lib.oracle_decode_lse.restype = i32
+        lib.oracle_attention_bwd.argtypes = [dp, dp, dp, dp, dp, dp, dp, i32, i32, i32, i64,
+                                             i64, i32, f64, i32, i32]
+        lib.oracle_attention_bwd.restype = i32
         _lib = lib
     return _lib
 
@@ -161,6 +164,24 @@ def decode_paged(q, kpages, vpages, page_table, seqlens, scale: float, return_ls
         o_b, l_b = attention(qd[b:b + 1], kc, vc, scale, True, return_lse=True)
         out[b], lse[b] = o_b[0], l_b[0].T
     return (out, lse) if return_lse else out
+
+
+def attention_bwd(q, k, v, dout, scale: float, causal: bool, nthreads=None):
+    """Gradients (dq [B,Sq,Hq,D], dk, dv [B,Sk,Hkv,D], float64) of the loss
+    sum(O * dout) for the forward pass above (same masking and GQA map)."""
+    lib = _load()
+    B, Sq, Hq, D = q.shape
+    _, Sk, Hkv, _ = k.shape
+    qd, kd, vd, dd = _f64(q), _f64(k), _f64(v), _f64(dout)
+    dq = np.zeros((B, Sq, Hq, D), dtype=np.float64)
+    dk = np.zeros((B, Sk, Hkv, D), dtype=np.float64)
+    dv = np.zeros((B, Sk, Hkv, D), dtype=np.float64)
+    rc = lib.oracle_attention_bwd(_ptr(qd), _ptr(kd), _ptr(vd), _ptr(dd), _ptr(dq), _ptr(dk),
+                                  _ptr(dv), B, Hq, Hkv, Sq, Sk, D, float(scale),
+                                  int(bool(causal)), int(nthreads or default_threads()))
+    if rc != 0:
+        raise RuntimeError(f"oracle_attention_bwd failed with status {rc}")
+    return dq, dk, dv
 
 
 def probs(q, k, v, scale: float, causal: bool, b: int, h: int, i: int):

@@ -250,3 +250,130 @@ int oracle_decode(const double* q, const double* kcache, const double* vcache,
                   int64_t L, double scale) {
   return oracle_decode_lse(q, kcache, vcache, o, NULL, B, Hq, Hkv, cap, D, L, scale);
 }
+
+/*
+ * Backward pass: gradients of the loss l = sum_{b,i,h,d} O[b,i,h,d] dO[b,i,h,d]
+ * with respect to Q, K and V (tessera #90, flash-attention backward commit
+ * note: the "_pre" pass forms Delta_i = sum_d dO_id O_id, then dV += P^T dO,
+ * dP = dO V^T, dS = P * (dP - Delta), dK += scale * dS^T Q, dQ += scale * dS K).
+ * Written out from the definition of the forward pass, row by row:
+ *   p_j    = exp(s_j - m) / sum_k exp(s_k - m)   over the row's visible keys
+ *   dV_j  += p_j dO
+ *   dp_j   = <dO, V_j>
+ *   Delta  = sum_j p_j dp_j                      (= <dO, O>)
+ *   ds_j   = p_j (dp_j - Delta)
+ *   dQ     = scale * sum_j ds_j K_j
+ *   dK_j  += scale * ds_j Q
+ * Query heads of a GQA group add into the same dK, dV.  One worker per
+ * (b, kv head) owns that head's dK/dV rows, so no two threads add to the same
+ * element.
+ */
+typedef struct {
+  const double *q, *k, *v, *dout;
+  double *dq, *dk, *dv;
+  int B, Hq, Hkv, D, causal;
+  int64_t Sq, Sk;
+  double scale;
+  int64_t u0, u1; /* (b, kv head) units of this worker */
+  int status;
+} bwd_job_t;
+
+static void* bwd_worker(void* arg) {
+  bwd_job_t* J = (bwd_job_t*)arg;
+  const int G = J->Hq / J->Hkv, D = J->D;
+  double* pr = (double*)malloc(sizeof(double) * (size_t)(J->Sk > 0 ? J->Sk : 1));
+  double* dp = (double*)malloc(sizeof(double) * (size_t)(J->Sk > 0 ? J->Sk : 1));
+  if (!pr || !dp) { free(pr); free(dp); J->status = 1; return NULL; }
+  const int64_t kstride = (int64_t)J->Hkv * D;
+  int64_t u, i, j;
+  int g, d;
+  for (u = J->u0; u < J->u1; ++u) {
+    const int64_t b = u / J->Hkv, kv = u % J->Hkv;
+    const double* kb = J->k + (b * J->Sk * J->Hkv + kv) * D;
+    const double* vb = J->v + (b * J->Sk * J->Hkv + kv) * D;
+    double* dkb = J->dk + (b * J->Sk * J->Hkv + kv) * D;
+    double* dvb = J->dv + (b * J->Sk * J->Hkv + kv) * D;
+    for (g = 0; g < G; ++g) {
+      const int64_t h = kv * G + g;
+      for (i = 0; i < J->Sq; ++i) {
+        const double* qi = J->q + ((b * J->Sq + i) * J->Hq + h) * D;
+        const double* doi = J->dout + ((b * J->Sq + i) * J->Hq + h) * D;
+        double* dqi = J->dq + ((b * J->Sq + i) * J->Hq + h) * D;
+        for (d = 0; d < D; ++d) dqi[d] = 0.0;
+        const int64_t n_vis = visible_keys(i, J->Sq, J->Sk, J->causal);
+        if (n_vis <= 0) continue;
+        /* the row's probabilities pr_j, as in the forward pass */
+        double mx = -INFINITY;
+        for (j = 0; j < n_vis; ++j) {
+          double dot = 0.0;
+          for (d = 0; d < D; ++d) dot += qi[d] * kb[j * kstride + d];
+          pr[j] = J->scale * dot;
+          mx = pr[j] > mx ? pr[j] : mx;
+        }
+        double den = 0.0;
+        for (j = 0; j < n_vis; ++j) {
+          pr[j] = exp(pr[j] - mx);
+          den += pr[j];
+        }
+        double delta = 0.0;
+        for (j = 0; j < n_vis; ++j) {
+          pr[j] /= den;
+          double dot = 0.0;
+          for (d = 0; d < D; ++d) dot += doi[d] * vb[j * kstride + d];
+          dp[j] = dot;
+          delta += pr[j] * dp[j];
+        }
+        for (j = 0; j < n_vis; ++j) {
+          const double ds = pr[j] * (dp[j] - delta);
+          for (d = 0; d < D; ++d) {
+            dvb[j * kstride + d] += pr[j] * doi[d];
+            dqi[d] += J->scale * ds * kb[j * kstride + d];
+            dkb[j * kstride + d] += J->scale * ds * qi[d];
+          }
+        }
+      }
+    }
+  }
+  free(pr);
+  free(dp);
+  J->status = 0;
+  return NULL;
+}
+
+/* dQ [B, Sq, Hq, D], dK / dV [B, Sk, Hkv, D] (overwritten) for the loss
+ * sum(O * dO).  Returns 0 on success. */
+int oracle_attention_bwd(const double* q, const double* k, const double* v,
+                         const double* dout, double* dq, double* dk, double* dv, int B,
+                         int Hq, int Hkv, int64_t Sq, int64_t Sk, int D, double scale,
+                         int causal, int nthreads) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || D <= 0 || Sq < 0 || Sk < 0) return 2;
+  memset(dk, 0, sizeof(double) * (size_t)B * (size_t)Sk * (size_t)Hkv * (size_t)D);
+  memset(dv, 0, sizeof(double) * (size_t)B * (size_t)Sk * (size_t)Hkv * (size_t)D);
+  memset(dq, 0, sizeof(double) * (size_t)B * (size_t)Sq * (size_t)Hq * (size_t)D);
+  const int64_t units = (int64_t)B * Hkv;
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > units) nthreads = (int)(units > 0 ? units : 1);
+  bwd_job_t* jobs = (bwd_job_t*)calloc((size_t)nthreads, sizeof(bwd_job_t));
+  pthread_t* th = (pthread_t*)calloc((size_t)nthreads, sizeof(pthread_t));
+  if (!jobs || !th) { free(jobs); free(th); return 1; }
+  int t, rc = 0;
+  for (t = 0; t < nthreads; ++t) {
+    bwd_job_t* J = &jobs[t];
+    J->q = q; J->k = k; J->v = v; J->dout = dout; J->dq = dq; J->dk = dk; J->dv = dv;
+    J->B = B; J->Hq = Hq; J->Hkv = Hkv; J->D = D; J->causal = causal;
+    J->Sq = Sq; J->Sk = Sk; J->scale = scale;
+    J->u0 = units * t / nthreads;
+    J->u1 = units * (t + 1) / nthreads;
+    J->status = 1;
+  }
+  if (nthreads == 1) {
+    bwd_worker(&jobs[0]);
+  } else {
+    for (t = 0; t < nthreads; ++t) pthread_create(&th[t], NULL, bwd_worker, &jobs[t]);
+    for (t = 0; t < nthreads; ++t) pthread_join(th[t], NULL);
+  }
+  for (t = 0; t < nthreads; ++t) rc |= jobs[t].status;
+  free(jobs);
+  free(th);
+  return rc;
+}

@@ -560,7 +560,77 @@ def test_paged_decode_several_new_tokens_is_causal_within_them():
 
 
 # ---------------------------------------------------------------------------
-# 12. Stored oracle values (tests/golden/oracle_tiny.txt, written by
+# 12. Backward pass: gradients of sum(O * dO).
+# ---------------------------------------------------------------------------
+def test_bwd_matches_central_differences_of_the_forward():
+    """Each gradient entry against (f(x + h) - f(x - h)) / 2h of the forward
+    oracle's loss sum(O * dO), in fp64: independent of the backward code."""
+    B, Hq, Hkv, Sq, Sk, D = 1, 2, 1, 5, 7, 4
+    q, k, v = fa_inputs.prefill_inputs(B, Hq, Hkv, Sq, Sk, D, torch.float64, seed=30)
+    dout = torch.randn(B, Sq, Hq, D, generator=torch.Generator().manual_seed(31),
+                       dtype=torch.float64)
+    for causal in (True, False):
+        dq, dk, dv = oracle.attention_bwd(q, k, v, dout, 0.7, causal)
+        loss = lambda q_, k_, v_: float((oracle.attention(q_, k_, v_, 0.7, causal)  # noqa: E731
+                                         * dout.numpy()).sum())
+        h = 1e-5
+        for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+            flat = x.reshape(-1)
+            num = np.zeros(flat.numel())
+            for n in range(flat.numel()):
+                xp, xm = flat.clone(), flat.clone()
+                xp[n] += h
+                xm[n] -= h
+                args = [q, k, v]
+                idx = "qkv".index(name)
+                args[idx] = xp.reshape(x.shape)
+                fp = loss(*args)
+                args[idx] = xm.reshape(x.shape)
+                num[n] = (fp - loss(*args)) / (2 * h)
+            np.testing.assert_allclose(g.reshape(-1), num, rtol=0, atol=1e-7, err_msg=name)
+
+
+def test_bwd_matches_torch_autograd_fp64():
+    """torch CPU fp64 scaled_dot_product_attention + autograd, GQA via
+    repeat_interleave (whose gradient sums a group's heads), bottom-right
+    causal via an explicit mask."""
+    B, Hq, Hkv, Sq, Sk, D = 2, 4, 2, 9, 13, 8
+    q, k, v = fa_inputs.prefill_inputs(B, Hq, Hkv, Sq, Sk, D, torch.bfloat16, seed=32)
+    dout = torch.randn(B, Sq, Hq, D, generator=torch.Generator().manual_seed(33))
+    for causal in (True, False):
+        dq, dk, dv = oracle.attention_bwd(q, k, v, dout, 0.3, causal)
+        qt, kt, vt = (x.to(torch.float64).requires_grad_() for x in (q, k, v))
+        G = Hq // Hkv
+        mask = None
+        if causal:
+            mask = torch.arange(Sk)[None, :] <= torch.arange(Sq)[:, None] + (Sk - Sq)
+        o = torch.nn.functional.scaled_dot_product_attention(
+            qt.permute(0, 2, 1, 3), kt.repeat_interleave(G, 2).permute(0, 2, 1, 3),
+            vt.repeat_interleave(G, 2).permute(0, 2, 1, 3), attn_mask=mask, scale=0.3)
+        (o.permute(0, 2, 1, 3) * dout.to(torch.float64)).sum().backward()
+        np.testing.assert_allclose(dq, qt.grad.numpy(), rtol=0, atol=1e-11)
+        np.testing.assert_allclose(dk, kt.grad.numpy(), rtol=0, atol=1e-11)
+        np.testing.assert_allclose(dv, vt.grad.numpy(), rtol=0, atol=1e-11)
+
+
+def test_bwd_key_gradients_sum_to_zero_and_uniform_value_gradients():
+    """Softmax rows are shift invariant, so sum_j dS_ij = 0 and (non-causal)
+    sum_j dK_j = 0; with Q = 0 every row weights its keys equally, so
+    dV_j = sum_i dO_i / Sk."""
+    B, Hq, Hkv, Sq, Sk, D = 1, 2, 2, 6, 10, 8
+    q, k, v = fa_inputs.prefill_inputs(B, Hq, Hkv, Sq, Sk, D, torch.bfloat16, seed=34)
+    dout = torch.randn(B, Sq, Hq, D, generator=torch.Generator().manual_seed(35))
+    _, dk, _ = oracle.attention_bwd(q, k, v, dout, 0.5, False)
+    np.testing.assert_allclose(dk.sum(axis=1), 0.0, atol=1e-12)
+    q0 = torch.zeros_like(q)
+    _, _, dv = oracle.attention_bwd(q0, k, v, dout, 0.5, False)
+    want = dout.to(torch.float64).numpy().sum(axis=1) / Sk          # [B, Hq, D], Hq == Hkv
+    for j in range(Sk):
+        np.testing.assert_allclose(dv[:, j], want, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# 13. Stored oracle values (tests/golden/oracle_tiny.txt, written by
 #     tests/golden/make_golden.py from the oracle alone): drift guard.
 # ---------------------------------------------------------------------------
 def test_golden_oracle_values_unchanged():

@@ -70,6 +70,15 @@ MUTANTS = [
      "if (lse) *lse = m + log(l);", "if (lse) *lse = m + log(l / (double)n_vis);"),
     ("lse_empty_row_zero",
      "if (lse) *lse = -INFINITY;", "if (lse) *lse = 0.0;"),
+    ("bwd_delta_dropped",
+     "const double ds = pr[j] * (dp[j] - delta);", "const double ds = pr[j] * dp[j];"),
+    ("bwd_key_gradient_unscaled",
+     "dkb[j * kstride + d] += J->scale * ds * qi[d];", "dkb[j * kstride + d] += ds * qi[d];"),
+    ("bwd_value_gradient_uses_dp",
+     "dvb[j * kstride + d] += pr[j] * doi[d];", "dvb[j * kstride + d] += dp[j] * doi[d];"),
+    ("bwd_query_gradient_uses_values",
+     "dqi[d] += J->scale * ds * kb[j * kstride + d];",
+     "dqi[d] += J->scale * ds * vb[j * kstride + d];"),
 ]
 
 PIN_ARGS = ["-m", "pytest", os.path.join(ROOT, "tests", "test_oracle.py"), "-x", "-q",
