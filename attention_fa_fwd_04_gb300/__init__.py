@@ -7,7 +7,7 @@ no fallback: if the library is missing or cannot be loaded, every call raises.
 Raw entry points (same names and argument order as the C ABI; pointers are
 integers, ``stream`` a ``cudaStream_t`` value):
     fa_prefill_fwd, fa_prefill_fwd_lse, fa_prefill_varlen_fwd, fa_decode_fwd, fa_decode_fwd_lse,
-    fa_decode_paged_fwd,
+    fa_decode_paged_fwd, fa_backward,
     fa_decode_fwd_noalloc, fa_status_string, fa_device_error, fa_last_cuda_error,
     fa_num_sms, fa_prefill_work_item
 Tensor conveniences (contiguous CUDA tensors, caller-owned outputs):
@@ -17,6 +17,7 @@ Tensor conveniences (contiguous CUDA tensors, caller-owned outputs):
     decode(q, kcache, vcache, valid_len, scale, out=None, stream=None, lse=None)
     decode_paged(q, kpages, vpages, page_table, seqlens, scale, out=None, stream=None,
                  lse=None)
+    backward(q, k, v, o, dout, lse, scale, causal, stream=None) -> (dq, dk, dv)
     (lse=True allocates the fp32 log-sum-exp output; a tensor is used as is.)
 """
 import ctypes
@@ -32,7 +33,7 @@ FA_ERR_BOUNDS = 6
 
 # Every symbol include/fa.h declares (checked by the tests against the header).
 EXPORTS = ("fa_prefill_fwd", "fa_prefill_fwd_lse", "fa_prefill_varlen_fwd", "fa_decode_fwd",
-           "fa_decode_fwd_lse", "fa_decode_paged_fwd",
+           "fa_decode_fwd_lse", "fa_decode_paged_fwd", "fa_backward",
            "fa_decode_fwd_noalloc", "fa_status_string", "fa_device_error", "fa_last_cuda_error",
            "fa_num_sms", "fa_prefill_work_item")
 
@@ -75,6 +76,9 @@ def load(path: str = LIB_PATH):
     lib.fa_decode_paged_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
                                         i32, i32, f32, vp]
     lib.fa_decode_paged_fwd.restype = i32
+    lib.fa_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
+                                f32, i32, i32, vp]
+    lib.fa_backward.restype = i32
     lib.fa_decode_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp]
     lib.fa_decode_fwd_noalloc.restype = i32
     lib.fa_status_string.argtypes = [i32]
@@ -361,3 +365,34 @@ def decode_paged(q, kpages, vpages, page_table, seqlens, scale, out=None, stream
     if st != FA_OK:
         raise FAError(st, "fa_decode_paged_fwd")
     return (out, lse) if lse_ptr else out
+
+
+def fa_backward(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, Sq, Sk, D, scale, causal, dtype,
+                stream):
+    return load().fa_backward(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, Sq, Sk, D, scale,
+                              causal, dtype, stream)
+
+
+def backward(q, k, v, o, dout, lse, scale, causal, stream=None):
+    """Gradients (dq, dk, dv) of sum(o * dout) for the forward call that
+    produced o and lse (fa_prefill_fwd_lse).  q/o/dout [B,Sq,Hq,D], k/v
+    [B,Sk,Hkv,D] contiguous CUDA tensors of one dtype; lse float32
+    [B,Hq,Sq]."""
+    import torch
+    B, Sq, Hq, D = q.shape
+    _, Sk, Hkv, _ = k.shape
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dout, "dout"), (lse, "lse")):
+        _check(t, n)
+    if tuple(o.shape) != tuple(q.shape) or tuple(dout.shape) != tuple(q.shape) or \
+            tuple(v.shape) != tuple(k.shape) or tuple(lse.shape) != (B, Hq, Sq):
+        raise ValueError("shape mismatch among q, k, v, o, dout, lse")
+    if lse.dtype != torch.float32:
+        raise TypeError("lse must be float32")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    st = fa_backward(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
+                     lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv, Sq,
+                     Sk, D, float(scale), int(bool(causal)), _dtype_code(q),
+                     _stream_handle(stream))
+    if st != FA_OK:
+        raise FAError(st, "fa_backward")
+    return dq, dk, dv

@@ -143,6 +143,47 @@ extern "C" int fa_prefill_varlen_fwd(const void* q, const void* k, const void* v
                      "prefill varlen launch");
 }
 
+extern "C" int fa_backward(const void* q, const void* k, const void* v, const void* o,
+                           const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                           int B, int Hq, int Hkv, int Sq, int Sk, int D, float scale,
+                           int causal, int dtype, cudaStream_t stream) {
+  if (B < 0 || Hq < 0 || Hkv < 0 || Sq < 0 || Sk < 0) return FA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return FA_ERR_INVALID_ARG;
+  if (dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_INVALID_ARG;
+  if (!isfinite(scale)) return FA_ERR_INVALID_ARG;
+  if (B == 0 || Hq == 0) return FA_OK;
+  if (Hkv == 0 || Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
+  if (Sq > 0 && (!q || !o || !dout || !dq || !lse || !aligned16(q) || !aligned16(o) ||
+                 !aligned16(dout) || !aligned16(dq) || !aligned4(lse)))
+    return FA_ERR_INVALID_ARG;
+  if (Sk > 0 && (!k || !v || !dk || !dv || !aligned16(k) || !aligned16(v) || !aligned16(dk) ||
+                 !aligned16(dv)))
+    return FA_ERR_INVALID_ARG;
+  const int64_t items_q = (int64_t)B * Hq * ((Sq + 127) / 128);
+  const int64_t items_k = (int64_t)B * Hkv * ((Sk + 127) / 128);
+  if (items_q > INT32_MAX || items_k > INT32_MAX) return FA_ERR_INVALID_ARG;
+  if ((int64_t)Sq * Hq * D * 2 >= (1ll << 40) || (int64_t)Sk * Hkv * D * 2 >= (1ll << 40))
+    return FA_ERR_INVALID_ARG;
+  // No key: dQ = 0 (and no dK, dV rows).  No query row: dK = dV = 0.
+  if (Sq == 0 || Sk == 0) {
+    cudaError_t e = cudaSuccess;
+    if (Sk == 0 && Sq > 0) e = cudaMemsetAsync(dq, 0, (size_t)B * Sq * Hq * D * 2, stream);
+    if (e == cudaSuccess && Sq == 0 && Sk > 0) {
+      e = cudaMemsetAsync(dk, 0, (size_t)B * Sk * Hkv * D * 2, stream);
+      if (e == cudaSuccess) e = cudaMemsetAsync(dv, 0, (size_t)B * Sk * Hkv * D * 2, stream);
+    }
+    return cuda_status(e, "backward zero-fill");
+  }
+  void* delta = nullptr;
+  cudaError_t e = cudaMallocAsync(&delta, (size_t)B * Hq * Sq * sizeof(float), stream);
+  if (e != cudaSuccess) return cuda_status(e, "backward cudaMallocAsync");
+  int r = fa::launch_backward(q, k, v, o, dout, lse, dq, dk, dv, static_cast<float*>(delta), B,
+                              Hq, Hkv, Sq, Sk, D, scale, causal, dtype == FA_BF16, stream);
+  cudaError_t ef = cudaFreeAsync(delta, stream);
+  if (r != 0) return cuda_status(r, "backward launch");
+  return cuda_status(ef, "backward cudaFreeAsync");
+}
+
 static int decode_impl(const void* q, const void* kcache, const void* vcache,
                        const int32_t* valid_len_dev, void* o, float* lse, bool want_lse, int B,
                        int Hq, int Hkv, int cap, int D, float scale, cudaStream_t stream) {
@@ -254,9 +295,11 @@ extern "C" const char* fa_status_string(int status) {
 
 extern "C" int fa_device_error(int reset, unsigned int* detail) {
   if (cudaDeviceSynchronize() != cudaSuccess) return FA_ERR_CUDA;
-  unsigned int a = 0, b = 0;
+  unsigned int a = 0, b = 0, c = 0;
   if (fa::read_prefill_error(&a, reset) != 0) return FA_ERR_CUDA;
   if (fa::read_decode_error(&b, reset) != 0) return FA_ERR_CUDA;
+  if (fa::read_backward_error(&c, reset) != 0) return FA_ERR_CUDA;
+  a |= c;  // the backward kernels report in the prefill half
   if (detail) *detail = (a & 0xFFFFu) | (b << 16);
   if ((a | b) & 1u) return FA_ERR_TIMEOUT;
   return (a | b) ? FA_ERR_BOUNDS : FA_OK;

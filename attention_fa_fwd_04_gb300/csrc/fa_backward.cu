@@ -1,0 +1,859 @@
+// fa_backward.cu -- attention backward pass on the 5th-generation tensor cores.
+//
+// Gradients of the loss l = sum(O * dO) with respect to Q, K and V, in the
+// three passes of the flash-attention backward commit note of tessera #90
+// ("compiler-generated flash_attn fwd+bwd"):
+//   pre :  Delta_i = sum_d dO_id O_id                       (per query row)
+//   dq  :  per 128-row query tile, over its visible key tiles:
+//            S = Q K^T, P = exp(scale S - lse), dP = dO V^T,
+//            dS = P * (dP - Delta),  dQ += scale * dS K
+//   dkdv:  per 128-key tile, over the query tiles (and query heads of the
+//          GQA group) that see it:
+//            S^T = K Q^T, P^T, dP^T = V dO^T, dS^T = P^T * (dP^T - Delta),
+//            dV += P^T dO,  dK += scale * dS^T Q
+// lse is the forward pass's per-row log-sum-exp (fa_prefill_fwd_lse), so P is
+// recomputed exactly as the forward computed it, with no row max or sum.
+//
+// Both tensor-core kernels are persistent (one CTA per SM) and
+// warp-specialised: warps 0-3 turn the S / dP accumulators into dS (and P)
+// one TMEM lane per thread and write the results back into TMEM as the next
+// MMA's A operand; warp 4 issues TMA tile loads; warp 5 allocates TMEM and
+// issues tcgen05.mma.  All waits are bounded (see fa_ptx.cuh).
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <math.h>
+
+#include "fa_internal.h"
+#include "fa_ptx.cuh"
+
+namespace fa {
+
+__device__ unsigned int g_backward_err = 0;
+
+namespace bw {
+constexpr int BT = 128;                // rows of every tile
+constexpr int HALF_BYTES = 128 * 128;  // 128 rows x 64 elements x 2 bytes
+constexpr int THREADS = 192;           // warps 0-3 elementwise, 4 producer, 5 MMA
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t COL_S = 0, COL_DP = 128, COL_ACC = 256;
+constexpr float LOG2E = 1.4426950408889634f;
+
+template <int D>
+struct Cfg {
+  static constexpr int HALVES = D / 64;
+  static constexpr int TILE_BYTES = HALVES * HALF_BYTES;  // one 128-row tile
+  static constexpr int NSTAGE_DQ = 4;    // K/V ring of the dq kernel (K_j, V_j alternate)
+  static constexpr int NSTAGE_DKV = 2;   // (Q, dO) ring of the dkdv kernel
+  static constexpr int SMEM_BAR = 512;
+  static constexpr int SMEM_DQ = 1024 + 2 * TILE_BYTES + NSTAGE_DQ * TILE_BYTES + SMEM_BAR;
+  // dkdv stage: Q tile, dO tile, then lse*log2(e) and Delta of its 128 rows.
+  static constexpr int STAGE_DKV = 2 * TILE_BYTES + 2 * BT * 4;
+  static constexpr int SMEM_DKV = 1024 + 2 * TILE_BYTES + NSTAGE_DKV * STAGE_DKV + SMEM_BAR;
+};
+}  // namespace bw
+
+struct BwdParams {
+  void* dq;             // [B, Sq, Hq, D]
+  void* dk;             // [B, Sk, Hkv, D]
+  void* dv;             // [B, Sk, Hkv, D]
+  const float* lse;     // [B, Hq, Sq] natural log
+  const float* delta;   // [B, Hq, Sq]
+  int B, Hq, Hkv, Sq, Sk, G, causal;
+  int n_qt, n_kt, n_items;
+  float c;              // scale * log2(e)
+  float scale;
+};
+
+template <typename T>
+struct BPack;
+template <>
+struct BPack<__nv_bfloat16> {
+  static __device__ __forceinline__ uint32_t pack(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+  static __device__ __forceinline__ float2 unpack(uint32_t u) {
+    __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&u);
+    return __bfloat1622float2(v);
+  }
+};
+template <>
+struct BPack<__half> {
+  static __device__ __forceinline__ uint32_t pack(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+  static __device__ __forceinline__ float2 unpack(uint32_t u) {
+    __half2 v = *reinterpret_cast<__half2*>(&u);
+    return __half22float2(v);
+  }
+};
+template <typename T>
+struct BIsBF16 {
+  static constexpr bool value = false;
+};
+template <>
+struct BIsBF16<__nv_bfloat16> {
+  static constexpr bool value = true;
+};
+
+// ------------------------------------------------------------------------------
+// pre: Delta[b, h, i] = sum_d dO[b,i,h,d] * O[b,i,h,d], one warp per row.
+// ------------------------------------------------------------------------------
+template <int D, typename T>
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const T* __restrict__ o,
+                                                      const T* __restrict__ dout,
+                                                      float* __restrict__ delta, int B, int Sq,
+                                                      int Hq) {
+  const size_t rows = (size_t)B * Sq * Hq;
+  const int lane = threadIdx.x & 31;
+  for (size_t r = (blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5; r < rows;
+       r += ((size_t)gridDim.x * blockDim.x) >> 5) {
+    // r indexes [B, Sq, Hq] rows of O; Delta is stored [B, Hq, Sq].
+    const size_t h = r % Hq, bi = r / Hq, i = bi % Sq, b = bi / Sq;
+    float acc = 0.f;
+    // D / 64 pairs of bf16x2 per lane (D = 64: 1, D = 128: 2)
+#pragma unroll
+    for (int x = 0; x < D / 64; ++x) {
+      const uint32_t a = reinterpret_cast<const uint32_t*>(o + r * D)[x * 32 + lane];
+      const uint32_t g = reinterpret_cast<const uint32_t*>(dout + r * D)[x * 32 + lane];
+      const float2 fa = BPack<T>::unpack(a), fg = BPack<T>::unpack(g);
+      acc += fa.x * fg.x + fa.y * fg.y;
+    }
+#pragma unroll
+    for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+    if (lane == 0) delta[(b * Hq + h) * Sq + i] = acc;
+  }
+}
+
+// Work items.  dq: (b, hq, query tile), kv-head-major, longest causal tiles
+// first.  dkdv: (b, hkv, key tile), kv-head-major, key tiles ascending (the
+// ones seen by the most query tiles first).
+__device__ __forceinline__ void dq_item(int w, const BwdParams& p, int* b, int* hq, int* qt) {
+  const int per_b = p.n_qt * p.G, per_kv = p.B * per_b;
+  const int hkv = w / per_kv;
+  int r = w - hkv * per_kv;
+  *b = r / per_b;
+  r -= *b * per_b;
+  const int qr = r / p.G;
+  *hq = hkv * p.G + (r - qr * p.G);
+  *qt = p.n_qt - 1 - qr;
+}
+__device__ __forceinline__ void dkv_item(int w, const BwdParams& p, int* b, int* hkv, int* kt) {
+  const int per_kv = p.B * p.n_kt;
+  *hkv = w / per_kv;
+  const int r = w - *hkv * per_kv;
+  *b = r / p.n_kt;
+  *kt = r - *b * p.n_kt;
+}
+// Key tiles seen by query tile rows [r0, r0 + 128).
+__device__ __forceinline__ int bw_key_tiles(int r0, const BwdParams& p) {
+  if (r0 >= p.Sq || p.Sk <= 0) return 0;
+  int nk = p.Sk;
+  if (p.causal) {
+    const int last = (r0 + bw::BT - 1 < p.Sq - 1 ? r0 + bw::BT - 1 : p.Sq - 1) + (p.Sk - p.Sq);
+    nk = last + 1 < p.Sk ? last + 1 : p.Sk;
+    if (nk <= 0) return 0;
+  }
+  return (nk + bw::BT - 1) / bw::BT;
+}
+// First query tile that sees key tile rows [k0, k0 + 128) (n_qt if none).
+__device__ __forceinline__ int bw_first_query_tile(int k0, const BwdParams& p) {
+  if (!p.causal) return 0;
+  const int i0 = k0 - (p.Sk - p.Sq);  // the first query row that sees key k0
+  if (i0 >= p.Sq) return p.n_qt;
+  return i0 <= 0 ? 0 : i0 / bw::BT;
+}
+
+// ------------------------------------------------------------------------------
+// dq
+// ------------------------------------------------------------------------------
+template <int D, typename T>
+__global__ void __launch_bounds__(bw::THREADS, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                  const BwdParams p) {
+  using C = bw::Cfg<D>;
+  constexpr bool kBF16 = BIsBF16<T>::value;
+  constexpr int NS = C::NSTAGE_DQ;
+  constexpr float NEG_INF = -INFINITY;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint8_t* sQ = smem;
+  uint8_t* sDO = smem + C::TILE_BYTES;
+  uint8_t* sKV = smem + 2 * C::TILE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + NS * C::TILE_BYTES);
+  uint64_t* full = bars;            // [NS]
+  uint64_t* empty = bars + NS;      // [NS]
+  uint64_t* q_full = bars + 2 * NS;
+  uint64_t* q_empty = q_full + 1;
+  uint64_t* s_full = q_full + 2;    // S and dP in TMEM
+  uint64_t* ds_full = q_full + 3;   // dS in TMEM (128 arrivals)
+  uint64_t* o_full = q_full + 4;    // dQ complete
+  uint64_t* drain = q_full + 5;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(q_full + 6);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
+    mbar_init(s_full, 1);
+    mbar_init(ds_full, bw::BT);
+    mbar_init(o_full, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(tmem_holder, bw::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const bool leader = lane == 0;
+  const int off = p.Sk - p.Sq;
+
+  if (warp == 4) {
+    // ================================ producer ================================
+    if (leader) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmDO);
+    }
+    const uint64_t pol_q = l2_policy_evict_first();
+    const uint64_t pol_kv = l2_policy_evict_last();
+    uint32_t kv_cnt = 0, local = 0;
+    bool ok = true, q_issued = false;
+    for (int w = blockIdx.x; w < p.n_items && ok; w += gridDim.x, ++local) {
+      int b, hq, qt;
+      dq_item(w, p, &b, &hq, &qt);
+      const int hkv = hq / p.G;
+      const int n = bw_key_tiles(qt * bw::BT, p);
+      q_issued = false;
+      if (local > 0 && !(ok = mbar_wait(q_empty, (local - 1) & 1, abort_flag, &g_backward_err, 1)))
+        break;
+      if (leader) {
+        mbar_arrive_expect_tx(q_full, 2 * C::TILE_BYTES);
+#pragma unroll
+        for (int h = 0; h < C::HALVES; ++h) {
+          tma_load_4d_hint(sQ + h * bw::HALF_BYTES, &tmQ, q_full, h * 64, hq, qt * bw::BT, b, pol_q);
+          tma_load_4d_hint(sDO + h * bw::HALF_BYTES, &tmDO, q_full, h * 64, hq, qt * bw::BT, b,
+                           pol_q);
+        }
+      }
+      __syncwarp();
+      q_issued = true;
+      for (int j = 0; j < n && ok; ++j) {
+#pragma unroll
+        for (int sel = 0; sel < 2; ++sel) {  // K_j, then V_j
+          const int s = kv_cnt % NS;
+          const uint32_t ph = (kv_cnt / NS) & 1;
+          if (!(ok = mbar_wait(&empty[s], ph ^ 1, abort_flag, &g_backward_err, 2))) break;
+          if (leader) {
+            mbar_arrive_expect_tx(&full[s], C::TILE_BYTES);
+            const CUtensorMap* m = sel ? &tmV : &tmK;
+#pragma unroll
+            for (int h = 0; h < C::HALVES; ++h)
+              tma_load_4d_hint(sKV + s * C::TILE_BYTES + h * bw::HALF_BYTES, m, &full[s], h * 64,
+                               hkv, j * bw::BT, b, pol_kv);
+          }
+          __syncwarp();
+          ++kv_cnt;
+        }
+      }
+    }
+    if (!ok) {
+      const uint32_t first = kv_cnt > (uint32_t)NS ? kv_cnt - NS : 0u;
+      for (uint32_t u = first; u < kv_cnt; ++u) mbar_wait_drain(&full[u % NS], (u / NS) & 1);
+      if (q_issued) mbar_wait_drain(q_full, local & 1);
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    // ================================== MMA ===================================
+    constexpr uint32_t IDESC_S = idesc_f16(bw::BT, bw::BT, kBF16, false);
+    constexpr uint32_t IDESC_ACC = idesc_f16(bw::BT, D, kBF16, true);
+    const uint32_t sq_addr = smem_u32(sQ), sdo_addr = smem_u32(sDO), skv_addr = smem_u32(sKV);
+    uint32_t kv_cnt = 0, local = 0, ds_cnt = 0;
+    bool ok = true;
+    // D_tmem = A (K-major smem) x B^T (K-major smem) over D/16 k-steps.
+    auto issue_nt = [&](uint32_t d_col, uint32_t a_addr, uint32_t b_addr) {
+      if (leader) {
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t hoff = (k >> 2) * bw::HALF_BYTES + (k & 3) * 32;
+          mma_ss(tmem + d_col, sdesc_sw128(a_addr + hoff, 16, 1024),
+                 sdesc_sw128(b_addr + hoff, 16, 1024), IDESC_S, k > 0 ? 1u : 0u);
+        }
+      }
+      __syncwarp();
+    };
+    auto commit = [&](uint64_t* bar) {
+      if (leader) mma_commit(bar);
+      __syncwarp();
+    };
+    auto ring_wait = [&](uint32_t idx, unsigned int site) {
+      const bool r =
+          mbar_wait(&full[idx % NS], (idx / NS) & 1, abort_flag, &g_backward_err, site);
+      tc_fence_after();
+      return r;
+    };
+    for (int w = blockIdx.x; w < p.n_items && ok; w += gridDim.x, ++local) {
+      int b, hq, qt;
+      dq_item(w, p, &b, &hq, &qt);
+      const int n = bw_key_tiles(qt * bw::BT, p);
+      if (!(ok = mbar_wait(q_full, local & 1, abort_flag, &g_backward_err, 3))) break;
+      tc_fence_after();
+      if (n == 0) {
+        commit(q_empty);
+        commit(o_full);  // dQ = 0 for this tile (accumulator not written)
+        continue;
+      }
+      const uint32_t kb = kv_cnt;
+      kv_cnt += 2 * n;
+      for (int j = 0; j < n && ok; ++j) {
+        const uint32_t iK = kb + 2 * j, iV = iK + 1;
+        if (!(ok = ring_wait(iK, 4))) break;
+        issue_nt(bw::COL_S, sq_addr, skv_addr + (iK % NS) * C::TILE_BYTES);   // S = Q K_j^T
+        if (!(ok = ring_wait(iV, 5))) break;
+        issue_nt(bw::COL_DP, sdo_addr, skv_addr + (iV % NS) * C::TILE_BYTES); // dP = dO V_j^T
+        commit(s_full);
+        commit(&empty[iV % NS]);
+        if (j == n - 1) commit(q_empty);
+        if (!(ok = mbar_wait(ds_full, ds_cnt & 1, abort_flag, &g_backward_err, 6))) break;
+        ++ds_cnt;
+        tc_fence_after();
+        // dQ += dS K_j: dS (16-bit, TMEM columns [0, 64)), K_j MN-major.
+        if (leader) {
+#pragma unroll
+          for (int k = 0; k < bw::BT / 16; ++k) {
+            const uint64_t bd = sdesc_sw128(skv_addr + (iK % NS) * C::TILE_BYTES + k * 16 * 128,
+                                            bw::HALF_BYTES, 1024);
+            mma_ts(tmem + bw::COL_ACC, tmem + bw::COL_S + k * 8, bd, IDESC_ACC,
+                   (j > 0 || k > 0) ? 1u : 0u);
+          }
+        }
+        __syncwarp();
+        commit(&empty[iK % NS]);
+      }
+      commit(o_full);
+    }
+    commit(drain);
+    mbar_wait_drain(drain, 0);
+    __syncwarp();
+  } else {
+    // ============================ dS (warps 0-3) ============================
+    const int r = warp * 32 + lane;  // TMEM lane = query row within the tile
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    uint32_t s_cnt = 0, o_cnt = 0;
+    bool ok = true;
+    T* const DQ = static_cast<T*>(p.dq);
+    for (int w = blockIdx.x; w < p.n_items && ok; w += gridDim.x) {
+      int b, hq, qt;
+      dq_item(w, p, &b, &hq, &qt);
+      const int n = bw_key_tiles(qt * bw::BT, p);
+      const int i = qt * bw::BT + r;  // query row
+      const bool row_ok = i < p.Sq;
+      const size_t lrow = ((size_t)b * p.Hq + hq) * p.Sq + (row_ok ? i : 0);
+      const float l2 = row_ok ? p.lse[lrow] * bw::LOG2E : 0.f;
+      const float dl = row_ok ? p.delta[lrow] : 0.f;
+      const bool any_key = row_ok && p.lse[lrow] != NEG_INF;
+      const int lim_c = p.causal ? i + off + 1 : p.Sk;  // keys [0, lim) visible
+      const int lim = any_key ? (lim_c < p.Sk ? lim_c : p.Sk) : 0;
+      for (int j = 0; j < n && ok; ++j) {
+        if (!(ok = mbar_wait(s_full, s_cnt & 1, abort_flag, &g_backward_err, 7))) break;
+        ++s_cnt;
+        __syncwarp();
+        tc_fence_after();
+        const int k0 = j * bw::BT;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint32_t sr[32], pr[32];
+          tmem_ld32(t_lane + bw::COL_S + q4 * 32, sr);
+          tmem_ld32(t_lane + bw::COL_DP + q4 * 32, pr);
+          tmem_wait_ld();
+          reg_fence32(sr);
+          reg_fence32(pr);
+          uint32_t pk[16];
+#pragma unroll
+          for (int x = 0; x < 16; ++x) {
+            float ds[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int key = k0 + q4 * 32 + 2 * x + e;
+              const float pv = key < lim
+                                   ? fast_exp2(__uint_as_float(sr[2 * x + e]) * p.c - l2)
+                                   : 0.f;
+              ds[e] = pv * (__uint_as_float(pr[2 * x + e]) - dl);
+            }
+            pk[x] = BPack<T>::pack(ds[0], ds[1]);
+          }
+          tmem_st16(t_lane + bw::COL_S + q4 * 16, pk);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(ds_full);
+      }
+      if (!ok) break;
+      // Epilogue: dQ = scale * accumulator, rounded once.
+      if (!(ok = mbar_wait(o_full, o_cnt & 1, abort_flag, &g_backward_err, 8))) break;
+      ++o_cnt;
+      __syncwarp();
+      tc_fence_after();
+      T* const drow = DQ + (((size_t)b * p.Sq + (row_ok ? i : 0)) * p.Hq + hq) * D;
+#pragma unroll
+      for (int q4 = 0; q4 < D / 32; ++q4) {
+        uint32_t ar[32];
+        if (n > 0) {
+          tmem_ld32(t_lane + bw::COL_ACC + q4 * 32, ar);
+          tmem_wait_ld();
+          reg_fence32(ar);
+        } else {
+#pragma unroll
+          for (int x = 0; x < 32; ++x) ar[x] = 0u;
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int x = 0; x < 16; ++x)
+          pk[x] = BPack<T>::pack(__uint_as_float(ar[2 * x]) * p.scale,
+                                 __uint_as_float(ar[2 * x + 1]) * p.scale);
+        if (row_ok) {
+          if (b >= p.B || hq >= p.Hq) {
+            atomicOr(&g_backward_err, kErrBounds);
+            continue;
+          }
+          uint4* dst = reinterpret_cast<uint4*>(drow + q4 * 32);
+#pragma unroll
+          for (int x = 0; x < 4; ++x)
+            dst[x] = make_uint4(pk[4 * x], pk[4 * x + 1], pk[4 * x + 2], pk[4 * x + 3]);
+        }
+      }
+      tc_fence_before();
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, bw::TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------------------
+// dk, dv
+// ------------------------------------------------------------------------------
+template <int D, typename T>
+__global__ void __launch_bounds__(bw::THREADS, 1)
+    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ,
+                    const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV,
+                    const __grid_constant__ CUtensorMap tmDO, const BwdParams p) {
+  using C = bw::Cfg<D>;
+  constexpr bool kBF16 = BIsBF16<T>::value;
+  constexpr int NS = C::NSTAGE_DKV;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint8_t* sK = smem;
+  uint8_t* sV = smem + C::TILE_BYTES;
+  uint8_t* sStage = smem + 2 * C::TILE_BYTES;  // [NS] x (Q, dO, lse*log2e, Delta)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sStage + NS * C::STAGE_DKV);
+  uint64_t* full = bars;          // [NS]
+  uint64_t* empty = bars + NS;    // [NS]: MMA commit + 128 elementwise arrivals
+  uint64_t* kv_full = bars + 2 * NS;
+  uint64_t* kv_empty = kv_full + 1;
+  uint64_t* st_full = kv_full + 2;  // S^T and dP^T in TMEM
+  uint64_t* pd_full = kv_full + 3;  // P^T and dS^T in TMEM (128 arrivals)
+  uint64_t* o_full = kv_full + 4;   // dK, dV complete
+  uint64_t* drain = kv_full + 5;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(kv_full + 6);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    // full[s]: the producer arrives twice per phase (with the tile bytes
+    // expected, then after writing the stage's lse / Delta rows).
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full[s], 2);
+      mbar_init(&empty[s], 1 + bw::BT);
+    }
+    mbar_init(kv_full, 1);
+    mbar_init(kv_empty, 1);
+    mbar_init(st_full, 1);
+    mbar_init(pd_full, bw::BT);
+    mbar_init(o_full, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(tmem_holder, bw::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const bool leader = lane == 0;
+  const int off = p.Sk - p.Sq;
+
+  if (warp == 4) {
+    // ================================ producer ================================
+    if (leader) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmDO);
+    }
+    const uint64_t pol_kv = l2_policy_evict_first();
+    const uint64_t pol_q = l2_policy_evict_last();
+    uint32_t st_cnt = 0, local = 0;
+    bool ok = true, kv_issued = false;
+    for (int w = blockIdx.x; w < p.n_items && ok; w += gridDim.x, ++local) {
+      int b, hkv, kt;
+      dkv_item(w, p, &b, &hkv, &kt);
+      const int t0 = bw_first_query_tile(kt * bw::BT, p);
+      kv_issued = false;
+      if (local > 0 &&
+          !(ok = mbar_wait(kv_empty, (local - 1) & 1, abort_flag, &g_backward_err, 1)))
+        break;
+      if (leader) {
+        mbar_arrive_expect_tx(kv_full, 2 * C::TILE_BYTES);
+#pragma unroll
+        for (int h = 0; h < C::HALVES; ++h) {
+          tma_load_4d_hint(sK + h * bw::HALF_BYTES, &tmK, kv_full, h * 64, hkv, kt * bw::BT, b,
+                           pol_kv);
+          tma_load_4d_hint(sV + h * bw::HALF_BYTES, &tmV, kv_full, h * 64, hkv, kt * bw::BT, b,
+                           pol_kv);
+        }
+      }
+      __syncwarp();
+      kv_issued = true;
+      for (int g = 0; g < p.G && ok; ++g) {
+        const int hq = hkv * p.G + g;
+        for (int t = t0; t < p.n_qt && ok; ++t) {
+          const int s = st_cnt % NS;
+          const uint32_t ph = (st_cnt / NS) & 1;
+          if (!(ok = mbar_wait(&empty[s], ph ^ 1, abort_flag, &g_backward_err, 2))) break;
+          uint8_t* st = sStage + s * C::STAGE_DKV;
+          float* sL = reinterpret_cast<float*>(st + 2 * C::TILE_BYTES);
+          float* sD = sL + bw::BT;
+          if (leader) {
+            mbar_arrive_expect_tx(&full[s], 2 * C::TILE_BYTES);
+#pragma unroll
+            for (int h = 0; h < C::HALVES; ++h) {
+              tma_load_4d_hint(st + h * bw::HALF_BYTES, &tmQ, &full[s], h * 64, hq, t * bw::BT, b,
+                               pol_q);
+              tma_load_4d_hint(st + C::TILE_BYTES + h * bw::HALF_BYTES, &tmDO, &full[s], h * 64,
+                               hq, t * bw::BT, b, pol_q);
+            }
+          }
+          // lse * log2(e) and Delta of the tile's 128 query rows (+inf / 0 past Sq:
+          // those columns get P = 0).
+          const size_t base = ((size_t)b * p.Hq + hq) * p.Sq;
+#pragma unroll
+          for (int x = 0; x < 4; ++x) {
+            const int i = t * bw::BT + x * 32 + lane;
+            sL[x * 32 + lane] = i < p.Sq ? p.lse[base + i] * bw::LOG2E : INFINITY;
+            sD[x * 32 + lane] = i < p.Sq ? p.delta[base + i] : 0.f;
+          }
+          __syncwarp();
+          if (leader) mbar_arrive(&full[s]);  // the second arrival, after the smem writes
+          __syncwarp();
+          ++st_cnt;
+        }
+      }
+    }
+    if (!ok) {
+      const uint32_t first = st_cnt > (uint32_t)NS ? st_cnt - NS : 0u;
+      for (uint32_t u = first; u < st_cnt; ++u) mbar_wait_drain(&full[u % NS], (u / NS) & 1);
+      if (kv_issued) mbar_wait_drain(kv_full, local & 1);
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    // ================================== MMA ===================================
+    constexpr uint32_t IDESC_S = idesc_f16(bw::BT, bw::BT, kBF16, false);
+    constexpr uint32_t IDESC_ACC = idesc_f16(bw::BT, D, kBF16, true);
+    const uint32_t sk_addr = smem_u32(sK), sv_addr = smem_u32(sV), sst = smem_u32(sStage);
+    uint32_t st_cnt = 0, local = 0, pd_cnt = 0;
+    bool ok = true;
+    auto issue_nt = [&](uint32_t d_col, uint32_t a_addr, uint32_t b_addr) {
+      if (leader) {
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t hoff = (k >> 2) * bw::HALF_BYTES + (k & 3) * 32;
+          mma_ss(tmem + d_col, sdesc_sw128(a_addr + hoff, 16, 1024),
+                 sdesc_sw128(b_addr + hoff, 16, 1024), IDESC_S, k > 0 ? 1u : 0u);
+        }
+      }
+      __syncwarp();
+    };
+    // acc += A (TMEM, 16-bit, columns a_col..) x B (MN-major smem tile).
+    auto issue_acc = [&](uint32_t d_col, uint32_t a_col, uint32_t b_addr, bool accumulate) {
+      if (leader) {
+#pragma unroll
+        for (int k = 0; k < bw::BT / 16; ++k) {
+          const uint64_t bd = sdesc_sw128(b_addr + k * 16 * 128, bw::HALF_BYTES, 1024);
+          mma_ts(tmem + d_col, tmem + a_col + k * 8, bd, IDESC_ACC,
+                 (accumulate || k > 0) ? 1u : 0u);
+        }
+      }
+      __syncwarp();
+    };
+    auto commit = [&](uint64_t* bar) {
+      if (leader) mma_commit(bar);
+      __syncwarp();
+    };
+    for (int w = blockIdx.x; w < p.n_items && ok; w += gridDim.x, ++local) {
+      int b, hkv, kt;
+      dkv_item(w, p, &b, &hkv, &kt);
+      const int t0 = bw_first_query_tile(kt * bw::BT, p);
+      const int steps = p.G * (p.n_qt - t0);
+      if (!(ok = mbar_wait(kv_full, local & 1, abort_flag, &g_backward_err, 3))) break;
+      tc_fence_after();
+      for (int u = 0; u < steps && ok; ++u) {
+        const int s = st_cnt % NS;
+        const uint32_t ph = (st_cnt / NS) & 1;
+        ++st_cnt;
+        if (!(ok = mbar_wait(&full[s], ph, abort_flag, &g_backward_err, 4))) break;
+        tc_fence_after();
+        const uint32_t sq = sst + s * C::STAGE_DKV, sdo = sq + C::TILE_BYTES;
+        issue_nt(bw::COL_S, sk_addr, sq);    // S^T = K Q^T
+        issue_nt(bw::COL_DP, sv_addr, sdo);  // dP^T = V dO^T
+        commit(st_full);
+        if (!(ok = mbar_wait(pd_full, pd_cnt & 1, abort_flag, &g_backward_err, 5))) break;
+        ++pd_cnt;
+        tc_fence_after();
+        issue_acc(bw::COL_ACC, bw::COL_S, sdo, u > 0);      // dV += P^T dO
+        issue_acc(bw::COL_ACC + D, bw::COL_DP, sq, u > 0);  // dK += dS^T Q
+        commit(&empty[s]);
+      }
+      commit(kv_empty);
+      commit(o_full);
+    }
+    commit(drain);
+    mbar_wait_drain(drain, 0);
+    __syncwarp();
+  } else {
+    // ======================= P^T and dS^T (warps 0-3) =======================
+    const int r = warp * 32 + lane;  // TMEM lane = key row within the tile
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    uint32_t st_cnt = 0, ph_cnt = 0, o_cnt = 0;
+    bool ok = true;
+    T* const DK = static_cast<T*>(p.dk);
+    T* const DV = static_cast<T*>(p.dv);
+    for (int w = blockIdx.x; w < p.n_items && ok; w += gridDim.x) {
+      int b, hkv, kt;
+      dkv_item(w, p, &b, &hkv, &kt);
+      const int t0 = bw_first_query_tile(kt * bw::BT, p);
+      const int j = kt * bw::BT + r;  // key row
+      for (int g = 0; g < p.G && ok; ++g) {
+        for (int t = t0; t < p.n_qt && ok; ++t) {
+          const int s = ph_cnt % NS;
+          const uint32_t fph = (ph_cnt / NS) & 1;
+          ++ph_cnt;
+          // The stage's lse / Delta rows are written by the producer before
+          // its arrival on full[s].
+          if (!(ok = mbar_wait(&full[s], fph, abort_flag, &g_backward_err, 9))) break;
+          if (!(ok = mbar_wait(st_full, st_cnt & 1, abort_flag, &g_backward_err, 7))) break;
+          ++st_cnt;
+          __syncwarp();
+          tc_fence_after();
+          const float* sL =
+              reinterpret_cast<const float*>(sStage + s * C::STAGE_DKV + 2 * C::TILE_BYTES);
+          const float* sD = sL + bw::BT;
+          // Query row i sees key j when i < Sq and (not causal or j <= i + off).
+          const int i_min = p.causal ? j - off : 0;  // first query row seeing key j
+          const bool key_ok = j < p.Sk;
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint32_t sr[32], pr[32];
+            tmem_ld32(t_lane + bw::COL_S + q4 * 32, sr);
+            tmem_ld32(t_lane + bw::COL_DP + q4 * 32, pr);
+            tmem_wait_ld();
+            reg_fence32(sr);
+            reg_fence32(pr);
+            uint32_t pp[16], pd[16];
+#pragma unroll
+            for (int x = 0; x < 16; ++x) {
+              float pv[2], dv2[2];
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int ic = q4 * 32 + 2 * x + e;  // query column within the tile
+                const int i = t * bw::BT + ic;
+                const bool vis = key_ok && i < p.Sq && i >= i_min;
+                pv[e] = vis ? fast_exp2(__uint_as_float(sr[2 * x + e]) * p.c - sL[ic]) : 0.f;
+                dv2[e] = pv[e] * (__uint_as_float(pr[2 * x + e]) - sD[ic]);
+              }
+              pp[x] = BPack<T>::pack(pv[0], pv[1]);
+              pd[x] = BPack<T>::pack(dv2[0], dv2[1]);
+            }
+            tmem_st16(t_lane + bw::COL_S + q4 * 16, pp);
+            tmem_st16(t_lane + bw::COL_DP + q4 * 16, pd);
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(pd_full);
+          mbar_arrive(&empty[s]);  // this thread is done with the stage's lse / Delta
+        }
+      }
+      if (!ok) break;
+      // Epilogue: dV, dK (= scale * accumulator) of this thread's key row.
+      if (!(ok = mbar_wait(o_full, o_cnt & 1, abort_flag, &g_backward_err, 8))) break;
+      ++o_cnt;
+      __syncwarp();
+      tc_fence_after();
+      const bool any = p.G * (p.n_qt - t0) > 0;
+      const bool row_ok = j < p.Sk;
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {  // 0: dV, 1: dK
+        T* const row = (which ? DK : DV) + (((size_t)b * p.Sk + (row_ok ? j : 0)) * p.Hkv + hkv) * D;
+        const float mul = which ? p.scale : 1.f;
+#pragma unroll
+        for (int q4 = 0; q4 < D / 32; ++q4) {
+          uint32_t ar[32];
+          if (any) {
+            tmem_ld32(t_lane + bw::COL_ACC + which * D + q4 * 32, ar);
+            tmem_wait_ld();
+            reg_fence32(ar);
+          } else {
+#pragma unroll
+            for (int x = 0; x < 32; ++x) ar[x] = 0u;
+          }
+          uint32_t pk[16];
+#pragma unroll
+          for (int x = 0; x < 16; ++x)
+            pk[x] = BPack<T>::pack(__uint_as_float(ar[2 * x]) * mul,
+                                   __uint_as_float(ar[2 * x + 1]) * mul);
+          if (row_ok) {
+            if (b >= p.B || hkv >= p.Hkv) {
+              atomicOr(&g_backward_err, kErrBounds);
+              continue;
+            }
+            uint4* dst = reinterpret_cast<uint4*>(row + q4 * 32);
+#pragma unroll
+            for (int x = 0; x < 4; ++x)
+              dst[x] = make_uint4(pk[4 * x], pk[4 * x + 1], pk[4 * x + 2], pk[4 * x + 3]);
+          }
+        }
+      }
+      tc_fence_before();
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, bw::TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------------------
+// Host
+// ------------------------------------------------------------------------------
+template <int D, typename T>
+static int launch_backward_t(const void* q, const void* k, const void* v, const void* o,
+                             const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                             float* delta, int B, int Hq, int Hkv, int Sq, int Sk, float scale,
+                             int causal, cudaStream_t stream) {
+  using C = bw::Cfg<D>;
+  // pre: Delta
+  {
+    const size_t rows = (size_t)B * Sq * Hq;
+    const unsigned blocks = (unsigned)((rows * 32 + 255) / 256 < 65535 ? (rows * 32 + 255) / 256
+                                                                       : 65535);
+    bwd_pre_kernel<D, T><<<blocks, 256, 0, stream>>>(static_cast<const T*>(o),
+                                                     static_cast<const T*>(dout), delta, B, Sq,
+                                                     Hq);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  CUtensorMap tq, tk, tv, tdo;
+  if (encode_tmap_rows(&tq, q, D, Hq, Sq, B, bw::BT)) return cudaErrorInvalidValue;
+  if (encode_tmap_rows(&tdo, dout, D, Hq, Sq, B, bw::BT)) return cudaErrorInvalidValue;
+  if (encode_tmap_rows(&tk, k, D, Hkv, Sk, B, bw::BT)) return cudaErrorInvalidValue;
+  if (encode_tmap_rows(&tv, v, D, Hkv, Sk, B, bw::BT)) return cudaErrorInvalidValue;
+  static int attr_set[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(bwd_dq_kernel<D, T>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_DQ);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(bwd_dkdv_kernel<D, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::SMEM_DKV);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = 1;
+  }
+  BwdParams p;
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.lse = lse;
+  p.delta = delta;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.Sq = Sq;
+  p.Sk = Sk;
+  p.G = Hq / Hkv;
+  p.causal = causal ? 1 : 0;
+  p.n_qt = (Sq + bw::BT - 1) / bw::BT;
+  p.n_kt = (Sk + bw::BT - 1) / bw::BT;
+  p.scale = scale;
+  p.c = scale * bw::LOG2E;
+  const int sms = sm_count() > 0 ? sm_count() : 148;
+  p.n_items = B * Hq * p.n_qt;
+  if (p.n_items > 0) {
+    const int grid = p.n_items < sms ? p.n_items : sms;
+    bwd_dq_kernel<D, T><<<grid, bw::THREADS, C::SMEM_DQ, stream>>>(tq, tk, tv, tdo, p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  p.n_items = B * Hkv * p.n_kt;
+  if (p.n_items > 0) {
+    const int grid = p.n_items < sms ? p.n_items : sms;
+    bwd_dkdv_kernel<D, T><<<grid, bw::THREADS, C::SMEM_DKV, stream>>>(tq, tk, tv, tdo, p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+int launch_backward(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                    const float* lse, void* dq, void* dk, void* dv, float* delta, int B, int Hq,
+                    int Hkv, int Sq, int Sk, int D, float scale, int causal, bool bf16,
+                    cudaStream_t stream) {
+  if (D == 64)
+    return bf16 ? launch_backward_t<64, __nv_bfloat16>(q, k, v, o, dout, lse, dq, dk, dv, delta,
+                                                       B, Hq, Hkv, Sq, Sk, scale, causal, stream)
+                : launch_backward_t<64, __half>(q, k, v, o, dout, lse, dq, dk, dv, delta, B, Hq,
+                                                Hkv, Sq, Sk, scale, causal, stream);
+  return bf16 ? launch_backward_t<128, __nv_bfloat16>(q, k, v, o, dout, lse, dq, dk, dv, delta, B,
+                                                      Hq, Hkv, Sq, Sk, scale, causal, stream)
+              : launch_backward_t<128, __half>(q, k, v, o, dout, lse, dq, dk, dv, delta, B, Hq,
+                                               Hkv, Sq, Sk, scale, causal, stream);
+}
+
+int read_backward_error(unsigned int* out, int reset) {
+  unsigned int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_backward_err, sizeof(v));
+  if (e != cudaSuccess) return e;
+  if (reset && v) {
+    const unsigned int z = 0;
+    e = cudaMemcpyToSymbol(g_backward_err, &z, sizeof(z));
+    if (e != cudaSuccess) return e;
+  }
+  *out = v;
+  return 0;
+}
+
+}  // namespace fa

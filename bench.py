@@ -281,6 +281,7 @@ def run_ours(args, rank, world, local_rank):
     # ---------------- end to end through the C ABI with host buffers ----------------
     e2e = run_e2e(args, fa, torch, dev, q_h, k_h, v_h, sh, stream, dist)
     varlen = run_varlen(args, fa, torch, dev, sh, stream)
+    backward = run_backward(args, fa, torch, dev, q, k, v, sh, stream)
 
     if rank != 0:
         if dist:
@@ -378,6 +379,7 @@ def run_ours(args, rank, world, local_rank):
         },
         "e2e": e2e,
         "varlen": varlen,
+        "backward": backward,
         "gpu_launches": (5 + 2 * (n_r1 + n_r2)) * K,
         "gpu_launches_note": f"per step: 1 prefill + {2 + n_r1 + n_r2} decode calls x "
                              "(split + combine); the varlen and e2e runs follow the timed "
@@ -429,6 +431,49 @@ def run_varlen(args, fa, torch, dev, sh, stream):
             "workload": f"packed causal prefill, {len(lens)} sequences, lengths {lens} "
                         f"({tq} tokens), Hq{Hq}/Hkv{Hkv} D{D} bf16",
             "flop_convention": "sum_b 2*Hq*Sq_b*Sk_b*D (causal)", "launches": n}
+
+
+def run_backward(args, fa, torch, dev, q, k, v, sh, stream):
+    """Backward pass (fa_backward: Delta, dQ and dK/dV kernels) of the headline
+    prefill, with o and lse from fa_prefill_fwd_lse and a seeded dO; events
+    around each call, inputs larger than L2."""
+    B, Hq, Hkv, S, D = PREFILL.B, PREFILL.Hq, PREFILL.Hkv, PREFILL.Sq, PREFILL.D
+    o = torch.empty_like(q)
+    lse = torch.empty(B, Hq, S, dtype=torch.float32, device=dev)
+    st = fa.fa_prefill_fwd_lse(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                               lse.data_ptr(), B, Hq, Hkv, S, S, D, PREFILL.scale, 1, fa.FA_BF16,
+                               sh)
+    if st:
+        raise fa.FAError(st, "fa_prefill_fwd_lse")
+    g = torch.Generator().manual_seed(1)
+    dout = torch.randn(q.shape, generator=g).to(torch.bfloat16).to(dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+    def launch():
+        r = fa.fa_backward(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                           dout.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                           dv.data_ptr(), B, Hq, Hkv, S, S, D, PREFILL.scale, 1, fa.FA_BF16, sh)
+        if r:
+            raise fa.FAError(r, "fa_backward")
+    for _ in range(2):
+        launch()
+    n = max(3, min(args.steps, 10))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(n):
+        launch()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    st, detail = fa.fa_device_error()
+    if st != fa.FA_OK:
+        raise RuntimeError(f"device error word {detail:#x} in the backward run")
+    t = e0.elapsed_time(e1) / 1e3 / n
+    flops = 2.5 * PREFILL.flops
+    return {"value": round(flops / t / 1e12, 2), "unit": "TFLOP/s", "ms": round(t * 1e3, 4),
+            "workload": PREFILL.name + " backward (dQ, dK, dV of sum(O * dO))",
+            "flop_convention": "2.5 x the forward's 2*B*Hq*Sq*Sk*D (five matmuls against two)",
+            "launches": n, "kernels_per_call": 3}
 
 
 def run_e2e(args, fa, torch, dev, q_h, k_h, v_h, sh, stream, dist):

@@ -250,6 +250,30 @@ int fa_decode_fwd_noalloc(const void* q, const void* kcache, const void* vcache,
                           int B, int Hq, int Hkv, int cap, int D, float scale,
                           cudaStream_t stream);
 
+/*
+ * fa_backward -- gradients of the loss sum(O * dout) with respect to q, k and
+ * v (the flash-attention backward of tessera #90's backward commit note:
+ * a "_pre" pass Delta = rowsum(dout * O), then dQ and dK/dV passes that
+ * recompute P from the forward's log-sum-exp).
+ *
+ *   q, o, dout [B, Sq, Hq, D]    the forward's inputs, output, and the
+ *                                output gradient (dtype), read only
+ *   k, v       [B, Sk, Hkv, D]   read only
+ *   lse        [B, Hq, Sq] fp32  the forward's log-sum-exp
+ *                                (fa_prefill_fwd_lse), read only
+ *   dq         [B, Sq, Hq, D]    written
+ *   dk, dv     [B, Sk, Hkv, D]   written; query heads of a GQA group add
+ *                                into their kv head
+ *   scale, causal                as in the forward call
+ *
+ * Delta lives in stream-ordered scratch (B * Hq * Sq fp32).  Three kernels
+ * are enqueued.  Other rules as fa_prefill_fwd.
+ */
+int fa_backward(const void* q, const void* k, const void* v, const void* o,
+                const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                int B, int Hq, int Hkv, int Sq, int Sk, int D, float scale, int causal,
+                int dtype, cudaStream_t stream);
+
 /* Static, human-readable name of a status code (never NULL). */
 const char* fa_status_string(int status);
 
@@ -260,8 +284,8 @@ const char* fa_status_string(int status);
  * hit its time limit, FA_ERR_BOUNDS if only bounds checks fired (packed
  * offsets or page ids out of range, or an index self-check), FA_ERR_CUDA if
  * the read itself failed.
- * If detail != NULL it receives the raw bits: the prefill word in bits 0-15,
- * the decode word in bits 16-31; in each, bit 0 = a wait timed out (bits 8-15:
+ * If detail != NULL it receives the raw bits: the prefill (and backward) word
+ * in bits 0-15, the decode word in bits 16-31; in each, bit 0 = a wait timed out (bits 8-15:
  * which wait), bit 1 = a bounds check fired.
  */
 int fa_device_error(int reset, unsigned int* detail);
