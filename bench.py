@@ -470,7 +470,18 @@ def run_backward(args, fa, torch, dev, q, k, v, sh, stream):
         raise RuntimeError(f"device error word {detail:#x} in the backward run")
     t = e0.elapsed_time(e1) / 1e3 / n
     flops = 2.5 * PREFILL.flops
-    return {"value": round(flops / t / 1e12, 2), "unit": "TFLOP/s", "ms": round(t * 1e3, 4),
+    pk, pk_src = peaks()
+    bwd_hash = source_hash("attention_fa_fwd_04_gb300/csrc/fa_backward.cu",
+                           "attention_fa_fwd_04_gb300/csrc/fa_ptx.cuh")
+    ach = flops / t / 1e12
+    roof = {"bound": "tensor", "achieved": round(ach, 2), "peak": pk["bf16_tflops"],
+            "unit": "TFLOP/s", "frac": round(ach / pk["bf16_tflops"], 4),
+            "peak_source": f"{pk_src} bf16 burst",
+            "scope": "whole call (Delta, dQ and dK/dV kernels); traffic: the dK/dV kernel, "
+                     "about 70 % of the call",
+            "traffic": stored_traffic("bwd_dkdv_kernel_D128_bf16", bwd_hash)}
+    return {"value": round(ach, 2), "unit": "TFLOP/s", "ms": round(t * 1e3, 4),
+            "roofline": roof,
             "workload": PREFILL.name + " backward (dQ, dK, dV of sum(O * dO))",
             "flop_convention": "2.5 x the forward's 2*B*Hq*Sq*Sk*D (five matmuls against two)",
             "launches": n, "kernels_per_call": 3}
@@ -540,8 +551,10 @@ def oracle_prefill_sample(n_rows, seed=0, inputs=None):
 
 def cpu_baseline(budget_s=15.0):
     inputs = fa_inputs.prefill_inputs_for(PREFILL, seed=0)
-    t_cal, f_cal, nth = oracle_prefill_sample(128, seed=1, inputs=inputs)
-    n = int(max(128, min(200000, 128 * budget_s / max(t_cal, 1e-3))))
+    # Calibrate on enough rows that thread start-up does not dominate.
+    n_cal = 4096
+    t_cal, f_cal, nth = oracle_prefill_sample(n_cal, seed=1, inputs=inputs)
+    n = int(max(n_cal, min(2000000, n_cal * budget_s / max(t_cal, 1e-3))))
     t, f, nth = oracle_prefill_sample(n, seed=2, inputs=inputs)
     return {"value": round(f / t / 1e12, 6), "unit": "TFLOP/s", "cores": nth, "kind": "oracle",
             "seconds": round(t, 2),
@@ -610,7 +623,9 @@ def run_profile_case(args, local_rank):
     case of a few hundred MB (inputs larger than L2), no timing contract.
       prefill_small: B1 Hq64 Hkv4 S8192 D128 causal bf16 (same kernel as the
                      headline; Q+O = 256 MiB)
-      decode_full:   the 65536-token decode, L2 flushed before every launch"""
+      decode_full:   the 65536-token decode, L2 flushed before every launch
+      backward_small: fa_backward on B1 Hq64 Hkv4 S8192 D128 causal bf16 (the
+                     headline backward's kernels at half its query heads)"""
     import torch
     import attention_fa_fwd_04_gb300 as fa
     torch.cuda.set_device(local_rank)
@@ -629,6 +644,27 @@ def run_profile_case(args, local_rank):
                 raise fa.FAError(st, "fa_prefill_fwd")
         work = {"workload": f"prefill B{B} Hq{Hq} Hkv{Hkv} S{S} D{D} causal bf16",
                 "flops_per_launch": 2.0 * B * Hq * S * S * D}
+    elif args.profile == "backward_small":
+        B, Hq, Hkv, S, D = 1, 64, 4, 8192, 128
+        scale = 1 / math.sqrt(D)
+        q, k, v = (t.to(dev) for t in fa_inputs.prefill_inputs(B, Hq, Hkv, S, S, D, seed=0))
+        o = torch.empty_like(q)
+        lse = torch.empty(B, Hq, S, dtype=torch.float32, device=dev)
+        st = fa.fa_prefill_fwd_lse(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                   lse.data_ptr(), B, Hq, Hkv, S, S, D, scale, 1, fa.FA_BF16, sh)
+        if st:
+            raise fa.FAError(st, "fa_prefill_fwd_lse")
+        g = torch.Generator().manual_seed(1)
+        dout = torch.randn(q.shape, generator=g).to(torch.bfloat16).to(dev)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        for _ in range(n):
+            st = fa.fa_backward(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                dout.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                dv.data_ptr(), B, Hq, Hkv, S, S, D, scale, 1, fa.FA_BF16, sh)
+            if st:
+                raise fa.FAError(st, "fa_backward")
+        work = {"workload": f"backward B{B} Hq{Hq} Hkv{Hkv} S{S} D{D} causal bf16",
+                "flops_per_launch": 2.5 * 2.0 * B * Hq * S * S * D}
     else:
         dq, kc, vc, L = fa_inputs.decode_inputs_for(DECODE, seed=0, L=DECODE.cap)
         dq, kc, vc = dq.to(dev), kc.to(dev), vc.to(dev)
@@ -655,7 +691,7 @@ def run_profile_case(args, local_rank):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--profile", choices=["prefill_small", "decode_full"], default=None,
+    ap.add_argument("--profile", choices=["prefill_small", "decode_full", "backward_small"], default=None,
                     help="launch-only driver for ncu captures (no timing)")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=300)
