@@ -175,7 +175,8 @@ extern "C" int fa_backward(const void* q, const void* k, const void* v, const vo
     return cuda_status(e, "backward zero-fill");
   }
   void* delta = nullptr;
-  cudaError_t e = cudaMallocAsync(&delta, (size_t)B * Hq * Sq * sizeof(float), stream);
+  // Delta [B, Hq, Sq], then the two work counters of the dq and dkdv kernels.
+  cudaError_t e = cudaMallocAsync(&delta, ((size_t)B * Hq * Sq + 2) * sizeof(float), stream);
   if (e != cudaSuccess) return cuda_status(e, "backward cudaMallocAsync");
   int r = fa::launch_backward(q, k, v, o, dout, lse, dq, dk, dv, static_cast<float*>(delta), B,
                               Hq, Hkv, Sq, Sk, D, scale, causal, dtype == FA_BF16, stream);

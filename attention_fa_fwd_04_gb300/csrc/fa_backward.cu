@@ -58,6 +58,10 @@ struct BwdParams {
   void* dv;             // [B, Sk, Hkv, D]
   const float* lse;     // [B, Hq, Sq] natural log
   const float* delta;   // [B, Hq, Sq]
+  // Work counter of the kernel (zeroed by the Delta kernel before it runs):
+  // persistent CTAs take items in index order, so items are numbered longest
+  // first and every CTA takes the next one when it is free.
+  unsigned int* work_ctr;
   int B, Hq, Hkv, Sq, Sk, G, causal;
   int n_qt, n_kt, n_items;
   float c;              // scale * log2(e)
@@ -104,7 +108,12 @@ template <int D, typename T>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const T* __restrict__ o,
                                                       const T* __restrict__ dout,
                                                       float* __restrict__ delta, int B, int Sq,
-                                                      int Hq) {
+                                                      int Hq, unsigned int* __restrict__ ctr) {
+  // The dq and dkdv kernels, launched after this one, take work from ctr[0], ctr[1].
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    ctr[0] = 0u;
+    ctr[1] = 0u;
+  }
   const size_t rows = (size_t)B * Sq * Hq;
   const int lane = threadIdx.x & 31;
   for (size_t r = (blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5; r < rows;
@@ -126,25 +135,55 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const T* __restrict__ o,
   }
 }
 
-// Work items.  dq: (b, hq, query tile), kv-head-major, longest causal tiles
-// first.  dkdv: (b, hkv, key tile), kv-head-major, key tiles ascending (the
-// ones seen by the most query tiles first).
+// Work items, numbered longest first (the order CTAs take them in).
+// dq: (b, hq, query tile), query tiles descending (a causal tile sees more
+// keys the later it is); within a tile, batch-major then head, so the query
+// heads of one kv head run side by side and share its K/V tiles in L2.
+// dkdv: (b, hkv, key tile), key tiles ascending (the earliest key tile is
+// seen by the most query tiles); within a tile, batch-major then kv head.
 __device__ __forceinline__ void dq_item(int w, const BwdParams& p, int* b, int* hq, int* qt) {
-  const int per_b = p.n_qt * p.G, per_kv = p.B * per_b;
-  const int hkv = w / per_kv;
-  int r = w - hkv * per_kv;
-  *b = r / per_b;
-  r -= *b * per_b;
-  const int qr = r / p.G;
-  *hq = hkv * p.G + (r - qr * p.G);
+  const int per_t = p.B * p.Hq;
+  const int qr = w / per_t;
+  const int r = w - qr * per_t;
+  *b = r / p.Hq;
+  *hq = r - *b * p.Hq;
   *qt = p.n_qt - 1 - qr;
 }
 __device__ __forceinline__ void dkv_item(int w, const BwdParams& p, int* b, int* hkv, int* kt) {
-  const int per_kv = p.B * p.n_kt;
-  *hkv = w / per_kv;
-  const int r = w - *hkv * per_kv;
-  *b = r / p.n_kt;
-  *kt = r - *b * p.n_kt;
+  const int per_t = p.B * p.Hkv;
+  *kt = w / per_t;
+  const int r = w - *kt * per_t;
+  *b = r / p.Hkv;
+  *hkv = r - *b * p.Hkv;
+}
+
+// The CTA's item schedule: the producer warp takes an index from the work
+// counter and hands it to the MMA warp and the four element-wise warps through
+// a two-slot ring (sched_full: 1 arrival; sched_empty: MMA warp + 4 warps).
+// Returns the item, -1 when there is no more work, or -2 after an abort.
+__device__ __forceinline__ int sched_produce(uint32_t k, const BwdParams& p, uint64_t* sfull,
+                                             uint64_t* sempty, volatile int* sched,
+                                             volatile int* abort_flag, bool leader) {
+  const int slot = k & 1;
+  if (!mbar_wait(&sempty[slot], ((k >> 1) & 1) ^ 1, abort_flag, &g_backward_err, 10)) return -2;
+  int w = -1;
+  if (leader) {
+    const unsigned int t = atomicAdd(p.work_ctr, 1u);
+    w = t < (unsigned int)p.n_items ? (int)t : -1;
+    sched[slot] = w;
+    mbar_arrive(&sfull[slot]);
+  }
+  return __shfl_sync(0xffffffffu, w, 0);
+}
+__device__ __forceinline__ int sched_consume(uint32_t k, uint64_t* sfull, uint64_t* sempty,
+                                             volatile int* sched, volatile int* abort_flag,
+                                             unsigned int site) {
+  const int slot = k & 1;
+  if (!mbar_wait(&sfull[slot], (k >> 1) & 1, abort_flag, &g_backward_err, site)) return -2;
+  const int w = sched[slot];
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(&sempty[slot]);
+  return w;
 }
 // Key tiles seen by query tile rows [r0, r0 + 128).
 __device__ __forceinline__ int bw_key_tiles(int r0, const BwdParams& p) {
@@ -191,8 +230,11 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
   uint64_t* ds_full = q_full + 3;   // dS in TMEM (128 arrivals)
   uint64_t* o_full = q_full + 4;    // dQ complete
   uint64_t* drain = q_full + 5;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(q_full + 6);
+  uint64_t* sched_full = q_full + 6;   // [2]
+  uint64_t* sched_empty = q_full + 8;  // [2]
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(q_full + 10);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  volatile int* sched = abort_flag + 1;  // [2]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -206,6 +248,10 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
     mbar_init(ds_full, bw::BT);
     mbar_init(o_full, 1);
     mbar_init(drain, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sched_full[i], 1);
+      mbar_init(&sched_empty[i], 5);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -232,7 +278,12 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
     const uint64_t pol_kv = l2_policy_evict_last();
     uint32_t kv_cnt = 0, local = 0;
     bool ok = true, q_issued = false;
-    for (int w = blockIdx.x; w < p.n_items && ok; w += gridDim.x, ++local) {
+    for (uint32_t k = 0; ok; ++k, ++local) {
+      const int w = sched_produce(k, p, sched_full, sched_empty, sched, abort_flag, leader);
+      if (w < 0) {
+        ok = w == -1;
+        break;
+      }
       int b, hq, qt;
       dq_item(w, p, &b, &hq, &qt);
       const int hkv = hq / p.G;
@@ -305,7 +356,12 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
       tc_fence_after();
       return r;
     };
-    for (int w = blockIdx.x; w < p.n_items && ok; w += gridDim.x, ++local) {
+    for (uint32_t it = 0; ok; ++it, ++local) {
+      const int w = sched_consume(it, sched_full, sched_empty, sched, abort_flag, 11);
+      if (w < 0) {
+        ok = w == -1;
+        break;
+      }
       int b, hq, qt;
       dq_item(w, p, &b, &hq, &qt);
       const int n = bw_key_tiles(qt * bw::BT, p);
@@ -355,7 +411,12 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
     uint32_t s_cnt = 0, o_cnt = 0;
     bool ok = true;
     T* const DQ = static_cast<T*>(p.dq);
-    for (int w = blockIdx.x; w < p.n_items && ok; w += gridDim.x) {
+    for (uint32_t it = 0; ok; ++it) {
+      const int w = sched_consume(it, sched_full, sched_empty, sched, abort_flag, 12);
+      if (w < 0) {
+        ok = w == -1;
+        break;
+      }
       int b, hq, qt;
       dq_item(w, p, &b, &hq, &qt);
       const int n = bw_key_tiles(qt * bw::BT, p);
@@ -473,8 +534,11 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
   uint64_t* pd_full = kv_full + 3;  // P^T and dS^T in TMEM (128 arrivals)
   uint64_t* o_full = kv_full + 4;   // dK, dV complete
   uint64_t* drain = kv_full + 5;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(kv_full + 6);
+  uint64_t* sched_full = kv_full + 6;   // [2]
+  uint64_t* sched_empty = kv_full + 8;  // [2]
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(kv_full + 10);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  volatile int* sched = abort_flag + 1;  // [2]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -490,6 +554,10 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
     mbar_init(pd_full, bw::BT);
     mbar_init(o_full, 1);
     mbar_init(drain, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sched_full[i], 1);
+      mbar_init(&sched_empty[i], 5);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -516,7 +584,12 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
     const uint64_t pol_q = l2_policy_evict_last();
     uint32_t st_cnt = 0, local = 0;
     bool ok = true, kv_issued = false;
-    for (int w = blockIdx.x; w < p.n_items && ok; w += gridDim.x, ++local) {
+    for (uint32_t k = 0; ok; ++k, ++local) {
+      const int w = sched_produce(k, p, sched_full, sched_empty, sched, abort_flag, leader);
+      if (w < 0) {
+        ok = w == -1;
+        break;
+      }
       int b, hkv, kt;
       dkv_item(w, p, &b, &hkv, &kt);
       const int t0 = bw_first_query_tile(kt * bw::BT, p);
@@ -536,9 +609,11 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
       }
       __syncwarp();
       kv_issued = true;
-      for (int g = 0; g < p.G && ok; ++g) {
-        const int hq = hkv * p.G + g;
-        for (int t = t0; t < p.n_qt && ok; ++t) {
+      // Query tiles descending, the group's heads innermost: the items of one
+      // kv head then read the same Q / dO tiles at about the same time.
+      for (int t = p.n_qt - 1; t >= t0 && ok; --t) {
+        for (int g = 0; g < p.G && ok; ++g) {
+          const int hq = hkv * p.G + g;
           const int s = st_cnt % NS;
           const uint32_t ph = (st_cnt / NS) & 1;
           if (!(ok = mbar_wait(&empty[s], ph ^ 1, abort_flag, &g_backward_err, 2))) break;
@@ -611,7 +686,12 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
       if (leader) mma_commit(bar);
       __syncwarp();
     };
-    for (int w = blockIdx.x; w < p.n_items && ok; w += gridDim.x, ++local) {
+    for (uint32_t it = 0; ok; ++it, ++local) {
+      const int w = sched_consume(it, sched_full, sched_empty, sched, abort_flag, 11);
+      if (w < 0) {
+        ok = w == -1;
+        break;
+      }
       int b, hkv, kt;
       dkv_item(w, p, &b, &hkv, &kt);
       const int t0 = bw_first_query_tile(kt * bw::BT, p);
@@ -649,13 +729,18 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
     bool ok = true;
     T* const DK = static_cast<T*>(p.dk);
     T* const DV = static_cast<T*>(p.dv);
-    for (int w = blockIdx.x; w < p.n_items && ok; w += gridDim.x) {
+    for (uint32_t it = 0; ok; ++it) {
+      const int w = sched_consume(it, sched_full, sched_empty, sched, abort_flag, 12);
+      if (w < 0) {
+        ok = w == -1;
+        break;
+      }
       int b, hkv, kt;
       dkv_item(w, p, &b, &hkv, &kt);
       const int t0 = bw_first_query_tile(kt * bw::BT, p);
       const int j = kt * bw::BT + r;  // key row
-      for (int g = 0; g < p.G && ok; ++g) {
-        for (int t = t0; t < p.n_qt && ok; ++t) {
+      for (int t = p.n_qt - 1; t >= t0 && ok; --t) {
+        for (int g = 0; g < p.G && ok; ++g) {
           const int s = ph_cnt % NS;
           const uint32_t fph = (ph_cnt / NS) & 1;
           ++ph_cnt;
@@ -765,6 +850,8 @@ static int launch_backward_t(const void* q, const void* k, const void* v, const 
                              float* delta, int B, int Hq, int Hkv, int Sq, int Sk, float scale,
                              int causal, cudaStream_t stream) {
   using C = bw::Cfg<D>;
+  // The two work counters follow Delta in the scratch.
+  unsigned int* ctr = reinterpret_cast<unsigned int*>(delta + (size_t)B * Hq * Sq);
   // pre: Delta
   {
     const size_t rows = (size_t)B * Sq * Hq;
@@ -772,7 +859,7 @@ static int launch_backward_t(const void* q, const void* k, const void* v, const 
                                                                        : 65535);
     bwd_pre_kernel<D, T><<<blocks, 256, 0, stream>>>(static_cast<const T*>(o),
                                                      static_cast<const T*>(dout), delta, B, Sq,
-                                                     Hq);
+                                                     Hq, ctr);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -812,6 +899,7 @@ static int launch_backward_t(const void* q, const void* k, const void* v, const 
   p.c = scale * bw::LOG2E;
   const int sms = sm_count() > 0 ? sm_count() : 148;
   p.n_items = B * Hq * p.n_qt;
+  p.work_ctr = ctr;
   if (p.n_items > 0) {
     const int grid = p.n_items < sms ? p.n_items : sms;
     bwd_dq_kernel<D, T><<<grid, bw::THREADS, C::SMEM_DQ, stream>>>(tq, tk, tv, tdo, p);
@@ -819,6 +907,7 @@ static int launch_backward_t(const void* q, const void* k, const void* v, const 
     if (e != cudaSuccess) return e;
   }
   p.n_items = B * Hkv * p.n_kt;
+  p.work_ctr = ctr + 1;
   if (p.n_items > 0) {
     const int grid = p.n_items < sms ? p.n_items : sms;
     bwd_dkdv_kernel<D, T><<<grid, bw::THREADS, C::SMEM_DKV, stream>>>(tq, tk, tv, tdo, p);

@@ -59,7 +59,8 @@ int launch_decode_layout(const void* q, const void* kc, const void* vc, const De
 // Scratch floats the decode needs for these sizes (Sq new tokens per sequence).
 size_t decode_scratch_floats(int B, int Hq, int Hkv, int cap, int D, int Sq = 1);
 
-// Enqueue the backward pass: Delta into `delta` ([B, Hq, Sq] fp32 scratch),
+// Enqueue the backward pass: Delta into `delta` ([B, Hq, Sq] fp32 scratch, then
+// two uint32 work counters),
 // then dq [B, Sq, Hq, D] and dk, dv [B, Sk, Hkv, D] from q, k, v, the forward
 // output o, dout and the forward's lse ([B, Hq, Sq]).  Sq, Sk > 0.
 int launch_backward(const void* q, const void* k, const void* v, const void* o, const void* dout,
