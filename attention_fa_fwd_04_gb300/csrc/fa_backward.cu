@@ -157,34 +157,6 @@ __device__ __forceinline__ void dkv_item(int w, const BwdParams& p, int* b, int*
   *hkv = r - *b * p.Hkv;
 }
 
-// The CTA's item schedule: the producer warp takes an index from the work
-// counter and hands it to the MMA warp and the four element-wise warps through
-// a two-slot ring (sched_full: 1 arrival; sched_empty: MMA warp + 4 warps).
-// Returns the item, -1 when there is no more work, or -2 after an abort.
-__device__ __forceinline__ int sched_produce(uint32_t k, const BwdParams& p, uint64_t* sfull,
-                                             uint64_t* sempty, volatile int* sched,
-                                             volatile int* abort_flag, bool leader) {
-  const int slot = k & 1;
-  if (!mbar_wait(&sempty[slot], ((k >> 1) & 1) ^ 1, abort_flag, &g_backward_err, 10)) return -2;
-  int w = -1;
-  if (leader) {
-    const unsigned int t = atomicAdd(p.work_ctr, 1u);
-    w = t < (unsigned int)p.n_items ? (int)t : -1;
-    sched[slot] = w;
-    mbar_arrive(&sfull[slot]);
-  }
-  return __shfl_sync(0xffffffffu, w, 0);
-}
-__device__ __forceinline__ int sched_consume(uint32_t k, uint64_t* sfull, uint64_t* sempty,
-                                             volatile int* sched, volatile int* abort_flag,
-                                             unsigned int site) {
-  const int slot = k & 1;
-  if (!mbar_wait(&sfull[slot], (k >> 1) & 1, abort_flag, &g_backward_err, site)) return -2;
-  const int w = sched[slot];
-  __syncwarp();
-  if ((threadIdx.x & 31) == 0) mbar_arrive(&sempty[slot]);
-  return w;
-}
 // Key tiles seen by query tile rows [r0, r0 + 128).
 __device__ __forceinline__ int bw_key_tiles(int r0, const BwdParams& p) {
   if (r0 >= p.Sq || p.Sk <= 0) return 0;
@@ -230,11 +202,11 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
   uint64_t* ds_full = q_full + 3;   // dS in TMEM (128 arrivals)
   uint64_t* o_full = q_full + 4;    // dQ complete
   uint64_t* drain = q_full + 5;
-  uint64_t* sched_full = q_full + 6;   // [2]
-  uint64_t* sched_empty = q_full + 8;  // [2]
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(q_full + 10);
+  uint64_t* sched_full = q_full + 6;                 // [kSchedSlots]
+  uint64_t* sched_empty = sched_full + kSchedSlots;  // [kSchedSlots]
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sched_empty + kSchedSlots);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-  volatile int* sched = abort_flag + 1;  // [2]
+  volatile int* sched = abort_flag + 1;  // [kSchedSlots]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -248,7 +220,7 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
     mbar_init(ds_full, bw::BT);
     mbar_init(o_full, 1);
     mbar_init(drain, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kSchedSlots; ++i) {
       mbar_init(&sched_full[i], 1);
       mbar_init(&sched_empty[i], 5);
     }
@@ -279,7 +251,8 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
     uint32_t kv_cnt = 0, local = 0;
     bool ok = true, q_issued = false;
     for (uint32_t k = 0; ok; ++k, ++local) {
-      const int w = sched_produce(k, p, sched_full, sched_empty, sched, abort_flag, leader);
+      const int w = sched_produce(k, p.work_ctr, p.n_items, sched_full, sched_empty, sched,
+                                  abort_flag, &g_backward_err, leader);
       if (w < 0) {
         ok = w == -1;
         break;
@@ -357,7 +330,7 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
       return r;
     };
     for (uint32_t it = 0; ok; ++it, ++local) {
-      const int w = sched_consume(it, sched_full, sched_empty, sched, abort_flag, 11);
+      const int w = sched_consume(it, sched_full, sched_empty, sched, abort_flag, &g_backward_err, 11);
       if (w < 0) {
         ok = w == -1;
         break;
@@ -412,7 +385,7 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
     bool ok = true;
     T* const DQ = static_cast<T*>(p.dq);
     for (uint32_t it = 0; ok; ++it) {
-      const int w = sched_consume(it, sched_full, sched_empty, sched, abort_flag, 12);
+      const int w = sched_consume(it, sched_full, sched_empty, sched, abort_flag, &g_backward_err, 12);
       if (w < 0) {
         ok = w == -1;
         break;
@@ -534,11 +507,11 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
   uint64_t* pd_full = kv_full + 3;  // P^T and dS^T in TMEM (128 arrivals)
   uint64_t* o_full = kv_full + 4;   // dK, dV complete
   uint64_t* drain = kv_full + 5;
-  uint64_t* sched_full = kv_full + 6;   // [2]
-  uint64_t* sched_empty = kv_full + 8;  // [2]
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(kv_full + 10);
+  uint64_t* sched_full = kv_full + 6;                // [kSchedSlots]
+  uint64_t* sched_empty = sched_full + kSchedSlots;  // [kSchedSlots]
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sched_empty + kSchedSlots);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-  volatile int* sched = abort_flag + 1;  // [2]
+  volatile int* sched = abort_flag + 1;  // [kSchedSlots]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -554,7 +527,7 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
     mbar_init(pd_full, bw::BT);
     mbar_init(o_full, 1);
     mbar_init(drain, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kSchedSlots; ++i) {
       mbar_init(&sched_full[i], 1);
       mbar_init(&sched_empty[i], 5);
     }
@@ -585,7 +558,8 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
     uint32_t st_cnt = 0, local = 0;
     bool ok = true, kv_issued = false;
     for (uint32_t k = 0; ok; ++k, ++local) {
-      const int w = sched_produce(k, p, sched_full, sched_empty, sched, abort_flag, leader);
+      const int w = sched_produce(k, p.work_ctr, p.n_items, sched_full, sched_empty, sched,
+                                  abort_flag, &g_backward_err, leader);
       if (w < 0) {
         ok = w == -1;
         break;
@@ -687,7 +661,7 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
       __syncwarp();
     };
     for (uint32_t it = 0; ok; ++it, ++local) {
-      const int w = sched_consume(it, sched_full, sched_empty, sched, abort_flag, 11);
+      const int w = sched_consume(it, sched_full, sched_empty, sched, abort_flag, &g_backward_err, 11);
       if (w < 0) {
         ok = w == -1;
         break;
@@ -730,7 +704,7 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
     T* const DK = static_cast<T*>(p.dk);
     T* const DV = static_cast<T*>(p.dv);
     for (uint32_t it = 0; ok; ++it) {
-      const int w = sched_consume(it, sched_full, sched_empty, sched, abort_flag, 12);
+      const int w = sched_consume(it, sched_full, sched_empty, sched, abort_flag, &g_backward_err, 12);
       if (w < 0) {
         ok = w == -1;
         break;

@@ -10,9 +10,10 @@
 //
 // Work unit ("Persistent (grid-stride) mode" of the gfx950 README): 256 query
 // rows of one query head, held as two 128-row Q tiles.  A persistent grid of
-// one CTA per SM walks the units in kv-head-major order (all query heads that
+// one CTA per SM takes the units in kv-head-major order (all query heads that
 // share a K/V head run together, so K/V stay in L2), longest causal units
-// first.
+// first; each CTA claims its next unit from a work counter when it is free,
+// instead of a fixed grid stride, which evens out the causal tail.
 //
 // CTA = 12 warps (3 warpgroups):
 //   warps 0-3  softmax/epilogue for Q tile 0 (TMEM lanes 0-127)
@@ -32,6 +33,9 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <math.h>
+
+#include <mutex>
+#include <unordered_map>
 
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
@@ -53,7 +57,6 @@ constexpr uint32_t REGS_LAUNCH = 168, REGS_SOFTMAX = 208, REGS_ISSUE = 88;
 static_assert(256 * REGS_SOFTMAX + 128 * REGS_ISSUE <= THREADS * REGS_LAUNCH,
               "register split exceeds the launch allocation");
 constexpr int HALF_BYTES = 128 * 128;  // 128 rows x 64 elements x 2 bytes
-constexpr float TAU = 8.0f;            // lazy-rescale threshold (log2 domain)
 
 template <int D>
 struct Cfg {
@@ -62,7 +65,7 @@ struct Cfg {
   static constexpr int NSTAGE = (D == 128) ? 5 : 9;
   static constexpr int SMEM_Q = 2 * TILE_BYTES;
   static constexpr int SMEM_KV = NSTAGE * TILE_BYTES;
-  static constexpr int SMEM_BAR = 256;
+  static constexpr int SMEM_BAR = 512;
   static constexpr int SMEM_TOTAL = 1024 + SMEM_Q + SMEM_KV + SMEM_BAR;
   static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O0 = 256, COL_O1 = 256 + D;
   static constexpr uint32_t TMEM_COLS = 512;
@@ -79,6 +82,13 @@ struct PrefillParams {
   const int32_t* cu_k;
   int total_q, total_k;
   int B, Hq, Hkv, Sq, Sk, G, causal, n_qb, n_items;
+  // Work counter [2] (claims, CTAs finished), zero when the launch starts:
+  // each persistent CTA claims the next work item when it is free (items keep
+  // their kv-head-major order); the last CTA to finish zeroes both again.
+  // Null for packed sequences, which keep the fixed grid stride: their many
+  // short items (and blocks past the end of short sequences) measured faster
+  // without the claim's round trips.
+  unsigned int* work_ctr;
   float c;  // scale * log2(e)
 };
 
@@ -94,27 +104,28 @@ struct SeqSpan {
 // decision.  Packed offsets that are not 0 <= cu[b] <= cu[b+1] <= total, or a
 // query length beyond the schedule's n_qb * 256 rows, make the sequence empty
 // and set the bounds bit of the error word.
+template <bool PACKED>
 __device__ __forceinline__ SeqSpan seq_span(const PrefillParams& p, int b, unsigned int* err) {
   SeqSpan s;
-  if (!p.cu_q) {
+  if constexpr (!PACKED) {
     s.q0 = 0;
     s.k0 = 0;
     s.tb = b;
     s.Sq = p.Sq;
     s.Sk = p.Sk;
     s.orow = (size_t)b * p.Sq;
-    return s;
+  } else {
+    const int q0 = p.cu_q[b], q1 = p.cu_q[b + 1], k0 = p.cu_k[b], k1 = p.cu_k[b + 1];
+    const bool ok = 0 <= q0 && q0 <= q1 && q1 <= p.total_q && 0 <= k0 && k0 <= k1 &&
+                    k1 <= p.total_k && q1 - q0 <= p.n_qb * 256;
+    if (!ok && err) atomicOr(err, kErrBounds);
+    s.q0 = ok ? q0 : 0;
+    s.k0 = ok ? k0 : 0;
+    s.tb = 0;
+    s.Sq = ok ? q1 - q0 : 0;
+    s.Sk = ok ? k1 - k0 : 0;
+    s.orow = (size_t)s.q0;
   }
-  const int q0 = p.cu_q[b], q1 = p.cu_q[b + 1], k0 = p.cu_k[b], k1 = p.cu_k[b + 1];
-  const bool ok = 0 <= q0 && q0 <= q1 && q1 <= p.total_q && 0 <= k0 && k0 <= k1 &&
-                  k1 <= p.total_k && q1 - q0 <= p.n_qb * 256;
-  if (!ok && err) atomicOr(err, kErrBounds);
-  s.q0 = ok ? q0 : 0;
-  s.k0 = ok ? k0 : 0;
-  s.tb = 0;
-  s.Sq = ok ? q1 - q0 : 0;
-  s.Sk = ok ? k1 - k0 : 0;
-  s.orow = (size_t)s.q0;
   return s;
 }
 
@@ -179,7 +190,11 @@ struct IsBF16<__nv_bfloat16> {
   static constexpr bool value = true;
 };
 
-template <int D, typename T>
+// PACKED: the batch is packed sequences (cu_q / cu_k set), scheduled by a
+// fixed grid stride; otherwise a dense batch, scheduled by the work counter.
+// (Separate instantiations: the dense kernel carries none of the packed-
+// sequence code.)
+template <int D, typename T, bool PACKED>
 __global__ void __launch_bounds__(pf::THREADS, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
@@ -204,8 +219,11 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
   uint64_t* p_full = q_full + 4;  // [2]
   uint64_t* o_full = q_full + 6;  // [2]
   uint64_t* drain = q_full + 8;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(q_full + 9);
+  uint64_t* sched_full = q_full + 9;                 // [kSchedSlots] work-item ring
+  uint64_t* sched_empty = sched_full + kSchedSlots;  // [kSchedSlots]
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sched_empty + kSchedSlots);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  volatile int* sched = abort_flag + 1;  // [kSchedSlots]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -222,6 +240,10 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       mbar_init(&o_full[i], 1);
     }
     mbar_init(drain, 1);
+    for (int i = 0; i < kSchedSlots; ++i) {
+      mbar_init(&sched_full[i], 1);
+      mbar_init(&sched_empty[i], 9);  // the MMA warp and the 8 softmax warps
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -240,6 +262,15 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
   // warp-aligned CTA barrier below, or tcgen05.dealloc, with lanes still
   // inside a role loop.)
   const bool leader = lane == 0;
+  // Work items.  Dense launches (work_ctr set): the producer claims each item
+  // from the counter and hands it to the MMA and softmax warps (sched_*).
+  // Packed sequences: every role walks the fixed grid stride itself.
+  constexpr bool dynamic = !PACKED;
+  auto next_stride = [&](uint32_t* pos) {
+    const int t = (int)(blockIdx.x + *pos * gridDim.x);
+    ++*pos;
+    return t < p.n_items ? t : -1;
+  };
   if (warp >= 8) {
    // ------------------ warpgroup 2: TMA producer and MMA issuer ------------------
    regs_decrease<pf::REGS_ISSUE>();
@@ -254,11 +285,20 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
     const uint64_t pol_kv = l2_policy_evict_last();
     uint32_t kv_cnt = 0, local = 0;
     bool ok = true, q_issued = false;
-    for (int w = blockIdx.x; w < p.n_items && ok; w += gridDim.x, ++local) {
+    uint32_t next = 0;
+    for (uint32_t k = 0; ok; ++k, ++local) {
+      const int w =
+          dynamic ? sched_produce(k, p.work_ctr, p.n_items, sched_full, sched_empty, sched,
+                                  abort_flag, &g_prefill_err, leader)
+                  : next_stride(&next);
+      if (w < 0) {
+        ok = w == -1;
+        break;
+      }
       int b, hq, qb;
       prefill_item(w, p.B, p.Hq, p.Hkv, p.n_qb, &b, &hq, &qb);
       const int hkv = hq / p.G;
-      const SeqSpan sq = seq_span(p, b, nullptr);
+      const SeqSpan sq = seq_span<PACKED>(p, b, nullptr);
       const int row0 = qb * pf::QBLOCK;
       const int n0 = kv_tiles_for(row0, sq.Sq, sq.Sk, p.causal);
       const int n1 = kv_tiles_for(row0 + pf::BM, sq.Sq, sq.Sk, p.causal);
@@ -310,7 +350,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
     constexpr uint32_t IDESC_O = idesc_f16(pf::BM, D, kBF16, true);
     const uint32_t sq_addr = smem_u32(sQ);
     const uint32_t skv_addr = smem_u32(sKV);
-    uint32_t kv_cnt = 0, local = 0, p_cnt0 = 0, p_cnt1 = 0;
+    uint32_t kv_cnt = 0, local = 0, p_cnt0 = 0, p_cnt1 = 0, next = 0;
     bool ok = true;
 
     // S_i = Q_i K^T over D/16 k-steps (K-major A and B, 128-byte swizzle).
@@ -351,10 +391,17 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
     auto ring_wait = [&](uint32_t idx, unsigned int site) {
       return mbar_wait(&full[idx % NSTAGE], (idx / NSTAGE) & 1, abort_flag, &g_prefill_err, site);
     };
-    for (int w = blockIdx.x; w < p.n_items && ok; w += gridDim.x, ++local) {
+    for (uint32_t it = 0; ok; ++it, ++local) {
+      const int w =
+          dynamic ? sched_consume(it, sched_full, sched_empty, sched, abort_flag, &g_prefill_err, 15)
+                  : next_stride(&next);
+      if (w < 0) {
+        ok = w == -1;
+        break;
+      }
       int b, hq, qb;
       prefill_item(w, p.B, p.Hq, p.Hkv, p.n_qb, &b, &hq, &qb);
-      const SeqSpan sq = seq_span(p, b, nullptr);
+      const SeqSpan sq = seq_span<PACKED>(p, b, nullptr);
       const int row0 = qb * pf::QBLOCK;
       const int nt0 = kv_tiles_for(row0, sq.Sq, sq.Sk, p.causal);
       const int nt1 = kv_tiles_for(row0 + pf::BM, sq.Sq, sq.Sk, p.causal);
@@ -440,27 +487,34 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
     const uint32_t tO = t_lane + (i ? C::COL_O1 : C::COL_O0);
     const float c = p.c;
     const bool neg_scale = c < 0.f;
-    uint32_t s_cnt = 0, o_cnt = 0;
+    uint32_t s_cnt = 0, o_cnt = 0, next = 0;
     bool ok = true;
     T* const O = static_cast<T*>(p.o);
 
-    for (int w = blockIdx.x; w < p.n_items && ok; w += gridDim.x) {
+    for (uint32_t it = 0; ok; ++it) {
+      const int w =
+          dynamic ? sched_consume(it, sched_full, sched_empty, sched, abort_flag, &g_prefill_err, 16)
+                  : next_stride(&next);
+      if (w < 0) {
+        ok = w == -1;
+        break;
+      }
       int b, hq, qb;
       prefill_item(w, p.B, p.Hq, p.Hkv, p.n_qb, &b, &hq, &qb);
       // (the bounds bit for bad packed offsets is set by one thread per item)
-      const SeqSpan sq = seq_span(p, b, (i == 0 && r == 0) ? &g_prefill_err : nullptr);
+      const SeqSpan sq = seq_span<PACKED>(p, b, (i == 0 && r == 0) ? &g_prefill_err : nullptr);
       const int Sq = sq.Sq, Sk = sq.Sk, off = Sk - Sq;  // bottom-right causal offset
       const int row0 = qb * pf::QBLOCK + i * pf::BM;
       const int grow = row0 + r;
       const int n_i = kv_tiles_for(row0, Sq, Sk, p.causal);
       T* const orow = O + (sq.orow + grow) * (size_t)p.Hq * D + (size_t)hq * D;
       float* const lse_row =
-          p.lse ? p.lse + (p.cu_q ? (size_t)hq * p.total_q + sq.orow + grow
+          p.lse ? p.lse + (PACKED ? (size_t)hq * p.total_q + sq.orow + grow
                                   : ((size_t)b * p.Hq + hq) * p.Sq + grow)
                 : nullptr;
       // Self-check: the row must lie inside O (records and skips otherwise).
       const bool row_ok = grow < Sq && b < p.B && hq < p.Hq &&
-                          (!p.cu_q || sq.orow + grow < (size_t)p.total_q);
+                          (!PACKED || sq.orow + grow < (size_t)p.total_q);
       if (n_i == 0) {
         if (row_ok) {
 #pragma unroll
@@ -653,6 +707,15 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
+  // Every CTA has made its last claim once it gets here.  The last CTA out
+  // sets the work counter back to zero for the next launch that uses it.
+  if (!PACKED && threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(p.work_ctr + 1, 1u) == gridDim.x - 1) {
+      p.work_ctr[0] = 0u;
+      p.work_ctr[1] = 0u;
+    }
+  }
 }
 
 // Sk == 0: no key is visible to any row, O = 0 and log-sum-exp -inf.
@@ -680,7 +743,7 @@ struct PrefillShape {
 template <int D, typename T>
 static int launch_prefill_t(const void* q, const void* k, const void* v, void* o, float* lse,
                             const PrefillShape& sh, float scale, int causal,
-                            cudaStream_t stream) {
+                            unsigned int* work_ctr, cudaStream_t stream) {
   using C = pf::Cfg<D>;
   const bool packed = sh.cu_q != nullptr;
   CUtensorMap tq, tk, tv;
@@ -697,9 +760,12 @@ static int launch_prefill_t(const void* q, const void* k, const void* v, void* o
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, T>,
+    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, T, false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_TOTAL);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(prefill_kernel<D, T, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_TOTAL);
     if (e != cudaSuccess) return e;
     attr_set[dev] = 1;
   }
@@ -719,14 +785,62 @@ static int launch_prefill_t(const void* q, const void* k, const void* v, void* o
   p.causal = causal ? 1 : 0;
   p.n_qb = (sh.Sq + pf::QBLOCK - 1) / pf::QBLOCK;
   p.n_items = sh.B * sh.Hq * p.n_qb;
+  p.work_ctr = work_ctr;
   p.c = scale * 1.4426950408889634f;
   // scale == 0: every visible score is 0.  A tiny positive c keeps that (all
   // exp2 arguments round to 0) while hidden keys still map to -inf, never NaN.
   if (p.c == 0.f) p.c = 1e-30f;
   const int sms = sm_count() > 0 ? sm_count() : 148;
   const int grid = p.n_items < sms ? p.n_items : sms;
-  prefill_kernel<D, T><<<grid, pf::THREADS, C::SMEM_TOTAL, stream>>>(tq, tk, tv, p);
+  if (packed)
+    prefill_kernel<D, T, true><<<grid, pf::THREADS, C::SMEM_TOTAL, stream>>>(tq, tk, tv, p);
+  else
+    prefill_kernel<D, T, false><<<grid, pf::THREADS, C::SMEM_TOTAL, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
+}
+
+// Per-stream work counters of the prefill kernel: two uint32 per stream
+// (claims, CTAs finished), zero between launches because the last CTA of
+// every launch zeroes them.  Streams are told apart by cudaStreamGetId, which
+// is unique for the life of the process (so two streams never share a slot,
+// and launches that share one are ordered by their stream).  Slots come from
+// zero-filled chunks of device memory that live as long as the process.
+// Returns null when no slot can be made: the stream is being captured and
+// has none yet, or the device is out of memory; the caller then uses
+// stream-ordered scratch instead.
+static unsigned int* work_counter_for_stream(cudaStream_t stream) {
+  constexpr int kChunkSlots = 4096;
+  struct Pool {
+    std::unordered_map<unsigned long long, unsigned int*> slot;
+    unsigned int* chunk = nullptr;
+    int used = kChunkSlots;
+  };
+  static std::mutex mu;
+  static Pool pools[64];
+  int dev = 0;
+  unsigned long long id = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (cudaStreamGetId(stream, &id) != cudaSuccess) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  Pool& pl = pools[dev];
+  auto it = pl.slot.find(id);
+  if (it != pl.slot.end()) return it->second;
+  if (pl.used == kChunkSlots) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone)
+      return nullptr;
+    void* c = nullptr;
+    if (cudaMalloc(&c, kChunkSlots * 2 * sizeof(unsigned int)) != cudaSuccess) return nullptr;
+    if (cudaMemset(c, 0, kChunkSlots * 2 * sizeof(unsigned int)) != cudaSuccess) {
+      cudaFree(c);
+      return nullptr;
+    }
+    pl.chunk = static_cast<unsigned int*>(c);
+    pl.used = 0;
+  }
+  unsigned int* s = pl.chunk + 2 * pl.used++;
+  pl.slot.emplace(id, s);
+  return s;
 }
 
 static int launch_prefill_shape(const void* q, const void* k, const void* v, void* o,
@@ -747,11 +861,30 @@ static int launch_prefill_shape(const void* q, const void* k, const void* v, voi
                                                               nl);
     return cudaGetLastError();
   }
-  if (D == 64)
-    return bf16 ? launch_prefill_t<64, __nv_bfloat16>(q, k, v, o, lse, sh, scale, causal, stream)
-                : launch_prefill_t<64, __half>(q, k, v, o, lse, sh, scale, causal, stream);
-  return bf16 ? launch_prefill_t<128, __nv_bfloat16>(q, k, v, o, lse, sh, scale, causal, stream)
-              : launch_prefill_t<128, __half>(q, k, v, o, lse, sh, scale, causal, stream);
+  // The kernel's work counter: the stream's own slot (zero between launches),
+  // or, while the stream is being captured and has no slot yet, stream-ordered
+  // scratch zeroed here.
+  void* ctr = packed ? nullptr : work_counter_for_stream(stream);
+  const bool own = !packed && ctr == nullptr;
+  cudaError_t e = cudaSuccess;
+  if (own) {
+    e = cudaMallocAsync(&ctr, 2 * sizeof(unsigned int), stream);
+    if (e != cudaSuccess) return e;
+    e = cudaMemsetAsync(ctr, 0, 2 * sizeof(unsigned int), stream);
+  }
+  int r = e;
+  if (e == cudaSuccess) {
+    unsigned int* c = static_cast<unsigned int*>(ctr);  // null: fixed grid stride
+    if (D == 64)
+      r = bf16 ? launch_prefill_t<64, __nv_bfloat16>(q, k, v, o, lse, sh, scale, causal, c, stream)
+               : launch_prefill_t<64, __half>(q, k, v, o, lse, sh, scale, causal, c, stream);
+    else
+      r = bf16 ? launch_prefill_t<128, __nv_bfloat16>(q, k, v, o, lse, sh, scale, causal, c,
+                                                      stream)
+               : launch_prefill_t<128, __half>(q, k, v, o, lse, sh, scale, causal, c, stream);
+  }
+  const cudaError_t ef = own ? cudaFreeAsync(ctr, stream) : cudaSuccess;
+  return r != 0 ? r : (int)ef;
 }
 
 int launch_prefill(const void* q, const void* k, const void* v, void* o, float* lse, int B,

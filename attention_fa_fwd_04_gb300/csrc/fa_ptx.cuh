@@ -96,6 +96,47 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) 
 }
 
 // ---------------------------------------------------------------------------
+// Dynamic work schedule of a persistent, warp-specialised kernel: the
+// producer warp takes the next item index from a global counter (zero when
+// the launch starts) and hands it to the consumer warps through a ring of
+// kSchedSlots slots in shared memory.  sfull[i] takes 1 arrival (the
+// producer); sempty[i] takes one arrival per consumer warp.  (A deeper ring
+// measured no faster: the producer's single Q buffer already keeps it within
+// an item of its consumers.)  Both return the item, -1 when the work is
+// exhausted, or -2 when a wait gave up (the CTA is aborting).
+// ---------------------------------------------------------------------------
+constexpr int kSchedSlots = 2;
+
+__device__ __forceinline__ int sched_produce(uint32_t k, unsigned int* ctr, int n_items,
+                                             uint64_t* sfull, uint64_t* sempty,
+                                             volatile int* sched, volatile int* abort_flag,
+                                             unsigned int* err_word, bool leader) {
+  const int slot = k % kSchedSlots;
+  if (!mbar_wait(&sempty[slot], ((k / kSchedSlots) & 1) ^ 1, abort_flag, err_word, 14))
+    return -2;
+  int w = -1;
+  if (leader) {
+    const unsigned int t = atomicAdd(ctr, 1u);
+    w = t < (unsigned int)n_items ? (int)t : -1;
+    sched[slot] = w;
+    mbar_arrive(&sfull[slot]);
+  }
+  return __shfl_sync(0xffffffffu, w, 0);
+}
+
+// Whole warp: the item the producer published for step k.
+__device__ __forceinline__ int sched_consume(uint32_t k, uint64_t* sfull, uint64_t* sempty,
+                                             volatile int* sched, volatile int* abort_flag,
+                                             unsigned int* err_word, unsigned int site) {
+  const int slot = k % kSchedSlots;
+  if (!mbar_wait(&sfull[slot], (k / kSchedSlots) & 1, abort_flag, err_word, site)) return -2;
+  const int w = sched[slot];
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(&sempty[slot]);
+  return w;
+}
+
+// ---------------------------------------------------------------------------
 // TMA (tiled tensor loads into shared memory, completion on an mbarrier)
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {

@@ -114,3 +114,25 @@ def test_repeated_calls_are_identical(fa):
     b = fa.prefill(qd, kd, vd, 0.09, True)
     torch.cuda.synchronize()
     assert torch.equal(a, b)
+
+
+def test_work_counter_across_calls_and_streams(fa):
+    """Persistent CTAs claim work items from a per-stream counter that the last
+    CTA of each launch zeroes again.  Launches on one stream, interleaved with
+    launches on a second stream, must each cover every item exactly once: the
+    outputs are bit-identical (each item's arithmetic does not depend on which
+    CTA runs it) and match the oracle."""
+    q, k, v = fa_inputs.prefill_inputs(1, 16, 4, 1500, 1500, 64, torch.bfloat16, 21)
+    dev = torch.device("cuda", 0)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    side = torch.cuda.Stream()
+    main_outs, side_outs = [], []
+    for _ in range(4):
+        main_outs.append(fa.prefill(qd, kd, vd, 0.125, True))
+        with torch.cuda.stream(side):
+            side_outs.append(fa.prefill(qd, kd, vd, 0.125, True, stream=side))
+    torch.cuda.synchronize()
+    for o in main_outs[1:] + side_outs:
+        assert torch.equal(o, main_outs[0])
+    compare(main_outs[0].float().cpu().numpy(), oracle.attention(q, k, v, 0.125, True))
+    assert fa.fa_device_error()[0] == fa.FA_OK
