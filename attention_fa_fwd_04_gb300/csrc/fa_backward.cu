@@ -330,7 +330,8 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
       return r;
     };
     for (uint32_t it = 0; ok; ++it, ++local) {
-      const int w = sched_consume(it, sched_full, sched_empty, sched, abort_flag, &g_backward_err, 11);
+      const int w =
+          sched_consume(it, sched_full, sched_empty, sched, abort_flag, &g_backward_err, 11);
       if (w < 0) {
         ok = w == -1;
         break;
@@ -385,7 +386,8 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
     bool ok = true;
     T* const DQ = static_cast<T*>(p.dq);
     for (uint32_t it = 0; ok; ++it) {
-      const int w = sched_consume(it, sched_full, sched_empty, sched, abort_flag, &g_backward_err, 12);
+      const int w =
+          sched_consume(it, sched_full, sched_empty, sched, abort_flag, &g_backward_err, 12);
       if (w < 0) {
         ok = w == -1;
         break;
@@ -406,7 +408,12 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
         ++s_cnt;
         __syncwarp();
         tc_fence_after();
-        const int k0 = j * bw::BT;
+        // Keys [0, lim) of this row are visible: columns from lim_t on are
+        // hidden (selected to 0), which only the tile holding key lim has.
+        const int lim_t = lim - j * bw::BT;
+        const bool edge = __any_sync(0xffffffffu, lim_t < bw::BT);
+        const float2 c2 = make_float2(p.c, p.c), nl2 = make_float2(-l2, -l2);
+        const float2 nd2 = make_float2(-dl, -dl);
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
           uint32_t sr[32], pr[32];
@@ -418,16 +425,18 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
           uint32_t pk[16];
 #pragma unroll
           for (int x = 0; x < 16; ++x) {
-            float ds[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int key = k0 + q4 * 32 + 2 * x + e;
-              const float pv = key < lim
-                                   ? fast_exp2(__uint_as_float(sr[2 * x + e]) * p.c - l2)
-                                   : 0.f;
-              ds[e] = pv * (__uint_as_float(pr[2 * x + e]) - dl);
+            const float2 a = __ffma2_rn(
+                make_float2(__uint_as_float(sr[2 * x]), __uint_as_float(sr[2 * x + 1])), c2, nl2);
+            float2 pv = make_float2(fast_exp2(a.x), fast_exp2(a.y));
+            if (edge) {
+              const int col = q4 * 32 + 2 * x;
+              pv.x = col < lim_t ? pv.x : 0.f;
+              pv.y = col + 1 < lim_t ? pv.y : 0.f;
             }
-            pk[x] = BPack<T>::pack(ds[0], ds[1]);
+            const float2 dd = __fadd2_rn(
+                make_float2(__uint_as_float(pr[2 * x]), __uint_as_float(pr[2 * x + 1])), nd2);
+            const float2 ds = __fmul2_rn(pv, dd);
+            pk[x] = BPack<T>::pack(ds.x, ds.y);
           }
           tmem_st16(t_lane + bw::COL_S + q4 * 16, pk);
         }
@@ -661,7 +670,8 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
       __syncwarp();
     };
     for (uint32_t it = 0; ok; ++it, ++local) {
-      const int w = sched_consume(it, sched_full, sched_empty, sched, abort_flag, &g_backward_err, 11);
+      const int w =
+          sched_consume(it, sched_full, sched_empty, sched, abort_flag, &g_backward_err, 11);
       if (w < 0) {
         ok = w == -1;
         break;
@@ -704,7 +714,8 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
     T* const DK = static_cast<T*>(p.dk);
     T* const DV = static_cast<T*>(p.dv);
     for (uint32_t it = 0; ok; ++it) {
-      const int w = sched_consume(it, sched_full, sched_empty, sched, abort_flag, &g_backward_err, 12);
+      const int w =
+          sched_consume(it, sched_full, sched_empty, sched, abort_flag, &g_backward_err, 12);
       if (w < 0) {
         ok = w == -1;
         break;
@@ -729,8 +740,14 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
               reinterpret_cast<const float*>(sStage + s * C::STAGE_DKV + 2 * C::TILE_BYTES);
           const float* sD = sL + bw::BT;
           // Query row i sees key j when i < Sq and (not causal or j <= i + off).
-          const int i_min = p.causal ? j - off : 0;  // first query row seeing key j
-          const bool key_ok = j < p.Sk;
+          // Rows past Sq have lse = +inf in the stage, so their P is 0 without
+          // a test.  Key rows past Sk read zeros (TMA fill) and only feed dK /
+          // dV rows that are never stored.  What remains is the causal edge:
+          // columns below ic_lo are hidden, which only a tile on the diagonal
+          // has (its P is selected to 0 there).
+          const int ic_lo = p.causal ? j - off - t * bw::BT : 0;
+          const bool edge = __any_sync(0xffffffffu, ic_lo > 0);
+          const float2 c2 = make_float2(p.c, p.c);
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
             uint32_t sr[32], pr[32];
@@ -741,18 +758,31 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
             reg_fence32(pr);
             uint32_t pp[16], pd[16];
 #pragma unroll
-            for (int x = 0; x < 16; ++x) {
-              float pv[2], dv2[2];
+            for (int x4 = 0; x4 < 8; ++x4) {
+              // lse*log2(e) and Delta of 4 query columns (broadcast loads).
+              const float4 l4 = reinterpret_cast<const float4*>(sL)[q4 * 8 + x4];
+              const float4 d4 = reinterpret_cast<const float4*>(sD)[q4 * 8 + x4];
 #pragma unroll
-              for (int e = 0; e < 2; ++e) {
-                const int ic = q4 * 32 + 2 * x + e;  // query column within the tile
-                const int i = t * bw::BT + ic;
-                const bool vis = key_ok && i < p.Sq && i >= i_min;
-                pv[e] = vis ? fast_exp2(__uint_as_float(sr[2 * x + e]) * p.c - sL[ic]) : 0.f;
-                dv2[e] = pv[e] * (__uint_as_float(pr[2 * x + e]) - sD[ic]);
+              for (int h = 0; h < 2; ++h) {
+                const int x = x4 * 2 + h;  // column pair within the 32-column chunk
+                const float2 nl = h ? make_float2(-l4.z, -l4.w) : make_float2(-l4.x, -l4.y);
+                const float2 dl = h ? make_float2(d4.z, d4.w) : make_float2(d4.x, d4.y);
+                const float2 a = __ffma2_rn(
+                    make_float2(__uint_as_float(sr[2 * x]), __uint_as_float(sr[2 * x + 1])), c2,
+                    nl);
+                float2 pv = make_float2(fast_exp2(a.x), fast_exp2(a.y));
+                if (edge) {  // hidden columns select 0 (whatever the scale's sign)
+                  const int col = q4 * 32 + 2 * x;
+                  pv.x = col < ic_lo ? 0.f : pv.x;
+                  pv.y = col + 1 < ic_lo ? 0.f : pv.y;
+                }
+                const float2 dd = __fadd2_rn(
+                    make_float2(__uint_as_float(pr[2 * x]), __uint_as_float(pr[2 * x + 1])),
+                    make_float2(-dl.x, -dl.y));
+                const float2 ds = __fmul2_rn(pv, dd);
+                pp[x] = BPack<T>::pack(pv.x, pv.y);
+                pd[x] = BPack<T>::pack(ds.x, ds.y);
               }
-              pp[x] = BPack<T>::pack(pv[0], pv[1]);
-              pd[x] = BPack<T>::pack(dv2[0], dv2[1]);
             }
             tmem_st16(t_lane + bw::COL_S + q4 * 16, pp);
             tmem_st16(t_lane + bw::COL_DP + q4 * 16, pd);
