@@ -33,6 +33,8 @@ __device__ unsigned int g_backward_err = 0;
 namespace bw {
 constexpr int BT = 128;                // rows of every tile
 constexpr int HALF_BYTES = 128 * 128;  // 128 rows x 64 elements x 2 bytes
+constexpr int QS = 64;                 // query rows of a dkdv sub-tile
+constexpr int SUB_HALF = QS * 128;     // 64 rows x 64 elements x 2 bytes
 constexpr int THREADS = 192;           // warps 0-3 elementwise, 4 producer, 5 MMA
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_S = 0, COL_DP = 128, COL_ACC = 256;
@@ -43,12 +45,15 @@ struct Cfg {
   static constexpr int HALVES = D / 64;
   static constexpr int TILE_BYTES = HALVES * HALF_BYTES;  // one 128-row tile
   static constexpr int NSTAGE_DQ = 4;    // K/V ring of the dq kernel (K_j, V_j alternate)
-  static constexpr int NSTAGE_DKV = 2;   // (Q, dO) ring of the dkdv kernel
+  static constexpr int NSTAGE_DKV = 4;   // (Q, dO) sub-tile ring of the dkdv kernel
   static constexpr int SMEM_BAR = 512;
   static constexpr int SMEM_DQ = 1024 + 2 * TILE_BYTES + NSTAGE_DQ * TILE_BYTES + SMEM_BAR;
-  // dkdv stage: Q tile, dO tile, then lse*log2(e) and Delta of its 128 rows.
-  static constexpr int STAGE_DKV = 2 * TILE_BYTES + 2 * BT * 4;
-  static constexpr int SMEM_DKV = 1024 + 2 * TILE_BYTES + NSTAGE_DKV * STAGE_DKV + SMEM_BAR;
+  // dkdv stage: a 64-row Q sub-tile and its dO sub-tile (1 KiB aligned); the
+  // stages' lse*log2(e) and Delta rows follow the ring.
+  static constexpr int SUB_BYTES = HALVES * SUB_HALF;
+  static constexpr int STAGE_DKV = 2 * SUB_BYTES;
+  static constexpr int SMEM_DKV =
+      1024 + 2 * TILE_BYTES + NSTAGE_DKV * (STAGE_DKV + 2 * QS * 4) + SMEM_BAR;
 };
 }  // namespace bw
 
@@ -414,31 +419,44 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
         const bool edge = __any_sync(0xffffffffu, lim_t < bw::BT);
         const float2 c2 = make_float2(p.c, p.c), nl2 = make_float2(-l2, -l2);
         const float2 nd2 = make_float2(-dl, -dl);
+        // Software-pipelined TMEM reads, as in the dK/dV kernel.
+        uint32_t sr[2][32], pr[2][32];
+        tmem_ld32(t_lane + bw::COL_S, sr[0]);
+        tmem_ld32(t_lane + bw::COL_DP, pr[0]);
+        tmem_wait_ld();
+        reg_fence32(sr[0]);
+        reg_fence32(pr[0]);
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
-          uint32_t sr[32], pr[32];
-          tmem_ld32(t_lane + bw::COL_S + q4 * 32, sr);
-          tmem_ld32(t_lane + bw::COL_DP + q4 * 32, pr);
-          tmem_wait_ld();
-          reg_fence32(sr);
-          reg_fence32(pr);
+          const int cur = q4 & 1;
+          if (q4 < 3) {
+            tmem_ld32(t_lane + bw::COL_S + (q4 + 1) * 32, sr[cur ^ 1]);
+            tmem_ld32(t_lane + bw::COL_DP + (q4 + 1) * 32, pr[cur ^ 1]);
+          }
           uint32_t pk[16];
 #pragma unroll
           for (int x = 0; x < 16; ++x) {
-            const float2 a = __ffma2_rn(
-                make_float2(__uint_as_float(sr[2 * x]), __uint_as_float(sr[2 * x + 1])), c2, nl2);
+            const float2 a = __ffma2_rn(make_float2(__uint_as_float(sr[cur][2 * x]),
+                                                    __uint_as_float(sr[cur][2 * x + 1])),
+                                        c2, nl2);
             float2 pv = make_float2(fast_exp2(a.x), fast_exp2(a.y));
             if (edge) {
               const int col = q4 * 32 + 2 * x;
               pv.x = col < lim_t ? pv.x : 0.f;
               pv.y = col + 1 < lim_t ? pv.y : 0.f;
             }
-            const float2 dd = __fadd2_rn(
-                make_float2(__uint_as_float(pr[2 * x]), __uint_as_float(pr[2 * x + 1])), nd2);
+            const float2 dd = __fadd2_rn(make_float2(__uint_as_float(pr[cur][2 * x]),
+                                                     __uint_as_float(pr[cur][2 * x + 1])),
+                                         nd2);
             const float2 ds = __fmul2_rn(pv, dd);
             pk[x] = BPack<T>::pack(ds.x, ds.y);
           }
           tmem_st16(t_lane + bw::COL_S + q4 * 16, pk);
+          if (q4 < 3) {
+            tmem_wait_ld();
+            reg_fence32(sr[cur ^ 1]);
+            reg_fence32(pr[cur ^ 1]);
+          }
         }
         tmem_wait_st();
         tc_fence_before();
@@ -492,6 +510,15 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
 
 // ------------------------------------------------------------------------------
 // dk, dv
+//
+// Per 128-key tile, the visible query rows are taken 64 at a time (a
+// sub-tile) so that S^T / dP^T can be double-buffered in TMEM:
+//   columns [0, 64) S^T(0), [64, 128) dP^T(0), [128, 192) S^T(1),
+//   [192, 256) dP^T(1), then dV and dK (D columns each).
+// While the element-wise warps turn buffer b into P^T / dS^T, the MMA warp
+// already computes the next sub-tile's S^T / dP^T into buffer b ^ 1; then it
+// issues dV += P^T dO and dK += dS^T Q for buffer b.  MMA issue order:
+//   S(u), dP(u), [wait P/dS(u-1)], dV(u-1), dK(u-1), S(u+1), ...
 // ------------------------------------------------------------------------------
 template <int D, typename T>
 __global__ void __launch_bounds__(bw::THREADS, 1)
@@ -502,21 +529,23 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
   using C = bw::Cfg<D>;
   constexpr bool kBF16 = BIsBF16<T>::value;
   constexpr int NS = C::NSTAGE_DKV;
+  constexpr int QS = bw::QS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sK = smem;
   uint8_t* sV = smem + C::TILE_BYTES;
-  uint8_t* sStage = smem + 2 * C::TILE_BYTES;  // [NS] x (Q, dO, lse*log2e, Delta)
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sStage + NS * C::STAGE_DKV);
-  uint64_t* full = bars;          // [NS]
-  uint64_t* empty = bars + NS;    // [NS]: MMA commit + 128 elementwise arrivals
+  uint8_t* sStage = smem + 2 * C::TILE_BYTES;  // [NS] x (Q sub-tile, dO sub-tile)
+  float* sLD = reinterpret_cast<float*>(sStage + NS * C::STAGE_DKV);  // [NS][lse*log2e, Delta][QS]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sLD + NS * 2 * QS);
+  uint64_t* full = bars;          // [NS]: producer (expect_tx) + producer (after lse/Delta)
+  uint64_t* empty = bars + NS;    // [NS]: MMA commit + 128 element-wise arrivals
   uint64_t* kv_full = bars + 2 * NS;
   uint64_t* kv_empty = kv_full + 1;
-  uint64_t* st_full = kv_full + 2;  // S^T and dP^T in TMEM
-  uint64_t* pd_full = kv_full + 3;  // P^T and dS^T in TMEM (128 arrivals)
-  uint64_t* o_full = kv_full + 4;   // dK, dV complete
-  uint64_t* drain = kv_full + 5;
-  uint64_t* sched_full = kv_full + 6;                // [kSchedSlots]
+  uint64_t* st_full = kv_full + 2;  // [2] S^T and dP^T of buffer b in TMEM
+  uint64_t* pd_full = kv_full + 4;  // [2] P^T and dS^T of buffer b in TMEM (128 arrivals)
+  uint64_t* o_full = kv_full + 6;   // dK, dV complete
+  uint64_t* drain = kv_full + 7;
+  uint64_t* sched_full = kv_full + 8;                // [kSchedSlots]
   uint64_t* sched_empty = sched_full + kSchedSlots;  // [kSchedSlots]
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sched_empty + kSchedSlots);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
@@ -524,16 +553,16 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    // full[s]: the producer arrives twice per phase (with the tile bytes
-    // expected, then after writing the stage's lse / Delta rows).
     for (int s = 0; s < NS; ++s) {
       mbar_init(&full[s], 2);
       mbar_init(&empty[s], 1 + bw::BT);
     }
     mbar_init(kv_full, 1);
     mbar_init(kv_empty, 1);
-    mbar_init(st_full, 1);
-    mbar_init(pd_full, bw::BT);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&st_full[i], 1);
+      mbar_init(&pd_full[i], bw::BT);
+    }
     mbar_init(o_full, 1);
     mbar_init(drain, 1);
     for (int i = 0; i < kSchedSlots; ++i) {
@@ -553,6 +582,15 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
   const uint32_t tmem = *tmem_holder;
   const bool leader = lane == 0;
   const int off = p.Sk - p.Sq;
+  const int n_qs = (p.Sq + QS - 1) / QS;
+  // First query sub-tile that sees key row k0 (n_qs if none).
+  auto first_sub = [&](int k0) {
+    if (!p.causal) return 0;
+    const int i0 = k0 - off;  // the first query row that sees key k0
+    if (i0 >= p.Sq) return n_qs;
+    return i0 <= 0 ? 0 : i0 / QS;
+  };
+  constexpr uint32_t COL_DV = 256, COL_DK = 256 + D;
 
   if (warp == 4) {
     // ================================ producer ================================
@@ -575,7 +613,7 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
       }
       int b, hkv, kt;
       dkv_item(w, p, &b, &hkv, &kt);
-      const int t0 = bw_first_query_tile(kt * bw::BT, p);
+      const int q0 = first_sub(kt * bw::BT);
       kv_issued = false;
       if (local > 0 &&
           !(ok = mbar_wait(kv_empty, (local - 1) & 1, abort_flag, &g_backward_err, 1)))
@@ -592,33 +630,33 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
       }
       __syncwarp();
       kv_issued = true;
-      // Query tiles descending, the group's heads innermost: the items of one
-      // kv head then read the same Q / dO tiles at about the same time.
-      for (int t = p.n_qt - 1; t >= t0 && ok; --t) {
+      // Query sub-tiles descending, the group's heads innermost: the items of
+      // one kv head then read the same Q / dO tiles at about the same time.
+      for (int qs = n_qs - 1; qs >= q0 && ok; --qs) {
         for (int g = 0; g < p.G && ok; ++g) {
           const int hq = hkv * p.G + g;
           const int s = st_cnt % NS;
           const uint32_t ph = (st_cnt / NS) & 1;
           if (!(ok = mbar_wait(&empty[s], ph ^ 1, abort_flag, &g_backward_err, 2))) break;
           uint8_t* st = sStage + s * C::STAGE_DKV;
-          float* sL = reinterpret_cast<float*>(st + 2 * C::TILE_BYTES);
-          float* sD = sL + bw::BT;
+          float* sL = sLD + s * 2 * QS;
+          float* sD = sL + QS;
           if (leader) {
-            mbar_arrive_expect_tx(&full[s], 2 * C::TILE_BYTES);
+            mbar_arrive_expect_tx(&full[s], 2 * C::SUB_BYTES);
 #pragma unroll
             for (int h = 0; h < C::HALVES; ++h) {
-              tma_load_4d_hint(st + h * bw::HALF_BYTES, &tmQ, &full[s], h * 64, hq, t * bw::BT, b,
+              tma_load_4d_hint(st + h * bw::SUB_HALF, &tmQ, &full[s], h * 64, hq, qs * QS, b,
                                pol_q);
-              tma_load_4d_hint(st + C::TILE_BYTES + h * bw::HALF_BYTES, &tmDO, &full[s], h * 64,
-                               hq, t * bw::BT, b, pol_q);
+              tma_load_4d_hint(st + C::SUB_BYTES + h * bw::SUB_HALF, &tmDO, &full[s], h * 64, hq,
+                               qs * QS, b, pol_q);
             }
           }
-          // lse * log2(e) and Delta of the tile's 128 query rows (+inf / 0 past Sq:
-          // those columns get P = 0).
+          // lse * log2(e) and Delta of the sub-tile's 64 query rows (+inf / 0
+          // past Sq: those columns get P = 0).
           const size_t base = ((size_t)b * p.Hq + hq) * p.Sq;
 #pragma unroll
-          for (int x = 0; x < 4; ++x) {
-            const int i = t * bw::BT + x * 32 + lane;
+          for (int x = 0; x < QS / 32; ++x) {
+            const int i = qs * QS + x * 32 + lane;
             sL[x * 32 + lane] = i < p.Sq ? p.lse[base + i] * bw::LOG2E : INFINITY;
             sD[x * 32 + lane] = i < p.Sq ? p.delta[base + i] : 0.f;
           }
@@ -637,28 +675,30 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
     __syncwarp();
   } else if (warp == 5) {
     // ================================== MMA ===================================
-    constexpr uint32_t IDESC_S = idesc_f16(bw::BT, bw::BT, kBF16, false);
+    constexpr uint32_t IDESC_S = idesc_f16(bw::BT, QS, kBF16, false);
     constexpr uint32_t IDESC_ACC = idesc_f16(bw::BT, D, kBF16, true);
     const uint32_t sk_addr = smem_u32(sK), sv_addr = smem_u32(sV), sst = smem_u32(sStage);
-    uint32_t st_cnt = 0, local = 0, pd_cnt = 0;
+    uint32_t st_cnt = 0, local = 0, gcnt = 0;
     bool ok = true;
+    // D_tmem (128 x 64) = A (128-row tile, K-major) x B^T (64-row sub-tile, K-major).
     auto issue_nt = [&](uint32_t d_col, uint32_t a_addr, uint32_t b_addr) {
       if (leader) {
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const uint32_t hoff = (k >> 2) * bw::HALF_BYTES + (k & 3) * 32;
-          mma_ss(tmem + d_col, sdesc_sw128(a_addr + hoff, 16, 1024),
-                 sdesc_sw128(b_addr + hoff, 16, 1024), IDESC_S, k > 0 ? 1u : 0u);
+          const uint32_t ka = (k >> 2) * bw::HALF_BYTES + (k & 3) * 32;
+          const uint32_t kb = (k >> 2) * bw::SUB_HALF + (k & 3) * 32;
+          mma_ss(tmem + d_col, sdesc_sw128(a_addr + ka, 16, 1024),
+                 sdesc_sw128(b_addr + kb, 16, 1024), IDESC_S, k > 0 ? 1u : 0u);
         }
       }
       __syncwarp();
     };
-    // acc += A (TMEM, 16-bit, columns a_col..) x B (MN-major smem tile).
+    // acc += A (TMEM, 16-bit, 64 columns of K) x B (64-row sub-tile, MN-major).
     auto issue_acc = [&](uint32_t d_col, uint32_t a_col, uint32_t b_addr, bool accumulate) {
       if (leader) {
 #pragma unroll
-        for (int k = 0; k < bw::BT / 16; ++k) {
-          const uint64_t bd = sdesc_sw128(b_addr + k * 16 * 128, bw::HALF_BYTES, 1024);
+        for (int k = 0; k < QS / 16; ++k) {
+          const uint64_t bd = sdesc_sw128(b_addr + k * 16 * 128, bw::SUB_HALF, 1024);
           mma_ts(tmem + d_col, tmem + a_col + k * 8, bd, IDESC_ACC,
                  (accumulate || k > 0) ? 1u : 0u);
         }
@@ -669,6 +709,17 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
       if (leader) mma_commit(bar);
       __syncwarp();
     };
+    // dV += P^T dO and dK += dS^T Q of the sub-step held in buffer gb, stage s.
+    auto issue_grads = [&](uint32_t gb, int s, bool accumulate) {
+      const int bb = gb & 1;
+      if (!mbar_wait(&pd_full[bb], (gb >> 1) & 1, abort_flag, &g_backward_err, 5)) return false;
+      tc_fence_after();
+      const uint32_t sq = sst + s * C::STAGE_DKV, sdo = sq + C::SUB_BYTES;
+      issue_acc(COL_DV, bb * 128, sdo, accumulate);      // dV += P^T dO
+      issue_acc(COL_DK, bb * 128 + 64, sq, accumulate);  // dK += dS^T Q
+      commit(&empty[s]);
+      return true;
+    };
     for (uint32_t it = 0; ok; ++it, ++local) {
       const int w =
           sched_consume(it, sched_full, sched_empty, sched, abort_flag, &g_backward_err, 11);
@@ -678,27 +729,26 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
       }
       int b, hkv, kt;
       dkv_item(w, p, &b, &hkv, &kt);
-      const int t0 = bw_first_query_tile(kt * bw::BT, p);
-      const int steps = p.G * (p.n_qt - t0);
+      const int steps = p.G * (n_qs - first_sub(kt * bw::BT));
       if (!(ok = mbar_wait(kv_full, local & 1, abort_flag, &g_backward_err, 3))) break;
       tc_fence_after();
-      for (int u = 0; u < steps && ok; ++u) {
+      int s_prev = 0;
+      for (int u = 0; u < steps && ok; ++u, ++gcnt) {
         const int s = st_cnt % NS;
         const uint32_t ph = (st_cnt / NS) & 1;
         ++st_cnt;
         if (!(ok = mbar_wait(&full[s], ph, abort_flag, &g_backward_err, 4))) break;
         tc_fence_after();
-        const uint32_t sq = sst + s * C::STAGE_DKV, sdo = sq + C::TILE_BYTES;
-        issue_nt(bw::COL_S, sk_addr, sq);    // S^T = K Q^T
-        issue_nt(bw::COL_DP, sv_addr, sdo);  // dP^T = V dO^T
-        commit(st_full);
-        if (!(ok = mbar_wait(pd_full, pd_cnt & 1, abort_flag, &g_backward_err, 5))) break;
-        ++pd_cnt;
-        tc_fence_after();
-        issue_acc(bw::COL_ACC, bw::COL_S, sdo, u > 0);      // dV += P^T dO
-        issue_acc(bw::COL_ACC + D, bw::COL_DP, sq, u > 0);  // dK += dS^T Q
-        commit(&empty[s]);
+        const uint32_t bb = gcnt & 1;
+        const uint32_t sq = sst + s * C::STAGE_DKV, sdo = sq + C::SUB_BYTES;
+        issue_nt(bb * 128, sk_addr, sq);       // S^T = K Q^T
+        issue_nt(bb * 128 + 64, sv_addr, sdo); // dP^T = V dO^T
+        commit(&st_full[bb]);
+        if (u > 0 && !(ok = issue_grads(gcnt - 1, s_prev, u > 1))) break;
+        s_prev = s;
       }
+      if (!ok) break;
+      if (steps > 0 && !(ok = issue_grads(gcnt - 1, s_prev, steps > 1))) break;
       commit(kv_empty);
       commit(o_full);
     }
@@ -709,10 +759,11 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
     // ======================= P^T and dS^T (warps 0-3) =======================
     const int r = warp * 32 + lane;  // TMEM lane = key row within the tile
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    uint32_t st_cnt = 0, ph_cnt = 0, o_cnt = 0;
+    uint32_t ph_cnt = 0, gcnt = 0, o_cnt = 0;
     bool ok = true;
     T* const DK = static_cast<T*>(p.dk);
     T* const DV = static_cast<T*>(p.dv);
+    const float2 c2 = make_float2(p.c, p.c);
     for (uint32_t it = 0; ok; ++it) {
       const int w =
           sched_consume(it, sched_full, sched_empty, sched, abort_flag, &g_backward_err, 12);
@@ -722,74 +773,86 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
       }
       int b, hkv, kt;
       dkv_item(w, p, &b, &hkv, &kt);
-      const int t0 = bw_first_query_tile(kt * bw::BT, p);
+      const int q0 = first_sub(kt * bw::BT);
       const int j = kt * bw::BT + r;  // key row
-      for (int t = p.n_qt - 1; t >= t0 && ok; --t) {
-        for (int g = 0; g < p.G && ok; ++g) {
+      for (int qs = n_qs - 1; qs >= q0 && ok; --qs) {
+        for (int g = 0; g < p.G && ok; ++g, ++gcnt) {
           const int s = ph_cnt % NS;
           const uint32_t fph = (ph_cnt / NS) & 1;
           ++ph_cnt;
+          const uint32_t bb = gcnt & 1;
           // The stage's lse / Delta rows are written by the producer before
-          // its arrival on full[s].
+          // its second arrival on full[s].
           if (!(ok = mbar_wait(&full[s], fph, abort_flag, &g_backward_err, 9))) break;
-          if (!(ok = mbar_wait(st_full, st_cnt & 1, abort_flag, &g_backward_err, 7))) break;
-          ++st_cnt;
+          if (!(ok = mbar_wait(&st_full[bb], (gcnt >> 1) & 1, abort_flag, &g_backward_err, 7)))
+            break;
           __syncwarp();
           tc_fence_after();
-          const float* sL =
-              reinterpret_cast<const float*>(sStage + s * C::STAGE_DKV + 2 * C::TILE_BYTES);
-          const float* sD = sL + bw::BT;
-          // Query row i sees key j when i < Sq and (not causal or j <= i + off).
-          // Rows past Sq have lse = +inf in the stage, so their P is 0 without
-          // a test.  Key rows past Sk read zeros (TMA fill) and only feed dK /
-          // dV rows that are never stored.  What remains is the causal edge:
-          // columns below ic_lo are hidden, which only a tile on the diagonal
-          // has (its P is selected to 0 there).
-          const int ic_lo = p.causal ? j - off - t * bw::BT : 0;
+          const float* sL = sLD + s * 2 * QS;
+          const float* sD = sL + QS;
+          // Query row i = qs * 64 + ic sees key j when i < Sq and (not causal or
+          // j <= i + off).  Rows past Sq have lse = +inf in the stage, so their
+          // P is 0 without a test; key rows past Sk read zeros (TMA fill) and
+          // only feed dK / dV rows that are never stored.  What remains is the
+          // causal edge: columns below ic_lo are hidden (P selected to 0),
+          // which only a sub-tile on the diagonal has.
+          const int ic_lo = p.causal ? j - off - qs * QS : 0;
           const bool edge = __any_sync(0xffffffffu, ic_lo > 0);
-          const float2 c2 = make_float2(p.c, p.c);
+          const uint32_t cs = bb * 128, cdp = bb * 128 + 64;
+          // Software-pipelined TMEM reads: chunk q + 1 in flight while chunk q
+          // is computed.
+          uint32_t sr[2][32], pr[2][32];
+          tmem_ld32(t_lane + cs, sr[0]);
+          tmem_ld32(t_lane + cdp, pr[0]);
+          tmem_wait_ld();
+          reg_fence32(sr[0]);
+          reg_fence32(pr[0]);
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            uint32_t sr[32], pr[32];
-            tmem_ld32(t_lane + bw::COL_S + q4 * 32, sr);
-            tmem_ld32(t_lane + bw::COL_DP + q4 * 32, pr);
-            tmem_wait_ld();
-            reg_fence32(sr);
-            reg_fence32(pr);
+          for (int q2 = 0; q2 < QS / 32; ++q2) {
+            const int cur = q2 & 1;
+            if (q2 + 1 < QS / 32) {
+              tmem_ld32(t_lane + cs + (q2 + 1) * 32, sr[cur ^ 1]);
+              tmem_ld32(t_lane + cdp + (q2 + 1) * 32, pr[cur ^ 1]);
+            }
             uint32_t pp[16], pd[16];
 #pragma unroll
             for (int x4 = 0; x4 < 8; ++x4) {
               // lse*log2(e) and Delta of 4 query columns (broadcast loads).
-              const float4 l4 = reinterpret_cast<const float4*>(sL)[q4 * 8 + x4];
-              const float4 d4 = reinterpret_cast<const float4*>(sD)[q4 * 8 + x4];
+              const float4 l4 = reinterpret_cast<const float4*>(sL)[q2 * 8 + x4];
+              const float4 d4 = reinterpret_cast<const float4*>(sD)[q2 * 8 + x4];
 #pragma unroll
               for (int h = 0; h < 2; ++h) {
                 const int x = x4 * 2 + h;  // column pair within the 32-column chunk
                 const float2 nl = h ? make_float2(-l4.z, -l4.w) : make_float2(-l4.x, -l4.y);
-                const float2 dl = h ? make_float2(d4.z, d4.w) : make_float2(d4.x, d4.y);
-                const float2 a = __ffma2_rn(
-                    make_float2(__uint_as_float(sr[2 * x]), __uint_as_float(sr[2 * x + 1])), c2,
-                    nl);
+                const float2 nd = h ? make_float2(-d4.z, -d4.w) : make_float2(-d4.x, -d4.y);
+                const float2 a = __ffma2_rn(make_float2(__uint_as_float(sr[cur][2 * x]),
+                                                        __uint_as_float(sr[cur][2 * x + 1])),
+                                            c2, nl);
                 float2 pv = make_float2(fast_exp2(a.x), fast_exp2(a.y));
-                if (edge) {  // hidden columns select 0 (whatever the scale's sign)
-                  const int col = q4 * 32 + 2 * x;
+                if (edge) {
+                  const int col = q2 * 32 + 2 * x;
                   pv.x = col < ic_lo ? 0.f : pv.x;
                   pv.y = col + 1 < ic_lo ? 0.f : pv.y;
                 }
-                const float2 dd = __fadd2_rn(
-                    make_float2(__uint_as_float(pr[2 * x]), __uint_as_float(pr[2 * x + 1])),
-                    make_float2(-dl.x, -dl.y));
+                const float2 dd = __fadd2_rn(make_float2(__uint_as_float(pr[cur][2 * x]),
+                                                         __uint_as_float(pr[cur][2 * x + 1])),
+                                             nd);
                 const float2 ds = __fmul2_rn(pv, dd);
                 pp[x] = BPack<T>::pack(pv.x, pv.y);
                 pd[x] = BPack<T>::pack(ds.x, ds.y);
               }
             }
-            tmem_st16(t_lane + bw::COL_S + q4 * 16, pp);
-            tmem_st16(t_lane + bw::COL_DP + q4 * 16, pd);
+            tmem_st16(t_lane + cs + q2 * 16, pp);
+            tmem_st16(t_lane + cdp + q2 * 16, pd);
+            if (q2 + 1 < QS / 32) {
+              tmem_wait_ld();
+              reg_fence32(sr[cur ^ 1]);
+              reg_fence32(pr[cur ^ 1]);
+            }
           }
           tmem_wait_st();
           tc_fence_before();
-          mbar_arrive(pd_full);
+          mbar_arrive(&pd_full[bb]);
           mbar_arrive(&empty[s]);  // this thread is done with the stage's lse / Delta
         }
       }
@@ -799,17 +862,18 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
       ++o_cnt;
       __syncwarp();
       tc_fence_after();
-      const bool any = p.G * (p.n_qt - t0) > 0;
+      const bool any = p.G * (n_qs - q0) > 0;
       const bool row_ok = j < p.Sk;
 #pragma unroll
       for (int which = 0; which < 2; ++which) {  // 0: dV, 1: dK
-        T* const row = (which ? DK : DV) + (((size_t)b * p.Sk + (row_ok ? j : 0)) * p.Hkv + hkv) * D;
+        T* const row =
+            (which ? DK : DV) + (((size_t)b * p.Sk + (row_ok ? j : 0)) * p.Hkv + hkv) * D;
         const float mul = which ? p.scale : 1.f;
 #pragma unroll
         for (int q4 = 0; q4 < D / 32; ++q4) {
           uint32_t ar[32];
           if (any) {
-            tmem_ld32(t_lane + bw::COL_ACC + which * D + q4 * 32, ar);
+            tmem_ld32(t_lane + (which ? COL_DK : COL_DV) + q4 * 32, ar);
             tmem_wait_ld();
             reg_fence32(ar);
           } else {
@@ -872,6 +936,10 @@ static int launch_backward_t(const void* q, const void* k, const void* v, const 
   if (encode_tmap_rows(&tdo, dout, D, Hq, Sq, B, bw::BT)) return cudaErrorInvalidValue;
   if (encode_tmap_rows(&tk, k, D, Hkv, Sk, B, bw::BT)) return cudaErrorInvalidValue;
   if (encode_tmap_rows(&tv, v, D, Hkv, Sk, B, bw::BT)) return cudaErrorInvalidValue;
+  // The dkdv kernel reads Q and dO in 64-row sub-tiles.
+  CUtensorMap tq64, tdo64;
+  if (encode_tmap_rows(&tq64, q, D, Hq, Sq, B, bw::QS)) return cudaErrorInvalidValue;
+  if (encode_tmap_rows(&tdo64, dout, D, Hq, Sq, B, bw::QS)) return cudaErrorInvalidValue;
   static int attr_set[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -914,7 +982,7 @@ static int launch_backward_t(const void* q, const void* k, const void* v, const 
   p.work_ctr = ctr + 1;
   if (p.n_items > 0) {
     const int grid = p.n_items < sms ? p.n_items : sms;
-    bwd_dkdv_kernel<D, T><<<grid, bw::THREADS, C::SMEM_DKV, stream>>>(tq, tk, tv, tdo, p);
+    bwd_dkdv_kernel<D, T><<<grid, bw::THREADS, C::SMEM_DKV, stream>>>(tq64, tk, tv, tdo64, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
