@@ -15,14 +15,12 @@
 //   grid   = (nsplit, Hkv * ceil(G/16), B), one CTA per SM, sized from cap and
 //            the SM count (not from L, which the host never reads);
 //   CTA    = 1 producer warp issuing TMA tile loads (32 tokens x D, K and V,
-//            128-byte swizzle) into a 6-stage mbarrier ring (12 for D = 64,
-//            96 KiB in flight), and 3 consumer
+//            128-byte swizzle) into an 8-stage mbarrier ring (16 for D = 64,
+//            128 KiB in flight), and 4 consumer
 //            warps that each own whole tiles: S = Q K^T and O += P V with
 //            mma.sync m16n8k16 (the group's query heads padded to M = 16), an
 //            exp2 online softmax per warp, then a cross-warp merge in shared
-//            memory (over the drained ring) into one (max, sum, o[D]) partial
-//            per head and split.  About 97 KiB a CTA: two fit on an SM, so the
-//            next call's CTAs are resident before this call's exit;
+//            memory into one (max, sum, o[D]) partial per head and split;
 //   combine= one CTA per (32 columns, head, b) merges the split partials with
 //            weights exp2(m_s - M).
 // Both kernels are launched as programmatic dependents of the grid before
@@ -42,7 +40,7 @@ __device__ unsigned int g_decode_err = 0;
 
 namespace dec {
 constexpr int TT = 32;        // tokens per tile
-constexpr int NWARPS = 3;     // consumer warps
+constexpr int NWARPS = 4;     // consumer warps
 constexpr int THREADS = (NWARPS + 1) * 32;
 constexpr int HB = 16;        // query heads per CTA: the MMA's M
 constexpr int HALF_BYTES = TT * 128;  // TT rows x 64 elements x 2 bytes
@@ -59,7 +57,7 @@ constexpr int PREFETCH_BYTES = 384 * 1024;
 template <int D>
 struct Cfg {
   static constexpr int HALVES = D / 64;
-  static constexpr int NSTAGE = (D == 128) ? 6 : 12;    // 96 KiB of tiles in flight
+  static constexpr int NSTAGE = (D == 128) ? 8 : 16;    // 128 KiB of tiles in flight
   static constexpr int KV_BYTES = HALVES * HALF_BYTES;  // one K (or V) tile
   static constexpr int STAGE_BYTES = 2 * KV_BYTES;      // K tile + V tile
   static constexpr int SMEM_STAGES = NSTAGE * STAGE_BYTES;
@@ -67,11 +65,7 @@ struct Cfg {
   static constexpr int SMEM_RED = NWARPS * HB * D * 4 + NWARPS * HB * 2 * 4 + NWARPS * HB * 4;
   static constexpr int SMEM_BAR = 2 * NSTAGE * 8 + 16 + NSTAGE * 4;
   static_assert(HALF_BYTES % 1024 == 0, "128-byte-swizzled tiles need 1 KiB alignment");
-  // The merge buffers reuse the tile ring once every tile is consumed.  At
-  // about 97 KiB a CTA, two fit on an SM: the next call's CTAs become resident
-  // (and warm L2 with their first tiles) while this call still streams.
-  static constexpr int SMEM_DATA = SMEM_STAGES > SMEM_RED ? SMEM_STAGES : SMEM_RED;
-  static constexpr int SMEM_TOTAL = 1024 + SMEM_DATA + SMEM_BAR;
+  static constexpr int SMEM_TOTAL = 1024 + SMEM_STAGES + SMEM_RED + SMEM_BAR;
 };
 }  // namespace dec
 
@@ -120,10 +114,10 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* stages = smem;
-  float* red_o = reinterpret_cast<float*>(smem);  // [NW][HB][D], over the tile ring
+  float* red_o = reinterpret_cast<float*>(smem + C::SMEM_STAGES);  // [NW][HB][D]
   float* red_ml = red_o + NW * HB * D;                             // [NW][HB][2]
   float* red_w = red_ml + NW * HB * 2;                             // [NW][HB] merge weights
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::SMEM_DATA);
+  uint64_t* full = reinterpret_cast<uint64_t*>(red_w + NW * HB);
   uint64_t* empty = full + NSTAGE;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + NSTAGE);
   // Per stage: 1 when the producer could not map the tile to a valid page (its
@@ -394,11 +388,6 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
     l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-  }
-  // Every tile has been consumed (and every load has landed): the ring is free
-  // for the merge buffers.
-  __syncthreads();
-  if (warp < NW) {
     if (tq == 0) {
       red_ml[(warp * HB + g) * 2 + 0] = m0;
       red_ml[(warp * HB + g) * 2 + 1] = l0;
@@ -480,9 +469,7 @@ constexpr int kMaxSplits = kCombineThreads;
 constexpr int kSplitsPerWarp = kMaxSplits / kCombineWarps;
 
 template <int D>
-// At most 48 registers a thread: a combine CTA then fits on an SM beside two
-// split CTAs (this call's and the next call's).
-__global__ void __launch_bounds__(kCombineThreads, 5) decode_combine_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const DecodeParams p) {
   // A programmatic dependent launched after this grid (the next call's split
   // kernel) may start its prologue now; it waits for this grid to complete
   // before it reads or writes anything.
