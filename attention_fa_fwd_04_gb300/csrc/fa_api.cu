@@ -287,9 +287,11 @@ extern "C" const char* fa_status_string(int status) {
     case FA_ERR_CUDA: return "FA_ERR_CUDA: CUDA call or kernel launch failed";
     case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a device pipeline wait hit its time limit";
     case FA_ERR_TOO_LARGE:
-      return "FA_ERR_TOO_LARGE: request needs more scratch than fa_decode_fwd_noalloc's fixed array";
+      return "FA_ERR_TOO_LARGE: request needs more scratch than "
+             "fa_decode_fwd_noalloc's fixed array";
     case FA_ERR_BOUNDS:
-      return "FA_ERR_BOUNDS: a device-side bounds check skipped an access (offsets or page ids out of range)";
+      return "FA_ERR_BOUNDS: a device-side bounds check skipped an access "
+             "(offsets or page ids out of range)";
     default: return "unknown status";
   }
 }

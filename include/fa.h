@@ -307,6 +307,11 @@ int fa_num_sms(void);
  * (b, hq, qblock); a qblock is 256 query rows.  Returns the number of items
  * n_items = B * Hq * ceil(Sq / 256), and fills *b, *hq, *qblock when
  * 0 <= w < n_items (the pointers may be NULL).  Returns -1 on bad arguments.
+ *
+ * Items are numbered kv-head-major, longest causal query blocks first.  In a
+ * dense launch the persistent CTAs claim items in that order from a work
+ * counter (the next free CTA takes the next item); packed sequences
+ * (fa_prefill_varlen_fwd) take them by a fixed grid stride.
  */
 int fa_prefill_work_item(int w, int B, int Hq, int Hkv, int Sq, int Sk, int causal,
                          int* b, int* hq, int* qblock);
