@@ -805,9 +805,10 @@ static int launch_prefill_t(const void* q, const void* k, const void* v, void* o
 // is unique for the life of the process (so two streams never share a slot,
 // and launches that share one are ordered by their stream).  Slots come from
 // zero-filled chunks of device memory that live as long as the process.
-// Returns null when no slot can be made: the stream is being captured and
-// has none yet, or the device is out of memory; the caller then uses
-// stream-ordered scratch instead.
+// Returns null -- the caller then uses stream-ordered scratch zeroed by a
+// memset -- while the stream is being captured (each captured graph then owns
+// its counter, so two graphs recorded on one stream may replay concurrently)
+// or when the device is out of memory.
 static unsigned int* work_counter_for_stream(cudaStream_t stream) {
   constexpr int kChunkSlots = 4096;
   struct Pool {
@@ -820,15 +821,15 @@ static unsigned int* work_counter_for_stream(cudaStream_t stream) {
   int dev = 0;
   unsigned long long id = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone)
+    return nullptr;
   if (cudaStreamGetId(stream, &id) != cudaSuccess) return nullptr;
   std::lock_guard<std::mutex> lock(mu);
   Pool& pl = pools[dev];
   auto it = pl.slot.find(id);
   if (it != pl.slot.end()) return it->second;
   if (pl.used == kChunkSlots) {
-    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone)
-      return nullptr;
     void* c = nullptr;
     if (cudaMalloc(&c, kChunkSlots * 2 * sizeof(unsigned int)) != cudaSuccess) return nullptr;
     if (cudaMemset(c, 0, kChunkSlots * 2 * sizeof(unsigned int)) != cudaSuccess) {
@@ -862,8 +863,8 @@ static int launch_prefill_shape(const void* q, const void* k, const void* v, voi
     return cudaGetLastError();
   }
   // The kernel's work counter: the stream's own slot (zero between launches),
-  // or, while the stream is being captured and has no slot yet, stream-ordered
-  // scratch zeroed here.
+  // or, while the stream is being captured, stream-ordered scratch zeroed here
+  // (an allocation and a memset node of the graph).
   void* ctr = packed ? nullptr : work_counter_for_stream(stream);
   const bool own = !packed && ctr == nullptr;
   cudaError_t e = cudaSuccess;
