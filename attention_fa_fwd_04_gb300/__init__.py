@@ -19,6 +19,8 @@ Tensor conveniences (contiguous CUDA tensors, caller-owned outputs):
                  lse=None)
     backward(q, k, v, o, dout, lse, scale, causal, stream=None) -> (dq, dk, dv)
     (lse=True allocates the fp32 log-sum-exp output; a tensor is used as is.)
+Host-to-host prefill (submodule ``host_pipeline``): HostPrefill overlaps the
+uploads of Q, K, V and the download of O with per-piece fa_prefill_fwd calls.
 """
 import ctypes
 import os
