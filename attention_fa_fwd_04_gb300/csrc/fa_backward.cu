@@ -37,14 +37,14 @@ constexpr int QS = 64;                 // query rows of a dkdv sub-tile
 constexpr int SUB_HALF = QS * 128;     // 64 rows x 64 elements x 2 bytes
 constexpr int THREADS = 192;           // warps 0-3 elementwise, 4 producer, 5 MMA
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t COL_S = 0, COL_DP = 128, COL_ACC = 256;
+constexpr int KRING = 3, VRING = 2;    // dq kernel: K and V tile rings
 constexpr float LOG2E = 1.4426950408889634f;
 
 template <int D>
 struct Cfg {
   static constexpr int HALVES = D / 64;
   static constexpr int TILE_BYTES = HALVES * HALF_BYTES;  // one 128-row tile
-  static constexpr int NSTAGE_DQ = 4;    // K/V ring of the dq kernel (K_j, V_j alternate)
+  static constexpr int NSTAGE_DQ = 5;    // dq: K ring (KRING slots) + V ring (VRING slots)
   static constexpr int NSTAGE_DKV = 4;   // (Q, dO) sub-tile ring of the dkdv kernel
   static constexpr int SMEM_BAR = 512;
   static constexpr int SMEM_DQ = 1024 + 2 * TILE_BYTES + NSTAGE_DQ * TILE_BYTES + SMEM_BAR;
@@ -183,6 +183,18 @@ __device__ __forceinline__ int bw_first_query_tile(int k0, const BwdParams& p) {
 
 // ------------------------------------------------------------------------------
 // dq
+//
+// TMEM: S(0) | S(1) | dP | dQ (128 + 128 + 128 + D columns).  S is
+// double-buffered and dP is handed back early, so the element-wise pass of key
+// tile j overlaps the MMAs around it:
+//   S(j+1) is issued a whole step ahead, into the other S buffer;
+//   the element-wise warps read all of dP(j) into registers first and say so
+//   (ld_done), which lets dP(j+1) be issued while they compute dS(j);
+//   dQ += dS(j) K_j follows once dS(j) is in TMEM, then S(j+2) into the buffer
+//   dQ(j) has just read.
+// K and V tiles sit in two rings: K (3 slots; K_j is read by S(j) and dQ(j)
+// and released after dQ(j)) and V (2 slots; V_j is released after dP(j)).
+// Each ring frees a slot about a step before its next tile is due.
 // ------------------------------------------------------------------------------
 template <int D, typename T>
 __global__ void __launch_bounds__(bw::THREADS, 1)
@@ -197,17 +209,19 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sQ = smem;
   uint8_t* sDO = smem + C::TILE_BYTES;
-  uint8_t* sKV = smem + 2 * C::TILE_BYTES;
+  uint8_t* sKV = smem + 2 * C::TILE_BYTES;  // K ring slots 0-2, then V ring slots 0-1
   uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + NS * C::TILE_BYTES);
-  uint64_t* full = bars;            // [NS]
+  uint64_t* full = bars;            // [NS] (K ring: 0-2, V ring: 3-4)
   uint64_t* empty = bars + NS;      // [NS]
   uint64_t* q_full = bars + 2 * NS;
   uint64_t* q_empty = q_full + 1;
-  uint64_t* s_full = q_full + 2;    // S and dP in TMEM
-  uint64_t* ds_full = q_full + 3;   // dS in TMEM (128 arrivals)
-  uint64_t* o_full = q_full + 4;    // dQ complete
-  uint64_t* drain = q_full + 5;
-  uint64_t* sched_full = q_full + 6;                 // [kSchedSlots]
+  uint64_t* s_full = q_full + 2;    // [2] S of buffer b in TMEM
+  uint64_t* dp_full = q_full + 4;   // dP in TMEM
+  uint64_t* ld_done = q_full + 5;   // dP read into registers (128 arrivals)
+  uint64_t* ds_full = q_full + 6;   // dS in TMEM (128 arrivals)
+  uint64_t* o_full = q_full + 7;    // dQ complete
+  uint64_t* drain = q_full + 8;
+  uint64_t* sched_full = q_full + 9;                 // [kSchedSlots]
   uint64_t* sched_empty = sched_full + kSchedSlots;  // [kSchedSlots]
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sched_empty + kSchedSlots);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
@@ -221,7 +235,10 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
     }
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
-    mbar_init(s_full, 1);
+    mbar_init(&s_full[0], 1);
+    mbar_init(&s_full[1], 1);
+    mbar_init(dp_full, 1);
+    mbar_init(ld_done, bw::BT);
     mbar_init(ds_full, bw::BT);
     mbar_init(o_full, 1);
     mbar_init(drain, 1);
@@ -253,7 +270,7 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
     }
     const uint64_t pol_q = l2_policy_evict_first();
     const uint64_t pol_kv = l2_policy_evict_last();
-    uint32_t kv_cnt = 0, local = 0;
+    uint32_t k_iss = 0, v_iss = 0, local = 0;  // K / V tiles issued so far
     bool ok = true, q_issued = false;
     for (uint32_t k = 0; ok; ++k, ++local) {
       const int w = sched_produce(k, p.work_ctr, p.n_items, sched_full, sched_empty, sched,
@@ -283,9 +300,11 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
       for (int j = 0; j < n && ok; ++j) {
 #pragma unroll
         for (int sel = 0; sel < 2; ++sel) {  // K_j, then V_j
-          const int s = kv_cnt % NS;
-          const uint32_t ph = (kv_cnt / NS) & 1;
-          if (!(ok = mbar_wait(&empty[s], ph ^ 1, abort_flag, &g_backward_err, 2))) break;
+          const uint32_t t = sel ? v_iss : k_iss;  // the tile's count in its ring
+          const uint32_t nr = sel ? bw::VRING : bw::KRING;
+          const int s = (sel ? bw::KRING : 0) + (int)(t % nr);
+          if (!(ok = mbar_wait(&empty[s], ((t / nr) & 1) ^ 1, abort_flag, &g_backward_err, 2)))
+            break;
           if (leader) {
             mbar_arrive_expect_tx(&full[s], C::TILE_BYTES);
             const CUtensorMap* m = sel ? &tmV : &tmK;
@@ -295,13 +314,17 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
                                hkv, j * bw::BT, b, pol_kv);
           }
           __syncwarp();
-          ++kv_cnt;
+          if (sel) ++v_iss; else ++k_iss;
         }
       }
     }
     if (!ok) {
-      const uint32_t first = kv_cnt > (uint32_t)NS ? kv_cnt - NS : 0u;
-      for (uint32_t u = first; u < kv_cnt; ++u) mbar_wait_drain(&full[u % NS], (u / NS) & 1);
+      // Wait (bounded) for the loads possibly still in flight: the last KRING
+      // K tiles and VRING V tiles issued.
+      for (uint32_t u = k_iss > (uint32_t)bw::KRING ? k_iss - bw::KRING : 0u; u < k_iss; ++u)
+        mbar_wait_drain(&full[u % bw::KRING], (u / bw::KRING) & 1);
+      for (uint32_t u = v_iss > (uint32_t)bw::VRING ? v_iss - bw::VRING : 0u; u < v_iss; ++u)
+        mbar_wait_drain(&full[bw::KRING + u % bw::VRING], (u / bw::VRING) & 1);
       if (q_issued) mbar_wait_drain(q_full, local & 1);
     }
     __syncwarp();
@@ -310,8 +333,9 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
     constexpr uint32_t IDESC_S = idesc_f16(bw::BT, bw::BT, kBF16, false);
     constexpr uint32_t IDESC_ACC = idesc_f16(bw::BT, D, kBF16, true);
     const uint32_t sq_addr = smem_u32(sQ), sdo_addr = smem_u32(sDO), skv_addr = smem_u32(sKV);
-    uint32_t kv_cnt = 0, local = 0, ds_cnt = 0;
+    uint32_t kv_cnt = 0, local = 0, g = 0;  // g: key-tile steps so far (buffers, parities)
     bool ok = true;
+    constexpr uint32_t COL_DP = 256, COL_DQ = 384;
     // D_tmem = A (K-major smem) x B^T (K-major smem) over D/16 k-steps.
     auto issue_nt = [&](uint32_t d_col, uint32_t a_addr, uint32_t b_addr) {
       if (leader) {
@@ -328,12 +352,22 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
       if (leader) mma_commit(bar);
       __syncwarp();
     };
-    auto ring_wait = [&](uint32_t idx, unsigned int site) {
-      const bool r =
-          mbar_wait(&full[idx % NS], (idx / NS) & 1, abort_flag, &g_backward_err, site);
+    // Tile t (a global count of key tiles) of the K ring or the V ring.
+    auto kslot = [&](uint32_t t) { return (int)(t % bw::KRING); };
+    auto vslot = [&](uint32_t t) { return bw::KRING + (int)(t % bw::VRING); };
+    auto wait_k = [&](uint32_t t, unsigned int site) {
+      const bool r = mbar_wait(&full[kslot(t)], (t / bw::KRING) & 1, abort_flag,
+                               &g_backward_err, site);
       tc_fence_after();
       return r;
     };
+    auto wait_v = [&](uint32_t t, unsigned int site) {
+      const bool r = mbar_wait(&full[vslot(t)], (t / bw::VRING) & 1, abort_flag,
+                               &g_backward_err, site);
+      tc_fence_after();
+      return r;
+    };
+    auto addr = [&](int s) { return skv_addr + s * C::TILE_BYTES; };
     for (uint32_t it = 0; ok; ++it, ++local) {
       const int w =
           sched_consume(it, sched_full, sched_empty, sched, abort_flag, &g_backward_err, 11);
@@ -351,33 +385,57 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
         commit(o_full);  // dQ = 0 for this tile (accumulator not written)
         continue;
       }
-      const uint32_t kb = kv_cnt;
-      kv_cnt += 2 * n;
+      const uint32_t kb = kv_cnt;  // K_j and V_j are tile kb + j of their rings
+      kv_cnt += n;
+      // Prologue: S(0), dP(0), S(1).
+      if (!(ok = wait_k(kb, 4))) break;
+      issue_nt((g & 1) * 128, sq_addr, addr(kslot(kb)));
+      commit(&s_full[g & 1]);
+      if (!(ok = wait_v(kb, 5))) break;
+      issue_nt(COL_DP, sdo_addr, addr(vslot(kb)));
+      commit(dp_full);
+      commit(&empty[vslot(kb)]);
+      if (n == 1) commit(q_empty);
+      if (n > 1) {
+        if (!(ok = wait_k(kb + 1, 4))) break;
+        issue_nt(((g + 1) & 1) * 128, sq_addr, addr(kslot(kb + 1)));
+        commit(&s_full[(g + 1) & 1]);
+      }
       for (int j = 0; j < n && ok; ++j) {
-        const uint32_t iK = kb + 2 * j, iV = iK + 1;
-        if (!(ok = ring_wait(iK, 4))) break;
-        issue_nt(bw::COL_S, sq_addr, skv_addr + (iK % NS) * C::TILE_BYTES);   // S = Q K_j^T
-        if (!(ok = ring_wait(iV, 5))) break;
-        issue_nt(bw::COL_DP, sdo_addr, skv_addr + (iV % NS) * C::TILE_BYTES); // dP = dO V_j^T
-        commit(s_full);
-        commit(&empty[iV % NS]);
-        if (j == n - 1) commit(q_empty);
-        if (!(ok = mbar_wait(ds_full, ds_cnt & 1, abort_flag, &g_backward_err, 6))) break;
-        ++ds_cnt;
+        const uint32_t gj = g + j;
+        // dP(j) is in the element-wise warps' registers: dP(j+1) may go.
+        if (!(ok = mbar_wait(ld_done, gj & 1, abort_flag, &g_backward_err, 6))) break;
         tc_fence_after();
-        // dQ += dS K_j: dS (16-bit, TMEM columns [0, 64)), K_j MN-major.
+        if (j + 1 < n) {
+          if (!(ok = wait_v(kb + j + 1, 5))) break;
+          issue_nt(COL_DP, sdo_addr, addr(vslot(kb + j + 1)));
+          commit(dp_full);
+          commit(&empty[vslot(kb + j + 1)]);
+          if (j + 1 == n - 1) commit(q_empty);  // the last S and dP are issued
+        }
+        // dQ += dS(j) K_j: dS (16-bit) in the first 64 columns of S buffer j.
+        if (!(ok = mbar_wait(ds_full, gj & 1, abort_flag, &g_backward_err, 6))) break;
+        tc_fence_after();
+        const uint32_t kaddr = addr(kslot(kb + j));
         if (leader) {
 #pragma unroll
           for (int k = 0; k < bw::BT / 16; ++k) {
-            const uint64_t bd = sdesc_sw128(skv_addr + (iK % NS) * C::TILE_BYTES + k * 16 * 128,
-                                            bw::HALF_BYTES, 1024);
-            mma_ts(tmem + bw::COL_ACC, tmem + bw::COL_S + k * 8, bd, IDESC_ACC,
+            const uint64_t bd = sdesc_sw128(kaddr + k * 16 * 128, bw::HALF_BYTES, 1024);
+            mma_ts(tmem + COL_DQ, tmem + (gj & 1) * 128 + k * 8, bd, IDESC_ACC,
                    (j > 0 || k > 0) ? 1u : 0u);
           }
         }
         __syncwarp();
-        commit(&empty[iK % NS]);
+        commit(&empty[kslot(kb + j)]);
+        // S(j+2) into the buffer dQ(j) has just read.
+        if (j + 2 < n) {
+          if (!(ok = wait_k(kb + j + 2, 4))) break;
+          issue_nt((gj & 1) * 128, sq_addr, addr(kslot(kb + j + 2)));
+          commit(&s_full[gj & 1]);
+        }
       }
+      if (!ok) break;
+      g += n;
       commit(o_full);
     }
     commit(drain);
@@ -387,9 +445,10 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
     // ============================ dS (warps 0-3) ============================
     const int r = warp * 32 + lane;  // TMEM lane = query row within the tile
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    uint32_t s_cnt = 0, o_cnt = 0;
+    uint32_t g = 0, o_cnt = 0;  // g: key-tile steps so far (buffers, parities)
     bool ok = true;
     T* const DQ = static_cast<T*>(p.dq);
+    constexpr uint32_t COL_DP = 256, COL_DQ = 384;
     for (uint32_t it = 0; ok; ++it) {
       const int w =
           sched_consume(it, sched_full, sched_empty, sched, abort_flag, &g_backward_err, 12);
@@ -408,31 +467,38 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
       const bool any_key = row_ok && p.lse[lrow] != NEG_INF;
       const int lim_c = p.causal ? i + off + 1 : p.Sk;  // keys [0, lim) visible
       const int lim = any_key ? (lim_c < p.Sk ? lim_c : p.Sk) : 0;
-      for (int j = 0; j < n && ok; ++j) {
-        if (!(ok = mbar_wait(s_full, s_cnt & 1, abort_flag, &g_backward_err, 7))) break;
-        ++s_cnt;
+      for (int j = 0; j < n && ok; ++j, ++g) {
+        const uint32_t cs = (g & 1) * 128;  // this step's S buffer
+        if (!(ok = mbar_wait(&s_full[g & 1], (g >> 1) & 1, abort_flag, &g_backward_err, 7)))
+          break;
+        if (!(ok = mbar_wait(dp_full, g & 1, abort_flag, &g_backward_err, 7))) break;
         __syncwarp();
         tc_fence_after();
+        // All of dP(j) into registers first, then hand the dP columns back so
+        // that dP(j+1) can be computed while dS(j) is.
+        uint32_t pr[4][32];
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) tmem_ld32(t_lane + COL_DP + q4 * 32, pr[q4]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) reg_fence32(pr[q4]);
+        tc_fence_before();
+        mbar_arrive(ld_done);
         // Keys [0, lim) of this row are visible: columns from lim_t on are
         // hidden (selected to 0), which only the tile holding key lim has.
         const int lim_t = lim - j * bw::BT;
         const bool edge = __any_sync(0xffffffffu, lim_t < bw::BT);
         const float2 c2 = make_float2(p.c, p.c), nl2 = make_float2(-l2, -l2);
         const float2 nd2 = make_float2(-dl, -dl);
-        // Software-pipelined TMEM reads, as in the dK/dV kernel.
-        uint32_t sr[2][32], pr[2][32];
-        tmem_ld32(t_lane + bw::COL_S, sr[0]);
-        tmem_ld32(t_lane + bw::COL_DP, pr[0]);
+        // S in 32-column chunks, one chunk ahead.
+        uint32_t sr[2][32];
+        tmem_ld32(t_lane + cs, sr[0]);
         tmem_wait_ld();
         reg_fence32(sr[0]);
-        reg_fence32(pr[0]);
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
           const int cur = q4 & 1;
-          if (q4 < 3) {
-            tmem_ld32(t_lane + bw::COL_S + (q4 + 1) * 32, sr[cur ^ 1]);
-            tmem_ld32(t_lane + bw::COL_DP + (q4 + 1) * 32, pr[cur ^ 1]);
-          }
+          if (q4 < 3) tmem_ld32(t_lane + cs + (q4 + 1) * 32, sr[cur ^ 1]);
           uint32_t pk[16];
 #pragma unroll
           for (int x = 0; x < 16; ++x) {
@@ -445,17 +511,17 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
               pv.x = col < lim_t ? pv.x : 0.f;
               pv.y = col + 1 < lim_t ? pv.y : 0.f;
             }
-            const float2 dd = __fadd2_rn(make_float2(__uint_as_float(pr[cur][2 * x]),
-                                                     __uint_as_float(pr[cur][2 * x + 1])),
+            const float2 dd = __fadd2_rn(make_float2(__uint_as_float(pr[q4][2 * x]),
+                                                     __uint_as_float(pr[q4][2 * x + 1])),
                                          nd2);
             const float2 ds = __fmul2_rn(pv, dd);
             pk[x] = BPack<T>::pack(ds.x, ds.y);
           }
-          tmem_st16(t_lane + bw::COL_S + q4 * 16, pk);
+          // 16-bit dS of these 32 keys over the S columns already read.
+          tmem_st16(t_lane + cs + q4 * 16, pk);
           if (q4 < 3) {
             tmem_wait_ld();
             reg_fence32(sr[cur ^ 1]);
-            reg_fence32(pr[cur ^ 1]);
           }
         }
         tmem_wait_st();
@@ -473,7 +539,7 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
       for (int q4 = 0; q4 < D / 32; ++q4) {
         uint32_t ar[32];
         if (n > 0) {
-          tmem_ld32(t_lane + bw::COL_ACC + q4 * 32, ar);
+          tmem_ld32(t_lane + COL_DQ + q4 * 32, ar);
           tmem_wait_ld();
           reg_fence32(ar);
         } else {
