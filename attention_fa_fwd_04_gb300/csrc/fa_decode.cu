@@ -16,11 +16,13 @@
 //            the SM count (not from L, which the host never reads);
 //   CTA    = 1 producer warp issuing TMA tile loads (32 tokens x D, K and V,
 //            128-byte swizzle) into an 8-stage mbarrier ring (16 for D = 64,
-//            128 KiB in flight), and 4 consumer
-//            warps that each own whole tiles: S = Q K^T and O += P V with
-//            mma.sync m16n8k16 (the group's query heads padded to M = 16), an
-//            exp2 online softmax per warp, then a cross-warp merge in shared
-//            memory into one (max, sum, o[D]) partial per head and split;
+//            128 KiB in flight), and 4 consumer warps that each own whole
+//            tiles: S^T = K Q^T and O^T += V^T P^T with mma.sync m16n8k16,
+//            tokens as the MMA's M and the group's query heads as its N (8 per
+//            block, so a GQA group of 4 wastes half of N instead of 3/4 of a
+//            16-row M), an exp2 online softmax per warp, then a cross-warp
+//            merge in shared memory into one (max, sum, o[D]) partial per head
+//            and split;
 //   combine= one CTA per (32 columns, head, b) merges the split partials with
 //            weights exp2(m_s - M).
 // Both kernels are launched as programmatic dependents of the grid before
@@ -42,7 +44,7 @@ namespace dec {
 constexpr int TT = 32;        // tokens per tile
 constexpr int NWARPS = 4;     // consumer warps
 constexpr int THREADS = (NWARPS + 1) * 32;
-constexpr int HB = 16;        // query heads per CTA: the MMA's M
+constexpr int HB = 16;        // row stride of the merge buffers (query rows per CTA at most)
 constexpr int HALF_BYTES = TT * 128;  // TT rows x 64 elements x 2 bytes
 // Bytes of K/V per CTA warmed in L2 before the grid wait: with one CTA per SM
 // that is at most about half of L2 in flight, whatever the cache length.
@@ -104,12 +106,16 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 
 // PAGED: K/V tiles are addressed through the page table (instantiated
 // separately so the contiguous path carries none of the paging code).
-template <int D, bool PAGED>
+// NB: query rows per CTA in blocks of 8 (the MMA's N): 1 when a kv head has at
+// most 8 rows (GQA groups up to 8 with one new token), else 2.
+template <int D, bool PAGED, int NB>
 __global__ void __launch_bounds__(dec::THREADS, 1)
     decode_split_kernel(const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const DecodeParams p) {
   using C = dec::Cfg<D>;
   constexpr int TT = dec::TT, NSTAGE = C::NSTAGE, HB = dec::HB, NW = dec::NWARPS;
+  constexpr int RB = 8 * NB;  // query rows of this CTA (HB is the buffers' row stride)
+  static_assert(RB <= HB, "row blocks must fit the merge buffers");
   constexpr float NEG_INF = -INFINITY;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -184,10 +190,6 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
   __syncthreads();
 
   const int g = lane >> 2, tq = lane & 3;
-  float m0 = NEG_INF, m1 = NEG_INF, l0 = 0.f, l1 = 0.f;
-  float acc[D / 8][4];
-#pragma unroll
-  for (int nd = 0; nd < D / 8; ++nd) acc[nd][0] = acc[nd][1] = acc[nd][2] = acc[nd][3] = 0.f;
 
   if (warp == NW) {
     // ---------------- producer warp: lanes stay converged, lane 0 issues ----------------
@@ -240,23 +242,44 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
     __syncwarp();
   } else {
     // ---------------- consumers: whole tiles, round-robin over warps ----------------
-    // Q as the MMA's A operand (rows = the CTA's query heads, padded to 16).
-    const int hi0 = hb * HB + g, hi1 = hi0 + 8;
-    const bool ok0 = hi0 < Sq * p.G, ok1 = hi1 < Sq * p.G;
-    const uint32_t* q0 = reinterpret_cast<const uint32_t*>(
-        p.q + decode_qrow(p, b, hkv, ok0 ? hi0 : 0, Sq) * D);
-    const uint32_t* q1 = reinterpret_cast<const uint32_t*>(
-        p.q + decode_qrow(p, b, hkv, ok1 ? hi1 : 0, Sq) * D);
-    // Keys each of the thread's two rows may see (causal among new tokens).
-    const int vis0 = L - Sq + 1 + (ok0 ? hi0 / p.G : 0);
-    const int vis1 = L - Sq + 1 + (ok1 ? hi1 / p.G : 0);
-    uint32_t qa[D / 16][4];
+    // Transposed products, so that the tile's tokens fill the MMA's M and the
+    // CTA's few query rows only its N (8 per block):
+    //   S^T = K Q^T   (A = K rows from shared memory, B = Q from registers),
+    //   O^T += V^T P^T (A = V through transposing ldmatrix, B = P^T, which is
+    //                   the S^T accumulator transposed per 8x8 by movmatrix).
+    // Lane (g, tq) holds, for row block nb, rows nb*8 + 2tq + {0,1} of tokens
+    // g and g + 8 of each 16-token block, and O^T at d = 16 dm + g (+8).
+    const int rows_all = Sq * p.G;
+    uint32_t qb[NB][D / 16][2];
+    int vis[NB][2];  // keys [0, vis) visible to the lane's rows (paged: causal new tokens)
 #pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-      qa[kk][0] = ok0 ? q0[kk * 8 + tq] : 0u;
-      qa[kk][1] = ok1 ? q1[kk * 8 + tq] : 0u;
-      qa[kk][2] = ok0 ? q0[kk * 8 + 4 + tq] : 0u;
-      qa[kk][3] = ok1 ? q1[kk * 8 + 4 + tq] : 0u;
+    for (int nb = 0; nb < NB; ++nb) {
+      const int r = hb * RB + nb * 8 + g;
+      const bool ok = r < rows_all;
+      const uint32_t* qr = reinterpret_cast<const uint32_t*>(
+          p.q + decode_qrow(p, b, hkv, ok ? r : 0, Sq) * D);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        qb[nb][kk][0] = ok ? qr[kk * 8 + tq] : 0u;
+        qb[nb][kk][1] = ok ? qr[kk * 8 + 4 + tq] : 0u;
+      }
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int rc = hb * RB + nb * 8 + 2 * tq + e;
+        vis[nb][e] = L - Sq + 1 + (rc < rows_all ? rc / p.G : 0);
+      }
+    }
+    float mr[NB][2], lr[NB][2];
+    float acc[NB][D / 16][4];
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        mr[nb][e] = NEG_INF;
+        lr[nb][e] = 0.f;
+      }
+#pragma unroll
+      for (int dm = 0; dm < D / 16; ++dm) acc[nb][dm][0] = acc[nb][dm][1] = acc[nb][dm][2] = acc[nb][dm][3] = 0.f;
     }
 
     for (int t = warp; t < n_tiles; t += NW) {
@@ -285,126 +308,131 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
         __syncwarp();
       }
 
-      // S = Q K^T: 16 heads x TT tokens, TT/8 n-blocks of 8 tokens.
-      constexpr int NB = TT / 8;
-      float sc[NB][4];
-#pragma unroll
-      for (int nb = 0; nb < NB; ++nb) sc[nb][0] = sc[nb][1] = sc[nb][2] = sc[nb][3] = 0.f;
-      const uint32_t kbase = smem_u32(st);
-      const int mi = lane >> 3;
-#pragma unroll
-      for (int np = 0; np < NB / 2; ++np) {
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const int tok = np * 16 + (mi >> 1) * 8 + (lane & 7);
-          const int chunk = kk * 2 + (mi & 1);
-          const uint32_t addr = kbase + (chunk >> 3) * dec::HALF_BYTES + tok * 128 +
-                                ((((chunk & 7) ^ (tok & 7))) << 4);
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(addr, b0, b1, b2, b3);
-          mma_bf16_16816(sc[2 * np], qa[kk], b0, b1);
-          mma_bf16_16816(sc[2 * np + 1], qa[kk], b2, b3);
-        }
-      }
-      // Scale into the log2 domain, then mask tokens >= L (and, with several
-      // new tokens, the keys after each row's own position).
+      // S^T: TT/16 token blocks x NB row blocks, 16 d per MMA.
+      constexpr int MB = TT / 16;
+      float sc[NB][MB][4];
 #pragma unroll
       for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          sc[nb][e] *= p.c;
-          if constexpr (PAGED) {
-            if (tok0 + nb * 8 + 2 * tq + (e & 1) >= ((e < 2) ? vis0 : vis1) ||
-                nb * 8 + 2 * tq + (e & 1) >= nvalid)
-              sc[nb][e] = NEG_INF;
-          } else {
-            if (nvalid < TT && nb * 8 + 2 * tq + (e & 1) >= nvalid) sc[nb][e] = NEG_INF;
-          }
+        for (int mb = 0; mb < MB; ++mb) sc[nb][mb][0] = sc[nb][mb][1] = sc[nb][mb][2] = sc[nb][mb][3] = 0.f;
+      const uint32_t kbase = smem_u32(st);
+      const int mi = lane >> 3;
+#pragma unroll
+      for (int mb = 0; mb < MB; ++mb) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const int tok = mb * 16 + (mi & 1) * 8 + (lane & 7);
+          const int chunk = kk * 2 + (mi >> 1);
+          const uint32_t addr = kbase + (chunk >> 3) * dec::HALF_BYTES + tok * 128 +
+                                ((((chunk & 7) ^ (tok & 7))) << 4);
+          uint32_t a[4];
+          ldsm_x4(addr, a[0], a[1], a[2], a[3]);
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb) mma_bf16_16816(sc[nb][mb], a, qb[nb][kk][0], qb[nb][kk][1]);
         }
-      // Online softmax over this warp's tiles.
-      float mx0 = NEG_INF, mx1 = NEG_INF;
+      }
+      // Scale into the log2 domain; mask tokens >= L (and, with several new
+      // tokens, the keys after each row's own position).
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+        for (int mb = 0; mb < MB; ++mb)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int tl = mb * 16 + g + (i >> 1) * 8;  // token within the tile
+            sc[nb][mb][i] *= p.c;
+            if constexpr (PAGED) {
+              if (tok0 + tl >= vis[nb][i & 1] || tl >= nvalid) sc[nb][mb][i] = NEG_INF;
+            } else {
+              if (nvalid < TT && tl >= nvalid) sc[nb][mb][i] = NEG_INF;
+            }
+          }
+      // Online softmax per row (column of S^T): the max over the tile's
+      // tokens is over the lane's 2 x MB values and the 8 lanes of its tq.
+      uint32_t pb[NB][MB][2];
 #pragma unroll
       for (int nb = 0; nb < NB; ++nb) {
-        mx0 = fmaxf(mx0, fmaxf(sc[nb][0], sc[nb][1]));
-        mx1 = fmaxf(mx1, fmaxf(sc[nb][2], sc[nb][3]));
-      }
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-      const float base0 = mn0 == NEG_INF ? 0.f : mn0;
-      const float base1 = mn1 == NEG_INF ? 0.f : mn1;
-      const float f0 = fast_exp2(m0 - base0), f1 = fast_exp2(m1 - base1);
-      m0 = mn0;
-      m1 = mn1;
-      float rs0 = 0.f, rs1 = 0.f;
+        float f[2], base[2];
 #pragma unroll
-      for (int nb = 0; nb < NB; ++nb) {
-        sc[nb][0] = fast_exp2(sc[nb][0] - base0);
-        sc[nb][1] = fast_exp2(sc[nb][1] - base0);
-        sc[nb][2] = fast_exp2(sc[nb][2] - base1);
-        sc[nb][3] = fast_exp2(sc[nb][3] - base1);
-        rs0 += sc[nb][0] + sc[nb][1];
-        rs1 += sc[nb][2] + sc[nb][3];
-      }
-      l0 = l0 * f0 + rs0;
-      l1 = l1 * f1 + rs1;
+        for (int e = 0; e < 2; ++e) {
+          float mx = NEG_INF;
 #pragma unroll
-      for (int nd = 0; nd < D / 8; ++nd) {
-        acc[nd][0] *= f0;
-        acc[nd][1] *= f0;
-        acc[nd][2] *= f1;
-        acc[nd][3] *= f1;
+          for (int mb = 0; mb < MB; ++mb) mx = fmaxf(mx, fmaxf(sc[nb][mb][e], sc[nb][mb][2 + e]));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+          const float mn = fmaxf(mr[nb][e], mx);
+          base[e] = mn == NEG_INF ? 0.f : mn;
+          f[e] = fast_exp2(mr[nb][e] - base[e]);
+          mr[nb][e] = mn;
+        }
+        float rs[2] = {0.f, 0.f};
+#pragma unroll
+        for (int mb = 0; mb < MB; ++mb) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            sc[nb][mb][i] = fast_exp2(sc[nb][mb][i] - base[i & 1]);
+            rs[i & 1] += sc[nb][mb][i];
+          }
+          // P^T B operand: rows tq-pairs of tokens g / g + 8, transposed per 8x8.
+          pb[nb][mb][0] = movmatrix_trans(pack_bf16(sc[nb][mb][0], sc[nb][mb][1]));
+          pb[nb][mb][1] = movmatrix_trans(pack_bf16(sc[nb][mb][2], sc[nb][mb][3]));
+        }
+#pragma unroll
+        for (int e = 0; e < 2; ++e) lr[nb][e] = lr[nb][e] * f[e] + rs[e];
+#pragma unroll
+        for (int dm = 0; dm < D / 16; ++dm) {
+          acc[nb][dm][0] *= f[0];
+          acc[nb][dm][1] *= f[1];
+          acc[nb][dm][2] *= f[0];
+          acc[nb][dm][3] *= f[1];
+        }
       }
-      // O += P V: P from the S accumulators (C layout == A layout), V via
-      // transposing ldmatrix.
+      // O^T += V^T P^T: A = V^T (16 d x 16 tokens) by transposing ldmatrix.
       const uint32_t vbase = kbase + C::KV_BYTES;
 #pragma unroll
-      for (int k2 = 0; k2 < TT / 16; ++k2) {
-        uint32_t a[4];
-        a[0] = pack_bf16(sc[2 * k2][0], sc[2 * k2][1]);
-        a[1] = pack_bf16(sc[2 * k2][2], sc[2 * k2][3]);
-        a[2] = pack_bf16(sc[2 * k2 + 1][0], sc[2 * k2 + 1][1]);
-        a[3] = pack_bf16(sc[2 * k2 + 1][2], sc[2 * k2 + 1][3]);
+      for (int mb = 0; mb < MB; ++mb) {
 #pragma unroll
-        for (int dn = 0; dn < D / 16; ++dn) {
-          const int tok = k2 * 16 + (mi & 1) * 8 + (lane & 7);
-          const int chunk = dn * 2 + (mi >> 1);
+        for (int dm = 0; dm < D / 16; ++dm) {
+          const int tok = mb * 16 + (mi >> 1) * 8 + (lane & 7);
+          const int chunk = dm * 2 + (mi & 1);
           const uint32_t addr = vbase + (chunk >> 3) * dec::HALF_BYTES + tok * 128 +
                                 ((((chunk & 7) ^ (tok & 7))) << 4);
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(addr, b0, b1, b2, b3);
-          mma_bf16_16816(acc[2 * dn], a, b0, b1);
-          mma_bf16_16816(acc[2 * dn + 1], a, b2, b3);
+          uint32_t a[4];
+          ldsm_x4_t(addr, a[0], a[1], a[2], a[3]);
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb) mma_bf16_16816(acc[nb][dm], a, pb[nb][mb][0], pb[nb][mb][1]);
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
     }
-    // Per-warp row sums (each quad holds one row's partial sums).
+    // Per-warp row sums over the 8 lanes that share tq, then this warp's
+    // (max, sum) and unnormalised O rows (only the CTA's real rows are kept).
     __syncwarp();
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-    if (tq == 0) {
-      red_ml[(warp * HB + g) * 2 + 0] = m0;
-      red_ml[(warp * HB + g) * 2 + 1] = l0;
-      red_ml[(warp * HB + g + 8) * 2 + 0] = m1;
-      red_ml[(warp * HB + g + 8) * 2 + 1] = l1;
-    }
-    // This warp's unnormalised O rows (only the CTA's real heads are kept).
+    const int nh_rows = (rows_all - hb * RB) < RB ? (rows_all - hb * RB) : RB;
     float* my_o = red_o + warp * HB * D;
-    const int nh_rows = (Sq * p.G - hb * HB) < HB ? (Sq * p.G - hb * HB) : HB;
 #pragma unroll
-    for (int nd = 0; nd < D / 8; ++nd) {
-      if (g < nh_rows)
-        *reinterpret_cast<float2*>(&my_o[g * D + nd * 8 + 2 * tq]) =
-            make_float2(acc[nd][0], acc[nd][1]);
-      if (g + 8 < nh_rows)
-        *reinterpret_cast<float2*>(&my_o[(g + 8) * D + nd * 8 + 2 * tq]) =
-            make_float2(acc[nd][2], acc[nd][3]);
+    for (int nb = 0; nb < NB; ++nb) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float l = lr[nb][e];
+        l += __shfl_xor_sync(0xffffffffu, l, 4);
+        l += __shfl_xor_sync(0xffffffffu, l, 8);
+        l += __shfl_xor_sync(0xffffffffu, l, 16);
+        const int row = nb * 8 + 2 * tq + e;
+        if (g == 0) {
+          red_ml[(warp * HB + row) * 2 + 0] = mr[nb][e];
+          red_ml[(warp * HB + row) * 2 + 1] = l;
+        }
+        if (row < nh_rows) {
+#pragma unroll
+          for (int dm = 0; dm < D / 16; ++dm) {
+            my_o[row * D + dm * 16 + g] = acc[nb][dm][e];
+            my_o[row * D + dm * 16 + g + 8] = acc[nb][dm][2 + e];
+          }
+        }
+      }
     }
   }
   __syncthreads();
@@ -412,9 +440,9 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
   // Merge the warps' partials (weights exp2(m_w - M)) and write this split's
   // partial for the CTA's heads: the weights once per row, then the outputs
   // four columns per thread.
-  int nh = (Sq * p.G - hb * HB) < HB ? (Sq * p.G - hb * HB) : HB;
+  int nh = (Sq * p.G - hb * RB) < RB ? (Sq * p.G - hb * RB) : RB;
   // Query row of CTA row `row` (partials and outputs are indexed by it).
-  auto qrow = [&](int row) { return decode_qrow(p, b, hkv, hb * HB + row, Sq); };
+  auto qrow = [&](int row) { return decode_qrow(p, b, hkv, hb * RB + row, Sq); };
   // Self-check: partial rows must lie inside the scratch (records and skips).
   if (b >= p.B || split >= p.nsplit ||
       (nh > 0 && qrow(nh - 1) >= (size_t)p.B * Sq * p.Hq)) {
@@ -587,13 +615,15 @@ static int launch_decode_t(const void* q, const void* kc, const void* vc, const 
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::SMEM_TOTAL);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(decode_split_kernel<D, true>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_TOTAL);
-    if (e != cudaSuccess) return e;
+    const void* kernels[4] = {(const void*)decode_split_kernel<D, false, 1>,
+                              (const void*)decode_split_kernel<D, false, 2>,
+                              (const void*)decode_split_kernel<D, true, 1>,
+                              (const void*)decode_split_kernel<D, true, 2>};
+    cudaError_t e = cudaSuccess;
+    for (const void* k : kernels) {
+      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_TOTAL);
+      if (e != cudaSuccess) return e;
+    }
     // Same shared-memory carveout as the split kernel, so that combine CTAs
     // can become resident beside split CTAs and wait there.
     e = cudaFuncSetAttribute(decode_combine_kernel<D>,
@@ -638,8 +668,15 @@ static int launch_decode_t(const void* q, const void* kc, const void* vc, const 
   sc.stream = stream;
   sc.attrs = attr;
   sc.numAttrs = 1;
-  cudaError_t e = paged ? cudaLaunchKernelEx(&sc, decode_split_kernel<D, true>, tk, tv, p)
-                        : cudaLaunchKernelEx(&sc, decode_split_kernel<D, false>, tk, tv, p);
+  // One block of 8 query rows per CTA when the kv head has at most 8 rows.
+  const bool nb1 = Sq * p.G <= 8;
+  cudaError_t e;
+  if (paged)
+    e = nb1 ? cudaLaunchKernelEx(&sc, decode_split_kernel<D, true, 1>, tk, tv, p)
+            : cudaLaunchKernelEx(&sc, decode_split_kernel<D, true, 2>, tk, tv, p);
+  else
+    e = nb1 ? cudaLaunchKernelEx(&sc, decode_split_kernel<D, false, 1>, tk, tv, p)
+            : cudaLaunchKernelEx(&sc, decode_split_kernel<D, false, 2>, tk, tv, p);
   if (e != cudaSuccess) return e;
 
   cudaLaunchConfig_t cfg = {};
