@@ -104,6 +104,14 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Transpose of an 8x8 matrix of 16-bit elements held one 32-bit pair per lane
+// (row lane/4, columns 2(lane%4), +1), returned in the same distribution.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
 // PAGED: K/V tiles are addressed through the page table (instantiated
 // separately so the contiguous path carries none of the paging code).
 // NB: query rows per CTA in blocks of 8 (the MMA's N): 1 when a kv head has at

@@ -375,13 +375,6 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
 }
 
 // D(16x8 f32) += A(16x16 bf16) * B(16x8 bf16)
-// Transpose of an 8x8 matrix of 16-bit elements held one 32-bit pair per lane
-// (row lane/4, columns 2(lane%4), +1), returned in the same distribution.
-__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
-  uint32_t y;
-  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
-  return y;
-}
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                                uint32_t b1) {
   asm volatile(
