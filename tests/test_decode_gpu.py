@@ -66,6 +66,7 @@ def test_valid_length_is_clamped(fa, L, expect):
     (2, 40, 2, 300, 64, 251),     # G = 20: two head blocks, D = 64
     (1, 4, 4, 200, 64, 77),       # MHA
     (2, 6, 1, 100, 128, 100),     # G = 6, no tail
+    (1, 16, 2, 500, 128, 333),    # G = 8: one full 8-row block
 ])
 def test_decode_shapes(fa, B, Hq, Hkv, cap, D, L):
     q, kc, vc, L = fa_inputs.decode_inputs(B, Hq, Hkv, cap, D, seed=3, L=L)

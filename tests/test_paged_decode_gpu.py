@@ -108,6 +108,7 @@ def test_paged_bad_page_id_is_masked_and_reported(fa):
     (2, 4, 8, 2, 128, 64, 16, [700, 3]),        # 4 tokens x 4 heads = 16 MMA rows; L < Sq
     (3, 2, 32, 4, 64, 32, 30, [1, 960, 513]),   # 2 x 8 rows per kv head
     (1, 5, 8, 1, 128, 128, 8, [1000]),          # 5 x 8 = 40 rows: three 16-row blocks
+    (2, 2, 8, 2, 128, 64, 16, [500, 64]),       # 2 x 4 = 8 rows: one 8-row block
 ])
 def test_paged_decode_several_new_tokens(fa, B, Sq, Hq, Hkv, D, page_size, max_pages, lens):
     """Sq new tokens per sequence (speculative decoding): bottom-right causal
