@@ -317,22 +317,55 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       }
       __syncwarp();
       q_issued = true;
-      for (int j = 0; j < n && ok; ++j) {
+      // Ring order K_0, V_0, K_1, V_1, ...  V_j and K_{j+1} are consumed
+      // together (P V_j, then S of step j + 1), so V_j completes on K_{j+1}'s
+      // barrier, armed for both tiles, and V_j's own barrier gets a plain
+      // arrival that keeps its phases in step: the MMA warp waits once per
+      // K/V step.  K_0 and the last V stand alone.
+      auto slot_free = [&](uint32_t cnt) {
+        return mbar_wait(&empty[cnt % NSTAGE], ((cnt / NSTAGE) & 1) ^ 1, abort_flag,
+                         &g_prefill_err, 2);
+      };
+      auto load_tile = [&](uint32_t cnt, const CUtensorMap* m, int kv_tile, uint64_t* bar) {
+        const int s = cnt % NSTAGE;
 #pragma unroll
-        for (int sel = 0; sel < 2; ++sel) {
-          const int s = kv_cnt % NSTAGE;
-          const uint32_t ph = (kv_cnt / NSTAGE) & 1;
-          if (!(ok = mbar_wait(&empty[s], ph ^ 1, abort_flag, &g_prefill_err, 2))) break;
+        for (int h = 0; h < C::HALVES; ++h)
+          tma_load_4d_hint(sKV + s * C::TILE_BYTES + h * pf::HALF_BYTES, m, bar, h * 64, hkv,
+                           sq.k0 + kv_tile * pf::BN, sq.tb, pol_kv);
+      };
+      if (n > 0) {
+        if ((ok = slot_free(kv_cnt))) {
           if (leader) {
-            mbar_arrive_expect_tx(&full[s], C::TILE_BYTES);
-            const CUtensorMap* m = sel ? &tmV : &tmK;
-#pragma unroll
-            for (int h = 0; h < C::HALVES; ++h)
-              tma_load_4d_hint(sKV + s * C::TILE_BYTES + h * pf::HALF_BYTES, m, &full[s], h * 64,
-                               hkv, sq.k0 + j * pf::BN, sq.tb, pol_kv);
+            mbar_arrive_expect_tx(&full[kv_cnt % NSTAGE], C::TILE_BYTES);
+            load_tile(kv_cnt, &tmK, 0, &full[kv_cnt % NSTAGE]);
           }
           __syncwarp();
           ++kv_cnt;
+        }
+      }
+      for (int j = 0; j < n && ok; ++j) {
+        const uint32_t cv = kv_cnt;  // V_j
+        if (j + 1 < n) {
+          const uint32_t ck = kv_cnt + 1;  // K_{j+1}
+          if (!(ok = slot_free(cv))) break;
+          if (!(ok = slot_free(ck))) break;
+          if (leader) {
+            uint64_t* bar = &full[ck % NSTAGE];
+            mbar_arrive_expect_tx(bar, 2 * C::TILE_BYTES);
+            mbar_arrive(&full[cv % NSTAGE]);
+            load_tile(cv, &tmV, j, bar);
+            load_tile(ck, &tmK, j + 1, bar);
+          }
+          __syncwarp();
+          kv_cnt += 2;
+        } else {
+          if (!(ok = slot_free(cv))) break;
+          if (leader) {
+            mbar_arrive_expect_tx(&full[cv % NSTAGE], C::TILE_BYTES);
+            load_tile(cv, &tmV, j, &full[cv % NSTAGE]);
+          }
+          __syncwarp();
+          kv_cnt += 1;
         }
       }
     }
@@ -387,7 +420,8 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       __syncwarp();
     };
 
-    // K_j / V_j of an item sit at ring positions kb + 2j / kb + 2j + 1.
+    // K_j / V_j of an item sit at ring positions kb + 2j / kb + 2j + 1; V_j
+    // and K_{j+1} complete together on K_{j+1}'s barrier (see the producer).
     auto ring_wait = [&](uint32_t idx, unsigned int site) {
       return mbar_wait(&full[idx % NSTAGE], (idx / NSTAGE) & 1, abort_flag, &g_prefill_err, site);
     };
@@ -427,9 +461,8 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       }
       commit(&empty[kb % NSTAGE]);
       if (n == 1) commit(q_empty);
-      // Operands of step 0: V_0 and K_1.
-      if (!(ok = ring_wait(kb + 1, 5))) break;
-      if (n > 1 && !(ok = ring_wait(kb + 2, 6))) break;
+      // Operands of step 0: V_0 and K_1 (one barrier: K_1's), or V_0 alone.
+      if (!(ok = ring_wait(n > 1 ? kb + 2 : kb + 1, 5))) break;
       tc_fence_after();
 
       // Per step j: PV0(j), S0(j+1), PV1(j), [operand waits of step j+1],
@@ -458,8 +491,8 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
         }
         commit(&empty[sV]);
         if (j + 1 < n) {
-          if (!(ok = ring_wait(kb + 2 * j + 3, 5))) break;                  // V_{j+1}
-          if (j + 2 < n && !(ok = ring_wait(kb + 2 * j + 4, 6))) break;     // K_{j+2}
+          // V_{j+1} and K_{j+2} on K_{j+2}'s barrier, or the last V alone.
+          if (!(ok = ring_wait(j + 2 < n ? kb + 2 * j + 4 : kb + 2 * j + 3, 6))) break;
           tc_fence_after();
           if (j + 1 < nt1) {
             issue_s(1, sK);
