@@ -465,9 +465,10 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       if (!(ok = ring_wait(n > 1 ? kb + 2 : kb + 1, 5))) break;
       tc_fence_after();
 
-      // Per step j: PV0(j), S0(j+1), PV1(j), [operand waits of step j+1],
-      // S1(j+1).  The waits sit where PV1(j) still fills the MMA queue, so
-      // their latency leaves less of the tensor pipe idle.
+      // Per step j: PV0(j), S0(j+1), PV1(j), S1(j+1), then the operand wait
+      // of step j+1 (V_{j+1} and K_{j+2}; K_{j+1} was waited for a step
+      // earlier).  The wait sits behind a whole batch of issued MMAs, so its
+      // latency leaves less of the tensor pipe idle.
       for (int j = 0; j < n && ok; ++j) {
         const int sV = (kb + 2 * j + 1) % NSTAGE;
         const int sK = (kb + 2 * j + 2) % NSTAGE;  // K_{j+1}
@@ -491,15 +492,15 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
         }
         commit(&empty[sV]);
         if (j + 1 < n) {
-          // V_{j+1} and K_{j+2} on K_{j+2}'s barrier, or the last V alone.
-          if (!(ok = ring_wait(j + 2 < n ? kb + 2 * j + 4 : kb + 2 * j + 3, 6))) break;
-          tc_fence_after();
           if (j + 1 < nt1) {
             issue_s(1, sK);
             commit(&s_full[1]);
           }
           commit(&empty[sK]);
           if (j + 1 == n - 1) commit(q_empty);
+          // V_{j+1} and K_{j+2} on K_{j+2}'s barrier, or the last V alone.
+          if (!(ok = ring_wait(j + 2 < n ? kb + 2 * j + 4 : kb + 2 * j + 3, 6))) break;
+          tc_fence_after();
         }
       }
     }
