@@ -386,16 +386,21 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
     uint32_t kv_cnt = 0, local = 0, p_cnt0 = 0, p_cnt1 = 0, next = 0;
     bool ok = true;
 
+    // Descriptors advance by adding (byte offset >> 4) to the base descriptor:
+    // the start-address field holds address bits 4-17, and shared-memory
+    // addresses stay below 2^18, so the addition never carries out of it.
+    const uint64_t q_desc[2] = {sdesc_sw128(sq_addr, 16, 1024),
+                                sdesc_sw128(sq_addr + C::TILE_BYTES, 16, 1024)};
     // S_i = Q_i K^T over D/16 k-steps (K-major A and B, 128-byte swizzle).
     auto issue_s = [&](int i, int stage) {
       if (leader) {
         const uint32_t d_tmem = tmem + (i ? C::COL_S1 : C::COL_S0);
+        const uint64_t a0 = q_desc[i];
+        const uint64_t b0 = sdesc_sw128(skv_addr + stage * C::TILE_BYTES, 16, 1024);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const uint32_t hoff = (k >> 2) * pf::HALF_BYTES + (k & 3) * 32;
-          const uint64_t a = sdesc_sw128(sq_addr + i * C::TILE_BYTES + hoff, 16, 1024);
-          const uint64_t bd = sdesc_sw128(skv_addr + stage * C::TILE_BYTES + hoff, 16, 1024);
-          mma_ss(d_tmem, a, bd, IDESC_S, k > 0 ? 1u : 0u);
+          const uint32_t hoff16 = ((k >> 2) * pf::HALF_BYTES + (k & 3) * 32) >> 4;
+          mma_ss(d_tmem, a0 + hoff16, b0 + hoff16, IDESC_S, k > 0 ? 1u : 0u);
         }
       }
       __syncwarp();
@@ -405,10 +410,10 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       if (leader) {
         const uint32_t d_tmem = tmem + (i ? C::COL_O1 : C::COL_O0);
         const uint32_t p_tmem = tmem + (i ? C::COL_S1 : C::COL_S0);
+        const uint64_t b0 = sdesc_sw128(skv_addr + stage * C::TILE_BYTES, pf::HALF_BYTES, 1024);
 #pragma unroll
         for (int k = 0; k < pf::BN / 16; ++k) {
-          const uint64_t bd =
-              sdesc_sw128(skv_addr + stage * C::TILE_BYTES + k * 16 * 128, pf::HALF_BYTES, 1024);
+          const uint64_t bd = b0 + (uint32_t)((k * 16 * 128) >> 4);
           mma_ts(d_tmem, p_tmem + k * 8, bd, IDESC_O, (accumulate || k > 0) ? 1u : 0u);
         }
       }
