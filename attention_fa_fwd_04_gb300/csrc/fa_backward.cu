@@ -337,13 +337,16 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
     bool ok = true;
     constexpr uint32_t COL_DP = 256, COL_DQ = 384;
     // D_tmem = A (K-major smem) x B^T (K-major smem) over D/16 k-steps.
+    // Descriptors advance by adding (byte offset >> 4) to one base each: the
+    // start-address field holds address bits 4-17, and shared-memory
+    // addresses stay below 2^18, so the addition never carries out of it.
     auto issue_nt = [&](uint32_t d_col, uint32_t a_addr, uint32_t b_addr) {
       if (leader) {
+        const uint64_t a0 = sdesc_sw128(a_addr, 16, 1024), b0 = sdesc_sw128(b_addr, 16, 1024);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const uint32_t hoff = (k >> 2) * bw::HALF_BYTES + (k & 3) * 32;
-          mma_ss(tmem + d_col, sdesc_sw128(a_addr + hoff, 16, 1024),
-                 sdesc_sw128(b_addr + hoff, 16, 1024), IDESC_S, k > 0 ? 1u : 0u);
+          const uint32_t hoff16 = ((k >> 2) * bw::HALF_BYTES + (k & 3) * 32) >> 4;
+          mma_ss(tmem + d_col, a0 + hoff16, b0 + hoff16, IDESC_S, k > 0 ? 1u : 0u);
         }
       }
       __syncwarp();
@@ -418,9 +421,10 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
         tc_fence_after();
         const uint32_t kaddr = addr(kslot(kb + j));
         if (leader) {
+          const uint64_t b0 = sdesc_sw128(kaddr, bw::HALF_BYTES, 1024);
 #pragma unroll
           for (int k = 0; k < bw::BT / 16; ++k) {
-            const uint64_t bd = sdesc_sw128(kaddr + k * 16 * 128, bw::HALF_BYTES, 1024);
+            const uint64_t bd = b0 + (uint32_t)((k * 16 * 128) >> 4);
             mma_ts(tmem + COL_DQ, tmem + (gj & 1) * 128 + k * 8, bd, IDESC_ACC,
                    (j > 0 || k > 0) ? 1u : 0u);
           }
@@ -747,14 +751,16 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
     uint32_t st_cnt = 0, local = 0, gcnt = 0;
     bool ok = true;
     // D_tmem (128 x 64) = A (128-row tile, K-major) x B^T (64-row sub-tile, K-major).
+    // Descriptors advance by adding (byte offset >> 4) to one base each (the
+    // start-address field never carries: shared memory lies below 2^18).
     auto issue_nt = [&](uint32_t d_col, uint32_t a_addr, uint32_t b_addr) {
       if (leader) {
+        const uint64_t a0 = sdesc_sw128(a_addr, 16, 1024), b0 = sdesc_sw128(b_addr, 16, 1024);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const uint32_t ka = (k >> 2) * bw::HALF_BYTES + (k & 3) * 32;
-          const uint32_t kb = (k >> 2) * bw::SUB_HALF + (k & 3) * 32;
-          mma_ss(tmem + d_col, sdesc_sw128(a_addr + ka, 16, 1024),
-                 sdesc_sw128(b_addr + kb, 16, 1024), IDESC_S, k > 0 ? 1u : 0u);
+          const uint32_t ka16 = ((k >> 2) * bw::HALF_BYTES + (k & 3) * 32) >> 4;
+          const uint32_t kb16 = ((k >> 2) * bw::SUB_HALF + (k & 3) * 32) >> 4;
+          mma_ss(tmem + d_col, a0 + ka16, b0 + kb16, IDESC_S, k > 0 ? 1u : 0u);
         }
       }
       __syncwarp();
@@ -762,9 +768,10 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
     // acc += A (TMEM, 16-bit, 64 columns of K) x B (64-row sub-tile, MN-major).
     auto issue_acc = [&](uint32_t d_col, uint32_t a_col, uint32_t b_addr, bool accumulate) {
       if (leader) {
+        const uint64_t b0 = sdesc_sw128(b_addr, bw::SUB_HALF, 1024);
 #pragma unroll
         for (int k = 0; k < QS / 16; ++k) {
-          const uint64_t bd = sdesc_sw128(b_addr + k * 16 * 128, bw::SUB_HALF, 1024);
+          const uint64_t bd = b0 + (uint32_t)((k * 16 * 128) >> 4);
           mma_ts(tmem + d_col, tmem + a_col + k * 8, bd, IDESC_ACC,
                  (accumulate || k > 0) ? 1u : 0u);
         }
