@@ -9,7 +9,8 @@ integers, ``stream`` a ``cudaStream_t`` value):
     fa_prefill_fwd, fa_prefill_fwd_lse, fa_prefill_varlen_fwd, fa_decode_fwd, fa_decode_fwd_lse,
     fa_decode_paged_fwd, fa_backward,
     fa_decode_fwd_noalloc, fa_status_string, fa_device_error, fa_last_cuda_error,
-    fa_num_sms, fa_prefill_work_item
+    fa_num_sms, fa_prefill_work_item, fa_prefill_rescale_count, fa_set_wait_limit_ns,
+    fa_prefill_fwd_host, fa_prefill_host_pieces
 Tensor conveniences (contiguous CUDA tensors, caller-owned outputs):
     prefill(q, k, v, scale, causal, out=None, stream=None, lse=None)
     prefill_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, scale, causal,
@@ -18,9 +19,8 @@ Tensor conveniences (contiguous CUDA tensors, caller-owned outputs):
     decode_paged(q, kpages, vpages, page_table, seqlens, scale, out=None, stream=None,
                  lse=None)
     backward(q, k, v, o, dout, lse, scale, causal, stream=None) -> (dq, dk, dv)
+    prefill_host(q, k, v, out, scale, causal, n_pieces=16, stream=None)
     (lse=True allocates the fp32 log-sum-exp output; a tensor is used as is.)
-Host-to-host prefill (submodule ``host_pipeline``): HostPrefill overlaps the
-uploads of Q, K, V and the download of O with per-piece fa_prefill_fwd calls.
 """
 import ctypes
 import os
@@ -37,7 +37,8 @@ FA_ERR_BOUNDS = 6
 EXPORTS = ("fa_prefill_fwd", "fa_prefill_fwd_lse", "fa_prefill_varlen_fwd", "fa_decode_fwd",
            "fa_decode_fwd_lse", "fa_decode_paged_fwd", "fa_backward",
            "fa_decode_fwd_noalloc", "fa_status_string", "fa_device_error", "fa_last_cuda_error",
-           "fa_num_sms", "fa_prefill_work_item")
+           "fa_num_sms", "fa_prefill_work_item", "fa_prefill_rescale_count",
+           "fa_set_wait_limit_ns", "fa_prefill_fwd_host", "fa_prefill_host_pieces")
 
 _lib = None
 
@@ -94,6 +95,15 @@ def load(path: str = LIB_PATH):
     ip = ctypes.POINTER(ctypes.c_int)
     lib.fa_prefill_work_item.argtypes = [i32, i32, i32, i32, i32, i32, i32, ip, ip, ip]
     lib.fa_prefill_work_item.restype = i32
+    lib.fa_prefill_rescale_count.argtypes = [i32, ctypes.POINTER(ctypes.c_ulonglong)]
+    lib.fa_prefill_rescale_count.restype = i32
+    lib.fa_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
+    lib.fa_set_wait_limit_ns.restype = i32
+    lib.fa_prefill_fwd_host.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, i32,
+                                        i32, i32, vp]
+    lib.fa_prefill_fwd_host.restype = i32
+    lib.fa_prefill_host_pieces.argtypes = [i32, i32, i32, i32, i32, ip, ip, ip, ip, i32]
+    lib.fa_prefill_host_pieces.restype = i32
     _lib = lib
     return lib
 
@@ -115,6 +125,25 @@ def fa_prefill_varlen_fwd(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, B, Hq, Hk
     return load().fa_prefill_varlen_fwd(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, B, Hq, Hkv,
                                         total_q, total_k, max_seqlen_q, D, scale, causal, dtype,
                                         stream)
+
+
+def fa_prefill_fwd_host(q_host, k_host, v_host, o_host, B, Hq, Hkv, Sq, Sk, D, scale, causal,
+                        dtype, n_pieces, stream):
+    return load().fa_prefill_fwd_host(q_host, k_host, v_host, o_host, B, Hq, Hkv, Sq, Sk, D,
+                                      scale, causal, dtype, n_pieces, stream)
+
+
+def fa_prefill_host_pieces(B, Sq, Sk, causal, n_pieces):
+    """The piece plan of fa_prefill_fwd_host: a list of (b, s0, s1, sk) in
+    upload order (rows [s0, s1) of sequence b see keys [0, sk))."""
+    lib = load()
+    n = lib.fa_prefill_host_pieces(B, Sq, Sk, int(bool(causal)), n_pieces, None, None, None,
+                                   None, 0)
+    if n < 0:
+        raise ValueError("bad arguments")
+    arr = [(ctypes.c_int * max(n, 1))() for _ in range(4)]
+    lib.fa_prefill_host_pieces(B, Sq, Sk, int(bool(causal)), n_pieces, *arr, n)
+    return [tuple(a[i] for a in arr) for i in range(n)]
 
 
 def fa_decode_fwd(q, kcache, vcache, valid_len_dev, o, B, Hq, Hkv, cap, D, scale, stream):
@@ -175,6 +204,20 @@ def fa_prefill_work_item(w, B, Hq, Hkv, Sq, Sk=0, causal=1):
     n = load().fa_prefill_work_item(w, B, Hq, Hkv, Sq, Sk, causal, ctypes.byref(b),
                                      ctypes.byref(hq), ctypes.byref(qb))
     return n, b.value, hq.value, qb.value
+
+
+def fa_prefill_rescale_count(reset=0):
+    """(status, count): prefill (row, K/V tile) steps that took the lazy
+    rescale since the last reset; synchronises."""
+    c = ctypes.c_ulonglong(0)
+    st = load().fa_prefill_rescale_count(int(reset), ctypes.byref(c))
+    return st, c.value
+
+
+def fa_set_wait_limit_ns(ns):
+    """Time limit of every device pipeline wait (0: the 2 s default);
+    synchronises."""
+    return load().fa_set_wait_limit_ns(int(ns))
 
 
 # ----------------------------------------------------------------------------
@@ -245,6 +288,29 @@ def prefill(q, k, v, scale, causal, out=None, stream=None, lse=None):
                         _stream_handle(stream))
     if st != FA_OK:
         raise FAError(st, "fa_prefill_fwd")
+    return out
+
+
+def prefill_host(q, k, v, out, scale, causal, n_pieces=16, stream=None):
+    """fa_prefill_fwd_host: O = softmax(scale * Q K^T [+ causal mask]) V from
+    host tensors q [B,Sq,Hq,D], k/v [B,Sk,Hkv,D] into the host tensor ``out``
+    (contiguous, bf16/fp16; pinned for the copies to overlap the kernels).
+    Enqueued on ``stream`` (default: torch's current stream); ``out`` is
+    complete once that stream reaches the point after this call."""
+    B, Sq, Hq, D = q.shape
+    Bk, Sk, Hkv, Dk = k.shape
+    if Bk != B or Dk != D or tuple(v.shape) != tuple(k.shape) or tuple(out.shape) != tuple(q.shape):
+        raise ValueError("shape mismatch between q, k, v, out")
+    if k.dtype != q.dtype or v.dtype != q.dtype or out.dtype != q.dtype:
+        raise TypeError("q, k, v, out must share a dtype")
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out")):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous host tensor")
+    st = fa_prefill_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, Hq, Hkv,
+                             Sq, Sk, D, float(scale), int(bool(causal)), _dtype_code(q),
+                             int(n_pieces), _stream_handle(stream))
+    if st != FA_OK:
+        raise FAError(st, "fa_prefill_fwd_host")
     return out
 
 

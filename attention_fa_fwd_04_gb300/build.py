@@ -14,7 +14,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libfa_gb300.so")
 SOURCES = ["fa_api.cu", "fa_prefill.cu", "fa_decode.cu", "fa_decode_noalloc.cu",
-           "fa_backward.cu"]
+           "fa_backward.cu", "fa_host.cu"]
 HEADERS = ["fa_ptx.cuh", "fa_internal.h"]
 
 NVCC = os.environ.get("NVCC", "nvcc")

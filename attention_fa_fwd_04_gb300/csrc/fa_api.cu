@@ -68,13 +68,15 @@ static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 static thread_local int t_last_cuda_error = 0;
 static thread_local const char* t_last_site = "";
 
-static int cuda_status(int e, const char* site) {
+int fa::record_cuda_status(int e, const char* site) {
   if (e == 0) return FA_OK;
   t_last_cuda_error = e;
   t_last_site = site;
   cudaGetLastError();  // clear a non-sticky error so later calls start clean
   return FA_ERR_CUDA;
 }
+
+static int cuda_status(int e, const char* site) { return fa::record_cuda_status(e, site); }
 
 static bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
@@ -309,6 +311,22 @@ extern "C" int fa_device_error(int reset, unsigned int* detail) {
 }
 
 extern "C" int fa_num_sms(void) { return fa::sm_count(); }
+
+extern "C" int fa_prefill_rescale_count(int reset, unsigned long long* count) {
+  if (!count) return FA_ERR_INVALID_ARG;
+  const cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_status(e, "rescale count synchronize");
+  return cuda_status(fa::read_prefill_rescales(count, reset), "rescale count read");
+}
+
+extern "C" int fa_set_wait_limit_ns(unsigned long long ns) {
+  const cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_status(e, "wait limit synchronize");
+  int r = fa::set_prefill_wait_limit(ns);
+  if (r == 0) r = fa::set_decode_wait_limit(ns);
+  if (r == 0) r = fa::set_backward_wait_limit(ns);
+  return cuda_status(r, "wait limit set");
+}
 
 extern "C" int fa_last_cuda_error(const char** site) {
   if (site) *site = t_last_site;

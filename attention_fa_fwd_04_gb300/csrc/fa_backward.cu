@@ -259,6 +259,11 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
   const uint32_t tmem = *tmem_holder;
   const bool leader = lane == 0;
   const int off = p.Sk - p.Sq;
+  // The producer's loads that may still be in flight if the CTA aborts (the
+  // last KRING K and VRING V tiles, the Q/dO tiles of its last item); drained
+  // after the final CTA barrier.
+  uint32_t prod_k = 0, prod_v = 0, prod_q_par = 0;
+  bool prod_q_any = false;
 
   if (warp == 4) {
     // ================================ producer ================================
@@ -271,7 +276,7 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
     const uint64_t pol_q = l2_policy_evict_first();
     const uint64_t pol_kv = l2_policy_evict_last();
     uint32_t k_iss = 0, v_iss = 0, local = 0;  // K / V tiles issued so far
-    bool ok = true, q_issued = false;
+    bool ok = true;
     for (uint32_t k = 0; ok; ++k, ++local) {
       const int w = sched_produce(k, p.work_ctr, p.n_items, sched_full, sched_empty, sched,
                                   abort_flag, &g_backward_err, leader);
@@ -283,7 +288,6 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
       dq_item(w, p, &b, &hq, &qt);
       const int hkv = hq / p.G;
       const int n = bw_key_tiles(qt * bw::BT, p);
-      q_issued = false;
       if (local > 0 && !(ok = mbar_wait(q_empty, (local - 1) & 1, abort_flag, &g_backward_err, 1)))
         break;
       if (leader) {
@@ -296,7 +300,8 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
         }
       }
       __syncwarp();
-      q_issued = true;
+      prod_q_par = local & 1;  // (Q of earlier items has landed: q_empty was waited for)
+      prod_q_any = true;
       for (int j = 0; j < n && ok; ++j) {
 #pragma unroll
         for (int sel = 0; sel < 2; ++sel) {  // K_j, then V_j
@@ -315,17 +320,10 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
           }
           __syncwarp();
           if (sel) ++v_iss; else ++k_iss;
+          prod_k = k_iss;
+          prod_v = v_iss;
         }
       }
-    }
-    if (!ok) {
-      // Wait (bounded) for the loads possibly still in flight: the last KRING
-      // K tiles and VRING V tiles issued.
-      for (uint32_t u = k_iss > (uint32_t)bw::KRING ? k_iss - bw::KRING : 0u; u < k_iss; ++u)
-        mbar_wait_drain(&full[u % bw::KRING], (u / bw::KRING) & 1);
-      for (uint32_t u = v_iss > (uint32_t)bw::VRING ? v_iss - bw::VRING : 0u; u < v_iss; ++u)
-        mbar_wait_drain(&full[bw::KRING + u % bw::VRING], (u / bw::VRING) & 1);
-      if (q_issued) mbar_wait_drain(q_full, local & 1);
     }
     __syncwarp();
   } else if (warp == 5) {
@@ -576,6 +574,16 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
     tc_fence_after();
     tmem_dealloc(tmem, bw::TMEM_COLS);
   }
+  // Aborted CTA: wait, bounded, for the loads that may still be in flight
+  // (older ones have landed: their slot was released before it was reused).
+  if (warp == 4 && *abort_flag) {
+    for (uint32_t u = prod_k > (uint32_t)bw::KRING ? prod_k - bw::KRING : 0u; u < prod_k; ++u)
+      mbar_wait_drain(&full[u % bw::KRING], (u / bw::KRING) & 1);
+    for (uint32_t u = prod_v > (uint32_t)bw::VRING ? prod_v - bw::VRING : 0u; u < prod_v; ++u)
+      mbar_wait_drain(&full[bw::KRING + u % bw::VRING], (u / bw::VRING) & 1);
+    if (prod_q_any) mbar_wait_drain(q_full, prod_q_par);
+    __syncwarp();
+  }
 }
 
 // ------------------------------------------------------------------------------
@@ -661,6 +669,11 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
     return i0 <= 0 ? 0 : i0 / QS;
   };
   constexpr uint32_t COL_DV = 256, COL_DK = 256 + D;
+  // The producer's loads that may still be in flight if the CTA aborts (the
+  // last NS sub-tile stages, the K/V tiles of its last item); drained after
+  // the final CTA barrier.
+  uint32_t prod_st = 0, prod_kv_par = 0;
+  bool prod_kv_any = false;
 
   if (warp == 4) {
     // ================================ producer ================================
@@ -673,7 +686,7 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
     const uint64_t pol_kv = l2_policy_evict_first();
     const uint64_t pol_q = l2_policy_evict_last();
     uint32_t st_cnt = 0, local = 0;
-    bool ok = true, kv_issued = false;
+    bool ok = true;
     for (uint32_t k = 0; ok; ++k, ++local) {
       const int w = sched_produce(k, p.work_ctr, p.n_items, sched_full, sched_empty, sched,
                                   abort_flag, &g_backward_err, leader);
@@ -684,7 +697,6 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
       int b, hkv, kt;
       dkv_item(w, p, &b, &hkv, &kt);
       const int q0 = first_sub(kt * bw::BT);
-      kv_issued = false;
       if (local > 0 &&
           !(ok = mbar_wait(kv_empty, (local - 1) & 1, abort_flag, &g_backward_err, 1)))
         break;
@@ -699,7 +711,8 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
         }
       }
       __syncwarp();
-      kv_issued = true;
+      prod_kv_par = local & 1;  // (K/V of earlier items has landed: kv_empty was waited for)
+      prod_kv_any = true;
       // Query sub-tiles descending, the group's heads innermost: the items of
       // one kv head then read the same Q / dO tiles at about the same time.
       for (int qs = n_qs - 1; qs >= q0 && ok; --qs) {
@@ -734,13 +747,9 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
           if (leader) mbar_arrive(&full[s]);  // the second arrival, after the smem writes
           __syncwarp();
           ++st_cnt;
+          prod_st = st_cnt;
         }
       }
-    }
-    if (!ok) {
-      const uint32_t first = st_cnt > (uint32_t)NS ? st_cnt - NS : 0u;
-      for (uint32_t u = first; u < st_cnt; ++u) mbar_wait_drain(&full[u % NS], (u / NS) & 1);
-      if (kv_issued) mbar_wait_drain(kv_full, local & 1);
     }
     __syncwarp();
   } else if (warp == 5) {
@@ -980,6 +989,13 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
     tc_fence_after();
     tmem_dealloc(tmem, bw::TMEM_COLS);
   }
+  // Aborted CTA: wait, bounded, for the loads that may still be in flight.
+  if (warp == 4 && *abort_flag) {
+    const uint32_t first = prod_st > (uint32_t)NS ? prod_st - NS : 0u;
+    for (uint32_t u = first; u < prod_st; ++u) mbar_wait_drain(&full[u % NS], (u / NS) & 1);
+    if (prod_kv_any) mbar_wait_drain(kv_full, prod_kv_par);
+    __syncwarp();
+  }
 }
 
 // ------------------------------------------------------------------------------
@@ -1076,6 +1092,8 @@ int launch_backward(const void* q, const void* k, const void* v, const void* o, 
               : launch_backward_t<128, __half>(q, k, v, o, dout, lse, dq, dk, dv, delta, B, Hq,
                                                Hkv, Sq, Sk, scale, causal, stream);
 }
+
+int set_backward_wait_limit(unsigned long long ns) { return set_wait_limit_this_unit(ns); }
 
 int read_backward_error(unsigned int* out, int reset) {
   unsigned int v = 0;

@@ -198,6 +198,8 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
   __syncthreads();
 
   const int g = lane >> 2, tq = lane & 3;
+  // Tiles the producer issued (drained at the end if the CTA aborted).
+  int prod_t = 0;
 
   if (warp == NW) {
     // ---------------- producer warp: lanes stay converged, lane 0 issues ----------------
@@ -242,11 +244,7 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
       }
       __syncwarp();
     }
-    if (t < n_tiles) {
-      // Aborted: let the loads already issued land before the CTA exits.
-      for (int u = (t - NSTAGE > 0 ? t - NSTAGE : 0); u < t; ++u)
-        mbar_wait_drain(&full[u % NSTAGE], (u / NSTAGE) & 1);
-    }
+    prod_t = t;
     __syncwarp();
   } else {
     // ---------------- consumers: whole tiles, round-robin over warps ----------------
@@ -488,6 +486,15 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
     }
     reinterpret_cast<float4*>(p.part_o + (qrow(row) * p.nsplit + split) * D)[d4] = o;
   }
+  // Aborted CTA (a wait gave up, in any warp, possibly after the producer
+  // issued its last tile): wait, bounded, for the loads that may still be in
+  // flight before the CTA exits.  Tiles older than the last NSTAGE have landed
+  // (their stage was released before the producer reused it).
+  if (warp == NW && *abort_flag) {
+    for (int u = (prod_t - NSTAGE > 0 ? prod_t - NSTAGE : 0); u < prod_t; ++u)
+      mbar_wait_drain(&full[u % NSTAGE], (u / NSTAGE) & 1);
+    __syncwarp();
+  }
 }
 
 // Combine: one CTA per (32 output columns, head, batch), 8 warps, up to
@@ -726,6 +733,8 @@ int launch_decode(const void* q, const void* kc, const void* vc, const int32_t* 
   return launch_decode_layout(q, kc, vc, ly, o, lse, B, Hq, Hkv, D, scale, scratch,
                               scratch_floats, stream);
 }
+
+int set_decode_wait_limit(unsigned long long ns) { return set_wait_limit_this_unit(ns); }
 
 int read_decode_error(unsigned int* out, int reset) {
   unsigned int v = 0;

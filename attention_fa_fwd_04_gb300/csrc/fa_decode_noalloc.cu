@@ -90,17 +90,17 @@ extern "C" int fa_decode_fwd_noalloc(const void* q, const void* kcache, const vo
   if ((int64_t)cap * Hkv * D * 2 >= (1ll << 40)) return FA_ERR_INVALID_ARG;
   if (cap == 0) {
     // No cache: O = 0, no partials needed.
-    return fa::launch_decode(q, kcache, vcache, valid_len_dev, o, nullptr, B, Hq, Hkv, 0, D,
-                             scale, nullptr, 0, stream) == 0
-               ? FA_OK
-               : FA_ERR_CUDA;
+    return fa::record_cuda_status(fa::launch_decode(q, kcache, vcache, valid_len_dev, o, nullptr,
+                                                    B, Hq, Hkv, 0, D, scale, nullptr, 0, stream),
+                                  "decode_noalloc zero-fill launch");
   }
   const size_t need = fa::decode_scratch_floats(B, Hq, Hkv, cap, D);
   if (need > kNoAllocScratchFloats) return FA_ERR_TOO_LARGE;
   cudaError_t err = cudaSuccess;
   float* scratch = scratch_for_current_device(&err);
-  if (!scratch) return FA_ERR_CUDA;
-  const int r = fa::launch_decode(q, kcache, vcache, valid_len_dev, o, nullptr, B, Hq, Hkv, cap,
-                                  D, scale, scratch, kNoAllocScratchFloats, stream);
-  return r == 0 ? FA_OK : FA_ERR_CUDA;
+  if (!scratch) return fa::record_cuda_status(err, "decode_noalloc cudaGetSymbolAddress");
+  return fa::record_cuda_status(fa::launch_decode(q, kcache, vcache, valid_len_dev, o, nullptr,
+                                                  B, Hq, Hkv, cap, D, scale, scratch,
+                                                  kNoAllocScratchFloats, stream),
+                                "decode_noalloc launch");
 }

@@ -73,6 +73,21 @@ int read_backward_error(unsigned int* out, int reset);
 int read_prefill_error(unsigned int* out, int reset);
 int read_decode_error(unsigned int* out, int reset);
 
+// Rows whose prefill lazy rescale fired since the last reset (read + optionally
+// clear).  Returns a cudaError_t.
+int read_prefill_rescales(unsigned long long* out, int reset);
+
+// Time limit of the pipeline waits of each kernel translation unit on the
+// current device (0 = the 2 s default).  Synchronous; return a cudaError_t.
+int set_prefill_wait_limit(unsigned long long ns);
+int set_decode_wait_limit(unsigned long long ns);
+int set_backward_wait_limit(unsigned long long ns);
+
+// Status of a CUDA call for the C ABI: FA_OK for 0, else FA_ERR_CUDA after
+// recording the raw error and the failing call (a static string) for
+// fa_last_cuda_error() in the calling thread.
+int record_cuda_status(int cuda_error, const char* site);
+
 // Work-item decode of the persistent prefill scheduler (host copy).
 void prefill_item_host(int w, int B, int Hq, int Hkv, int n_qb, int* b, int* hq, int* qb);
 

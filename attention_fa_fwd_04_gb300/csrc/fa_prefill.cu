@@ -27,9 +27,10 @@
 // MMA issue order per KV step j: PV0(j), S0(j+1), PV1(j), S1(j+1), so each
 // softmax group has two MMA blocks of time to turn S_i into P_i.
 // Softmax: exp2 domain with scale*log2(e) folded into one FMA; lazy rescale
-// (O and l are rescaled only when a row max grows by more than 2^8 in the
-// exp2 domain; the gfx950 README's "lazy" lever); causal and Sk-tail masks only
-// on the tiles that need them (its "diagonal-only causal masking").
+// (O and l are rescaled only when a tile's row sum of P, taken against the
+// stale running max, exceeds 2^60 for bf16 P or 2^15 for fp16 P; the gfx950
+// README's "lazy" lever); causal and Sk-tail masks only on the tiles that need
+// them (its "diagonal-only causal masking").
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <math.h>
@@ -43,6 +44,9 @@
 namespace fa {
 
 __device__ unsigned int g_prefill_err = 0;
+// Rows (summed over K/V tiles) whose lazy rescale fired: the slow path of the
+// softmax that rescales O and l to a new running max and recomputes P.
+__device__ unsigned long long g_prefill_rescales = 0;
 
 namespace pf {
 constexpr int BM = 128;         // rows per Q tile
@@ -75,19 +79,18 @@ struct Cfg {
 struct PrefillParams {
   void* o;     // [B, Sq, Hq, D]; packed sequences: [total_q, Hq, D]
   float* lse;  // [B, Hq, Sq]; packed: [Hq, total_q]; natural-log log-sum-exp, or null
-  // Packed (variable-length) sequences: prefix sums of the sequence lengths,
-  // [B + 1] each, in device memory; null for a dense batch.  Sq is then the
-  // longest query length (it sizes the schedule) and Sk is unused.
-  const int32_t* cu_q;
-  const int32_t* cu_k;
+  // Packed (variable-length) sequences: the work units, longest first, as
+  // written by varlen_plan_kernel (two int4 per unit: {q0, k0, Sq, Sk} of its
+  // sequence and {qb, b, 0, 0}), and their number (device).  Null for a dense
+  // batch.  Sq is then the longest query length and Sk is unused.
+  const int4* units;
+  const int* n_units;
   int total_q, total_k;
   int B, Hq, Hkv, Sq, Sk, G, causal, n_qb, n_items;
   // Work counter [2] (claims, CTAs finished), zero when the launch starts:
   // each persistent CTA claims the next work item when it is free (items keep
-  // their kv-head-major order); the last CTA to finish zeroes both again.
-  // Null for packed sequences, which keep the fixed grid stride: their many
-  // short items (and blocks past the end of short sequences) measured faster
-  // without the claim's round trips.
+  // their order: kv-head-major for a dense batch, the planned longest-first
+  // list for packed sequences); the last CTA to finish zeroes both again.
   unsigned int* work_ctr;
   float c;  // scale * log2(e)
 };
@@ -99,35 +102,6 @@ struct SeqSpan {
   int Sq, Sk;   // its lengths
   size_t orow;  // packed row index of its query row 0 (O is [rows, Hq, D])
 };
-
-// Every role calls this with the same arguments and so takes the same
-// decision.  Packed offsets that are not 0 <= cu[b] <= cu[b+1] <= total, or a
-// query length beyond the schedule's n_qb * 256 rows, make the sequence empty
-// and set the bounds bit of the error word.
-template <bool PACKED>
-__device__ __forceinline__ SeqSpan seq_span(const PrefillParams& p, int b, unsigned int* err) {
-  SeqSpan s;
-  if constexpr (!PACKED) {
-    s.q0 = 0;
-    s.k0 = 0;
-    s.tb = b;
-    s.Sq = p.Sq;
-    s.Sk = p.Sk;
-    s.orow = (size_t)b * p.Sq;
-  } else {
-    const int q0 = p.cu_q[b], q1 = p.cu_q[b + 1], k0 = p.cu_k[b], k1 = p.cu_k[b + 1];
-    const bool ok = 0 <= q0 && q0 <= q1 && q1 <= p.total_q && 0 <= k0 && k0 <= k1 &&
-                    k1 <= p.total_k && q1 - q0 <= p.n_qb * 256;
-    if (!ok && err) atomicOr(err, kErrBounds);
-    s.q0 = ok ? q0 : 0;
-    s.k0 = ok ? k0 : 0;
-    s.tb = 0;
-    s.Sq = ok ? q1 - q0 : 0;
-    s.Sk = ok ? k1 - k0 : 0;
-    s.orow = (size_t)s.q0;
-  }
-  return s;
-}
 
 // Work item w -> (b, hq, qb): kv-head-major, then batch, then query blocks in
 // decreasing order (longest causal rows first), then the query heads of the
@@ -150,9 +124,40 @@ void prefill_item_host(int w, int B, int Hq, int Hkv, int n_qb, int* b, int* hq,
   prefill_item(w, B, Hq, Hkv, n_qb, b, hq, qb);
 }
 
+// Work item w of either kind.  Dense: prefill_item.  Packed: unit w / Hq of
+// the planned list (longest first) with query head w % Hq, so the query heads
+// of one kv head, which read the same K/V, run side by side.
+template <bool PACKED>
+__device__ __forceinline__ SeqSpan work_item(const PrefillParams& p, int w, int* b, int* hq,
+                                             int* qb) {
+  SeqSpan s;
+  if constexpr (!PACKED) {
+    prefill_item(w, p.B, p.Hq, p.Hkv, p.n_qb, b, hq, qb);
+    s.q0 = 0;
+    s.k0 = 0;
+    s.tb = *b;
+    s.Sq = p.Sq;
+    s.Sk = p.Sk;
+    s.orow = (size_t)*b * p.Sq;
+  } else {
+    const int u = w / p.Hq;
+    *hq = w - u * p.Hq;
+    const int4 a = p.units[2 * u], c = p.units[2 * u + 1];
+    *qb = c.x;
+    *b = c.y;
+    s.q0 = a.x;
+    s.k0 = a.y;
+    s.tb = 0;
+    s.Sq = a.z;
+    s.Sk = a.w;
+    s.orow = (size_t)a.x;
+  }
+  return s;
+}
+
 // Number of K/V tiles Q tile rows [row0, row0+BM) need (0 if the tile is past
 // Sq or sees no key).
-__device__ __forceinline__ int kv_tiles_for(int row0, int Sq, int Sk, int causal) {
+__host__ __device__ __forceinline__ int kv_tiles_for(int row0, int Sq, int Sk, int causal) {
   if (row0 >= Sq || Sk <= 0) return 0;
   int nk = Sk;
   if (causal) {
@@ -162,6 +167,106 @@ __device__ __forceinline__ int kv_tiles_for(int row0, int Sq, int Sk, int causal
     if (nk <= 0) return 0;
   }
   return (nk + pf::BN - 1) / pf::BN;
+}
+
+// ---------------------------------------------------------------------------
+// Packed sequences: the work plan.  One CTA reads the offsets, checks each
+// sequence (0 <= cu[b] <= cu[b+1] <= total, query length <= n_qb_max * 256;
+// a failing sequence is left out and sets the bounds bit of the error word),
+// and lists every 256-row query block of every sequence ordered by its K/V
+// tile count, largest first (longest-processing-time order; blocks past a
+// sequence's end are not listed).  The gfx950 prefill README's TODO list asks
+// for this: per-sequence load balance, so that short and long sequences of a
+// batch do not serialise.  The plan also zeroes the prefill's work counter.
+// ---------------------------------------------------------------------------
+constexpr int kPlanThreads = 1024;
+constexpr int kPlanBuckets = 4096;  // K/V tile counts >= 4095 share the top bucket
+static_assert(kPlanBuckets == 4 * kPlanThreads, "each thread scans four buckets");
+
+__device__ __forceinline__ bool plan_span(const int32_t* cu_q, const int32_t* cu_k, int b,
+                                          int total_q, int total_k, int n_qb_max, int4* span) {
+  const int q0 = cu_q[b], q1 = cu_q[b + 1], k0 = cu_k[b], k1 = cu_k[b + 1];
+  const bool ok = 0 <= q0 && q0 <= q1 && q1 <= total_q && 0 <= k0 && k0 <= k1 && k1 <= total_k &&
+                  (long long)(q1 - q0) <= (long long)n_qb_max * pf::QBLOCK;
+  *span = make_int4(q0, k0, q1 - q0, k1 - k0);
+  return ok;
+}
+
+__device__ __forceinline__ int plan_bucket(int qb, const int4& sp, int causal) {
+  const int n0 = kv_tiles_for(qb * pf::QBLOCK, sp.z, sp.w, causal);
+  const int n1 = kv_tiles_for(qb * pf::QBLOCK + pf::BM, sp.z, sp.w, causal);
+  const int n = n0 > n1 ? n0 : n1;
+  return n < kPlanBuckets - 1 ? n : kPlanBuckets - 1;
+}
+
+__global__ void __launch_bounds__(kPlanThreads)
+    varlen_plan_kernel(const int32_t* cu_q, const int32_t* cu_k, int B, int total_q, int total_k,
+                       int n_qb_max, int causal, int4* units, int* n_units,
+                       unsigned int* work_ctr) {
+  __shared__ int start[kPlanBuckets];  // counts, then each bucket's next list slot
+  __shared__ int warp_sum[kPlanThreads / 32];
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  for (int i = t; i < kPlanBuckets; i += kPlanThreads) start[i] = 0;
+  __syncthreads();
+  for (int b = t; b < B; b += kPlanThreads) {
+    int4 sp;
+    if (!plan_span(cu_q, cu_k, b, total_q, total_k, n_qb_max, &sp)) {
+      atomicOr(&g_prefill_err, kErrBounds);
+      continue;
+    }
+    const int nb = (sp.z + pf::QBLOCK - 1) / pf::QBLOCK;
+    for (int qb = 0; qb < nb; ++qb) atomicAdd(&start[plan_bucket(qb, sp, causal)], 1);
+  }
+  __syncthreads();
+  // Exclusive prefix sum over the buckets from the largest tile count down:
+  // thread t owns buckets kPlanBuckets-1-4t .. kPlanBuckets-4-4t.
+  int c[4], sum = 0;
+#pragma unroll
+  for (int x = 0; x < 4; ++x) {
+    c[x] = start[kPlanBuckets - 1 - (4 * t + x)];
+    sum += c[x];
+  }
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_sum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int ws = warp_sum[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, ws, o);
+      if (lane >= o) ws += y;
+    }
+    warp_sum[lane] = ws;  // inclusive over warps
+  }
+  __syncthreads();
+  int run = incl - sum + (warp > 0 ? warp_sum[warp - 1] : 0);  // exclusive
+  const int total = warp_sum[kPlanThreads / 32 - 1];
+#pragma unroll
+  for (int x = 0; x < 4; ++x) {
+    start[kPlanBuckets - 1 - (4 * t + x)] = run;
+    run += c[x];
+  }
+  __syncthreads();
+  for (int b = t; b < B; b += kPlanThreads) {
+    int4 sp;
+    if (!plan_span(cu_q, cu_k, b, total_q, total_k, n_qb_max, &sp)) continue;
+    const int nb = (sp.z + pf::QBLOCK - 1) / pf::QBLOCK;
+    for (int qb = 0; qb < nb; ++qb) {
+      const int pos = atomicAdd(&start[plan_bucket(qb, sp, causal)], 1);
+      units[2 * pos] = sp;
+      units[2 * pos + 1] = make_int4(qb, b, 0, 0);
+    }
+  }
+  if (t == 0) {
+    *n_units = total;
+    work_ctr[0] = 0u;
+    work_ctr[1] = 0u;
+  }
 }
 
 template <typename T>
@@ -190,10 +295,10 @@ struct IsBF16<__nv_bfloat16> {
   static constexpr bool value = true;
 };
 
-// PACKED: the batch is packed sequences (cu_q / cu_k set), scheduled by a
-// fixed grid stride; otherwise a dense batch, scheduled by the work counter.
-// (Separate instantiations: the dense kernel carries none of the packed-
-// sequence code.)
+// PACKED: the batch is packed sequences, whose work items come from the list
+// varlen_plan_kernel wrote; otherwise a dense batch.  Both claim items from
+// the work counter.  (Separate instantiations: the dense kernel carries none
+// of the packed-sequence code.)
 template <int D, typename T, bool PACKED>
 __global__ void __launch_bounds__(pf::THREADS, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -224,6 +329,14 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sched_empty + kSchedSlots);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   volatile int* sched = abort_flag + 1;  // [kSchedSlots]
+  // The producer's loads that may still be in flight if the CTA aborts,
+  // written by the producer when it leaves its loop: [0] ring positions
+  // issued (loads [n - NSTAGE, n) may be in flight), [1] q_full phase parity
+  // of the last Q issued, [2] whether any Q was issued.
+  volatile uint32_t* prod_info = reinterpret_cast<volatile uint32_t*>(sched + kSchedSlots);
+  static_assert(2 * C::NSTAGE * 8 + (9 + 2 * kSchedSlots) * 8 + 8 + 4 * (kSchedSlots + 3) <=
+                    C::SMEM_BAR,
+                "barrier block overflow");
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -262,15 +375,8 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
   // warp-aligned CTA barrier below, or tcgen05.dealloc, with lanes still
   // inside a role loop.)
   const bool leader = lane == 0;
-  // Work items.  Dense launches (work_ctr set): the producer claims each item
-  // from the counter and hands it to the MMA and softmax warps (sched_*).
-  // Packed sequences: every role walks the fixed grid stride itself.
-  constexpr bool dynamic = !PACKED;
-  auto next_stride = [&](uint32_t* pos) {
-    const int t = (int)(blockIdx.x + *pos * gridDim.x);
-    ++*pos;
-    return t < p.n_items ? t : -1;
-  };
+  // Work items: the producer claims each item from the counter and hands it
+  // to the MMA and softmax warps (sched_*).
   if (warp >= 8) {
    // ------------------ warpgroup 2: TMA producer and MMA issuer ------------------
    regs_decrease<pf::REGS_ISSUE>();
@@ -283,27 +389,23 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
     }
     const uint64_t pol_q = l2_policy_evict_first();
     const uint64_t pol_kv = l2_policy_evict_last();
-    uint32_t kv_cnt = 0, local = 0;
-    bool ok = true, q_issued = false;
-    uint32_t next = 0;
+    uint32_t kv_cnt = 0, local = 0, q_par = 0;
+    bool ok = true, q_any = false;
+    const int n_items = PACKED ? p.Hq * *p.n_units : p.n_items;
     for (uint32_t k = 0; ok; ++k, ++local) {
-      const int w =
-          dynamic ? sched_produce(k, p.work_ctr, p.n_items, sched_full, sched_empty, sched,
-                                  abort_flag, &g_prefill_err, leader)
-                  : next_stride(&next);
+      const int w = sched_produce(k, p.work_ctr, n_items, sched_full, sched_empty, sched,
+                                  abort_flag, &g_prefill_err, leader);
       if (w < 0) {
         ok = w == -1;
         break;
       }
       int b, hq, qb;
-      prefill_item(w, p.B, p.Hq, p.Hkv, p.n_qb, &b, &hq, &qb);
+      const SeqSpan sq = work_item<PACKED>(p, w, &b, &hq, &qb);
       const int hkv = hq / p.G;
-      const SeqSpan sq = seq_span<PACKED>(p, b, nullptr);
       const int row0 = qb * pf::QBLOCK;
       const int n0 = kv_tiles_for(row0, sq.Sq, sq.Sk, p.causal);
       const int n1 = kv_tiles_for(row0 + pf::BM, sq.Sq, sq.Sk, p.causal);
       const int n = n0 > n1 ? n0 : n1;
-      q_issued = false;
       if (local > 0 && !(ok = mbar_wait(q_empty, (local - 1) & 1, abort_flag, &g_prefill_err, 1)))
         break;
       if (leader) {
@@ -316,7 +418,8 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
                              hq, sq.q0 + row0 + i * pf::BM, sq.tb, pol_q);
       }
       __syncwarp();
-      q_issued = true;
+      q_par = local & 1;  // (Q of earlier items has landed: q_empty was waited for)
+      q_any = true;
       // Ring order K_0, V_0, K_1, V_1, ...  V_j and K_{j+1} are consumed
       // together (P V_j, then S of step j + 1), so V_j completes on K_{j+1}'s
       // barrier, armed for both tiles, and V_j's own barrier gets a plain
@@ -369,12 +472,10 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
         }
       }
     }
-    if (!ok) {
-      // Aborted: wait (bounded) for the loads already in flight before exiting.
-      const uint32_t first = kv_cnt > (uint32_t)NSTAGE ? kv_cnt - NSTAGE : 0u;
-      for (uint32_t u = first; u < kv_cnt; ++u)
-        mbar_wait_drain(&full[u % NSTAGE], (u / NSTAGE) & 1);
-      if (q_issued) mbar_wait_drain(q_full, local & 1);
+    if (leader) {
+      prod_info[0] = kv_cnt;
+      prod_info[1] = q_par;
+      prod_info[2] = q_any ? 1u : 0u;
     }
     __syncwarp();
   } else if (warp == 9) {
@@ -383,7 +484,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
     constexpr uint32_t IDESC_O = idesc_f16(pf::BM, D, kBF16, true);
     const uint32_t sq_addr = smem_u32(sQ);
     const uint32_t skv_addr = smem_u32(sKV);
-    uint32_t kv_cnt = 0, local = 0, p_cnt0 = 0, p_cnt1 = 0, next = 0;
+    uint32_t kv_cnt = 0, local = 0, p_cnt0 = 0, p_cnt1 = 0;
     bool ok = true;
 
     // Descriptors advance by adding (byte offset >> 4) to the base descriptor:
@@ -432,15 +533,13 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
     };
     for (uint32_t it = 0; ok; ++it, ++local) {
       const int w =
-          dynamic ? sched_consume(it, sched_full, sched_empty, sched, abort_flag, &g_prefill_err, 15)
-                  : next_stride(&next);
+          sched_consume(it, sched_full, sched_empty, sched, abort_flag, &g_prefill_err, 15);
       if (w < 0) {
         ok = w == -1;
         break;
       }
       int b, hq, qb;
-      prefill_item(w, p.B, p.Hq, p.Hkv, p.n_qb, &b, &hq, &qb);
-      const SeqSpan sq = seq_span<PACKED>(p, b, nullptr);
+      const SeqSpan sq = work_item<PACKED>(p, w, &b, &hq, &qb);
       const int row0 = qb * pf::QBLOCK;
       const int nt0 = kv_tiles_for(row0, sq.Sq, sq.Sk, p.causal);
       const int nt1 = kv_tiles_for(row0 + pf::BM, sq.Sq, sq.Sk, p.causal);
@@ -526,22 +625,19 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
     const uint32_t tO = t_lane + (i ? C::COL_O1 : C::COL_O0);
     const float c = p.c;
     const bool neg_scale = c < 0.f;
-    uint32_t s_cnt = 0, o_cnt = 0, next = 0;
+    uint32_t s_cnt = 0, o_cnt = 0;
     bool ok = true;
     T* const O = static_cast<T*>(p.o);
 
     for (uint32_t it = 0; ok; ++it) {
       const int w =
-          dynamic ? sched_consume(it, sched_full, sched_empty, sched, abort_flag, &g_prefill_err, 16)
-                  : next_stride(&next);
+          sched_consume(it, sched_full, sched_empty, sched, abort_flag, &g_prefill_err, 16);
       if (w < 0) {
         ok = w == -1;
         break;
       }
       int b, hq, qb;
-      prefill_item(w, p.B, p.Hq, p.Hkv, p.n_qb, &b, &hq, &qb);
-      // (the bounds bit for bad packed offsets is set by one thread per item)
-      const SeqSpan sq = seq_span<PACKED>(p, b, (i == 0 && r == 0) ? &g_prefill_err : nullptr);
+      const SeqSpan sq = work_item<PACKED>(p, w, &b, &hq, &qb);
       const int Sq = sq.Sq, Sk = sq.Sk, off = Sk - Sq;  // bottom-right causal offset
       const int row0 = qb * pf::QBLOCK + i * pf::BM;
       const int grow = row0 + r;
@@ -666,10 +762,12 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
           }
           const float lt = (la.x + la.y) + (lb.x + lb.y);
           const bool resc = !(lt <= PBIG) || (m_used == NEG_INF && lim > 0);
-          if (__any_sync(0xffffffffu, resc)) {
+          const uint32_t resc_rows = __ballot_sync(0xffffffffu, resc);
+          if (resc_rows) {
             // Rare: rescale l and O by 2^(m_used - m_new) for those rows and
             // rewrite this tile's P.  P_i(j-1) @ V has completed (it was
             // issued before S_i(j)); P_i(j) is not read before p_full below.
+            if (lane == 0) atomicAdd(&g_prefill_rescales, (unsigned long long)__popc(resc_rows));
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) mask_and_max(sr[q4], q4);
             float f = 1.f;
@@ -746,9 +844,21 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
+  // Aborted CTA (a wait gave up, here or in another warp, possibly after the
+  // producer issued its last loads): wait, bounded, for every load that may
+  // still be in flight before the CTA exits.  A ring load older than the last
+  // NSTAGE has landed (its slot was released before the producer reused it),
+  // and so has the Q of any item before the last.
+  if (warp == 8 && *abort_flag) {
+    const uint32_t issued = prod_info[0];
+    const uint32_t first = issued > (uint32_t)NSTAGE ? issued - NSTAGE : 0u;
+    for (uint32_t u = first; u < issued; ++u) mbar_wait_drain(&full[u % NSTAGE], (u / NSTAGE) & 1);
+    if (prod_info[2]) mbar_wait_drain(q_full, prod_info[1]);
+    __syncwarp();
+  }
   // Every CTA has made its last claim once it gets here.  The last CTA out
   // sets the work counter back to zero for the next launch that uses it.
-  if (!PACKED && threadIdx.x == 0) {
+  if (threadIdx.x == 0) {
     __threadfence();
     if (atomicAdd(p.work_ctr + 1, 1u) == gridDim.x - 1) {
       p.work_ctr[0] = 0u;
@@ -779,10 +889,12 @@ struct PrefillShape {
   int total_q, total_k;
 };
 
+// units / n_units: the packed-sequence plan (device; null for a dense batch).
 template <int D, typename T>
 static int launch_prefill_t(const void* q, const void* k, const void* v, void* o, float* lse,
                             const PrefillShape& sh, float scale, int causal,
-                            unsigned int* work_ctr, cudaStream_t stream) {
+                            unsigned int* work_ctr, const int4* units, const int* n_units,
+                            cudaStream_t stream) {
   using C = pf::Cfg<D>;
   const bool packed = sh.cu_q != nullptr;
   CUtensorMap tq, tk, tv;
@@ -811,8 +923,8 @@ static int launch_prefill_t(const void* q, const void* k, const void* v, void* o
   PrefillParams p;
   p.o = o;
   p.lse = lse;
-  p.cu_q = sh.cu_q;
-  p.cu_k = sh.cu_k;
+  p.units = units;
+  p.n_units = n_units;
   p.total_q = sh.total_q;
   p.total_k = sh.total_k;
   p.B = sh.B;
@@ -831,6 +943,7 @@ static int launch_prefill_t(const void* q, const void* k, const void* v, void* o
   if (p.c == 0.f) p.c = 1e-30f;
   const int sms = sm_count() > 0 ? sm_count() : 148;
   const int grid = p.n_items < sms ? p.n_items : sms;
+  if (grid == 0) return cudaSuccess;  // packed: no sequence fits max_seqlen_q (bounds bit set)
   if (packed)
     prefill_kernel<D, T, true><<<grid, pf::THREADS, C::SMEM_TOTAL, stream>>>(tq, tk, tv, p);
   else
@@ -901,27 +1014,44 @@ static int launch_prefill_shape(const void* q, const void* k, const void* v, voi
                                                               nl);
     return cudaGetLastError();
   }
-  // The kernel's work counter: the stream's own slot (zero between launches),
-  // or, while the stream is being captured, stream-ordered scratch zeroed here
-  // (an allocation and a memset node of the graph).
+  // The kernel's work counter.  Dense batch: the stream's own slot (zero
+  // between launches), or, while the stream is being captured, stream-ordered
+  // scratch zeroed here (an allocation and a memset node of the graph).
+  // Packed sequences: stream-ordered scratch holding the counter, the number
+  // of planned units and the plan itself (two int4 per 256-row query block),
+  // all written by varlen_plan_kernel before the prefill starts.
+  const int n_qb = (sh.Sq + pf::QBLOCK - 1) / pf::QBLOCK;
+  const size_t plan_units = packed ? (size_t)sh.B * n_qb : 0;
   void* ctr = packed ? nullptr : work_counter_for_stream(stream);
-  const bool own = !packed && ctr == nullptr;
+  const bool own = ctr == nullptr;
   cudaError_t e = cudaSuccess;
   if (own) {
-    e = cudaMallocAsync(&ctr, 2 * sizeof(unsigned int), stream);
+    const size_t bytes = packed ? 16 + plan_units * 2 * sizeof(int4) : 2 * sizeof(unsigned int);
+    e = cudaMallocAsync(&ctr, bytes, stream);
     if (e != cudaSuccess) return e;
-    e = cudaMemsetAsync(ctr, 0, 2 * sizeof(unsigned int), stream);
+    if (!packed) e = cudaMemsetAsync(ctr, 0, 2 * sizeof(unsigned int), stream);
+  }
+  unsigned int* c = static_cast<unsigned int*>(ctr);
+  int4* units = packed ? reinterpret_cast<int4*>(static_cast<uint8_t*>(ctr) + 16) : nullptr;
+  int* n_units = packed ? reinterpret_cast<int*>(c + 2) : nullptr;
+  if (e == cudaSuccess && packed) {
+    varlen_plan_kernel<<<1, kPlanThreads, 0, stream>>>(sh.cu_q, sh.cu_k, sh.B, sh.total_q,
+                                                       sh.total_k, n_qb, causal, units, n_units,
+                                                       c);
+    e = cudaGetLastError();
   }
   int r = e;
   if (e == cudaSuccess) {
-    unsigned int* c = static_cast<unsigned int*>(ctr);  // null: fixed grid stride
     if (D == 64)
-      r = bf16 ? launch_prefill_t<64, __nv_bfloat16>(q, k, v, o, lse, sh, scale, causal, c, stream)
-               : launch_prefill_t<64, __half>(q, k, v, o, lse, sh, scale, causal, c, stream);
+      r = bf16 ? launch_prefill_t<64, __nv_bfloat16>(q, k, v, o, lse, sh, scale, causal, c, units,
+                                                     n_units, stream)
+               : launch_prefill_t<64, __half>(q, k, v, o, lse, sh, scale, causal, c, units,
+                                              n_units, stream);
     else
       r = bf16 ? launch_prefill_t<128, __nv_bfloat16>(q, k, v, o, lse, sh, scale, causal, c,
-                                                      stream)
-               : launch_prefill_t<128, __half>(q, k, v, o, lse, sh, scale, causal, c, stream);
+                                                      units, n_units, stream)
+               : launch_prefill_t<128, __half>(q, k, v, o, lse, sh, scale, causal, c, units,
+                                               n_units, stream);
   }
   const cudaError_t ef = own ? cudaFreeAsync(ctr, stream) : cudaSuccess;
   return r != 0 ? r : (int)ef;
@@ -941,6 +1071,21 @@ int launch_prefill_varlen(const void* q, const void* k, const void* v, void* o, 
   const PrefillShape sh{B, Hq, Hkv, max_seqlen_q, 0, cu_q, cu_k, total_q, total_k};
   return launch_prefill_shape(q, k, v, o, lse, sh, D, scale, causal, bf16, stream);
 }
+
+int read_prefill_rescales(unsigned long long* out, int reset) {
+  unsigned long long v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_prefill_rescales, sizeof(v));
+  if (e != cudaSuccess) return e;
+  if (reset && v) {
+    const unsigned long long z = 0;
+    e = cudaMemcpyToSymbol(g_prefill_rescales, &z, sizeof(z));
+    if (e != cudaSuccess) return e;
+  }
+  *out = v;
+  return cudaSuccess;
+}
+
+int set_prefill_wait_limit(unsigned long long ns) { return set_wait_limit_this_unit(ns); }
 
 int read_prefill_error(unsigned int* out, int reset) {
   unsigned int v = 0;

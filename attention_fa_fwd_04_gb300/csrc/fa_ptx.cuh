@@ -14,7 +14,26 @@ namespace fa {
 // ---------------------------------------------------------------------------
 constexpr unsigned int kErrTimeout = 1u;
 constexpr unsigned int kErrBounds = 2u;  // a global store index failed its self-check
-constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;  // 2 s per wait
+constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;  // default: 2 s per wait
+
+// Time limit of a pipeline wait (mbar_wait), per device and per translation
+// unit that includes this header (each kernel file has its own copy, set
+// through that file's setter; volatile, so the device code always reads the
+// value the host wrote).  Teardown waits (mbar_wait_drain) keep the fixed
+// kWaitTimeoutNs, so that loads already in flight always land before a CTA
+// exits, whatever this limit is.  A limit below kWatchdogNs turns a wait into
+// a non-suspending poll that checks the clock at every probe.
+constexpr unsigned long long kWatchdogNs = 1000000ull;  // 1 ms
+static __device__ volatile unsigned long long g_wait_limit_ns = kWaitTimeoutNs;
+
+// Host side: set this translation unit's copy on the current device
+// (0 restores the default).  Synchronous.  Returns a cudaError_t.
+static inline int set_wait_limit_this_unit(unsigned long long ns) {
+  const unsigned long long v = ns ? ns : kWaitTimeoutNs;
+  return (int)cudaMemcpyToSymbol(
+      reinterpret_cast<const void*>(const_cast<unsigned long long*>(&g_wait_limit_ns)), &v,
+      sizeof(v));
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -51,6 +70,21 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// Non-blocking test of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar_addr, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar_addr), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Test of the phase that may suspend the thread for a short, system-defined
+// time while the phase is incomplete.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -64,19 +98,35 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity
 }
 
 // Wait for the completion of the phase with the given parity.  Gives up after
-// kWaitTimeoutNs (or as soon as another warp of the CTA gave up), records the
+// g_wait_limit_ns (or as soon as another warp of the CTA gave up), records the
 // failure in *err_word and the CTA-wide abort flag, and returns false.
+// A phase already complete costs one non-blocking test.  Otherwise the wait
+// suspends in try_wait and looks at the clock every 64 probes; under a
+// watchdog limit (below kWatchdogNs) it polls without suspending and looks at
+// the clock and the abort flag at every probe.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
                                           volatile int* abort_flag, unsigned int* err_word,
                                           unsigned int site) {
   const uint32_t a = smem_u32(bar);
-  if (mbar_try_wait(a, parity)) return true;
+  if (mbar_test_wait(a, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
+  const uint64_t limit = g_wait_limit_ns;
+  if (limit < kWatchdogNs) {
+    for (;;) {
+      if (mbar_test_wait(a, parity)) return true;
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > limit) {
+        *abort_flag = 1;
+        atomicOr(err_word, kErrTimeout | (site << 8));
+        return false;
+      }
+    }
+  }
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(a, parity)) return true;
     if ((it & 63u) == 0) {
       if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+      if (globaltimer_ns() - t0 > limit) {
         *abort_flag = 1;
         atomicOr(err_word, kErrTimeout | (site << 8));
         return false;

@@ -496,19 +496,21 @@ def run_backward(args, fa, torch, dev, q, k, v, sh, stream):
 
 
 def run_e2e(args, fa, torch, dev, q_h, k_h, v_h, sh, stream, dist):
-    """Prefill from pinned HOST buffers to a pinned host O through the
-    library's host pipeline (HostPrefill): the upload of q, k, v and the
-    download of O are inside the timed region every step, overlapped with the
-    per-piece fa_prefill_fwd kernels."""
-    from attention_fa_fwd_04_gb300.host_pipeline import HostPrefill
+    """Prefill from pinned HOST buffers to a pinned host O through the C ABI's
+    fa_prefill_fwd_host: the upload of q, k, v and the download of O are
+    inside the timed region every step, overlapped with the per-piece prefill
+    kernels (E2E_CHUNKS query-row pieces)."""
     qp, kp, vp = q_h.pin_memory(), k_h.pin_memory(), v_h.pin_memory()
     op = torch.empty(q_h.shape, dtype=q_h.dtype).pin_memory()
-    hp = HostPrefill(PREFILL.B, PREFILL.Hq, PREFILL.Hkv, PREFILL.Sq, PREFILL.Sk, PREFILL.D,
-                     q_h.dtype, True, n_chunks=E2E_CHUNKS, device=dev)
     n = max(3, min(args.steps, 20))
+    P = PREFILL
 
     def step():
-        hp(qp, kp, vp, op, PREFILL.scale, stream=stream)
+        st = fa.fa_prefill_fwd_host(qp.data_ptr(), kp.data_ptr(), vp.data_ptr(), op.data_ptr(),
+                                    P.B, P.Hq, P.Hkv, P.Sq, P.Sk, P.D, P.scale, 1, fa.FA_BF16,
+                                    E2E_CHUNKS, sh)
+        if st:
+            raise fa.FAError(st, "fa_prefill_fwd_host")
 
     for _ in range(3):
         step()
@@ -525,11 +527,13 @@ def run_e2e(args, fa, torch, dev, q_h, k_h, v_h, sh, stream, dist):
     t = max_over_ranks([t], dist, dev)[0]
     world = dist.get_world_size() if dist else 1
     h2d = (q_h.numel() + k_h.numel() + v_h.numel()) * 2
-    return {"value": round(world * PREFILL.flops * n / t / 1e12, 2), "unit": "TFLOP/s",
+    pieces = fa.fa_prefill_host_pieces(P.B, P.Sq, P.Sk, 1, E2E_CHUNKS)
+    return {"value": round(world * P.flops * n / t / 1e12, 2), "unit": "TFLOP/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": q_h.numel() * 2, "steps": n,
-            "note": f"pinned host q,k,v -> device -> pinned host O per step through "
-                    f"HostPrefill: K/V first, then {len(hp.pieces)} row pieces whose "
-                    f"uploads, fa_prefill_fwd kernels and downloads overlap"}
+            "call": "fa_prefill_fwd_host (C ABI), pinned host buffers",
+            "note": f"pinned host q,k,v -> device -> pinned host O per step in one C call: "
+                    f"K/V first, then {len(pieces)} query-row pieces whose uploads, prefill "
+                    f"kernels and downloads overlap on two copy streams and a compute stream"}
 
 
 # ----------------------------------------------------------------------------

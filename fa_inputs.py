@@ -83,6 +83,41 @@ def prefill_inputs_for(shape: PrefillShape, seed=0):
                           shape.dtype, seed)
 
 
+def tile_gain_inputs(B, Hq, Hkv, Sq, Sk, D, dtype, gains, seed=0, tile=128):
+    """prefill_inputs with the keys of key tile t (rows [t*tile, (t+1)*tile)
+    of k) multiplied by gains[t] before rounding to dtype (tiles past the list
+    keep gain 1; q and v are unchanged).
+
+    A row's scores against tile t then spread gains[t] times wider, so a row
+    that has seen only ordinary scores meets, in a later tile, scores larger
+    by tens of units: the running max of an online softmax jumps there.  The
+    draw order and the unscaled values are those of prefill_inputs."""
+    g = torch.Generator().manual_seed(seed)
+    q = _randn(g, (B, Sq, Hq, D), dtype)
+    k32 = torch.randn(B, Sk, Hkv, D, generator=g, dtype=torch.float32)
+    v = _randn(g, (B, Sk, Hkv, D), dtype)
+    for t, gain in enumerate(gains):
+        k32[:, t * tile:(t + 1) * tile] *= float(gain)
+    return q, k32.to(dtype), v
+
+
+def first_tile_overflow_inputs(B, Hq, Hkv, Sq, Sk, D, seed=0, tile=128):
+    """bf16 inputs whose scores against key tile 0 are -2^112 * D in raw
+    units for every row, while every later key scores of order 2^-14 * sqrt(D).
+
+    q is 1 everywhere; the keys of tile 0 are -2^112 in every element (both
+    exact in bf16); later keys are 2^-14 * N(0, 1); v is N(0, 1).  With a
+    softmax scale near 2^12 / log2(e), the first tile's scaled scores leave
+    the fp32 range (below -2^128) although the raw scores fit it, and the
+    later tiles' scaled scores are of order one."""
+    g = torch.Generator().manual_seed(seed)
+    q = torch.ones(B, Sq, Hq, D, dtype=torch.float32).to(torch.bfloat16)
+    k32 = torch.randn(B, Sk, Hkv, D, generator=g, dtype=torch.float32) * 2.0 ** -14
+    k32[:, :tile] = -(2.0 ** 112)
+    v = _randn(g, (B, Sk, Hkv, D), torch.bfloat16)
+    return q, k32.to(torch.bfloat16), v
+
+
 def draw_valid_length(cap: int, seed=0) -> int:
     """The seeded valid length in [1, cap] (the first draw of the decode recipe)."""
     g = torch.Generator().manual_seed(seed)

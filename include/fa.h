@@ -122,13 +122,21 @@ int fa_prefill_fwd_lse(const void* q, const void* k, const void* v, void* o, flo
  *   cu_seqlens_q   [B + 1] int32 in device memory: sequence b's query rows are
  *   cu_seqlens_k   [cu_seqlens_q[b], cu_seqlens_q[b+1]), its keys likewise.
  *                  Read by the kernel only.
- *   max_seqlen_q   >= every query length (sizes the persistent schedule)
+ *   max_seqlen_q   >= every query length (bounds the work plan)
  *   lse            NULL, or [Hq, total_q] fp32 written with each row's
  *                  log-sum-exp (-inf for a row with no visible key)
  *
  * Causal masking is bottom-right per sequence: row i of sequence b sees keys
  * j <= i + (Sk_b - Sq_b).  Keys of the neighbouring packed sequence that share
- * a tile are masked like keys past Sk.  Offsets that are not
+ * a tile are masked like keys past Sk.
+ *
+ * Scheduling: a one-CTA planning kernel reads the offsets on the device and
+ * lists each sequence's 256-row query blocks, largest K/V tile count first;
+ * the persistent prefill CTAs then claim (block, query head) items from that
+ * list as they become free, so short and long sequences of a batch share the
+ * grid instead of serialising.  The plan and the work counter live in
+ * stream-ordered scratch (B * ceil(max_seqlen_q / 256) * 32 + 16 bytes).
+ * Offsets that are not
  * 0 <= cu[b] <= cu[b+1] <= total, or a query length above max_seqlen_q, make
  * that sequence's rows unwritten and set the bounds bit reported by
  * fa_device_error().  Other rules as fa_prefill_fwd.
@@ -274,6 +282,51 @@ int fa_backward(const void* q, const void* k, const void* v, const void* o,
                 int B, int Hq, int Hkv, int Sq, int Sk, int D, float scale, int causal,
                 int dtype, cudaStream_t stream);
 
+/*
+ * fa_prefill_fwd_host -- fa_prefill_fwd from host memory to host memory, with
+ * the copies overlapped with the kernels.
+ *
+ *   q_host, o_host  [B, Sq, Hq, D]   in host memory (read / written)
+ *   k_host, v_host  [B, Sk, Hkv, D]  in host memory (read)
+ *   n_pieces        >= 1: query-row pieces per sequence (16 suits long
+ *                   sequences; 1 = copies and kernel one after the other)
+ *   other arguments as fa_prefill_fwd.
+ *
+ * Host buffers should be page-locked (cudaHostAlloc / cudaHostRegister):
+ * with pageable memory the result is the same but the copies do not overlap.
+ * The query rows of each sequence are split into at most n_pieces pieces on
+ * 256-row boundaries; rows [s0, s1) see the key prefix [0, sk), sk = Sk, or
+ * with causal masking min(Sk, max(0, s1 + Sk - Sq)), and form an ordinary
+ * bottom-right aligned prefill of s1 - s0 rows over sk keys -- the same rows
+ * and keys as in the whole problem, so O is bit-identical to fa_prefill_fwd's.
+ * K and V are uploaded first, then Q piece by piece (heaviest piece first);
+ * each piece's kernel runs as soon as its rows have landed and its O rows go
+ * back while later pieces compute.
+ *
+ * Device copies of q, k, v, o are allocated stream-ordered on `stream`
+ * (2 * B * (Sq * Hq + Sk * Hkv) * D * 2 bytes, freed on `stream` after the
+ * last download).  Two copy streams and a compute stream per device, created
+ * on first use and kept, fork from `stream` and join it again: work already on
+ * `stream` runs first, and `stream` waits for the last download, so o_host is
+ * complete once `stream` reaches that point (the call itself does not
+ * synchronise).  Calls on one device are enqueued one at a time.
+ *
+ * Returns FA_OK, FA_ERR_INVALID_ARG (as fa_prefill_fwd, null host pointer,
+ * n_pieces < 1) or FA_ERR_CUDA.
+ */
+int fa_prefill_fwd_host(const void* q_host, const void* k_host, const void* v_host,
+                        void* o_host, int B, int Hq, int Hkv, int Sq, int Sk, int D,
+                        float scale, int causal, int dtype, int n_pieces, cudaStream_t stream);
+
+/*
+ * fa_prefill_host_pieces -- the piece plan of fa_prefill_fwd_host, for
+ * inspection and tests: fills b, s0, s1, sk (each may be NULL) for the first
+ * min(count, max_pieces) pieces in the order they are uploaded, and returns
+ * count, or -1 on bad arguments.  No GPU access.
+ */
+int fa_prefill_host_pieces(int B, int Sq, int Sk, int causal, int n_pieces,
+                           int* b, int* s0, int* s1, int* sk, int max_pieces);
+
 /* Static, human-readable name of a status code (never NULL). */
 const char* fa_status_string(int status);
 
@@ -302,6 +355,46 @@ int fa_last_cuda_error(const char** site);
 int fa_num_sms(void);
 
 /*
+ * fa_prefill_rescale_count -- how often the prefill softmax took its lazy
+ * rescale on the current device since the last reset: the number of
+ * (query row, K/V tile) steps at which O and the row sum were rescaled to a
+ * new running max and the tile's P recomputed.
+ *
+ * The lazy rescale is the "lazy" lever of "Dense flash-attention prefill
+ * (gfx950 / MI355X)", *Measured*: the softmax exponentiates each K/V tile
+ * against the row's running max without first taking the tile's own max, and
+ * only when the tile's row sum of P exceeds 2^60 (bf16 P) or 2^15 (fp16 P),
+ * or the row had no finite score before, does it find the new max, rescale
+ * and recompute.  Scores of ordinary inputs never trigger it; a count that
+ * grows on a workload says its scores jump by tens of units within rows.
+ *
+ *   reset  nonzero: clear the counter after reading it
+ *   count  receives the value (non-NULL)
+ *
+ * Synchronises the current device.  Returns FA_OK, FA_ERR_INVALID_ARG
+ * (count == NULL) or FA_ERR_CUDA.
+ */
+int fa_prefill_rescale_count(int reset, unsigned long long* count);
+
+/*
+ * fa_set_wait_limit_ns -- time limit of every device-side pipeline wait
+ * (mbarrier waits of the prefill, decode and backward kernels) on the current
+ * device; ns == 0 restores the default of 2 s.
+ *
+ * A wait that runs past the limit makes its CTA abort: every warp leaves its
+ * loop, the loads and MMAs already in flight are waited for (each such
+ * teardown wait keeps the fixed 2 s limit), tensor memory is freed, and the
+ * timeout bit plus the wait's site are set in the error word read by
+ * fa_device_error().  The outputs of an aborted call are undefined.  The
+ * default is far above any wait of a healthy call; a short limit serves as a
+ * watchdog, or in tests to make the timeout path run.
+ *
+ * Synchronises the current device and applies to calls enqueued afterwards.
+ * Returns FA_OK or FA_ERR_CUDA.
+ */
+int fa_set_wait_limit_ns(unsigned long long ns);
+
+/*
  * fa_prefill_work_item -- host copy of the persistent scheduler's work-item
  * decode, for inspection and tests.  Work item w in [0, n_items) maps to
  * (b, hq, qblock); a qblock is 256 query rows.  Returns the number of items
@@ -310,8 +403,8 @@ int fa_num_sms(void);
  *
  * Items are numbered kv-head-major, longest causal query blocks first.  In a
  * dense launch the persistent CTAs claim items in that order from a work
- * counter (the next free CTA takes the next item); packed sequences
- * (fa_prefill_varlen_fwd) take them by a fixed grid stride.
+ * counter (the next free CTA takes the next item).  (Packed sequences,
+ * fa_prefill_varlen_fwd, claim from a list planned on the device instead.)
  */
 int fa_prefill_work_item(int w, int B, int Hq, int Hkv, int Sq, int Sk, int causal,
                          int* b, int* hq, int* qblock);

@@ -26,34 +26,35 @@ from . import build as _build
 _lib = None
 
 
+def _bind(path):
+    """Load the compiled oracle at ``path`` and declare its C signatures."""
+    lib = ctypes.CDLL(path)
+    dp = ctypes.POINTER(ctypes.c_double)
+    lp = ctypes.POINTER(ctypes.c_int64)
+    i64, i32, f64 = ctypes.c_int64, ctypes.c_int, ctypes.c_double
+    lib.oracle_attention_rows.argtypes = [dp, dp, dp, dp, lp, i64, i32, i32,
+                                          i32, i64, i64, i32, f64, i32, i32]
+    lib.oracle_attention_rows.restype = i32
+    lib.oracle_attention_rows_lse.argtypes = [dp, dp, dp, dp, dp, lp, i64, i32, i32,
+                                              i32, i64, i64, i32, f64, i32, i32]
+    lib.oracle_attention_rows_lse.restype = i32
+    lib.oracle_attention_probs.argtypes = [dp, dp, dp, dp, dp, i32, i32, i64,
+                                           i32, i32, i32, i64, i64, i32, f64, i32]
+    lib.oracle_attention_probs.restype = i32
+    lib.oracle_decode.argtypes = [dp, dp, dp, dp, i32, i32, i32, i64, i32, i64, f64]
+    lib.oracle_decode.restype = i32
+    lib.oracle_decode_lse.argtypes = [dp, dp, dp, dp, dp, i32, i32, i32, i64, i32, i64, f64]
+    lib.oracle_decode_lse.restype = i32
+    lib.oracle_attention_bwd.argtypes = [dp, dp, dp, dp, dp, dp, dp, i32, i32, i32, i64,
+                                         i64, i32, f64, i32, i32]
+    lib.oracle_attention_bwd.restype = i32
+    return lib
+
+
 def _load():
     global _lib
     if _lib is None:
-        # A planted-mistake copy of the oracle, compiled by the mutation test
-        # (tests/test_oracle_mutants.py), is loaded through this variable so that
-        # the pins can be shown to catch it.
-        path = os.environ.get("FA_ORACLE_LIB_OVERRIDE") or _build.build()
-        lib = ctypes.CDLL(path)
-        dp = ctypes.POINTER(ctypes.c_double)
-        lp = ctypes.POINTER(ctypes.c_int64)
-        i64, i32, f64 = ctypes.c_int64, ctypes.c_int, ctypes.c_double
-        lib.oracle_attention_rows.argtypes = [dp, dp, dp, dp, lp, i64, i32, i32,
-                                              i32, i64, i64, i32, f64, i32, i32]
-        lib.oracle_attention_rows.restype = i32
-        lib.oracle_attention_rows_lse.argtypes = [dp, dp, dp, dp, dp, lp, i64, i32, i32,
-                                                  i32, i64, i64, i32, f64, i32, i32]
-        lib.oracle_attention_rows_lse.restype = i32
-        lib.oracle_attention_probs.argtypes = [dp, dp, dp, dp, dp, i32, i32, i64,
-                                               i32, i32, i32, i64, i64, i32, f64, i32]
-        lib.oracle_attention_probs.restype = i32
-        lib.oracle_decode.argtypes = [dp, dp, dp, dp, i32, i32, i32, i64, i32, i64, f64]
-        lib.oracle_decode.restype = i32
-        lib.oracle_decode_lse.argtypes = [dp, dp, dp, dp, dp, i32, i32, i32, i64, i32, i64, f64]
-        lib.oracle_decode_lse.restype = i32
-        lib.oracle_attention_bwd.argtypes = [dp, dp, dp, dp, dp, dp, dp, i32, i32, i32, i64,
-                                             i64, i32, f64, i32, i32]
-        lib.oracle_attention_bwd.restype = i32
-        _lib = lib
+        _lib = _bind(_build.build())
     return _lib
 
 

@@ -104,3 +104,8 @@ def test_lse_variants_reject_missing_or_misaligned_lse(lib):
                                 0) == fa.FA_ERR_INVALID_ARG
     assert fa.fa_prefill_fwd_lse(0, 0, 0, 0, 0, 0, 4, 2, 16, 16, 64, 0.1, 1, fa.FA_BF16,
                                  0) == fa.FA_OK
+
+
+def test_rescale_count_rejects_a_null_output(lib):
+    import attention_fa_fwd_04_gb300 as fa
+    assert lib.fa_prefill_rescale_count(0, None) == fa.FA_ERR_INVALID_ARG

@@ -97,8 +97,15 @@ def _build_and_run(tmpdir, name, old, new):
         f.write(src)
     subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
                            "-w", "-o", so_path, c_path, "-lm"])
-    env = dict(os.environ, FA_ORACLE_LIB_OVERRIDE=so_path, OMP_NUM_THREADS="1")
-    r = subprocess.run([sys.executable] + PIN_ARGS, cwd=ROOT, env=env,
+    # A pytest plugin, imported before the pins are collected, binds the oracle
+    # package to this copy of the library (the oracle itself has no switch).
+    plugin = f"mutant_plugin_{name}"
+    with open(os.path.join(tmpdir, plugin + ".py"), "w") as f:
+        f.write("import oracle\n"
+                f"oracle._lib = oracle._bind({so_path!r})\n")
+    path = os.pathsep.join([tmpdir, ROOT] + [p for p in [os.environ.get("PYTHONPATH")] if p])
+    env = dict(os.environ, PYTHONPATH=path, OMP_NUM_THREADS="1")
+    r = subprocess.run([sys.executable] + PIN_ARGS + ["-p", plugin], cwd=ROOT, env=env,
                        capture_output=True, text=True, timeout=600)
     return r.returncode, r.stdout[-2000:]
 

@@ -1,0 +1,59 @@
+"""Failure detection on the device without a fault: a pipeline wait that runs
+past its time limit makes the kernel abort and report, and the context stays
+usable.
+
+fa_set_wait_limit_ns(1) makes every mbarrier wait that is not satisfied at
+once give up: the CTA leaves its loops, waits (with the fixed 2 s teardown
+limit) for the loads and MMAs already in flight, frees its tensor memory and
+sets the timeout bit and the wait's site in the error word.  Nothing waits
+without a bound, and no kernel is altered for the test.  The test checks that
+a prefill and a 65536-token decode report FA_ERR_TIMEOUT with a site, then
+restores the default limit and checks that the next calls match the oracle.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import fa_inputs
+import oracle
+from tests.parity import compare
+
+pytestmark = pytest.mark.gpu
+
+
+def test_wait_limit_aborts_report_timeout_and_the_next_calls_are_correct(fa):
+    dev = torch.device("cuda", 0)
+    B, Hq, Hkv, S, D = 1, 8, 2, 1024, 128
+    scale = 1 / math.sqrt(D)
+    q, k, v = fa_inputs.prefill_inputs(B, Hq, Hkv, S, S, D, torch.bfloat16, seed=5)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    sd = fa_inputs.DECODE_1TOK
+    dq, kc, vc, L = fa_inputs.decode_inputs_for(sd, seed=5, L=sd.cap)
+    dqd, kcd, vcd = dq.to(dev), kc.to(dev), vc.to(dev)
+    vl = torch.tensor([L], dtype=torch.int32, device=dev)
+    assert fa.fa_device_error(reset=1)[0] == fa.FA_OK
+
+    try:
+        assert fa.fa_set_wait_limit_ns(1) == fa.FA_OK
+        fa.prefill(qd, kd, vd, scale, True)
+        st, detail = fa.fa_device_error(reset=1)
+        assert st == fa.FA_ERR_TIMEOUT, (st, hex(detail))
+        assert detail & 1 and (detail >> 8) & 0xFF, hex(detail)  # prefill word: bit 0 + site
+        fa.decode(dqd, kcd, vcd, vl, sd.scale)
+        st, detail = fa.fa_device_error(reset=1)
+        assert st == fa.FA_ERR_TIMEOUT, (st, hex(detail))
+        assert (detail >> 16) & 1 and (detail >> 24) & 0xFF, hex(detail)  # decode word
+    finally:
+        assert fa.fa_set_wait_limit_ns(0) == fa.FA_OK
+
+    out = fa.prefill(qd, kd, vd, scale, True)
+    od = fa.decode(dqd, kcd, vcd, vl, sd.scale)
+    torch.cuda.synchronize()
+    st, detail = fa.fa_device_error(reset=1)
+    assert st == fa.FA_OK, hex(detail)
+    compare(out.float().cpu().numpy(), oracle.attention(q, k, v, scale, True))
+    got = od.float().cpu().numpy().reshape(sd.B, sd.Hq, sd.D)
+    compare(got, oracle.decode(dq, kc, vc, L, sd.scale))
+    assert np.isfinite(got).all()

@@ -1,9 +1,16 @@
 """fa_decode_fwd_noalloc: the decode entry point for callers that cannot
-allocate device memory while they run (memory reserved once at start-up,
-allocator locks held, runtimes that forbid allocation after initialisation).
-Its split partials live in a fixed array inside the library instead of memory
-from cudaMallocAsync.  Its output must match fa_decode_fwd's on the same inputs,
-over two calls in a row that share that array.
+allocate device memory while they run -- a serving loop whose memory is
+reserved once at start-up, code that runs while an allocator lock is held, a
+runtime that forbids allocation after initialisation.  Its split partials live
+in one fixed array inside the library instead of memory from cudaMallocAsync,
+and every call on the device shares that array.
+
+The test makes two calls in a row: first a long request (L = 50001), then the
+seeded short one (L = 2733) with the same shape, so the short call's splits
+sit on the partials the long call left behind.  Each output must be
+bit-identical to fa_decode_fwd's on the same inputs (both run the same
+kernels with the same split count) and match the fp64 oracle; the caches'
+unused capacity holds NaN.
 
 This file sorts last so that a run stopping at the first failure has already
 run every other test."""
@@ -11,6 +18,7 @@ import pytest
 import torch
 
 import fa_inputs
+import oracle
 from tests.parity import compare
 
 pytestmark = pytest.mark.gpu
@@ -28,14 +36,14 @@ def _call(entry, t, shape, out, stream):
                  shape.B, shape.Hq, shape.Hkv, shape.cap, shape.D, shape.scale, stream)
 
 
-def test_noalloc_decode_matches_allocating_decode_on_two_calls_in_a_row(fa):
+def test_noalloc_decode_on_two_calls_in_a_row_matches_decode_and_oracle(fa):
     dev = torch.device("cuda", 0)
     shape = fa_inputs.DECODE_1TOK
     stream = torch.cuda.current_stream(dev).cuda_stream
-    # Two different requests: the seeded valid length and a longer one, so a
-    # call reading the previous call's partials would show.
-    runs = [_upload(fa_inputs.decode_inputs_for(shape, seed=0), dev),
-            _upload(fa_inputs.decode_inputs_for(shape, seed=7, L=50001), dev)]
+    host = [fa_inputs.decode_inputs_for(shape, seed=7, L=50001),   # long request first
+            fa_inputs.decode_inputs_for(shape, seed=0)]            # then the seeded L
+    assert host[1][3] < host[0][3]
+    runs = [_upload(h, dev) for h in host]
     refs = [torch.empty_like(r[0]) for r in runs]
     outs = [torch.empty_like(r[0]) for r in runs]
     for t, ref in zip(runs, refs):
@@ -45,8 +53,10 @@ def test_noalloc_decode_matches_allocating_decode_on_two_calls_in_a_row(fa):
         assert _call(fa.fa_decode_fwd_noalloc, t, shape, out, stream) == fa.FA_OK
     torch.cuda.synchronize()
     assert fa.fa_device_error()[0] == fa.FA_OK
-    for out, ref in zip(outs, refs):
-        compare(out.float().cpu().numpy(), ref.float().cpu().numpy())
+    for (q, kc, vc, L), out, ref in zip(host, outs, refs):
+        assert torch.equal(out, ref)
+        got = out.float().cpu().numpy().reshape(shape.B, shape.Hq, shape.D)
+        compare(got, oracle.decode(q, kc, vc, L, shape.scale))
 
 
 def test_noalloc_decode_rejects_requests_larger_than_its_scratch(fa):
