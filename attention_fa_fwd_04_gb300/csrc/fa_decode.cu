@@ -226,7 +226,7 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
         row = tok - page * p.page_size;
         tb = bad ? 0 : pid;  // a bad id loads page 0, and the tile is masked
       }
-      if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, &g_decode_err, 1)) break;
+      if (!mbar_wait<true>(&empty[s], ph ^ 1, abort_flag, &g_decode_err, 1)) break;
       if (leader) {
         if constexpr (PAGED) {
           stage_bad[s] = bad;
@@ -291,7 +291,7 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
     for (int t = warp; t < n_tiles; t += NW) {
       const int s = t % NSTAGE;
       const uint32_t ph = (t / NSTAGE) & 1;
-      if (!mbar_wait(&full[s], ph, abort_flag, &g_decode_err, 2)) break;
+      if (!mbar_wait<true>(&full[s], ph, abort_flag, &g_decode_err, 2)) break;
       __syncwarp();  // ldmatrix / mma.sync below are warp-collective
       uint8_t* st = stages + s * C::STAGE_BYTES;
       const int tok0 = (t_begin + t) * TT;

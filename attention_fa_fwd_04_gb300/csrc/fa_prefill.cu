@@ -299,7 +299,10 @@ struct IsBF16<__nv_bfloat16> {
 // varlen_plan_kernel wrote; otherwise a dense batch.  Both claim items from
 // the work counter.  (Separate instantiations: the dense kernel carries none
 // of the packed-sequence code.)
-template <int D, typename T, bool PACKED>
+// POLL: the waits poll without suspending under a watchdog limit (mbar_wait);
+// the host launches this instantiation (dense batches only) while the
+// device's wait limit is below kWatchdogNs, and the lean-wait one otherwise.
+template <int D, typename T, bool PACKED, bool POLL = false>
 __global__ void __launch_bounds__(pf::THREADS, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
@@ -393,7 +396,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
     bool ok = true, q_any = false;
     const int n_items = PACKED ? p.Hq * *p.n_units : p.n_items;
     for (uint32_t k = 0; ok; ++k, ++local) {
-      const int w = sched_produce(k, p.work_ctr, n_items, sched_full, sched_empty, sched,
+      const int w = sched_produce<POLL>(k, p.work_ctr, n_items, sched_full, sched_empty, sched,
                                   abort_flag, &g_prefill_err, leader);
       if (w < 0) {
         ok = w == -1;
@@ -406,7 +409,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       const int n0 = kv_tiles_for(row0, sq.Sq, sq.Sk, p.causal);
       const int n1 = kv_tiles_for(row0 + pf::BM, sq.Sq, sq.Sk, p.causal);
       const int n = n0 > n1 ? n0 : n1;
-      if (local > 0 && !(ok = mbar_wait(q_empty, (local - 1) & 1, abort_flag, &g_prefill_err, 1)))
+      if (local > 0 && !(ok = mbar_wait<POLL>(q_empty, (local - 1) & 1, abort_flag, &g_prefill_err, 1)))
         break;
       if (leader) {
         mbar_arrive_expect_tx(q_full, 2 * C::TILE_BYTES);
@@ -426,7 +429,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       // arrival that keeps its phases in step: the MMA warp waits once per
       // K/V step.  K_0 and the last V stand alone.
       auto slot_free = [&](uint32_t cnt) {
-        return mbar_wait(&empty[cnt % NSTAGE], ((cnt / NSTAGE) & 1) ^ 1, abort_flag,
+        return mbar_wait<POLL>(&empty[cnt % NSTAGE], ((cnt / NSTAGE) & 1) ^ 1, abort_flag,
                          &g_prefill_err, 2);
       };
       auto load_tile = [&](uint32_t cnt, const CUtensorMap* m, int kv_tile, uint64_t* bar) {
@@ -529,11 +532,11 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
     // K_j / V_j of an item sit at ring positions kb + 2j / kb + 2j + 1; V_j
     // and K_{j+1} complete together on K_{j+1}'s barrier (see the producer).
     auto ring_wait = [&](uint32_t idx, unsigned int site) {
-      return mbar_wait(&full[idx % NSTAGE], (idx / NSTAGE) & 1, abort_flag, &g_prefill_err, site);
+      return mbar_wait<POLL>(&full[idx % NSTAGE], (idx / NSTAGE) & 1, abort_flag, &g_prefill_err, site);
     };
     for (uint32_t it = 0; ok; ++it, ++local) {
       const int w =
-          sched_consume(it, sched_full, sched_empty, sched, abort_flag, &g_prefill_err, 15);
+          sched_consume<POLL>(it, sched_full, sched_empty, sched, abort_flag, &g_prefill_err, 15);
       if (w < 0) {
         ok = w == -1;
         break;
@@ -544,7 +547,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       const int nt0 = kv_tiles_for(row0, sq.Sq, sq.Sk, p.causal);
       const int nt1 = kv_tiles_for(row0 + pf::BM, sq.Sq, sq.Sk, p.causal);
       const int n = nt0 > nt1 ? nt0 : nt1;
-      if (!(ok = mbar_wait(q_full, local & 1, abort_flag, &g_prefill_err, 3))) break;
+      if (!(ok = mbar_wait<POLL>(q_full, local & 1, abort_flag, &g_prefill_err, 3))) break;
       tc_fence_after();
       if (n == 0) {
         commit(q_empty);
@@ -577,7 +580,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
         const int sV = (kb + 2 * j + 1) % NSTAGE;
         const int sK = (kb + 2 * j + 2) % NSTAGE;  // K_{j+1}
         if (j < nt0) {
-          if (!(ok = mbar_wait(&p_full[0], p_cnt0 & 1, abort_flag, &g_prefill_err, 7))) break;
+          if (!(ok = mbar_wait<POLL>(&p_full[0], p_cnt0 & 1, abort_flag, &g_prefill_err, 7))) break;
           ++p_cnt0;
           tc_fence_after();
           issue_pv(0, sV, j > 0);
@@ -588,7 +591,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
           }
         }
         if (j < nt1) {
-          if (!(ok = mbar_wait(&p_full[1], p_cnt1 & 1, abort_flag, &g_prefill_err, 8))) break;
+          if (!(ok = mbar_wait<POLL>(&p_full[1], p_cnt1 & 1, abort_flag, &g_prefill_err, 8))) break;
           ++p_cnt1;
           tc_fence_after();
           issue_pv(1, sV, j > 0);
@@ -631,7 +634,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
 
     for (uint32_t it = 0; ok; ++it) {
       const int w =
-          sched_consume(it, sched_full, sched_empty, sched, abort_flag, &g_prefill_err, 16);
+          sched_consume<POLL>(it, sched_full, sched_empty, sched, abort_flag, &g_prefill_err, 16);
       if (w < 0) {
         ok = w == -1;
         break;
@@ -662,7 +665,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       float m_used = NEG_INF;  // running max in the log2 domain (scaled units)
       float l = 0.f;
       for (int j = 0; j < n_i; ++j) {
-        if (!(ok = mbar_wait(&s_full[i], s_cnt & 1, abort_flag, &g_prefill_err, 9 + i))) break;
+        if (!(ok = mbar_wait<POLL>(&s_full[i], s_cnt & 1, abort_flag, &g_prefill_err, 9 + i))) break;
         ++s_cnt;
         __syncwarp();  // tcgen05.ld below is warp-collective
         tc_fence_after();
@@ -802,7 +805,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       }
       if (!ok) break;
       // Epilogue: O / l, rounded once, 16-byte stores.
-      if (!(ok = mbar_wait(&o_full[i], o_cnt & 1, abort_flag, &g_prefill_err, 11 + i))) break;
+      if (!(ok = mbar_wait<POLL>(&o_full[i], o_cnt & 1, abort_flag, &g_prefill_err, 11 + i))) break;
       ++o_cnt;
       __syncwarp();
       tc_fence_after();
@@ -879,6 +882,17 @@ __global__ void prefill_zero_kernel(T* o, size_t n, float* lse, size_t nl) {
       lse[x] = -INFINITY;
 }
 
+// Host copy of each device's wait limit: the launch picks the POLL
+// instantiation while it is a watchdog limit.
+static unsigned long long g_host_wait_limit[64];
+
+static bool watchdog_on_current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  const unsigned long long v = __atomic_load_n(&g_host_wait_limit[dev], __ATOMIC_RELAXED);
+  return v != 0 && v < kWatchdogNs;
+}
+
 // Dense batch: cu_q == nullptr, rows = Sq / Sk per sequence.  Packed
 // sequences: cu_q / cu_k device prefix sums, Sq = longest query length,
 // rows_q / rows_k = total packed rows.
@@ -918,6 +932,9 @@ static int launch_prefill_t(const void* q, const void* k, const void* v, void* o
     e = cudaFuncSetAttribute(prefill_kernel<D, T, true>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_TOTAL);
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(prefill_kernel<D, T, false, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_TOTAL);
+    if (e != cudaSuccess) return e;
     attr_set[dev] = 1;
   }
   PrefillParams p;
@@ -946,6 +963,8 @@ static int launch_prefill_t(const void* q, const void* k, const void* v, void* o
   if (grid == 0) return cudaSuccess;  // packed: no sequence fits max_seqlen_q (bounds bit set)
   if (packed)
     prefill_kernel<D, T, true><<<grid, pf::THREADS, C::SMEM_TOTAL, stream>>>(tq, tk, tv, p);
+  else if (watchdog_on_current_device())
+    prefill_kernel<D, T, false, true><<<grid, pf::THREADS, C::SMEM_TOTAL, stream>>>(tq, tk, tv, p);
   else
     prefill_kernel<D, T, false><<<grid, pf::THREADS, C::SMEM_TOTAL, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
@@ -1085,7 +1104,13 @@ int read_prefill_rescales(unsigned long long* out, int reset) {
   return cudaSuccess;
 }
 
-int set_prefill_wait_limit(unsigned long long ns) { return set_wait_limit_this_unit(ns); }
+int set_prefill_wait_limit(unsigned long long ns) {
+  const int e = set_wait_limit_this_unit(ns);
+  int dev = 0;
+  if (e == 0 && cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < 64)
+    __atomic_store_n(&g_host_wait_limit[dev], ns, __ATOMIC_RELAXED);
+  return e;
+}
 
 int read_prefill_error(unsigned int* out, int reset) {
   unsigned int v = 0;

@@ -18,21 +18,20 @@ constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;  // default: 2 s pe
 
 // Time limit of a pipeline wait (mbar_wait), per device and per translation
 // unit that includes this header (each kernel file has its own copy, set
-// through that file's setter; volatile, so the device code always reads the
-// value the host wrote).  Teardown waits (mbar_wait_drain) keep the fixed
+// through that file's setter).  It lives in constant memory: a wait reads it
+// from the constant cache, and kernels launched after the host writes it see
+// the new value.  Teardown waits (mbar_wait_drain) keep the fixed
 // kWaitTimeoutNs, so that loads already in flight always land before a CTA
-// exits, whatever this limit is.  A limit below kWatchdogNs turns a wait into
-// a non-suspending poll that checks the clock at every probe.
+// exits, whatever this limit is.  A limit below kWatchdogNs is a watchdog: the
+// waits check the clock at every probe (see mbar_wait for when they start).
 constexpr unsigned long long kWatchdogNs = 1000000ull;  // 1 ms
-static __device__ volatile unsigned long long g_wait_limit_ns = kWaitTimeoutNs;
+static __constant__ unsigned long long g_wait_limit_ns = kWaitTimeoutNs;
 
 // Host side: set this translation unit's copy on the current device
 // (0 restores the default).  Synchronous.  Returns a cudaError_t.
 static inline int set_wait_limit_this_unit(unsigned long long ns) {
   const unsigned long long v = ns ? ns : kWaitTimeoutNs;
-  return (int)cudaMemcpyToSymbol(
-      reinterpret_cast<const void*>(const_cast<unsigned long long*>(&g_wait_limit_ns)), &v,
-      sizeof(v));
+  return (int)cudaMemcpyToSymbol(g_wait_limit_ns, &v, sizeof(v));
 }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -70,19 +69,6 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
-// Non-blocking test of the phase with the given parity.
-__device__ __forceinline__ bool mbar_test_wait(uint32_t bar_addr, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar_addr), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
 // Test of the phase that may suspend the thread for a short, system-defined
 // time while the phase is incomplete.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity) {
@@ -97,36 +83,65 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity
   return ok != 0;
 }
 
+// Non-blocking test of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar_addr, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar_addr), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for the completion of the phase with the given parity.  Gives up after
 // g_wait_limit_ns (or as soon as another warp of the CTA gave up), records the
 // failure in *err_word and the CTA-wide abort flag, and returns false.
-// A phase already complete costs one non-blocking test.  Otherwise the wait
-// suspends in try_wait and looks at the clock every 64 probes; under a
-// watchdog limit (below kWatchdogNs) it polls without suspending and looks at
-// the clock and the abort flag at every probe.
+//
+// POLL = false (prefill and backward): each probe is a try_wait, which
+// suspends the thread for a short system-defined time (about 4 us measured
+// on GB300) while the phase is incomplete; the clock and the abort flag are
+// read every 64 probes, or at every probe after the first two under a
+// watchdog limit, so a watchdog trips only waits longer than about two
+// suspends.  The code is kept this small because it is inlined at every wait
+// of the MMA-issuing warp, whose instruction stream paces those kernels:
+// larger waits (a separate polling loop, a predicated probe, a suspend-time
+// hint) measured 1-9 % slower.
+// POLL = true (decode, bandwidth-bound): the first probe does not block, and
+// under a watchdog limit every probe is a non-blocking test followed by a
+// look at the clock and the abort flag, so a watchdog trips any wait that
+// outlasts it.
+template <bool POLL = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
                                           volatile int* abort_flag, unsigned int* err_word,
                                           unsigned int site) {
   const uint32_t a = smem_u32(bar);
-  if (mbar_test_wait(a, parity)) return true;
+  if constexpr (POLL) {
+    if (mbar_test_wait(a, parity)) return true;
+  } else {
+    if (mbar_try_wait(a, parity)) return true;
+  }
   const uint64_t t0 = globaltimer_ns();
-  const uint64_t limit = g_wait_limit_ns;
-  if (limit < kWatchdogNs) {
-    for (;;) {
-      if (mbar_test_wait(a, parity)) return true;
-      if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > limit) {
-        *abort_flag = 1;
-        atomicOr(err_word, kErrTimeout | (site << 8));
-        return false;
+  if constexpr (POLL) {
+    if (g_wait_limit_ns < kWatchdogNs) {
+      for (;;) {
+        if (mbar_test_wait(a, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > g_wait_limit_ns) {
+          *abort_flag = 1;
+          atomicOr(err_word, kErrTimeout | (site << 8));
+          return false;
+        }
       }
     }
   }
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(a, parity)) return true;
-    if ((it & 63u) == 0) {
+    if ((it & 63u) == 0 || g_wait_limit_ns < kWatchdogNs) {
       if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > limit) {
+      if (globaltimer_ns() - t0 > g_wait_limit_ns) {
         *abort_flag = 1;
         atomicOr(err_word, kErrTimeout | (site << 8));
         return false;
@@ -157,12 +172,13 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) 
 // ---------------------------------------------------------------------------
 constexpr int kSchedSlots = 2;
 
+template <bool POLL = false>
 __device__ __forceinline__ int sched_produce(uint32_t k, unsigned int* ctr, int n_items,
                                              uint64_t* sfull, uint64_t* sempty,
                                              volatile int* sched, volatile int* abort_flag,
                                              unsigned int* err_word, bool leader) {
   const int slot = k % kSchedSlots;
-  if (!mbar_wait(&sempty[slot], ((k / kSchedSlots) & 1) ^ 1, abort_flag, err_word, 14))
+  if (!mbar_wait<POLL>(&sempty[slot], ((k / kSchedSlots) & 1) ^ 1, abort_flag, err_word, 14))
     return -2;
   int w = -1;
   if (leader) {
@@ -175,11 +191,12 @@ __device__ __forceinline__ int sched_produce(uint32_t k, unsigned int* ctr, int 
 }
 
 // Whole warp: the item the producer published for step k.
+template <bool POLL = false>
 __device__ __forceinline__ int sched_consume(uint32_t k, uint64_t* sfull, uint64_t* sempty,
                                              volatile int* sched, volatile int* abort_flag,
                                              unsigned int* err_word, unsigned int site) {
   const int slot = k % kSchedSlots;
-  if (!mbar_wait(&sfull[slot], (k / kSchedSlots) & 1, abort_flag, err_word, site)) return -2;
+  if (!mbar_wait<POLL>(&sfull[slot], (k / kSchedSlots) & 1, abort_flag, err_word, site)) return -2;
   const int w = sched[slot];
   __syncwarp();
   if ((threadIdx.x & 31) == 0) mbar_arrive(&sempty[slot]);

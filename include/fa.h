@@ -389,6 +389,12 @@ int fa_prefill_rescale_count(int reset, unsigned long long* count);
  * default is far above any wait of a healthy call; a short limit serves as a
  * watchdog, or in tests to make the timeout path run.
  *
+ * Below 1 ms the limit is a watchdog: the decode kernels, and the dense
+ * prefill (whose launches then use a polling instantiation of the kernel),
+ * check it at every probe of every wait.  The packed-sequence prefill and the
+ * backward kernels keep suspending probes of about 4 us each, so there a wait
+ * trips the watchdog only once it has lasted about two of them.
+ *
  * Synchronises the current device and applies to calls enqueued afterwards.
  * Returns FA_OK or FA_ERR_CUDA.
  */

@@ -2,10 +2,12 @@
 past its time limit makes the kernel abort and report, and the context stays
 usable.
 
-fa_set_wait_limit_ns(1) makes every mbarrier wait that is not satisfied at
-once give up: the CTA leaves its loops, waits (with the fixed 2 s teardown
-limit) for the loads and MMAs already in flight, frees its tensor memory and
-sets the timeout bit and the wait's site in the error word.  Nothing waits
+fa_set_wait_limit_ns(1) is a watchdog limit: the dense prefill (through its
+polling instantiation) and the decode check the clock at every probe of every
+wait, so a wait that is not satisfied at once gives up.  The CTA leaves its
+loops, waits (with the fixed 2 s teardown limit) for the loads and MMAs
+already in flight, frees its tensor memory and sets the timeout bit and the
+wait's site in the error word.  Nothing waits
 without a bound, and no kernel is altered for the test.  The test checks that
 a prefill and a 65536-token decode report FA_ERR_TIMEOUT with a site, then
 restores the default limit and checks that the next calls match the oracle.
