@@ -328,120 +328,116 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
     __syncwarp();
   } else if (warp == 5) {
     // ================================== MMA ===================================
-    constexpr uint32_t IDESC_S = idesc_f16(bw::BT, bw::BT, kBF16, false);
-    constexpr uint32_t IDESC_ACC = idesc_f16(bw::BT, D, kBF16, true);
-    const uint32_t sq_addr = smem_u32(sQ), sdo_addr = smem_u32(sDO), skv_addr = smem_u32(sKV);
-    uint32_t kv_cnt = 0, local = 0, g = 0;  // g: key-tile steps so far (buffers, parities)
-    bool ok = true;
-    constexpr uint32_t COL_DP = 256, COL_DQ = 384;
-    // D_tmem = A (K-major smem) x B^T (K-major smem) over D/16 k-steps.
-    // Descriptors advance by adding (byte offset >> 4) to one base each: the
-    // start-address field holds address bits 4-17, and shared-memory
-    // addresses stay below 2^18, so the addition never carries out of it.
-    auto issue_nt = [&](uint32_t d_col, uint32_t a_addr, uint32_t b_addr) {
-      if (leader) {
-        const uint64_t a0 = sdesc_sw128(a_addr, 16, 1024), b0 = sdesc_sw128(b_addr, 16, 1024);
+    // Lane 0 alone runs the issuer loop; the other lanes wait at the
+    // __syncwarp below (the warp reconverges before the CTA barrier and
+    // tcgen05.dealloc).  Descriptors advance on their low 32 bits (see
+    // mma_ss_lh); the high halves (SBO, version, swizzle) are one constant.
+    if (lane == 0) {
+      const uint32_t sd_hi = (uint32_t)(sdesc_sw128(0u, 16, 1024) >> 32);
+      constexpr uint32_t IDESC_S = idesc_f16(bw::BT, bw::BT, kBF16, false);
+      constexpr uint32_t IDESC_ACC = idesc_f16(bw::BT, D, kBF16, true);
+      const uint32_t sq_addr = smem_u32(sQ), sdo_addr = smem_u32(sDO), skv_addr = smem_u32(sKV);
+      uint32_t kv_cnt = 0, local = 0, g = 0;  // g: key-tile steps so far (buffers, parities)
+      bool ok = true;
+      constexpr uint32_t COL_DP = 256, COL_DQ = 384;
+      // D_tmem = A (K-major smem) x B^T (K-major smem) over D/16 k-steps.
+      auto issue_nt = [&](uint32_t d_col, uint32_t a_addr, uint32_t b_addr) {
+        const uint32_t a0 = (uint32_t)sdesc_sw128(a_addr, 16, 1024);
+        const uint32_t b0 = (uint32_t)sdesc_sw128(b_addr, 16, 1024);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t hoff16 = ((k >> 2) * bw::HALF_BYTES + (k & 3) * 32) >> 4;
-          mma_ss(tmem + d_col, a0 + hoff16, b0 + hoff16, IDESC_S, k > 0 ? 1u : 0u);
+          mma_ss_lh(tmem + d_col, a0 + hoff16, sd_hi, b0 + hoff16, sd_hi, IDESC_S, k > 0 ? 1u : 0u);
         }
-      }
-      __syncwarp();
-    };
-    auto commit = [&](uint64_t* bar) {
-      if (leader) mma_commit(bar);
-      __syncwarp();
-    };
-    // Tile t (a global count of key tiles) of the K ring or the V ring.
-    auto kslot = [&](uint32_t t) { return (int)(t % bw::KRING); };
-    auto vslot = [&](uint32_t t) { return bw::KRING + (int)(t % bw::VRING); };
-    auto wait_k = [&](uint32_t t, unsigned int site) {
-      const bool r = mbar_wait(&full[kslot(t)], (t / bw::KRING) & 1, abort_flag,
-                               &g_backward_err, site);
-      tc_fence_after();
-      return r;
-    };
-    auto wait_v = [&](uint32_t t, unsigned int site) {
-      const bool r = mbar_wait(&full[vslot(t)], (t / bw::VRING) & 1, abort_flag,
-                               &g_backward_err, site);
-      tc_fence_after();
-      return r;
-    };
-    auto addr = [&](int s) { return skv_addr + s * C::TILE_BYTES; };
-    for (uint32_t it = 0; ok; ++it, ++local) {
-      const int w =
-          sched_consume(it, sched_full, sched_empty, sched, abort_flag, &g_backward_err, 11);
-      if (w < 0) {
-        ok = w == -1;
-        break;
-      }
-      int b, hq, qt;
-      dq_item(w, p, &b, &hq, &qt);
-      const int n = bw_key_tiles(qt * bw::BT, p);
-      if (!(ok = mbar_wait(q_full, local & 1, abort_flag, &g_backward_err, 3))) break;
-      tc_fence_after();
-      if (n == 0) {
-        commit(q_empty);
-        commit(o_full);  // dQ = 0 for this tile (accumulator not written)
-        continue;
-      }
-      const uint32_t kb = kv_cnt;  // K_j and V_j are tile kb + j of their rings
-      kv_cnt += n;
-      // Prologue: S(0), dP(0), S(1).
-      if (!(ok = wait_k(kb, 4))) break;
-      issue_nt((g & 1) * 128, sq_addr, addr(kslot(kb)));
-      commit(&s_full[g & 1]);
-      if (!(ok = wait_v(kb, 5))) break;
-      issue_nt(COL_DP, sdo_addr, addr(vslot(kb)));
-      commit(dp_full);
-      commit(&empty[vslot(kb)]);
-      if (n == 1) commit(q_empty);
-      if (n > 1) {
-        if (!(ok = wait_k(kb + 1, 4))) break;
-        issue_nt(((g + 1) & 1) * 128, sq_addr, addr(kslot(kb + 1)));
-        commit(&s_full[(g + 1) & 1]);
-      }
-      for (int j = 0; j < n && ok; ++j) {
-        const uint32_t gj = g + j;
-        // dP(j) is in the element-wise warps' registers: dP(j+1) may go.
-        if (!(ok = mbar_wait(ld_done, gj & 1, abort_flag, &g_backward_err, 6))) break;
+      };
+      auto commit = [&](uint64_t* bar) { mma_commit(bar); };
+      // Tile t (a global count of key tiles) of the K ring or the V ring.
+      auto kslot = [&](uint32_t t) { return (int)(t % bw::KRING); };
+      auto vslot = [&](uint32_t t) { return bw::KRING + (int)(t % bw::VRING); };
+      auto wait_k = [&](uint32_t t, unsigned int site) {
+        const bool r = mbar_wait(&full[kslot(t)], (t / bw::KRING) & 1, abort_flag,
+                                 &g_backward_err, site);
         tc_fence_after();
-        if (j + 1 < n) {
-          if (!(ok = wait_v(kb + j + 1, 5))) break;
-          issue_nt(COL_DP, sdo_addr, addr(vslot(kb + j + 1)));
-          commit(dp_full);
-          commit(&empty[vslot(kb + j + 1)]);
-          if (j + 1 == n - 1) commit(q_empty);  // the last S and dP are issued
+        return r;
+      };
+      auto wait_v = [&](uint32_t t, unsigned int site) {
+        const bool r = mbar_wait(&full[vslot(t)], (t / bw::VRING) & 1, abort_flag,
+                                 &g_backward_err, site);
+        tc_fence_after();
+        return r;
+      };
+      auto addr = [&](int s) { return skv_addr + s * C::TILE_BYTES; };
+      for (uint32_t it = 0; ok; ++it, ++local) {
+        const int w =
+            sched_consume_lane(it, sched_full, sched_empty, sched, abort_flag, &g_backward_err,
+                               11);
+        if (w < 0) {
+          ok = w == -1;
+          break;
         }
-        // dQ += dS(j) K_j: dS (16-bit) in the first 64 columns of S buffer j.
-        if (!(ok = mbar_wait(ds_full, gj & 1, abort_flag, &g_backward_err, 6))) break;
+        int b, hq, qt;
+        dq_item(w, p, &b, &hq, &qt);
+        const int n = bw_key_tiles(qt * bw::BT, p);
+        if (!(ok = mbar_wait(q_full, local & 1, abort_flag, &g_backward_err, 3))) break;
         tc_fence_after();
-        const uint32_t kaddr = addr(kslot(kb + j));
-        if (leader) {
-          const uint64_t b0 = sdesc_sw128(kaddr, bw::HALF_BYTES, 1024);
+        if (n == 0) {
+          commit(q_empty);
+          commit(o_full);  // dQ = 0 for this tile (accumulator not written)
+          continue;
+        }
+        const uint32_t kb = kv_cnt;  // K_j and V_j are tile kb + j of their rings
+        kv_cnt += n;
+        // Prologue: S(0), dP(0), S(1).
+        if (!(ok = wait_k(kb, 4))) break;
+        issue_nt((g & 1) * 128, sq_addr, addr(kslot(kb)));
+        commit(&s_full[g & 1]);
+        if (!(ok = wait_v(kb, 5))) break;
+        issue_nt(COL_DP, sdo_addr, addr(vslot(kb)));
+        commit(dp_full);
+        commit(&empty[vslot(kb)]);
+        if (n == 1) commit(q_empty);
+        if (n > 1) {
+          if (!(ok = wait_k(kb + 1, 4))) break;
+          issue_nt(((g + 1) & 1) * 128, sq_addr, addr(kslot(kb + 1)));
+          commit(&s_full[(g + 1) & 1]);
+        }
+        for (int j = 0; j < n && ok; ++j) {
+          const uint32_t gj = g + j;
+          // dP(j) is in the element-wise warps' registers: dP(j+1) may go.
+          if (!(ok = mbar_wait(ld_done, gj & 1, abort_flag, &g_backward_err, 6))) break;
+          tc_fence_after();
+          if (j + 1 < n) {
+            if (!(ok = wait_v(kb + j + 1, 5))) break;
+            issue_nt(COL_DP, sdo_addr, addr(vslot(kb + j + 1)));
+            commit(dp_full);
+            commit(&empty[vslot(kb + j + 1)]);
+            if (j + 1 == n - 1) commit(q_empty);  // the last S and dP are issued
+          }
+          // dQ += dS(j) K_j: dS (16-bit) in the first 64 columns of S buffer j.
+          if (!(ok = mbar_wait(ds_full, gj & 1, abort_flag, &g_backward_err, 6))) break;
+          tc_fence_after();
+          const uint32_t b0 = (uint32_t)sdesc_sw128(addr(kslot(kb + j)), bw::HALF_BYTES, 1024);
 #pragma unroll
           for (int k = 0; k < bw::BT / 16; ++k) {
-            const uint64_t bd = b0 + (uint32_t)((k * 16 * 128) >> 4);
-            mma_ts(tmem + COL_DQ, tmem + (gj & 1) * 128 + k * 8, bd, IDESC_ACC,
-                   (j > 0 || k > 0) ? 1u : 0u);
+            mma_ts_lh(tmem + COL_DQ, tmem + (gj & 1) * 128 + k * 8,
+                      b0 + (uint32_t)((k * 16 * 128) >> 4), sd_hi, IDESC_ACC,
+                      (j > 0 || k > 0) ? 1u : 0u);
+          }
+          commit(&empty[kslot(kb + j)]);
+          // S(j+2) into the buffer dQ(j) has just read.
+          if (j + 2 < n) {
+            if (!(ok = wait_k(kb + j + 2, 4))) break;
+            issue_nt((gj & 1) * 128, sq_addr, addr(kslot(kb + j + 2)));
+            commit(&s_full[gj & 1]);
           }
         }
-        __syncwarp();
-        commit(&empty[kslot(kb + j)]);
-        // S(j+2) into the buffer dQ(j) has just read.
-        if (j + 2 < n) {
-          if (!(ok = wait_k(kb + j + 2, 4))) break;
-          issue_nt((gj & 1) * 128, sq_addr, addr(kslot(kb + j + 2)));
-          commit(&s_full[gj & 1]);
-        }
+        if (!ok) break;
+        g += n;
+        commit(o_full);
       }
-      if (!ok) break;
-      g += n;
-      commit(o_full);
+      commit(drain);
+      mbar_wait_drain(drain, 0);
     }
-    commit(drain);
-    mbar_wait_drain(drain, 0);
     __syncwarp();
   } else {
     // ============================ dS (warps 0-3) ============================
@@ -754,88 +750,85 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
     __syncwarp();
   } else if (warp == 5) {
     // ================================== MMA ===================================
-    constexpr uint32_t IDESC_S = idesc_f16(bw::BT, QS, kBF16, false);
-    constexpr uint32_t IDESC_ACC = idesc_f16(bw::BT, D, kBF16, true);
-    const uint32_t sk_addr = smem_u32(sK), sv_addr = smem_u32(sV), sst = smem_u32(sStage);
-    uint32_t st_cnt = 0, local = 0, gcnt = 0;
-    bool ok = true;
-    // D_tmem (128 x 64) = A (128-row tile, K-major) x B^T (64-row sub-tile, K-major).
-    // Descriptors advance by adding (byte offset >> 4) to one base each (the
-    // start-address field never carries: shared memory lies below 2^18).
-    auto issue_nt = [&](uint32_t d_col, uint32_t a_addr, uint32_t b_addr) {
-      if (leader) {
-        const uint64_t a0 = sdesc_sw128(a_addr, 16, 1024), b0 = sdesc_sw128(b_addr, 16, 1024);
+    // Lane 0 alone runs the issuer loop; the other lanes wait at the
+    // __syncwarp below (the warp reconverges before the CTA barrier and
+    // tcgen05.dealloc).  Descriptors advance on their low 32 bits (see
+    // mma_ss_lh); the high halves (SBO, version, swizzle) are one constant.
+    if (lane == 0) {
+      const uint32_t sd_hi = (uint32_t)(sdesc_sw128(0u, 16, 1024) >> 32);
+      constexpr uint32_t IDESC_S = idesc_f16(bw::BT, QS, kBF16, false);
+      constexpr uint32_t IDESC_ACC = idesc_f16(bw::BT, D, kBF16, true);
+      const uint32_t sk_addr = smem_u32(sK), sv_addr = smem_u32(sV), sst = smem_u32(sStage);
+      uint32_t st_cnt = 0, local = 0, gcnt = 0;
+      bool ok = true;
+      // D_tmem (128 x 64) = A (128-row tile, K-major) x B^T (64-row sub-tile, K-major).
+      auto issue_nt = [&](uint32_t d_col, uint32_t a_addr, uint32_t b_addr) {
+        const uint32_t a0 = (uint32_t)sdesc_sw128(a_addr, 16, 1024);
+        const uint32_t b0 = (uint32_t)sdesc_sw128(b_addr, 16, 1024);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t ka16 = ((k >> 2) * bw::HALF_BYTES + (k & 3) * 32) >> 4;
           const uint32_t kb16 = ((k >> 2) * bw::SUB_HALF + (k & 3) * 32) >> 4;
-          mma_ss(tmem + d_col, a0 + ka16, b0 + kb16, IDESC_S, k > 0 ? 1u : 0u);
+          mma_ss_lh(tmem + d_col, a0 + ka16, sd_hi, b0 + kb16, sd_hi, IDESC_S, k > 0 ? 1u : 0u);
         }
-      }
-      __syncwarp();
-    };
-    // acc += A (TMEM, 16-bit, 64 columns of K) x B (64-row sub-tile, MN-major).
-    auto issue_acc = [&](uint32_t d_col, uint32_t a_col, uint32_t b_addr, bool accumulate) {
-      if (leader) {
-        const uint64_t b0 = sdesc_sw128(b_addr, bw::SUB_HALF, 1024);
+      };
+      // acc += A (TMEM, 16-bit, 64 columns of K) x B (64-row sub-tile, MN-major).
+      auto issue_acc = [&](uint32_t d_col, uint32_t a_col, uint32_t b_addr, bool accumulate) {
+        const uint32_t b0 = (uint32_t)sdesc_sw128(b_addr, bw::SUB_HALF, 1024);
 #pragma unroll
         for (int k = 0; k < QS / 16; ++k) {
-          const uint64_t bd = b0 + (uint32_t)((k * 16 * 128) >> 4);
-          mma_ts(tmem + d_col, tmem + a_col + k * 8, bd, IDESC_ACC,
-                 (accumulate || k > 0) ? 1u : 0u);
+          mma_ts_lh(tmem + d_col, tmem + a_col + k * 8, b0 + (uint32_t)((k * 16 * 128) >> 4),
+                    sd_hi, IDESC_ACC, (accumulate || k > 0) ? 1u : 0u);
         }
-      }
-      __syncwarp();
-    };
-    auto commit = [&](uint64_t* bar) {
-      if (leader) mma_commit(bar);
-      __syncwarp();
-    };
-    // dV += P^T dO and dK += dS^T Q of the sub-step held in buffer gb, stage s.
-    auto issue_grads = [&](uint32_t gb, int s, bool accumulate) {
-      const int bb = gb & 1;
-      if (!mbar_wait(&pd_full[bb], (gb >> 1) & 1, abort_flag, &g_backward_err, 5)) return false;
-      tc_fence_after();
-      const uint32_t sq = sst + s * C::STAGE_DKV, sdo = sq + C::SUB_BYTES;
-      issue_acc(COL_DV, bb * 128, sdo, accumulate);      // dV += P^T dO
-      issue_acc(COL_DK, bb * 128 + 64, sq, accumulate);  // dK += dS^T Q
-      commit(&empty[s]);
-      return true;
-    };
-    for (uint32_t it = 0; ok; ++it, ++local) {
-      const int w =
-          sched_consume(it, sched_full, sched_empty, sched, abort_flag, &g_backward_err, 11);
-      if (w < 0) {
-        ok = w == -1;
-        break;
-      }
-      int b, hkv, kt;
-      dkv_item(w, p, &b, &hkv, &kt);
-      const int steps = p.G * (n_qs - first_sub(kt * bw::BT));
-      if (!(ok = mbar_wait(kv_full, local & 1, abort_flag, &g_backward_err, 3))) break;
-      tc_fence_after();
-      int s_prev = 0;
-      for (int u = 0; u < steps && ok; ++u, ++gcnt) {
-        const int s = st_cnt % NS;
-        const uint32_t ph = (st_cnt / NS) & 1;
-        ++st_cnt;
-        if (!(ok = mbar_wait(&full[s], ph, abort_flag, &g_backward_err, 4))) break;
+      };
+      auto commit = [&](uint64_t* bar) { mma_commit(bar); };
+      // dV += P^T dO and dK += dS^T Q of the sub-step held in buffer gb, stage s.
+      auto issue_grads = [&](uint32_t gb, int s, bool accumulate) {
+        const int bb = gb & 1;
+        if (!mbar_wait(&pd_full[bb], (gb >> 1) & 1, abort_flag, &g_backward_err, 5)) return false;
         tc_fence_after();
-        const uint32_t bb = gcnt & 1;
         const uint32_t sq = sst + s * C::STAGE_DKV, sdo = sq + C::SUB_BYTES;
-        issue_nt(bb * 128, sk_addr, sq);       // S^T = K Q^T
-        issue_nt(bb * 128 + 64, sv_addr, sdo); // dP^T = V dO^T
-        commit(&st_full[bb]);
-        if (u > 0 && !(ok = issue_grads(gcnt - 1, s_prev, u > 1))) break;
-        s_prev = s;
+        issue_acc(COL_DV, bb * 128, sdo, accumulate);      // dV += P^T dO
+        issue_acc(COL_DK, bb * 128 + 64, sq, accumulate);  // dK += dS^T Q
+        commit(&empty[s]);
+        return true;
+      };
+      for (uint32_t it = 0; ok; ++it, ++local) {
+        const int w =
+            sched_consume_lane(it, sched_full, sched_empty, sched, abort_flag, &g_backward_err,
+                               11);
+        if (w < 0) {
+          ok = w == -1;
+          break;
+        }
+        int b, hkv, kt;
+        dkv_item(w, p, &b, &hkv, &kt);
+        const int steps = p.G * (n_qs - first_sub(kt * bw::BT));
+        if (!(ok = mbar_wait(kv_full, local & 1, abort_flag, &g_backward_err, 3))) break;
+        tc_fence_after();
+        int s_prev = 0;
+        for (int u = 0; u < steps && ok; ++u, ++gcnt) {
+          const int s = st_cnt % NS;
+          const uint32_t ph = (st_cnt / NS) & 1;
+          ++st_cnt;
+          if (!(ok = mbar_wait(&full[s], ph, abort_flag, &g_backward_err, 4))) break;
+          tc_fence_after();
+          const uint32_t bb = gcnt & 1;
+          const uint32_t sq = sst + s * C::STAGE_DKV, sdo = sq + C::SUB_BYTES;
+          issue_nt(bb * 128, sk_addr, sq);       // S^T = K Q^T
+          issue_nt(bb * 128 + 64, sv_addr, sdo); // dP^T = V dO^T
+          commit(&st_full[bb]);
+          if (u > 0 && !(ok = issue_grads(gcnt - 1, s_prev, u > 1))) break;
+          s_prev = s;
+        }
+        if (!ok) break;
+        if (steps > 0 && !(ok = issue_grads(gcnt - 1, s_prev, steps > 1))) break;
+        commit(kv_empty);
+        commit(o_full);
       }
-      if (!ok) break;
-      if (steps > 0 && !(ok = issue_grads(gcnt - 1, s_prev, steps > 1))) break;
-      commit(kv_empty);
-      commit(o_full);
+      commit(drain);
+      mbar_wait_drain(drain, 0);
     }
-    commit(drain);
-    mbar_wait_drain(drain, 0);
     __syncwarp();
   } else {
     // ======================= P^T and dS^T (warps 0-3) =======================

@@ -372,11 +372,11 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
-  // The producer and MMA warps run their loops with all 32 lanes converged:
-  // every lane waits on the barriers, lane 0 alone issues TMA / MMA / commit,
-  // and __syncwarp() follows each issue.  (A warp must never reach the
-  // warp-aligned CTA barrier below, or tcgen05.dealloc, with lanes still
-  // inside a role loop.)
+  // The producer warp runs its loop with all 32 lanes converged: every lane
+  // waits on the barriers, lane 0 alone issues TMA loads, and __syncwarp()
+  // follows each issue.  The MMA warp's loop runs on lane 0 alone, the other
+  // lanes waiting at its end.  (A warp must never reach the warp-aligned CTA
+  // barrier below, or tcgen05.dealloc, with lanes still inside a role loop.)
   const bool leader = lane == 0;
   // Work items: the producer claims each item from the counter and hands it
   // to the MMA and softmax warps (sched_*).
@@ -483,138 +483,141 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
     __syncwarp();
   } else if (warp == 9) {
     // ============================ MMA issuer ============================
-    constexpr uint32_t IDESC_S = idesc_f16(pf::BM, pf::BN, kBF16, false);
-    constexpr uint32_t IDESC_O = idesc_f16(pf::BM, D, kBF16, true);
-    const uint32_t sq_addr = smem_u32(sQ);
-    const uint32_t skv_addr = smem_u32(sKV);
-    uint32_t kv_cnt = 0, local = 0, p_cnt0 = 0, p_cnt1 = 0;
-    bool ok = true;
+    // Lane 0 alone runs the issuer loop (waits, MMAs, commits); the other
+    // lanes wait at the __syncwarp below, so the warp reconverges before the
+    // CTA barrier and tcgen05.dealloc.  (With all 32 lanes in the loop, every
+    // issue and commit was followed by a __syncwarp: a single-lane loop took
+    // those, and the leader tests, out of the issuer's instruction stream.)
+    if (lane == 0) {
+      constexpr uint32_t IDESC_S = idesc_f16(pf::BM, pf::BN, kBF16, false);
+      constexpr uint32_t IDESC_O = idesc_f16(pf::BM, D, kBF16, true);
+      const uint32_t sq_addr = smem_u32(sQ);
+      const uint32_t skv_addr = smem_u32(sKV);
+      uint32_t kv_cnt = 0, local = 0, p_cnt0 = 0, p_cnt1 = 0;
+      bool ok = true;
 
-    // Descriptors advance by adding (byte offset >> 4) to the base descriptor:
-    // the start-address field holds address bits 4-17, and shared-memory
-    // addresses stay below 2^18, so the addition never carries out of it.
-    const uint64_t q_desc[2] = {sdesc_sw128(sq_addr, 16, 1024),
-                                sdesc_sw128(sq_addr + C::TILE_BYTES, 16, 1024)};
-    // S_i = Q_i K^T over D/16 k-steps (K-major A and B, 128-byte swizzle).
-    auto issue_s = [&](int i, int stage) {
-      if (leader) {
+      // Descriptors advance by adding (byte offset >> 4) to their low 32 bits
+      // (the start-address field holds address bits 4-17 and shared-memory
+      // addresses stay below 2^18, so the addition never carries out of it):
+      // one 32-bit add per operand and MMA.  The high halves are constants.
+      const uint64_t dq0 = sdesc_sw128(sq_addr, 16, 1024);
+      const uint64_t dkv = sdesc_sw128(skv_addr, 16, 1024);          // K, stage 0
+      const uint64_t dv = sdesc_sw128(skv_addr, pf::HALF_BYTES, 1024);  // V, stage 0
+      const uint32_t q_lo[2] = {(uint32_t)dq0, (uint32_t)dq0 + (C::TILE_BYTES >> 4)};
+      const uint32_t sd_hi = (uint32_t)(dq0 >> 32);  // SBO, version, swizzle: shared
+      const uint32_t k_lo0 = (uint32_t)dkv, v_lo0 = (uint32_t)dv;
+      // S_i = Q_i K^T over D/16 k-steps (K-major A and B, 128-byte swizzle).
+      auto issue_s = [&](int i, int stage) {
         const uint32_t d_tmem = tmem + (i ? C::COL_S1 : C::COL_S0);
-        const uint64_t a0 = q_desc[i];
-        const uint64_t b0 = sdesc_sw128(skv_addr + stage * C::TILE_BYTES, 16, 1024);
+        const uint32_t a0 = q_lo[i];
+        const uint32_t b0 = k_lo0 + stage * (C::TILE_BYTES >> 4);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t hoff16 = ((k >> 2) * pf::HALF_BYTES + (k & 3) * 32) >> 4;
-          mma_ss(d_tmem, a0 + hoff16, b0 + hoff16, IDESC_S, k > 0 ? 1u : 0u);
+          mma_ss_lh(d_tmem, a0 + hoff16, sd_hi, b0 + hoff16, sd_hi, IDESC_S, k > 0 ? 1u : 0u);
         }
-      }
-      __syncwarp();
-    };
-    // O_i (+)= P_i V over BN/16 k-steps; P_i from TMEM, V MN-major in smem.
-    auto issue_pv = [&](int i, int stage, bool accumulate) {
-      if (leader) {
+      };
+      // O_i (+)= P_i V over BN/16 k-steps; P_i from TMEM, V MN-major in smem.
+      auto issue_pv = [&](int i, int stage, bool accumulate) {
         const uint32_t d_tmem = tmem + (i ? C::COL_O1 : C::COL_O0);
         const uint32_t p_tmem = tmem + (i ? C::COL_S1 : C::COL_S0);
-        const uint64_t b0 = sdesc_sw128(skv_addr + stage * C::TILE_BYTES, pf::HALF_BYTES, 1024);
+        const uint32_t b0 = v_lo0 + stage * (C::TILE_BYTES >> 4);
 #pragma unroll
         for (int k = 0; k < pf::BN / 16; ++k) {
-          const uint64_t bd = b0 + (uint32_t)((k * 16 * 128) >> 4);
-          mma_ts(d_tmem, p_tmem + k * 8, bd, IDESC_O, (accumulate || k > 0) ? 1u : 0u);
+          mma_ts_lh(d_tmem, p_tmem + k * 8, b0 + (uint32_t)((k * 16 * 128) >> 4), sd_hi, IDESC_O,
+                    (accumulate || k > 0) ? 1u : 0u);
         }
-      }
-      __syncwarp();
-    };
-    // tcgen05.commit from the issuing lane: arrive on *bar once its MMAs are done.
-    auto commit = [&](uint64_t* bar) {
-      if (leader) mma_commit(bar);
-      __syncwarp();
-    };
+      };
+      // tcgen05.commit from the issuing lane: arrive on *bar once its MMAs are done.
+      auto commit = [&](uint64_t* bar) { mma_commit(bar); };
 
-    // K_j / V_j of an item sit at ring positions kb + 2j / kb + 2j + 1; V_j
-    // and K_{j+1} complete together on K_{j+1}'s barrier (see the producer).
-    auto ring_wait = [&](uint32_t idx, unsigned int site) {
-      return mbar_wait<POLL>(&full[idx % NSTAGE], (idx / NSTAGE) & 1, abort_flag, &g_prefill_err, site);
-    };
-    for (uint32_t it = 0; ok; ++it, ++local) {
-      const int w =
-          sched_consume<POLL>(it, sched_full, sched_empty, sched, abort_flag, &g_prefill_err, 15);
-      if (w < 0) {
-        ok = w == -1;
-        break;
-      }
-      int b, hq, qb;
-      const SeqSpan sq = work_item<PACKED>(p, w, &b, &hq, &qb);
-      const int row0 = qb * pf::QBLOCK;
-      const int nt0 = kv_tiles_for(row0, sq.Sq, sq.Sk, p.causal);
-      const int nt1 = kv_tiles_for(row0 + pf::BM, sq.Sq, sq.Sk, p.causal);
-      const int n = nt0 > nt1 ? nt0 : nt1;
-      if (!(ok = mbar_wait<POLL>(q_full, local & 1, abort_flag, &g_prefill_err, 3))) break;
-      tc_fence_after();
-      if (n == 0) {
-        commit(q_empty);
-        continue;
-      }
-      const uint32_t kb = kv_cnt;
-      kv_cnt += 2 * n;
-      // K_0 -> S_0(0), S_1(0)
-      if (!(ok = ring_wait(kb, 4))) break;
-      tc_fence_after();
-      if (nt0 > 0) {
-        issue_s(0, kb % NSTAGE);
-        commit(&s_full[0]);
-      }
-      if (nt1 > 0) {
-        issue_s(1, kb % NSTAGE);
-        commit(&s_full[1]);
-      }
-      commit(&empty[kb % NSTAGE]);
-      if (n == 1) commit(q_empty);
-      // Operands of step 0: V_0 and K_1 (one barrier: K_1's), or V_0 alone.
-      if (!(ok = ring_wait(n > 1 ? kb + 2 : kb + 1, 5))) break;
-      tc_fence_after();
+      // K_j / V_j of an item sit at ring positions kb + 2j / kb + 2j + 1; V_j
+      // and K_{j+1} complete together on K_{j+1}'s barrier (see the producer).
+      auto ring_wait = [&](uint32_t idx, unsigned int site) {
+        return mbar_wait<POLL>(&full[idx % NSTAGE], (idx / NSTAGE) & 1, abort_flag, &g_prefill_err, site);
+      };
+      for (uint32_t it = 0; ok; ++it, ++local) {
+        const int w = sched_consume_lane<POLL>(it, sched_full, sched_empty, sched, abort_flag,
+                                             &g_prefill_err, 15);
+        if (w < 0) {
+          ok = w == -1;
+          break;
+        }
+        int b, hq, qb;
+        const SeqSpan sq = work_item<PACKED>(p, w, &b, &hq, &qb);
+        const int row0 = qb * pf::QBLOCK;
+        const int nt0 = kv_tiles_for(row0, sq.Sq, sq.Sk, p.causal);
+        const int nt1 = kv_tiles_for(row0 + pf::BM, sq.Sq, sq.Sk, p.causal);
+        const int n = nt0 > nt1 ? nt0 : nt1;
+        if (!(ok = mbar_wait<POLL>(q_full, local & 1, abort_flag, &g_prefill_err, 3))) break;
+        tc_fence_after();
+        if (n == 0) {
+          commit(q_empty);
+          continue;
+        }
+        const uint32_t kb = kv_cnt;
+        kv_cnt += 2 * n;
+        // K_0 -> S_0(0), S_1(0)
+        if (!(ok = ring_wait(kb, 4))) break;
+        tc_fence_after();
+        if (nt0 > 0) {
+          issue_s(0, kb % NSTAGE);
+          commit(&s_full[0]);
+        }
+        if (nt1 > 0) {
+          issue_s(1, kb % NSTAGE);
+          commit(&s_full[1]);
+        }
+        commit(&empty[kb % NSTAGE]);
+        if (n == 1) commit(q_empty);
+        // Operands of step 0: V_0 and K_1 (one barrier: K_1's), or V_0 alone.
+        if (!(ok = ring_wait(n > 1 ? kb + 2 : kb + 1, 5))) break;
+        tc_fence_after();
 
-      // Per step j: PV0(j), S0(j+1), PV1(j), S1(j+1), then the operand wait
-      // of step j+1 (V_{j+1} and K_{j+2}; K_{j+1} was waited for a step
-      // earlier).  The wait sits behind a whole batch of issued MMAs, so its
-      // latency leaves less of the tensor pipe idle.
-      for (int j = 0; j < n && ok; ++j) {
-        const int sV = (kb + 2 * j + 1) % NSTAGE;
-        const int sK = (kb + 2 * j + 2) % NSTAGE;  // K_{j+1}
-        if (j < nt0) {
-          if (!(ok = mbar_wait<POLL>(&p_full[0], p_cnt0 & 1, abort_flag, &g_prefill_err, 7))) break;
-          ++p_cnt0;
-          tc_fence_after();
-          issue_pv(0, sV, j > 0);
-          if (j == nt0 - 1) commit(&o_full[0]);
-          if (j + 1 < nt0) {
-            issue_s(0, sK);
-            commit(&s_full[0]);
+        // Per step j: PV0(j), S0(j+1), PV1(j), S1(j+1), then the operand wait
+        // of step j+1 (V_{j+1} and K_{j+2}; K_{j+1} was waited for a step
+        // earlier).  The wait sits behind a whole batch of issued MMAs, so its
+        // latency leaves less of the tensor pipe idle.
+        for (int j = 0; j < n && ok; ++j) {
+          const int sV = (kb + 2 * j + 1) % NSTAGE;
+          const int sK = (kb + 2 * j + 2) % NSTAGE;  // K_{j+1}
+          if (j < nt0) {
+            if (!(ok = mbar_wait<POLL>(&p_full[0], p_cnt0 & 1, abort_flag, &g_prefill_err, 7))) break;
+            ++p_cnt0;
+            tc_fence_after();
+            issue_pv(0, sV, j > 0);
+            if (j == nt0 - 1) commit(&o_full[0]);
+            if (j + 1 < nt0) {
+              issue_s(0, sK);
+              commit(&s_full[0]);
+            }
+          }
+          if (j < nt1) {
+            if (!(ok = mbar_wait<POLL>(&p_full[1], p_cnt1 & 1, abort_flag, &g_prefill_err, 8))) break;
+            ++p_cnt1;
+            tc_fence_after();
+            issue_pv(1, sV, j > 0);
+            if (j == nt1 - 1) commit(&o_full[1]);
+          }
+          commit(&empty[sV]);
+          if (j + 1 < n) {
+            if (j + 1 < nt1) {
+              issue_s(1, sK);
+              commit(&s_full[1]);
+            }
+            commit(&empty[sK]);
+            if (j + 1 == n - 1) commit(q_empty);
+            // V_{j+1} and K_{j+2} on K_{j+2}'s barrier, or the last V alone.
+            if (!(ok = ring_wait(j + 2 < n ? kb + 2 * j + 4 : kb + 2 * j + 3, 6))) break;
+            tc_fence_after();
           }
         }
-        if (j < nt1) {
-          if (!(ok = mbar_wait<POLL>(&p_full[1], p_cnt1 & 1, abort_flag, &g_prefill_err, 8))) break;
-          ++p_cnt1;
-          tc_fence_after();
-          issue_pv(1, sV, j > 0);
-          if (j == nt1 - 1) commit(&o_full[1]);
-        }
-        commit(&empty[sV]);
-        if (j + 1 < n) {
-          if (j + 1 < nt1) {
-            issue_s(1, sK);
-            commit(&s_full[1]);
-          }
-          commit(&empty[sK]);
-          if (j + 1 == n - 1) commit(q_empty);
-          // V_{j+1} and K_{j+2} on K_{j+2}'s barrier, or the last V alone.
-          if (!(ok = ring_wait(j + 2 < n ? kb + 2 * j + 4 : kb + 2 * j + 3, 6))) break;
-          tc_fence_after();
-        }
       }
+      // Every MMA this lane issued has completed (and its commits have
+      // landed) before the CTA barrier that precedes the TMEM dealloc.
+      commit(drain);
+      mbar_wait_drain(drain, 0);
     }
-    // Every MMA this warp issued has completed (and its commits have landed)
-    // before the CTA barrier that precedes the TMEM dealloc.
-    commit(drain);
-    mbar_wait_drain(drain, 0);
     __syncwarp();
    }
   } else {

@@ -203,6 +203,18 @@ __device__ __forceinline__ int sched_consume(uint32_t k, uint64_t* sfull, uint64
   return w;
 }
 
+// One lane alone (the rest of its warp elsewhere): the published item.
+template <bool POLL = false>
+__device__ __forceinline__ int sched_consume_lane(uint32_t k, uint64_t* sfull, uint64_t* sempty,
+                                                  volatile int* sched, volatile int* abort_flag,
+                                                  unsigned int* err_word, unsigned int site) {
+  const int slot = k % kSchedSlots;
+  if (!mbar_wait<POLL>(&sfull[slot], (k / kSchedSlots) & 1, abort_flag, err_word, site)) return -2;
+  const int w = sched[slot];
+  mbar_arrive(&sempty[slot]);
+  return w;
+}
+
 // ---------------------------------------------------------------------------
 // TMA (tiled tensor loads into shared memory, completion on an mbarrier)
 // ---------------------------------------------------------------------------
@@ -304,6 +316,36 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// The same two MMA forms with each shared-memory descriptor given as its two
+// 32-bit halves.  Callers advance a descriptor along a tile by adding
+// (byte offset >> 4) to the low half alone: the start-address field (bits
+// 0-13) holds address bits 4-17 and shared-memory addresses stay below 2^18,
+// so the addition never carries out of the low word, and one 32-bit add
+// replaces a 64-bit add with its carry.
+__device__ __forceinline__ void mma_ss_lh(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi,
+                                          uint32_t b_lo, uint32_t b_hi, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+      "mov.b64 da, {%1, %2};\n\t"
+      "mov.b64 db, {%3, %4};\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_ts_lh(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
+                                          uint32_t b_hi, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
+      "mov.b64 db, {%2, %3};\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
