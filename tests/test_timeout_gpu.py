@@ -59,3 +59,35 @@ def test_wait_limit_aborts_report_timeout_and_the_next_calls_are_correct(fa):
     got = od.float().cpu().numpy().reshape(sd.B, sd.Hq, sd.D)
     compare(got, oracle.decode(dq, kc, vc, L, sd.scale))
     assert np.isfinite(got).all()
+
+
+def test_watchdog_limit_that_no_wait_reaches_gives_correct_results(fa):
+    """Under a watchdog limit (below 1 ms) the dense prefill runs its polling
+    instantiation and the decode polls its waits.  A limit of 500 us is far
+    above any wait of these calls, so nothing times out and the outputs must
+    match the oracle, for the dense and the packed prefill and the decode."""
+    dev = torch.device("cuda", 0)
+    q, k, v = fa_inputs.prefill_inputs(2, 8, 2, 700, 900, 128, torch.bfloat16, seed=9)
+    sd = fa_inputs.DECODE_1TOK
+    dq, kc, vc, L = fa_inputs.decode_inputs_for(sd, seed=9)
+    vl = torch.tensor([L], dtype=torch.int32, device=dev)
+    lens = [300, 0, 257, 129]  # 686 rows: within the 700 query and 900 key rows drawn
+    qp, kp, vp = (t[0, :sum(lens)].contiguous() for t in (q, k, v))
+    cu = torch.tensor([0] + list(np.cumsum(lens)), dtype=torch.int32)
+    assert fa.fa_device_error(reset=1)[0] == fa.FA_OK
+    try:
+        assert fa.fa_set_wait_limit_ns(500_000) == fa.FA_OK
+        out = fa.prefill(q.to(dev), k.to(dev), v.to(dev), 0.088, True)
+        outp = fa.prefill_varlen(qp.to(dev), kp.to(dev), vp.to(dev), cu.to(dev), cu.to(dev),
+                                 max(lens), 0.088, True)
+        od = fa.decode(dq.to(dev), kc.to(dev), vc.to(dev), vl, sd.scale)
+        torch.cuda.synchronize()
+        st, detail = fa.fa_device_error(reset=1)
+    finally:
+        assert fa.fa_set_wait_limit_ns(0) == fa.FA_OK
+    assert st == fa.FA_OK, hex(detail)
+    compare(out.float().cpu().numpy(), oracle.attention(q, k, v, 0.088, True))
+    compare(outp.float().cpu().numpy(),
+            oracle.attention_varlen(qp, kp, vp, cu.tolist(), cu.tolist(), 0.088, True))
+    compare(od.float().cpu().numpy().reshape(sd.B, sd.Hq, sd.D),
+            oracle.decode(dq, kc, vc, L, sd.scale))
