@@ -535,10 +535,13 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const D
     const int sp = warp + k * kCombineWarps;
     ov[k] = (sp < p.nsplit && d < D) ? p.part_o[(base + sp) * D + d] : 0.f;
   }
+  // (max, sum) of split t as one 8-byte load: selecting on the sum after a
+  // second, dependent load would cost a second L2 round trip.
   float m_t = -INFINITY, l_t = 0.f;
   if (t < p.nsplit) {
-    l_t = p.part_ml[(base + t) * 2 + 1];
-    m_t = l_t > 0.f ? p.part_ml[(base + t) * 2] : -INFINITY;
+    const float2 ml = reinterpret_cast<const float2*>(p.part_ml)[base + t];
+    l_t = ml.y;
+    m_t = l_t > 0.f ? ml.x : -INFINITY;
   }
   // M = block max of m_t.
   float M = m_t;
