@@ -15,10 +15,15 @@
 // recomputed exactly as the forward computed it, with no row max or sum.
 //
 // Both tensor-core kernels are persistent (one CTA per SM) and
-// warp-specialised: warps 0-3 turn the S / dP accumulators into dS (and P)
-// one TMEM lane per thread and write the results back into TMEM as the next
-// MMA's A operand; warp 4 issues TMA tile loads; warp 5 allocates TMEM and
-// issues tcgen05.mma.  All waits are bounded (see fa_ptx.cuh).
+// warp-specialised: element-wise warps turn the S / dP accumulators into dS
+// (and P) one TMEM lane per thread and write the results back into TMEM as
+// the next MMA's A operand; the next warp issues TMA tile loads, and the one
+// after it allocates TMEM and issues tcgen05.mma.  The dq kernel and the
+// D = 128 dkdv kernel have 4 element-wise warps (warps 0-3; producer 4, MMA
+// 5).  The D = 64 dkdv kernel, whose element-wise pass is the longer part of
+// a step, has 8: two per TMEM lane quarter, each on half of the query
+// columns (warps 0-7; producer 8, MMA 9).  All waits are bounded (see
+// fa_ptx.cuh).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <math.h>
@@ -35,7 +40,7 @@ constexpr int BT = 128;                // rows of every tile
 constexpr int HALF_BYTES = 128 * 128;  // 128 rows x 64 elements x 2 bytes
 constexpr int QS = 64;                 // query rows of a dkdv sub-tile
 constexpr int SUB_HALF = QS * 128;     // 64 rows x 64 elements x 2 bytes
-constexpr int THREADS = 192;           // warps 0-3 elementwise, 4 producer, 5 MMA
+constexpr int THREADS = 192;           // dq: warps 0-3 elementwise, 4 producer, 5 MMA
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int KRING = 3, VRING = 2;    // dq kernel: K and V tile rings
 constexpr float LOG2E = 1.4426950408889634f;
@@ -46,6 +51,10 @@ struct Cfg {
   static constexpr int TILE_BYTES = HALVES * HALF_BYTES;  // one 128-row tile
   static constexpr int NSTAGE_DQ = 5;    // dq: K ring (KRING slots) + V ring (VRING slots)
   static constexpr int NSTAGE_DKV = 4;   // (Q, dO) sub-tile ring of the dkdv kernel
+  // dkdv element-wise warps: 8 at D = 64 (measured +15 % there), 4 at D = 128
+  // (where 8 measured 2 % slower: its MMAs already set the pace).
+  static constexpr int DKV_EW = D == 64 ? 8 : 4;
+  static constexpr int DKV_THREADS = (DKV_EW + 2) * 32;
   static constexpr int SMEM_BAR = 512;
   static constexpr int SMEM_DQ = 1024 + 2 * TILE_BYTES + NSTAGE_DQ * TILE_BYTES + SMEM_BAR;
   // dkdv stage: a 64-row Q sub-tile and its dO sub-tile (1 KiB aligned); the
@@ -595,7 +604,7 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
 //   S(u), dP(u), [wait P/dS(u-1)], dV(u-1), dK(u-1), S(u+1), ...
 // ------------------------------------------------------------------------------
 template <int D, typename T>
-__global__ void __launch_bounds__(bw::THREADS, 1)
+__global__ void __launch_bounds__(bw::Cfg<D>::DKV_THREADS, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV,
@@ -604,6 +613,13 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
   constexpr bool kBF16 = BIsBF16<T>::value;
   constexpr int NS = C::NSTAGE_DKV;
   constexpr int QS = bw::QS;
+  constexpr int EW = C::DKV_EW;                 // element-wise warps 0 .. EW-1
+  constexpr int PRODUCER = EW, MMA = EW + 1;    // then the producer and MMA warps
+  // 16-bit P^T / dS^T of query half h start at column PST * h of S^T / dP^T.
+  // With 8 warps, two threads share each TMEM lane, one per half, and each
+  // writes within the 32 columns it has read (PST = 32); with 4, one thread
+  // owns the lane and the halves pack contiguously (PST = 16).
+  constexpr int PST = EW == 8 ? 32 : 16;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sK = smem;
@@ -612,11 +628,11 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
   float* sLD = reinterpret_cast<float*>(sStage + NS * C::STAGE_DKV);  // [NS][lse*log2e, Delta][QS]
   uint64_t* bars = reinterpret_cast<uint64_t*>(sLD + NS * 2 * QS);
   uint64_t* full = bars;          // [NS]: producer (expect_tx) + producer (after lse/Delta)
-  uint64_t* empty = bars + NS;    // [NS]: MMA commit + 128 element-wise arrivals
+  uint64_t* empty = bars + NS;    // [NS]: MMA commit + one arrival per element-wise thread
   uint64_t* kv_full = bars + 2 * NS;
   uint64_t* kv_empty = kv_full + 1;
   uint64_t* st_full = kv_full + 2;  // [2] S^T and dP^T of buffer b in TMEM
-  uint64_t* pd_full = kv_full + 4;  // [2] P^T and dS^T of buffer b in TMEM (128 arrivals)
+  uint64_t* pd_full = kv_full + 4;  // [2] P^T and dS^T of buffer b in TMEM (all element-wise threads)
   uint64_t* o_full = kv_full + 6;   // dK, dV complete
   uint64_t* drain = kv_full + 7;
   uint64_t* sched_full = kv_full + 8;                // [kSchedSlots]
@@ -629,24 +645,24 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(&full[s], 2);
-      mbar_init(&empty[s], 1 + bw::BT);
+      mbar_init(&empty[s], 1 + EW * 32);
     }
     mbar_init(kv_full, 1);
     mbar_init(kv_empty, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&st_full[i], 1);
-      mbar_init(&pd_full[i], bw::BT);
+      mbar_init(&pd_full[i], EW * 32);
     }
     mbar_init(o_full, 1);
     mbar_init(drain, 1);
     for (int i = 0; i < kSchedSlots; ++i) {
       mbar_init(&sched_full[i], 1);
-      mbar_init(&sched_empty[i], 5);
+      mbar_init(&sched_empty[i], EW + 1);
     }
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == MMA) {
     tmem_alloc(tmem_holder, bw::TMEM_COLS);
     tmem_relinquish();
   }
@@ -671,7 +687,7 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
   uint32_t prod_st = 0, prod_kv_par = 0;
   bool prod_kv_any = false;
 
-  if (warp == 4) {
+  if (warp == PRODUCER) {
     // ================================ producer ================================
     if (leader) {
       tma_prefetch_desc(&tmQ);
@@ -748,7 +764,7 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == MMA) {
     // ================================== MMA ===================================
     // Lane 0 alone runs the issuer loop; the other lanes wait at the
     // __syncwarp below (the warp reconverges before the CTA barrier and
@@ -772,12 +788,15 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
           mma_ss_lh(tmem + d_col, a0 + ka16, sd_hi, b0 + kb16, sd_hi, IDESC_S, k > 0 ? 1u : 0u);
         }
       };
-      // acc += A (TMEM, 16-bit, 64 columns of K) x B (64-row sub-tile, MN-major).
+      // acc += A (TMEM, 16-bit) x B (64-row sub-tile, MN-major).  A's 64 query
+      // columns are two halves of 32, half h packed from column PST * h, so
+      // k-steps 2h and 2h + 1 read columns PST * h and PST * h + 8.
       auto issue_acc = [&](uint32_t d_col, uint32_t a_col, uint32_t b_addr, bool accumulate) {
         const uint32_t b0 = (uint32_t)sdesc_sw128(b_addr, bw::SUB_HALF, 1024);
 #pragma unroll
         for (int k = 0; k < QS / 16; ++k) {
-          mma_ts_lh(tmem + d_col, tmem + a_col + k * 8, b0 + (uint32_t)((k * 16 * 128) >> 4),
+          mma_ts_lh(tmem + d_col, tmem + a_col + (k >> 1) * PST + (k & 1) * 8,
+                    b0 + (uint32_t)((k * 16 * 128) >> 4),
                     sd_hi, IDESC_ACC, (accumulate || k > 0) ? 1u : 0u);
         }
       };
@@ -831,9 +850,14 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
     }
     __syncwarp();
   } else {
-    // ======================= P^T and dS^T (warps 0-3) =======================
-    const int r = warp * 32 + lane;  // TMEM lane = key row within the tile
-    const uint32_t t_lane = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    // ================== P^T and dS^T (element-wise warps) ==================
+    // Warp w serves TMEM lane quarter w % 4.  With 8 warps, warp w takes the
+    // query half w / 4 of each sub-tile; with 4, each thread takes both.  The
+    // pass is element-wise given lse and Delta, so the halves never talk.
+    constexpr int NH = 8 / EW;                // query halves per thread
+    const int quarter = warp & 3, qh0 = EW == 8 ? warp >> 2 : 0;
+    const int r = quarter * 32 + lane;  // TMEM lane = key row within the tile
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     uint32_t ph_cnt = 0, gcnt = 0, o_cnt = 0;
     bool ok = true;
     T* const DK = static_cast<T*>(p.dk);
@@ -873,57 +897,59 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
           // which only a sub-tile on the diagonal has.
           const int ic_lo = p.causal ? j - off - qs * QS : 0;
           const bool edge = __any_sync(0xffffffffu, ic_lo > 0);
-          const uint32_t cs = bb * 128, cdp = bb * 128 + 64;
-          // Software-pipelined TMEM reads: chunk q + 1 in flight while chunk q
-          // is computed.
-          uint32_t sr[2][32], pr[2][32];
-          tmem_ld32(t_lane + cs, sr[0]);
-          tmem_ld32(t_lane + cdp, pr[0]);
-          tmem_wait_ld();
-          reg_fence32(sr[0]);
-          reg_fence32(pr[0]);
-#pragma unroll
-          for (int q2 = 0; q2 < QS / 32; ++q2) {
-            const int cur = q2 & 1;
-            if (q2 + 1 < QS / 32) {
-              tmem_ld32(t_lane + cs + (q2 + 1) * 32, sr[cur ^ 1]);
-              tmem_ld32(t_lane + cdp + (q2 + 1) * 32, pr[cur ^ 1]);
-            }
+          // P^T, dS^T of query half qh from registers sr / pr (its S^T, dP^T),
+          // stored 16-bit from column PST * qh: over columns this thread has
+          // already read, never over another thread's.
+          auto half_pass = [&](int qh, const uint32_t (&sr)[32], const uint32_t (&pr)[32]) {
             uint32_t pp[16], pd[16];
 #pragma unroll
             for (int x4 = 0; x4 < 8; ++x4) {
               // lse*log2(e) and Delta of 4 query columns (broadcast loads).
-              const float4 l4 = reinterpret_cast<const float4*>(sL)[q2 * 8 + x4];
-              const float4 d4 = reinterpret_cast<const float4*>(sD)[q2 * 8 + x4];
+              const float4 l4 = reinterpret_cast<const float4*>(sL)[qh * 8 + x4];
+              const float4 d4 = reinterpret_cast<const float4*>(sD)[qh * 8 + x4];
 #pragma unroll
               for (int h = 0; h < 2; ++h) {
-                const int x = x4 * 2 + h;  // column pair within the 32-column chunk
+                const int x = x4 * 2 + h;  // column pair within the half
                 const float2 nl = h ? make_float2(-l4.z, -l4.w) : make_float2(-l4.x, -l4.y);
                 const float2 nd = h ? make_float2(-d4.z, -d4.w) : make_float2(-d4.x, -d4.y);
-                const float2 a = __ffma2_rn(make_float2(__uint_as_float(sr[cur][2 * x]),
-                                                        __uint_as_float(sr[cur][2 * x + 1])),
+                const float2 a = __ffma2_rn(make_float2(__uint_as_float(sr[2 * x]),
+                                                        __uint_as_float(sr[2 * x + 1])),
                                             c2, nl);
                 float2 pv = make_float2(fast_exp2(a.x), fast_exp2(a.y));
                 if (edge) {
-                  const int col = q2 * 32 + 2 * x;
+                  const int col = qh * 32 + 2 * x;
                   pv.x = col < ic_lo ? 0.f : pv.x;
                   pv.y = col + 1 < ic_lo ? 0.f : pv.y;
                 }
-                const float2 dd = __fadd2_rn(make_float2(__uint_as_float(pr[cur][2 * x]),
-                                                         __uint_as_float(pr[cur][2 * x + 1])),
+                const float2 dd = __fadd2_rn(make_float2(__uint_as_float(pr[2 * x]),
+                                                         __uint_as_float(pr[2 * x + 1])),
                                              nd);
                 const float2 ds = __fmul2_rn(pv, dd);
                 pp[x] = BPack<T>::pack(pv.x, pv.y);
                 pd[x] = BPack<T>::pack(ds.x, ds.y);
               }
             }
-            tmem_st16(t_lane + cs + q2 * 16, pp);
-            tmem_st16(t_lane + cdp + q2 * 16, pd);
-            if (q2 + 1 < QS / 32) {
-              tmem_wait_ld();
-              reg_fence32(sr[cur ^ 1]);
-              reg_fence32(pr[cur ^ 1]);
-            }
+            tmem_st16(t_lane + bb * 128 + qh * PST, pp);
+            tmem_st16(t_lane + bb * 128 + 64 + qh * PST, pd);
+          };
+          uint32_t sr[NH][32], pr[NH][32];
+          tmem_ld32(t_lane + bb * 128 + qh0 * 32, sr[0]);
+          tmem_ld32(t_lane + bb * 128 + 64 + qh0 * 32, pr[0]);
+          tmem_wait_ld();
+          reg_fence32(sr[0]);
+          reg_fence32(pr[0]);
+          if constexpr (NH == 1) {
+            half_pass(qh0, sr[0], pr[0]);
+          } else {
+            // Both halves: the second half's reads are in flight while the
+            // first half is computed.
+            tmem_ld32(t_lane + bb * 128 + 32, sr[NH - 1]);
+            tmem_ld32(t_lane + bb * 128 + 96, pr[NH - 1]);
+            half_pass(0, sr[0], pr[0]);
+            tmem_wait_ld();
+            reg_fence32(sr[NH - 1]);
+            reg_fence32(pr[NH - 1]);
+            half_pass(1, sr[NH - 1], pr[NH - 1]);
           }
           tmem_wait_st();
           tc_fence_before();
@@ -932,7 +958,8 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
         }
       }
       if (!ok) break;
-      // Epilogue: dV, dK (= scale * accumulator) of this thread's key row.
+      // Epilogue: dV, dK (= scale * accumulator) of this thread's key row; with
+      // 8 warps, each warp of a lane quarter stores half of the D columns.
       if (!(ok = mbar_wait(o_full, o_cnt & 1, abort_flag, &g_backward_err, 8))) break;
       ++o_cnt;
       __syncwarp();
@@ -944,8 +971,10 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
         T* const row =
             (which ? DK : DV) + (((size_t)b * p.Sk + (row_ok ? j : 0)) * p.Hkv + hkv) * D;
         const float mul = which ? p.scale : 1.f;
+        constexpr int NQ = (D / 32) / (EW / 4);  // 32-column chunks per thread
 #pragma unroll
-        for (int q4 = 0; q4 < D / 32; ++q4) {
+        for (int qq = 0; qq < NQ; ++qq) {
+          const int q4 = qh0 * NQ + qq;
           uint32_t ar[32];
           if (any) {
             tmem_ld32(t_lane + (which ? COL_DK : COL_DV) + q4 * 32, ar);
@@ -977,13 +1006,13 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == MMA) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, bw::TMEM_COLS);
   }
   // Aborted CTA: wait, bounded, for the loads that may still be in flight.
-  if (warp == 4 && *abort_flag) {
+  if (warp == PRODUCER && *abort_flag) {
     const uint32_t first = prod_st > (uint32_t)NS ? prod_st - NS : 0u;
     for (uint32_t u = first; u < prod_st; ++u) mbar_wait_drain(&full[u % NS], (u / NS) & 1);
     if (prod_kv_any) mbar_wait_drain(kv_full, prod_kv_par);
@@ -1064,7 +1093,7 @@ static int launch_backward_t(const void* q, const void* k, const void* v, const 
   p.work_ctr = ctr + 1;
   if (p.n_items > 0) {
     const int grid = p.n_items < sms ? p.n_items : sms;
-    bwd_dkdv_kernel<D, T><<<grid, bw::THREADS, C::SMEM_DKV, stream>>>(tq64, tk, tv, tdo64, p);
+    bwd_dkdv_kernel<D, T><<<grid, C::DKV_THREADS, C::SMEM_DKV, stream>>>(tq64, tk, tv, tdo64, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
