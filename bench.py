@@ -572,12 +572,23 @@ def cpu_baseline(budget_s=15.0):
             "cpu": cpu_model()}
 
 
+# Arm CPU part numbers (implementer 0x41) of server cores, for a readable name.
+ARM_PARTS = {"0xd0c": "Neoverse-N1", "0xd40": "Neoverse-V1", "0xd49": "Neoverse-N2",
+             "0xd4f": "Neoverse-V2", "0xd8e": "Neoverse-N3", "0xd84": "Neoverse-V3"}
+
+
 def cpu_model():
+    """The host CPU's model: the x86 model name, or the Arm core's part name."""
     try:
         with open("/proc/cpuinfo") as f:
             for ln in f:
-                if ln.lower().startswith(("model name", "cpu part")):
-                    return ln.split(":", 1)[1].strip()
+                key, _, val = ln.partition(":")
+                key, val = key.strip().lower(), val.strip()
+                if key == "model name":
+                    return val
+                if key == "cpu part":
+                    name = ARM_PARTS.get(val.lower())
+                    return f"Arm {name} (CPU part {val})" if name else f"Arm CPU part {val}"
     except Exception:
         pass
     return os.uname().machine
