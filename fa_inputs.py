@@ -78,6 +78,20 @@ def prefill_inputs(B, Hq, Hkv, Sq, Sk, D, dtype=torch.bfloat16, seed=0):
     return q, k, v
 
 
+def sparse_q_prefill_inputs(rows, Hkv, Sk, D, B=1, dtype=torch.bfloat16, seed=0):
+    """For a query tensor too large to draw on the host: only the listed query
+    rows get values, every other row of q is left zero by the caller.
+
+    rows: int64 [n, 3] of (b, h, i).  Returns q_rows [n, D] (the rows' values,
+    in the order of ``rows``) and k/v [B, Sk, Hkv, D], i.i.d. N(0, 1) rounded
+    to dtype, drawn in that order from the seed."""
+    g = torch.Generator().manual_seed(seed)
+    q_rows = _randn(g, (len(rows), D), dtype)
+    k = _randn(g, (B, Sk, Hkv, D), dtype)
+    v = _randn(g, (B, Sk, Hkv, D), dtype)
+    return q_rows, k, v
+
+
 def prefill_inputs_for(shape: PrefillShape, seed=0):
     return prefill_inputs(shape.B, shape.Hq, shape.Hkv, shape.Sq, shape.Sk, shape.D,
                           shape.dtype, seed)
