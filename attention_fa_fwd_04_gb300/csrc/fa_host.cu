@@ -90,7 +90,14 @@ int pipe_for_device(Pipe** out) {
     if (!r) r = make_event(&p->start);
     if (!r) r = make_event(&p->kv);
     if (!r) r = make_event(&p->done);
-    if (r) return r;  // (the partly built pipe is dropped; the call fails)
+    if (r) {  // the call fails: release what was created
+      for (cudaStream_t s : {p->up, p->comp, p->down})
+        if (s) cudaStreamDestroy(s);
+      for (cudaEvent_t ev : {p->start, p->kv, p->done})
+        if (ev) cudaEventDestroy(ev);
+      delete p;
+      return r;
+    }
     pipes[dev] = p;
   }
   *out = pipes[dev];
@@ -145,7 +152,10 @@ extern "C" int fa_prefill_fwd_host(const void* q_host, const void* k_host, const
     cudaEvent_t a = nullptr, c = nullptr;
     r = make_event(&a);
     if (!r) r = make_event(&c);
-    if (r) return fa::record_cuda_status(r, "host prefill event set-up");
+    if (r) {
+      if (a) cudaEventDestroy(a);
+      return fa::record_cuda_status(r, "host prefill event set-up");
+    }
     pp->ev_q.push_back(a);
     pp->ev_o.push_back(c);
   }
