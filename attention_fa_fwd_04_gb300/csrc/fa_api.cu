@@ -255,7 +255,7 @@ extern "C" int fa_decode_paged_fwd(const void* q, const void* kpages, const void
     return cuda_status(fa::launch_decode_layout(q, kpages, vpages, ly, o, lse, B, Hq, Hkv, D,
                                                 scale, nullptr, 0, stream),
                        "paged decode zero-fill launch");
-  const size_t nf = fa::decode_scratch_floats(B, Hq, Hkv, cap, D, Sq);
+  const size_t nf = fa::decode_scratch_floats(B, Hq, Hkv, cap, D, Sq, true);
   void* scratch = nullptr;
   cudaError_t e = cudaMallocAsync(&scratch, nf * sizeof(float), stream);
   if (e != cudaSuccess) return cuda_status(e, "paged decode cudaMallocAsync");

@@ -56,10 +56,14 @@ constexpr int PREFETCH_BYTES = 384 * 1024;
 // must never run ahead by a phase: if two warps shared a stage, the faster one
 // could see the stage's previous phase as "complete" and consume a tile that
 // has not landed.)
-template <int D>
+// PAGED: the paged (batched) decode streams long ranges from HBM, where the
+// bytes in flight per SM set the rate: its ring is 192 KiB deep.  The
+// single-sequence decode keeps 128 KiB, which leaves room beside it for the
+// combine's CTAs.
+template <int D, bool PAGED = false>
 struct Cfg {
   static constexpr int HALVES = D / 64;
-  static constexpr int NSTAGE = (D == 128) ? 8 : 16;    // 128 KiB of tiles in flight
+  static constexpr int NSTAGE = (D == 128) ? (PAGED ? 12 : 8) : (PAGED ? 24 : 16);
   static constexpr int KV_BYTES = HALVES * HALF_BYTES;  // one K (or V) tile
   static constexpr int STAGE_BYTES = 2 * KV_BYTES;      // K tile + V tile
   static constexpr int SMEM_STAGES = NSTAGE * STAGE_BYTES;
@@ -68,6 +72,7 @@ struct Cfg {
   static constexpr int SMEM_BAR = 2 * NSTAGE * 8 + 16 + NSTAGE * 4;
   static_assert(HALF_BYTES % 1024 == 0, "128-byte-swizzled tiles need 1 KiB alignment");
   static constexpr int SMEM_TOTAL = 1024 + SMEM_STAGES + SMEM_RED + SMEM_BAR;
+  static_assert(SMEM_TOTAL <= 227 * 1024, "shared memory per CTA");
 };
 }  // namespace dec
 
@@ -84,6 +89,11 @@ struct DecodeParams {
   __nv_bfloat16* o;          // [B, Hq, D]
   float* lse;                // [B, Hq] natural-log log-sum-exp per head, or null
   int B, Hq, Hkv, cap, G, nsplit, n_hb;
+  // Balanced splits (paged caches only): the grid is nsplit CTAs in x, and
+  // each finds its (sequence, kv head, row block, split) from the lengths;
+  // partials are indexed by CTA (part_o [nsplit, HB, D], part_ml
+  // [nsplit, HB, 2]).  0: the grid is (nsplit, Hkv * n_hb, B).
+  int balanced;
   // New query tokens per sequence (paged path; 1 otherwise).  The MMA's 16
   // rows are (token, head) pairs r = s * G + g of one kv head; token s sees
   // the keys [0, L - Sq + s] (bottom-right causal).
@@ -97,6 +107,88 @@ __device__ __forceinline__ size_t decode_qrow(const DecodeParams& p, int b, int 
                                               int Sq) {
   const int s = r / p.G, g = r - s * p.G;
   return ((size_t)b * Sq + s) * p.Hq + (size_t)hkv * p.G + g;
+}
+
+// Balanced splits for a batch of sequences of different lengths (the lengths
+// are device data, so the host cannot size the splits).  A unit is one
+// (sequence, kv head, row block); a unit of sequence b has T_b = ceil(L_b / TT)
+// K/V tiles.  Each unit of b gets S_b = ceil(T_b / lam) splits, lam being the
+// smallest tile budget per split for which all units' splits fit the nsplit
+// CTAs (binary search; lam = max T_b always fits, since there are fewer units
+// than CTAs).  So no split holds more than lam tiles, and lam is within about
+// one tile per unit of the even share.  The units of b take the CTAs (and
+// partial slots) sP[b] + j * S_b + k, j = hkv * n_hb + hb, k < S_b.
+// Block-cooperative, one thread per sequence (B <= blockDim.x); every thread
+// of the block must call it, after griddepcontrol.wait; ends with
+// __syncthreads().  sRed: 2 * warps entries.
+__device__ void balanced_splits(const DecodeParams& p, int* sS, int* sP, long long* sRed) {
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5, nw = (blockDim.x + 31) >> 5;
+  const int U = p.Hkv * p.n_hb;
+  int T = 0;
+  if (t < p.B) {
+    int L = p.valid_len[(size_t)t * p.len_stride];
+    L = L < 0 ? 0 : (L > p.cap ? p.cap : L);
+    T = (L + dec::TT - 1) / dec::TT;
+  }
+  // Block sum of a (per thread) and block max of m, into every thread.
+  auto reduce = [&](long long a, long long m, long long* sum, long long* mx) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      a += __shfl_xor_sync(0xffffffffu, a, o);
+      const long long y = __shfl_xor_sync(0xffffffffu, m, o);
+      m = y > m ? y : m;
+    }
+    __syncthreads();  // the previous round's values have been read
+    if (lane == 0) {
+      sRed[2 * warp] = a;
+      sRed[2 * warp + 1] = m;
+    }
+    __syncthreads();
+    long long s2 = 0, m2 = 0;
+    for (int w = 0; w < nw; ++w) {
+      s2 += sRed[2 * w];
+      m2 = sRed[2 * w + 1] > m2 ? sRed[2 * w + 1] : m2;
+    }
+    *sum = s2;
+    *mx = m2;
+  };
+  long long all_tiles, max_t;
+  reduce((long long)T * U, T, &all_tiles, &max_t);
+  long long lam = 1;
+  if (all_tiles > 0) {
+    long long lo = (all_tiles + p.nsplit - 1) / p.nsplit, hi = max_t;
+    if (lo < 1) lo = 1;
+    if (lo > hi) lo = hi;
+    while (lo < hi) {  // block-uniform: every thread sees the same sums
+      const long long mid = (lo + hi) / 2;
+      long long need, unused;
+      reduce(T > 0 ? (long long)U * ((T + mid - 1) / mid) : 0, 0, &need, &unused);
+      if (need <= p.nsplit)
+        hi = mid;
+      else
+        lo = mid + 1;
+    }
+    lam = lo;
+  }
+  const int S = T > 0 ? (int)((T + lam - 1) / lam) : 0;
+  // Exclusive prefix sum of U * S over the sequences.
+  const int v = U * S;
+  int inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += y;
+  }
+  __syncthreads();  // every thread has read sRed above
+  if (lane == 31) sRed[warp] = inc;
+  __syncthreads();
+  int before = 0;
+  for (int w = 0; w < warp; ++w) before += (int)sRed[w];
+  if (t < p.B) {
+    sS[t] = S;
+    sP[t] = before + inc - v;
+  }
+  __syncthreads();
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -120,7 +212,7 @@ template <int D, bool PAGED, int NB>
 __global__ void __launch_bounds__(dec::THREADS, 1)
     decode_split_kernel(const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const DecodeParams p) {
-  using C = dec::Cfg<D>;
+  using C = dec::Cfg<D, PAGED>;
   constexpr int TT = dec::TT, NSTAGE = C::NSTAGE, HB = dec::HB, NW = dec::NWARPS;
   constexpr int RB = 8 * NB;  // query rows of this CTA (HB is the buffers' row stride)
   static_assert(RB <= HB, "row blocks must fit the merge buffers");
@@ -139,9 +231,11 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
   volatile int* stage_bad = abort_flag + 4;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int split = blockIdx.x;
-  const int hkv = blockIdx.y / p.n_hb, hb = blockIdx.y % p.n_hb;
-  const int b = blockIdx.z;
+  // This CTA's sequence, kv head, row block and split: from the grid, or in
+  // balanced mode from the lengths once they can be read (below).
+  int split = blockIdx.x;
+  int hkv = blockIdx.y / p.n_hb, hb = blockIdx.y % p.n_hb;
+  int b = blockIdx.z;
 
   // The combine grid may become resident now; it blocks until this grid ends.
   pdl_launch_dependents();
@@ -187,11 +281,49 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
   // grid in the stream to complete.
   pdl_wait_primary();
 
-  int L = PAGED ? p.valid_len[(size_t)b * p.len_stride] : *p.valid_len;
+  int nsplit = p.nsplit;  // splits of this CTA's unit
+  bool idle = false;      // balanced mode: a CTA beyond the splits in use
+  if constexpr (PAGED) {
+    if (p.balanced) {
+      // The merge buffers are free until the end: scratch for the assignment.
+      int* sS = reinterpret_cast<int*>(red_o);
+      int* sP = sS + dec::THREADS;
+      int* sRes = sP + dec::THREADS;
+      long long* sRed = reinterpret_cast<long long*>(sRes + 8);
+      if (threadIdx.x == 0) sRes[0] = -1;
+      balanced_splits(p, sS, sP, sRed);
+      const int c = blockIdx.x, U = p.Hkv * p.n_hb;
+      if (threadIdx.x < p.B) {
+        const int t = threadIdx.x, S = sS[t], first = sP[t];
+        if (S > 0 && c >= first && c < first + U * S) {
+          sRes[0] = t;
+          sRes[1] = (c - first) / S;
+          sRes[2] = (c - first) % S;
+          sRes[3] = S;
+        }
+      }
+      __syncthreads();
+      if (sRes[0] < 0) {
+        idle = true;
+        b = 0;
+        hkv = 0;
+        hb = 0;
+        split = 0;
+        nsplit = 1;
+      } else {
+        b = sRes[0];
+        hkv = sRes[1] / p.n_hb;
+        hb = sRes[1] % p.n_hb;
+        split = sRes[2];
+        nsplit = sRes[3];
+      }
+    }
+  }
+  int L = idle ? 0 : (PAGED ? p.valid_len[(size_t)b * p.len_stride] : *p.valid_len);
   const int Sq = PAGED ? p.Sq : 1;  // compile-time 1 on the contiguous path
   L = L < 0 ? 0 : (L > p.cap ? p.cap : L);
   const int tiles_total = (L + TT - 1) / TT;
-  const int tps = (tiles_total + p.nsplit - 1) / p.nsplit;
+  const int tps = (tiles_total + nsplit - 1) / nsplit;
   const int t_begin = split * tps;
   int n_tiles = tiles_total - t_begin;
   n_tiles = n_tiles < 0 ? 0 : (n_tiles > tps ? tps : n_tiles);
@@ -449,8 +581,16 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
   int nh = (Sq * p.G - hb * RB) < RB ? (Sq * p.G - hb * RB) : RB;
   // Query row of CTA row `row` (partials and outputs are indexed by it).
   auto qrow = [&](int row) { return decode_qrow(p, b, hkv, hb * RB + row, Sq); };
+  // Partial slot of CTA row `row`: (query row, split), or in balanced mode
+  // (CTA, row).
+  const bool bal = PAGED && p.balanced;
+  auto pslot = [&](int row) -> size_t {
+    return bal ? (size_t)blockIdx.x * HB + row : qrow(row) * p.nsplit + split;
+  };
+  if (idle) nh = 0;  // no unit: nothing to write
   // Self-check: partial rows must lie inside the scratch (records and skips).
-  if (b >= p.B || split >= p.nsplit ||
+  if (b >= p.B || split >= nsplit || (!bal && split >= p.nsplit) ||
+      (bal && (int)blockIdx.x >= p.nsplit) ||
       (nh > 0 && qrow(nh - 1) >= (size_t)p.B * Sq * p.Hq)) {
     if (threadIdx.x == 0) atomicOr(&g_decode_err, kErrBounds);
     nh = 0;
@@ -468,8 +608,8 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
       red_w[w * HB + row] = wt;
       Ls += red_ml[(w * HB + row) * 2 + 1] * wt;
     }
-    p.part_ml[(qrow(row) * p.nsplit + split) * 2 + 0] = M;
-    p.part_ml[(qrow(row) * p.nsplit + split) * 2 + 1] = Ls;
+    p.part_ml[pslot(row) * 2 + 0] = M;
+    p.part_ml[pslot(row) * 2 + 1] = Ls;
   }
   __syncthreads();
   for (int x = threadIdx.x; x < nh * (D / 4); x += dec::THREADS) {
@@ -484,7 +624,7 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
       o.z += v.z * wt;
       o.w += v.w * wt;
     }
-    reinterpret_cast<float4*>(p.part_o + (qrow(row) * p.nsplit + split) * D)[d4] = o;
+    reinterpret_cast<float4*>(p.part_o + pslot(row) * D)[d4] = o;
   }
   // Aborted CTA (a wait gave up, in any warp, possibly after the producer
   // issued its last tile): wait, bounded, for the loads that may still be in
@@ -511,7 +651,9 @@ constexpr int kCombineThreads = kCombineWarps * 32;
 constexpr int kMaxSplits = kCombineThreads;
 constexpr int kSplitsPerWarp = kMaxSplits / kCombineWarps;
 
-template <int D>
+// BAL: balanced splits (paged batches); a separate instantiation, so the
+// contiguous decode's combine carries none of the assignment code.
+template <int D, bool BAL>
 __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const DecodeParams p) {
   // A programmatic dependent launched after this grid (the next call's split
   // kernel) may start its prologue now; it waits for this grid to complete
@@ -528,18 +670,35 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const D
     if (t == 0) atomicOr(&g_decode_err, kErrBounds << 4);
     return;
   }
-  const size_t base = ((size_t)b * p.Sq * p.Hq + h) * p.nsplit;  // h: row in [Sq, Hq]
+  // Partials of this row (h: row in [Sq, Hq]): split k at slot base + k * step.
+  size_t base = ((size_t)b * p.Sq * p.Hq + h) * p.nsplit;
+  size_t step = 1;
+  int ns = p.nsplit;
+  if constexpr (BAL) {
+    __shared__ int sS[kCombineThreads], sP[kCombineThreads];
+    __shared__ long long sTot[2 * kCombineWarps];
+    if (p.B > kCombineThreads) {  // the assignment takes one thread per sequence
+      if (t == 0) atomicOr(&g_decode_err, kErrBounds << 4);
+      return;
+    }
+    balanced_splits(p, sS, sP, sTot);
+    const int s = h / p.Hq, hq = h - s * p.Hq, hkv = hq / p.G;
+    const int r = s * p.G + (hq - hkv * p.G), hb = r / dec::HB;
+    ns = sS[b];
+    base = (size_t)(sP[b] + (hkv * p.n_hb + hb) * ns) * dec::HB + (r - hb * dec::HB);
+    step = dec::HB;
+  }
   float ov[kSplitsPerWarp];
 #pragma unroll
   for (int k = 0; k < kSplitsPerWarp; ++k) {
     const int sp = warp + k * kCombineWarps;
-    ov[k] = (sp < p.nsplit && d < D) ? p.part_o[(base + sp) * D + d] : 0.f;
+    ov[k] = (sp < ns && d < D) ? p.part_o[(base + sp * step) * D + d] : 0.f;
   }
   // (max, sum) of split t as one 8-byte load: selecting on the sum after a
   // second, dependent load would cost a second L2 round trip.
   float m_t = -INFINITY, l_t = 0.f;
-  if (t < p.nsplit) {
-    const float2 ml = reinterpret_cast<const float2*>(p.part_ml)[base + t];
+  if (t < ns) {
+    const float2 ml = reinterpret_cast<const float2*>(p.part_ml)[base + t * step];
     l_t = ml.y;
     m_t = l_t > 0.f ? ml.x : -INFINITY;
   }
@@ -563,7 +722,7 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const D
 #pragma unroll
   for (int k = 0; k < kSplitsPerWarp; ++k) {
     const int sp = warp + k * kCombineWarps;
-    if (sp < p.nsplit) acc += ov[k] * sW[sp];
+    if (sp < ns) acc += ov[k] * sW[sp];
   }
   sAcc[warp][lane] = acc;
   __syncthreads();
@@ -607,7 +766,23 @@ static int decode_nsplit(int B, int Hq, int Hkv, int cap, int Sq) {
   return (int)ns;
 }
 
-size_t decode_scratch_floats(int B, int Hq, int Hkv, int cap, int D, int Sq) {
+// Balanced splits for a paged batch: only when its units fit in fewer CTAs
+// than the SMs (the lengths can then differ per sequence and the grid can
+// still cover every SM); the CTA count is the SM count.
+static bool decode_balanced(int B, int Hq, int Hkv, int Sq, bool paged) {
+  if (!paged) return false;
+  const int G = Hq / Hkv;
+  const int n_hb = (Sq * G + dec::HB - 1) / dec::HB;
+  const long units = (long)B * Hkv * n_hb;
+  const int sms = sm_count() > 0 ? sm_count() : 148;
+  return units < sms && sms <= kMaxSplits && B <= dec::THREADS;
+}
+
+size_t decode_scratch_floats(int B, int Hq, int Hkv, int cap, int D, int Sq, bool paged) {
+  if (decode_balanced(B, Hq, Hkv, Sq, paged)) {
+    const size_t sms = (size_t)(sm_count() > 0 ? sm_count() : 148);
+    return sms * dec::HB * ((size_t)D + 2);
+  }
   const size_t ns = (size_t)decode_nsplit(B, Hq, Hkv, cap, Sq);
   return (size_t)B * Sq * Hq * ns * ((size_t)D + 2);
 }
@@ -616,7 +791,8 @@ template <int D>
 static int launch_decode_t(const void* q, const void* kc, const void* vc, const DecodeLayout& ly,
                            void* o, float* lse, int B, int Hq, int Hkv, float scale,
                            float* scratch, cudaStream_t stream) {
-  using C = dec::Cfg<D>;
+  using CC = dec::Cfg<D, false>;  // contiguous caches
+  using CP = dec::Cfg<D, true>;   // paged caches
   const bool paged = ly.page_table != nullptr;
   const int cap = paged ? ly.max_pages * ly.page_size : ly.cap;
   CUtensorMap tk, tv;
@@ -637,17 +813,20 @@ static int launch_decode_t(const void* q, const void* kc, const void* vc, const 
                               (const void*)decode_split_kernel<D, false, 2>,
                               (const void*)decode_split_kernel<D, true, 1>,
                               (const void*)decode_split_kernel<D, true, 2>};
+    const int smem[4] = {CC::SMEM_TOTAL, CC::SMEM_TOTAL, CP::SMEM_TOTAL, CP::SMEM_TOTAL};
     cudaError_t e = cudaSuccess;
-    for (const void* k : kernels) {
-      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_TOTAL);
+    for (int i = 0; i < 4; ++i) {
+      e = cudaFuncSetAttribute(kernels[i], cudaFuncAttributeMaxDynamicSharedMemorySize, smem[i]);
       if (e != cudaSuccess) return e;
     }
     // Same shared-memory carveout as the split kernel, so that combine CTAs
     // can become resident beside split CTAs and wait there.
-    e = cudaFuncSetAttribute(decode_combine_kernel<D>,
-                             cudaFuncAttributePreferredSharedMemoryCarveout,
-                             (int)cudaSharedmemCarveoutMaxShared);
-    if (e != cudaSuccess) return e;
+    for (const void* k : {(const void*)decode_combine_kernel<D, false>,
+                          (const void*)decode_combine_kernel<D, true>}) {
+      e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               (int)cudaSharedmemCarveoutMaxShared);
+      if (e != cudaSuccess) return e;
+    }
     attr_set[dev] = 1;
   }
   DecodeParams p;
@@ -659,9 +838,11 @@ static int launch_decode_t(const void* q, const void* kc, const void* vc, const 
   p.max_pages = ly.max_pages;
   p.num_pages = ly.num_pages;
   const int Sq = paged ? ly.Sq : 1;
-  const int ns = decode_nsplit(B, Hq, Hkv, cap, Sq);
+  const bool bal = decode_balanced(B, Hq, Hkv, Sq, paged);
+  const int ns = bal ? (sm_count() > 0 ? sm_count() : 148) : decode_nsplit(B, Hq, Hkv, cap, Sq);
   p.part_o = scratch;
-  p.part_ml = scratch + (size_t)B * Sq * Hq * ns * D;
+  p.part_ml = scratch + (bal ? (size_t)ns * dec::HB * D : (size_t)B * Sq * Hq * ns * D);
+  p.balanced = bal ? 1 : 0;
   p.Sq = Sq;
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;
@@ -680,9 +861,9 @@ static int launch_decode_t(const void* q, const void* kc, const void* vc, const 
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t sc = {};
-  sc.gridDim = dim3(ns, Hkv * p.n_hb, B);
+  sc.gridDim = bal ? dim3(ns, 1, 1) : dim3(ns, Hkv * p.n_hb, B);
   sc.blockDim = dim3(dec::THREADS, 1, 1);
-  sc.dynamicSmemBytes = C::SMEM_TOTAL;
+  sc.dynamicSmemBytes = paged ? CP::SMEM_TOTAL : CC::SMEM_TOTAL;
   sc.stream = stream;
   sc.attrs = attr;
   sc.numAttrs = 1;
@@ -704,7 +885,8 @@ static int launch_decode_t(const void* q, const void* kc, const void* vc, const 
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, decode_combine_kernel<D>, p);
+  e = bal ? cudaLaunchKernelEx(&cfg, decode_combine_kernel<D, true>, p)
+          : cudaLaunchKernelEx(&cfg, decode_combine_kernel<D, false>, p);
   return e;
 }
 
@@ -720,7 +902,8 @@ int launch_decode_layout(const void* q, const void* kc, const void* vc, const De
     return cudaGetLastError();
   }
   const int Sq = ly.page_table ? ly.Sq : 1;
-  if (scratch_floats < decode_scratch_floats(B, Hq, Hkv, cap, D, Sq)) return cudaErrorInvalidValue;
+  if (scratch_floats < decode_scratch_floats(B, Hq, Hkv, cap, D, Sq, ly.page_table != nullptr))
+    return cudaErrorInvalidValue;
   if (D == 64)
     return launch_decode_t<64>(q, kc, vc, ly, o, lse, B, Hq, Hkv, scale, scratch, stream);
   return launch_decode_t<128>(q, kc, vc, ly, o, lse, B, Hq, Hkv, scale, scratch, stream);

@@ -57,7 +57,8 @@ int launch_decode_layout(const void* q, const void* kc, const void* vc, const De
                          float* scratch, size_t scratch_floats, cudaStream_t stream);
 
 // Scratch floats the decode needs for these sizes (Sq new tokens per sequence).
-size_t decode_scratch_floats(int B, int Hq, int Hkv, int cap, int D, int Sq = 1);
+size_t decode_scratch_floats(int B, int Hq, int Hkv, int cap, int D, int Sq = 1,
+                             bool paged = false);
 
 // Enqueue the backward pass: Delta into `delta` ([B, Hq, Sq] fp32 scratch, then
 // two uint32 work counters),

@@ -288,7 +288,9 @@ def run_ours(args, rank, world, local_rank):
     # ---------------- end to end through the C ABI with host buffers ----------------
     e2e = run_e2e(args, fa, torch, dev, q_h, k_h, v_h, sh, stream, dist)
     varlen = run_varlen(args, fa, torch, dev, sh, stream)
+    prefill_lse = run_prefill_lse(args, fa, torch, dev, q, k, v, sh, stream)
     backward = run_backward(args, fa, torch, dev, q, k, v, sh, stream)
+    paged = run_paged(args, fa, torch, dev, sh, stream)
 
     if rank != 0:
         if dist:
@@ -387,11 +389,13 @@ def run_ours(args, rank, world, local_rank):
         },
         "e2e": e2e,
         "varlen": varlen,
+        "prefill_lse": prefill_lse,
         "backward": backward,
+        "paged_decode": paged,
         "gpu_launches": (5 + 2 * (n_r1 + n_r2)) * K,
         "gpu_launches_note": f"per step: 1 prefill + {2 + n_r1 + n_r2} decode calls x "
-                             "(split + combine); the varlen and e2e runs follow the timed "
-                             "region",
+                             "(split + combine); the e2e, varlen, prefill_lse, backward and "
+                             "paged_decode runs follow the timed region",
         "clocks": clk,
         "wall_s_timed": round(wall, 3),
     }
@@ -439,6 +443,82 @@ def run_varlen(args, fa, torch, dev, sh, stream):
             "workload": f"packed causal prefill, {len(lens)} sequences, lengths {lens} "
                         f"({tq} tokens), Hq{Hq}/Hkv{Hkv} D{D} bf16",
             "flop_convention": "sum_b 2*Hq*Sq_b*Sk_b*D (causal)", "launches": n}
+
+
+def run_paged(args, fa, torch, dev, sh, stream):
+    """Batched decode over a paged cache (fa_decode_paged_fwd): 16 sequences
+    with seeded lengths in [1, 65536], 256-token pages in a seeded random
+    physical order, Hq 8 / Hkv 2, D 128, bf16; one new token per sequence, and
+    again with 4 (speculative decoding).  A call reads every sequence's valid
+    K/V, about 0.5 GB (several times L2), so every call streams from HBM."""
+    lens = fa_inputs.varlen_lengths(n=16, max_len=DECODE.cap, seed=0)
+    Hq, Hkv, D, page = DECODE.Hq, DECODE.Hkv, DECODE.D, 256
+    nbytes = sum(2 * L * Hkv * D * 2 for L in lens)
+    pk, _ = peaks()
+    res = {"workload": f"paged decode, {len(lens)} sequences, lengths {lens} "
+                       f"({sum(lens)} tokens), page size {page}, Hq{Hq}/Hkv{Hkv} D{D} bf16",
+           "bytes_per_call": nbytes, "unit": "GB/s"}
+    for sq in (1, 4):
+        q, kp, vp, table, sl = fa_inputs.paged_decode_batch(lens, sq, Hq, Hkv, D, page, seed=0,
+                                                            device=dev)
+        out = torch.empty_like(q)
+
+        def call():
+            fa.decode_paged(q, kp, vp, table, sl, DECODE.scale, out=out, stream=stream)
+        for _ in range(3):
+            call()
+        n = max(3, min(args.steps, 20))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(n):
+            call()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        st, detail = fa.fa_device_error()
+        if st != fa.FA_OK:
+            raise RuntimeError(f"device error word {detail:#x} in the paged decode run")
+        t = e0.elapsed_time(e1) / 1e3 / n
+        gbs = nbytes / t / 1e9
+        entry = {"value": round(gbs, 1), "us": round(t * 1e6, 2), "launches": n,
+                 "roofline": {"bound": "hbm", "achieved": round(gbs, 1),
+                              "peak": pk["hbm_gbs"], "unit": "GB/s",
+                              "frac": round(gbs / pk["hbm_gbs"], 4)}}
+        if sq == 1:
+            res.update(entry)
+        else:
+            res[f"new_tokens_{sq}"] = entry
+        del q, kp, vp, table, sl, out
+    return res
+
+
+def run_prefill_lse(args, fa, torch, dev, q, k, v, sh, stream):
+    """The headline prefill through fa_prefill_fwd_lse (O and each row's
+    log-sum-exp): events around back-to-back calls, inputs larger than L2."""
+    B, Hq, Hkv, S, D = PREFILL.B, PREFILL.Hq, PREFILL.Hkv, PREFILL.Sq, PREFILL.D
+    o = torch.empty_like(q)
+    lse = torch.empty(B, Hq, S, dtype=torch.float32, device=dev)
+
+    def launch():
+        st = fa.fa_prefill_fwd_lse(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                   lse.data_ptr(), B, Hq, Hkv, S, S, D, PREFILL.scale, 1,
+                                   fa.FA_BF16, sh)
+        if st:
+            raise fa.FAError(st, "fa_prefill_fwd_lse")
+    for _ in range(2):
+        launch()
+    n = max(3, min(args.steps, 10))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(n):
+        launch()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t = e0.elapsed_time(e1) / 1e3 / n
+    return {"value": round(PREFILL.flops / t / 1e12, 2), "unit": "TFLOP/s",
+            "ms": round(t * 1e3, 4), "launches": n,
+            "workload": PREFILL.name + " with the log-sum-exp output"}
 
 
 def run_backward(args, fa, torch, dev, q, k, v, sh, stream):

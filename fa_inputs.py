@@ -189,6 +189,41 @@ def decode_inputs_for(shape: DecodeShape, seed=0, L=None):
                          seed, L)
 
 
+def paged_decode_batch(lens, Sq, Hq, Hkv, D, page_size, seed=0, device="cuda", spare_pages=8):
+    """A batch of sequences in a paged bf16 KV cache, drawn on ``device`` (the
+    pages are large; torch's generator of that device, seeded).
+
+    Sequence b holds lens[b] tokens (its Sq new ones included) in
+    ceil(lens[b] / page_size) pages taken in a seeded random physical order;
+    every slot past a length and every spare page is the bf16 NaN 0x7FC0.
+    Returns q [B, Sq, Hq, D], kpages, vpages [num_pages, page_size, Hkv, D],
+    page_table int32 [B, max_pages] (unused entries 0) and seqlens int32 [B]."""
+    B = len(lens)
+    n_pages = [(L + page_size - 1) // page_size for L in lens]
+    num_pages, max_pages = sum(n_pages) + spare_pages, max(1, max(n_pages))
+    g_host = torch.Generator().manual_seed(seed)
+    perm = torch.randperm(num_pages, generator=g_host)
+    table = torch.zeros(B, max_pages, dtype=torch.int32)
+    used = 0
+    for b, n in enumerate(n_pages):
+        table[b, :n] = perm[used:used + n].to(torch.int32)
+        used += n
+    g = torch.Generator(device=device).manual_seed(seed)
+    kp = torch.randn(num_pages, page_size, Hkv, D, generator=g, device=device).to(torch.bfloat16)
+    vp = torch.randn(num_pages, page_size, Hkv, D, generator=g, device=device).to(torch.bfloat16)
+    q = torch.randn(B, Sq, Hq, D, generator=g, device=device).to(torch.bfloat16)
+    nan = poison_value(torch.bfloat16).to(device)
+    for b, L in enumerate(lens):
+        if L % page_size:
+            last = int(table[b, n_pages[b] - 1])
+            kp[last, L % page_size:] = nan
+            vp[last, L % page_size:] = nan
+    spare = perm[used:].to(device)
+    kp[spare] = nan
+    vp[spare] = nan
+    return q, kp, vp, table.to(device), torch.tensor(lens, dtype=torch.int32, device=device)
+
+
 def poison_value(dtype) -> torch.Tensor:
     """A scalar NaN of the given dtype; for bf16 exactly the bit pattern 0x7FC0."""
     if dtype == torch.bfloat16:

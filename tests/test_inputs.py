@@ -44,3 +44,25 @@ def test_flop_convention():
     s = fa_inputs.GQA_CAUSAL_8K
     assert s.flops == 2 * 1 * 128 * 8192 * 8192 * 128
     assert fa_inputs.RAGGED_NONCAUSAL.flops == 4 * 2 * 8 * 1000 * 1536 * 64
+
+
+def test_paged_decode_batch_layout():
+    """Valid tokens are finite and sit in their sequence's pages in order;
+    every slot past a length and every spare page is the bf16 NaN 0x7FC0."""
+    lens = [1, 33, 64, 100]
+    q, kp, vp, table, sl = fa_inputs.paged_decode_batch(lens, 2, 8, 2, 64, 32, seed=0,
+                                                        device="cpu")
+    assert q.shape == (4, 2, 8, 64) and sl.tolist() == lens
+    used = set()
+    for b, L in enumerate(lens):
+        for t in range(-(-L // 32) * 32):
+            pid = int(table[b, t // 32])
+            used.add(pid)
+            finite = bool(torch.isfinite(kp[pid, t % 32].float()).all()) and \
+                bool(torch.isfinite(vp[pid, t % 32].float()).all())
+            assert finite == (t < L), (b, t)
+    spare = [p for p in range(kp.shape[0]) if p not in used]
+    assert len(spare) == 8
+    for p in spare:
+        assert bool((kp[p].view(torch.int16) == 0x7FC0).all())
+        assert bool((vp[p].view(torch.int16) == 0x7FC0).all())
