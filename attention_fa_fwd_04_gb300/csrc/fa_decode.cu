@@ -92,8 +92,11 @@ struct DecodeParams {
   // Balanced splits (paged caches only): the grid is nsplit CTAs in x, and
   // each finds its (sequence, kv head, row block, split) from the lengths;
   // partials are indexed by CTA (part_o [nsplit, HB, D], part_ml
-  // [nsplit, HB, 2]).  0: the grid is (nsplit, Hkv * n_hb, B).
+  // [nsplit, HB, 2]), and CTA 0 writes unit_map[u] = (first CTA, splits) of
+  // every unit u = (b * Hkv + hkv) * n_hb + hb for the combine.  0: the grid
+  // is (nsplit, Hkv * n_hb, B).
   int balanced;
+  int2* unit_map;
   // New query tokens per sequence (paged path; 1 otherwise).  The MMA's 16
   // rows are (token, head) pairs r = s * G + g of one kv head; token s sees
   // the keys [0, L - Sq + s] (bottom-right causal).
@@ -293,6 +296,10 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
       if (threadIdx.x == 0) sRes[0] = -1;
       balanced_splits(p, sS, sP, sRed);
       const int c = blockIdx.x, U = p.Hkv * p.n_hb;
+      if (c == 0 && threadIdx.x < p.B) {  // the combine's map of every unit
+        const int t = threadIdx.x;
+        for (int j = 0; j < U; ++j) p.unit_map[t * U + j] = make_int2(sP[t] + j * sS[t], sS[t]);
+      }
       if (threadIdx.x < p.B) {
         const int t = threadIdx.x, S = sS[t], first = sP[t];
         if (S > 0 && c >= first && c < first + U * S) {
@@ -340,6 +347,15 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
     // Paged caches: lane l holds the page id of logical page pg_base + l, so
     // the page-table reads of 32 pages cost one load latency.
     int pg_base = -(1 << 30), pid_lane = 0;
+    // Paged caches: the page of the next tile and the tile's row in it.  Tiles
+    // advance by TT tokens and page_size is a multiple of TT, so they step
+    // without a division per tile (the producer's issue rate paces long
+    // streams).
+    int page = 0, pos = 0;
+    if constexpr (PAGED) {
+      page = t_begin * TT / p.page_size;
+      pos = t_begin * TT - page * p.page_size;
+    }
     int t = 0;
     for (; t < n_tiles; ++t) {
       const int s = t % NSTAGE;
@@ -347,7 +363,6 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
       const int tok = (t_begin + t) * TT;
       int row = tok, tb = b, bad = 0;  // tensor-map row / batch coordinates of the tile
       if constexpr (PAGED) {
-        const int page = tok / p.page_size;
         if (page < pg_base || page >= pg_base + 32) {  // warp-uniform
           pg_base = page;
           const int pg = pg_base + lane;
@@ -355,8 +370,13 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
         }
         const int pid = __shfl_sync(0xffffffffu, pid_lane, page - pg_base);
         bad = (pid < 0 || pid >= p.num_pages) ? 1 : 0;
-        row = tok - page * p.page_size;
+        row = pos;
         tb = bad ? 0 : pid;  // a bad id loads page 0, and the tile is masked
+        pos += TT;
+        if (pos == p.page_size) {
+          pos = 0;
+          ++page;
+        }
       }
       if (!mbar_wait<true>(&empty[s], ph ^ 1, abort_flag, &g_decode_err, 1)) break;
       if (leader) {
@@ -675,18 +695,17 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const D
   size_t step = 1;
   int ns = p.nsplit;
   if constexpr (BAL) {
-    __shared__ int sS[kCombineThreads], sP[kCombineThreads];
-    __shared__ long long sTot[2 * kCombineWarps];
-    if (p.B > kCombineThreads) {  // the assignment takes one thread per sequence
-      if (t == 0) atomicOr(&g_decode_err, kErrBounds << 4);
-      return;
-    }
-    balanced_splits(p, sS, sP, sTot);
+    // The split grid's CTA 0 mapped this row's unit to its CTAs (partials).
     const int s = h / p.Hq, hq = h - s * p.Hq, hkv = hq / p.G;
     const int r = s * p.G + (hq - hkv * p.G), hb = r / dec::HB;
-    ns = sS[b];
-    base = (size_t)(sP[b] + (hkv * p.n_hb + hb) * ns) * dec::HB + (r - hb * dec::HB);
+    const int2 um = p.unit_map[((size_t)b * p.Hkv + hkv) * p.n_hb + hb];
+    ns = um.y < 0 ? 0 : (um.y > p.nsplit ? p.nsplit : um.y);
+    base = (size_t)(um.x < 0 ? 0 : um.x) * dec::HB + (r - hb * dec::HB);
     step = dec::HB;
+    if (um.x < 0 || um.x + ns > p.nsplit) {  // self-check: inside the partials
+      if (t == 0) atomicOr(&g_decode_err, kErrBounds << 4);
+      ns = 0;
+    }
   }
   float ov[kSplitsPerWarp];
 #pragma unroll
@@ -781,7 +800,8 @@ static bool decode_balanced(int B, int Hq, int Hkv, int Sq, bool paged) {
 size_t decode_scratch_floats(int B, int Hq, int Hkv, int cap, int D, int Sq, bool paged) {
   if (decode_balanced(B, Hq, Hkv, Sq, paged)) {
     const size_t sms = (size_t)(sm_count() > 0 ? sm_count() : 148);
-    return sms * dec::HB * ((size_t)D + 2);
+    const size_t units = (size_t)B * Hkv * ((Sq * (Hq / Hkv) + dec::HB - 1) / dec::HB);
+    return sms * dec::HB * ((size_t)D + 2) + 2 * units + 2;  // + the unit map (int2, aligned)
   }
   const size_t ns = (size_t)decode_nsplit(B, Hq, Hkv, cap, Sq);
   return (size_t)B * Sq * Hq * ns * ((size_t)D + 2);
@@ -843,6 +863,10 @@ static int launch_decode_t(const void* q, const void* kc, const void* vc, const 
   p.part_o = scratch;
   p.part_ml = scratch + (bal ? (size_t)ns * dec::HB * D : (size_t)B * Sq * Hq * ns * D);
   p.balanced = bal ? 1 : 0;
+  {  // the unit map follows the partials, 8-byte aligned
+    const size_t off = (size_t)ns * dec::HB * (D + 2);
+    p.unit_map = bal ? reinterpret_cast<int2*>(scratch + off + (off & 1)) : nullptr;
+  }
   p.Sq = Sq;
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;
