@@ -671,9 +671,7 @@ constexpr int kCombineThreads = kCombineWarps * 32;
 constexpr int kMaxSplits = kCombineThreads;
 constexpr int kSplitsPerWarp = kMaxSplits / kCombineWarps;
 
-// BAL: balanced splits (paged batches); a separate instantiation, so the
-// contiguous decode's combine carries none of the assignment code.
-template <int D, bool BAL>
+template <int D>
 __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const DecodeParams p) {
   // A programmatic dependent launched after this grid (the next call's split
   // kernel) may start its prologue now; it waits for this grid to complete
@@ -690,34 +688,19 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const D
     if (t == 0) atomicOr(&g_decode_err, kErrBounds << 4);
     return;
   }
-  // Partials of this row (h: row in [Sq, Hq]): split k at slot base + k * step.
-  size_t base = ((size_t)b * p.Sq * p.Hq + h) * p.nsplit;
-  size_t step = 1;
-  int ns = p.nsplit;
-  if constexpr (BAL) {
-    // The split grid's CTA 0 mapped this row's unit to its CTAs (partials).
-    const int s = h / p.Hq, hq = h - s * p.Hq, hkv = hq / p.G;
-    const int r = s * p.G + (hq - hkv * p.G), hb = r / dec::HB;
-    const int2 um = p.unit_map[((size_t)b * p.Hkv + hkv) * p.n_hb + hb];
-    ns = um.y < 0 ? 0 : (um.y > p.nsplit ? p.nsplit : um.y);
-    base = (size_t)(um.x < 0 ? 0 : um.x) * dec::HB + (r - hb * dec::HB);
-    step = dec::HB;
-    if (um.x < 0 || um.x + ns > p.nsplit) {  // self-check: inside the partials
-      if (t == 0) atomicOr(&g_decode_err, kErrBounds << 4);
-      ns = 0;
-    }
-  }
+  const size_t base = ((size_t)b * p.Sq * p.Hq + h) * p.nsplit;  // h: row in [Sq, Hq]
+  const int ns = p.nsplit;
   float ov[kSplitsPerWarp];
 #pragma unroll
   for (int k = 0; k < kSplitsPerWarp; ++k) {
     const int sp = warp + k * kCombineWarps;
-    ov[k] = (sp < ns && d < D) ? p.part_o[(base + sp * step) * D + d] : 0.f;
+    ov[k] = (sp < ns && d < D) ? p.part_o[(base + sp) * D + d] : 0.f;
   }
   // (max, sum) of split t as one 8-byte load: selecting on the sum after a
   // second, dependent load would cost a second L2 round trip.
   float m_t = -INFINITY, l_t = 0.f;
   if (t < ns) {
-    const float2 ml = reinterpret_cast<const float2*>(p.part_ml)[base + t * step];
+    const float2 ml = reinterpret_cast<const float2*>(p.part_ml)[base + t];
     l_t = ml.y;
     m_t = l_t > 0.f ? ml.x : -INFINITY;
   }
@@ -759,6 +742,84 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const D
       p.lse[(size_t)b * p.Sq * p.Hq + h] = dsum > 0.f ? 0.6931471805599453f * (M + __log2f(dsum))
                                                : -INFINITY;
   }
+}
+
+// Combine for balanced splits (paged batches): one warp per output row
+// (b, s, hq), lane l holding columns [l * D/32, (l + 1) * D/32).  The row's
+// unit lists its splits' partials (unit map from the split grid's first CTA);
+// a row has few of them, so they are loaded four at a time and merged online:
+// running max M, and the output and the sum l rescaled by 2^(M_old - M_new)
+// when M grows -- O = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s as in the
+// other combine.  Splits with l_s == 0 get weight 0.  No shared memory and no
+// block barrier: a block is 8 independent rows.
+constexpr int kRowWarps = 8;
+template <int D>
+__global__ void __launch_bounds__(kRowWarps * 32) decode_combine_rows_kernel(const DecodeParams p) {
+  pdl_launch_dependents();
+  pdl_wait_primary();
+  constexpr int CPL = D / 32;  // columns per lane
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const size_t row = (size_t)blockIdx.x * kRowWarps + warp;  // in [B, Sq, Hq]
+  const size_t rows_per_b = (size_t)p.Sq * p.Hq;
+  if (row >= (size_t)p.B * rows_per_b) return;
+  const int b = (int)(row / rows_per_b), h = (int)(row - (size_t)b * rows_per_b);
+  const int s = h / p.Hq, hq = h - s * p.Hq, hkv = hq / p.G;
+  const int r = s * p.G + (hq - hkv * p.G), hb = r / dec::HB;
+  const int2 um = p.unit_map[((size_t)b * p.Hkv + hkv) * p.n_hb + hb];
+  int ns = um.y;
+  if (um.x < 0 || ns < 0 || um.x + ns > p.nsplit) {  // self-check: inside the partials
+    if (lane == 0) atomicOr(&g_decode_err, kErrBounds << 4);
+    ns = 0;
+  }
+  const size_t base = (size_t)(um.x < 0 ? 0 : um.x) * dec::HB + (r - hb * dec::HB);
+  float M = -INFINITY, den = 0.f, acc[CPL];
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) acc[c] = 0.f;
+  for (int k0 = 0; k0 < ns; k0 += 4) {
+    float2 ml[4];
+    float ov[4][CPL];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {  // every load of the batch before any use
+      const size_t slot = base + (size_t)(k0 + u) * dec::HB;
+      if (k0 + u < ns) {
+        ml[u] = reinterpret_cast<const float2*>(p.part_ml)[slot];
+        const float* src = p.part_o + slot * D + lane * CPL;
+        if constexpr (CPL == 4) {
+          const float4 v = *reinterpret_cast<const float4*>(src);
+          ov[u][0] = v.x; ov[u][1] = v.y; ov[u][2] = v.z; ov[u][3] = v.w;
+        } else {
+          const float2 v = *reinterpret_cast<const float2*>(src);
+          ov[u][0] = v.x; ov[u][1] = v.y;
+        }
+      } else {
+        ml[u] = make_float2(-INFINITY, 0.f);
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) ov[u][c] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float m_u = ml[u].y > 0.f ? ml[u].x : -INFINITY;
+      if (m_u > M) {  // rescale what was merged so far (M = -inf: nothing yet)
+        const float f = M == -INFINITY ? 0.f : fast_exp2(M - m_u);
+        den *= f;
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) acc[c] *= f;
+        M = m_u;
+      }
+      const float w = m_u == -INFINITY ? 0.f : fast_exp2(m_u - M);
+      den += w * ml[u].y;
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) acc[c] += w * ov[u][c];
+    }
+  }
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+  __nv_bfloat16* dst = p.o + row * D + lane * CPL;
+#pragma unroll
+  for (int c = 0; c < CPL; c += 2)
+    *reinterpret_cast<uint32_t*>(dst + c) = pack_bf16(acc[c] * inv, acc[c + 1] * inv);
+  if (p.lse && lane == 0)
+    p.lse[row] = den > 0.f ? 0.6931471805599453f * (M + __log2f(den)) : -INFINITY;
 }
 
 // Degenerate cache (cap == 0): every output is zero, every log-sum-exp -inf.
@@ -841,8 +902,8 @@ static int launch_decode_t(const void* q, const void* kc, const void* vc, const 
     }
     // Same shared-memory carveout as the split kernel, so that combine CTAs
     // can become resident beside split CTAs and wait there.
-    for (const void* k : {(const void*)decode_combine_kernel<D, false>,
-                          (const void*)decode_combine_kernel<D, true>}) {
+    for (const void* k : {(const void*)decode_combine_kernel<D>,
+                          (const void*)decode_combine_rows_kernel<D>}) {
       e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
                                (int)cudaSharedmemCarveoutMaxShared);
       if (e != cudaSuccess) return e;
@@ -903,14 +964,16 @@ static int launch_decode_t(const void* q, const void* kc, const void* vc, const 
   if (e != cudaSuccess) return e;
 
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((D + 31) / 32, Sq * Hq, B);
-  cfg.blockDim = dim3(kCombineThreads, 1, 1);
+  const size_t n_rows = (size_t)B * Sq * Hq;
+  cfg.gridDim = bal ? dim3((unsigned)((n_rows + kRowWarps - 1) / kRowWarps), 1, 1)
+                    : dim3((D + 31) / 32, Sq * Hq, B);
+  cfg.blockDim = dim3(bal ? kRowWarps * 32 : kCombineThreads, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = bal ? cudaLaunchKernelEx(&cfg, decode_combine_kernel<D, true>, p)
-          : cudaLaunchKernelEx(&cfg, decode_combine_kernel<D, false>, p);
+  e = bal ? cudaLaunchKernelEx(&cfg, decode_combine_rows_kernel<D>, p)
+          : cudaLaunchKernelEx(&cfg, decode_combine_kernel<D>, p);
   return e;
 }
 

@@ -67,7 +67,10 @@ def test_paged_decode_against_oracle(fa, B, Hq, Hkv, D, page_size, max_pages, le
 
 def test_paged_with_one_page_per_sequence_matches_contiguous_decode(fa):
     """page_size = cap, page_table[b] = b: the paged path reads the same tiles
-    as fa_decode_fwd, so with one shared length the outputs are identical."""
+    as fa_decode_fwd.  The two merge their splits in a different order (the
+    paged rows online, one warp per row), so the outputs agree to the last
+    rounding: within 2 bf16 ulps of the largest output, and both match the
+    oracle.  A tile read from the wrong place moves an output by O(1)."""
     B, Hq, Hkv, cap, D = 2, 8, 2, 4096, 128
     q, kc, vc, L = fa_inputs.decode_inputs(B, Hq, Hkv, cap, D, seed=31, L=3000)
     dev = torch.device("cuda", 0)
@@ -78,7 +81,10 @@ def test_paged_with_one_page_per_sequence_matches_contiguous_decode(fa):
     lens = torch.full((B,), L, dtype=torch.int32, device=dev)
     got = fa.decode_paged(qd, kd, vd, table, lens, 0.088)
     torch.cuda.synchronize()
-    assert torch.equal(got, ref)
+    g, r = got.float().cpu(), ref.float().cpu()
+    assert (g - r).abs().max().item() <= 2 * 2.0 ** -8 * r.abs().max().item()
+    want = oracle.decode(q, kc, vc, L, 0.088)
+    compare(g.numpy().reshape(want.shape), want)
 
 
 def test_paged_bad_page_id_is_masked_and_reported(fa):
