@@ -128,3 +128,27 @@ def test_paged_decode_several_new_tokens(fa, B, Sq, Hq, Hkv, D, page_size, max_p
                                      return_lse=True)
     compare(o, ref)
     lse_compare(l, ref_l)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,D", [
+    (75, 4, 2, 64),    # 150 (sequence, kv head) units: balanced splits, scan over 3 warps
+    (76, 4, 2, 64),    # 152 units, as many as SMs on GB300: splits sized from the capacity
+    (150, 4, 1, 128),  # the largest batch with balanced splits on 152 SMs: 5 warps of sequences
+])
+def test_paged_decode_large_ragged_batches(fa, B, Hq, Hkv, D):
+    """Many sequences of different lengths (some empty) on 32-token pages:
+    with fewer units than SMs the kernels size each sequence's splits from the
+    lengths on the device; with more, from the capacity.  Both must match the
+    oracle for every sequence, and every output must be finite."""
+    g = torch.Generator().manual_seed(B + Hkv)
+    lens = [0 if x < 40 else int(x) for x in torch.randint(0, 700, (B,), generator=g).tolist()]
+    page_size, max_pages = 32, 22
+    q, kp, vp, table, L = paged_inputs(B, Hq, Hkv, D, page_size, max_pages, lens, seed=B * 7,
+                                       spare_pages=3)
+    scale = 1 / math.sqrt(D)
+    got, lse = run_paged(fa, q, kp, vp, table, L, scale)
+    assert np.isfinite(got).all()
+    want, want_lse = oracle.decode_paged(q, kp, vp, table.tolist(), L.tolist(), scale,
+                                         return_lse=True)
+    compare(got, want)
+    lse_compare(lse, want_lse)
