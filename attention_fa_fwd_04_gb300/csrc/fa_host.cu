@@ -64,9 +64,14 @@ std::vector<Piece> plan(int B, int Sq, int Sk, int causal, int n_pieces) {
 
 // Per device: the copy and compute streams and the events that order them,
 // created on first use and kept for the life of the process.  Calls on one
-// device enqueue under a lock (they share the streams and events).
+// device enqueue under a lock (they share the streams and events).  The
+// pieces' kernels alternate between two compute streams: a piece is a few
+// waves of work items, and the next piece's CTAs then take the SMs that the
+// current piece's last wave leaves idle.
+constexpr int kCompStreams = 2;
 struct Pipe {
-  cudaStream_t up = nullptr, comp = nullptr, down = nullptr;
+  cudaStream_t up = nullptr, down = nullptr;
+  cudaStream_t comp[kCompStreams] = {nullptr, nullptr};
   cudaEvent_t start = nullptr, kv = nullptr, done = nullptr;
   std::vector<cudaEvent_t> ev_q, ev_o;
   std::mutex mu;
@@ -85,13 +90,14 @@ int pipe_for_device(Pipe** out) {
   if (!pipes[dev]) {
     Pipe* p = new Pipe();
     int r = (int)cudaStreamCreateWithFlags(&p->up, cudaStreamNonBlocking);
-    if (!r) r = (int)cudaStreamCreateWithFlags(&p->comp, cudaStreamNonBlocking);
+    for (int c = 0; c < kCompStreams && !r; ++c)
+      r = (int)cudaStreamCreateWithFlags(&p->comp[c], cudaStreamNonBlocking);
     if (!r) r = (int)cudaStreamCreateWithFlags(&p->down, cudaStreamNonBlocking);
     if (!r) r = make_event(&p->start);
     if (!r) r = make_event(&p->kv);
     if (!r) r = make_event(&p->done);
     if (r) {  // the call fails: release what was created
-      for (cudaStream_t s : {p->up, p->comp, p->down})
+      for (cudaStream_t s : {p->up, p->comp[0], p->comp[1], p->down})
         if (s) cudaStreamDestroy(s);
       for (cudaEvent_t ev : {p->start, p->kv, p->done})
         if (ev) cudaEventDestroy(ev);
@@ -176,7 +182,7 @@ extern "C" int fa_prefill_fwd_host(const void* q_host, const void* k_host, const
   // caller's stream (including the allocation).
   e = cudaEventRecord(pp->start, stream);
   if (!e) e = cudaStreamWaitEvent(pp->up, pp->start, 0);
-  if (!e) e = cudaStreamWaitEvent(pp->comp, pp->start, 0);
+  for (int c = 0; c < kCompStreams && !e; ++c) e = cudaStreamWaitEvent(pp->comp[c], pp->start, 0);
   if (!e) e = cudaStreamWaitEvent(pp->down, pp->start, 0);
   // K and V first, then Q piece by piece.
   if (!e && bk) e = cudaMemcpyAsync(dk, k_host, bk, H2D, pp->up);
@@ -188,21 +194,23 @@ extern "C" int fa_prefill_fwd_host(const void* q_host, const void* k_host, const
                         (size_t)(ps[i].s1 - ps[i].s0) * row_q, H2D, pp->up);
     if (!e) e = cudaEventRecord(pp->ev_q[i], pp->up);
   }
-  // One prefill per piece, each as soon as its Q rows have landed.
-  if (!e) e = cudaStreamWaitEvent(pp->comp, pp->kv, 0);
+  // One prefill per piece, each as soon as its Q rows have landed, on the
+  // compute streams in turn.
+  for (int c = 0; c < kCompStreams && !e; ++c) e = cudaStreamWaitEvent(pp->comp[c], pp->kv, 0);
   for (size_t i = 0; i < ps.size() && !e; ++i) {
     const Piece& c = ps[i];
+    cudaStream_t cs = pp->comp[i % kCompStreams];
     const size_t qo = ((size_t)c.b * Sq + c.s0) * row_q, kv = (size_t)c.b * Sk * row_k;
-    e = cudaStreamWaitEvent(pp->comp, pp->ev_q[i], 0);
+    e = cudaStreamWaitEvent(cs, pp->ev_q[i], 0);
     if (!e) {
       const int lr = fa::launch_prefill(dq + qo, dk + kv, dv + kv, dout + qo, nullptr, 1, Hq, Hkv,
-                                        c.s1 - c.s0, c.sk, D, scale, causal, bf16, pp->comp);
+                                        c.s1 - c.s0, c.sk, D, scale, causal, bf16, cs);
       if (lr) {
         e = (cudaError_t)lr;
         site = "host prefill launch";
       }
     }
-    if (!e) e = cudaEventRecord(pp->ev_o[i], pp->comp);
+    if (!e) e = cudaEventRecord(pp->ev_o[i], cs);
   }
   // O back piece by piece; the caller's stream joins the last download.
   for (size_t i = 0; i < ps.size() && !e; ++i) {
@@ -212,15 +220,16 @@ extern "C" int fa_prefill_fwd_host(const void* q_host, const void* k_host, const
       e = cudaMemcpyAsync(static_cast<uint8_t*>(o_host) + off, dout + off,
                           (size_t)(ps[i].s1 - ps[i].s0) * row_q, cudaMemcpyDeviceToHost, pp->down);
   }
-  // The down stream has waited for every piece's kernel (and the comp stream
-  // for every upload), so its last event orders all of the call's work.
+  // The down stream has waited for every piece's kernel (and the compute
+  // streams for every upload), so its last event orders all of the call's
+  // work.
   if (!e) e = cudaEventRecord(pp->done, pp->down);
   if (!e) e = cudaStreamWaitEvent(stream, pp->done, 0);
   if (e) {
     // Something failed part-way: let what was enqueued finish before the
     // buffer is released (the host waits here; failures only).
     cudaStreamSynchronize(pp->up);
-    cudaStreamSynchronize(pp->comp);
+    for (int c = 0; c < kCompStreams; ++c) cudaStreamSynchronize(pp->comp[c]);
     cudaStreamSynchronize(pp->down);
     const int st = fa::record_cuda_status((int)e, site);
     cudaFreeAsync(buf, stream);

@@ -613,7 +613,7 @@ def run_e2e(args, fa, torch, dev, q_h, k_h, v_h, sh, stream, dist):
             "call": "fa_prefill_fwd_host (C ABI), pinned host buffers",
             "note": f"pinned host q,k,v -> device -> pinned host O per step in one C call: "
                     f"K/V first, then {len(pieces)} query-row pieces whose uploads, prefill "
-                    f"kernels and downloads overlap on two copy streams and a compute stream"}
+                    f"kernels and downloads overlap on two copy streams and two compute streams"}
 
 
 # ----------------------------------------------------------------------------

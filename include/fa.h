@@ -305,8 +305,10 @@ int fa_backward(const void* q, const void* k, const void* v, const void* o,
  *
  * Device copies of q, k, v, o are allocated stream-ordered on `stream`
  * (2 * B * (Sq * Hq + Sk * Hkv) * D * 2 bytes, freed on `stream` after the
- * last download).  Two copy streams and a compute stream per device, created
- * on first use and kept, fork from `stream` and join it again: work already on
+ * last download).  Two copy streams and two compute streams per device (the
+ * pieces' kernels alternate between them, so each fills the SMs the other's
+ * last wave leaves idle), created on first use and kept, fork from `stream`
+ * and join it again: work already on
  * `stream` runs first, and `stream` waits for the last download, so o_host is
  * complete once `stream` reaches that point (the call itself does not
  * synchronise).  Calls on one device are enqueued one at a time.
