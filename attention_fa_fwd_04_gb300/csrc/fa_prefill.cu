@@ -101,6 +101,11 @@ struct SeqSpan {
   int tb;       // tensor-map batch coordinate
   int Sq, Sk;   // its lengths
   size_t orow;  // packed row index of its query row 0 (O is [rows, Hq, D])
+  // Packed sequences: 1 when the item is a head pair -- Q tile i is query
+  // head hq + i on the block's first 128 rows (a block with at most 128 rows,
+  // whose second tile would otherwise be empty); 0: tile i is rows
+  // [128 i, 128 i + 128) of the block, query head hq.
+  int pair;
 };
 
 // Work item w -> (b, hq, qb): kv-head-major, then batch, then query blocks in
@@ -139,18 +144,23 @@ __device__ __forceinline__ SeqSpan work_item(const PrefillParams& p, int w, int*
     s.Sq = p.Sq;
     s.Sk = p.Sk;
     s.orow = (size_t)*b * p.Sq;
+    s.pair = 0;
   } else {
     const int u = w / p.Hq;
-    *hq = w - u * p.Hq;
+    const int hh = w - u * p.Hq;
     const int4 a = p.units[2 * u], c = p.units[2 * u + 1];
     *qb = c.x;
     *b = c.y;
     s.q0 = a.x;
     s.k0 = a.y;
     s.tb = 0;
-    s.Sq = a.z;
     s.Sk = a.w;
     s.orow = (size_t)a.x;
+    s.pair = c.z;
+    // A head-pair unit's items h >= Hq / 2 are empty: no rows.
+    const bool empty = c.z && hh >= p.Hq / 2;
+    *hq = c.z ? (empty ? 0 : 2 * hh) : hh;
+    s.Sq = empty ? 0 : a.z;
   }
   return s;
 }
@@ -199,9 +209,13 @@ __device__ __forceinline__ int plan_bucket(int qb, const int4& sp, int causal) {
   return n < kPlanBuckets - 1 ? n : kPlanBuckets - 1;
 }
 
+// pair_heads (the GQA group size is even, so heads 2h and 2h + 1 read the
+// same K/V): a block of at most 128 rows becomes a head-pair unit, whose work
+// items h < Hq / 2 run heads 2h and 2h + 1 as its two Q tiles (the items
+// h >= Hq / 2 are empty), so its K/V steps run with both tiles full.
 __global__ void __launch_bounds__(kPlanThreads)
     varlen_plan_kernel(const int32_t* cu_q, const int32_t* cu_k, int B, int total_q, int total_k,
-                       int n_qb_max, int causal, int4* units, int* n_units,
+                       int n_qb_max, int causal, int pair_heads, int4* units, int* n_units,
                        unsigned int* work_ctr) {
   __shared__ int start[kPlanBuckets];  // counts, then each bucket's next list slot
   __shared__ int warp_sum[kPlanThreads / 32];
@@ -258,8 +272,9 @@ __global__ void __launch_bounds__(kPlanThreads)
     const int nb = (sp.z + pf::QBLOCK - 1) / pf::QBLOCK;
     for (int qb = 0; qb < nb; ++qb) {
       const int pos = atomicAdd(&start[plan_bucket(qb, sp, causal)], 1);
+      const int pair = pair_heads && sp.z - qb * pf::QBLOCK <= pf::BM ? 1 : 0;
       units[2 * pos] = sp;
-      units[2 * pos + 1] = make_int4(qb, b, 0, 0);
+      units[2 * pos + 1] = make_int4(qb, b, pair, 0);
     }
   }
   if (t == 0) {
@@ -407,7 +422,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       const int hkv = hq / p.G;
       const int row0 = qb * pf::QBLOCK;
       const int n0 = kv_tiles_for(row0, sq.Sq, sq.Sk, p.causal);
-      const int n1 = kv_tiles_for(row0 + pf::BM, sq.Sq, sq.Sk, p.causal);
+      const int n1 = kv_tiles_for(row0 + (sq.pair ? 0 : pf::BM), sq.Sq, sq.Sk, p.causal);
       const int n = n0 > n1 ? n0 : n1;
       if (local > 0 && !(ok = mbar_wait<POLL>(q_empty, (local - 1) & 1, abort_flag, &g_prefill_err, 1)))
         break;
@@ -418,7 +433,8 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
 #pragma unroll
           for (int h = 0; h < C::HALVES; ++h)
             tma_load_4d_hint(sQ + i * C::TILE_BYTES + h * pf::HALF_BYTES, &tmQ, q_full, h * 64,
-                             hq, sq.q0 + row0 + i * pf::BM, sq.tb, pol_q);
+                             hq + (sq.pair ? i : 0), sq.q0 + row0 + (sq.pair ? 0 : i * pf::BM),
+                             sq.tb, pol_q);
       }
       __syncwarp();
       q_par = local & 1;  // (Q of earlier items has landed: q_empty was waited for)
@@ -547,7 +563,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
         const SeqSpan sq = work_item<PACKED>(p, w, &b, &hq, &qb);
         const int row0 = qb * pf::QBLOCK;
         const int nt0 = kv_tiles_for(row0, sq.Sq, sq.Sk, p.causal);
-        const int nt1 = kv_tiles_for(row0 + pf::BM, sq.Sq, sq.Sk, p.causal);
+        const int nt1 = kv_tiles_for(row0 + (sq.pair ? 0 : pf::BM), sq.Sq, sq.Sk, p.causal);
         const int n = nt0 > nt1 ? nt0 : nt1;
         if (!(ok = mbar_wait<POLL>(q_full, local & 1, abort_flag, &g_prefill_err, 3))) break;
         tc_fence_after();
@@ -645,16 +661,17 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       int b, hq, qb;
       const SeqSpan sq = work_item<PACKED>(p, w, &b, &hq, &qb);
       const int Sq = sq.Sq, Sk = sq.Sk, off = Sk - Sq;  // bottom-right causal offset
-      const int row0 = qb * pf::QBLOCK + i * pf::BM;
+      const int row0 = qb * pf::QBLOCK + (sq.pair ? 0 : i * pf::BM);
+      const int hq_i = hq + (sq.pair ? i : 0);  // this tile's query head
       const int grow = row0 + r;
       const int n_i = kv_tiles_for(row0, Sq, Sk, p.causal);
-      T* const orow = O + (sq.orow + grow) * (size_t)p.Hq * D + (size_t)hq * D;
+      T* const orow = O + (sq.orow + grow) * (size_t)p.Hq * D + (size_t)hq_i * D;
       float* const lse_row =
-          p.lse ? p.lse + (PACKED ? (size_t)hq * p.total_q + sq.orow + grow
-                                  : ((size_t)b * p.Hq + hq) * p.Sq + grow)
+          p.lse ? p.lse + (PACKED ? (size_t)hq_i * p.total_q + sq.orow + grow
+                                  : ((size_t)b * p.Hq + hq_i) * p.Sq + grow)
                 : nullptr;
       // Self-check: the row must lie inside O (records and skips otherwise).
-      const bool row_ok = grow < Sq && b < p.B && hq < p.Hq &&
+      const bool row_ok = grow < Sq && b < p.B && hq_i < p.Hq &&
                           (!PACKED || sq.orow + grow < (size_t)p.total_q);
       if (n_i == 0) {
         if (row_ok) {
@@ -1057,9 +1074,10 @@ static int launch_prefill_shape(const void* q, const void* k, const void* v, voi
   int4* units = packed ? reinterpret_cast<int4*>(static_cast<uint8_t*>(ctr) + 16) : nullptr;
   int* n_units = packed ? reinterpret_cast<int*>(c + 2) : nullptr;
   if (e == cudaSuccess && packed) {
+    const int pair_heads = sh.Hkv > 0 && (sh.Hq / sh.Hkv) % 2 == 0 ? 1 : 0;
     varlen_plan_kernel<<<1, kPlanThreads, 0, stream>>>(sh.cu_q, sh.cu_k, sh.B, sh.total_q,
-                                                       sh.total_k, n_qb, causal, units, n_units,
-                                                       c);
+                                                       sh.total_k, n_qb, causal, pair_heads,
+                                                       units, n_units, c);
     e = cudaGetLastError();
   }
   int r = e;
