@@ -209,6 +209,13 @@ int fa_decode_fwd(const void* q, const void* kcache, const void* vcache,
  * slots past its length in its last page, may hold anything (NaN included).
  * A contiguous cache with per-sequence lengths is the case page_size = cap,
  * max_pages = 1, page_table[b] = b.  Other rules as fa_decode_fwd.
+ *
+ * Scheduling: while the batch has fewer (sequence, kv head) units than SMs,
+ * the kernels read the lengths on the device and give each sequence a number
+ * of splits in proportion to its length (one CTA per SM), so a batch of very
+ * different lengths keeps every SM streaming; otherwise each unit's share of
+ * the SMs is sized from the capacity.  Either way the lengths are never read
+ * on the host.
  */
 int fa_decode_paged_fwd(const void* q, const void* kpages, const void* vpages,
                         const int32_t* page_table, const int32_t* seqlens, void* o, float* lse,
