@@ -724,7 +724,9 @@ def run_profile_case(args, local_rank):
                      headline; Q+O = 256 MiB)
       decode_full:   the 65536-token decode, L2 flushed before every launch
       backward_small: fa_backward on B1 Hq64 Hkv4 S8192 D128 causal bf16 (the
-                     headline backward's kernels at half its query heads)"""
+                     headline backward's kernels at half its query heads)
+      paged_batch:   the paged decode of the bench's 16 ragged sequences, one new
+                     token each (585 MB of K/V per launch)"""
     import torch
     import attention_fa_fwd_04_gb300 as fa
     torch.cuda.set_device(local_rank)
@@ -764,6 +766,17 @@ def run_profile_case(args, local_rank):
                 raise fa.FAError(st, "fa_backward")
         work = {"workload": f"backward B{B} Hq{Hq} Hkv{Hkv} S{S} D{D} causal bf16",
                 "flops_per_launch": 2.5 * 2.0 * B * Hq * S * S * D}
+    elif args.profile == "paged_batch":
+        lens = fa_inputs.varlen_lengths(n=16, max_len=DECODE.cap, seed=0)
+        Hq, Hkv, D = DECODE.Hq, DECODE.Hkv, DECODE.D
+        q, kp, vp, table, sl = fa_inputs.paged_decode_batch(lens, 1, Hq, Hkv, D, 256, seed=0,
+                                                            device=dev)
+        out = torch.empty_like(q)
+        for _ in range(n):
+            fa.decode_paged(q, kp, vp, table, sl, DECODE.scale, out=out)
+        work = {"workload": f"paged decode, 16 sequences ({sum(lens)} tokens), page 256, "
+                            f"Hq{Hq}/Hkv{Hkv} D{D}",
+                "bytes_per_launch": sum(2 * L * Hkv * D * 2 for L in lens)}
     else:
         dq, kc, vc, L = fa_inputs.decode_inputs_for(DECODE, seed=0, L=DECODE.cap)
         dq, kc, vc = dq.to(dev), kc.to(dev), vc.to(dev)
@@ -790,7 +803,8 @@ def run_profile_case(args, local_rank):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--profile", choices=["prefill_small", "decode_full", "backward_small"], default=None,
+    ap.add_argument("--profile", choices=["prefill_small", "decode_full", "backward_small", "paged_batch"],
+                    default=None,
                     help="launch-only driver for ncu captures (no timing)")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=300)
