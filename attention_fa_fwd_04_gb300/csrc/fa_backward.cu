@@ -14,16 +14,16 @@
 // lse is the forward pass's per-row log-sum-exp (fa_prefill_fwd_lse), so P is
 // recomputed exactly as the forward computed it, with no row max or sum.
 //
-// Both tensor-core kernels are persistent (one CTA per SM) and
+// The tensor-core kernels are persistent (one CTA per SM) and
 // warp-specialised: element-wise warps turn the S / dP accumulators into dS
 // (and P) one TMEM lane per thread and write the results back into TMEM as
 // the next MMA's A operand; the next warp issues TMA tile loads, and the one
-// after it allocates TMEM and issues tcgen05.mma.  The dq kernel and the
-// D = 128 dkdv kernel have 4 element-wise warps (warps 0-3; producer 4, MMA
-// 5).  The D = 64 dkdv kernel, whose element-wise pass is the longer part of
-// a step, has 8: two per TMEM lane quarter, each on half of the query
-// columns (warps 0-7; producer 8, MMA 9).  All waits are bounded (see
-// fa_ptx.cuh).
+// after it allocates TMEM and issues tcgen05.mma.  The dq kernel has 4
+// element-wise warps (warps 0-3; producer 4, MMA 5).  The dkdv kernels have
+// 8, two per TMEM lane quarter, each on half of the query columns (warps
+// 0-7; producer 8, MMA 9): at D = 64 64-row query sub-tiles, double-buffered
+// in TMEM; at D = 128 128-row sub-tiles with one TMEM buffer (see each
+// kernel).  All waits are bounded (see fa_ptx.cuh).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <math.h>
@@ -50,10 +50,9 @@ struct Cfg {
   static constexpr int HALVES = D / 64;
   static constexpr int TILE_BYTES = HALVES * HALF_BYTES;  // one 128-row tile
   static constexpr int NSTAGE_DQ = 5;    // dq: K ring (KRING slots) + V ring (VRING slots)
-  static constexpr int NSTAGE_DKV = 4;   // (Q, dO) sub-tile ring of the dkdv kernel
-  // dkdv element-wise warps: 8 at D = 64 (measured +15 % there), 4 at D = 128
-  // (where 8 measured 2 % slower: its MMAs already set the pace).
-  static constexpr int DKV_EW = D == 64 ? 8 : 4;
+  static constexpr int NSTAGE_DKV = 4;   // (Q, dO) sub-tile ring of the D = 64 dkdv kernel
+  // D = 64 dkdv kernel: 8 element-wise warps, then the producer and MMA warps.
+  static constexpr int DKV_EW = 8;
   static constexpr int DKV_THREADS = (DKV_EW + 2) * 32;
   static constexpr int SMEM_BAR = 512;
   static constexpr int SMEM_DQ = 1024 + 2 * TILE_BYTES + NSTAGE_DQ * TILE_BYTES + SMEM_BAR;
@@ -63,6 +62,18 @@ struct Cfg {
   static constexpr int STAGE_DKV = 2 * SUB_BYTES;
   static constexpr int SMEM_DKV =
       1024 + 2 * TILE_BYTES + NSTAGE_DKV * (STAGE_DKV + 2 * QS * 4) + SMEM_BAR;
+};
+// dkdv kernel at D = 128 (128-row query sub-tiles): K, V, a Q ring, a dO ring
+// and a ring of lse / Delta rows.  The rings fill the 227 KiB a CTA may use,
+// leaving PAD_MAX bytes to align the tiles to 1 KiB.
+struct Wide {
+  static constexpr int QSLOTS = 3, DOSLOTS = 2, LDSLOTS = 2;
+  static constexpr int TILE = 2 * HALF_BYTES;  // a 128-row, D = 128 tile
+  static constexpr int BAR_BYTES = 256;
+  static constexpr int CORE = (2 + QSLOTS + DOSLOTS) * TILE + LDSLOTS * 2 * BT * 4 + BAR_BYTES;
+  static constexpr int SMEM = 227 * 1024;
+  static constexpr int PAD_MAX = SMEM - CORE;
+  static_assert(PAD_MAX >= 0, "wide dkdv layout exceeds the shared memory of a CTA");
 };
 }  // namespace bw
 
@@ -592,7 +603,7 @@ __global__ void __launch_bounds__(bw::THREADS, 1)
 }
 
 // ------------------------------------------------------------------------------
-// dk, dv
+// dk, dv at D = 64
 //
 // Per 128-key tile, the visible query rows are taken 64 at a time (a
 // sub-tile) so that S^T / dP^T can be double-buffered in TMEM:
@@ -613,13 +624,13 @@ __global__ void __launch_bounds__(bw::Cfg<D>::DKV_THREADS, 1)
   constexpr bool kBF16 = BIsBF16<T>::value;
   constexpr int NS = C::NSTAGE_DKV;
   constexpr int QS = bw::QS;
+  static_assert(D == 64, "the 64-row sub-tile dkdv kernel serves D = 64");
   constexpr int EW = C::DKV_EW;                 // element-wise warps 0 .. EW-1
   constexpr int PRODUCER = EW, MMA = EW + 1;    // then the producer and MMA warps
-  // 16-bit P^T / dS^T of query half h start at column PST * h of S^T / dP^T.
-  // With 8 warps, two threads share each TMEM lane, one per half, and each
-  // writes within the 32 columns it has read (PST = 32); with 4, one thread
-  // owns the lane and the halves pack contiguously (PST = 16).
-  constexpr int PST = EW == 8 ? 32 : 16;
+  // 16-bit P^T / dS^T of query half h start at column PST * h of S^T / dP^T:
+  // two threads share each TMEM lane, one per half, and each writes within
+  // the 32 columns it has read.
+  constexpr int PST = 32;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sK = smem;
@@ -854,8 +865,7 @@ __global__ void __launch_bounds__(bw::Cfg<D>::DKV_THREADS, 1)
     // Warp w serves TMEM lane quarter w % 4.  With 8 warps, warp w takes the
     // query half w / 4 of each sub-tile; with 4, each thread takes both.  The
     // pass is element-wise given lse and Delta, so the halves never talk.
-    constexpr int NH = 8 / EW;                // query halves per thread
-    const int quarter = warp & 3, qh0 = EW == 8 ? warp >> 2 : 0;
+    const int quarter = warp & 3, qh0 = warp >> 2;
     const int r = quarter * 32 + lane;  // TMEM lane = key row within the tile
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     uint32_t ph_cnt = 0, gcnt = 0, o_cnt = 0;
@@ -932,25 +942,13 @@ __global__ void __launch_bounds__(bw::Cfg<D>::DKV_THREADS, 1)
             tmem_st16(t_lane + bb * 128 + qh * PST, pp);
             tmem_st16(t_lane + bb * 128 + 64 + qh * PST, pd);
           };
-          uint32_t sr[NH][32], pr[NH][32];
-          tmem_ld32(t_lane + bb * 128 + qh0 * 32, sr[0]);
-          tmem_ld32(t_lane + bb * 128 + 64 + qh0 * 32, pr[0]);
+          uint32_t sr[32], pr[32];
+          tmem_ld32(t_lane + bb * 128 + qh0 * 32, sr);
+          tmem_ld32(t_lane + bb * 128 + 64 + qh0 * 32, pr);
           tmem_wait_ld();
-          reg_fence32(sr[0]);
-          reg_fence32(pr[0]);
-          if constexpr (NH == 1) {
-            half_pass(qh0, sr[0], pr[0]);
-          } else {
-            // Both halves: the second half's reads are in flight while the
-            // first half is computed.
-            tmem_ld32(t_lane + bb * 128 + 32, sr[NH - 1]);
-            tmem_ld32(t_lane + bb * 128 + 96, pr[NH - 1]);
-            half_pass(0, sr[0], pr[0]);
-            tmem_wait_ld();
-            reg_fence32(sr[NH - 1]);
-            reg_fence32(pr[NH - 1]);
-            half_pass(1, sr[NH - 1], pr[NH - 1]);
-          }
+          reg_fence32(sr);
+          reg_fence32(pr);
+          half_pass(qh0, sr, pr);
           tmem_wait_st();
           tc_fence_before();
           mbar_arrive(&pd_full[bb]);
@@ -971,7 +969,7 @@ __global__ void __launch_bounds__(bw::Cfg<D>::DKV_THREADS, 1)
         T* const row =
             (which ? DK : DV) + (((size_t)b * p.Sk + (row_ok ? j : 0)) * p.Hkv + hkv) * D;
         const float mul = which ? p.scale : 1.f;
-        constexpr int NQ = (D / 32) / (EW / 4);  // 32-column chunks per thread
+        constexpr int NQ = D / 64;  // 32-column chunks per thread
 #pragma unroll
         for (int qq = 0; qq < NQ; ++qq) {
           const int q4 = qh0 * NQ + qq;
@@ -1020,6 +1018,510 @@ __global__ void __launch_bounds__(bw::Cfg<D>::DKV_THREADS, 1)
   }
 }
 
+
+// ------------------------------------------------------------------------------
+// dkdv, D = 128: 128-row query sub-tiles, one TMEM buffer.
+//
+// TMEM: S^T [0, 128) | dP^T [128, 256) | dV [256, 384) | dK [384, 512).
+// S^T = K Q^T and dP^T = V dO^T are N = 128 products (a 64-row sub-tile
+// makes them N = 64, whose shared-memory operand reads, not the tensor math,
+// set their rate).  There is no room for a second S^T / dP^T buffer, so the
+// steps overlap this way:
+//   the element-wise warps read all of S^T(u) into registers and say so
+//   (s_free); S^T(u+1) is issued then, so P(u+1) is computed while the MMAs
+//   of step u still run;
+//   P^T and dS^T (16-bit) of query half h go over the dP^T columns of that
+//   half, and each half is signalled on its own, so dV, dK of half 0 run
+//   while half 1 is computed;
+//   dP^T(u+1) follows dV, dK of half 1, the last readers of its columns.
+// Shared memory holds K, V, a 3-slot Q ring, a 2-slot dO ring and a 2-slot
+// ring of the sub-tiles' lse and Delta rows, each ring with its own
+// barriers: S^T(u+1) waits only for Q(u+1), whose slot frees two steps
+// earlier than a combined Q / dO stage would.
+// Eight element-wise warps: warp w serves TMEM lane quarter w % 4 and query
+// columns 32 (w / 4) + [0, 32) of each half.  A thread writes its 16-bit
+// results only over columns it has already read, so the two warps of a lane
+// quarter never touch each other's columns.
+// ------------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(10 * 32, 1)
+    bwd_dkdv_wide_kernel(const __grid_constant__ CUtensorMap tmQ,
+                         const __grid_constant__ CUtensorMap tmK,
+                         const __grid_constant__ CUtensorMap tmV,
+                         const __grid_constant__ CUtensorMap tmDO, const BwdParams p) {
+  constexpr int D = 128;
+  using C = bw::Cfg<D>;
+  using W = bw::Wide;
+  constexpr bool kBF16 = BIsBF16<T>::value;
+  constexpr int QN = W::QSLOTS, DN = W::DOSLOTS, LN = W::LDSLOTS;
+  constexpr int QW = bw::BT;                 // query rows of a sub-tile
+  constexpr int EW = 8, PRODUCER = 8, MMA = 9;
+  extern __shared__ uint8_t smem_raw[];
+  // The launch reserves W::PAD_MAX bytes for aligning the tiles to 1 KiB.  A
+  // base needing more (not seen: the dynamic shared window starts aligned)
+  // is reported, and the CTA leaves before touching shared memory.
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  if (pad > (uint32_t)W::PAD_MAX) {
+    if (threadIdx.x == 0) atomicOr(&g_backward_err, kErrBounds | (15u << 8));
+    return;
+  }
+  uint8_t* smem = smem_raw + pad;
+  uint8_t* sK = smem;
+  uint8_t* sV = smem + C::TILE_BYTES;
+  uint8_t* sQ = smem + 2 * C::TILE_BYTES;  // [QN] Q tiles
+  uint8_t* sDO = sQ + QN * C::TILE_BYTES;  // [DN] dO tiles
+  float* sLD = reinterpret_cast<float*>(sDO + DN * C::TILE_BYTES);  // [LN][lse*log2e, Delta][QW]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sLD + LN * 2 * QW);
+  uint64_t* q_full = bars;              // [QN] producer (expect_tx)
+  uint64_t* q_empty = q_full + QN;      // [QN] MMA commit
+  uint64_t* do_full = q_empty + QN;     // [DN] producer (expect_tx)
+  uint64_t* do_empty = do_full + DN;    // [DN] MMA commit
+  uint64_t* ld_full = do_empty + DN;    // [LN] producer, after its shared-memory writes
+  uint64_t* ld_empty = ld_full + LN;    // [LN] one arrival per element-wise thread
+  uint64_t* kv_full = ld_empty + LN;
+  uint64_t* kv_empty = kv_full + 1;
+  uint64_t* s_full = kv_full + 2;   // S^T(u) in TMEM
+  uint64_t* dp_full = kv_full + 3;  // dP^T(u) in TMEM
+  uint64_t* h_ready = kv_full + 4;  // [2] P^T / dS^T of query half h (all element-wise threads)
+  uint64_t* o_full = kv_full + 6;   // dK, dV complete
+  uint64_t* drain = kv_full + 7;
+  uint64_t* s_free = kv_full + 8;   // S^T(u) read into registers (all element-wise threads)
+  uint64_t* sched_full = kv_full + 9;                // [kSchedSlots]
+  uint64_t* sched_empty = sched_full + kSchedSlots;  // [kSchedSlots]
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sched_empty + kSchedSlots);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  volatile int* sched = abort_flag + 1;  // [kSchedSlots]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < QN; ++s) {
+      mbar_init(&q_full[s], 1);
+      mbar_init(&q_empty[s], 1);
+    }
+    for (int s = 0; s < DN; ++s) {
+      mbar_init(&do_full[s], 1);
+      mbar_init(&do_empty[s], 1);
+    }
+    for (int s = 0; s < LN; ++s) {
+      mbar_init(&ld_full[s], 1);
+      mbar_init(&ld_empty[s], EW * 32);
+    }
+    mbar_init(kv_full, 1);
+    mbar_init(kv_empty, 1);
+    mbar_init(s_full, 1);
+    mbar_init(dp_full, 1);
+    mbar_init(&h_ready[0], EW * 32);
+    mbar_init(&h_ready[1], EW * 32);
+    mbar_init(s_free, EW * 32);
+    mbar_init(o_full, 1);
+    mbar_init(drain, 1);
+    for (int i = 0; i < kSchedSlots; ++i) {
+      mbar_init(&sched_full[i], 1);
+      mbar_init(&sched_empty[i], EW + 1);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == MMA) {
+    tmem_alloc(tmem_holder, bw::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const bool leader = lane == 0;
+  const int off = p.Sk - p.Sq;
+  const int n_qw = (p.Sq + QW - 1) / QW;
+  // First query sub-tile that sees key row k0 (n_qw if none).
+  auto first_sub = [&](int k0) {
+    if (!p.causal) return 0;
+    const int i0 = k0 - off;  // the first query row that sees key k0
+    if (i0 >= p.Sq) return n_qw;
+    return i0 <= 0 ? 0 : i0 / QW;
+  };
+  constexpr uint32_t COL_DP = 128, COL_DV = 256, COL_DK = 384;
+  // The producer's loads that may still be in flight if the CTA aborts: the
+  // last QN Q tiles, the last DN dO tiles, the K / V tiles of its last item.
+  uint32_t prod_q = 0, prod_do = 0, prod_kv_par = 0;
+  bool prod_kv_any = false;
+
+  if (warp == PRODUCER) {
+    // ================================ producer ================================
+    if (leader) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmDO);
+    }
+    const uint64_t pol_kv = l2_policy_evict_first();
+    const uint64_t pol_q = l2_policy_evict_last();
+    uint32_t st = 0, local = 0;  // st: sub-tile steps so far (slots, parities)
+    bool ok = true;
+    for (uint32_t k = 0; ok; ++k, ++local) {
+      const int w = sched_produce(k, p.work_ctr, p.n_items, sched_full, sched_empty, sched,
+                                  abort_flag, &g_backward_err, leader);
+      if (w < 0) {
+        ok = w == -1;
+        break;
+      }
+      int b, hkv, kt;
+      dkv_item(w, p, &b, &hkv, &kt);
+      const int q0 = first_sub(kt * bw::BT);
+      if (local > 0 &&
+          !(ok = mbar_wait(kv_empty, (local - 1) & 1, abort_flag, &g_backward_err, 1)))
+        break;
+      if (leader) {
+        mbar_arrive_expect_tx(kv_full, 2 * C::TILE_BYTES);
+#pragma unroll
+        for (int h = 0; h < C::HALVES; ++h) {
+          tma_load_4d_hint(sK + h * bw::HALF_BYTES, &tmK, kv_full, h * 64, hkv, kt * bw::BT, b,
+                           pol_kv);
+          tma_load_4d_hint(sV + h * bw::HALF_BYTES, &tmV, kv_full, h * 64, hkv, kt * bw::BT, b,
+                           pol_kv);
+        }
+      }
+      __syncwarp();
+      prod_kv_par = local & 1;
+      prod_kv_any = true;
+      // Query sub-tiles descending, the group's heads innermost: the items of
+      // one kv head then read the same Q / dO tiles at about the same time.
+      for (int qs = n_qw - 1; qs >= q0 && ok; --qs) {
+        for (int g = 0; g < p.G && ok; ++g, ++st) {
+          const int hq = hkv * p.G + g;
+          // lse * log2(e) and Delta of the sub-tile's query rows (+inf / 0
+          // past Sq: those columns get P = 0), read before the waits so that
+          // their latency is off the rings' paths.
+          const size_t base = ((size_t)b * p.Hq + hq) * p.Sq;
+          float lv[QW / 32], dv[QW / 32];
+#pragma unroll
+          for (int x = 0; x < QW / 32; ++x) {
+            const int i = qs * QW + x * 32 + lane;
+            lv[x] = i < p.Sq ? p.lse[base + i] * bw::LOG2E : INFINITY;
+            dv[x] = i < p.Sq ? p.delta[base + i] : 0.f;
+          }
+          // Q first (S^T needs only Q), then dO, then the lse / Delta rows.
+          const int qsl = st % QN, dsl = st % DN, lsl = st % LN;
+          if (!(ok = mbar_wait(&q_empty[qsl], ((st / QN) & 1) ^ 1, abort_flag, &g_backward_err,
+                               2)))
+            break;
+          if (leader) {
+            mbar_arrive_expect_tx(&q_full[qsl], C::TILE_BYTES);
+#pragma unroll
+            for (int h = 0; h < C::HALVES; ++h)
+              tma_load_4d_hint(sQ + qsl * C::TILE_BYTES + h * bw::HALF_BYTES, &tmQ, &q_full[qsl],
+                               h * 64, hq, qs * QW, b, pol_q);
+          }
+          __syncwarp();
+          prod_q = st + 1;
+          if (!(ok = mbar_wait(&do_empty[dsl], ((st / DN) & 1) ^ 1, abort_flag, &g_backward_err,
+                               2)))
+            break;
+          if (leader) {
+            mbar_arrive_expect_tx(&do_full[dsl], C::TILE_BYTES);
+#pragma unroll
+            for (int h = 0; h < C::HALVES; ++h)
+              tma_load_4d_hint(sDO + dsl * C::TILE_BYTES + h * bw::HALF_BYTES, &tmDO,
+                               &do_full[dsl], h * 64, hq, qs * QW, b, pol_q);
+          }
+          __syncwarp();
+          prod_do = st + 1;
+          if (!(ok = mbar_wait(&ld_empty[lsl], ((st / LN) & 1) ^ 1, abort_flag, &g_backward_err,
+                               2)))
+            break;
+          float* sL = sLD + lsl * 2 * QW;
+          float* sD = sL + QW;
+#pragma unroll
+          for (int x = 0; x < QW / 32; ++x) {
+            sL[x * 32 + lane] = lv[x];
+            sD[x * 32 + lane] = dv[x];
+          }
+          __syncwarp();
+          if (leader) mbar_arrive(&ld_full[lsl]);  // after the shared-memory writes
+          __syncwarp();
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == MMA) {
+    // ================================== MMA ===================================
+    // Lane 0 alone runs the issuer loop; descriptors advance on their low 32
+    // bits (see mma_ss_lh).
+    if (lane == 0) {
+      const uint32_t sd_hi = (uint32_t)(sdesc_sw128(0u, 16, 1024) >> 32);
+      constexpr uint32_t IDESC_S = idesc_f16(bw::BT, QW, kBF16, false);
+      constexpr uint32_t IDESC_ACC = idesc_f16(bw::BT, D, kBF16, true);
+      const uint32_t sk_addr = smem_u32(sK), sv_addr = smem_u32(sV);
+      const uint32_t sq_addr = smem_u32(sQ), sdo_addr = smem_u32(sDO);
+      uint32_t st = 0, local = 0;
+      bool ok = true;
+      // D_tmem (128 x 128) = A (128-row tile, K-major) x B^T (128-row tile, K-major).
+      auto issue_nt = [&](uint32_t d_col, uint32_t a_addr, uint32_t b_addr) {
+        const uint32_t a0 = (uint32_t)sdesc_sw128(a_addr, 16, 1024);
+        const uint32_t b0 = (uint32_t)sdesc_sw128(b_addr, 16, 1024);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t k16 = ((k >> 2) * bw::HALF_BYTES + (k & 3) * 32) >> 4;
+          mma_ss_lh(tmem + d_col, a0 + k16, sd_hi, b0 + k16, sd_hi, IDESC_S, k > 0 ? 1u : 0u);
+        }
+      };
+      // acc += A (TMEM, 16-bit) x B (rows 64 h .. 64 h + 63 of a 128-row
+      // tile, MN-major).  The half's 16-bit A columns are two runs of 16, one
+      // per element-wise warp of the lane quarter, 32 columns apart: k-steps
+      // 2e and 2e + 1 read columns a_col + 32 e and a_col + 32 e + 8.
+      auto issue_acc = [&](uint32_t d_col, uint32_t a_col, uint32_t b_addr, int h,
+                           bool accumulate) {
+        const uint32_t b0 =
+            (uint32_t)sdesc_sw128(b_addr + h * (QW / 2) * 128, bw::HALF_BYTES, 1024);
+#pragma unroll
+        for (int k = 0; k < QW / 2 / 16; ++k) {
+          mma_ts_lh(tmem + d_col, tmem + a_col + (k >> 1) * 32 + (k & 1) * 8,
+                    b0 + (uint32_t)((k * 16 * 128) >> 4), sd_hi, IDESC_ACC,
+                    (accumulate || k > 0) ? 1u : 0u);
+        }
+      };
+      auto commit = [&](uint64_t* bar) { mma_commit(bar); };
+      auto q_addr = [&](uint32_t t) { return sq_addr + (t % QN) * C::TILE_BYTES; };
+      auto do_addr = [&](uint32_t t) { return sdo_addr + (t % DN) * C::TILE_BYTES; };
+      auto wait_q = [&](uint32_t t) {
+        return mbar_wait(&q_full[t % QN], (t / QN) & 1, abort_flag, &g_backward_err, 4);
+      };
+      auto wait_do = [&](uint32_t t) {
+        return mbar_wait(&do_full[t % DN], (t / DN) & 1, abort_flag, &g_backward_err, 4);
+      };
+      for (uint32_t it = 0; ok; ++it, ++local) {
+        const int w =
+            sched_consume_lane(it, sched_full, sched_empty, sched, abort_flag, &g_backward_err,
+                               11);
+        if (w < 0) {
+          ok = w == -1;
+          break;
+        }
+        int b, hkv, kt;
+        dkv_item(w, p, &b, &hkv, &kt);
+        const int steps = p.G * (n_qw - first_sub(kt * bw::BT));
+        if (!(ok = mbar_wait(kv_full, local & 1, abort_flag, &g_backward_err, 3))) break;
+        tc_fence_after();
+        if (steps > 0) {
+          if (!(ok = wait_q(st))) break;
+          tc_fence_after();
+          issue_nt(0, sk_addr, q_addr(st));  // S^T(0) = K Q^T
+          commit(s_full);
+          if (!(ok = wait_do(st))) break;
+          tc_fence_after();
+          issue_nt(COL_DP, sv_addr, do_addr(st));  // dP^T(0) = V dO^T
+          commit(dp_full);
+        }
+        for (int u = 0; u < steps && ok; ++u, ++st) {
+          const uint32_t g = st;  // step counter shared with the element-wise warps
+          // S^T(u+1) as soon as the element-wise warps hold S^T(u) in
+          // registers: no 16-bit result is written over S^T.
+          if (!(ok = mbar_wait(s_free, g & 1, abort_flag, &g_backward_err, 5))) break;
+          if (u + 1 < steps) {
+            if (!(ok = wait_q(st + 1))) break;
+            tc_fence_after();
+            issue_nt(0, sk_addr, q_addr(st + 1));
+            commit(s_full);
+          }
+          // Half 0: P^T and dS^T over dP^T columns [128, 192).
+          if (!(ok = mbar_wait(&h_ready[0], g & 1, abort_flag, &g_backward_err, 5))) break;
+          tc_fence_after();
+          issue_acc(COL_DV, COL_DP, do_addr(st), 0, u > 0);       // dV += P^T dO
+          issue_acc(COL_DK, COL_DP + 16, q_addr(st), 0, u > 0);   // dK += dS^T Q
+          // Half 1: P^T and dS^T over dP^T columns [192, 256).
+          if (!(ok = mbar_wait(&h_ready[1], g & 1, abort_flag, &g_backward_err, 5))) break;
+          tc_fence_after();
+          issue_acc(COL_DK, COL_DP + 80, q_addr(st), 1, true);
+          commit(&q_empty[st % QN]);
+          issue_acc(COL_DV, COL_DP + 64, do_addr(st), 1, true);
+          commit(&do_empty[st % DN]);
+          if (u + 1 < steps) {
+            if (!(ok = wait_do(st + 1))) break;
+            tc_fence_after();
+            issue_nt(COL_DP, sv_addr, do_addr(st + 1));
+            commit(dp_full);
+          }
+        }
+        if (!ok) break;
+        commit(kv_empty);
+        commit(o_full);
+      }
+      commit(drain);
+      mbar_wait_drain(drain, 0);
+    }
+    __syncwarp();
+  } else {
+    // ================== P^T and dS^T (element-wise warps) ==================
+    const int quarter = warp & 3, e = warp >> 2;
+    const int r = quarter * 32 + lane;  // TMEM lane = key row within the tile
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    uint32_t st = 0, o_cnt = 0;
+    bool ok = true;
+    T* const DK = static_cast<T*>(p.dk);
+    T* const DV = static_cast<T*>(p.dv);
+    const float2 c2 = make_float2(p.c, p.c);
+    for (uint32_t it = 0; ok; ++it) {
+      const int w =
+          sched_consume(it, sched_full, sched_empty, sched, abort_flag, &g_backward_err, 12);
+      if (w < 0) {
+        ok = w == -1;
+        break;
+      }
+      int b, hkv, kt;
+      dkv_item(w, p, &b, &hkv, &kt);
+      const int q0 = first_sub(kt * bw::BT);
+      const int j = kt * bw::BT + r;  // key row
+      for (int qs = n_qw - 1; qs >= q0 && ok; --qs) {
+        for (int g = 0; g < p.G && ok; ++g, ++st) {
+          const int lsl = st % LN;
+          if (!(ok = mbar_wait(&ld_full[lsl], (st / LN) & 1, abort_flag, &g_backward_err, 9)))
+            break;
+          if (!(ok = mbar_wait(s_full, st & 1, abort_flag, &g_backward_err, 7))) break;
+          __syncwarp();
+          tc_fence_after();
+          const float* sL = sLD + lsl * 2 * QW;
+          const float* sD = sL + QW;
+          // Query row i = qs * 128 + ic sees key j when i < Sq and (not causal
+          // or j <= i + off).  Rows past Sq have lse = +inf (P = 0); key rows
+          // past Sk read zeros and feed only dK / dV rows never stored.  Only
+          // a sub-tile on the causal edge hides columns (ic < ic_lo).
+          const int ic_lo = p.causal ? j - off - qs * QW : 0;
+          const bool edge = __any_sync(0xffffffffu, ic_lo > 0);
+          // P of this thread's 32 columns of both halves, from S^T.
+          uint32_t pv[2][32];
+          tmem_ld32(t_lane + e * 32, pv[0]);
+          tmem_ld32(t_lane + 64 + e * 32, pv[1]);
+          tmem_wait_ld();
+          reg_fence32(pv[0]);
+          reg_fence32(pv[1]);
+          tc_fence_before();
+          mbar_arrive(s_free);  // S^T(u+1) may now be written over S^T(u)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+#pragma unroll
+            for (int x4 = 0; x4 < 8; ++x4) {
+              const float4 l4 = reinterpret_cast<const float4*>(sL)[h * 16 + e * 8 + x4];
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh) {
+                const int x = x4 * 2 + hh;
+                const float2 nl = hh ? make_float2(-l4.z, -l4.w) : make_float2(-l4.x, -l4.y);
+                const float2 a = __ffma2_rn(make_float2(__uint_as_float(pv[h][2 * x]),
+                                                        __uint_as_float(pv[h][2 * x + 1])),
+                                            c2, nl);
+                float2 pf = make_float2(fast_exp2(a.x), fast_exp2(a.y));
+                if (edge) {
+                  const int col = h * 64 + e * 32 + 2 * x;
+                  pf.x = col < ic_lo ? 0.f : pf.x;
+                  pf.y = col + 1 < ic_lo ? 0.f : pf.y;
+                }
+                pv[h][2 * x] = __float_as_uint(pf.x);
+                pv[h][2 * x + 1] = __float_as_uint(pf.y);
+              }
+            }
+          }
+          if (!(ok = mbar_wait(dp_full, st & 1, abort_flag, &g_backward_err, 7))) break;
+          __syncwarp();
+          tc_fence_after();
+          uint32_t pr[2][32];
+          tmem_ld32(t_lane + COL_DP + e * 32, pr[0]);
+          tmem_ld32(t_lane + COL_DP + 64 + e * 32, pr[1]);
+          tmem_wait_ld();
+          reg_fence32(pr[0]);
+          reg_fence32(pr[1]);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t pp[16], pd[16];
+#pragma unroll
+            for (int x4 = 0; x4 < 8; ++x4) {
+              const float4 d4 = reinterpret_cast<const float4*>(sD)[h * 16 + e * 8 + x4];
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh) {
+                const int x = x4 * 2 + hh;
+                const float2 nd = hh ? make_float2(-d4.z, -d4.w) : make_float2(-d4.x, -d4.y);
+                const float2 pf = make_float2(__uint_as_float(pv[h][2 * x]),
+                                              __uint_as_float(pv[h][2 * x + 1]));
+                const float2 dd = __fadd2_rn(make_float2(__uint_as_float(pr[h][2 * x]),
+                                                         __uint_as_float(pr[h][2 * x + 1])),
+                                             nd);
+                const float2 ds = __fmul2_rn(pf, dd);
+                pp[x] = BPack<T>::pack(pf.x, pf.y);
+                pd[x] = BPack<T>::pack(ds.x, ds.y);
+              }
+            }
+            // P^T, then dS^T, over the 32 dP^T columns of half h this thread read.
+            tmem_st16(t_lane + COL_DP + h * 64 + e * 32, pp);
+            tmem_st16(t_lane + COL_DP + h * 64 + e * 32 + 16, pd);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&h_ready[h]);
+          }
+          mbar_arrive(&ld_empty[lsl]);  // this thread is done with the slot's lse / Delta
+        }
+      }
+      if (!ok) break;
+      // Epilogue: dV, dK (= scale * accumulator) of this thread's key row;
+      // each warp of a lane quarter stores half of the D columns.
+      if (!(ok = mbar_wait(o_full, o_cnt & 1, abort_flag, &g_backward_err, 8))) break;
+      ++o_cnt;
+      __syncwarp();
+      tc_fence_after();
+      const bool any = p.G * (n_qw - q0) > 0;
+      const bool row_ok = j < p.Sk;
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {  // 0: dV, 1: dK
+        T* const row =
+            (which ? DK : DV) + (((size_t)b * p.Sk + (row_ok ? j : 0)) * p.Hkv + hkv) * D;
+        const float mul = which ? p.scale : 1.f;
+#pragma unroll
+        for (int qq = 0; qq < 2; ++qq) {
+          const int q4 = e * 2 + qq;
+          uint32_t ar[32];
+          if (any) {
+            tmem_ld32(t_lane + (which ? COL_DK : COL_DV) + q4 * 32, ar);
+            tmem_wait_ld();
+            reg_fence32(ar);
+          } else {
+#pragma unroll
+            for (int x = 0; x < 32; ++x) ar[x] = 0u;
+          }
+          uint32_t pk[16];
+#pragma unroll
+          for (int x = 0; x < 16; ++x)
+            pk[x] = BPack<T>::pack(__uint_as_float(ar[2 * x]) * mul,
+                                   __uint_as_float(ar[2 * x + 1]) * mul);
+          if (row_ok) {
+            if (b >= p.B || hkv >= p.Hkv) {
+              atomicOr(&g_backward_err, kErrBounds);
+              continue;
+            }
+            uint4* dst = reinterpret_cast<uint4*>(row + q4 * 32);
+#pragma unroll
+            for (int x = 0; x < 4; ++x)
+              dst[x] = make_uint4(pk[4 * x], pk[4 * x + 1], pk[4 * x + 2], pk[4 * x + 3]);
+          }
+        }
+      }
+      tc_fence_before();
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == MMA) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, bw::TMEM_COLS);
+  }
+  // Aborted CTA: wait, bounded, for the loads that may still be in flight.
+  if (warp == PRODUCER && *abort_flag) {
+    for (uint32_t t = prod_q > (uint32_t)QN ? prod_q - QN : 0u; t < prod_q; ++t)
+      mbar_wait_drain(&q_full[t % QN], (t / QN) & 1);
+    for (uint32_t t = prod_do > (uint32_t)DN ? prod_do - DN : 0u; t < prod_do; ++t)
+      mbar_wait_drain(&do_full[t % DN], (t / DN) & 1);
+    if (prod_kv_any) mbar_wait_drain(kv_full, prod_kv_par);
+    __syncwarp();
+  }
+}
+
 // ------------------------------------------------------------------------------
 // Host
 // ------------------------------------------------------------------------------
@@ -1047,10 +1549,12 @@ static int launch_backward_t(const void* q, const void* k, const void* v, const 
   if (encode_tmap_rows(&tdo, dout, D, Hq, Sq, B, bw::BT)) return cudaErrorInvalidValue;
   if (encode_tmap_rows(&tk, k, D, Hkv, Sk, B, bw::BT)) return cudaErrorInvalidValue;
   if (encode_tmap_rows(&tv, v, D, Hkv, Sk, B, bw::BT)) return cudaErrorInvalidValue;
-  // The dkdv kernel reads Q and dO in 64-row sub-tiles.
+  // The D = 64 dkdv kernel reads Q and dO in 64-row sub-tiles.
   CUtensorMap tq64, tdo64;
-  if (encode_tmap_rows(&tq64, q, D, Hq, Sq, B, bw::QS)) return cudaErrorInvalidValue;
-  if (encode_tmap_rows(&tdo64, dout, D, Hq, Sq, B, bw::QS)) return cudaErrorInvalidValue;
+  if (D == 64) {
+    if (encode_tmap_rows(&tq64, q, D, Hq, Sq, B, bw::QS)) return cudaErrorInvalidValue;
+    if (encode_tmap_rows(&tdo64, dout, D, Hq, Sq, B, bw::QS)) return cudaErrorInvalidValue;
+  }
   static int attr_set[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -1058,8 +1562,13 @@ static int launch_backward_t(const void* q, const void* k, const void* v, const 
     cudaError_t e = cudaFuncSetAttribute(bwd_dq_kernel<D, T>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_DQ);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(bwd_dkdv_kernel<D, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::SMEM_DKV);
+    if constexpr (D == 128) {
+      e = cudaFuncSetAttribute(bwd_dkdv_wide_kernel<T>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, bw::Wide::SMEM);
+    } else {
+      e = cudaFuncSetAttribute(bwd_dkdv_kernel<D, T>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_DKV);
+    }
     if (e != cudaSuccess) return e;
     attr_set[dev] = 1;
   }
@@ -1093,7 +1602,10 @@ static int launch_backward_t(const void* q, const void* k, const void* v, const 
   p.work_ctr = ctr + 1;
   if (p.n_items > 0) {
     const int grid = p.n_items < sms ? p.n_items : sms;
-    bwd_dkdv_kernel<D, T><<<grid, C::DKV_THREADS, C::SMEM_DKV, stream>>>(tq64, tk, tv, tdo64, p);
+    if constexpr (D == 128)
+      bwd_dkdv_wide_kernel<T><<<grid, 10 * 32, bw::Wide::SMEM, stream>>>(tq, tk, tv, tdo, p);
+    else
+      bwd_dkdv_kernel<D, T><<<grid, C::DKV_THREADS, C::SMEM_DKV, stream>>>(tq64, tk, tv, tdo64, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

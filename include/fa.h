@@ -348,7 +348,9 @@ const char* fa_status_string(int status);
  * the read itself failed.
  * If detail != NULL it receives the raw bits: the prefill (and backward) word
  * in bits 0-15, the decode word in bits 16-31; in each, bit 0 = a wait timed out (bits 8-15:
- * which wait), bit 1 = a bounds check fired.
+ * which wait), bit 1 = a bounds check fired.  Bounds bit with site 15: the
+ * D = 128 backward dK/dV kernel found its dynamic shared memory too far from
+ * a 1 KiB boundary to lay out its rings, and its CTAs left without work.
  */
 int fa_device_error(int reset, unsigned int* detail);
 

@@ -55,6 +55,7 @@ def run_backward(fa, q, k, v, dout, scale, causal):
     (1, 8, 2, 1024, 1024, 128, True, torch.bfloat16),   # GQA: dk/dv sum 4 heads
     (1, 4, 1, 500, 200, 128, True, torch.bfloat16),     # Sq > Sk: rows with no key
     (2, 2, 1, 77, 900, 64, False, torch.bfloat16),
+    (1, 4, 2, 700, 300, 128, False, torch.float16),    # D = 128 fp16, no mask
 ])
 def test_backward_against_oracle(fa, B, Hq, Hkv, Sq, Sk, D, causal, dt):
     q, k, v = fa_inputs.prefill_inputs(B, Hq, Hkv, Sq, Sk, D, dt, seed=Sq + Sk + D)

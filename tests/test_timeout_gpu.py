@@ -8,9 +8,10 @@ wait, so a wait that is not satisfied at once gives up.  The CTA leaves its
 loops, waits (with the fixed 2 s teardown limit) for the loads and MMAs
 already in flight, frees its tensor memory and sets the timeout bit and the
 wait's site in the error word.  Nothing waits
-without a bound, and no kernel is altered for the test.  The test checks that
-a prefill and a 65536-token decode report FA_ERR_TIMEOUT with a site, then
-restores the default limit and checks that the next calls match the oracle.
+without a bound, and no kernel is altered for the test.  The tests check that
+a prefill, a 65536-token decode and a backward call (D = 128 and 64) report
+FA_ERR_TIMEOUT with a site, then restore the default limit and check that the
+next calls match the oracle.
 """
 import math
 
@@ -91,3 +92,38 @@ def test_watchdog_limit_that_no_wait_reaches_gives_correct_results(fa):
             oracle.attention_varlen(qp, kp, vp, cu.tolist(), cu.tolist(), 0.088, True))
     compare(od.float().cpu().numpy().reshape(sd.B, sd.Hq, sd.D),
             oracle.decode(dq, kc, vc, L, sd.scale))
+
+
+@pytest.mark.parametrize("D", [128, 64])
+def test_backward_wait_limit_aborts_report_timeout_and_the_next_call_is_correct(fa, D):
+    """The backward kernels under a 1 ns limit.  Their waits keep suspending
+    probes of about 4 us, so a wait gives up once it has lasted about two of
+    them; the first key tile of a 2048-token causal GQA call takes hundreds
+    of microseconds, so its epilogue wait (and others) give up.  Each aborted
+    CTA tears down as the forward's do; then, at the default limit, a small
+    backward call matches the oracle's gradients."""
+    from tests.test_backward_gpu import grad_compare, run_backward
+    dev = torch.device("cuda", 0)
+    B, Hq, Hkv, S = 1, 16, 1, 2048
+    scale = 1 / math.sqrt(D)
+    q, k, v = fa_inputs.prefill_inputs(B, Hq, Hkv, S, S, D, torch.bfloat16, seed=21)
+    dout = torch.randn(B, S, Hq, D, generator=torch.Generator().manual_seed(22)).to(torch.bfloat16)
+    qd, kd, vd, dd = q.to(dev), k.to(dev), v.to(dev), dout.to(dev)
+    o, lse = fa.prefill(qd, kd, vd, scale, True, lse=True)
+    torch.cuda.synchronize()
+    assert fa.fa_device_error(reset=1)[0] == fa.FA_OK
+    try:
+        assert fa.fa_set_wait_limit_ns(1) == fa.FA_OK
+        fa.backward(qd, kd, vd, o, dd, lse, scale, True)
+        st, detail = fa.fa_device_error(reset=1)
+        assert st == fa.FA_ERR_TIMEOUT, (st, hex(detail))
+        assert detail & 1 and (detail >> 8) & 0xFF, hex(detail)  # backward word: bit 0 + site
+    finally:
+        assert fa.fa_set_wait_limit_ns(0) == fa.FA_OK
+
+    q2, k2, v2 = fa_inputs.prefill_inputs(1, 4, 2, 300, 300, D, torch.bfloat16, seed=23)
+    do2 = torch.randn(1, 300, 4, D, generator=torch.Generator().manual_seed(24)).to(torch.bfloat16)
+    got = run_backward(fa, q2, k2, v2, do2, scale, True)
+    ref = oracle.attention_bwd(q2, k2, v2, do2, scale, True)
+    for g, r, name in zip(got, ref, ("dq", "dk", "dv")):
+        grad_compare(g, r, name)
