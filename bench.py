@@ -566,7 +566,7 @@ def run_backward(args, fa, torch, dev, q, k, v, sh, stream):
             "unit": "TFLOP/s", "frac": round(ach / pk["bf16_tflops"], 4),
             "peak_source": f"{pk_src} bf16 burst",
             "scope": "whole call (Delta, dQ and dK/dV kernels); traffic: the dK/dV kernel, "
-                     "about 70 % of the call",
+                     "about 56 % of the call",
             "traffic": stored_traffic("bwd_dkdv_kernel_D128_bf16", bwd_hash)}
     return {"value": round(ach, 2), "unit": "TFLOP/s", "ms": round(t * 1e3, 4),
             "roofline": roof,
