@@ -9,9 +9,9 @@ loops, waits (with the fixed 2 s teardown limit) for the loads and MMAs
 already in flight, frees its tensor memory and sets the timeout bit and the
 wait's site in the error word.  Nothing waits
 without a bound, and no kernel is altered for the test.  The tests check that
-a prefill, a 65536-token decode and a backward call (D = 128 and 64) report
-FA_ERR_TIMEOUT with a site, then restore the default limit and check that the
-next calls match the oracle.
+a prefill, a 65536-token decode, a backward call (D = 128 and 64), a paged
+decode and a packed-sequence prefill report FA_ERR_TIMEOUT with a site, then
+restore the default limit and check that the next calls match the oracle.
 """
 import math
 
@@ -127,3 +127,47 @@ def test_backward_wait_limit_aborts_report_timeout_and_the_next_call_is_correct(
     ref = oracle.attention_bwd(q2, k2, v2, do2, scale, True)
     for g, r, name in zip(got, ref, ("dq", "dk", "dv")):
         grad_compare(g, r, name)
+
+
+def test_paged_decode_and_packed_prefill_wait_limit_abort_and_recover(fa):
+    """A paged decode (balanced splits, row combine) and a packed-sequence
+    prefill under a 1 ns limit report FA_ERR_TIMEOUT; then small calls of both
+    at the default limit match the oracle.  The paged decode polls, so its
+    first unsatisfied wait gives up.  The packed prefill suspends (about 4 us
+    a probe); with items of up to 32 K/V tiles its producer waits for a whole
+    item before loading the next item's Q, so that wait gives up."""
+    from tests.test_paged_decode_gpu import paged_inputs, run_paged
+    dev = torch.device("cuda", 0)
+    lens = [16384, 8000, 12000, 3000, 16000, 9000, 15000, 11000]
+    qd, kpd, vpd, tabd, sld = fa_inputs.paged_decode_batch(lens, 1, 8, 2, 128, 256, seed=3,
+                                                           device=dev)
+    vl = [4096, 3000, 2048]
+    qv, kv, vv, cq, ck = fa_inputs.varlen_inputs(vl, vl, 16, 2, 128, seed=4)
+    qv, kv, vv, cq, ck = (t.to(dev) for t in (qv, kv, vv, cq, ck))
+    torch.cuda.synchronize()
+    assert fa.fa_device_error(reset=1)[0] == fa.FA_OK
+    try:
+        assert fa.fa_set_wait_limit_ns(1) == fa.FA_OK
+        fa.decode_paged(qd, kpd, vpd, tabd, sld, 1 / math.sqrt(128))
+        st, detail = fa.fa_device_error(reset=1)
+        assert st == fa.FA_ERR_TIMEOUT, (st, hex(detail))
+        assert (detail >> 16) & 1 and (detail >> 24) & 0xFF, hex(detail)  # decode word
+        fa.prefill_varlen(qv, kv, vv, cq, ck, max(vl), 1 / math.sqrt(128), True)
+        st, detail = fa.fa_device_error(reset=1)
+        assert st == fa.FA_ERR_TIMEOUT, (st, hex(detail))
+        assert detail & 1 and (detail >> 8) & 0xFF, hex(detail)  # prefill word
+    finally:
+        assert fa.fa_set_wait_limit_ns(0) == fa.FA_OK
+
+    q, kp, vp, table, L = paged_inputs(4, 8, 2, 128, 32, 40, [0, 1, 1000, 1280], seed=5)
+    o, _ = run_paged(fa, q, kp, vp, table, L, 1 / math.sqrt(128))
+    compare(o, oracle.decode_paged(q, kp, vp, table.tolist(), L.tolist(), 1 / math.sqrt(128)))
+    small = [300, 0, 257, 129]
+    qs, ks, vs, cqs, cks = fa_inputs.varlen_inputs(small, small, 8, 2, 128, seed=6)
+    out = fa.prefill_varlen(qs.to(dev), ks.to(dev), vs.to(dev), cqs.to(dev), cks.to(dev),
+                            max(small), 0.088, True)
+    torch.cuda.synchronize()
+    st, detail = fa.fa_device_error(reset=1)
+    assert st == fa.FA_OK, hex(detail)
+    compare(out.float().cpu().numpy(),
+            oracle.attention_varlen(qs, ks, vs, cqs.tolist(), cks.tolist(), 0.088, True))
