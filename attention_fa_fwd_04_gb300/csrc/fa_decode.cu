@@ -141,7 +141,7 @@ __device__ void balanced_splits(const DecodeParams& p, int* sS, int* sP, long lo
       const long long y = __shfl_xor_sync(0xffffffffu, m, o);
       m = y > m ? y : m;
     }
-    __syncthreads();  // the previous round's values have been read
+    __syncthreads();  // the previous reduction has read sRed
     if (lane == 0) {
       sRed[2 * warp] = a;
       sRed[2 * warp + 1] = m;
