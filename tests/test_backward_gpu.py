@@ -56,6 +56,7 @@ def run_backward(fa, q, k, v, dout, scale, causal):
     (1, 4, 1, 500, 200, 128, True, torch.bfloat16),     # Sq > Sk: rows with no key
     (2, 2, 1, 77, 900, 64, False, torch.bfloat16),
     (1, 4, 2, 700, 300, 128, False, torch.float16),    # D = 128 fp16, no mask
+    (1, 6, 2, 384, 384, 128, True, torch.bfloat16),     # G = 3 query heads per kv head
 ])
 def test_backward_against_oracle(fa, B, Hq, Hkv, Sq, Sk, D, causal, dt):
     q, k, v = fa_inputs.prefill_inputs(B, Hq, Hkv, Sq, Sk, D, dt, seed=Sq + Sk + D)
@@ -79,16 +80,20 @@ def test_backward_gqa_causal_2k(fa):
     grad_compare(dv, rv, "dv")
 
 
-def test_backward_empty_sides(fa):
+@pytest.mark.parametrize("D", [64, 128])
+def test_backward_empty_sides(fa, D):
+    """No keys: dQ is zero.  No query rows: the dK/dV kernel runs items with
+    no query steps (at D = 128 the 128-row sub-tile kernel), whose epilogue
+    writes zero gradients."""
     dev = torch.device("cuda", 0)
-    q = torch.randn(1, 10, 4, 64, device=dev).to(torch.bfloat16)
-    kz = torch.empty(1, 0, 2, 64, device=dev, dtype=torch.bfloat16)
+    q = torch.randn(1, 10, 4, D, device=dev).to(torch.bfloat16)
+    kz = torch.empty(1, 0, 2, D, device=dev, dtype=torch.bfloat16)
     lse = torch.full((1, 4, 10), -math.inf, device=dev)
     dq, dk, dv = fa.backward(q, kz, kz, torch.zeros_like(q), q, lse, 0.1, True)
     torch.cuda.synchronize()
     assert torch.equal(dq, torch.zeros_like(dq)) and dk.numel() == 0
-    qz = torch.empty(1, 0, 4, 64, device=dev, dtype=torch.bfloat16)
-    k = torch.randn(1, 7, 2, 64, device=dev).to(torch.bfloat16)
+    qz = torch.empty(1, 0, 4, D, device=dev, dtype=torch.bfloat16)
+    k = torch.randn(1, 7, 2, D, device=dev).to(torch.bfloat16)
     lz = torch.empty(1, 4, 0, device=dev)
     dq, dk, dv = fa.backward(qz, k, k, qz, qz, lz, 0.1, False)
     torch.cuda.synchronize()
