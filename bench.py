@@ -726,7 +726,9 @@ def run_profile_case(args, local_rank):
       backward_small: fa_backward on B1 Hq64 Hkv4 S8192 D128 causal bf16 (the
                      headline backward's kernels at half its query heads)
       paged_batch:   the paged decode of the bench's 16 ragged sequences, one new
-                     token each (585 MB of K/V per launch)"""
+                     token each (585 MB of K/V per launch)
+      varlen_batch:  the packed causal prefill of the bench's 16 sequences at the
+                     headline's heads (Q + O = 2.3 GB)"""
     import torch
     import attention_fa_fwd_04_gb300 as fa
     torch.cuda.set_device(local_rank)
@@ -766,6 +768,22 @@ def run_profile_case(args, local_rank):
                 raise fa.FAError(st, "fa_backward")
         work = {"workload": f"backward B{B} Hq{Hq} Hkv{Hkv} S{S} D{D} causal bf16",
                 "flops_per_launch": 2.5 * 2.0 * B * Hq * S * S * D}
+    elif args.profile == "varlen_batch":
+        lens = fa_inputs.varlen_lengths()
+        Hq, Hkv, D = PREFILL.Hq, PREFILL.Hkv, PREFILL.D
+        q_h, k_h, v_h, cq, ck = fa_inputs.varlen_inputs(lens, lens, Hq, Hkv, D, seed=0)
+        q, k, v, cq, ck = (t.to(dev) for t in (q_h, k_h, v_h, cq, ck))
+        o = torch.empty_like(q)
+        for _ in range(n):
+            st = fa.fa_prefill_varlen_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), 0,
+                                          cq.data_ptr(), ck.data_ptr(), len(lens), Hq, Hkv,
+                                          q.shape[0], k.shape[0], max(lens), D, PREFILL.scale, 1,
+                                          fa.FA_BF16, sh)
+            if st:
+                raise fa.FAError(st, "fa_prefill_varlen_fwd")
+        work = {"workload": f"packed causal prefill, 16 sequences ({sum(lens)} tokens), "
+                            f"Hq{Hq}/Hkv{Hkv} D{D} bf16",
+                "flops_per_launch": sum(2.0 * Hq * x * x * D for x in lens)}
     elif args.profile == "paged_batch":
         lens = fa_inputs.varlen_lengths(n=16, max_len=DECODE.cap, seed=0)
         Hq, Hkv, D = DECODE.Hq, DECODE.Hkv, DECODE.D
@@ -803,7 +821,8 @@ def run_profile_case(args, local_rank):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--profile", choices=["prefill_small", "decode_full", "backward_small", "paged_batch"],
+    ap.add_argument("--profile", choices=["prefill_small", "decode_full", "backward_small", "paged_batch",
+                             "varlen_batch"],
                     default=None,
                     help="launch-only driver for ncu captures (no timing)")
     ap.add_argument("--gpus", type=int, default=1)
