@@ -862,9 +862,9 @@ __global__ void __launch_bounds__(bw::Cfg<D>::DKV_THREADS, 1)
     __syncwarp();
   } else {
     // ================== P^T and dS^T (element-wise warps) ==================
-    // Warp w serves TMEM lane quarter w % 4.  With 8 warps, warp w takes the
-    // query half w / 4 of each sub-tile; with 4, each thread takes both.  The
-    // pass is element-wise given lse and Delta, so the halves never talk.
+    // Warp w serves TMEM lane quarter w % 4 and takes the query half w / 4 of
+    // each sub-tile.  The pass is element-wise given lse and Delta, so the
+    // halves never talk.
     const int quarter = warp & 3, qh0 = warp >> 2;
     const int r = quarter * 32 + lane;  // TMEM lane = key row within the tile
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
@@ -956,8 +956,8 @@ __global__ void __launch_bounds__(bw::Cfg<D>::DKV_THREADS, 1)
         }
       }
       if (!ok) break;
-      // Epilogue: dV, dK (= scale * accumulator) of this thread's key row; with
-      // 8 warps, each warp of a lane quarter stores half of the D columns.
+      // Epilogue: dV, dK (= scale * accumulator) of this thread's key row; each
+      // warp of a lane quarter stores half of the D columns.
       if (!(ok = mbar_wait(o_full, o_cnt & 1, abort_flag, &g_backward_err, 8))) break;
       ++o_cnt;
       __syncwarp();
