@@ -650,6 +650,9 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
     uint32_t s_cnt = 0, o_cnt = 0;
     bool ok = true;
     T* const O = static_cast<T*>(p.o);
+    // 32-byte O stores (D = 128, O's base 32-byte aligned; rows are multiples
+    // of 256 bytes): see the epilogue.
+    const bool o_wide = D == 128 && (reinterpret_cast<uintptr_t>(p.o) & 31u) == 0;
 
     for (uint32_t it = 0; ok; ++it) {
       const int w =
@@ -850,10 +853,27 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
             atomicOr(&g_prefill_err, kErrBounds);
             continue;
           }
-          uint4* dst = reinterpret_cast<uint4*>(orow + q4 * 32);
+          if (o_wide) {
+            // 32-byte stores.  Each thread stores its own row, so every store
+            // instruction touches 32 rows; the load-store unit works through
+            // them for a couple of thousand clocks after the last one issues,
+            // and this warpgroup's next shared-memory operations (its waits on
+            // the next item's S) queue behind them.  Half as many instructions
+            // halve that drain.
 #pragma unroll
-          for (int x = 0; x < 4; ++x)
-            dst[x] = make_uint4(pk[4 * x], pk[4 * x + 1], pk[4 * x + 2], pk[4 * x + 3]);
+            for (int x = 0; x < 2; ++x)
+              asm volatile(
+                  "st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(
+                      orow + q4 * 32 + x * 16),
+                  "r"(pk[8 * x]), "r"(pk[8 * x + 1]), "r"(pk[8 * x + 2]), "r"(pk[8 * x + 3]),
+                  "r"(pk[8 * x + 4]), "r"(pk[8 * x + 5]), "r"(pk[8 * x + 6]), "r"(pk[8 * x + 7])
+                  : "memory");
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(orow + q4 * 32);
+#pragma unroll
+            for (int x = 0; x < 4; ++x)
+              dst[x] = make_uint4(pk[4 * x], pk[4 * x + 1], pk[4 * x + 2], pk[4 * x + 3]);
+          }
         }
       }
       tc_fence_before();

@@ -136,3 +136,26 @@ def test_work_counter_across_calls_and_streams(fa):
         assert torch.equal(o, main_outs[0])
     compare(main_outs[0].float().cpu().numpy(), oracle.attention(q, k, v, 0.125, True))
     assert fa.fa_device_error()[0] == fa.FA_OK
+
+
+def test_output_aligned_to_16_bytes_only(fa):
+    """At D = 128 the epilogue uses 32-byte stores when O's base is 32-byte
+    aligned and 16-byte stores otherwise (the ABI asks for 16).  An output
+    view 16 bytes into a buffer takes the second path; both must give the
+    same bits, and match the oracle."""
+    dev = torch.device("cuda", 0)
+    B, Hq, Hkv, S, D = 1, 8, 2, 640, 128
+    q, k, v = fa_inputs.prefill_inputs(B, Hq, Hkv, S, S, D, torch.bfloat16, seed=41)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    n = q.numel()
+    buf = torch.empty(n + 8, dtype=torch.bfloat16, device=dev)
+    assert buf.data_ptr() % 32 == 0
+    out16 = buf[8:8 + n].view(q.shape)  # 16 bytes past a 32-byte boundary
+    assert out16.data_ptr() % 32 == 16
+    fa.prefill(qd, kd, vd, 1 / math.sqrt(D), True, out=out16)
+    out32 = fa.prefill(qd, kd, vd, 1 / math.sqrt(D), True)
+    torch.cuda.synchronize()
+    st, detail = fa.fa_device_error()
+    assert st == fa.FA_OK, hex(detail)
+    assert torch.equal(out16, out32)
+    compare(out16.float().cpu().numpy(), oracle.attention(q, k, v, 1 / math.sqrt(D), True))
