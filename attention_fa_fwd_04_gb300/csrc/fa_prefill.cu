@@ -62,19 +62,61 @@ static_assert(256 * REGS_SOFTMAX + 128 * REGS_ISSUE <= THREADS * REGS_LAUNCH,
               "register split exceeds the launch allocation");
 constexpr int HALF_BYTES = 128 * 128;  // 128 rows x 64 elements x 2 bytes
 
-template <int D>
+template <int D, bool PACKED>
 struct Cfg {
   static constexpr int HALVES = D / 64;
   static constexpr int TILE_BYTES = HALVES * HALF_BYTES;  // one 128-row tile
-  static constexpr int NSTAGE = (D == 128) ? 5 : 9;
+  static constexpr int NSTAGE = (D == 128) ? 4 : 9;
   static constexpr int SMEM_Q = 2 * TILE_BYTES;
   static constexpr int SMEM_KV = NSTAGE * TILE_BYTES;
+  // Packed sequences at D = 128: O leaves through a staging area per softmax
+  // warp (32 rows x 64 columns, 4 KiB, swizzled as the tensor map says) and
+  // that warp's own TMA stores.
+  static constexpr bool O_TMA = D == 128 && PACKED;
+  static constexpr int OST_WARP = 32 * 128;
+  static constexpr int SMEM_OST = O_TMA ? 8 * OST_WARP : 0;
   static constexpr int SMEM_BAR = 512;
-  static constexpr int SMEM_TOTAL = 1024 + SMEM_Q + SMEM_KV + SMEM_BAR;
+  static constexpr int SMEM_TOTAL = 1024 + SMEM_Q + SMEM_KV + SMEM_OST + SMEM_BAR;
+  static_assert(SMEM_TOTAL <= 227 * 1024, "shared memory per CTA");
   static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O0 = 256, COL_O1 = 256 + D;
   static constexpr uint32_t TMEM_COLS = 512;
 };
 }  // namespace pf
+
+// TMA stores of O (the packed kernel's epilogue at D = 128).
+// TMA store of one 4-D tile from shared memory (laid out as the tensor map's
+// swizzle says) to global memory; elements outside the tensor are not
+// written.  Completion is tracked by the issuing thread's bulk async-groups.
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap* m, const void* src, int c0, int c1,
+                                             int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(m)),
+      "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Wait until this thread's committed bulk stores have read their shared memory.
+__device__ __forceinline__ void bulk_wait_group_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Wait until this thread's committed bulk stores have completed.
+__device__ __forceinline__ void bulk_wait_group0() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+// Order this thread's generic-proxy shared-memory writes before later
+// async-proxy (TMA) reads of them.
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
 
 struct PrefillParams {
   void* o;     // [B, Sq, Hq, D]; packed sequences: [total_q, Hq, D]
@@ -320,8 +362,9 @@ struct IsBF16<__nv_bfloat16> {
 template <int D, typename T, bool PACKED, bool POLL = false>
 __global__ void __launch_bounds__(pf::THREADS, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                   const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
-  using C = pf::Cfg<D>;
+                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                   const PrefillParams p) {
+  using C = pf::Cfg<D, PACKED>;
   constexpr bool kBF16 = IsBF16<T>::value;
   // Largest row sum of unnormalised P a step may leave (see the lazy rescale
   // below): 2^60 for bf16 P (range to 2^127), 2^15 for fp16 P (max 65504).
@@ -333,7 +376,8 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sQ = smem;
   uint8_t* sKV = smem + C::SMEM_Q;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + C::SMEM_KV);
+  uint8_t* sOst = sKV + C::SMEM_KV;  // [8] O staging areas (packed, D = 128)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sOst + C::SMEM_OST);
   uint64_t* full = bars;
   uint64_t* empty = bars + NSTAGE;
   uint64_t* q_full = bars + 2 * NSTAGE;
@@ -827,7 +871,8 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
         mbar_arrive(&p_full[i]);
       }
       if (!ok) break;
-      // Epilogue: O / l, rounded once, 16-byte stores.
+      // Epilogue: O / l, rounded once; TMA stores (packed, D = 128), else
+      // 32- or 16-byte stores.
       if (!(ok = mbar_wait<POLL>(&o_full[i], o_cnt & 1, abort_flag, &g_prefill_err, 11 + i))) break;
       ++o_cnt;
       __syncwarp();
@@ -837,8 +882,52 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       // s * log2(e) the P values were taken against.
       if (lse_row && row_ok)
         *lse_row = l > 0.f ? 0.6931471805599453f * (m_used + __log2f(l)) : NEG_INF;
+      // Packed sequences, D = 128: the warp's 32 rows go out through its
+      // staging area and its own TMA stores, 64 columns at a time, when all of
+      // them belong to this sequence (rows past its end would be the next
+      // sequence's).  Stores from the threads, each its own row, leave the
+      // load-store unit a queue of transactions that this warp's next
+      // shared-memory operations (its waits on the next item's S) sit behind;
+      // packed batches have many short items, so that cost recurs often.
+      const int wrow0 = row0 + wq * 32;
+      const bool o_tma = C::O_TMA && b < p.B && hq_i < p.Hq && wrow0 + 32 <= Sq &&
+                         sq.orow + wrow0 + 32 <= (size_t)p.total_q;
+      if (o_tma) {
+        uint8_t* const ost = sOst + warp * C::OST_WARP;  // this warp's staging area
 #pragma unroll
-      for (int q4 = 0; q4 < D / 32; ++q4) {
+        for (int hh = 0; hh < D / 64; ++hh) {
+          uint32_t pk[2][16];
+#pragma unroll
+          for (int q2 = 0; q2 < 2; ++q2) {
+            uint32_t orr[32];
+            tmem_ld32(tO + (hh * 2 + q2) * 32, orr);
+            tmem_wait_ld();
+            reg_fence32(orr);
+#pragma unroll
+            for (int x = 0; x < 16; ++x)
+              pk[q2][x] = Pack2<T>::pack(__uint_as_float(orr[2 * x]) * inv,
+                                         __uint_as_float(orr[2 * x + 1]) * inv);
+          }
+          // The staging area is free once the warp's previous store has read it.
+          if (lane == 0) bulk_wait_group_read0();
+          __syncwarp();
+          // Row `lane`, 16-byte chunk c at lane * 128 + ((c ^ (lane & 7)) << 4):
+          // the tensor map's 128-byte swizzle (each 8 lanes hit distinct banks).
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            st_shared_v4(smem_u32(ost) + lane * 128 + ((c ^ (lane & 7)) << 4),
+                         pk[c >> 2][4 * (c & 3)], pk[c >> 2][4 * (c & 3) + 1],
+                         pk[c >> 2][4 * (c & 3) + 2], pk[c >> 2][4 * (c & 3) + 3]);
+          fence_proxy_async_shared();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_4d(&tmO, ost, hh * 64, hq_i, sq.q0 + wrow0, sq.tb);
+            bulk_commit_group();
+          }
+        }
+      }
+#pragma unroll
+      for (int q4 = 0; q4 < D / 32 && !o_tma; ++q4) {
         uint32_t orr[32];
         tmem_ld32(tO + q4 * 32, orr);
         tmem_wait_ld();
@@ -878,6 +967,8 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       }
       tc_fence_before();
     }
+    // The TMA stores this warp issued complete before the CTA ends.
+    if (C::O_TMA && lane == 0) bulk_wait_group0();
   }
 
   tc_fence_before();
@@ -949,10 +1040,13 @@ static int launch_prefill_t(const void* q, const void* k, const void* v, void* o
                             const PrefillShape& sh, float scale, int causal,
                             unsigned int* work_ctr, const int4* units, const int* n_units,
                             cudaStream_t stream) {
-  using C = pf::Cfg<D>;
+  using CD = pf::Cfg<D, false>;  // dense batches
+  using CP = pf::Cfg<D, true>;   // packed sequences
   const bool packed = sh.cu_q != nullptr;
-  CUtensorMap tq, tk, tv;
+  // to: O in 32-row boxes, for the packed kernel's TMA stores at D = 128.
+  CUtensorMap tq, tk, tv, to{};  // to stays unused (zero) for a dense batch
   if (packed) {
+    if (encode_tmap_rows(&to, o, D, sh.Hq, sh.total_q, 1, 32)) return cudaErrorInvalidValue;
     if (encode_tmap_rows(&tq, q, D, sh.Hq, sh.total_q, 1, pf::BM)) return cudaErrorInvalidValue;
     if (encode_tmap_rows(&tk, k, D, sh.Hkv, sh.total_k, 1, pf::BN)) return cudaErrorInvalidValue;
     if (encode_tmap_rows(&tv, v, D, sh.Hkv, sh.total_k, 1, pf::BN)) return cudaErrorInvalidValue;
@@ -967,13 +1061,13 @@ static int launch_prefill_t(const void* q, const void* k, const void* v, void* o
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
     cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, T, false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::SMEM_TOTAL);
+                                         CD::SMEM_TOTAL);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(prefill_kernel<D, T, true>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_TOTAL);
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, CP::SMEM_TOTAL);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(prefill_kernel<D, T, false, true>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_TOTAL);
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, CD::SMEM_TOTAL);
     if (e != cudaSuccess) return e;
     attr_set[dev] = 1;
   }
@@ -1002,11 +1096,12 @@ static int launch_prefill_t(const void* q, const void* k, const void* v, void* o
   const int grid = p.n_items < sms ? p.n_items : sms;
   if (grid == 0) return cudaSuccess;  // packed: no sequence fits max_seqlen_q (bounds bit set)
   if (packed)
-    prefill_kernel<D, T, true><<<grid, pf::THREADS, C::SMEM_TOTAL, stream>>>(tq, tk, tv, p);
+    prefill_kernel<D, T, true><<<grid, pf::THREADS, CP::SMEM_TOTAL, stream>>>(tq, tk, tv, to, p);
   else if (watchdog_on_current_device())
-    prefill_kernel<D, T, false, true><<<grid, pf::THREADS, C::SMEM_TOTAL, stream>>>(tq, tk, tv, p);
+    prefill_kernel<D, T, false, true><<<grid, pf::THREADS, CD::SMEM_TOTAL, stream>>>(tq, tk, tv, to,
+                                                                                  p);
   else
-    prefill_kernel<D, T, false><<<grid, pf::THREADS, C::SMEM_TOTAL, stream>>>(tq, tk, tv, p);
+    prefill_kernel<D, T, false><<<grid, pf::THREADS, CD::SMEM_TOTAL, stream>>>(tq, tk, tv, to, p);
   return cudaGetLastError();
 }
 
