@@ -69,10 +69,10 @@ struct Cfg {
   static constexpr int NSTAGE = (D == 128) ? 4 : 9;
   static constexpr int SMEM_Q = 2 * TILE_BYTES;
   static constexpr int SMEM_KV = NSTAGE * TILE_BYTES;
-  // Packed sequences at D = 128: O leaves through a staging area per softmax
-  // warp (32 rows x 64 columns, 4 KiB, swizzled as the tensor map says) and
-  // that warp's own TMA stores.
-  static constexpr bool O_TMA = D == 128 && PACKED;
+  // Packed sequences: O leaves through a staging area per softmax warp (32
+  // rows x 64 columns, 4 KiB, swizzled as the tensor map says) and that
+  // warp's own TMA stores.
+  static constexpr bool O_TMA = PACKED;
   static constexpr int OST_WARP = 32 * 128;
   static constexpr int SMEM_OST = O_TMA ? 8 * OST_WARP : 0;
   static constexpr int SMEM_BAR = 512;
@@ -83,7 +83,7 @@ struct Cfg {
 };
 }  // namespace pf
 
-// TMA stores of O (the packed kernel's epilogue at D = 128).
+// TMA stores of O (the packed kernel's epilogue).
 // TMA store of one 4-D tile from shared memory (laid out as the tensor map's
 // swizzle says) to global memory; elements outside the tensor are not
 // written.  Completion is tracked by the issuing thread's bulk async-groups.
@@ -376,7 +376,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sQ = smem;
   uint8_t* sKV = smem + C::SMEM_Q;
-  uint8_t* sOst = sKV + C::SMEM_KV;  // [8] O staging areas (packed, D = 128)
+  uint8_t* sOst = sKV + C::SMEM_KV;  // [8] O staging areas (packed sequences)
   uint64_t* bars = reinterpret_cast<uint64_t*>(sOst + C::SMEM_OST);
   uint64_t* full = bars;
   uint64_t* empty = bars + NSTAGE;
@@ -871,7 +871,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
         mbar_arrive(&p_full[i]);
       }
       if (!ok) break;
-      // Epilogue: O / l, rounded once; TMA stores (packed, D = 128), else
+      // Epilogue: O / l, rounded once; TMA stores (packed sequences), else
       // 32- or 16-byte stores.
       if (!(ok = mbar_wait<POLL>(&o_full[i], o_cnt & 1, abort_flag, &g_prefill_err, 11 + i))) break;
       ++o_cnt;
@@ -882,7 +882,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       // s * log2(e) the P values were taken against.
       if (lse_row && row_ok)
         *lse_row = l > 0.f ? 0.6931471805599453f * (m_used + __log2f(l)) : NEG_INF;
-      // Packed sequences, D = 128: the warp's 32 rows go out through its
+      // Packed sequences: the warp's 32 rows go out through its
       // staging area and its own TMA stores, 64 columns at a time, when all of
       // them belong to this sequence (rows past its end would be the next
       // sequence's).  Stores from the threads, each its own row, leave the
@@ -1043,7 +1043,7 @@ static int launch_prefill_t(const void* q, const void* k, const void* v, void* o
   using CD = pf::Cfg<D, false>;  // dense batches
   using CP = pf::Cfg<D, true>;   // packed sequences
   const bool packed = sh.cu_q != nullptr;
-  // to: O in 32-row boxes, for the packed kernel's TMA stores at D = 128.
+  // to: O in 32-row boxes, for the packed kernel's TMA stores.
   CUtensorMap tq, tk, tv, to{};  // to stays unused (zero) for a dense batch
   if (packed) {
     if (encode_tmap_rows(&to, o, D, sh.Hq, sh.total_q, 1, 32)) return cudaErrorInvalidValue;
