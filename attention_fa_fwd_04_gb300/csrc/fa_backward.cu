@@ -127,8 +127,14 @@ struct BIsBF16<__nv_bfloat16> {
 };
 
 // ------------------------------------------------------------------------------
-// pre: Delta[b, h, i] = sum_d dO[b,i,h,d] * O[b,i,h,d], one warp per row.
+// pre: Delta[b, h, i] = sum_d dO[b,i,h,d] * O[b,i,h,d].  Rows are taken in
+// memory order ([B, Sq, Hq]); D / 8 lanes share a row, each loading 16 bytes
+// of O and of dO, and a warp issues the loads of PRE_STEPS steps of rows (8 KiB
+// at D = 128) before it reduces any of them, so enough bytes are in flight to
+// keep HBM busy.
 // ------------------------------------------------------------------------------
+constexpr int PRE_STEPS = 4;
+
 template <int D, typename T>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const T* __restrict__ o,
                                                       const T* __restrict__ dout,
@@ -139,24 +145,55 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const T* __restrict__ o,
     ctr[0] = 0u;
     ctr[1] = 0u;
   }
+  constexpr int LPR = D / 8;          // lanes per row
+  constexpr int RPS = 32 / LPR;       // rows per warp and step
+  constexpr int RPI = RPS * PRE_STEPS;  // rows per warp and iteration
   const size_t rows = (size_t)B * Sq * Hq;
-  const int lane = threadIdx.x & 31;
-  for (size_t r = (blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5; r < rows;
-       r += ((size_t)gridDim.x * blockDim.x) >> 5) {
-    // r indexes [B, Sq, Hq] rows of O; Delta is stored [B, Hq, Sq].
-    const size_t h = r % Hq, bi = r / Hq, i = bi % Sq, b = bi / Sq;
-    float acc = 0.f;
-    // D / 64 pairs of bf16x2 per lane (D = 64: 1, D = 128: 2)
+  const int lane = threadIdx.x & 31, sub = lane / LPR, l = lane % LPR;
+  const size_t warps = ((size_t)gridDim.x * blockDim.x) >> 5;
+  for (size_t r0 = ((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5) * RPI; r0 < rows;
+       r0 += warps * RPI) {
+    uint4 a[PRE_STEPS], g[PRE_STEPS];
 #pragma unroll
-    for (int x = 0; x < D / 64; ++x) {
-      const uint32_t a = reinterpret_cast<const uint32_t*>(o + r * D)[x * 32 + lane];
-      const uint32_t g = reinterpret_cast<const uint32_t*>(dout + r * D)[x * 32 + lane];
-      const float2 fa = BPack<T>::unpack(a), fg = BPack<T>::unpack(g);
-      acc += fa.x * fg.x + fa.y * fg.y;
+    for (int st = 0; st < PRE_STEPS; ++st) {
+      const size_t r = r0 + st * RPS + sub;
+      a[st] = g[st] = make_uint4(0u, 0u, 0u, 0u);
+      if (r < rows) {
+        a[st] = reinterpret_cast<const uint4*>(o + r * D)[l];
+        g[st] = reinterpret_cast<const uint4*>(dout + r * D)[l];
+      }
     }
 #pragma unroll
-    for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
-    if (lane == 0) delta[(b * Hq + h) * Sq + i] = acc;
+    for (int st = 0; st < PRE_STEPS; ++st) {
+      const uint32_t av[4] = {a[st].x, a[st].y, a[st].z, a[st].w};
+      const uint32_t gv[4] = {g[st].x, g[st].y, g[st].z, g[st].w};
+      float acc = 0.f;
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        const float2 fa = BPack<T>::unpack(av[x]), fg = BPack<T>::unpack(gv[x]);
+        acc += fa.x * fg.x + fa.y * fg.y;
+      }
+#pragma unroll
+      for (int m = LPR / 2; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
+      const size_t r = r0 + st * RPS + sub;
+      if (l == 0 && r < rows) {
+        // r indexes [B, Sq, Hq] rows of O; Delta is stored [B, Hq, Sq].  Row
+        // counts below 2^32 (every tensor that fits in memory) divide in 32 bits.
+        size_t h, i, b;
+        if (rows <= 0xffffffffull) {
+          const uint32_t ru = (uint32_t)r, bi = ru / (uint32_t)Hq;
+          h = ru - bi * (uint32_t)Hq;
+          b = bi / (uint32_t)Sq;
+          i = bi - (uint32_t)b * (uint32_t)Sq;
+        } else {
+          const size_t bi = r / Hq;
+          h = r - bi * Hq;
+          b = bi / Sq;
+          i = bi - b * Sq;
+        }
+        delta[(b * Hq + h) * Sq + i] = acc;
+      }
+    }
   }
 }
 
@@ -1535,9 +1572,20 @@ static int launch_backward_t(const void* q, const void* k, const void* v, const 
   unsigned int* ctr = reinterpret_cast<unsigned int*>(delta + (size_t)B * Hq * Sq);
   // pre: Delta
   {
+    // A grid-stride loop over as many blocks as fit on the SMs at once (each
+    // warp with PRE_STEPS steps of loads in flight), fewer when the rows run
+    // out first.
+    static int per_sm = 0;
+    if (per_sm <= 0 &&
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, bwd_pre_kernel<D, T>, 256, 0) !=
+            cudaSuccess)
+      per_sm = 2;
+    if (per_sm <= 0) per_sm = 1;
     const size_t rows = (size_t)B * Sq * Hq;
-    const unsigned blocks = (unsigned)((rows * 32 + 255) / 256 < 65535 ? (rows * 32 + 255) / 256
-                                                                       : 65535);
+    const size_t rows_per_block = (size_t)8 * (32 / (D / 8)) * PRE_STEPS;
+    const size_t cap = (size_t)(sm_count() > 0 ? sm_count() : 148) * per_sm;
+    const size_t want = (rows + rows_per_block - 1) / rows_per_block;
+    const unsigned blocks = (unsigned)(want < cap ? want : cap);
     bwd_pre_kernel<D, T><<<blocks, 256, 0, stream>>>(static_cast<const T*>(o),
                                                      static_cast<const T*>(dout), delta, B, Sq,
                                                      Hq, ctr);
