@@ -370,6 +370,8 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
   // below): 2^60 for bf16 P (range to 2^127), 2^15 for fp16 P (max 65504).
   constexpr float PBIG = kBF16 ? 1.152921504606846976e18f : 32768.f;
   constexpr int NSTAGE = C::NSTAGE;
+  constexpr bool PAIRED = NSTAGE % 2 == 0;  // ring slots released in fixed pairs
+  constexpr int NPAIR = NSTAGE / 2;
   constexpr float NEG_INF = -INFINITY;
 
   extern __shared__ uint8_t smem_raw[];
@@ -488,9 +490,19 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       // barrier, armed for both tiles, and V_j's own barrier gets a plain
       // arrival that keeps its phases in step: the MMA warp waits once per
       // K/V step.  K_0 and the last V stand alone.
+      // An even ring pairs its slots for good: ring positions 2g - 1 (a V) and
+      // 2g (the K after it) always share a pair of slots, released together
+      // by one commit on empty[g % NPAIR] (see the MMA warp).  Loading either
+      // position of pair g waits for the release of pair g - NPAIR.
       auto slot_free = [&](uint32_t cnt) {
-        return mbar_wait<POLL>(&empty[cnt % NSTAGE], ((cnt / NSTAGE) & 1) ^ 1, abort_flag,
-                         &g_prefill_err, 2);
+        if constexpr (PAIRED) {
+          const uint32_t g = (cnt + 1) >> 1;
+          return mbar_wait<POLL>(&empty[g % NPAIR], ((g / NPAIR) & 1) ^ 1, abort_flag,
+                                 &g_prefill_err, 2);
+        } else {
+          return mbar_wait<POLL>(&empty[cnt % NSTAGE], ((cnt / NSTAGE) & 1) ^ 1, abort_flag,
+                                 &g_prefill_err, 2);
+        }
       };
       auto load_tile = [&](uint32_t cnt, const CUtensorMap* m, int kv_tile, uint64_t* bar) {
         const int s = cnt % NSTAGE;
@@ -514,7 +526,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
         if (j + 1 < n) {
           const uint32_t ck = kv_cnt + 1;  // K_{j+1}
           if (!(ok = slot_free(cv))) break;
-          if (!(ok = slot_free(ck))) break;
+          if (!PAIRED && !(ok = slot_free(ck))) break;  // paired: ck shares cv's pair
           if (leader) {
             uint64_t* bar = &full[ck % NSTAGE];
             mbar_arrive_expect_tx(bar, 2 * C::TILE_BYTES);
@@ -628,7 +640,9 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
           issue_s(1, kb % NSTAGE);
           commit(&s_full[1]);
         }
-        commit(&empty[kb % NSTAGE]);
+        // Paired: K_0 (position kb, even) completes pair kb / 2 with the
+        // previous item's last V.
+        commit(PAIRED ? &empty[(kb >> 1) % NPAIR] : &empty[kb % NSTAGE]);
         if (n == 1) commit(q_empty);
         // Operands of step 0: V_0 and K_1 (one barrier: K_1's), or V_0 alone.
         if (!(ok = ring_wait(n > 1 ? kb + 2 : kb + 1, 5))) break;
@@ -659,13 +673,15 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
             issue_pv(1, sV, j > 0);
             if (j == nt1 - 1) commit(&o_full[1]);
           }
-          commit(&empty[sV]);
+          if (!PAIRED) commit(&empty[sV]);  // paired: released with K_{j+1} below
           if (j + 1 < n) {
             if (j + 1 < nt1) {
               issue_s(1, sK);
               commit(&s_full[1]);
             }
-            commit(&empty[sK]);
+            // Paired: V_j and K_{j+1} (positions kb + 2j + 1, + 2) are pair
+            // kb / 2 + j + 1.  The last V of an item waits for the next item's K_0.
+            commit(PAIRED ? &empty[((kb >> 1) + j + 1) % NPAIR] : &empty[sK]);
             if (j + 1 == n - 1) commit(q_empty);
             // V_{j+1} and K_{j+2} on K_{j+2}'s barrier, or the last V alone.
             if (!(ok = ring_wait(j + 2 < n ? kb + 2 * j + 4 : kb + 2 * j + 3, 6))) break;
