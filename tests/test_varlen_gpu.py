@@ -130,3 +130,30 @@ def test_varlen_many_sequences_longest_first_plan(fa):
     ref, ref_l = oracle.attention_varlen(q, k, v, cq, ck, 0.125, True, return_lse=True)
     compare(o, ref, max_abs=rounding_bound(ref, v.abs().max().item(), 8))
     lse_compare(l, ref_l)
+
+
+@pytest.mark.parametrize("D", [128, 64])
+def test_varlen_output_aligned_to_16_bytes_only(fa, D):
+    """The packed kernel writes O with TMA stores through a tensor map, and the
+    ABI asks only for 16-byte alignment.  An output view 16 bytes past a
+    32-byte boundary must give the same bits as an aligned one and match the
+    oracle; the lengths leave warps whose 32 rows run past their sequence
+    (those keep the threads' own stores) beside whole ones."""
+    dev = torch.device("cuda", 0)
+    lens = [300, 33, 256, 97]
+    q, k, v, cq, ck = packed_inputs(lens, lens, 8, 2, D, torch.bfloat16, seed=43)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    cqd, ckd = torch.from_numpy(cq).to(dev), torch.from_numpy(ck).to(dev)
+    scale = 1 / math.sqrt(D)
+    n = q.numel()
+    buf = torch.empty(n + 8, dtype=torch.bfloat16, device=dev)
+    assert buf.data_ptr() % 32 == 0
+    out16 = buf[8:8 + n].view(q.shape)  # 16 bytes past a 32-byte boundary
+    assert out16.data_ptr() % 32 == 16
+    fa.prefill_varlen(qd, kd, vd, cqd, ckd, max(lens), scale, True, out=out16)
+    out32 = fa.prefill_varlen(qd, kd, vd, cqd, ckd, max(lens), scale, True)
+    torch.cuda.synchronize()
+    st, detail = fa.fa_device_error()
+    assert st == fa.FA_OK, hex(detail)
+    assert torch.equal(out16, out32)
+    compare(out16.float().cpu().numpy(), oracle.attention_varlen(q, k, v, cq, ck, scale, True))
