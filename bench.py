@@ -314,6 +314,9 @@ def run_ours(args, rank, world, local_rank):
     rot2_us = t_rot2 / (K * n_r2) * 1e6
     rot1_gbs = dec_bytes(L_seed) / (rot1_us * 1e-6) / 1e9
     rot2_gbs = dec_bytes(DECODE.cap) / (rot2_us * 1e-6) / 1e9
+    # Spread of the per-step bursts (this rank): the figures above are their mean.
+    burst_us = sorted(e[6].elapsed_time(e[7]) * 1e3 / n_r2 for e in timed)
+    burst_med = burst_us[len(burst_us) // 2] if burst_us else 0.0
 
     out = {
         "metric": METRIC,
@@ -376,6 +379,13 @@ def run_ours(args, rank, world, local_rank):
                          "unit": "GB/s", "frac": round(rot2_gbs / pk["hbm_gbs"], 4),
                          "traffic": stored_traffic("decode_split_kernel_D128", dec_hash),
                          "bytes_algorithmic": dec_bytes(DECODE.cap)},
+            "bursts": {"us_median": round(burst_med, 3),
+                       "us_min": round(burst_us[0], 3) if burst_us else None,
+                       "us_max": round(burst_us[-1], 3) if burst_us else None,
+                       "frac_median": round(dec_bytes(DECODE.cap) / (burst_med * 1e-6) / 1e9
+                                            / pk["hbm_gbs"], 4) if burst_med else None,
+                       "note": "per-step burst time / calls over the timed steps; us, value "
+                               "and roofline above are the mean over all of them"},
             "single_call": {"us": round(t_dec2 / K * 1e6, 3), "value": round(dec2_gbs, 1),
                             "unit": "GB/s",
                             "note": "one call after an L2 flush, events around it: includes the "
