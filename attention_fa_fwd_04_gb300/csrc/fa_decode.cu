@@ -14,10 +14,11 @@
 // Design (HBM-bound: 2*L*Hkv*D*2 bytes read, ~4 flop per byte):
 //   grid   = (nsplit, Hkv * ceil(G/16), B), one CTA per SM, sized from cap and
 //            the SM count (not from L, which the host never reads);
-//   CTA    = 1 producer warp issuing TMA tile loads (32 tokens x D, K and V,
-//            128-byte swizzle) into an 8-stage mbarrier ring (16 for D = 64,
-//            128 KiB in flight), and 4 consumer warps that each own whole
-//            tiles: S^T = K Q^T and O^T += V^T P^T with mma.sync m16n8k16,
+//   CTA    = 1 producer warp issuing TMA tile loads (64 tokens x D, K and V,
+//            128-byte swizzle) into a 4-stage mbarrier ring (8 for D = 64,
+//            128 KiB in flight), and 2 consumer warps that each own whole
+//            tiles (paged caches: 32-token tiles, 4 warps, a deeper ring):
+//            S^T = K Q^T and O^T += V^T P^T with mma.sync m16n8k16,
 //            tokens as the MMA's M and the group's query heads as its N (8 per
 //            block, so a GQA group of 4 wastes half of N instead of 3/4 of a
 //            16-row M), an exp2 online softmax per warp, then a cross-warp
@@ -41,34 +42,39 @@ namespace fa {
 __device__ unsigned int g_decode_err = 0;
 
 namespace dec {
-constexpr int TT = 32;        // tokens per tile
-constexpr int NWARPS = 4;     // consumer warps
+constexpr int TT = 32;        // tokens per tile of a paged cache (page sizes are multiples)
+constexpr int NWARPS = 4;     // consumer warps, at most (paged caches)
 constexpr int THREADS = (NWARPS + 1) * 32;
 constexpr int HB = 16;        // row stride of the merge buffers (query rows per CTA at most)
-constexpr int HALF_BYTES = TT * 128;  // TT rows x 64 elements x 2 bytes
 // Bytes of K/V per CTA warmed in L2 before the grid wait: with one CTA per SM
 // that is at most about half of L2 in flight, whatever the cache length.
 constexpr int PREFETCH_BYTES = 384 * 1024;
 
-// Tile t lives in stage t % NSTAGE and is consumed by warp t % NWARPS.  With
-// NSTAGE a multiple of NWARPS every stage belongs to exactly one warp, which
+// Tile t lives in stage t % NSTAGE and is consumed by warp t % NW.  With
+// NSTAGE a multiple of NW every stage belongs to exactly one warp, which
 // therefore waits on that stage's phases strictly in order.  (A parity wait
 // must never run ahead by a phase: if two warps shared a stage, the faster one
 // could see the stage's previous phase as "complete" and consume a tile that
 // has not landed.)
-// PAGED: the paged (batched) decode streams long ranges from HBM, where the
-// bytes in flight per SM set the rate: its ring is 192 KiB deep.  The
-// single-sequence decode keeps 128 KiB, which leaves room beside it for the
-// combine's CTAs.
+// Contiguous caches: 64-token tiles (64-row TMA boxes; the SM takes in
+// 32-row boxes more slowly) over 2 consumer warps with 2 stages each, 128 KiB
+// in flight, which leaves room beside the CTA for the combine's CTAs.
+// PAGED: pages may be 32 tokens, so tiles are 32 tokens over 4 warps; the
+// paged (batched) decode streams long ranges from HBM, where the bytes in
+// flight per SM set the rate: its ring is 192 KiB deep.
 template <int D, bool PAGED = false>
 struct Cfg {
   static constexpr int HALVES = D / 64;
-  static constexpr int NSTAGE = (D == 128) ? (PAGED ? 12 : 8) : (PAGED ? 24 : 16);
+  static constexpr int TT = PAGED ? dec::TT : 64;  // tokens per tile
+  static constexpr int NW = PAGED ? dec::NWARPS : 2;  // consumer warps
+  static constexpr int THREADS = (NW + 1) * 32;
+  static constexpr int HALF_BYTES = TT * 128;  // TT rows x 64 elements x 2 bytes
+  static constexpr int NSTAGE = (D == 128) ? (PAGED ? 12 : 4) : (PAGED ? 24 : 8);
   static constexpr int KV_BYTES = HALVES * HALF_BYTES;  // one K (or V) tile
   static constexpr int STAGE_BYTES = 2 * KV_BYTES;      // K tile + V tile
   static constexpr int SMEM_STAGES = NSTAGE * STAGE_BYTES;
-  static_assert(NSTAGE % NWARPS == 0, "each stage must belong to one consumer warp");
-  static constexpr int SMEM_RED = NWARPS * HB * D * 4 + NWARPS * HB * 2 * 4 + NWARPS * HB * 4;
+  static_assert(NSTAGE % NW == 0, "each stage must belong to one consumer warp");
+  static constexpr int SMEM_RED = NW * HB * D * 4 + NW * HB * 2 * 4 + NW * HB * 4;
   static constexpr int SMEM_BAR = 2 * NSTAGE * 8 + 16 + NSTAGE * 4;
   static_assert(HALF_BYTES % 1024 == 0, "128-byte-swizzled tiles need 1 KiB alignment");
   static constexpr int SMEM_TOTAL = 1024 + SMEM_STAGES + SMEM_RED + SMEM_BAR;
@@ -216,7 +222,7 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
     decode_split_kernel(const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const DecodeParams p) {
   using C = dec::Cfg<D, PAGED>;
-  constexpr int TT = dec::TT, NSTAGE = C::NSTAGE, HB = dec::HB, NW = dec::NWARPS;
+  constexpr int TT = C::TT, NSTAGE = C::NSTAGE, HB = dec::HB, NW = C::NW;
   constexpr int RB = 8 * NB;  // query rows of this CTA (HB is the buffers' row stride)
   static_assert(RB <= HB, "row blocks must fit the merge buffers");
   constexpr float NEG_INF = -INFINITY;
@@ -245,7 +251,7 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
   // Prologue that reads nothing an earlier kernel may still be writing (the
   // tensor maps are kernel parameters); this kernel is launched as a
   // programmatic dependent, so it overlaps the tail of the previous grid.
-  if (threadIdx.x == dec::NWARPS * 32) {  // producer lane 0: fetch the maps early
+  if (threadIdx.x == NW * 32) {  // producer lane 0: fetch the maps early
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
   } else if (!PAGED && lane == 0 && warp < NW) {
@@ -388,10 +394,10 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
         uint8_t* st = stages + s * C::STAGE_BYTES;
 #pragma unroll
         for (int h = 0; h < C::HALVES; ++h)
-          tma_load_4d_hint(st + h * dec::HALF_BYTES, &tmK, &full[s], h * 64, hkv, row, tb, pol);
+          tma_load_4d_hint(st + h * C::HALF_BYTES, &tmK, &full[s], h * 64, hkv, row, tb, pol);
 #pragma unroll
         for (int h = 0; h < C::HALVES; ++h)
-          tma_load_4d_hint(st + C::KV_BYTES + h * dec::HALF_BYTES, &tmV, &full[s], h * 64, hkv,
+          tma_load_4d_hint(st + C::KV_BYTES + h * C::HALF_BYTES, &tmV, &full[s], h * 64, hkv,
                            row, tb, pol);
       }
       __syncwarp();
@@ -459,7 +465,7 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
           r /= nz;
           const int half = r % C::HALVES;
           const int kv = r / C::HALVES;
-          *reinterpret_cast<uint4*>(st + kv * C::KV_BYTES + half * dec::HALF_BYTES + row * 128 +
+          *reinterpret_cast<uint4*>(st + kv * C::KV_BYTES + half * C::HALF_BYTES + row * 128 +
                                     chunk * 16) = make_uint4(0u, 0u, 0u, 0u);
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -481,7 +487,7 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
         for (int kk = 0; kk < D / 16; ++kk) {
           const int tok = mb * 16 + (mi & 1) * 8 + (lane & 7);
           const int chunk = kk * 2 + (mi >> 1);
-          const uint32_t addr = kbase + (chunk >> 3) * dec::HALF_BYTES + tok * 128 +
+          const uint32_t addr = kbase + (chunk >> 3) * C::HALF_BYTES + tok * 128 +
                                 ((((chunk & 7) ^ (tok & 7))) << 4);
           uint32_t a[4];
           ldsm_x4(addr, a[0], a[1], a[2], a[3]);
@@ -554,7 +560,7 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
         for (int dm = 0; dm < D / 16; ++dm) {
           const int tok = mb * 16 + (mi >> 1) * 8 + (lane & 7);
           const int chunk = dm * 2 + (mi & 1);
-          const uint32_t addr = vbase + (chunk >> 3) * dec::HALF_BYTES + tok * 128 +
+          const uint32_t addr = vbase + (chunk >> 3) * C::HALF_BYTES + tok * 128 +
                                 ((((chunk & 7) ^ (tok & 7))) << 4);
           uint32_t a[4];
           ldsm_x4_t(addr, a[0], a[1], a[2], a[3]);
@@ -632,7 +638,7 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
     p.part_ml[pslot(row) * 2 + 1] = Ls;
   }
   __syncthreads();
-  for (int x = threadIdx.x; x < nh * (D / 4); x += dec::THREADS) {
+  for (int x = threadIdx.x; x < nh * (D / 4); x += C::THREADS) {
     const int row = x / (D / 4), d4 = x % (D / 4);
     float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
@@ -833,13 +839,14 @@ __global__ void decode_zero_kernel(__nv_bfloat16* o, size_t n, float* lse, size_
       lse[i] = -INFINITY;
 }
 
-static int decode_nsplit(int B, int Hq, int Hkv, int cap, int Sq) {
+static int decode_nsplit(int B, int Hq, int Hkv, int cap, int Sq, bool paged) {
   const int G = Hq / Hkv;
   const int n_hb = (Sq * G + dec::HB - 1) / dec::HB;
   const long units = (long)B * Hkv * n_hb;
   const int sms = sm_count() > 0 ? sm_count() : 148;
   long ns = sms / (units > 0 ? units : 1);
-  const long max_tiles = ((long)cap + dec::TT - 1) / dec::TT;
+  const int tt = paged ? dec::Cfg<128, true>::TT : dec::Cfg<128, false>::TT;
+  const long max_tiles = ((long)cap + tt - 1) / tt;
   if (ns > max_tiles) ns = max_tiles;
   if (ns > kMaxSplits) ns = kMaxSplits;  // the combine's one-pass limit
   if (ns < 1) ns = 1;
@@ -864,7 +871,7 @@ size_t decode_scratch_floats(int B, int Hq, int Hkv, int cap, int D, int Sq, boo
     const size_t units = (size_t)B * Hkv * ((Sq * (Hq / Hkv) + dec::HB - 1) / dec::HB);
     return sms * dec::HB * ((size_t)D + 2) + 2 * units + 2;  // + the unit map (int2, aligned)
   }
-  const size_t ns = (size_t)decode_nsplit(B, Hq, Hkv, cap, Sq);
+  const size_t ns = (size_t)decode_nsplit(B, Hq, Hkv, cap, Sq, paged);
   return (size_t)B * Sq * Hq * ns * ((size_t)D + 2);
 }
 
@@ -878,13 +885,13 @@ static int launch_decode_t(const void* q, const void* kc, const void* vc, const 
   const int cap = paged ? ly.max_pages * ly.page_size : ly.cap;
   CUtensorMap tk, tv;
   if (paged) {
-    if (encode_tmap_rows(&tk, kc, D, Hkv, ly.page_size, ly.num_pages, dec::TT))
+    if (encode_tmap_rows(&tk, kc, D, Hkv, ly.page_size, ly.num_pages, CP::TT))
       return cudaErrorInvalidValue;
-    if (encode_tmap_rows(&tv, vc, D, Hkv, ly.page_size, ly.num_pages, dec::TT))
+    if (encode_tmap_rows(&tv, vc, D, Hkv, ly.page_size, ly.num_pages, CP::TT))
       return cudaErrorInvalidValue;
   } else {
-    if (encode_tmap_rows(&tk, kc, D, Hkv, cap, B, dec::TT)) return cudaErrorInvalidValue;
-    if (encode_tmap_rows(&tv, vc, D, Hkv, cap, B, dec::TT)) return cudaErrorInvalidValue;
+    if (encode_tmap_rows(&tk, kc, D, Hkv, cap, B, CC::TT)) return cudaErrorInvalidValue;
+    if (encode_tmap_rows(&tv, vc, D, Hkv, cap, B, CC::TT)) return cudaErrorInvalidValue;
   }
   static int attr_set[64] = {0};
   int dev = 0;
@@ -920,7 +927,7 @@ static int launch_decode_t(const void* q, const void* kc, const void* vc, const 
   p.num_pages = ly.num_pages;
   const int Sq = paged ? ly.Sq : 1;
   const bool bal = decode_balanced(B, Hq, Hkv, Sq, paged);
-  const int ns = bal ? (sm_count() > 0 ? sm_count() : 148) : decode_nsplit(B, Hq, Hkv, cap, Sq);
+  const int ns = bal ? (sm_count() > 0 ? sm_count() : 148) : decode_nsplit(B, Hq, Hkv, cap, Sq, paged);
   p.part_o = scratch;
   p.part_ml = scratch + (bal ? (size_t)ns * dec::HB * D : (size_t)B * Sq * Hq * ns * D);
   p.balanced = bal ? 1 : 0;
@@ -947,7 +954,7 @@ static int launch_decode_t(const void* q, const void* kc, const void* vc, const 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t sc = {};
   sc.gridDim = bal ? dim3(ns, 1, 1) : dim3(ns, Hkv * p.n_hb, B);
-  sc.blockDim = dim3(dec::THREADS, 1, 1);
+  sc.blockDim = dim3(paged ? CP::THREADS : CC::THREADS, 1, 1);
   sc.dynamicSmemBytes = paged ? CP::SMEM_TOTAL : CC::SMEM_TOTAL;
   sc.stream = stream;
   sc.attrs = attr;
