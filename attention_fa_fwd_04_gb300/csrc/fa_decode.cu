@@ -17,7 +17,9 @@
 //   CTA    = 1 producer warp issuing TMA tile loads (64 tokens x D, K and V,
 //            128-byte swizzle) into a 4-stage mbarrier ring (8 for D = 64,
 //            128 KiB in flight), and 2 consumer warps that each own whole
-//            tiles (paged caches: 32-token tiles, 4 warps, a deeper ring):
+//            tiles (paged caches: 64-token tiles over 2 warps in a 6-stage
+//            ring, or 32-token tiles over 4 warps when pages are not a
+//            multiple of 64 tokens):
 //            S^T = K Q^T and O^T += V^T P^T with mma.sync m16n8k16,
 //            tokens as the MMA's M and the group's query heads as its N (8 per
 //            block, so a GQA group of 4 wastes half of N instead of 3/4 of a
@@ -42,8 +44,8 @@ namespace fa {
 __device__ unsigned int g_decode_err = 0;
 
 namespace dec {
-constexpr int TT = 32;        // tokens per tile of a paged cache (page sizes are multiples)
-constexpr int NWARPS = 4;     // consumer warps, at most (paged caches)
+constexpr int TT = 32;        // the smallest tile: pages are multiples of it
+constexpr int NWARPS = 4;     // consumer warps, at most (32-token tiles)
 constexpr int THREADS = (NWARPS + 1) * 32;
 constexpr int HB = 16;        // row stride of the merge buffers (query rows per CTA at most)
 // Bytes of K/V per CTA warmed in L2 before the grid wait: with one CTA per SM
@@ -56,20 +58,21 @@ constexpr int PREFETCH_BYTES = 384 * 1024;
 // must never run ahead by a phase: if two warps shared a stage, the faster one
 // could see the stage's previous phase as "complete" and consume a tile that
 // has not landed.)
-// Contiguous caches: 64-token tiles (64-row TMA boxes; the SM takes in
-// 32-row boxes more slowly) over 2 consumer warps with 2 stages each, 128 KiB
-// in flight, which leaves room beside the CTA for the combine's CTAs.
-// PAGED: pages may be 32 tokens, so tiles are 32 tokens over 4 warps; the
-// paged (batched) decode streams long ranges from HBM, where the bytes in
-// flight per SM set the rate: its ring is 192 KiB deep.
-template <int D, bool PAGED = false>
+// TILE = 64: 64-token tiles (64-row TMA boxes; an SM takes in 32-row boxes
+// more slowly) over 2 consumer warps.  Contiguous caches keep 2 stages per
+// warp, 128 KiB in flight, which leaves room beside the CTA for the combine's
+// CTAs.  PAGED: the paged (batched) decode streams long ranges from HBM, where
+// the bytes in flight per SM set the rate: its ring is 192 KiB deep.  Pages
+// that are not a multiple of 64 tokens take TILE = 32 (32-token tiles over 4
+// warps).
+template <int D, bool PAGED = false, int TILE = 64>
 struct Cfg {
   static constexpr int HALVES = D / 64;
-  static constexpr int TT = PAGED ? dec::TT : 64;  // tokens per tile
-  static constexpr int NW = PAGED ? dec::NWARPS : 2;  // consumer warps
+  static constexpr int TT = TILE;  // tokens per tile (32 or 64)
+  static constexpr int NW = TILE == 64 ? 2 : dec::NWARPS;  // consumer warps
   static constexpr int THREADS = (NW + 1) * 32;
   static constexpr int HALF_BYTES = TT * 128;  // TT rows x 64 elements x 2 bytes
-  static constexpr int NSTAGE = (D == 128) ? (PAGED ? 12 : 4) : (PAGED ? 24 : 8);
+  static constexpr int NSTAGE = (D == 128 ? 1 : 2) * (PAGED ? (TILE == 64 ? 6 : 12) : 4);
   static constexpr int KV_BYTES = HALVES * HALF_BYTES;  // one K (or V) tile
   static constexpr int STAGE_BYTES = 2 * KV_BYTES;      // K tile + V tile
   static constexpr int SMEM_STAGES = NSTAGE * STAGE_BYTES;
@@ -130,14 +133,14 @@ __device__ __forceinline__ size_t decode_qrow(const DecodeParams& p, int b, int 
 // Block-cooperative, one thread per sequence (B <= blockDim.x); every thread
 // of the block must call it, after griddepcontrol.wait; ends with
 // __syncthreads().  sRed: 2 * warps entries.
-__device__ void balanced_splits(const DecodeParams& p, int* sS, int* sP, long long* sRed) {
+__device__ void balanced_splits(const DecodeParams& p, int* sS, int* sP, long long* sRed, int tt) {
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5, nw = (blockDim.x + 31) >> 5;
   const int U = p.Hkv * p.n_hb;
   int T = 0;
   if (t < p.B) {
     int L = p.valid_len[(size_t)t * p.len_stride];
     L = L < 0 ? 0 : (L > p.cap ? p.cap : L);
-    T = (L + dec::TT - 1) / dec::TT;
+    T = (L + tt - 1) / tt;
   }
   // Block sum of a (per thread) and block max of m, into every thread.
   auto reduce = [&](long long a, long long m, long long* sum, long long* mx) {
@@ -217,11 +220,11 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
 // separately so the contiguous path carries none of the paging code).
 // NB: query rows per CTA in blocks of 8 (the MMA's N): 1 when a kv head has at
 // most 8 rows (GQA groups up to 8 with one new token), else 2.
-template <int D, bool PAGED, int NB>
+template <int D, bool PAGED, int NB, int TILE>
 __global__ void __launch_bounds__(dec::THREADS, 1)
     decode_split_kernel(const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const DecodeParams p) {
-  using C = dec::Cfg<D, PAGED>;
+  using C = dec::Cfg<D, PAGED, TILE>;
   constexpr int TT = C::TT, NSTAGE = C::NSTAGE, HB = dec::HB, NW = C::NW;
   constexpr int RB = 8 * NB;  // query rows of this CTA (HB is the buffers' row stride)
   static_assert(RB <= HB, "row blocks must fit the merge buffers");
@@ -300,7 +303,7 @@ __global__ void __launch_bounds__(dec::THREADS, 1)
       int* sRes = sP + dec::THREADS;
       long long* sRed = reinterpret_cast<long long*>(sRes + 8);
       if (threadIdx.x == 0) sRes[0] = -1;
-      balanced_splits(p, sS, sP, sRed);
+      balanced_splits(p, sS, sP, sRed, TT);
       const int c = blockIdx.x, U = p.Hkv * p.n_hb;
       if (c == 0 && threadIdx.x < p.B) {  // the combine's map of every unit
         const int t = threadIdx.x;
@@ -839,13 +842,12 @@ __global__ void decode_zero_kernel(__nv_bfloat16* o, size_t n, float* lse, size_
       lse[i] = -INFINITY;
 }
 
-static int decode_nsplit(int B, int Hq, int Hkv, int cap, int Sq, bool paged) {
+static int decode_nsplit(int B, int Hq, int Hkv, int cap, int Sq, int tt) {
   const int G = Hq / Hkv;
   const int n_hb = (Sq * G + dec::HB - 1) / dec::HB;
   const long units = (long)B * Hkv * n_hb;
   const int sms = sm_count() > 0 ? sm_count() : 148;
   long ns = sms / (units > 0 ? units : 1);
-  const int tt = paged ? dec::Cfg<128, true>::TT : dec::Cfg<128, false>::TT;
   const long max_tiles = ((long)cap + tt - 1) / tt;
   if (ns > max_tiles) ns = max_tiles;
   if (ns > kMaxSplits) ns = kMaxSplits;  // the combine's one-pass limit
@@ -871,7 +873,8 @@ size_t decode_scratch_floats(int B, int Hq, int Hkv, int cap, int D, int Sq, boo
     const size_t units = (size_t)B * Hkv * ((Sq * (Hq / Hkv) + dec::HB - 1) / dec::HB);
     return sms * dec::HB * ((size_t)D + 2) + 2 * units + 2;  // + the unit map (int2, aligned)
   }
-  const size_t ns = (size_t)decode_nsplit(B, Hq, Hkv, cap, Sq, paged);
+  // Paged caches may take 32-token tiles: the most splits either tile allows.
+  const size_t ns = (size_t)decode_nsplit(B, Hq, Hkv, cap, Sq, paged ? dec::TT : 64);
   return (size_t)B * Sq * Hq * ns * ((size_t)D + 2);
 }
 
@@ -879,15 +882,22 @@ template <int D>
 static int launch_decode_t(const void* q, const void* kc, const void* vc, const DecodeLayout& ly,
                            void* o, float* lse, int B, int Hq, int Hkv, float scale,
                            float* scratch, cudaStream_t stream) {
-  using CC = dec::Cfg<D, false>;  // contiguous caches
-  using CP = dec::Cfg<D, true>;   // paged caches
+  using CC = dec::Cfg<D, false, 64>;  // contiguous caches
+  using CP = dec::Cfg<D, true, 32>;   // paged caches, pages of 32-token multiples
+  using CP64 = dec::Cfg<D, true, 64>; // paged caches, pages of 64-token multiples
   const bool paged = ly.page_table != nullptr;
   const int cap = paged ? ly.max_pages * ly.page_size : ly.cap;
+  const int Sq = paged ? ly.Sq : 1;
+  const bool bal = decode_balanced(B, Hq, Hkv, Sq, paged);
+  // 64-token tiles for pages of 64-token multiples (in balanced mode the
+  // split planner takes one thread per sequence, so also B <= its threads).
+  const bool big = paged && ly.page_size % 64 == 0 && (!bal || B <= CP64::THREADS);
   CUtensorMap tk, tv;
   if (paged) {
-    if (encode_tmap_rows(&tk, kc, D, Hkv, ly.page_size, ly.num_pages, CP::TT))
+    const int tt = big ? CP64::TT : CP::TT;
+    if (encode_tmap_rows(&tk, kc, D, Hkv, ly.page_size, ly.num_pages, tt))
       return cudaErrorInvalidValue;
-    if (encode_tmap_rows(&tv, vc, D, Hkv, ly.page_size, ly.num_pages, CP::TT))
+    if (encode_tmap_rows(&tv, vc, D, Hkv, ly.page_size, ly.num_pages, tt))
       return cudaErrorInvalidValue;
   } else {
     if (encode_tmap_rows(&tk, kc, D, Hkv, cap, B, CC::TT)) return cudaErrorInvalidValue;
@@ -897,13 +907,16 @@ static int launch_decode_t(const void* q, const void* kc, const void* vc, const 
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    const void* kernels[4] = {(const void*)decode_split_kernel<D, false, 1>,
-                              (const void*)decode_split_kernel<D, false, 2>,
-                              (const void*)decode_split_kernel<D, true, 1>,
-                              (const void*)decode_split_kernel<D, true, 2>};
-    const int smem[4] = {CC::SMEM_TOTAL, CC::SMEM_TOTAL, CP::SMEM_TOTAL, CP::SMEM_TOTAL};
+    const void* kernels[6] = {(const void*)decode_split_kernel<D, false, 1, 64>,
+                              (const void*)decode_split_kernel<D, false, 2, 64>,
+                              (const void*)decode_split_kernel<D, true, 1, 32>,
+                              (const void*)decode_split_kernel<D, true, 2, 32>,
+                              (const void*)decode_split_kernel<D, true, 1, 64>,
+                              (const void*)decode_split_kernel<D, true, 2, 64>};
+    const int smem[6] = {CC::SMEM_TOTAL, CC::SMEM_TOTAL, CP::SMEM_TOTAL, CP::SMEM_TOTAL,
+                         CP64::SMEM_TOTAL, CP64::SMEM_TOTAL};
     cudaError_t e = cudaSuccess;
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < 6; ++i) {
       e = cudaFuncSetAttribute(kernels[i], cudaFuncAttributeMaxDynamicSharedMemorySize, smem[i]);
       if (e != cudaSuccess) return e;
     }
@@ -925,9 +938,8 @@ static int launch_decode_t(const void* q, const void* kc, const void* vc, const 
   p.page_size = ly.page_size;
   p.max_pages = ly.max_pages;
   p.num_pages = ly.num_pages;
-  const int Sq = paged ? ly.Sq : 1;
-  const bool bal = decode_balanced(B, Hq, Hkv, Sq, paged);
-  const int ns = bal ? (sm_count() > 0 ? sm_count() : 148) : decode_nsplit(B, Hq, Hkv, cap, Sq, paged);
+  const int ns = bal ? (sm_count() > 0 ? sm_count() : 148)
+                     : decode_nsplit(B, Hq, Hkv, cap, Sq, paged && !big ? CP::TT : 64);
   p.part_o = scratch;
   p.part_ml = scratch + (bal ? (size_t)ns * dec::HB * D : (size_t)B * Sq * Hq * ns * D);
   p.balanced = bal ? 1 : 0;
@@ -954,20 +966,23 @@ static int launch_decode_t(const void* q, const void* kc, const void* vc, const 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t sc = {};
   sc.gridDim = bal ? dim3(ns, 1, 1) : dim3(ns, Hkv * p.n_hb, B);
-  sc.blockDim = dim3(paged ? CP::THREADS : CC::THREADS, 1, 1);
-  sc.dynamicSmemBytes = paged ? CP::SMEM_TOTAL : CC::SMEM_TOTAL;
+  sc.blockDim = dim3(!paged ? CC::THREADS : (big ? CP64::THREADS : CP::THREADS), 1, 1);
+  sc.dynamicSmemBytes = !paged ? CC::SMEM_TOTAL : (big ? CP64::SMEM_TOTAL : CP::SMEM_TOTAL);
   sc.stream = stream;
   sc.attrs = attr;
   sc.numAttrs = 1;
   // One block of 8 query rows per CTA when the kv head has at most 8 rows.
   const bool nb1 = Sq * p.G <= 8;
   cudaError_t e;
-  if (paged)
-    e = nb1 ? cudaLaunchKernelEx(&sc, decode_split_kernel<D, true, 1>, tk, tv, p)
-            : cudaLaunchKernelEx(&sc, decode_split_kernel<D, true, 2>, tk, tv, p);
+  if (paged && big)
+    e = nb1 ? cudaLaunchKernelEx(&sc, decode_split_kernel<D, true, 1, 64>, tk, tv, p)
+            : cudaLaunchKernelEx(&sc, decode_split_kernel<D, true, 2, 64>, tk, tv, p);
+  else if (paged)
+    e = nb1 ? cudaLaunchKernelEx(&sc, decode_split_kernel<D, true, 1, 32>, tk, tv, p)
+            : cudaLaunchKernelEx(&sc, decode_split_kernel<D, true, 2, 32>, tk, tv, p);
   else
-    e = nb1 ? cudaLaunchKernelEx(&sc, decode_split_kernel<D, false, 1>, tk, tv, p)
-            : cudaLaunchKernelEx(&sc, decode_split_kernel<D, false, 2>, tk, tv, p);
+    e = nb1 ? cudaLaunchKernelEx(&sc, decode_split_kernel<D, false, 1, 64>, tk, tv, p)
+            : cudaLaunchKernelEx(&sc, decode_split_kernel<D, false, 2, 64>, tk, tv, p);
   if (e != cudaSuccess) return e;
 
   cudaLaunchConfig_t cfg = {};
