@@ -15,8 +15,8 @@
 //   grid   = (nsplit, Hkv * ceil(G/16), B), one CTA per SM, sized from cap and
 //            the SM count (not from L, which the host never reads);
 //   CTA    = 1 producer warp issuing TMA tile loads (64 tokens x D, K and V,
-//            128-byte swizzle) into a 4-stage mbarrier ring (8 for D = 64,
-//            128 KiB in flight), and 2 consumer warps that each own whole
+//            128-byte swizzle) into a 6-stage mbarrier ring (12 for D = 64,
+//            192 KiB in flight), and 3 consumer warps that each own whole
 //            tiles (paged caches: 64-token tiles over 2 warps in a 6-stage
 //            ring, or 32-token tiles over 4 warps when pages are not a
 //            multiple of 64 tokens):
@@ -59,20 +59,19 @@ constexpr int PREFETCH_BYTES = 384 * 1024;
 // could see the stage's previous phase as "complete" and consume a tile that
 // has not landed.)
 // TILE = 64: 64-token tiles (64-row TMA boxes; an SM takes in 32-row boxes
-// more slowly) over 2 consumer warps.  Contiguous caches keep 2 stages per
-// warp, 128 KiB in flight, which leaves room beside the CTA for the combine's
-// CTAs.  PAGED: the paged (batched) decode streams long ranges from HBM, where
-// the bytes in flight per SM set the rate: its ring is 192 KiB deep.  Pages
-// that are not a multiple of 64 tokens take TILE = 32 (32-token tiles over 4
-// warps).
+// more slowly).  Contiguous caches: 3 consumer warps with 2 stages each.
+// PAGED: 2 consumer warps with 3 stages each.  Both keep 192 KiB in flight,
+// since the bytes in flight per SM set the rate of a long stream from HBM.
+// Pages that are not a multiple of 64 tokens take TILE = 32 (32-token tiles
+// over 4 warps).
 template <int D, bool PAGED = false, int TILE = 64>
 struct Cfg {
   static constexpr int HALVES = D / 64;
   static constexpr int TT = TILE;  // tokens per tile (32 or 64)
-  static constexpr int NW = TILE == 64 ? 2 : dec::NWARPS;  // consumer warps
+  static constexpr int NW = TILE == 64 ? (PAGED ? 2 : 3) : dec::NWARPS;  // consumer warps
   static constexpr int THREADS = (NW + 1) * 32;
   static constexpr int HALF_BYTES = TT * 128;  // TT rows x 64 elements x 2 bytes
-  static constexpr int NSTAGE = (D == 128 ? 1 : 2) * (PAGED ? (TILE == 64 ? 6 : 12) : 4);
+  static constexpr int NSTAGE = (D == 128 ? 1 : 2) * (PAGED ? (TILE == 64 ? 6 : 12) : 6);
   static constexpr int KV_BYTES = HALVES * HALF_BYTES;  // one K (or V) tile
   static constexpr int STAGE_BYTES = 2 * KV_BYTES;      // K tile + V tile
   static constexpr int SMEM_STAGES = NSTAGE * STAGE_BYTES;
