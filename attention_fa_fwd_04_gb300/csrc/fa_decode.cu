@@ -17,9 +17,8 @@
 //   CTA    = 1 producer warp issuing TMA tile loads (64 tokens x D, K and V,
 //            128-byte swizzle) into a 6-stage mbarrier ring (12 for D = 64,
 //            192 KiB in flight), and 3 consumer warps that each own whole
-//            tiles (paged caches: 64-token tiles over 2 warps in a 6-stage
-//            ring, or 32-token tiles over 4 warps when pages are not a
-//            multiple of 64 tokens):
+//            tiles (paged caches whose pages are not a multiple of 64 tokens:
+//            32-token tiles over 4 warps):
 //            S^T = K Q^T and O^T += V^T P^T with mma.sync m16n8k16,
 //            tokens as the MMA's M and the group's query heads as its N (8 per
 //            block, so a GQA group of 4 wastes half of N instead of 3/4 of a
@@ -59,16 +58,15 @@ constexpr int PREFETCH_BYTES = 384 * 1024;
 // could see the stage's previous phase as "complete" and consume a tile that
 // has not landed.)
 // TILE = 64: 64-token tiles (64-row TMA boxes; an SM takes in 32-row boxes
-// more slowly).  Contiguous caches: 3 consumer warps with 2 stages each.
-// PAGED: 2 consumer warps with 3 stages each.  Both keep 192 KiB in flight,
-// since the bytes in flight per SM set the rate of a long stream from HBM.
+// more slowly), 3 consumer warps with 2 stages each, 192 KiB in flight: the
+// bytes in flight per SM set the rate of a long stream from HBM.
 // Pages that are not a multiple of 64 tokens take TILE = 32 (32-token tiles
 // over 4 warps).
 template <int D, bool PAGED = false, int TILE = 64>
 struct Cfg {
   static constexpr int HALVES = D / 64;
   static constexpr int TT = TILE;  // tokens per tile (32 or 64)
-  static constexpr int NW = TILE == 64 ? (PAGED ? 2 : 3) : dec::NWARPS;  // consumer warps
+  static constexpr int NW = TILE == 64 ? 3 : dec::NWARPS;  // consumer warps
   static constexpr int THREADS = (NW + 1) * 32;
   static constexpr int HALF_BYTES = TT * 128;  // TT rows x 64 elements x 2 bytes
   static constexpr int NSTAGE = (D == 128 ? 1 : 2) * (PAGED ? (TILE == 64 ? 6 : 12) : 6);
