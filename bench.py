@@ -395,7 +395,7 @@ def run_ours(args, rank, world, local_rank):
                        "single_call": {"us": round(t_dec1 / K * 1e6, 3),
                                        "value": round(dec1_gbs, 1)},
                        "note": "small L (5.6 MB): launch- and latency-bound"},
-            "kernels": ["fa::decode_split_kernel<128, false, 1>", "fa::decode_combine_kernel<128>"],
+            "kernels": ["fa::decode_split_kernel<128, false, 1, 64>", "fa::decode_combine_kernel<128>"],
         },
         "e2e": e2e,
         "varlen": varlen,
